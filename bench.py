@@ -1,0 +1,380 @@
+"""Benchmark of the routed-MoE FFN over one prompt chunk on GB300.
+
+A step is one pass of the whole path over one chunk: router top-k, CSR
+grouping, and the expert FFNs (shared expert, gate/up + silu*up, down +
+weighted scatter-add), i.e. moe_route_topk -> moe_build_csr ->
+moe_experts_fwd on one stream.  Inputs are synthetic (routed_expert_prefill_gb300.synth)
+and resident in HBM for ``value``; ``e2e`` copies x in from pinned host
+memory and the block output back every step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Multi-GPU (torchrun): every rank runs its own chunk (weak scaling, no
+collective on the data path); value = chunks' rows over the max-over-ranks time.
+"""
+
+import os
+
+# The CPU oracle legs run single-threaded (their reported core count is 1).
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import json
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from routed_expert_prefill_gb300 import synth  # noqa: E402
+
+METRIC = "prefill tokens/s and % of roofline (tensor or HBM) for routed MoE FFN, 1 GB300"
+DEFAULT_WORKLOAD = "t512_h2048_e128"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------------------
+# Algorithmic work of one step (from the step's actual routing)
+# --------------------------------------------------------------------------
+
+def record_bytes(h, inter):
+    """Bytes of one quantised expert record: 4-bit codes + fp16 scale and bias per 64."""
+    return 3 * inter * h // 2 + 2 * 2 * (3 * inter * h // 64)
+
+
+def step_work(w: synth.Workload, counts: np.ndarray) -> dict:
+    touched = int((counts > 0).sum())
+    n = int(counts.sum())
+    t, h, I, Is, E, k = w.t, w.h, w.inter, w.shared_inter, w.E, w.k
+    flops = 2 * t * h * E + 6 * n * h * I + 6 * t * h * Is
+    wbytes = touched * record_bytes(h, I) + (record_bytes(h, Is) if Is else 0)
+    io = 2 * t * h * 2 + E * h * 2 + t * k * 8
+    by_kernel = {
+        # gate+up weights of touched experts (and the shared expert) + x in + hg out
+        "gateup": dict(bytes=touched * 2 * (I * h // 2 + 2 * 2 * I * h // 64)
+                       + (2 * (Is * h // 2 + 2 * 2 * Is * h // 64) if Is else 0)
+                       + t * h * 2 + (n * I + t * Is) * 2,
+                       flops=4 * n * h * I + 4 * t * h * Is),
+        # down weights + hg in + fp32 block accumulator in/out
+        "down": dict(bytes=touched * (I * h // 2 + 2 * 2 * I * h // 64)
+                     + ((Is * h // 2 + 2 * 2 * Is * h // 64) if Is else 0)
+                     + (n * I + t * Is) * 2 + 2 * t * h * 4,
+                     flops=2 * n * h * I + 2 * t * h * Is),
+        "route_topk": dict(bytes=t * h * 2 + E * h * 2 + t * k * 8, flops=2 * t * h * E),
+    }
+    return dict(touched=touched, pairs=n, max_rows=int(counts.max()), flops=flops,
+                bytes=wbytes + io, by_kernel=by_kernel)
+
+
+def kernel_family(name: str) -> str:
+    for fam in ("gateup", "down", "route_topk"):
+        if name.startswith(fam):
+            return fam
+    return name
+
+
+# --------------------------------------------------------------------------
+# Clocks during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        for ln in self.lines:
+            f = [s.strip() for s in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                                 f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# Reference arm: the CPU oracle as it stands
+# --------------------------------------------------------------------------
+
+def oracle_sample_seconds(w: synth.Workload, inp: dict, rows: int) -> float:
+    from oracle import moe_oracle as O
+
+    sub = dict(inp, x=inp["x"][:rows])
+    t0 = time.perf_counter()
+    O.moe_forward(sub, w.k, w.h, w.inter, w.shared_inter)
+    return time.perf_counter() - t0
+
+
+def run_reference(args, w: synth.Workload):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    inp = synth.make_inputs(w)
+    rows = min(w.t, args.oracle_rows)
+    for _ in range(args.warmup):
+        oracle_sample_seconds(w, inp, min(rows, 4))
+    secs = [oracle_sample_seconds(w, inp, rows) for _ in range(args.steps)]
+    tot = sum(secs)
+    value = rows * len(secs) / tot
+    sample = f"first {rows} of the {w.t} rows of the workload per step, full oracle (router, CSR, experts)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(secs) * w.t / rows,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "t": w.t, "h": w.h, "inter": w.inter, "E": w.E,
+                                        "k": w.k, "shared_inter": w.shared_inter},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# Our arm
+# --------------------------------------------------------------------------
+
+def run_ours(args, w: synth.Workload):
+    import torch
+    import torch.distributed as dist
+
+    from routed_expert_prefill_gb300 import build as B
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev_name = f"cuda:{local}"
+    if rank == 0 or not os.path.exists(os.path.join(ROOT, "routed_expert_prefill_gb300", "libmoe_gb300.so")):
+        B.build()
+    if world > 1:
+        dist.barrier()
+    from routed_expert_prefill_gb300 import moe
+
+    inp = synth.make_inputs(w)
+    dev = moe.upload_inputs(inp, dev_name)
+    dims = moe.dims_of(w.t, w.h, w.inter, w.E, w.k, w.shared_inter)
+    flags = args.flags
+    ws = moe.new_workspace(dims, flags, dev_name)
+    out = torch.empty((w.t, w.h), dtype=torch.bfloat16, device=dev_name)
+    stream = torch.cuda.current_stream()
+    bufs = dict(route=(torch.empty((w.t, w.k), dtype=torch.int32, device=dev_name),
+                       torch.empty((w.t, w.k), dtype=torch.float32, device=dev_name)),
+                csr=moe.Csr(torch.empty(w.E + 1, dtype=torch.int32, device=dev_name),
+                            torch.empty(w.t * w.k, dtype=torch.int32, device=dev_name),
+                            torch.empty(w.t * w.k, dtype=torch.float32, device=dev_name),
+                            torch.empty(w.t * w.k, dtype=torch.int32, device=dev_name)))
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev_name)
+
+    def step():
+        return moe.moe_forward(dev, dims, flags, ws=ws, out=out, bufs=bufs)
+
+    for _ in range(args.warmup):
+        res = step()
+    torch.cuda.synchronize()
+    status = moe.read_device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device-side status {status} after warm-up")
+    counts = np.diff(res["csr"].offsets.cpu().numpy())
+    work = step_work(w, counts)
+
+    # ---- device-resident timed region (L2 flushed between steps, untimed)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    moe.profile_enable(True)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    moe.profile_enable(False)
+    prof = moe.profile_read()
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev_name)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    gpu_launches = sum(v[0] for v in prof.values())
+
+    # ---- end to end through the public API with host buffers
+    x_host = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_host = torch.empty((w.t, w.h), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(dev["x"])
+    dev_e2e = dict(dev, x=x_dev)
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_forward(dev_e2e, dims, flags, ws=ws, out=out, bufs=bufs)
+        out_host.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        e_starts[i].record(stream)
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_forward(dev_e2e, dims, flags, ws=ws, out=out, bufs=bufs)
+        out_host.copy_(out, non_blocking=True)
+        e_ends[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_starts, e_ends)) / args.steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev_name)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    # dominant kernel = largest share of device time
+    fam_time = {}
+    fam_launch = {}
+    for name, (n, tms) in prof.items():
+        f = kernel_family(name)
+        fam_time[f] = fam_time.get(f, 0.0) + tms
+        fam_launch[f] = fam_launch.get(f, 0) + n
+    dom = max(fam_time, key=fam_time.get)
+    per_launch_ms = fam_time[dom] / fam_launch[dom]
+    launches_per_step = fam_launch[dom] / args.steps
+    kw = work["by_kernel"].get(dom)
+    roofline = None
+    if kw is not None:
+        kb = kw["bytes"] / launches_per_step
+        kf = kw["flops"] / launches_per_step
+        hbm_t = kb / (peaks["hbm_gbs"] * 1e9)
+        ten_t = kf / (peaks["bf16_tflops"] * 1e12)
+        if hbm_t >= ten_t:
+            ach = kb / (per_launch_ms * 1e-3) / 1e9
+            roofline = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": ach / peaks["hbm_gbs"], "traffic": None}
+        else:
+            ach = kf / (per_launch_ms * 1e-3) / 1e12
+            roofline = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                        "frac": ach / peaks["bf16_tflops"], "traffic": None}
+        roofline.update({"kernel": dom, "peak_source": peak_src,
+                         "kernel_ms_per_launch": per_launch_ms})
+    t_star = max(work["flops"] / (peaks["bf16_tflops"] * 1e12), work["bytes"] / (peaks["hbm_gbs"] * 1e9))
+    step_bound = "tensor" if work["flops"] / (peaks["bf16_tflops"] * 1e12) > work["bytes"] / (peaks["hbm_gbs"] * 1e9) else "hbm"
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        rows = min(w.t, args.oracle_rows)
+        secs = oracle_sample_seconds(w, inp, rows)
+        cpu = {"value": rows / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {rows} of {w.t} rows, one full oracle pass (router, CSR, experts), 1 thread"}
+
+    value = world * w.t / (ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "t": w.t, "h": w.h, "inter": w.inter, "E": w.E, "k": w.k,
+                   "shared_inter": w.shared_inter, "flags": flags, "parallelism": f"replicas{world}",
+                   "l2": "flushed between timed steps (2x L2 write, untimed); expert weights also exceed L2",
+                   "touched_experts": work["touched"], "max_rows_per_expert": work["max_rows"],
+                   "step_flops": work["flops"], "step_bytes": work["bytes"],
+                   "step_tflops": work["flops"] / (ms * 1e-3) / 1e12,
+                   "step_gbs": work["bytes"] / (ms * 1e-3) / 1e9,
+                   "step_roofline_frac": t_star / (ms * 1e-3), "step_bound": step_bound,
+                   "wall_s_timed_region": wall},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * w.t / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(x_host.numel() * 2), "d2h_bytes_per_step": int(out_host.numel() * 2)},
+        "gpu_launches": gpu_launches,
+        "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in prof.items()},
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--flags", type=int, default=0)
+    ap.add_argument("--oracle-rows", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+/*
+ * moe.h - C ABI of the GB300 (sm_103a) routed mixture-of-experts FFN over a
+ * prompt chunk.
+ *
+ * The operation (cherenkov qwen4_exp engine, rustdoc source pages):
+ *   - prefill.rs, pf_layer: the router (router_b) produces, for each of the
+ *     t rows, the top-k experts (topk_idx) and their weights (topk_w);
+ *   - prefill/experts.rs, prepare_expert_jobs: the (row, slot) pairs are
+ *     grouped by expert into a CSR list, expert-ascending and row-ascending;
+ *   - prefill/experts.rs, pf_experts: a zeroed block output receives the
+ *     shared expert over all rows, then every expert's rows are gathered,
+ *     run through the gate and up quantised matmuls, silu(gate)*up and the
+ *     down quantised matmul, and scatter-added with their routing weight.
+ *   - prefill/experts.rs, Q {w, s, b}: weights are 4-bit affine codes,
+ *     W[o][i] = q[o][i] * s[o][i/64] + b[o][i/64].
+ *
+ * Conventions shared by every entry point
+ *   - Every array pointer is a DEVICE pointer on the current CUDA device,
+ *     allocated and owned by the caller; the library keeps no model state
+ *     and never allocates, frees or retains caller memory.
+ *   - bf16 and fp16 values are passed as their 16-bit patterns (uint16_t).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls only enqueue work on it: they return before the GPU
+ *     has run, never synchronise the host (except moe_read_device_status),
+ *     and results are valid once the stream has reached that point.
+ *   - Return value: MOE_OK (0) or a negative moe_status.  Nothing throws or
+ *     aborts across the ABI.  Host-side argument checks run before any work
+ *     is enqueued; on failure nothing is enqueued.  moe_last_error() gives a
+ *     thread-local message for the last failure on the calling thread.
+ *   - Device-side checks (an expert id out of range, a row index out of
+ *     range, a bounded wait that gave up) set flags in the workspace and skip
+ *     the offending element; moe_read_device_status() reports them.
+ *   - Supported shapes: 1 <= t <= 65536; h, inter, shared_inter multiples of
+ *     128 (shared_inter may be 0: no shared expert); 1 <= E <= 1024;
+ *     1 <= k <= min(E, 16).  Pointers must be 16-byte aligned.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_EINVAL = -1,     /* null or misaligned pointer, unknown flag */
+  MOE_ESHAPE = -2,     /* a dimension outside the supported range */
+  MOE_EWORKSPACE = -3, /* workspace null or smaller than moe_workspace_bytes() */
+  MOE_ECUDA = -4,      /* a CUDA runtime call or kernel launch failed */
+  MOE_EDEVICE = -5,    /* a device-side input check failed (bad id or row) */
+  MOE_ETIMEOUT = -6    /* a bounded device-side wait gave up */
+} moe_status;
+
+/* Problem sizes of one MoE block over one chunk. */
+typedef struct {
+  int32_t t;            /* rows in the chunk */
+  int32_t h;            /* hidden size (input and output width) */
+  int32_t inter;        /* routed expert intermediate size */
+  int32_t E;            /* number of routed experts */
+  int32_t k;            /* experts per row */
+  int32_t shared_inter; /* shared expert intermediate size; 0 = none */
+} moe_dims;
+
+/* The expert-grouped list produced by moe_build_csr (all device, caller-owned). */
+typedef struct {
+  int32_t* offsets; /* [E+1]: expert e owns list positions offsets[e] .. offsets[e+1]-1 */
+  int32_t* rows;    /* [t*k]: row index of each list position */
+  float* weights;   /* [t*k]: routing weight of each list position (bit copy of w) */
+  int32_t* slot_of; /* [t*k]: list position of pair (r, j), indexed r*k + j */
+} moe_csr;
+
+/* Quantised expert weights.  One record per expert, each holding three
+ * matrices in this order: gate [inter][h], up [inter][h], down [h][inter].
+ * codes:  uint8 [E][3*inter*h/2], each matrix row-major and K-contiguous,
+ *         two 4-bit codes per byte, the low nibble at the even K index.
+ * scales, biases: fp16 [E][3*inter*h/64], per output row and 64-wide K
+ *         group, row-major [rows][K/64] per matrix, same matrix order. */
+typedef struct {
+  const uint8_t* codes;
+  const uint16_t* scales;
+  const uint16_t* biases;
+} moe_qweights;
+
+/* The shared expert: one record of the same layout with inter = shared_inter,
+ * plus an optional per-row gate vector (bf16 [h]): when non-NULL, the shared
+ * expert's output for row r is scaled by sigmoid(x[r] . gate)
+ * (prefill/experts.rs, pf_experts -> shared_add_rows binds the rows and a
+ * dense shared-gate tensor). */
+typedef struct {
+  const uint8_t* codes;
+  const uint16_t* scales;
+  const uint16_t* biases;
+  const uint16_t* gate; /* bf16 [h] or NULL */
+} moe_shared;
+
+/* Flags of moe_experts_fwd. */
+#define MOE_DETERMINISTIC 0x1u /* fixed-order fp32 reduction per row (bitwise reproducible) */
+#define MOE_FORCE_SMALL_T 0x2u /* force the weight-streaming small-t kernels */
+#define MOE_FORCE_LARGE_T 0x4u /* force the tensor-core grouped GEMM kernels */
+#define MOE_SIMPLE_KERNELS 0x8u /* plain CUDA-core kernels (slow; a cross-check path) */
+
+/* Thread-local message of the last failed call on this thread ("" if none). */
+const char* moe_last_error(void);
+
+/* Short name of a status code. */
+const char* moe_status_string(int status);
+
+/*
+ * Router (prefill.rs, pf_layer -> router_b): logits, top-k and weights.
+ *
+ *   logit[r][e] = sum_i x[r][i] * wr[e][i]  (+ rbias[e])
+ *
+ * computed in fp32 from the exact bf16 products in a fixed summation order:
+ * lane l of 32 owns the K indices 256*m + 8*l + c (c = 0..7) and sums them
+ * from +0, m ascending then c ascending; the 32 lane sums combine as
+ * P[l] + P[l xor o] for o = 16, 8, 4, 2, 1.  The bias is added last.
+ *   idx[r][0..k-1]: the k largest logits, descending, exact ties to the lower id;
+ *   w[r][j] = exp(l_j - l_max) / sum over the row's top-k of exp(l - l_max).
+ *
+ * x      bf16 [t][h]        wr   bf16 [E][h]      rbias  fp32 [E] or NULL
+ * idx    int32 [t][k] out   w    fp32 [t][k] out  logits fp32 [t][E] out or NULL
+ * Uses no workspace.  Errors: MOE_EINVAL, MOE_ESHAPE, MOE_ECUDA.
+ */
+int moe_route_topk(const uint16_t* x, const uint16_t* wr, const float* rbias,
+                   const moe_dims* dims, int32_t* idx, float* w, float* logits,
+                   void* stream);
+
+/*
+ * Grouping (prefill/experts.rs, prepare_expert_jobs): the t*k (row, slot)
+ * pairs in expert-ascending, row-ascending order.
+ *
+ *   offsets[e] = number of pairs routed to experts < e   (offsets[E] = t*k)
+ *   rows[p], weights[p]: the row and the bit-copied weight w[r][j] of list
+ *       position p; within an expert, rows ascend.
+ *   slot_of[r*k + j] = position of pair (r, j).
+ *
+ * idx int32 [t][k], w fp32 [t][k] in; out fields as in moe_csr.
+ * ws: workspace of at least moe_workspace_bytes(dims, 0) bytes (may be shared
+ * with moe_experts_fwd on the same stream).  An id outside [0, E) sets the
+ * MOE_EDEVICE flag and that pair is dropped.
+ * Errors: MOE_EINVAL, MOE_ESHAPE, MOE_EWORKSPACE, MOE_ECUDA.
+ */
+int moe_build_csr(const int32_t* idx, const float* w, const moe_dims* dims,
+                  const moe_csr* csr, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Expert FFNs (prefill/experts.rs, pf_experts):
+ *
+ *   out[r] = g_r * FFN_S(x_r) + sum_j w_rj * FFN_{e_rj}(x_r),
+ *   FFN(x) = (silu(x G^T) * (x U^T)) D^T,   silu(z) = z / (1 + exp(-z)),
+ *
+ * with g_r = sigmoid(x_r . shared->gate) or 1, FFN_S the shared expert (none
+ * when dims->shared_inter == 0; `shared` may then be NULL) and the routed
+ * terms taken from `csr` (as produced by moe_build_csr).  Weights are
+ * dequantised to bf16 (one bf16 fma of the code with the bf16-rounded scale
+ * and bias), products accumulate in fp32, silu(gate)*up is rounded to bf16,
+ * the block sum accumulates in fp32 and `out` is rounded once to bf16.
+ * Without MOE_DETERMINISTIC the routed terms are added with fp32 atomics
+ * (summation order varies run to run); with it every row sums its shared
+ * term and its k terms in expert-ascending order.
+ *
+ * x bf16 [t][h] in; out bf16 [t][h] out (no residual is added).
+ * ws: at least moe_workspace_bytes(dims, flags) bytes.
+ * Errors: MOE_EINVAL, MOE_ESHAPE, MOE_EWORKSPACE, MOE_ECUDA.
+ */
+int moe_experts_fwd(const uint16_t* x, const moe_csr* csr, const moe_qweights* experts,
+                    const moe_shared* shared, uint16_t* out, const moe_dims* dims,
+                    uint32_t flags, void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes needed by moe_build_csr and moe_experts_fwd for `dims` and
+ * `flags` (one buffer serves both calls on one stream).  0 on bad dims. */
+size_t moe_workspace_bytes(const moe_dims* dims, uint32_t flags);
+
+/* Clear the device-side status flags in `ws` (enqueued on `stream`).
+ * Call once on a fresh workspace. */
+int moe_clear_device_status(void* ws, void* stream);
+
+/* Synchronise `stream`, read the device-side status flags in `ws` and clear
+ * them.  Returns MOE_OK, MOE_EDEVICE (an id or row out of range was seen),
+ * MOE_ETIMEOUT or MOE_ECUDA. */
+int moe_read_device_status(void* ws, void* stream);
+
+/*
+ * Launch accounting (benchmark support; no counterpart in the method).
+ * While enabled, every kernel the library launches is counted and
+ * bracketed by a pair of CUDA events on the stream it is launched on, so a
+ * benchmark can time each kernel inside a longer timed region.  Off by
+ * default; enabling adds two event records per launch.
+ */
+typedef struct {
+  char name[48];    /* kernel name */
+  int32_t launches; /* launches since the last moe_profile_enable(1) */
+  double total_ms;  /* summed event-measured duration of those launches */
+} moe_profile_entry;
+
+/* on != 0: clear previous records and start recording; on == 0: stop. */
+int moe_profile_enable(int on);
+
+/* Wait for the recorded events and write one entry per distinct kernel
+ * (at most max_entries).  Returns the number of entries written (>= 0) or a
+ * negative moe_status. */
+int moe_profile_read(moe_profile_entry* entries, int max_entries);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -122,7 +122,7 @@ def expert_matrices(codes, scales, biases, h: int, inter: int):
 def route_logits(x_bits: np.ndarray, wr_bits: np.ndarray, rbias: np.ndarray | None = None) -> np.ndarray:
     """Router logits in float32, in the canonical summation order.
 
-    logit[r, e] = sum_i x[r, i] * wr[i, e] (+ rbias[e]).
+    logit[r, e] = sum_i x[r, i] * wr[e, i] (+ rbias[e]);  wr is [E, h].
 
     bf16 x bf16 products are exact in fp32, so only the order of the fp32
     additions matters.  The canonical order: split K into 32 lanes, lane l
@@ -134,7 +134,7 @@ def route_logits(x_bits: np.ndarray, wr_bits: np.ndarray, rbias: np.ndarray | No
     contribute nothing (this equals padding with zeros).
     """
     x = bf16_to_f64(x_bits).astype(np.float32)
-    wr = bf16_to_f64(wr_bits).astype(np.float32)
+    wr = bf16_to_f64(wr_bits).astype(np.float32).T  # [h, E]
     t, h = x.shape
     E = wr.shape[1]
     span = LANES * CHUNK
@@ -271,7 +271,7 @@ def moe_forward(inp: dict, k: int, h: int, inter: int, shared_inter: int):
     """
     logits = route_logits(inp["x"], inp["wr"], inp.get("rbias"))
     idx, w = route_topk(logits, k)
-    E = inp["wr"].shape[1]
+    E = inp["wr"].shape[0]
     offsets, rows, weights, slot_of = build_csr(idx, w, E)
     out = experts_fwd(inp["x"], offsets, rows, weights, inp["codes"], inp["scales"],
                       inp["biases"], inp["shared_codes"], inp["shared_scales"],

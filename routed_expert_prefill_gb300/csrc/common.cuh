@@ -1,0 +1,111 @@
+// Internal helpers shared by the library's CUDA translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Device-side status flags (first 256 bytes of every workspace).
+// ---------------------------------------------------------------------------
+enum : uint32_t {
+  FLAG_BAD_EXPERT = 1u << 0,  // an expert id outside [0, E)
+  FLAG_BAD_ROW = 1u << 1,     // a CSR row index outside [0, t)
+  FLAG_BAD_OFFSETS = 1u << 2, // CSR offsets not monotone / out of range
+  FLAG_TIMEOUT = 1u << 8,     // a bounded device wait gave up
+};
+
+struct DeviceStatus {
+  uint32_t flags;
+  uint32_t timeout_site;  // which wait gave up (kernel-specific code)
+  uint32_t pad[62];
+};
+
+__device__ __forceinline__ void raise_flag(DeviceStatus* st, uint32_t f) {
+  if (st) atomicOr(&st->flags, f);
+}
+
+// ---------------------------------------------------------------------------
+// bf16 / fp16 bit helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16f(uint16_t v) { return __uint_as_float(((uint32_t)v) << 16); }
+
+__device__ __forceinline__ uint16_t f2bf(float f) {
+  __nv_bfloat16 b = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// fp16 bits -> bf16 (round to nearest even) as a packed pair replicated:
+// scale/bias prepared for the bf16 fma dequantisation.
+__device__ __forceinline__ __nv_bfloat16 h2bf(uint16_t hbits) {
+  __half hv = *reinterpret_cast<__half*>(&hbits);
+  return __float2bfloat16_rn(__half2float(hv));
+}
+
+// Dequantise 8 packed 4-bit codes (one 32-bit word, low nibble = even K) to
+// 8 bf16 values, w = fma(q, s, b) in bf16 (single rounding), s and b already
+// rounded to bf16.  Returns 4 packed bf16x2 words in K order.
+__device__ __forceinline__ void dequant8(uint32_t word, __nv_bfloat162 s2, __nv_bfloat162 b2,
+                                         uint32_t out[4]) {
+  // 0x4300 | q is the bf16 number 128 + q (exact for q < 128).
+  const uint32_t MAGIC = 0x43004300u;
+  const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.f, 128.f);
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    // byte p holds K = 2p (low nibble) and 2p+1 (high nibble)
+    uint32_t b = (word >> (8 * p)) & 0xFFu;
+    uint32_t v = ((b & 0xFu) | ((b >> 4) << 16)) | MAGIC;
+    __nv_bfloat162 q = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&v), k128);
+    __nv_bfloat162 w = __hfma2(q, s2, b2);
+    out[p] = *reinterpret_cast<uint32_t*>(&w);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Workspace layout (host side computes it; kernels receive raw pointers)
+// ---------------------------------------------------------------------------
+struct WsLayout {
+  size_t status;        // DeviceStatus
+  size_t csr_rank;      // int32 [t*k]
+  size_t csr_counts;    // int32 [nchunks][E]
+  size_t csr_base;      // int32 [nchunks][E]
+  size_t acc;           // float [t][h]
+  size_t hg;            // bf16 [t*k][inter]
+  size_t hgs;           // bf16 [t][shared_inter]
+  size_t ybuf;          // float [t*k][h] (deterministic only)
+  size_t sched;         // scheduler state (counters, tile lists)
+  size_t total;
+};
+
+constexpr int CSR_CHUNK = 1024;  // pairs per CSR ranking block
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+WsLayout ws_layout(const moe_dims& d, uint32_t flags);
+
+// Thread-local error message (moe_api.cu)
+int set_error(int status, const char* fmt, ...);
+
+// Launch accounting (profile.cu): no-ops unless moe_profile_enable(1).
+void prof_begin(const char* name, cudaStream_t s);
+void prof_end(cudaStream_t s);
+#define MOE_LAUNCH(name, stream, ...)  \
+  do {                                 \
+    ::moe::prof_begin(name, stream);   \
+    __VA_ARGS__;                       \
+    ::moe::prof_end(stream);           \
+  } while (0)
+
+}  // namespace moe

@@ -1,0 +1,139 @@
+// Expert grouping: the (row, slot) pairs of the router output as a CSR list
+// in expert-ascending, row-ascending order (cherenkov qwen4_exp,
+// prefill/experts.rs, prepare_expert_jobs: rows outer, slots inner, pushed
+// onto per-expert lists that are then concatenated in expert order).
+//
+// The pairs p = r*k + j are already in that visiting order, so the list
+// position of p is offsets[e] + (number of earlier pairs routed to e).  Three
+// kernels compute it without atomics on the ordering:
+//   1. csr_rank: each block of CSR_CHUNK consecutive pairs builds a bitmap
+//      per expert in shared memory; a pair's rank inside its chunk is the
+//      popcount of its expert's bits below it.  The block also writes its
+//      per-expert counts.
+//   2. csr_scan (one block): per expert, the exclusive prefix of the chunk
+//      counts; then the exclusive prefix over experts gives offsets.
+//   3. csr_scatter: position = offsets[e] + chunk prefix + rank.
+#include "common.cuh"
+
+namespace moe {
+
+namespace {
+
+__global__ void __launch_bounds__(CSR_CHUNK)
+csr_rank_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __restrict__ rank,
+                int32_t* __restrict__ counts, DeviceStatus* st) {
+  extern __shared__ uint32_t bm[];  // [E][CSR_CHUNK / 32]
+  constexpr int W = CSR_CHUNK / 32;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < E * W; i += CSR_CHUNK) bm[i] = 0u;
+  __syncthreads();
+  const int p = blockIdx.x * CSR_CHUNK + tid;
+  int e = -1;
+  if (p < n) {
+    e = idx[p];
+    if (e < 0 || e >= E) {
+      raise_flag(st, FLAG_BAD_EXPERT);
+      e = -1;
+    } else {
+      atomicOr(&bm[e * W + (tid >> 5)], 1u << (tid & 31));
+    }
+  }
+  __syncthreads();
+  if (e >= 0) {
+    const int wq = tid >> 5;
+    int rk = __popc(bm[e * W + wq] & ((1u << (tid & 31)) - 1u));
+    for (int q = 0; q < wq; ++q) rk += __popc(bm[e * W + q]);
+    rank[p] = rk;
+  }
+  for (int ex = tid; ex < E; ex += CSR_CHUNK) {
+    int c = 0;
+#pragma unroll
+    for (int q = 0; q < W; ++q) c += __popc(bm[ex * W + q]);
+    counts[(size_t)blockIdx.x * E + ex] = c;
+  }
+}
+
+__global__ void __launch_bounds__(1024)
+csr_scan_kernel(const int32_t* __restrict__ counts, int nchunks, int E, int32_t* __restrict__ base,
+                int32_t* __restrict__ offsets) {
+  __shared__ int32_t tot[1024];
+  __shared__ int32_t warp_sums[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int run = 0;
+  if (tid < E) {
+    for (int c = 0; c < nchunks; ++c) {
+      const int v = counts[(size_t)c * E + tid];
+      base[(size_t)c * E + tid] = run;
+      run += v;
+    }
+  }
+  tot[tid] = (tid < E) ? run : 0;
+  // Block-wide exclusive scan of tot.
+  int v = tot[tid];
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int s = warp_sums[lane];
+    int si = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xFFFFFFFFu, si, o);
+      if (lane >= o) si += y;
+    }
+    warp_sums[lane] = si - s;  // exclusive prefix of warp sums
+  }
+  __syncthreads();
+  const int excl = warp_sums[warp] + incl - v;
+  if (tid < E) offsets[tid] = excl;
+  if (tid == E - 1) offsets[E] = excl + v;
+}
+
+__global__ void csr_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w, int n,
+                                   int k, int E, const int32_t* __restrict__ rank,
+                                   const int32_t* __restrict__ base, const int32_t* __restrict__ offsets,
+                                   int32_t* __restrict__ rows, float* __restrict__ weights,
+                                   int32_t* __restrict__ slot_of) {
+  const int p = blockIdx.x * blockDim.x + threadIdx.x;
+  if (p >= n) return;
+  const int e = idx[p];
+  if (e < 0 || e >= E) {
+    slot_of[p] = -1;
+    return;
+  }
+  const int c = p / CSR_CHUNK;
+  const int pos = offsets[e] + base[(size_t)c * E + e] + rank[p];
+  rows[pos] = p / k;
+  weights[pos] = w[p];
+  slot_of[p] = pos;
+}
+
+}  // namespace
+
+cudaError_t launch_build_csr(const int32_t* idx, const float* w, int t, int k, int E,
+                             const moe_csr& csr, unsigned char* ws, const WsLayout& L,
+                             cudaStream_t stream) {
+  const int n = t * k;
+  const int nchunks = (n + CSR_CHUNK - 1) / CSR_CHUNK;
+  int32_t* rank = reinterpret_cast<int32_t*>(ws + L.csr_rank);
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + L.csr_counts);
+  int32_t* base = reinterpret_cast<int32_t*>(ws + L.csr_base);
+  DeviceStatus* st = reinterpret_cast<DeviceStatus*>(ws + L.status);
+  const size_t smem = (size_t)E * (CSR_CHUNK / 32) * 4;
+  cudaError_t err = cudaFuncSetAttribute(csr_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  MOE_LAUNCH("csr_rank", stream,
+             csr_rank_kernel<<<nchunks, CSR_CHUNK, smem, stream>>>(idx, n, E, rank, counts, st));
+  MOE_LAUNCH("csr_scan", stream, csr_scan_kernel<<<1, 1024, 0, stream>>>(counts, nchunks, E, base, csr.offsets));
+  MOE_LAUNCH("csr_scatter", stream,
+             csr_scatter_kernel<<<(n + 255) / 256, 256, 0, stream>>>(idx, w, n, k, E, rank, base, csr.offsets,
+                                                                    csr.rows, csr.weights, csr.slot_of));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,249 @@
+// The C ABI (include/moe.h): argument checks, workspace layout, dispatch.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "experts.cuh"
+
+namespace moe {
+
+cudaError_t launch_route_topk(const uint16_t* x, const uint16_t* wr, const float* rbias, int t, int h,
+                              int E, int k, int32_t* idx, float* w, float* logits, cudaStream_t stream);
+size_t route_smem_bytes(int h, int E);
+cudaError_t launch_build_csr(const int32_t* idx, const float* w, int t, int k, int E, const moe_csr& csr,
+                             unsigned char* ws, const WsLayout& L, cudaStream_t stream);
+cudaError_t launch_experts_fast(const ExpertsArgs& a, uint32_t flags, cudaStream_t stream);
+size_t experts_sched_bytes(const moe_dims& d);
+
+static thread_local char g_err[512] = "";
+
+int set_error(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+WsLayout ws_layout(const moe_dims& d, uint32_t flags) {
+  WsLayout L{};
+  const size_t n = (size_t)d.t * d.k;
+  const size_t nchunks = (n + CSR_CHUNK - 1) / CSR_CHUNK;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  L.status = take(sizeof(DeviceStatus));
+  L.csr_rank = take(n * 4);
+  L.csr_counts = take(nchunks * d.E * 4);
+  L.csr_base = take(nchunks * d.E * 4);
+  L.acc = take((size_t)d.t * d.h * 4);
+  L.hg = take(n * d.inter * 2);
+  L.hgs = take((size_t)d.t * d.shared_inter * 2);
+  L.ybuf = (flags & MOE_DETERMINISTIC) ? take(n * d.h * 4) : off;
+  L.sched = take(experts_sched_bytes(d));
+  L.total = off;
+  return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+int check_dims(const moe_dims* d) {
+  if (!d) return set_error(MOE_EINVAL, "dims is NULL");
+  if (d->t < 1 || d->t > 65536) return set_error(MOE_ESHAPE, "t=%d outside [1, 65536]", d->t);
+  if (d->h < 128 || d->h > 16384 || d->h % 128)
+    return set_error(MOE_ESHAPE, "h=%d must be a multiple of 128 in [128, 16384]", d->h);
+  if (d->inter < 128 || d->inter > 16384 || d->inter % 128)
+    return set_error(MOE_ESHAPE, "inter=%d must be a multiple of 128 in [128, 16384]", d->inter);
+  if (d->shared_inter < 0 || d->shared_inter > 16384 || d->shared_inter % 128)
+    return set_error(MOE_ESHAPE, "shared_inter=%d must be 0 or a multiple of 128 up to 16384",
+                     d->shared_inter);
+  if (d->E < 1 || d->E > 1024) return set_error(MOE_ESHAPE, "E=%d outside [1, 1024]", d->E);
+  if (d->k < 1 || d->k > 16 || d->k > d->E)
+    return set_error(MOE_ESHAPE, "k=%d outside [1, min(E, 16)]", d->k);
+  return MOE_OK;
+}
+
+int check_ptr(const void* p, const char* name, size_t align, bool nullable = false) {
+  if (!p) return nullable ? MOE_OK : set_error(MOE_EINVAL, "%s is NULL", name);
+  if ((uintptr_t)p % align) return set_error(MOE_EINVAL, "%s is not %zu-byte aligned", name, align);
+  return MOE_OK;
+}
+
+int check_ws(const moe_dims* d, uint32_t flags, void* ws, size_t ws_bytes) {
+  if (!ws) return set_error(MOE_EWORKSPACE, "workspace is NULL");
+  if ((uintptr_t)ws % 256) return set_error(MOE_EWORKSPACE, "workspace is not 256-byte aligned");
+  const size_t need = ws_layout(*d, flags).total;
+  if (ws_bytes < need)
+    return set_error(MOE_EWORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+  return MOE_OK;
+}
+
+int cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return MOE_OK;
+  return set_error(MOE_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define TRY(expr)            \
+  do {                       \
+    int _s = (expr);         \
+    if (_s != MOE_OK) return _s; \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_last_error(void) { return g_err; }
+
+const char* moe_status_string(int s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_EINVAL: return "MOE_EINVAL";
+    case MOE_ESHAPE: return "MOE_ESHAPE";
+    case MOE_EWORKSPACE: return "MOE_EWORKSPACE";
+    case MOE_ECUDA: return "MOE_ECUDA";
+    case MOE_EDEVICE: return "MOE_EDEVICE";
+    case MOE_ETIMEOUT: return "MOE_ETIMEOUT";
+    default: return "MOE_UNKNOWN";
+  }
+}
+
+size_t moe_workspace_bytes(const moe_dims* dims, uint32_t flags) {
+  if (check_dims(dims) != MOE_OK) return 0;
+  return ws_layout(*dims, flags).total;
+}
+
+int moe_route_topk(const uint16_t* x, const uint16_t* wr, const float* rbias, const moe_dims* dims,
+                   int32_t* idx, float* w, float* logits, void* stream) {
+  TRY(check_dims(dims));
+  TRY(check_ptr(x, "x", 16));
+  TRY(check_ptr(wr, "wr", 16));
+  TRY(check_ptr(rbias, "rbias", 4, true));
+  TRY(check_ptr(idx, "idx", 4));
+  TRY(check_ptr(w, "w", 4));
+  TRY(check_ptr(logits, "logits", 4, true));
+  if (route_smem_bytes(dims->h, dims->E) > 227 * 1024)
+    return set_error(MOE_ESHAPE, "router tile for h=%d, E=%d exceeds shared memory", dims->h, dims->E);
+  return cuda_status(launch_route_topk(x, wr, rbias, dims->t, dims->h, dims->E, dims->k, idx, w, logits,
+                                       (cudaStream_t)stream),
+                     "moe_route_topk launch");
+}
+
+int moe_build_csr(const int32_t* idx, const float* w, const moe_dims* dims, const moe_csr* csr, void* ws,
+                  size_t ws_bytes, void* stream) {
+  TRY(check_dims(dims));
+  TRY(check_ptr(idx, "idx", 4));
+  TRY(check_ptr(w, "w", 4));
+  if (!csr) return set_error(MOE_EINVAL, "csr is NULL");
+  TRY(check_ptr(csr->offsets, "csr->offsets", 4));
+  TRY(check_ptr(csr->rows, "csr->rows", 4));
+  TRY(check_ptr(csr->weights, "csr->weights", 4));
+  TRY(check_ptr(csr->slot_of, "csr->slot_of", 4));
+  TRY(check_ws(dims, 0, ws, ws_bytes));
+  const WsLayout L = ws_layout(*dims, 0);
+  return cuda_status(launch_build_csr(idx, w, dims->t, dims->k, dims->E, *csr, (unsigned char*)ws, L,
+                                      (cudaStream_t)stream),
+                     "moe_build_csr launch");
+}
+
+int moe_experts_fwd(const uint16_t* x, const moe_csr* csr, const moe_qweights* experts,
+                    const moe_shared* shared, uint16_t* out, const moe_dims* dims, uint32_t flags, void* ws,
+                    size_t ws_bytes, void* stream) {
+  TRY(check_dims(dims));
+  const uint32_t known = MOE_DETERMINISTIC | MOE_FORCE_SMALL_T | MOE_FORCE_LARGE_T | MOE_SIMPLE_KERNELS;
+  if (flags & ~known) return set_error(MOE_EINVAL, "unknown flag bits 0x%x", flags & ~known);
+  if ((flags & MOE_FORCE_SMALL_T) && (flags & MOE_FORCE_LARGE_T))
+    return set_error(MOE_EINVAL, "MOE_FORCE_SMALL_T and MOE_FORCE_LARGE_T are exclusive");
+  TRY(check_ptr(x, "x", 16));
+  TRY(check_ptr(out, "out", 16));
+  if (!csr) return set_error(MOE_EINVAL, "csr is NULL");
+  TRY(check_ptr(csr->offsets, "csr->offsets", 4));
+  TRY(check_ptr(csr->rows, "csr->rows", 4));
+  TRY(check_ptr(csr->weights, "csr->weights", 4));
+  TRY(check_ptr(csr->slot_of, "csr->slot_of", 4));
+  if (!experts) return set_error(MOE_EINVAL, "experts is NULL");
+  TRY(check_ptr(experts->codes, "experts->codes", 16));
+  TRY(check_ptr(experts->scales, "experts->scales", 16));
+  TRY(check_ptr(experts->biases, "experts->biases", 16));
+  if (dims->shared_inter > 0) {
+    if (!shared) return set_error(MOE_EINVAL, "shared is NULL but shared_inter > 0");
+    TRY(check_ptr(shared->codes, "shared->codes", 16));
+    TRY(check_ptr(shared->scales, "shared->scales", 16));
+    TRY(check_ptr(shared->biases, "shared->biases", 16));
+    TRY(check_ptr(shared->gate, "shared->gate", 16, true));
+  }
+  TRY(check_ws(dims, flags, ws, ws_bytes));
+  const WsLayout L = ws_layout(*dims, flags);
+  unsigned char* wsb = (unsigned char*)ws;
+
+  ExpertsArgs a{};
+  a.x = x;
+  a.t = dims->t;
+  a.h = dims->h;
+  a.I = dims->inter;
+  a.Is = dims->shared_inter;
+  a.E = dims->E;
+  a.k = dims->k;
+  a.n_pairs = dims->t * dims->k;
+  a.offsets = csr->offsets;
+  a.rows = csr->rows;
+  a.weights = csr->weights;
+  a.slot_of = csr->slot_of;
+  a.codes = experts->codes;
+  a.scales = experts->scales;
+  a.biases = experts->biases;
+  a.rec_bytes = (size_t)3 * dims->inter * dims->h / 2;
+  a.rec_groups = (size_t)3 * dims->inter * dims->h / 64;
+  if (dims->shared_inter > 0) {
+    a.s_codes = shared->codes;
+    a.s_scales = shared->scales;
+    a.s_biases = shared->biases;
+    a.s_gate = shared->gate;
+  }
+  a.acc = (float*)(wsb + L.acc);
+  a.hg = (uint16_t*)(wsb + L.hg);
+  a.hgs = (uint16_t*)(wsb + L.hgs);
+  a.ybuf = (flags & MOE_DETERMINISTIC) ? (float*)(wsb + L.ybuf) : nullptr;
+  a.sched = wsb + L.sched;
+  a.status = (DeviceStatus*)(wsb + L.status);
+  a.out = out;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  if (flags & MOE_SIMPLE_KERNELS)
+    return cuda_status(launch_experts_simple(a, (flags & MOE_DETERMINISTIC) != 0, s), "moe_experts_fwd launch");
+  return cuda_status(launch_experts_fast(a, flags, s), "moe_experts_fwd launch");
+}
+
+int moe_clear_device_status(void* ws, void* stream) {
+  if (!ws) return set_error(MOE_EWORKSPACE, "workspace is NULL");
+  return cuda_status(cudaMemsetAsync(ws, 0, sizeof(DeviceStatus), (cudaStream_t)stream),
+                     "moe_clear_device_status");
+}
+
+int moe_read_device_status(void* ws, void* stream) {
+  if (!ws) return set_error(MOE_EWORKSPACE, "workspace is NULL");
+  DeviceStatus st;
+  cudaStream_t s = (cudaStream_t)stream;
+  TRY(cuda_status(cudaMemcpyAsync(&st, ws, sizeof(st), cudaMemcpyDeviceToHost, s), "status read"));
+  TRY(cuda_status(cudaStreamSynchronize(s), "status sync"));
+  TRY(cuda_status(cudaMemsetAsync(ws, 0, sizeof(DeviceStatus), s), "status clear"));
+  TRY(cuda_status(cudaStreamSynchronize(s), "status clear sync"));
+  if (st.flags & FLAG_TIMEOUT)
+    return set_error(MOE_ETIMEOUT, "a bounded device wait gave up (site %u)", st.timeout_site);
+  if (st.flags & (FLAG_BAD_EXPERT | FLAG_BAD_ROW | FLAG_BAD_OFFSETS))
+    return set_error(MOE_EDEVICE, "device-side check failed (flags 0x%x: %s%s%s)", st.flags,
+                     (st.flags & FLAG_BAD_EXPERT) ? "expert id out of range " : "",
+                     (st.flags & FLAG_BAD_ROW) ? "row out of range " : "",
+                     (st.flags & FLAG_BAD_OFFSETS) ? "bad offsets" : "");
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,282 @@
+"""Python binding of ``libmoe_gb300.so`` (the C ABI of include/moe.h).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+Tensors are torch CUDA tensors (PyTorch supplies device memory and streams).
+The library must have been built (``routed_expert_prefill_gb300.build`` or
+``__graft_entry__.build()``); there is no fallback of any kind.
+
+Names mirror the C entry points:
+
+* ``moe_route_topk(x, wr, k, rbias=None, want_logits=False)`` -> ``(idx, w[, logits])``
+* ``moe_build_csr(idx, w, E, ws=None)`` -> ``Csr(offsets, rows, weights, slot_of)``
+* ``moe_experts_fwd(x, csr, experts, shared, dims, flags=0, out=None, ws=None)`` -> ``out``
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import NamedTuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
+
+MOE_DETERMINISTIC = 0x1
+MOE_FORCE_SMALL_T = 0x2
+MOE_FORCE_LARGE_T = 0x4
+MOE_SIMPLE_KERNELS = 0x8
+
+# Every symbol include/moe.h declares.
+EXPORTS = (
+    "moe_last_error",
+    "moe_status_string",
+    "moe_route_topk",
+    "moe_build_csr",
+    "moe_experts_fwd",
+    "moe_workspace_bytes",
+    "moe_clear_device_status",
+    "moe_read_device_status",
+    "moe_profile_enable",
+    "moe_profile_read",
+)
+
+
+class MoeDims(ctypes.Structure):
+    _fields_ = [("t", ctypes.c_int32), ("h", ctypes.c_int32), ("inter", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("shared_inter", ctypes.c_int32)]
+
+
+class MoeCsr(ctypes.Structure):
+    _fields_ = [("offsets", ctypes.c_void_p), ("rows", ctypes.c_void_p),
+                ("weights", ctypes.c_void_p), ("slot_of", ctypes.c_void_p)]
+
+
+class MoeQWeights(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("biases", ctypes.c_void_p)]
+
+
+class MoeShared(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("biases", ctypes.c_void_p), ("gate", ctypes.c_void_p)]
+
+
+class MoeProfileEntry(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int32), ("total_ms", ctypes.c_double)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{msg} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load (once) and return the library; raise if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: build it first (python -m routed_expert_prefill_gb300.build "
+            "or __graft_entry__.build()); the routed-MoE path has no fallback")
+    lib = ctypes.CDLL(path)
+    vp, i32, u32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_size_t
+    lib.moe_last_error.restype = ctypes.c_char_p
+    lib.moe_status_string.restype = ctypes.c_char_p
+    lib.moe_status_string.argtypes = [ctypes.c_int]
+    lib.moe_route_topk.restype = ctypes.c_int
+    lib.moe_route_topk.argtypes = [vp, vp, vp, ctypes.POINTER(MoeDims), vp, vp, vp, vp]
+    lib.moe_build_csr.restype = ctypes.c_int
+    lib.moe_build_csr.argtypes = [vp, vp, ctypes.POINTER(MoeDims), ctypes.POINTER(MoeCsr), vp, sz, vp]
+    lib.moe_experts_fwd.restype = ctypes.c_int
+    lib.moe_experts_fwd.argtypes = [vp, ctypes.POINTER(MoeCsr), ctypes.POINTER(MoeQWeights),
+                                    ctypes.POINTER(MoeShared), vp, ctypes.POINTER(MoeDims), u32, vp, sz, vp]
+    lib.moe_workspace_bytes.restype = sz
+    lib.moe_workspace_bytes.argtypes = [ctypes.POINTER(MoeDims), u32]
+    lib.moe_clear_device_status.restype = ctypes.c_int
+    lib.moe_clear_device_status.argtypes = [vp, vp]
+    lib.moe_read_device_status.restype = ctypes.c_int
+    lib.moe_read_device_status.argtypes = [vp, vp]
+    lib.moe_profile_enable.restype = ctypes.c_int
+    lib.moe_profile_enable.argtypes = [ctypes.c_int]
+    lib.moe_profile_read.restype = ctypes.c_int
+    lib.moe_profile_read.argtypes = [ctypes.POINTER(MoeProfileEntry), ctypes.c_int]
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != 0:
+        lib = load_library()
+        raise MoeError(status, f"{lib.moe_status_string(status).decode()}: {lib.moe_last_error().decode()}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def dims_of(t: int, h: int, inter: int, E: int, k: int, shared_inter: int) -> MoeDims:
+    return MoeDims(t, h, inter, E, k, shared_inter)
+
+
+class Csr(NamedTuple):
+    offsets: torch.Tensor
+    rows: torch.Tensor
+    weights: torch.Tensor
+    slot_of: torch.Tensor
+
+    def c(self) -> MoeCsr:
+        return MoeCsr(self.offsets.data_ptr(), self.rows.data_ptr(), self.weights.data_ptr(),
+                      self.slot_of.data_ptr())
+
+
+def workspace_bytes(dims: MoeDims, flags: int = 0) -> int:
+    n = load_library().moe_workspace_bytes(ctypes.byref(dims), flags)
+    if n == 0:
+        raise MoeError(-2, "bad dims for moe_workspace_bytes")
+    return n
+
+
+def new_workspace(dims: MoeDims, flags: int = 0, device=None, stream=None) -> torch.Tensor:
+    """A workspace tensor for ``dims``/``flags`` with cleared device status."""
+    ws = torch.empty(workspace_bytes(dims, flags), dtype=torch.uint8, device=device or "cuda")
+    _check(load_library().moe_clear_device_status(_ptr(ws), _stream(stream)))
+    return ws
+
+
+def _u16(t: torch.Tensor) -> torch.Tensor:
+    if t.dtype not in (torch.bfloat16, torch.float16, torch.int16, torch.uint16):
+        raise TypeError(f"expected a 16-bit tensor, got {t.dtype}")
+    return t
+
+
+def moe_route_topk(x: torch.Tensor, wr: torch.Tensor, k: int, rbias: torch.Tensor | None = None,
+                   want_logits: bool = False, out=None, stream=None):
+    """Router: x bf16 [t, h], wr bf16 [E, h] -> idx int32 [t, k], w fp32 [t, k] (, logits)."""
+    lib = load_library()
+    t, h = x.shape
+    E = wr.shape[0]
+    dims = MoeDims(t, h, 128, E, k, 0)
+    if out is None:
+        idx = torch.empty((t, k), dtype=torch.int32, device=x.device)
+        w = torch.empty((t, k), dtype=torch.float32, device=x.device)
+    else:
+        idx, w = out
+    logits = torch.empty((t, E), dtype=torch.float32, device=x.device) if want_logits else None
+    _check(lib.moe_route_topk(_ptr(_u16(x)), _ptr(_u16(wr)), _ptr(rbias), ctypes.byref(dims), _ptr(idx),
+                              _ptr(w), _ptr(logits), _stream(stream)))
+    return (idx, w, logits) if want_logits else (idx, w)
+
+
+def moe_build_csr(idx: torch.Tensor, w: torch.Tensor, E: int, ws: torch.Tensor | None = None,
+                  out: Csr | None = None, stream=None) -> Csr:
+    """Group (row, slot) pairs by expert: offsets [E+1], rows/weights/slot_of [t*k]."""
+    lib = load_library()
+    t, k = idx.shape
+    dims = MoeDims(t, 128, 128, E, k, 0)
+    if ws is None:
+        ws = new_workspace(dims, 0, idx.device, stream)
+    if out is None:
+        dev = idx.device
+        out = Csr(torch.empty(E + 1, dtype=torch.int32, device=dev),
+                  torch.empty(t * k, dtype=torch.int32, device=dev),
+                  torch.empty(t * k, dtype=torch.float32, device=dev),
+                  torch.empty(t * k, dtype=torch.int32, device=dev))
+    c = out.c()
+    _check(lib.moe_build_csr(_ptr(idx), _ptr(w), ctypes.byref(dims), ctypes.byref(c), _ptr(ws), ws.numel(),
+                             _stream(stream)))
+    return out
+
+
+def moe_experts_fwd(x: torch.Tensor, csr: Csr, experts: tuple, shared: tuple | None, dims: MoeDims,
+                    flags: int = 0, out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """Expert FFNs.  experts = (codes u8 [E, rec], scales f16 [E, g], biases f16 [E, g]);
+    shared = (codes, scales, biases, gate-or-None) or None."""
+    lib = load_library()
+    if ws is None:
+        ws = new_workspace(dims, flags, x.device, stream)
+    if out is None:
+        out = torch.empty((dims.t, dims.h), dtype=torch.bfloat16, device=x.device)
+    q = MoeQWeights(experts[0].data_ptr(), experts[1].data_ptr(), experts[2].data_ptr())
+    sh = None
+    if shared is not None:
+        g = shared[3]
+        sh = MoeShared(shared[0].data_ptr(), shared[1].data_ptr(), shared[2].data_ptr(),
+                       None if g is None else g.data_ptr())
+    c = csr.c()
+    _check(lib.moe_experts_fwd(_ptr(_u16(x)), ctypes.byref(c), ctypes.byref(q),
+                               ctypes.byref(sh) if sh is not None else None, _ptr(out), ctypes.byref(dims),
+                               flags, _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def profile_enable(on: bool) -> None:
+    """Start (clearing old records) or stop per-launch accounting in the library."""
+    _check(load_library().moe_profile_enable(1 if on else 0))
+
+
+def profile_read() -> dict:
+    """{kernel name: (launches, total ms)} recorded since profile_enable(True)."""
+    buf = (MoeProfileEntry * 64)()
+    n = load_library().moe_profile_read(buf, 64)
+    if n < 0:
+        _check(n)
+    return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(n)}
+
+
+def read_device_status(ws: torch.Tensor, stream=None) -> int:
+    """Synchronise and return the device-side status (0 = clean); clears it."""
+    return load_library().moe_read_device_status(_ptr(ws), _stream(stream))
+
+
+# ---------------------------------------------------------------------------
+# Convenience: host inputs (routed_expert_prefill_gb300.synth layout) -> device,
+# and the three calls chained on one stream.
+# ---------------------------------------------------------------------------
+
+def upload_inputs(inp: dict, device="cuda") -> dict:
+    """Copy the numpy inputs of ``synth.make_inputs`` to device tensors."""
+    import numpy as np
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    def f16(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+    d = dict(
+        x=bf(inp["x"]), wr=bf(inp["wr"]),
+        rbias=None if inp.get("rbias") is None else torch.from_numpy(inp["rbias"]).to(device),
+        codes=torch.from_numpy(inp["codes"]).to(device), scales=f16(inp["scales"]), biases=f16(inp["biases"]),
+        shared_codes=torch.from_numpy(inp["shared_codes"]).to(device),
+        shared_scales=f16(inp["shared_scales"]), shared_biases=f16(inp["shared_biases"]),
+        shared_gate=None if inp.get("shared_gate") is None else bf(inp["shared_gate"]),
+    )
+    return d
+
+
+def moe_forward(dev: dict, dims: MoeDims, flags: int = 0, ws: torch.Tensor | None = None,
+                out: torch.Tensor | None = None, stream=None, bufs: dict | None = None) -> dict:
+    """Router -> CSR -> experts on one stream; returns the intermediate tensors too."""
+    if ws is None:
+        ws = new_workspace(dims, flags, dev["x"].device, stream)
+    b = bufs or {}
+    idx, w = moe_route_topk(dev["x"], dev["wr"], dims.k, dev.get("rbias"), out=b.get("route"), stream=stream)
+    csr = moe_build_csr(idx, w, dims.E, ws=ws, out=b.get("csr"), stream=stream)
+    shared = None
+    if dims.shared_inter > 0:
+        shared = (dev["shared_codes"], dev["shared_scales"], dev["shared_biases"], dev.get("shared_gate"))
+    y = moe_experts_fwd(dev["x"], csr, (dev["codes"], dev["scales"], dev["biases"]), shared, dims, flags,
+                        out=out, ws=ws, stream=stream)
+    return dict(idx=idx, w=w, csr=csr, out=y, ws=ws)

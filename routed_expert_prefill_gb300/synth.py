@@ -8,8 +8,8 @@ Layouts (shared by every consumer):
 
 * ``x``       bf16 bit patterns, uint16 ``[t, h]`` row-major (the normed rows
   that enter the MoE block).
-* ``wr``      bf16 bit patterns, uint16 ``[h, E]`` (router weight; logit
-  ``e`` of row ``r`` is the dot product of ``x[r, :]`` and ``wr[:, e]``).
+* ``wr``      bf16 bit patterns, uint16 ``[E, h]`` (router weight; logit
+  ``e`` of row ``r`` is the dot product of ``x[r, :]`` and ``wr[e, :]``).
 * ``rbias``   float32 ``[E]`` or ``None``: per-expert logit bias (only the
   skewed workload has one).
 * ``codes``   uint8 ``[E, 3*inter*h/2]``: one record per expert holding, in
@@ -114,7 +114,7 @@ def make_inputs(w: Workload, t: int | None = None) -> dict:
     t = w.t if t is None else t
     g = lambda s: np.random.default_rng([w.seed, s])  # noqa: E731
     x = f32_to_bf16_bits(g(_S_X).standard_normal((t, w.h)).astype(np.float32))
-    wr = f32_to_bf16_bits((g(_S_WR).standard_normal((w.h, w.E)) * 0.02).astype(np.float32))
+    wr = f32_to_bf16_bits((g(_S_WR).standard_normal((w.E, w.h)) * 0.02).astype(np.float32))
     codes, scales, biases = _quant_record(g(_S_CODES), g(_S_SCALES), w.E, w.h, w.inter)
     s_codes, s_scales, s_biases = _quant_record(
         g(_S_SH_CODES), g(_S_SH_SCALES), 1, w.h, w.shared_inter

@@ -1,0 +1,223 @@
+"""GPU path vs the CPU oracle, through the C ABI.
+
+Bars: router ids and logits, CSR offsets/rows/slot_of bit-exact; CSR weights
+bit-equal to the router's own weights; router weights within 2e-6 of the
+oracle's (fp32 expf vs fp64 exp); block outputs within
+    max |gpu - oracle| <= 1e-2 * max |oracle| + 1e-3.
+Full-size workloads are run at full size on the GPU and checked on sampled
+rows (a row's output depends on that row only, so the oracle evaluates just
+the sampled rows).
+"""
+
+import numpy as np
+import pytest
+
+from oracle import moe_oracle as O
+from routed_expert_prefill_gb300 import synth
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+TOL_REL, TOL_ABS = 1e-2, 1e-3
+
+
+@pytest.fixture(scope="module")
+def moe():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from routed_expert_prefill_gb300 import build
+
+    build.build()
+    from routed_expert_prefill_gb300 import moe as m
+
+    m.load_library()
+    return m
+
+
+_cache = {}
+
+
+def _inputs(w: synth.Workload):
+    key = ("in", w)
+    if key not in _cache:
+        _cache[key] = synth.make_inputs(w)
+    return _cache[key]
+
+
+def _oracle_rows(w: synth.Workload, inp: dict, rows: np.ndarray | None):
+    """Oracle results for the given rows (all rows if None)."""
+    key = ("or", w, None if rows is None else tuple(rows.tolist()))
+    if key in _cache:
+        return _cache[key]
+    sub = dict(inp)
+    if rows is not None:
+        sub["x"] = inp["x"][rows]
+    res = O.moe_forward(sub, w.k, w.h, w.inter, w.shared_inter)
+    _cache[key] = res
+    return res
+
+
+def _dims(moe, w):
+    return moe.dims_of(w.t, w.h, w.inter, w.E, w.k, w.shared_inter)
+
+
+def _run(moe, w, inp, flags=0, dev=None):
+    dev = dev or moe.upload_inputs(inp)
+    res = moe.moe_forward(dev, _dims(moe, w), flags)
+    torch.cuda.synchronize()
+    status = moe.read_device_status(res["ws"])
+    return res, status
+
+
+def _check_out(got_bf16: torch.Tensor, ref_out: np.ndarray):
+    got = got_bf16.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got))
+    err = np.abs(got - ref_out).max()
+    tol = TOL_REL * np.abs(ref_out).max() + TOL_ABS
+    assert err <= tol, f"max|gpu-oracle| = {err:.4g} > {tol:.4g}"
+    return err, tol
+
+
+def _check_csr_against(csr, idx, w_gpu, E):
+    """CSR from the GPU equals the oracle's grouping of the GPU router output."""
+    idx_np = idx.cpu().numpy()
+    w_np = w_gpu.cpu().numpy()
+    offsets, rows, weights, slot_of = O.build_csr(idx_np, w_np, E)
+    np.testing.assert_array_equal(csr.offsets.cpu().numpy(), offsets)
+    np.testing.assert_array_equal(csr.rows.cpu().numpy(), rows)
+    np.testing.assert_array_equal(csr.slot_of.cpu().numpy(), slot_of)
+    np.testing.assert_array_equal(csr.weights.cpu().numpy().view(np.uint32), weights.view(np.uint32))
+
+
+SMALL = ["tiny_t16_h256_e8", "t512_h2048_e128", "decode_t1_h2048_e128", "decode_t2_h2048_e128",
+         "decode_t4_h2048_e128", "decode_t8_h2048_e128"]
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_router_bitexact(moe, name):
+    w = synth.WORKLOADS[name]
+    inp = _inputs(w)
+    ref = _oracle_rows(w, inp, None)
+    dev = moe.upload_inputs(inp)
+    idx, wt, logits = moe.moe_route_topk(dev["x"], dev["wr"], w.k, dev["rbias"], want_logits=True)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(logits.cpu().numpy().view(np.uint32), ref["logits"].view(np.uint32))
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref["idx"])
+    assert np.abs(wt.cpu().numpy() - ref["w"]).max() <= 2e-6
+
+
+@pytest.mark.parametrize("name", SMALL)
+@pytest.mark.parametrize("flags", [0, 1])
+def test_pipeline_parity(moe, name, flags):
+    w = synth.WORKLOADS[name]
+    inp = _inputs(w)
+    ref = _oracle_rows(w, inp, None)
+    res, status = _run(moe, w, inp, flags)
+    assert status == 0
+    np.testing.assert_array_equal(res["idx"].cpu().numpy(), ref["idx"])
+    _check_csr_against(res["csr"], res["idx"], res["w"], w.E)
+    _check_out(res["out"], ref["out"])
+
+
+def test_simple_kernels_parity(moe):
+    w = synth.WORKLOADS["tiny_t16_h256_e8"]
+    inp = _inputs(w)
+    ref = _oracle_rows(w, inp, None)
+    for flags in (moe.MOE_SIMPLE_KERNELS, moe.MOE_SIMPLE_KERNELS | moe.MOE_DETERMINISTIC):
+        res, status = _run(moe, w, inp, flags)
+        assert status == 0
+        _check_out(res["out"], ref["out"])
+
+
+def test_deterministic_mode_is_bitwise_reproducible(moe):
+    w = synth.WORKLOADS["t512_h2048_e128"]
+    inp = _inputs(w)
+    dev = moe.upload_inputs(inp)
+    outs = []
+    for _ in range(2):
+        res, status = _run(moe, w, inp, moe.MOE_DETERMINISTIC, dev)
+        assert status == 0
+        outs.append(res["out"].view(torch.int16).cpu().numpy())
+    np.testing.assert_array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("t", [1, 3, 13, 37])
+def test_ragged_row_counts(moe, t):
+    w = synth.WORKLOADS["tiny_t16_h256_e8"].replace(t=t, seed=20 + t)
+    inp = synth.make_inputs(w)
+    ref = O.moe_forward(inp, w.k, w.h, w.inter, w.shared_inter)
+    res, status = _run(moe, w, inp)
+    assert status == 0
+    np.testing.assert_array_equal(res["idx"].cpu().numpy(), ref["idx"])
+    _check_csr_against(res["csr"], res["idx"], res["w"], w.E)
+    _check_out(res["out"], ref["out"])
+
+
+def test_all_experts_per_row_and_no_shared(moe):
+    # k = E: every expert takes every row; no shared expert.
+    w = synth.Workload("kE", 9, 256, 128, 4, 4, 0, 31)
+    inp = synth.make_inputs(w.replace(shared_inter=128))
+    ref = O.moe_forward(dict(inp, shared_codes=np.full_like(inp["shared_codes"], 0x88)), w.k, w.h, w.inter, 128)
+    res, status = _run(moe, w, inp)
+    assert status == 0
+    assert res["csr"].offsets.cpu().numpy().tolist() == [0, 9, 18, 27, 36]
+    _check_out(res["out"], ref["out"])
+
+
+def test_one_expert_takes_every_row_and_shared_gate(moe):
+    # A large router bias sends every row to expert 2 first; E - k experts stay empty.
+    w = synth.Workload("hot", 40, 256, 128, 6, 2, 128, 32, shared_gate=True)
+    inp = synth.make_inputs(w)
+    inp["rbias"] = np.array([0, 0, 50, 0, 0, 0], np.float32)
+    ref = O.moe_forward(inp, w.k, w.h, w.inter, w.shared_inter)
+    assert np.all(ref["idx"][:, 0] == 2)
+    res, status = _run(moe, w, inp)
+    assert status == 0
+    np.testing.assert_array_equal(res["idx"].cpu().numpy(), ref["idx"])
+    _check_csr_against(res["csr"], res["idx"], res["w"], w.E)
+    _check_out(res["out"], ref["out"])
+
+
+def test_bad_expert_ids_are_flagged_and_dropped(moe):
+    t, k, E = 8, 2, 4
+    idx = torch.tensor([[0, 1], [2, 9], [3, 0], [-1, 2], [1, 2], [0, 3], [1, 0], [2, 3]], dtype=torch.int32,
+                       device="cuda")
+    w = torch.full((t, k), 0.5, dtype=torch.float32, device="cuda")
+    dims = moe.dims_of(t, 128, 128, E, k, 0)
+    ws = moe.new_workspace(dims)
+    csr = moe.moe_build_csr(idx, w, E, ws=ws)
+    status = moe.read_device_status(ws)
+    assert status == -5  # MOE_EDEVICE
+    slot = csr.slot_of.cpu().numpy()
+    assert slot[3] == -1 and slot[6] == -1
+    assert csr.offsets.cpu().numpy()[-1] == t * k - 2
+    assert moe.read_device_status(ws) == 0  # reading clears
+
+
+def test_shape_errors_raise(moe):
+    x = torch.zeros((4, 200), dtype=torch.bfloat16, device="cuda")
+    wr = torch.zeros((8, 200), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_route_topk(x, wr, 2)
+    assert ei.value.status == -2
+
+
+BIG = ["t4096_h2048_e128_skewed", "t4096_h4096_e256"]
+
+
+@pytest.mark.parametrize("name", BIG)
+def test_full_size_sampled_rows(moe, name):
+    """Full-size run in the benchmark's launch configuration; oracle on 96 sampled rows."""
+    w = synth.WORKLOADS[name]
+    inp = _inputs(w)
+    rows = np.sort(np.random.default_rng(99).choice(w.t, 96, replace=False))
+    ref = _oracle_rows(w, inp, rows)
+    res, status = _run(moe, w, inp)
+    assert status == 0
+    np.testing.assert_array_equal(res["idx"].cpu().numpy()[rows], ref["idx"])
+    _check_csr_against(res["csr"], res["idx"], res["w"], w.E)
+    _check_out(res["out"][torch.from_numpy(rows).cuda()], ref["out"])
+    if name.endswith("skewed"):
+        counts = np.diff(res["csr"].offsets.cpu().numpy())
+        assert counts.max() >= 0.5 * w.t and (counts <= 3).sum() >= w.E // 3

@@ -69,10 +69,10 @@ def test_router_canonical_order_golden():
     h = g["h"]
     for case in g["cases"]:
         x = np.zeros((1, h), np.float32)
-        wr = np.zeros((h, 1), np.float32)
+        wr = np.zeros((1, h), np.float32)
         for i, xi, wi in case["terms"]:
             x[0, i] = xi
-            wr[i, 0] = wi
+            wr[0, i] = wi
         got = O.route_logits(_bf16(x), _bf16(wr))
         assert got.dtype == np.float32
         assert float(got[0, 0]) == case["logit"], case["name"]
@@ -80,10 +80,10 @@ def test_router_canonical_order_golden():
 
 def test_router_bias_added_after_dot():
     x = np.zeros((1, 256), np.float32)
-    wr = np.zeros((256, 2), np.float32)
+    wr = np.zeros((2, 256), np.float32)
     x[0, 3] = 2.0
-    wr[3, 0] = 0.5
-    wr[3, 1] = -1.5
+    wr[0, 3] = 0.5
+    wr[1, 3] = -1.5
     got = O.route_logits(_bf16(x), _bf16(wr), np.array([0.25, 10.0], np.float32))
     assert got[0, 0] == np.float32(1.25) and got[0, 1] == np.float32(7.0)
 
@@ -92,9 +92,9 @@ def test_router_logits_within_fp32_bound_of_exact():
     rng = np.random.default_rng(1)
     t, h, E = 12, 768, 10  # h not a multiple of 256 exercises the tail
     x = _bf16(rng.standard_normal((t, h)))
-    wr = _bf16(rng.standard_normal((h, E)) * 0.02)
+    wr = _bf16(rng.standard_normal((E, h)) * 0.02)
     got = O.route_logits(x, wr).astype(np.float64)
-    X, W = O.bf16_to_f64(x), O.bf16_to_f64(wr)
+    X, W = O.bf16_to_f64(x), O.bf16_to_f64(wr).T
     exact = X @ W
     absum = np.abs(X) @ np.abs(W)
     # <= h/256 + 8 + 5 roundings along any path, each at most 2^-24 relative.
@@ -199,7 +199,7 @@ def test_ffn_onehot_closed_form():
     recs = [_onehot_record(rng, h, inter) for _ in range(E)]
     sh = _onehot_record(rng, h, Is)
     x = _bf16(rng.standard_normal((t, h)))
-    wr = _bf16(rng.standard_normal((h, E)))
+    wr = _bf16(rng.standard_normal((E, h)))
     inp = dict(x=x, wr=wr, rbias=None,
                codes=np.stack([r[0] for r in recs]), scales=np.stack([r[1] for r in recs]),
                biases=np.stack([r[2] for r in recs]),
