@@ -1,0 +1,920 @@
+// Grouped expert GEMMs on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// The routed experts (cherenkov qwen4_exp, prefill/experts.rs, pf_experts:
+// per expert gather_rows -> gate/up quantised matmuls -> silu_mul -> down
+// quantised matmul -> scatter_add_rows) and the shared expert run as two
+// persistent kernels over a device-built tile schedule:
+//
+//   schedule:  per expert, its CSR rows split into tiles of <= 256 rows
+//              (the shared expert: all t rows), ordered largest first.
+//   gateup_tc: unit = (tile, 128 output features).  The weights are the
+//              MMA's M operand (128 rows of gate and 128 rows of up), the
+//              gathered token rows its N operand (16..256), so one dequantised
+//              weight tile serves every row of the tile.  A producer warp
+//              streams the 4-bit code tiles with TMA and gathers the token
+//              rows with TMA gather4 (four CSR rows per instruction, 128-byte
+//              swizzle); eight warps dequantise codes to bf16
+//              (w = fma(q, s, b) in bf16) straight into the UMMA K-major
+//              swizzled layout; one thread issues tcgen05.mma into two TMEM
+//              accumulators (gate, up); the same eight warps then read TMEM,
+//              apply silu(gate) * up and write hg (bf16, CSR order).
+//   down_tc:   unit = (tile, 128 output features of h); A = dequantised down
+//              rows, B = hg rows (contiguous in CSR order, plain TMA tiles);
+//              the epilogue multiplies by the routing weight and adds into
+//              the fp32 block accumulator with atomics, or, deterministic
+//              mode, writes the unweighted result per list position.
+//
+// Every mbarrier wait is bounded (2 s of global time); a wait that gives up
+// records MOE_ETIMEOUT in the workspace status, raises a CTA-wide abort
+// flag so every role leaves its loop, lets in-flight copies and MMAs land,
+// frees TMEM and returns.
+#include <string.h>
+
+#include "experts.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+using namespace tc;
+
+constexpr int TILE_MAX = 256;  // rows per tile (MMA N <= 256)
+constexpr int KC = 64;         // K per chunk = one quantisation group
+constexpr uint64_t WAIT_NS = 2000000000ull;
+
+// Gate/up kernel: stages of codes, dequantised A and gathered B.
+constexpr int GU_SC = 6, GU_SA = 2, GU_SB = 3;
+constexpr int GU_A_BYTES = 2 * 128 * 128;    // gate + up, 128 rows x 128 B
+constexpr int GU_B_BYTES = TILE_MAX * 128;   // up to 256 rows x 128 B
+constexpr int GU_C_BYTES = 2 * 128 * 32;     // gate + up codes, 128 rows x 32 B
+// Down kernel
+constexpr int DN_SC = 8, DN_SA = 2, DN_SB = 3;
+constexpr int DN_A_BYTES = 128 * 128;
+constexpr int DN_B_BYTES = TILE_MAX * 128;
+constexpr int DN_C_BYTES = 128 * 32;
+
+constexpr int NWARPS = 10;  // 0 producer, 1 MMA + TMEM owner, 2..9 dequant + epilogue
+constexpr int NTHREADS = NWARPS * 32;
+
+struct SchedHdr {
+  int n_tiles;
+  int n_units_gu;
+  int n_units_dn;
+  int pad[13];
+};
+
+struct TcParams {
+  int t, h, I, Is, E, k;
+  int deterministic;
+  const int32_t* offsets;
+  const int32_t* rows;
+  const float* weights;
+  const uint16_t* scales;
+  const uint16_t* biases;
+  size_t rec_groups;
+  const uint16_t* s_scales;
+  const uint16_t* s_biases;
+  const float* gate_vals;  // per-row shared-expert gate, or null
+  float* acc;
+  uint16_t* hg;
+  uint16_t* hgs;
+  float* ybuf;
+  const SchedHdr* hdr;
+  const int4* tiles;       // {expert (E = shared), start, rows, 0}
+  const int* units_gu;     // (tile << 8) | feature tile
+  DeviceStatus* status;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void note_timeout(DeviceStatus* st, volatile int* abort, uint32_t site) {
+  if (atomicOr(&st->flags, FLAG_TIMEOUT) == 0) st->timeout_site = site;
+  *abort = 1;
+}
+
+// After an abort: wait (bounded, ignoring the abort flag) for copies or MMAs
+// already issued, so nothing lands in shared memory or TMEM after exit.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const int never = 0;
+  mbar_wait(bar, parity, &never, 100000000ull);
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
+// 64 codes of one weight row (two 16-byte words, low nibble = even K) ->
+// 8 chunks of 8 bf16 (w = fma(q, s, b) with bf16 s, b, single rounding),
+// written to the 128B-swizzled K-major tile row `row`.
+__device__ __forceinline__ void dequant_row_store(const uint32_t (&wd)[8], __nv_bfloat162 s2, __nv_bfloat162 b2,
+                                                  uint8_t* tile, int row, int chunk0, int nchunks) {
+  const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.f, 128.f);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    if (c >= nchunks) break;
+    const uint32_t w = wd[c];
+    // (128 + K0, 128 + K4), (128 + K1, 128 + K5), ... as bf16 pairs
+    const uint32_t A = (w & 0x000F000Fu) | 0x43004300u;
+    const uint32_t B = ((w >> 4) & 0x000F000Fu) | 0x43004300u;
+    const uint32_t C = ((w >> 8) & 0x000F000Fu) | 0x43004300u;
+    const uint32_t D = ((w >> 12) & 0x000F000Fu) | 0x43004300u;
+    uint32_t pr[4];
+    pr[0] = __byte_perm(A, B, 0x5410);  // K0, K1
+    pr[1] = __byte_perm(C, D, 0x5410);  // K2, K3
+    pr[2] = __byte_perm(A, B, 0x7632);  // K4, K5
+    pr[3] = __byte_perm(C, D, 0x7632);  // K6, K7
+    uint4 o;
+    uint32_t* ov = &o.x;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 q = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&pr[i]), k128);
+      __nv_bfloat162 v = __hfma2(q, s2, b2);
+      ov[i] = *reinterpret_cast<uint32_t*>(&v);
+    }
+    *reinterpret_cast<uint4*>(tile + sw128_off(row, chunk0 + c)) = o;
+  }
+}
+
+__device__ __forceinline__ __nv_bfloat162 bf2_from_half(uint16_t hb) {
+  __nv_bfloat16 b = h2bf(hb);
+  return __halves2bfloat162(b, b);
+}
+
+// ----------------------------------------------------------------------------
+// Tile schedule (one block)
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024)
+schedule_kernel(TcParams p, SchedHdr* hdr, int4* tiles, int* units_gu, int max_tiles) {
+  __shared__ int bucket_cnt[16], bucket_base[16], bucket_fill[16];
+  __shared__ int n_tiles_s;
+  __shared__ int scan_carry;
+  __shared__ int warp_sums[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nexp = p.E + (p.Is > 0 ? 1 : 0);
+  if (tid < 16) {
+    bucket_cnt[tid] = 0;
+    bucket_fill[tid] = 0;
+  }
+  __syncthreads();
+  // pass 1: count tiles per size bucket (bucket = ceil(size / 16) - 1)
+  for (int e = tid; e < nexp; e += blockDim.x) {
+    int n;
+    if (e < p.E) {
+      n = p.offsets[e + 1] - p.offsets[e];
+      if (n < 0 || p.offsets[e] < 0 || p.offsets[e + 1] > p.t * p.k) {
+        raise_flag(p.status, FLAG_BAD_OFFSETS);
+        n = 0;
+      }
+    } else {
+      n = p.t;
+    }
+    if (n == 0) continue;
+    const int nt = (n + TILE_MAX - 1) / TILE_MAX;
+    const int sz = (n + nt - 1) / nt;
+    for (int i = 0; i < nt; ++i) {
+      const int rows = min(sz, n - i * sz);
+      if (rows <= 0) break;
+      atomicAdd(&bucket_cnt[(rows + 15) / 16 - 1], 1);
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int b = 15; b >= 0; --b) {  // largest tiles first
+      bucket_base[b] = run;
+      run += bucket_cnt[b];
+    }
+    n_tiles_s = min(run, max_tiles);
+  }
+  __syncthreads();
+  // pass 2: place tiles
+  for (int e = tid; e < nexp; e += blockDim.x) {
+    int n, start;
+    if (e < p.E) {
+      n = p.offsets[e + 1] - p.offsets[e];
+      start = p.offsets[e];
+      if (n < 0 || start < 0 || p.offsets[e + 1] > p.t * p.k) n = 0;
+    } else {
+      n = p.t;
+      start = 0;
+    }
+    if (n == 0) continue;
+    const int nt = (n + TILE_MAX - 1) / TILE_MAX;
+    const int sz = (n + nt - 1) / nt;
+    for (int i = 0; i < nt; ++i) {
+      const int rows = min(sz, n - i * sz);
+      if (rows <= 0) break;
+      const int b = (rows + 15) / 16 - 1;
+      const int pos = bucket_base[b] + atomicAdd(&bucket_fill[b], 1);
+      if (pos < max_tiles) tiles[pos] = make_int4(e, start + i * sz, rows, 0);
+    }
+  }
+  __syncthreads();
+  // gate/up units: tile-major, feature tiles of 128 (I/128 routed, Is/128 shared)
+  const int nt_all = n_tiles_s;
+  if (tid == 0) scan_carry = 0;
+  __syncthreads();
+  for (int base = 0; base < nt_all; base += blockDim.x) {
+    const int i = base + tid;
+    int f = 0;
+    if (i < nt_all) f = (tiles[i].x == p.E) ? p.Is / 128 : p.I / 128;
+    int incl = f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int s = warp_sums[lane];
+      int si = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xFFFFFFFFu, si, o);
+        if (lane >= o) si += y;
+      }
+      warp_sums[lane] = si - s;
+    }
+    __syncthreads();
+    const int ub = scan_carry + warp_sums[warp] + incl - f;
+    for (int ft = 0; ft < f; ++ft) units_gu[ub + ft] = (i << 8) | ft;
+    __syncthreads();
+    if (tid == blockDim.x - 1) scan_carry = ub + f;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    hdr->n_tiles = nt_all;
+    hdr->n_units_gu = scan_carry;
+    hdr->n_units_dn = nt_all * (p.h / 128);
+  }
+}
+
+// Per-row shared-expert gate sigmoid(x_r . g): one warp per row.
+__global__ void shared_gate_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ g, int t, int h,
+                                   float* __restrict__ out) {
+  const int r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (r >= t) return;
+  float d = 0.f;
+  for (int i = lane * 8; i < h; i += 256) {
+    const uint4 xv = *reinterpret_cast<const uint4*>(x + (size_t)r * h + i);
+    const uint4 gv = *reinterpret_cast<const uint4*>(g + i);
+    const uint32_t* xa = &xv.x;
+    const uint32_t* ga = &gv.x;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      d = fmaf(bf16lo(xa[c]), bf16lo(ga[c]), d);
+      d = fmaf(bf16hi(xa[c]), bf16hi(ga[c]), d);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xFFFFFFFFu, d, o);
+  if (lane == 0) out[r] = 1.f / (1.f + expf(-d));
+}
+
+// ----------------------------------------------------------------------------
+// Gate/up kernel
+// ----------------------------------------------------------------------------
+struct GuSmem {
+  uint64_t code_full[GU_SC], code_empty[GU_SC];
+  uint64_t a_full[GU_SA], a_empty[GU_SA];
+  uint64_t b_full[GU_SB], b_empty[GU_SB];
+  uint64_t acc_full, acc_empty, drain;
+  uint32_t tmem_slot;
+  int abort;
+  int rowidx[TILE_MAX];
+};
+constexpr size_t GU_SMEM = 1024 + (size_t)GU_SA * GU_A_BYTES + (size_t)GU_SB * GU_B_BYTES +
+                           (size_t)GU_SC * GU_C_BYTES + sizeof(GuSmem);
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+gateup_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scodes,
+                 const __grid_constant__ CUtensorMap tm_x, TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  uint8_t* a_s = base;
+  uint8_t* b_s = a_s + GU_SA * GU_A_BYTES;
+  uint8_t* c_s = b_s + GU_SB * GU_B_BYTES;
+  GuSmem& S = *reinterpret_cast<GuSmem*>(c_s + GU_SC * GU_C_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = p.h, nkc = h / KC;
+
+  // The fp32 block accumulator starts at zero (atomic mode, or no shared
+  // expert to initialise it); the down kernel runs after this one on the
+  // same stream.
+  if (!p.deterministic || p.Is == 0) {
+    float4* acc4 = reinterpret_cast<float4*>(p.acc);
+    const size_t n4 = (size_t)p.t * h / 4;
+    for (size_t i = (size_t)blockIdx.x * NTHREADS + threadIdx.x; i < n4; i += (size_t)gridDim.x * NTHREADS)
+      acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < GU_SC; ++i) {
+      mbar_init(&S.code_full[i], 1);
+      mbar_init(&S.code_empty[i], 8);
+    }
+    for (int i = 0; i < GU_SA; ++i) {
+      mbar_init(&S.a_full[i], 8);
+      mbar_init(&S.a_empty[i], 1);
+    }
+    for (int i = 0; i < GU_SB; ++i) {
+      mbar_init(&S.b_full[i], 1);
+      mbar_init(&S.b_empty[i], 1);
+    }
+    mbar_init(&S.acc_full, 1);
+    mbar_init(&S.acc_empty, 8);
+    mbar_init(&S.drain, 1);
+    S.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&S.tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_slot;
+  volatile int* abort = &S.abort;
+  const int n_units = p.hdr->n_units_gu;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_codes);
+      prefetch_tmap(&tm_x);
+      if (p.Is > 0) prefetch_tmap(&tm_scodes);
+    }
+    uint32_t cit = 0, bit = 0;
+    bool armed_c[GU_SC], armed_b[GU_SB];
+    uint32_t par_c[GU_SC], par_b[GU_SB];
+#pragma unroll
+    for (int i = 0; i < GU_SC; ++i) armed_c[i] = false, par_c[i] = 0;
+#pragma unroll
+    for (int i = 0; i < GU_SB; ++i) armed_b[i] = false, par_b[i] = 0;
+    for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
+      const int code = p.units_gu[u];
+      const int4 T = p.tiles[code >> 8];
+      const int ft = code & 255;
+      const bool shared = (T.x == p.E);
+      const int n = T.z, Nm = (n + 15) & ~15;
+      __syncwarp();
+      for (int i = lane; i < Nm; i += 32) {
+        const int r = min(i, n - 1);
+        S.rowidx[i] = shared ? T.y + r : p.rows[T.y + r];
+      }
+      __syncwarp();
+      if (lane == 0) {
+        const CUtensorMap* tmc = shared ? &tm_scodes : &tm_codes;
+        const int rows_per_rec = 3 * (shared ? p.Is : p.I);
+        const int rowg = (shared ? 0 : T.x * rows_per_rec) + ft * 128;
+        const int rowu = rowg + (shared ? p.Is : p.I);
+        for (int kc = 0; kc < nkc; ++kc) {
+          const int sc = cit % GU_SC;
+          if (!mbar_wait(&S.code_empty[sc], ((cit / GU_SC) & 1) ^ 1, abort, WAIT_NS)) {
+            note_timeout(p.status, abort, 11);
+            break;
+          }
+          mbar_arrive_expect_tx(&S.code_full[sc], GU_C_BYTES);
+          tma_load_2d(c_s + sc * GU_C_BYTES, tmc, kc * 32, rowg, &S.code_full[sc]);
+          tma_load_2d(c_s + sc * GU_C_BYTES + 128 * 32, tmc, kc * 32, rowu, &S.code_full[sc]);
+          armed_c[sc] = true;
+          par_c[sc] = (cit / GU_SC) & 1;
+          ++cit;
+          const int sb = bit % GU_SB;
+          if (!mbar_wait(&S.b_empty[sb], ((bit / GU_SB) & 1) ^ 1, abort, WAIT_NS)) {
+            note_timeout(p.status, abort, 12);
+            break;
+          }
+          mbar_arrive_expect_tx(&S.b_full[sb], Nm * 128);
+          uint8_t* bd = b_s + sb * GU_B_BYTES;
+          for (int g = 0; g < Nm / 4; ++g)
+            tma_gather4(bd + g * 512, &tm_x, kc * KC, S.rowidx[4 * g], S.rowidx[4 * g + 1], S.rowidx[4 * g + 2],
+                        S.rowidx[4 * g + 3], &S.b_full[sb]);
+          armed_b[sb] = true;
+          par_b[sb] = (bit / GU_SB) & 1;
+          ++bit;
+        }
+      }
+      __syncwarp();
+    }
+    if (lane == 0 && *abort) {
+      // let issued copies land before the CTA can exit
+      for (int i = 0; i < GU_SC; ++i)
+        if (armed_c[i]) drain_wait(&S.code_full[i], par_c[i]);
+      for (int i = 0; i < GU_SB; ++i)
+        if (armed_b[i]) drain_wait(&S.b_full[i], par_b[i]);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t ait = 0, bit = 0, uit = 0;
+      for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
+        const int code = p.units_gu[u];
+        const int4 T = p.tiles[code >> 8];
+        const int Nm = (T.z + 15) & ~15;
+        const uint32_t idesc = idesc_bf16(128, Nm);
+        if (uit > 0 && !mbar_wait(&S.acc_empty, (uit - 1) & 1, abort, WAIT_NS)) {
+          note_timeout(p.status, abort, 13);
+          break;
+        }
+        tc_fence_after();
+        bool ok = true;
+        for (int kc = 0; kc < nkc; ++kc) {
+          const int sa = ait % GU_SA, sb = bit % GU_SB;
+          if (!mbar_wait(&S.a_full[sa], (ait / GU_SA) & 1, abort, WAIT_NS) ||
+              !mbar_wait(&S.b_full[sb], (bit / GU_SB) & 1, abort, WAIT_NS)) {
+            note_timeout(p.status, abort, 14);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ag = desc_sw128(smem_u32(a_s + sa * GU_A_BYTES));
+          const uint64_t au = desc_sw128(smem_u32(a_s + sa * GU_A_BYTES + 128 * 128));
+          const uint64_t bd = desc_sw128(smem_u32(b_s + sb * GU_B_BYTES));
+#pragma unroll
+          for (int kk = 0; kk < KC / 16; ++kk) {
+            const uint32_t accum = (kc | kk) != 0;
+            mma_bf16(tmem, ag + 2 * kk, bd + 2 * kk, idesc, accum);
+            mma_bf16(tmem + 256, au + 2 * kk, bd + 2 * kk, idesc, accum);
+          }
+          mma_commit(&S.a_empty[sa]);
+          mma_commit(&S.b_empty[sb]);
+          ++ait;
+          ++bit;
+        }
+        if (!ok) break;
+        mma_commit(&S.acc_full);
+      }
+      if (*abort) {
+        mma_commit(&S.drain);  // completes once every MMA issued so far has
+        drain_wait(&S.drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dequant + epilogue
+    const int dw = warp - 2;            // 0..7
+    const int mtx = dw >> 2;            // 0 gate, 1 up
+    const int o = (dw & 3) * 32 + lane; // weight row within the 128-row tile
+    const int q = warp & 3;             // TMEM lane quarter of this warp
+    const int half = dw >> 2;           // column half for the epilogue
+    uint32_t cit = 0, ait = 0, uit = 0;
+    for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
+      const int code = p.units_gu[u];
+      const int4 T = p.tiles[code >> 8];
+      const int ft = code & 255;
+      const bool shared = (T.x == p.E);
+      const int n = T.z, Nm = (n + 15) & ~15;
+      const int Iu = shared ? p.Is : p.I;
+      const int f0 = ft * 128;
+      const size_t goff = (size_t)mtx * Iu * (h / KC) + (size_t)(f0 + o) * (h / KC);
+      const uint16_t* sp = shared ? p.s_scales + goff : p.scales + (size_t)T.x * p.rec_groups + goff;
+      const uint16_t* bp = shared ? p.s_biases + goff : p.biases + (size_t)T.x * p.rec_groups + goff;
+      bool ok = true;
+      for (int kc = 0; kc < nkc; ++kc) {
+        const int sc = cit % GU_SC, sa = ait % GU_SA;
+        const __nv_bfloat162 s2 = bf2_from_half(__ldg(sp + kc));
+        const __nv_bfloat162 b2 = bf2_from_half(__ldg(bp + kc));
+        if (!mbar_wait(&S.code_full[sc], (cit / GU_SC) & 1, abort, WAIT_NS) ||
+            !mbar_wait(&S.a_empty[sa], ((ait / GU_SA) & 1) ^ 1, abort, WAIT_NS)) {
+          note_timeout(p.status, abort, 15);
+          ok = false;
+          break;
+        }
+        const uint4* src = reinterpret_cast<const uint4*>(c_s + sc * GU_C_BYTES + mtx * 128 * 32 + o * 32);
+        const uint4 c0 = src[0], c1 = src[1];
+        const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        dequant_row_store(wd, s2, b2, a_s + sa * GU_A_BYTES + mtx * 128 * 128, o, 0, 8);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&S.a_full[sa]);
+          mbar_arrive(&S.code_empty[sc]);
+        }
+        ++cit;
+        ++ait;
+      }
+      if (!ok) break;
+      // epilogue: TMEM -> silu(gate) * up -> hg (bf16)
+      if (!mbar_wait(&S.acc_full, uit & 1, abort, WAIT_NS)) {
+        note_timeout(p.status, abort, 16);
+        break;
+      }
+      tc_fence_after();
+      const int feat = f0 + q * 32 + lane;
+      uint16_t* dst = shared ? p.hgs + feat : p.hg + feat;
+      const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+      for (int c = half; c * 16 < Nm; c += 2) {
+        uint32_t g[16], v[16];
+        tmem_ld16(lane_base + c * 16, g);
+        tmem_ld16(lane_base + 256 + c * 16, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int col = c * 16 + j;
+          if (col < n) dst[(size_t)(T.y + col) * Iu] = f2bf(silu_mul(__uint_as_float(g[j]), __uint_as_float(v[j])));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.acc_empty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// Down kernel
+// ----------------------------------------------------------------------------
+struct DnSmem {
+  uint64_t code_full[DN_SC], code_empty[DN_SC];
+  uint64_t a_full[DN_SA], a_empty[DN_SA];
+  uint64_t b_full[DN_SB], b_empty[DN_SB];
+  uint64_t acc_full, acc_empty, drain;
+  uint32_t tmem_slot;
+  int abort;
+};
+constexpr size_t DN_SMEM = 1024 + (size_t)DN_SA * DN_A_BYTES + (size_t)DN_SB * DN_B_BYTES +
+                           (size_t)DN_SC * DN_C_BYTES + sizeof(DnSmem);
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+down_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scodes,
+               const __grid_constant__ CUtensorMap tm_hg, const __grid_constant__ CUtensorMap tm_hgs, TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  uint8_t* a_s = base;
+  uint8_t* b_s = a_s + DN_SA * DN_A_BYTES;
+  uint8_t* c_s = b_s + DN_SB * DN_B_BYTES;
+  DnSmem& S = *reinterpret_cast<DnSmem*>(c_s + DN_SC * DN_C_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = p.h;
+  const int nmt = h / 128;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < DN_SC; ++i) {
+      mbar_init(&S.code_full[i], 1);
+      mbar_init(&S.code_empty[i], 8);
+    }
+    for (int i = 0; i < DN_SA; ++i) {
+      mbar_init(&S.a_full[i], 8);
+      mbar_init(&S.a_empty[i], 1);
+    }
+    for (int i = 0; i < DN_SB; ++i) {
+      mbar_init(&S.b_full[i], 1);
+      mbar_init(&S.b_empty[i], 1);
+    }
+    mbar_init(&S.acc_full, 1);
+    mbar_init(&S.acc_empty, 8);
+    mbar_init(&S.drain, 1);
+    S.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&S.tmem_slot, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_slot;
+  volatile int* abort = &S.abort;
+  const int n_units = p.hdr->n_units_dn;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tm_codes);
+      prefetch_tmap(&tm_hg);
+      if (p.Is > 0) {
+        prefetch_tmap(&tm_scodes);
+        prefetch_tmap(&tm_hgs);
+      }
+      uint32_t cit = 0, bit = 0;
+      bool armed_c[DN_SC], armed_b[DN_SB];
+      uint32_t par_c[DN_SC], par_b[DN_SB];
+      for (int i = 0; i < DN_SC; ++i) armed_c[i] = false, par_c[i] = 0;
+      for (int i = 0; i < DN_SB; ++i) armed_b[i] = false, par_b[i] = 0;
+      bool stop = false;
+      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+        const int4 T = p.tiles[u / nmt];
+        const int mt = u % nmt;
+        const bool shared = (T.x == p.E);
+        const int Nm = (T.z + 15) & ~15;
+        const int K = shared ? p.Is : p.I;
+        const CUtensorMap* tmc = shared ? &tm_scodes : &tm_codes;
+        const CUtensorMap* tmb = shared ? &tm_hgs : &tm_hg;
+        const int rowd = (shared ? 0 : T.x * 3 * h) + 2 * h + mt * 128;
+        for (int kc = 0; kc < K / KC; ++kc) {
+          const int sc = cit % DN_SC;
+          if (!mbar_wait(&S.code_empty[sc], ((cit / DN_SC) & 1) ^ 1, abort, WAIT_NS)) {
+            note_timeout(p.status, abort, 21);
+            stop = true;
+            break;
+          }
+          mbar_arrive_expect_tx(&S.code_full[sc], DN_C_BYTES);
+          tma_load_2d(c_s + sc * DN_C_BYTES, tmc, kc * 32, rowd, &S.code_full[sc]);
+          armed_c[sc] = true;
+          par_c[sc] = (cit / DN_SC) & 1;
+          ++cit;
+          const int sb = bit % DN_SB;
+          if (!mbar_wait(&S.b_empty[sb], ((bit / DN_SB) & 1) ^ 1, abort, WAIT_NS)) {
+            note_timeout(p.status, abort, 22);
+            stop = true;
+            break;
+          }
+          mbar_arrive_expect_tx(&S.b_full[sb], Nm * 128);
+          uint8_t* bd = b_s + sb * DN_B_BYTES;
+          for (int g = 0; g < Nm / 16; ++g) tma_load_2d(bd + g * 2048, tmb, kc * KC, T.y + 16 * g, &S.b_full[sb]);
+          armed_b[sb] = true;
+          par_b[sb] = (bit / DN_SB) & 1;
+          ++bit;
+        }
+        if (*abort) stop = true;
+      }
+      if (*abort) {
+        for (int i = 0; i < DN_SC; ++i)
+          if (armed_c[i]) drain_wait(&S.code_full[i], par_c[i]);
+        for (int i = 0; i < DN_SB; ++i)
+          if (armed_b[i]) drain_wait(&S.b_full[i], par_b[i]);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t ait = 0, bit = 0, uit = 0;
+      for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
+        const int4 T = p.tiles[u / nmt];
+        const bool shared = (T.x == p.E);
+        const int Nm = (T.z + 15) & ~15;
+        const int K = shared ? p.Is : p.I;
+        const uint32_t idesc = idesc_bf16(128, Nm);
+        if (uit > 0 && !mbar_wait(&S.acc_empty, (uit - 1) & 1, abort, WAIT_NS)) {
+          note_timeout(p.status, abort, 23);
+          break;
+        }
+        tc_fence_after();
+        bool ok = true;
+        for (int kc = 0; kc < K / KC; ++kc) {
+          const int sa = ait % DN_SA, sb = bit % DN_SB;
+          if (!mbar_wait(&S.a_full[sa], (ait / DN_SA) & 1, abort, WAIT_NS) ||
+              !mbar_wait(&S.b_full[sb], (bit / DN_SB) & 1, abort, WAIT_NS)) {
+            note_timeout(p.status, abort, 24);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = desc_sw128(smem_u32(a_s + sa * DN_A_BYTES));
+          const uint64_t bd = desc_sw128(smem_u32(b_s + sb * DN_B_BYTES));
+#pragma unroll
+          for (int kk = 0; kk < KC / 16; ++kk) mma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kc | kk) != 0);
+          mma_commit(&S.a_empty[sa]);
+          mma_commit(&S.b_empty[sb]);
+          ++ait;
+          ++bit;
+        }
+        if (!ok) break;
+        mma_commit(&S.acc_full);
+      }
+      if (*abort) {
+        mma_commit(&S.drain);
+        drain_wait(&S.drain, 0);
+      }
+    }
+  } else {
+    const int dw = warp - 2;             // 0..7
+    const int o = (dw & 3) * 32 + lane;  // weight row
+    const int khalf = dw >> 2;           // which 32 of the 64 K of a chunk
+    const int q = warp & 3;
+    const int half = dw >> 2;
+    uint32_t cit = 0, ait = 0, uit = 0;
+    for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
+      const int4 T = p.tiles[u / nmt];
+      const int mt = u % nmt;
+      const bool shared = (T.x == p.E);
+      const int n = T.z, Nm = (n + 15) & ~15;
+      const int K = shared ? p.Is : p.I;
+      const int m0 = mt * 128;
+      const size_t goff = (size_t)2 * K * (h / KC) + (size_t)(m0 + o) * (K / KC);
+      const uint16_t* sp = shared ? p.s_scales + goff : p.scales + (size_t)T.x * p.rec_groups + goff;
+      const uint16_t* bp = shared ? p.s_biases + goff : p.biases + (size_t)T.x * p.rec_groups + goff;
+      bool ok = true;
+      for (int kc = 0; kc < K / KC; ++kc) {
+        const int sc = cit % DN_SC, sa = ait % DN_SA;
+        const __nv_bfloat162 s2 = bf2_from_half(__ldg(sp + kc));
+        const __nv_bfloat162 b2 = bf2_from_half(__ldg(bp + kc));
+        if (!mbar_wait(&S.code_full[sc], (cit / DN_SC) & 1, abort, WAIT_NS) ||
+            !mbar_wait(&S.a_empty[sa], ((ait / DN_SA) & 1) ^ 1, abort, WAIT_NS)) {
+          note_timeout(p.status, abort, 25);
+          ok = false;
+          break;
+        }
+        const uint4 cw = *reinterpret_cast<const uint4*>(c_s + sc * DN_C_BYTES + o * 32 + khalf * 16);
+        const uint32_t wd[8] = {cw.x, cw.y, cw.z, cw.w, 0u, 0u, 0u, 0u};
+        dequant_row_store(wd, s2, b2, a_s + sa * DN_A_BYTES, o, khalf * 4, 4);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&S.a_full[sa]);
+          mbar_arrive(&S.code_empty[sc]);
+        }
+        ++cit;
+        ++ait;
+      }
+      if (!ok) break;
+      if (!mbar_wait(&S.acc_full, uit & 1, abort, WAIT_NS)) {
+        note_timeout(p.status, abort, 26);
+        break;
+      }
+      tc_fence_after();
+      const int f = m0 + q * 32 + lane;
+      const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+      for (int c = half; c * 16 < Nm; c += 2) {
+        uint32_t y[16];
+        tmem_ld16(lane_base + c * 16, y);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int col = c * 16 + j;
+          if (col >= n) break;
+          const float yv = __uint_as_float(y[j]);
+          if (shared) {
+            const int r = T.y + col;
+            const float gr = p.gate_vals ? p.gate_vals[r] : 1.f;
+            if (p.deterministic) p.acc[(size_t)r * h + f] = gr * yv;
+            else atomicAdd(&p.acc[(size_t)r * h + f], gr * yv);
+          } else {
+            const int pos = T.y + col;
+            if (p.deterministic) {
+              p.ybuf[(size_t)pos * h + f] = yv;
+            } else {
+              const int r = p.rows[pos];
+              if (r >= 0 && r < p.t) atomicAdd(&p.acc[(size_t)r * h + f], p.weights[pos] * yv);
+              else if (f == 0) raise_flag(p.status, FLAG_BAD_ROW);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.acc_empty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// Host side
+// ----------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2D map: width (elements), height (rows), row stride bytes, box {bw, bh}.
+cudaError_t make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t width, uint64_t height,
+                     uint64_t stride_bytes, uint32_t bw, uint32_t bh, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {width, height};
+  cuuint64_t strides[1] = {stride_bytes};
+  cuuint32_t box[2] = {bw, bh};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+}  // namespace
+
+size_t tc_max_tiles(const moe_dims& d) {
+  return (size_t)d.t * d.k / TILE_MAX + d.E + d.t / TILE_MAX + 2;
+}
+
+size_t tc_sched_bytes(const moe_dims& d) {
+  const size_t mt = tc_max_tiles(d);
+  const int fmax = (d.inter > d.shared_inter ? d.inter : d.shared_inter) / 128;
+  return sizeof(SchedHdr) + mt * sizeof(int4) + mt * fmax * sizeof(int) + (size_t)d.t * sizeof(float) + 256;
+}
+
+cudaError_t launch_experts_tc(const ExpertsArgs& a, bool deterministic, cudaStream_t stream) {
+  moe_dims d{a.t, a.h, a.I, a.E, a.k, a.Is};
+  const size_t mt = tc_max_tiles(d);
+  const int fmax = (a.I > a.Is ? a.I : a.Is) / 128;
+  SchedHdr* hdr = reinterpret_cast<SchedHdr*>(a.sched);
+  int4* tiles = reinterpret_cast<int4*>(a.sched + sizeof(SchedHdr));
+  int* units = reinterpret_cast<int*>(tiles + mt);
+  float* gate_vals = reinterpret_cast<float*>(units + mt * fmax);
+
+  TcParams p{};
+  p.t = a.t;
+  p.h = a.h;
+  p.I = a.I;
+  p.Is = a.Is;
+  p.E = a.E;
+  p.k = a.k;
+  p.deterministic = deterministic ? 1 : 0;
+  p.offsets = a.offsets;
+  p.rows = a.rows;
+  p.weights = a.weights;
+  p.scales = a.scales;
+  p.biases = a.biases;
+  p.rec_groups = a.rec_groups;
+  p.s_scales = a.s_scales;
+  p.s_biases = a.s_biases;
+  p.gate_vals = (a.Is > 0 && a.s_gate) ? gate_vals : nullptr;
+  p.acc = a.acc;
+  p.hg = a.hg;
+  p.hgs = a.hgs;
+  p.ybuf = a.ybuf;
+  p.hdr = hdr;
+  p.tiles = tiles;
+  p.units_gu = units;
+  p.status = a.status;
+
+  CUtensorMap tm_codes_gu, tm_scodes_gu, tm_x, tm_codes_dn, tm_scodes_dn, tm_hg, tm_hgs;
+  cudaError_t err;
+  const uint64_t h = a.h, I = a.I, Is = a.Is;
+  // codes viewed as rows of h/2 bytes (gate/up) or I/2 bytes (down)
+  if ((err = make_map(&tm_codes_gu, a.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, h / 2, (uint64_t)a.E * 3 * I, h / 2, 32,
+                      128, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+    return err;
+  if ((err = make_map(&tm_codes_dn, a.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, I / 2, (uint64_t)a.E * 3 * h, I / 2, 32,
+                      128, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+    return err;
+  if ((err = make_map(&tm_x, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, a.t, h * 2, 64, 1,
+                      CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    return err;
+  if ((err = make_map(&tm_hg, a.hg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, I, (uint64_t)a.t * a.k, I * 2, 64, 16,
+                      CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    return err;
+  if (Is > 0) {
+    if ((err = make_map(&tm_scodes_gu, a.s_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, h / 2, 3 * Is, h / 2, 32, 128,
+                        CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+      return err;
+    if ((err = make_map(&tm_scodes_dn, a.s_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, Is / 2, 3 * h, Is / 2, 32, 128,
+                        CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+      return err;
+    if ((err = make_map(&tm_hgs, a.hgs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Is, a.t, Is * 2, 64, 16,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+      return err;
+  } else {
+    tm_scodes_gu = tm_codes_gu;
+    tm_scodes_dn = tm_codes_dn;
+    tm_hgs = tm_hg;
+  }
+
+  static bool attr_done = false;
+  if (!attr_done) {
+    if ((err = cudaFuncSetAttribute(gateup_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GU_SMEM)) !=
+        cudaSuccess)
+      return err;
+    if ((err = cudaFuncSetAttribute(down_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DN_SMEM)) !=
+        cudaSuccess)
+      return err;
+    attr_done = true;
+  }
+
+  MOE_LAUNCH("schedule", stream, schedule_kernel<<<1, 1024, 0, stream>>>(p, hdr, tiles, units, (int)mt));
+  if (p.gate_vals)
+    MOE_LAUNCH("shared_gate", stream,
+               shared_gate_kernel<<<(a.t + 7) / 8, 256, 0, stream>>>(a.x, a.s_gate, a.t, a.h, gate_vals));
+  const int grid = num_sms();
+  MOE_LAUNCH("gateup_tc", stream,
+             gateup_tc_kernel<<<grid, NTHREADS, GU_SMEM, stream>>>(tm_codes_gu, tm_scodes_gu, tm_x, p));
+  MOE_LAUNCH("down_tc", stream,
+             down_tc_kernel<<<grid, NTHREADS, DN_SMEM, stream>>>(tm_codes_dn, tm_scodes_dn, tm_hg, tm_hgs, p));
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  return launch_finalize(a, deterministic, stream);
+}
+
+}  // namespace moe
