@@ -43,19 +43,6 @@ constexpr int TILE_MAX = 256;  // rows per tile (MMA N <= 256)
 constexpr int KC = 64;         // K per chunk = one quantisation group
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
-// Gate/up kernel: stages of codes, dequantised A and gathered B.
-constexpr int GU_SC = 6, GU_SA = 2, GU_SB = 3;
-constexpr int GU_A_BYTES = 2 * 128 * 128;    // gate + up, 128 rows x 128 B
-constexpr int GU_B_BYTES = TILE_MAX * 128;   // up to 256 rows x 128 B
-constexpr int GU_C_BYTES = 2 * 128 * 32;     // gate + up codes, 128 rows x 32 B
-// Down kernel
-constexpr int DN_SC = 8, DN_SA = 2, DN_SB = 3;
-constexpr int DN_A_BYTES = 128 * 128;
-constexpr int DN_B_BYTES = TILE_MAX * 128;
-constexpr int DN_C_BYTES = 128 * 32;
-
-constexpr int NWARPS = 10;  // 0 producer, 1 MMA + TMEM owner, 2..9 dequant + epilogue
-constexpr int NTHREADS = NWARPS * 32;
 
 struct SchedHdr {
   int n_tiles;
@@ -275,52 +262,112 @@ __global__ void shared_gate_kernel(const uint16_t* __restrict__ x, const uint16_
 }
 
 // ----------------------------------------------------------------------------
-// Gate/up kernel
+// The grouped GEMM kernel (gate/up or down)
 // ----------------------------------------------------------------------------
-struct GuSmem {
-  uint64_t code_full[GU_SC], code_empty[GU_SC];
-  uint64_t a_full[GU_SA], a_empty[GU_SA];
-  uint64_t b_full[GU_SB], b_empty[GU_SB];
+// Warp roles: 0 code producer (TMA), 1 MMA issuer + TMEM owner, 2..9 dequant +
+// epilogue, 10 B producer (TMA gather4 of token rows, or TMA tiles of hg).
+constexpr int W_CODE = 0, W_MMA = 1, W_DQ0 = 2, W_B = 10;
+constexpr int KWARPS = 11;
+constexpr int KTHREADS = KWARPS * 32;
+constexpr int SA = 2;                 // dequantised A stages (one K-chunk each)
+constexpr int SB = 3;                 // B stages, 32 KB each (KPS K-chunks)
+constexpr int B_STAGE = 32768;
+
+template <bool GATEUP>
+struct Cfg {
+  static constexpr int NMAT = GATEUP ? 2 : 1;         // gate + up, or down
+  static constexpr int CPS = GATEUP ? 2 : 4;          // K-chunks per code stage
+  static constexpr int SC = GATEUP ? 4 : 5;           // code stages
+  static constexpr int C_STAGE = NMAT * 128 * CPS * 32;
+  static constexpr int A_STAGE = NMAT * 128 * 128;
+  static constexpr int TMEM_COLS = GATEUP ? 512 : 256;
+};
+
+template <bool GATEUP>
+struct KSmem {
+  uint64_t code_full[Cfg<GATEUP>::SC], code_empty[Cfg<GATEUP>::SC];
+  uint64_t a_full[SA], a_empty[SA];
+  uint64_t b_full[SB], b_empty[SB];
   uint64_t acc_full, acc_empty, drain;
   uint32_t tmem_slot;
   int abort;
   int rowidx[TILE_MAX];
 };
-constexpr size_t GU_SMEM = 1024 + (size_t)GU_SA * GU_A_BYTES + (size_t)GU_SB * GU_B_BYTES +
-                           (size_t)GU_SC * GU_C_BYTES + sizeof(GuSmem);
 
-__global__ void __launch_bounds__(NTHREADS, 1)
-gateup_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scodes,
-                 const __grid_constant__ CUtensorMap tm_x, TcParams p) {
+template <bool GATEUP>
+constexpr size_t kernel_smem() {
+  return 1024 + (size_t)SA * Cfg<GATEUP>::A_STAGE + (size_t)SB * B_STAGE +
+         (size_t)Cfg<GATEUP>::SC * Cfg<GATEUP>::C_STAGE + sizeof(KSmem<GATEUP>);
+}
+
+// What a unit is, decoded identically by every role.
+struct Unit {
+  int e;        // expert, E = shared
+  int start;    // first CSR position (routed) or row (shared)
+  int n;        // rows
+  int Nm;       // MMA N = rows rounded up to 16
+  int f0;       // first output feature of the unit
+  int nkc;      // K-chunks
+  int kps;      // K-chunks per B stage
+  bool shared;
+};
+
+template <bool GATEUP>
+__device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
+  Unit U;
+  int4 T;
+  if (GATEUP) {
+    const int code = p.units_gu[u];
+    T = p.tiles[code >> 8];
+    U.f0 = (code & 255) * 128;
+  } else {
+    const int nmt = p.h / 128;
+    T = p.tiles[u / nmt];
+    U.f0 = (u % nmt) * 128;
+  }
+  U.e = T.x;
+  U.start = T.y;
+  U.n = T.z;
+  U.Nm = (T.z + 15) & ~15;
+  U.shared = (T.x == p.E);
+  U.nkc = GATEUP ? p.h / KC : (U.shared ? p.Is : p.I) / KC;
+  U.kps = min(TILE_MAX / U.Nm, U.nkc);
+  return U;
+}
+
+template <bool GATEUP>
+__global__ void __launch_bounds__(KTHREADS, 1)
+expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scodes,
+                   const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_sb, TcParams p) {
+  using C = Cfg<GATEUP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   uint8_t* a_s = base;
-  uint8_t* b_s = a_s + GU_SA * GU_A_BYTES;
-  uint8_t* c_s = b_s + GU_SB * GU_B_BYTES;
-  GuSmem& S = *reinterpret_cast<GuSmem*>(c_s + GU_SC * GU_C_BYTES);
+  uint8_t* b_s = a_s + SA * C::A_STAGE;
+  uint8_t* c_s = b_s + SB * B_STAGE;
+  KSmem<GATEUP>& S = *reinterpret_cast<KSmem<GATEUP>*>(c_s + C::SC * C::C_STAGE);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = p.h, nkc = h / KC;
+  const int h = p.h;
 
-  // The fp32 block accumulator starts at zero (atomic mode, or no shared
-  // expert to initialise it); the down kernel runs after this one on the
-  // same stream.
-  if (!p.deterministic || p.Is == 0) {
+  if (GATEUP && (!p.deterministic || p.Is == 0)) {
+    // The fp32 block accumulator starts at zero (atomic mode, or no shared
+    // expert to initialise it); the down kernel runs after this one.
     float4* acc4 = reinterpret_cast<float4*>(p.acc);
     const size_t n4 = (size_t)p.t * h / 4;
-    for (size_t i = (size_t)blockIdx.x * NTHREADS + threadIdx.x; i < n4; i += (size_t)gridDim.x * NTHREADS)
+    for (size_t i = (size_t)blockIdx.x * KTHREADS + threadIdx.x; i < n4; i += (size_t)gridDim.x * KTHREADS)
       acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < GU_SC; ++i) {
+    for (int i = 0; i < C::SC; ++i) {
       mbar_init(&S.code_full[i], 1);
       mbar_init(&S.code_empty[i], 8);
     }
-    for (int i = 0; i < GU_SA; ++i) {
+    for (int i = 0; i < SA; ++i) {
       mbar_init(&S.a_full[i], 8);
       mbar_init(&S.a_empty[i], 1);
     }
-    for (int i = 0; i < GU_SB; ++i) {
+    for (int i = 0; i < SB; ++i) {
       mbar_init(&S.b_full[i], 1);
       mbar_init(&S.b_empty[i], 1);
     }
@@ -330,118 +377,147 @@ gateup_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
     S.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(&S.tmem_slot, 512);
+  if (warp == W_MMA) tmem_alloc(&S.tmem_slot, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_slot;
   volatile int* abort = &S.abort;
-  const int n_units = p.hdr->n_units_gu;
+  const int n_units = GATEUP ? p.hdr->n_units_gu : p.hdr->n_units_dn;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == W_CODE) {
+    // ------------------------------------------------------------ code producer
     if (lane == 0) {
       prefetch_tmap(&tm_codes);
-      prefetch_tmap(&tm_x);
       if (p.Is > 0) prefetch_tmap(&tm_scodes);
-    }
-    uint32_t cit = 0, bit = 0;
-    bool armed_c[GU_SC], armed_b[GU_SB];
-    uint32_t par_c[GU_SC], par_b[GU_SB];
+      uint32_t it = 0;
+      bool armed[C::SC];
+      uint32_t par[C::SC];
 #pragma unroll
-    for (int i = 0; i < GU_SC; ++i) armed_c[i] = false, par_c[i] = 0;
+      for (int i = 0; i < C::SC; ++i) armed[i] = false, par[i] = 0;
+      bool stop = false;
+      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+        const Unit U = decode_unit<GATEUP>(p, u);
+        const CUtensorMap* tm = U.shared ? &tm_scodes : &tm_codes;
+        int row0;
+        if (GATEUP) row0 = (U.shared ? 0 : U.e * 3 * p.I) + U.f0;
+        else row0 = (U.shared ? 0 : U.e * 3 * h) + 2 * h + U.f0;
+        const int mstride = U.shared ? p.Is : p.I;  // rows between gate and up
+        for (int kc0 = 0; kc0 < U.nkc; kc0 += C::CPS, ++it) {
+          const int sc = it % C::SC;
+          if (!mbar_wait(&S.code_empty[sc], ((it / C::SC) & 1) ^ 1, abort, WAIT_NS)) {
+            note_timeout(p.status, abort, GATEUP ? 11 : 21);
+            stop = true;
+            break;
+          }
+          mbar_arrive_expect_tx(&S.code_full[sc], C::C_STAGE);
 #pragma unroll
-    for (int i = 0; i < GU_SB; ++i) armed_b[i] = false, par_b[i] = 0;
-    for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
-      const int code = p.units_gu[u];
-      const int4 T = p.tiles[code >> 8];
-      const int ft = code & 255;
-      const bool shared = (T.x == p.E);
-      const int n = T.z, Nm = (n + 15) & ~15;
-      __syncwarp();
-      for (int i = lane; i < Nm; i += 32) {
-        const int r = min(i, n - 1);
-        S.rowidx[i] = shared ? T.y + r : p.rows[T.y + r];
+          for (int m = 0; m < C::NMAT; ++m)
+            tma_load_2d(c_s + sc * C::C_STAGE + m * 128 * C::CPS * 32, tm, kc0 * 32, row0 + m * mstride,
+                        &S.code_full[sc]);
+          armed[sc] = true;
+          par[sc] = (it / C::SC) & 1;
+        }
+        if (*abort) stop = true;
       }
-      __syncwarp();
+      if (*abort)
+        for (int i = 0; i < C::SC; ++i)
+          if (armed[i]) drain_wait(&S.code_full[i], par[i]);
+    }
+  } else if (warp == W_B) {
+    // ------------------------------------------------------------ B producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_b);
+      if (p.Is > 0) prefetch_tmap(&tm_sb);
+    }
+    uint32_t it = 0;
+    bool armed[SB];
+    uint32_t par[SB];
+#pragma unroll
+    for (int i = 0; i < SB; ++i) armed[i] = false, par[i] = 0;
+    for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
+      const Unit U = decode_unit<GATEUP>(p, u);
+      if (GATEUP) {
+        __syncwarp();
+        for (int i = lane; i < U.Nm; i += 32) {
+          const int r = min(i, U.n - 1);
+          S.rowidx[i] = U.shared ? U.start + r : p.rows[U.start + r];
+        }
+        __syncwarp();
+      }
       if (lane == 0) {
-        const CUtensorMap* tmc = shared ? &tm_scodes : &tm_codes;
-        const int rows_per_rec = 3 * (shared ? p.Is : p.I);
-        const int rowg = (shared ? 0 : T.x * rows_per_rec) + ft * 128;
-        const int rowu = rowg + (shared ? p.Is : p.I);
-        for (int kc = 0; kc < nkc; ++kc) {
-          const int sc = cit % GU_SC;
-          if (!mbar_wait(&S.code_empty[sc], ((cit / GU_SC) & 1) ^ 1, abort, WAIT_NS)) {
-            note_timeout(p.status, abort, 11);
+        const CUtensorMap* tm = U.shared ? &tm_sb : &tm_b;
+        for (int kc0 = 0; kc0 < U.nkc; kc0 += U.kps, ++it) {
+          const int sb = it % SB;
+          if (!mbar_wait(&S.b_empty[sb], ((it / SB) & 1) ^ 1, abort, WAIT_NS)) {
+            note_timeout(p.status, abort, GATEUP ? 12 : 22);
             break;
           }
-          mbar_arrive_expect_tx(&S.code_full[sc], GU_C_BYTES);
-          tma_load_2d(c_s + sc * GU_C_BYTES, tmc, kc * 32, rowg, &S.code_full[sc]);
-          tma_load_2d(c_s + sc * GU_C_BYTES + 128 * 32, tmc, kc * 32, rowu, &S.code_full[sc]);
-          armed_c[sc] = true;
-          par_c[sc] = (cit / GU_SC) & 1;
-          ++cit;
-          const int sb = bit % GU_SB;
-          if (!mbar_wait(&S.b_empty[sb], ((bit / GU_SB) & 1) ^ 1, abort, WAIT_NS)) {
-            note_timeout(p.status, abort, 12);
-            break;
+          const int nk = min(U.kps, U.nkc - kc0);
+          mbar_arrive_expect_tx(&S.b_full[sb], (uint32_t)(nk * U.Nm * 128));
+          uint8_t* bd = b_s + sb * B_STAGE;
+          for (int s = 0; s < nk; ++s) {
+            uint8_t* sub = bd + s * U.Nm * 128;
+            if (GATEUP) {
+              for (int g = 0; g < U.Nm / 4; ++g)
+                tma_gather4(sub + g * 512, tm, (kc0 + s) * KC, S.rowidx[4 * g], S.rowidx[4 * g + 1],
+                            S.rowidx[4 * g + 2], S.rowidx[4 * g + 3], &S.b_full[sb]);
+            } else {
+              for (int g = 0; g < U.Nm / 16; ++g)
+                tma_load_2d(sub + g * 2048, tm, (kc0 + s) * KC, U.start + 16 * g, &S.b_full[sb]);
+            }
           }
-          mbar_arrive_expect_tx(&S.b_full[sb], Nm * 128);
-          uint8_t* bd = b_s + sb * GU_B_BYTES;
-          for (int g = 0; g < Nm / 4; ++g)
-            tma_gather4(bd + g * 512, &tm_x, kc * KC, S.rowidx[4 * g], S.rowidx[4 * g + 1], S.rowidx[4 * g + 2],
-                        S.rowidx[4 * g + 3], &S.b_full[sb]);
-          armed_b[sb] = true;
-          par_b[sb] = (bit / GU_SB) & 1;
-          ++bit;
+          armed[sb] = true;
+          par[sb] = (it / SB) & 1;
         }
       }
       __syncwarp();
     }
-    if (lane == 0 && *abort) {
-      // let issued copies land before the CTA can exit
-      for (int i = 0; i < GU_SC; ++i)
-        if (armed_c[i]) drain_wait(&S.code_full[i], par_c[i]);
-      for (int i = 0; i < GU_SB; ++i)
-        if (armed_b[i]) drain_wait(&S.b_full[i], par_b[i]);
-    }
-  } else if (warp == 1) {
+    if (lane == 0 && *abort)
+      for (int i = 0; i < SB; ++i)
+        if (armed[i]) drain_wait(&S.b_full[i], par[i]);
+  } else if (warp == W_MMA) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       uint32_t ait = 0, bit = 0, uit = 0;
       for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
-        const int code = p.units_gu[u];
-        const int4 T = p.tiles[code >> 8];
-        const int Nm = (T.z + 15) & ~15;
-        const uint32_t idesc = idesc_bf16(128, Nm);
+        const Unit U = decode_unit<GATEUP>(p, u);
+        const uint32_t idesc = idesc_bf16(128, U.Nm);
         if (uit > 0 && !mbar_wait(&S.acc_empty, (uit - 1) & 1, abort, WAIT_NS)) {
-          note_timeout(p.status, abort, 13);
+          note_timeout(p.status, abort, GATEUP ? 13 : 23);
           break;
         }
         tc_fence_after();
         bool ok = true;
-        for (int kc = 0; kc < nkc; ++kc) {
-          const int sa = ait % GU_SA, sb = bit % GU_SB;
-          if (!mbar_wait(&S.a_full[sa], (ait / GU_SA) & 1, abort, WAIT_NS) ||
-              !mbar_wait(&S.b_full[sb], (bit / GU_SB) & 1, abort, WAIT_NS)) {
-            note_timeout(p.status, abort, 14);
+        for (int kc = 0; kc < U.nkc && ok; ++kc) {
+          const int sub = kc % U.kps;
+          const int sb = bit % SB;
+          if (sub == 0 && !mbar_wait(&S.b_full[sb], (bit / SB) & 1, abort, WAIT_NS)) {
+            note_timeout(p.status, abort, GATEUP ? 14 : 24);
+            ok = false;
+            break;
+          }
+          const int sa = ait % SA;
+          if (!mbar_wait(&S.a_full[sa], (ait / SA) & 1, abort, WAIT_NS)) {
+            note_timeout(p.status, abort, GATEUP ? 15 : 25);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ag = desc_sw128(smem_u32(a_s + sa * GU_A_BYTES));
-          const uint64_t au = desc_sw128(smem_u32(a_s + sa * GU_A_BYTES + 128 * 128));
-          const uint64_t bd = desc_sw128(smem_u32(b_s + sb * GU_B_BYTES));
+          const uint64_t bd = desc_sw128(smem_u32(b_s + sb * B_STAGE + sub * U.Nm * 128));
 #pragma unroll
-          for (int kk = 0; kk < KC / 16; ++kk) {
-            const uint32_t accum = (kc | kk) != 0;
-            mma_bf16(tmem, ag + 2 * kk, bd + 2 * kk, idesc, accum);
-            mma_bf16(tmem + 256, au + 2 * kk, bd + 2 * kk, idesc, accum);
+          for (int m = 0; m < C::NMAT; ++m) {
+            const uint64_t ad = desc_sw128(smem_u32(a_s + sa * C::A_STAGE + m * 128 * 128));
+#pragma unroll
+            for (int kk = 0; kk < KC / 16; ++kk)
+              mma_bf16(tmem + m * 256, ad + 2 * kk, bd + 2 * kk, idesc, (kc | kk) != 0);
           }
           mma_commit(&S.a_empty[sa]);
-          mma_commit(&S.b_empty[sb]);
           ++ait;
-          ++bit;
+          if (sub == U.kps - 1 || kc == U.nkc - 1) {
+            mma_commit(&S.b_empty[sb]);
+            ++bit;
+          }
         }
         if (!ok) break;
         mma_commit(&S.acc_full);
@@ -453,304 +529,125 @@ gateup_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
     }
   } else {
     // ------------------------------------------------------------ dequant + epilogue
-    const int dw = warp - 2;            // 0..7
-    const int mtx = dw >> 2;            // 0 gate, 1 up
-    const int o = (dw & 3) * 32 + lane; // weight row within the 128-row tile
-    const int q = warp & 3;             // TMEM lane quarter of this warp
-    const int half = dw >> 2;           // column half for the epilogue
+    const int dw = warp - W_DQ0;         // 0..7
+    const int o = (dw & 3) * 32 + lane;  // weight row within the 128-row tile
+    const int mtx = GATEUP ? (dw >> 2) : 0;
+    const int khalf = GATEUP ? 0 : (dw >> 2);  // down: two threads per row, 32 K each
+    const int q = warp & 3;              // this warp's TMEM lane quarter
+    const int half = dw >> 2;            // epilogue column half
     uint32_t cit = 0, ait = 0, uit = 0;
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
-      const int code = p.units_gu[u];
-      const int4 T = p.tiles[code >> 8];
-      const int ft = code & 255;
-      const bool shared = (T.x == p.E);
-      const int n = T.z, Nm = (n + 15) & ~15;
-      const int Iu = shared ? p.Is : p.I;
-      const int f0 = ft * 128;
-      const size_t goff = (size_t)mtx * Iu * (h / KC) + (size_t)(f0 + o) * (h / KC);
-      const uint16_t* sp = shared ? p.s_scales + goff : p.scales + (size_t)T.x * p.rec_groups + goff;
-      const uint16_t* bp = shared ? p.s_biases + goff : p.biases + (size_t)T.x * p.rec_groups + goff;
-      bool ok = true;
-      for (int kc = 0; kc < nkc; ++kc) {
-        const int sc = cit % GU_SC, sa = ait % GU_SA;
-        const __nv_bfloat162 s2 = bf2_from_half(__ldg(sp + kc));
-        const __nv_bfloat162 b2 = bf2_from_half(__ldg(bp + kc));
-        if (!mbar_wait(&S.code_full[sc], (cit / GU_SC) & 1, abort, WAIT_NS) ||
-            !mbar_wait(&S.a_empty[sa], ((ait / GU_SA) & 1) ^ 1, abort, WAIT_NS)) {
-          note_timeout(p.status, abort, 15);
-          ok = false;
-          break;
-        }
-        const uint4* src = reinterpret_cast<const uint4*>(c_s + sc * GU_C_BYTES + mtx * 128 * 32 + o * 32);
-        const uint4 c0 = src[0], c1 = src[1];
-        const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        dequant_row_store(wd, s2, b2, a_s + sa * GU_A_BYTES + mtx * 128 * 128, o, 0, 8);
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&S.a_full[sa]);
-          mbar_arrive(&S.code_empty[sc]);
-        }
-        ++cit;
-        ++ait;
-      }
-      if (!ok) break;
-      // epilogue: TMEM -> silu(gate) * up -> hg (bf16)
-      if (!mbar_wait(&S.acc_full, uit & 1, abort, WAIT_NS)) {
-        note_timeout(p.status, abort, 16);
-        break;
-      }
-      tc_fence_after();
-      const int feat = f0 + q * 32 + lane;
-      uint16_t* dst = shared ? p.hgs + feat : p.hg + feat;
-      const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-      for (int c = half; c * 16 < Nm; c += 2) {
-        uint32_t g[16], v[16];
-        tmem_ld16(lane_base + c * 16, g);
-        tmem_ld16(lane_base + 256 + c * 16, v);
-        tmem_ld_wait();
+      const Unit U = decode_unit<GATEUP>(p, u);
+      const int K = GATEUP ? h : (U.shared ? p.Is : p.I);
+      const int Iu = U.shared ? p.Is : p.I;
+      // scale/bias of (row f0 + o, group kc): matrix offset + row offset
+      size_t goff;
+      if (GATEUP) goff = (size_t)mtx * Iu * (h / KC) + (size_t)(U.f0 + o) * (h / KC);
+      else goff = (size_t)2 * Iu * (h / KC) + (size_t)(U.f0 + o) * (K / KC);
+      const uint16_t* sp = U.shared ? p.s_scales + goff : p.scales + (size_t)U.e * p.rec_groups + goff;
+      const uint16_t* bp = U.shared ? p.s_biases + goff : p.biases + (size_t)U.e * p.rec_groups + goff;
+      uint16_t s_cur[4], b_cur[4], s_nxt[4], b_nxt[4];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int col = c * 16 + j;
-          if (col < n) dst[(size_t)(T.y + col) * Iu] = f2bf(silu_mul(__uint_as_float(g[j]), __uint_as_float(v[j])));
+      for (int j = 0; j < 4; ++j) {
+        s_cur[j] = j < U.nkc ? __ldg(sp + j) : 0;
+        b_cur[j] = j < U.nkc ? __ldg(bp + j) : 0;
+      }
+      bool ok = true;
+      for (int kc0 = 0; kc0 < U.nkc && ok; kc0 += 4) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          s_nxt[j] = kc0 + 4 + j < U.nkc ? __ldg(sp + kc0 + 4 + j) : 0;
+          b_nxt[j] = kc0 + 4 + j < U.nkc ? __ldg(bp + kc0 + 4 + j) : 0;
         }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.acc_empty);
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
-
-// ----------------------------------------------------------------------------
-// Down kernel
-// ----------------------------------------------------------------------------
-struct DnSmem {
-  uint64_t code_full[DN_SC], code_empty[DN_SC];
-  uint64_t a_full[DN_SA], a_empty[DN_SA];
-  uint64_t b_full[DN_SB], b_empty[DN_SB];
-  uint64_t acc_full, acc_empty, drain;
-  uint32_t tmem_slot;
-  int abort;
-};
-constexpr size_t DN_SMEM = 1024 + (size_t)DN_SA * DN_A_BYTES + (size_t)DN_SB * DN_B_BYTES +
-                           (size_t)DN_SC * DN_C_BYTES + sizeof(DnSmem);
-
-__global__ void __launch_bounds__(NTHREADS, 1)
-down_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scodes,
-               const __grid_constant__ CUtensorMap tm_hg, const __grid_constant__ CUtensorMap tm_hgs, TcParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = align1024(smem_raw);
-  uint8_t* a_s = base;
-  uint8_t* b_s = a_s + DN_SA * DN_A_BYTES;
-  uint8_t* c_s = b_s + DN_SB * DN_B_BYTES;
-  DnSmem& S = *reinterpret_cast<DnSmem*>(c_s + DN_SC * DN_C_BYTES);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = p.h;
-  const int nmt = h / 128;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < DN_SC; ++i) {
-      mbar_init(&S.code_full[i], 1);
-      mbar_init(&S.code_empty[i], 8);
-    }
-    for (int i = 0; i < DN_SA; ++i) {
-      mbar_init(&S.a_full[i], 8);
-      mbar_init(&S.a_empty[i], 1);
-    }
-    for (int i = 0; i < DN_SB; ++i) {
-      mbar_init(&S.b_full[i], 1);
-      mbar_init(&S.b_empty[i], 1);
-    }
-    mbar_init(&S.acc_full, 1);
-    mbar_init(&S.acc_empty, 8);
-    mbar_init(&S.drain, 1);
-    S.abort = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) tmem_alloc(&S.tmem_slot, 256);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = S.tmem_slot;
-  volatile int* abort = &S.abort;
-  const int n_units = p.hdr->n_units_dn;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      prefetch_tmap(&tm_codes);
-      prefetch_tmap(&tm_hg);
-      if (p.Is > 0) {
-        prefetch_tmap(&tm_scodes);
-        prefetch_tmap(&tm_hgs);
-      }
-      uint32_t cit = 0, bit = 0;
-      bool armed_c[DN_SC], armed_b[DN_SB];
-      uint32_t par_c[DN_SC], par_b[DN_SB];
-      for (int i = 0; i < DN_SC; ++i) armed_c[i] = false, par_c[i] = 0;
-      for (int i = 0; i < DN_SB; ++i) armed_b[i] = false, par_b[i] = 0;
-      bool stop = false;
-      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
-        const int4 T = p.tiles[u / nmt];
-        const int mt = u % nmt;
-        const bool shared = (T.x == p.E);
-        const int Nm = (T.z + 15) & ~15;
-        const int K = shared ? p.Is : p.I;
-        const CUtensorMap* tmc = shared ? &tm_scodes : &tm_codes;
-        const CUtensorMap* tmb = shared ? &tm_hgs : &tm_hg;
-        const int rowd = (shared ? 0 : T.x * 3 * h) + 2 * h + mt * 128;
-        for (int kc = 0; kc < K / KC; ++kc) {
-          const int sc = cit % DN_SC;
-          if (!mbar_wait(&S.code_empty[sc], ((cit / DN_SC) & 1) ^ 1, abort, WAIT_NS)) {
-            note_timeout(p.status, abort, 21);
-            stop = true;
-            break;
-          }
-          mbar_arrive_expect_tx(&S.code_full[sc], DN_C_BYTES);
-          tma_load_2d(c_s + sc * DN_C_BYTES, tmc, kc * 32, rowd, &S.code_full[sc]);
-          armed_c[sc] = true;
-          par_c[sc] = (cit / DN_SC) & 1;
-          ++cit;
-          const int sb = bit % DN_SB;
-          if (!mbar_wait(&S.b_empty[sb], ((bit / DN_SB) & 1) ^ 1, abort, WAIT_NS)) {
-            note_timeout(p.status, abort, 22);
-            stop = true;
-            break;
-          }
-          mbar_arrive_expect_tx(&S.b_full[sb], Nm * 128);
-          uint8_t* bd = b_s + sb * DN_B_BYTES;
-          for (int g = 0; g < Nm / 16; ++g) tma_load_2d(bd + g * 2048, tmb, kc * KC, T.y + 16 * g, &S.b_full[sb]);
-          armed_b[sb] = true;
-          par_b[sb] = (bit / DN_SB) & 1;
-          ++bit;
-        }
-        if (*abort) stop = true;
-      }
-      if (*abort) {
-        for (int i = 0; i < DN_SC; ++i)
-          if (armed_c[i]) drain_wait(&S.code_full[i], par_c[i]);
-        for (int i = 0; i < DN_SB; ++i)
-          if (armed_b[i]) drain_wait(&S.b_full[i], par_b[i]);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      uint32_t ait = 0, bit = 0, uit = 0;
-      for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
-        const int4 T = p.tiles[u / nmt];
-        const bool shared = (T.x == p.E);
-        const int Nm = (T.z + 15) & ~15;
-        const int K = shared ? p.Is : p.I;
-        const uint32_t idesc = idesc_bf16(128, Nm);
-        if (uit > 0 && !mbar_wait(&S.acc_empty, (uit - 1) & 1, abort, WAIT_NS)) {
-          note_timeout(p.status, abort, 23);
-          break;
-        }
-        tc_fence_after();
-        bool ok = true;
-        for (int kc = 0; kc < K / KC; ++kc) {
-          const int sa = ait % DN_SA, sb = bit % DN_SB;
-          if (!mbar_wait(&S.a_full[sa], (ait / DN_SA) & 1, abort, WAIT_NS) ||
-              !mbar_wait(&S.b_full[sb], (bit / DN_SB) & 1, abort, WAIT_NS)) {
-            note_timeout(p.status, abort, 24);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int kc = kc0 + j;
+          if (kc >= U.nkc) break;
+          const int sub = kc % C::CPS;
+          const int sc = cit % C::SC;
+          const int sa = ait % SA;
+          if ((sub == 0 && !mbar_wait(&S.code_full[sc], (cit / C::SC) & 1, abort, WAIT_NS)) ||
+              !mbar_wait(&S.a_empty[sa], ((ait / SA) & 1) ^ 1, abort, WAIT_NS)) {
+            note_timeout(p.status, abort, GATEUP ? 16 : 26);
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint64_t ad = desc_sw128(smem_u32(a_s + sa * DN_A_BYTES));
-          const uint64_t bd = desc_sw128(smem_u32(b_s + sb * DN_B_BYTES));
-#pragma unroll
-          for (int kk = 0; kk < KC / 16; ++kk) mma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kc | kk) != 0);
-          mma_commit(&S.a_empty[sa]);
-          mma_commit(&S.b_empty[sb]);
+          const __nv_bfloat162 s2 = bf2_from_half(s_cur[j]);
+          const __nv_bfloat162 b2 = bf2_from_half(b_cur[j]);
+          const uint8_t* crow = c_s + sc * C::C_STAGE + mtx * 128 * C::CPS * 32 + o * C::CPS * 32 + sub * 32;
+          uint8_t* atile = a_s + sa * C::A_STAGE + mtx * 128 * 128;
+          if (GATEUP) {
+            const uint4 c0 = reinterpret_cast<const uint4*>(crow)[0];
+            const uint4 c1 = reinterpret_cast<const uint4*>(crow)[1];
+            const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            dequant_row_store(wd, s2, b2, atile, o, 0, 8);
+          } else {
+            const uint4 cw = reinterpret_cast<const uint4*>(crow)[khalf];
+            const uint32_t wd[8] = {cw.x, cw.y, cw.z, cw.w, 0u, 0u, 0u, 0u};
+            dequant_row_store(wd, s2, b2, atile, o, khalf * 4, 4);
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&S.a_full[sa]);
+            if (sub == C::CPS - 1 || kc == U.nkc - 1) mbar_arrive(&S.code_empty[sc]);
+          }
           ++ait;
-          ++bit;
+          if (sub == C::CPS - 1 || kc == U.nkc - 1) ++cit;
         }
-        if (!ok) break;
-        mma_commit(&S.acc_full);
-      }
-      if (*abort) {
-        mma_commit(&S.drain);
-        drain_wait(&S.drain, 0);
-      }
-    }
-  } else {
-    const int dw = warp - 2;             // 0..7
-    const int o = (dw & 3) * 32 + lane;  // weight row
-    const int khalf = dw >> 2;           // which 32 of the 64 K of a chunk
-    const int q = warp & 3;
-    const int half = dw >> 2;
-    uint32_t cit = 0, ait = 0, uit = 0;
-    for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
-      const int4 T = p.tiles[u / nmt];
-      const int mt = u % nmt;
-      const bool shared = (T.x == p.E);
-      const int n = T.z, Nm = (n + 15) & ~15;
-      const int K = shared ? p.Is : p.I;
-      const int m0 = mt * 128;
-      const size_t goff = (size_t)2 * K * (h / KC) + (size_t)(m0 + o) * (K / KC);
-      const uint16_t* sp = shared ? p.s_scales + goff : p.scales + (size_t)T.x * p.rec_groups + goff;
-      const uint16_t* bp = shared ? p.s_biases + goff : p.biases + (size_t)T.x * p.rec_groups + goff;
-      bool ok = true;
-      for (int kc = 0; kc < K / KC; ++kc) {
-        const int sc = cit % DN_SC, sa = ait % DN_SA;
-        const __nv_bfloat162 s2 = bf2_from_half(__ldg(sp + kc));
-        const __nv_bfloat162 b2 = bf2_from_half(__ldg(bp + kc));
-        if (!mbar_wait(&S.code_full[sc], (cit / DN_SC) & 1, abort, WAIT_NS) ||
-            !mbar_wait(&S.a_empty[sa], ((ait / DN_SA) & 1) ^ 1, abort, WAIT_NS)) {
-          note_timeout(p.status, abort, 25);
-          ok = false;
-          break;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          s_cur[j] = s_nxt[j];
+          b_cur[j] = b_nxt[j];
         }
-        const uint4 cw = *reinterpret_cast<const uint4*>(c_s + sc * DN_C_BYTES + o * 32 + khalf * 16);
-        const uint32_t wd[8] = {cw.x, cw.y, cw.z, cw.w, 0u, 0u, 0u, 0u};
-        dequant_row_store(wd, s2, b2, a_s + sa * DN_A_BYTES, o, khalf * 4, 4);
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&S.a_full[sa]);
-          mbar_arrive(&S.code_empty[sc]);
-        }
-        ++cit;
-        ++ait;
       }
       if (!ok) break;
+      // epilogue
       if (!mbar_wait(&S.acc_full, uit & 1, abort, WAIT_NS)) {
-        note_timeout(p.status, abort, 26);
+        note_timeout(p.status, abort, GATEUP ? 17 : 27);
         break;
       }
       tc_fence_after();
-      const int f = m0 + q * 32 + lane;
+      const int feat = U.f0 + q * 32 + lane;
       const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-      for (int c = half; c * 16 < Nm; c += 2) {
-        uint32_t y[16];
-        tmem_ld16(lane_base + c * 16, y);
-        tmem_ld_wait();
+      if (GATEUP) {
+        uint16_t* dst = U.shared ? p.hgs + feat : p.hg + feat;
+        for (int c = half; c * 16 < U.Nm; c += 2) {
+          uint32_t g[16], v[16];
+          tmem_ld16(lane_base + c * 16, g);
+          tmem_ld16(lane_base + 256 + c * 16, v);
+          tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int col = c * 16 + j;
-          if (col >= n) break;
-          const float yv = __uint_as_float(y[j]);
-          if (shared) {
-            const int r = T.y + col;
-            const float gr = p.gate_vals ? p.gate_vals[r] : 1.f;
-            if (p.deterministic) p.acc[(size_t)r * h + f] = gr * yv;
-            else atomicAdd(&p.acc[(size_t)r * h + f], gr * yv);
-          } else {
-            const int pos = T.y + col;
-            if (p.deterministic) {
-              p.ybuf[(size_t)pos * h + f] = yv;
+          for (int j = 0; j < 16; ++j) {
+            const int col = c * 16 + j;
+            if (col < U.n)
+              dst[(size_t)(U.start + col) * Iu] = f2bf(silu_mul(__uint_as_float(g[j]), __uint_as_float(v[j])));
+          }
+        }
+      } else {
+        for (int c = half; c * 16 < U.Nm; c += 2) {
+          uint32_t y[16];
+          tmem_ld16(lane_base + c * 16, y);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int col = c * 16 + j;
+            if (col >= U.n) break;
+            const float yv = __uint_as_float(y[j]);
+            if (U.shared) {
+              const int r = U.start + col;
+              const float gr = p.gate_vals ? p.gate_vals[r] : 1.f;
+              if (p.deterministic) p.acc[(size_t)r * h + feat] = gr * yv;
+              else atomicAdd(&p.acc[(size_t)r * h + feat], gr * yv);
             } else {
-              const int r = p.rows[pos];
-              if (r >= 0 && r < p.t) atomicAdd(&p.acc[(size_t)r * h + f], p.weights[pos] * yv);
-              else if (f == 0) raise_flag(p.status, FLAG_BAD_ROW);
+              const int pos = U.start + col;
+              if (p.deterministic) {
+                p.ybuf[(size_t)pos * h + feat] = yv;
+              } else {
+                const int r = p.rows[pos];
+                if (r >= 0 && r < p.t) atomicAdd(&p.acc[(size_t)r * h + feat], p.weights[pos] * yv);
+                else if (feat == 0) raise_flag(p.status, FLAG_BAD_ROW);
+              }
             }
           }
         }
@@ -763,9 +660,9 @@ down_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_consta
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == W_MMA) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
@@ -865,11 +762,12 @@ cudaError_t launch_experts_tc(const ExpertsArgs& a, bool deterministic, cudaStre
   cudaError_t err;
   const uint64_t h = a.h, I = a.I, Is = a.Is;
   // codes viewed as rows of h/2 bytes (gate/up) or I/2 bytes (down)
-  if ((err = make_map(&tm_codes_gu, a.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, h / 2, (uint64_t)a.E * 3 * I, h / 2, 32,
-                      128, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+  const uint32_t cw_gu = Cfg<true>::CPS * 32, cw_dn = Cfg<false>::CPS * 32;  // code box widths (bytes)
+  if ((err = make_map(&tm_codes_gu, a.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, h / 2, (uint64_t)a.E * 3 * I, h / 2,
+                      cw_gu, 128, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
     return err;
-  if ((err = make_map(&tm_codes_dn, a.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, I / 2, (uint64_t)a.E * 3 * h, I / 2, 32,
-                      128, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+  if ((err = make_map(&tm_codes_dn, a.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, I / 2, (uint64_t)a.E * 3 * h, I / 2,
+                      cw_dn, 128, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
     return err;
   if ((err = make_map(&tm_x, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, a.t, h * 2, 64, 1,
                       CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
@@ -878,10 +776,10 @@ cudaError_t launch_experts_tc(const ExpertsArgs& a, bool deterministic, cudaStre
                       CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
     return err;
   if (Is > 0) {
-    if ((err = make_map(&tm_scodes_gu, a.s_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, h / 2, 3 * Is, h / 2, 32, 128,
+    if ((err = make_map(&tm_scodes_gu, a.s_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, h / 2, 3 * Is, h / 2, cw_gu, 128,
                         CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
       return err;
-    if ((err = make_map(&tm_scodes_dn, a.s_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, Is / 2, 3 * h, Is / 2, 32, 128,
+    if ((err = make_map(&tm_scodes_dn, a.s_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, Is / 2, 3 * h, Is / 2, cw_dn, 128,
                         CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
       return err;
     if ((err = make_map(&tm_hgs, a.hgs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Is, a.t, Is * 2, 64, 16,
@@ -895,11 +793,11 @@ cudaError_t launch_experts_tc(const ExpertsArgs& a, bool deterministic, cudaStre
 
   static bool attr_done = false;
   if (!attr_done) {
-    if ((err = cudaFuncSetAttribute(gateup_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GU_SMEM)) !=
-        cudaSuccess)
+    if ((err = cudaFuncSetAttribute(expert_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kernel_smem<true>())) != cudaSuccess)
       return err;
-    if ((err = cudaFuncSetAttribute(down_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DN_SMEM)) !=
-        cudaSuccess)
+    if ((err = cudaFuncSetAttribute(expert_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kernel_smem<false>())) != cudaSuccess)
       return err;
     attr_done = true;
   }
@@ -910,9 +808,11 @@ cudaError_t launch_experts_tc(const ExpertsArgs& a, bool deterministic, cudaStre
                shared_gate_kernel<<<(a.t + 7) / 8, 256, 0, stream>>>(a.x, a.s_gate, a.t, a.h, gate_vals));
   const int grid = num_sms();
   MOE_LAUNCH("gateup_tc", stream,
-             gateup_tc_kernel<<<grid, NTHREADS, GU_SMEM, stream>>>(tm_codes_gu, tm_scodes_gu, tm_x, p));
+             expert_gemm_kernel<true><<<grid, KTHREADS, kernel_smem<true>(), stream>>>(tm_codes_gu, tm_scodes_gu,
+                                                                                     tm_x, tm_x, p));
   MOE_LAUNCH("down_tc", stream,
-             down_tc_kernel<<<grid, NTHREADS, DN_SMEM, stream>>>(tm_codes_dn, tm_scodes_dn, tm_hg, tm_hgs, p));
+             expert_gemm_kernel<false><<<grid, KTHREADS, kernel_smem<false>(), stream>>>(tm_codes_dn, tm_scodes_dn,
+                                                                                       tm_hg, tm_hgs, p));
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   return launch_finalize(a, deterministic, stream);
 }
