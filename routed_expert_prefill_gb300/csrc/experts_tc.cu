@@ -602,7 +602,30 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
         }
       }
       if (!ok) break;
-      // epilogue
+      // epilogue.  The per-column row index and routing weight are loaded
+      // lane-parallel before the accumulator wait (one load per 32 columns)
+      // and broadcast with shuffles, so no global load sits on the
+      // TMEM -> store path.
+      const int ncw = (U.Nm + 31) / 32;  // 32-column groups
+      int col_row[8];
+      float col_w[8];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        col_row[g] = 0;
+        col_w[g] = 1.f;
+        const int col = g * 32 + lane;
+        if (g < ncw && col < U.n) {
+          if (GATEUP) {
+            col_row[g] = U.start + col;
+          } else if (U.shared) {
+            col_row[g] = U.start + col;
+            col_w[g] = p.gate_vals ? p.gate_vals[U.start + col] : 1.f;
+          } else {
+            col_row[g] = p.rows[U.start + col];
+            col_w[g] = p.weights[U.start + col];
+          }
+        }
+      }
       if (!mbar_wait(&S.acc_full, uit & 1, abort, WAIT_NS)) {
         note_timeout(p.status, abort, GATEUP ? 17 : 27);
         break;
@@ -625,32 +648,36 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
           }
         }
       } else {
+        bool bad_row = false;
         for (int c = half; c * 16 < U.Nm; c += 2) {
           uint32_t y[16];
           tmem_ld16(lane_base + c * 16, y);
           tmem_ld_wait();
+          const int grp = c >> 1;  // 32-column group holding columns c*16 .. c*16+15
+          int rsel = col_row[0];
+          float wsel = col_w[0];
+#pragma unroll
+          for (int g = 1; g < 8; ++g)
+            if (g == grp) rsel = col_row[g], wsel = col_w[g];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = c * 16 + j;
-            if (col >= U.n) break;
+            const int src = (c & 1) * 16 + j;  // lane holding this column's row/weight
+            const int r = __shfl_sync(0xFFFFFFFFu, rsel, src);
+            const float wv = __shfl_sync(0xFFFFFFFFu, wsel, src);
+            if (col >= U.n) continue;
             const float yv = __uint_as_float(y[j]);
-            if (U.shared) {
-              const int r = U.start + col;
-              const float gr = p.gate_vals ? p.gate_vals[r] : 1.f;
-              if (p.deterministic) p.acc[(size_t)r * h + feat] = gr * yv;
-              else atomicAdd(&p.acc[(size_t)r * h + feat], gr * yv);
+            if (p.deterministic) {
+              if (U.shared) p.acc[(size_t)r * h + feat] = wv * yv;
+              else p.ybuf[(size_t)(U.start + col) * h + feat] = yv;
+            } else if (r >= 0 && r < p.t) {
+              atomicAdd(&p.acc[(size_t)r * h + feat], wv * yv);
             } else {
-              const int pos = U.start + col;
-              if (p.deterministic) {
-                p.ybuf[(size_t)pos * h + feat] = yv;
-              } else {
-                const int r = p.rows[pos];
-                if (r >= 0 && r < p.t) atomicAdd(&p.acc[(size_t)r * h + feat], p.weights[pos] * yv);
-                else if (feat == 0) raise_flag(p.status, FLAG_BAD_ROW);
-              }
+              bad_row = true;
             }
           }
         }
+        if (bad_row && lane == 0) raise_flag(p.status, FLAG_BAD_ROW);
       }
       tc_fence_before();
       __syncwarp();
