@@ -101,6 +101,7 @@ typedef struct {
 #define MOE_FORCE_SMALL_T 0x2u /* force the weight-streaming small-t kernels */
 #define MOE_FORCE_LARGE_T 0x4u /* force the tensor-core grouped GEMM kernels */
 #define MOE_SIMPLE_KERNELS 0x8u /* plain CUDA-core kernels (slow; a cross-check path) */
+#define MOE_PACKED_WEIGHTS 0x10u /* experts->codes and shared->codes hold moe_pack_experts output */
 
 /* Thread-local message of the last failed call on this thread ("" if none). */
 const char* moe_last_error(void);
@@ -169,6 +170,30 @@ int moe_build_csr(const int32_t* idx, const float* w, const moe_dims* dims,
 int moe_experts_fwd(const uint16_t* x, const moe_csr* csr, const moe_qweights* experts,
                     const moe_shared* shared, uint16_t* out, const moe_dims* dims,
                     uint32_t flags, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Weight packing (a one-time, model-load step; no counterpart in the method).
+ * Rewrites row-major 4-bit expert records (the moe_qweights layout) into
+ * tile-contiguous blocks that moe_experts_fwd streams with one bulk copy per
+ * 64-wide K chunk.  Per record: the gate/up part, for each 128-row feature
+ * tile and each 64-wide K chunk, a gate block then an up block; then the
+ * down part, for each 128-row tile of h and each 64-wide K chunk of inter, a
+ * down block.  A block is 128 rows x 32 bytes of codes (each 32-bit word holds
+ * 8 consecutive K: the even ones in its low 16 bits, the odd ones in its high
+ * 16 bits, 4 bits each, lowest K first), then 128 bf16 scales, then 128 bf16
+ * biases (4608 bytes).  Scales and biases are rounded from fp16 to bf16 (round
+ * to nearest even), the rounding the kernels apply anyway.
+ *
+ * shared = 0: the E routed records (inter); shared = 1: the shared expert's
+ * record (shared_inter; scales/biases of moe_shared, passed as moe_qweights).
+ * dst: device buffer of at least moe_packed_bytes(dims, shared) bytes,
+ * 16-byte aligned.  Pass the packed buffers to moe_experts_fwd in
+ * experts->codes / shared->codes with flag MOE_PACKED_WEIGHTS (scales and
+ * biases may then be NULL).  Errors: MOE_EINVAL, MOE_ESHAPE, MOE_ECUDA.
+ */
+size_t moe_packed_bytes(const moe_dims* dims, int shared);
+int moe_pack_experts(const moe_qweights* src, const moe_dims* dims, int shared, void* dst, size_t dst_bytes,
+                     void* stream);
 
 /* Workspace bytes needed by moe_build_csr and moe_experts_fwd for `dims` and
  * `flags` (one buffer serves both calls on one stream).  0 on bad dims. */

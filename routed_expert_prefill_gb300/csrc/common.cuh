@@ -85,6 +85,7 @@ struct WsLayout {
   size_t hg;            // bf16 [t*k][inter]
   size_t hgs;           // bf16 [t][shared_inter]
   size_t ybuf;          // float [t*k][h] (deterministic only)
+  size_t xg;            // bf16 gathered token images (packed-weight path only)
   size_t sched;         // scheduler state (counters, tile lists)
   size_t total;
 };

@@ -1,0 +1,663 @@
+// Expert FFNs on pre-packed (tile-contiguous) weights: the streaming-friendly
+// form of the grouped GEMMs of cherenkov qwen4_exp, prefill/experts.rs,
+// pf_experts (gather_rows -> gate/up quantised matmuls -> silu_mul -> down
+// quantised matmul -> scatter_add_rows, plus the shared expert).
+//
+// Packed weight record (moe_pack_experts), per expert (the shared expert has
+// its own record with inter = shared_inter):
+//   gate/up part: for each 128-row feature tile rt, for each 64-wide K chunk
+//     kc: [gate block][up block], where a block is 128 rows x 32 bytes of
+//     4-bit codes, then 128 bf16 scales, then 128 bf16 biases (4608 bytes).
+//   down part: for each 128-row tile of h, for each 64-wide K chunk of
+//     inter: one block.
+//   Inside each 32-bit word of codes (8 consecutive K), even K sit in the low
+//   half and odd K in the high half (K0 K2 K4 K6 | K1 K3 K5 K7, 4 bits each),
+//   so (word >> 4i) & 0x000F000F is the pair (K2i, K2i+1).
+// Scales and biases are rounded to bf16 once, when packing.
+//
+// Per call:
+//   schedule: tiles of <= 128 rows per expert, largest first, each with a
+//     padded-row offset (rows rounded up to 16).
+//   gather:   the token rows of every tile are copied, chunk by chunk, into
+//     the 128-byte-swizzled K-major image the MMA reads (xg), so one bulk
+//     copy moves a whole B stage.
+//   gateup:   warp 0 streams packed weight blocks (one bulk copy per K
+//     chunk), warp 10 streams xg stages, eight warps dequantise one weight
+//     row each (w = fma(q, s, b) in bf16) straight into TMEM with
+//     tcgen05.st, warp 1 issues tcgen05.mma with A in TMEM and B in shared
+//     memory, and the eight warps read the gate and up accumulators back,
+//     apply silu(gate) * up and write hg, again as swizzled K-major images.
+//   down:     the same pipeline on the down blocks and hg images; the
+//     epilogue scales by the routing weight and adds into the fp32 block
+//     accumulator (atomics) or, deterministic mode, stores per list position.
+#include "tc_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+using namespace tc;
+
+constexpr int PTILE = 128;  // rows per tile: MMA N <= 128
+constexpr int KC = 64;      // K per chunk = one quantisation group
+constexpr int QB = 4096 + 256 + 256;  // one packed 128 x 64 block
+constexpr uint64_t WAIT_NS = 2000000000ull;
+
+constexpr int W_CODE = 0, W_MMA = 1, W_DQ0 = 2, W_B = 10;
+constexpr int KWARPS = 11;
+constexpr int KTHREADS = KWARPS * 32;
+constexpr int SB = 4;                 // B stages
+constexpr int B_STAGE = 32768;        // bytes: KPS chunks of Nm rows x 128 B
+constexpr int ACC_UP = 128;           // TMEM column of the up accumulator
+constexpr int A_COL = 256;            // TMEM columns 256..511 hold the A ring
+
+template <bool GATEUP>
+struct PCfg {
+  static constexpr int NMAT = GATEUP ? 2 : 1;
+  static constexpr int C_STAGE = NMAT * QB;       // one K chunk of packed blocks
+  static constexpr int SC = GATEUP ? 8 : 16;      // code stages
+  static constexpr int SA = GATEUP ? 4 : 8;       // A stages in TMEM
+  static constexpr int A_STRIDE = NMAT * 32;      // TMEM columns per A stage
+};
+
+__host__ __device__ inline size_t gu_bytes(int h, int I) { return (size_t)(I / 128) * (h / KC) * 2 * QB; }
+__host__ __device__ inline size_t rec_bytes(int h, int I) { return gu_bytes(h, I) + (size_t)(h / 128) * (I / KC) * QB; }
+
+__device__ __forceinline__ uint32_t pack_word(uint32_t w) {
+  return (w & 0xFu) | (((w >> 4) & 0xFu) << 16) | (((w >> 8) & 0xFu) << 4) | (((w >> 12) & 0xFu) << 20) |
+         (((w >> 16) & 0xFu) << 8) | (((w >> 20) & 0xFu) << 24) | (((w >> 24) & 0xFu) << 12) |
+         (((w >> 28) & 0xFu) << 28);
+}
+
+// ----------------------------------------------------------------------------
+// Packing: one 128-thread block per packed block (thread = weight row)
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(128)
+pack_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
+            const uint16_t* __restrict__ biases, int h, int I, size_t src_rec_bytes, size_t src_rec_groups,
+            uint8_t* __restrict__ dst) {
+  const int rec = blockIdx.y;
+  const int nkc_gu = h / KC, nkc_d = I / KC;
+  const int nblk_gu = (I / 128) * nkc_gu;  // gate/up block pairs
+  int blk = blockIdx.x;
+  int mat, rt, kc, K, rows;
+  size_t dst_off;
+  if (blk < 2 * nblk_gu) {
+    const int pair = blk >> 1;
+    mat = blk & 1;  // 0 gate, 1 up
+    rt = pair / nkc_gu;
+    kc = pair % nkc_gu;
+    K = h;
+    rows = I;
+    dst_off = (size_t)pair * 2 * QB + (size_t)mat * QB;
+  } else {
+    blk -= 2 * nblk_gu;
+    mat = 2;
+    rt = blk / nkc_d;
+    kc = blk % nkc_d;
+    K = I;
+    rows = h;
+    dst_off = gu_bytes(h, I) + (size_t)blk * QB;
+  }
+  const int o = threadIdx.x;
+  const size_t mat_bytes = (size_t)I * h / 2, mat_groups = (size_t)I * h / KC;
+  const uint8_t* src = codes + rec * src_rec_bytes + mat * mat_bytes + (size_t)(rt * 128 + o) * (K / 2) + kc * 32;
+  const size_t g = rec * src_rec_groups + mat * mat_groups + (size_t)(rt * 128 + o) * (K / KC) + kc;
+  uint8_t* d = dst + rec * rec_bytes(h, I) + dst_off;
+  const uint4 c0 = reinterpret_cast<const uint4*>(src)[0];
+  const uint4 c1 = reinterpret_cast<const uint4*>(src)[1];
+  uint4 p0, p1;
+  p0.x = pack_word(c0.x), p0.y = pack_word(c0.y), p0.z = pack_word(c0.z), p0.w = pack_word(c0.w);
+  p1.x = pack_word(c1.x), p1.y = pack_word(c1.y), p1.z = pack_word(c1.z), p1.w = pack_word(c1.w);
+  reinterpret_cast<uint4*>(d + o * 32)[0] = p0;
+  reinterpret_cast<uint4*>(d + o * 32)[1] = p1;
+  __nv_bfloat16 sb = h2bf(scales[g]), bb = h2bf(biases[g]);
+  reinterpret_cast<__nv_bfloat16*>(d + 4096)[o] = sb;
+  reinterpret_cast<__nv_bfloat16*>(d + 4096 + 256)[o] = bb;
+  (void)rows;
+}
+
+// ----------------------------------------------------------------------------
+// Gather: token rows of every tile -> swizzled K-major images (one block per tile)
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ rows, const SchedHdr* hdr,
+              const int4* __restrict__ tiles, int t, int h, int E, uint16_t* __restrict__ xg, DeviceStatus* st) {
+  if ((int)blockIdx.x >= hdr->n_tiles) return;
+  const int4 T = tiles[blockIdx.x];
+  const int n = T.z, Nm = (n + 15) & ~15;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* base = reinterpret_cast<uint8_t*>(xg + (size_t)T.w * h);
+  const int npieces = h / 8;
+  for (int j = warp; j < Nm; j += 8) {
+    const int jj = min(j, n - 1);
+    int r = (T.x == E) ? T.y + jj : rows[T.y + jj];
+    const bool ok = (r >= 0 && r < t);
+    if (!ok && lane == 0) raise_flag(st, FLAG_BAD_ROW);
+    for (int pc = lane; pc < npieces; pc += 32) {
+      const uint4 v = ok ? reinterpret_cast<const uint4*>(x + (size_t)r * h)[pc] : make_uint4(0, 0, 0, 0);
+      const int kc = pc >> 3, c = pc & 7;
+      *reinterpret_cast<uint4*>(base + (size_t)kc * Nm * 128 + sw128_off(j, c)) = v;
+    }
+  }
+}
+
+__device__ __forceinline__ void note_timeout(DeviceStatus* st, volatile int* abort, uint32_t site) {
+  if (atomicOr(&st->flags, FLAG_TIMEOUT) == 0) st->timeout_site = site;
+  *abort = 1;
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const int never = 0;
+  mbar_wait(bar, parity, &never, 100000000ull);
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&r)[N]);
+template <>
+__device__ __forceinline__ void tmem_st<32>(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_st<16>(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Dequantise packed words (pairs (K2i, K2i+1) at (word >> 4i) & 0x000F000F)
+// to bf16 pairs in natural K order: out[4 * j + i] = (K 8j + 2i, K 8j + 2i + 1).
+template <int NW>
+__device__ __forceinline__ void dequant_packed(const uint32_t* w, __nv_bfloat162 s2, __nv_bfloat162 b2,
+                                               uint32_t* out) {
+  const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.f, 128.f);
+#pragma unroll
+  for (int j = 0; j < NW; ++j) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t v = ((w[j] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
+      __nv_bfloat162 q = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&v), k128);
+      __nv_bfloat162 r = __hfma2(q, s2, b2);
+      out[4 * j + i] = *reinterpret_cast<uint32_t*>(&r);
+    }
+  }
+}
+
+struct PUnit {
+  int e, start, n, Nm, f0, nkc, kps, pad;
+  bool shared;
+};
+
+template <bool GATEUP>
+__device__ __forceinline__ PUnit decode_punit(const TcParams& p, int u) {
+  PUnit U;
+  int4 T;
+  if (GATEUP) {
+    const int code = p.units_gu[u];
+    T = p.tiles[code >> 8];
+    U.f0 = (code & 255) * 128;
+  } else {
+    const int nmt = p.h / 128;
+    T = p.tiles[u / nmt];
+    U.f0 = (u % nmt) * 128;
+  }
+  U.e = T.x;
+  U.start = T.y;
+  U.n = T.z;
+  U.Nm = (T.z + 15) & ~15;
+  U.pad = T.w;
+  U.shared = (T.x == p.E);
+  U.nkc = GATEUP ? p.h / KC : (U.shared ? p.Is : p.I) / KC;
+  U.kps = min(B_STAGE / (U.Nm * 128), U.nkc);
+  return U;
+}
+
+struct PParams {
+  TcParams p;
+  const uint8_t* packed;    // routed records
+  const uint8_t* s_packed;  // shared record
+  const uint16_t* xg;       // gathered token images
+  int kmax;                 // max(I, Is): hg row pitch in the padded space
+};
+
+template <bool GATEUP>
+struct PSmem {
+  uint64_t code_full[PCfg<GATEUP>::SC], code_empty[PCfg<GATEUP>::SC];
+  uint64_t a_full[PCfg<GATEUP>::SA], a_empty[PCfg<GATEUP>::SA];
+  uint64_t b_full[SB], b_empty[SB];
+  uint64_t acc_full, acc_empty, drain;
+  uint32_t tmem_slot;
+  int abort;
+};
+
+template <bool GATEUP>
+constexpr size_t psmem_bytes() {
+  return 1024 + (size_t)SB * B_STAGE + (size_t)PCfg<GATEUP>::SC * PCfg<GATEUP>::C_STAGE + sizeof(PSmem<GATEUP>);
+}
+
+template <bool GATEUP>
+__global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
+  using C = PCfg<GATEUP>;
+  const TcParams& p = P.p;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* b_s = base;
+  uint8_t* c_s = b_s + SB * B_STAGE;
+  PSmem<GATEUP>& S = *reinterpret_cast<PSmem<GATEUP>*>(c_s + C::SC * C::C_STAGE);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = p.h;
+
+  if (GATEUP && (!p.deterministic || p.Is == 0)) {
+    float4* acc4 = reinterpret_cast<float4*>(p.acc);
+    const size_t n4 = (size_t)p.t * h / 4;
+    for (size_t i = (size_t)blockIdx.x * KTHREADS + threadIdx.x; i < n4; i += (size_t)gridDim.x * KTHREADS)
+      acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::SC; ++i) {
+      mbar_init(&S.code_full[i], 1);
+      mbar_init(&S.code_empty[i], 8);
+    }
+    for (int i = 0; i < C::SA; ++i) {
+      mbar_init(&S.a_full[i], 8);
+      mbar_init(&S.a_empty[i], 1);
+    }
+    for (int i = 0; i < SB; ++i) {
+      mbar_init(&S.b_full[i], 1);
+      mbar_init(&S.b_empty[i], 1);
+    }
+    mbar_init(&S.acc_full, 1);
+    mbar_init(&S.acc_empty, 8);
+    mbar_init(&S.drain, 1);
+    S.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == W_MMA) tmem_alloc(&S.tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_slot;
+  volatile int* abort = &S.abort;
+  const int n_units = GATEUP ? p.hdr->n_units_gu : p.hdr->n_units_dn;
+
+  if (warp == W_CODE) {
+    // ------------------------------------------------------------ packed weight blocks
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool armed[C::SC];
+      uint32_t par[C::SC];
+#pragma unroll
+      for (int i = 0; i < C::SC; ++i) armed[i] = false, par[i] = 0;
+      bool stop = false;
+      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+        const PUnit U = decode_punit<GATEUP>(p, u);
+        const int Iu = U.shared ? p.Is : p.I;
+        const uint8_t* rec = U.shared ? P.s_packed : P.packed + (size_t)U.e * rec_bytes(h, p.I);
+        const uint8_t* src;
+        if (GATEUP) src = rec + (size_t)(U.f0 / 128) * (h / KC) * 2 * QB;
+        else src = rec + gu_bytes(h, Iu) + (size_t)(U.f0 / 128) * (Iu / KC) * QB;
+        for (int kc = 0; kc < U.nkc; ++kc, ++it) {
+          const int sc = it % C::SC;
+          if (!mbar_wait(&S.code_empty[sc], ((it / C::SC) & 1) ^ 1, abort, WAIT_NS)) {
+            note_timeout(p.status, abort, GATEUP ? 31 : 41);
+            stop = true;
+            break;
+          }
+          mbar_arrive_expect_tx(&S.code_full[sc], C::C_STAGE);
+          bulk_load(c_s + sc * C::C_STAGE, src + (size_t)kc * C::C_STAGE, C::C_STAGE, &S.code_full[sc]);
+          armed[sc] = true;
+          par[sc] = (it / C::SC) & 1;
+        }
+        if (*abort) stop = true;
+      }
+      if (*abort)
+        for (int i = 0; i < C::SC; ++i)
+          if (armed[i]) drain_wait(&S.code_full[i], par[i]);
+    }
+  } else if (warp == W_B) {
+    // ------------------------------------------------------------ token images
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool armed[SB];
+      uint32_t par[SB];
+#pragma unroll
+      for (int i = 0; i < SB; ++i) armed[i] = false, par[i] = 0;
+      bool stop = false;
+      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+        const PUnit U = decode_punit<GATEUP>(p, u);
+        const uint8_t* src = GATEUP ? reinterpret_cast<const uint8_t*>(P.xg + (size_t)U.pad * h)
+                                    : reinterpret_cast<const uint8_t*>(p.hg + (size_t)U.pad * P.kmax);
+        for (int kc0 = 0; kc0 < U.nkc; kc0 += U.kps, ++it) {
+          const int sb = it % SB;
+          if (!mbar_wait(&S.b_empty[sb], ((it / SB) & 1) ^ 1, abort, WAIT_NS)) {
+            note_timeout(p.status, abort, GATEUP ? 32 : 42);
+            stop = true;
+            break;
+          }
+          const uint32_t bytes = (uint32_t)(min(U.kps, U.nkc - kc0) * U.Nm * 128);
+          mbar_arrive_expect_tx(&S.b_full[sb], bytes);
+          bulk_load(b_s + sb * B_STAGE, src + (size_t)kc0 * U.Nm * 128, bytes, &S.b_full[sb]);
+          armed[sb] = true;
+          par[sb] = (it / SB) & 1;
+        }
+        if (*abort) stop = true;
+      }
+      if (*abort)
+        for (int i = 0; i < SB; ++i)
+          if (armed[i]) drain_wait(&S.b_full[i], par[i]);
+    }
+  } else if (warp == W_MMA) {
+    // ------------------------------------------------------------ MMA (A in TMEM)
+    if (lane == 0) {
+      uint32_t ait = 0, bit = 0, uit = 0;
+      for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
+        const PUnit U = decode_punit<GATEUP>(p, u);
+        const uint32_t idesc = idesc_bf16(128, U.Nm);
+        if (uit > 0 && !mbar_wait(&S.acc_empty, (uit - 1) & 1, abort, WAIT_NS)) {
+          note_timeout(p.status, abort, GATEUP ? 33 : 43);
+          break;
+        }
+        tc_fence_after();
+        bool ok = true;
+        for (int kc = 0; kc < U.nkc; ++kc) {
+          const int sub = kc % U.kps;
+          const int sb = bit % SB;
+          if (sub == 0 && !mbar_wait(&S.b_full[sb], (bit / SB) & 1, abort, WAIT_NS)) {
+            note_timeout(p.status, abort, GATEUP ? 34 : 44);
+            ok = false;
+            break;
+          }
+          const int sa = ait % C::SA;
+          if (!mbar_wait(&S.a_full[sa], (ait / C::SA) & 1, abort, WAIT_NS)) {
+            note_timeout(p.status, abort, GATEUP ? 35 : 45);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t bd = desc_sw128(smem_u32(b_s + sb * B_STAGE + sub * U.Nm * 128));
+#pragma unroll
+          for (int m = 0; m < C::NMAT; ++m) {
+            const uint32_t a_tm = tmem + A_COL + sa * C::A_STRIDE + m * 32;
+#pragma unroll
+            for (int kk = 0; kk < KC / 16; ++kk)
+              mma_bf16_ta(tmem + m * ACC_UP, a_tm + 8 * kk, bd + 2 * kk, idesc, (kc | kk) != 0);
+          }
+          mma_commit(&S.a_empty[sa]);
+          ++ait;
+          if (sub == U.kps - 1 || kc == U.nkc - 1) {
+            mma_commit(&S.b_empty[sb]);
+            ++bit;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&S.acc_full);
+      }
+      if (*abort) {
+        mma_commit(&S.drain);
+        drain_wait(&S.drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dequant + epilogue
+    const int dw = warp - W_DQ0;         // 0..7
+    const int q = warp & 3;              // TMEM lane quarter this warp may access
+    const int o = q * 32 + lane;         // weight row (= TMEM lane) this thread dequantises
+    const int part = dw >> 2;            // gate/up: matrix; down: K half
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    uint32_t cit = 0, ait = 0, uit = 0;
+    for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
+      const PUnit U = decode_punit<GATEUP>(p, u);
+      const int Iu = U.shared ? p.Is : p.I;
+      bool ok = true;
+      for (int kc = 0; kc < U.nkc; ++kc) {
+        const int sc = cit % C::SC, sa = ait % C::SA;
+        if (!mbar_wait(&S.code_full[sc], (cit / C::SC) & 1, abort, WAIT_NS) ||
+            !mbar_wait(&S.a_empty[sa], ((ait / C::SA) & 1) ^ 1, abort, WAIT_NS)) {
+          note_timeout(p.status, abort, GATEUP ? 36 : 46);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint8_t* blk = c_s + sc * C::C_STAGE + (GATEUP ? part * QB : 0);
+        const __nv_bfloat16 sv = reinterpret_cast<const __nv_bfloat16*>(blk + 4096)[o];
+        const __nv_bfloat16 bv = reinterpret_cast<const __nv_bfloat16*>(blk + 4096 + 256)[o];
+        const __nv_bfloat162 s2 = __halves2bfloat162(sv, sv), b2 = __halves2bfloat162(bv, bv);
+        if (GATEUP) {
+          const uint4 c0 = reinterpret_cast<const uint4*>(blk + o * 32)[0];
+          const uint4 c1 = reinterpret_cast<const uint4*>(blk + o * 32)[1];
+          const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          uint32_t r[32];
+          dequant_packed<8>(wd, s2, b2, r);
+          tmem_st<32>(lane_base + A_COL + sa * C::A_STRIDE + part * 32, r);
+        } else {
+          const uint4 cw = reinterpret_cast<const uint4*>(blk + o * 32)[part];
+          const uint32_t wd[4] = {cw.x, cw.y, cw.z, cw.w};
+          uint32_t r[16];
+          dequant_packed<4>(wd, s2, b2, r);
+          tmem_st<16>(lane_base + A_COL + sa * C::A_STRIDE + part * 16, r);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&S.a_full[sa]);
+          mbar_arrive(&S.code_empty[sc]);
+        }
+        ++ait;
+        ++cit;
+      }
+      if (!ok) break;
+      // ---- epilogue: columns split between the two warps of each lane quarter
+      const int ncw = (U.Nm + 31) / 32;
+      int col_row[4];
+      float col_w[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        col_row[g] = 0;
+        col_w[g] = 1.f;
+        const int col = g * 32 + lane;
+        if (!GATEUP && g < ncw && col < U.n) {
+          if (U.shared) {
+            col_row[g] = U.start + col;
+            col_w[g] = p.gate_vals ? p.gate_vals[U.start + col] : 1.f;
+          } else {
+            col_row[g] = p.rows[U.start + col];
+            col_w[g] = p.weights[U.start + col];
+          }
+        }
+      }
+      if (!mbar_wait(&S.acc_full, uit & 1, abort, WAIT_NS)) {
+        note_timeout(p.status, abort, GATEUP ? 37 : 47);
+        break;
+      }
+      tc_fence_after();
+      const int feat = U.f0 + o;  // output feature of this TMEM lane
+      if (GATEUP) {
+        // hg image: K chunk feat / 64, 16-byte piece (feat % 64) / 8, element feat % 8
+        uint8_t* img = reinterpret_cast<uint8_t*>(p.hg + (size_t)U.pad * P.kmax) +
+                       (size_t)(feat / 64) * U.Nm * 128;
+        const int c8 = (feat % 64) / 8, e8 = feat % 8;
+        for (int c = part; c * 16 < U.Nm; c += 2) {
+          uint32_t g[16], v[16];
+          tmem_ld16(lane_base + c * 16, g);
+          tmem_ld16(lane_base + ACC_UP + c * 16, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int col = c * 16 + j;
+            const float hv = silu_mul(__uint_as_float(g[j]), __uint_as_float(v[j]));
+            // padding columns get zeros so the down GEMM reads finite values
+            *reinterpret_cast<uint16_t*>(img + sw128_off(col, c8) + e8 * 2) = col < U.n ? f2bf(hv) : (uint16_t)0;
+          }
+        }
+        (void)Iu;
+      } else {
+        bool bad_row = false;
+        for (int c = part; c * 16 < U.Nm; c += 2) {
+          uint32_t y[16];
+          tmem_ld16(lane_base + c * 16, y);
+          tmem_ld_wait();
+          const int grp = c >> 1;
+          int rsel = col_row[0];
+          float wsel = col_w[0];
+#pragma unroll
+          for (int g = 1; g < 4; ++g)
+            if (g == grp) rsel = col_row[g], wsel = col_w[g];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int col = c * 16 + j;
+            const int src = (c & 1) * 16 + j;
+            const int r = __shfl_sync(0xFFFFFFFFu, rsel, src);
+            const float wv = __shfl_sync(0xFFFFFFFFu, wsel, src);
+            if (col >= U.n) continue;
+            const float yv = __uint_as_float(y[j]);
+            if (p.deterministic) {
+              if (U.shared) p.acc[(size_t)r * h + feat] = wv * yv;
+              else p.ybuf[(size_t)(U.start + col) * h + feat] = yv;
+            } else if (r >= 0 && r < p.t) {
+              atomicAdd(&p.acc[(size_t)r * h + feat], wv * yv);
+            } else {
+              bad_row = true;
+            }
+          }
+        }
+        if (bad_row && lane == 0) raise_flag(p.status, FLAG_BAD_ROW);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.acc_empty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == W_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+}  // namespace
+
+size_t packed_record_bytes(int h, int I) { return rec_bytes(h, I); }
+
+size_t packed_max_tiles(const moe_dims& d) { return (size_t)d.t * d.k / PTILE + d.E + d.t / PTILE + 2; }
+
+// Upper bound of the padded row space (rows rounded up to 16 per tile).
+size_t packed_pad_rows(const moe_dims& d) {
+  return (size_t)d.t * d.k + d.t + 16 * packed_max_tiles(d);
+}
+
+cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, const uint16_t* biases, int h, int I,
+                        int nrec, uint8_t* dst, cudaStream_t stream) {
+  const int nblk = 2 * (I / 128) * (h / KC) + (h / 128) * (I / KC);
+  dim3 grid(nblk, nrec);
+  MOE_LAUNCH("pack", stream,
+             pack_kernel<<<grid, 128, 0, stream>>>(codes, scales, biases, h, I, (size_t)3 * I * h / 2,
+                                                   (size_t)3 * I * h / KC, dst));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, const uint8_t* s_packed,
+                                  uint16_t* xg, bool deterministic, cudaStream_t stream) {
+  moe_dims d{a.t, a.h, a.I, a.E, a.k, a.Is};
+  const size_t mt = packed_max_tiles(d);
+  const int fmax = (a.I > a.Is ? a.I : a.Is) / 128;
+  SchedHdr* hdr = reinterpret_cast<SchedHdr*>(a.sched);
+  int4* tiles = reinterpret_cast<int4*>(a.sched + sizeof(SchedHdr));
+  int* units = reinterpret_cast<int*>(tiles + mt);
+  float* gate_vals = reinterpret_cast<float*>(units + mt * fmax);
+
+  PParams P{};
+  TcParams& p = P.p;
+  p.t = a.t;
+  p.h = a.h;
+  p.I = a.I;
+  p.Is = a.Is;
+  p.E = a.E;
+  p.k = a.k;
+  p.deterministic = deterministic ? 1 : 0;
+  p.offsets = a.offsets;
+  p.rows = a.rows;
+  p.weights = a.weights;
+  p.gate_vals = (a.Is > 0 && a.s_gate) ? gate_vals : nullptr;
+  p.acc = a.acc;
+  p.hg = a.hg;
+  p.hgs = a.hgs;
+  p.ybuf = a.ybuf;
+  p.hdr = hdr;
+  p.tiles = tiles;
+  p.units_gu = units;
+  p.status = a.status;
+  P.packed = packed;
+  P.s_packed = s_packed;
+  P.xg = xg;
+  P.kmax = a.I > a.Is ? a.I : a.Is;
+
+  cudaError_t err;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if ((err = cudaFuncSetAttribute(packed_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)psmem_bytes<true>())) != cudaSuccess)
+      return err;
+    if ((err = cudaFuncSetAttribute(packed_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)psmem_bytes<false>())) != cudaSuccess)
+      return err;
+    attr_done = true;
+  }
+  if ((err = launch_schedule(p, hdr, tiles, units, (int)mt, PTILE, stream)) != cudaSuccess) return err;
+  if (p.gate_vals && (err = launch_shared_gate(a.x, a.s_gate, a.t, a.h, gate_vals, stream)) != cudaSuccess)
+    return err;
+  MOE_LAUNCH("gather", stream,
+             gather_kernel<<<(unsigned)mt, 256, 0, stream>>>(a.x, a.rows, hdr, tiles, a.t, a.h, a.E, xg, a.status));
+  const int grid = num_sms();
+  MOE_LAUNCH("gateup_packed", stream,
+             packed_gemm_kernel<true><<<grid, KTHREADS, psmem_bytes<true>(), stream>>>(P));
+  MOE_LAUNCH("down_packed", stream,
+             packed_gemm_kernel<false><<<grid, KTHREADS, psmem_bytes<false>(), stream>>>(P));
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  return launch_finalize(a, deterministic, stream);
+}
+
+}  // namespace moe

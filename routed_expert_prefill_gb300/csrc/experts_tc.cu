@@ -30,7 +30,7 @@
 // frees TMEM and returns.
 #include <string.h>
 
-#include "experts.cuh"
+#include "tc_common.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -43,35 +43,6 @@ constexpr int TILE_MAX = 256;  // rows per tile (MMA N <= 256)
 constexpr int KC = 64;         // K per chunk = one quantisation group
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
-
-struct SchedHdr {
-  int n_tiles;
-  int n_units_gu;
-  int n_units_dn;
-  int pad[13];
-};
-
-struct TcParams {
-  int t, h, I, Is, E, k;
-  int deterministic;
-  const int32_t* offsets;
-  const int32_t* rows;
-  const float* weights;
-  const uint16_t* scales;
-  const uint16_t* biases;
-  size_t rec_groups;
-  const uint16_t* s_scales;
-  const uint16_t* s_biases;
-  const float* gate_vals;  // per-row shared-expert gate, or null
-  float* acc;
-  uint16_t* hg;
-  uint16_t* hgs;
-  float* ybuf;
-  const SchedHdr* hdr;
-  const int4* tiles;       // {expert (E = shared), start, rows, 0}
-  const int* units_gu;     // (tile << 8) | feature tile
-  DeviceStatus* status;
-};
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -132,7 +103,7 @@ __device__ __forceinline__ __nv_bfloat162 bf2_from_half(uint16_t hb) {
 // Tile schedule (one block)
 // ----------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024)
-schedule_kernel(TcParams p, SchedHdr* hdr, int4* tiles, int* units_gu, int max_tiles) {
+schedule_kernel(TcParams p, SchedHdr* hdr, int4* tiles, int* units_gu, int max_tiles, int tile_max) {
   __shared__ int bucket_cnt[16], bucket_base[16], bucket_fill[16];
   __shared__ int n_tiles_s;
   __shared__ int scan_carry;
@@ -157,7 +128,7 @@ schedule_kernel(TcParams p, SchedHdr* hdr, int4* tiles, int* units_gu, int max_t
       n = p.t;
     }
     if (n == 0) continue;
-    const int nt = (n + TILE_MAX - 1) / TILE_MAX;
+    const int nt = (n + tile_max - 1) / tile_max;
     const int sz = (n + nt - 1) / nt;
     for (int i = 0; i < nt; ++i) {
       const int rows = min(sz, n - i * sz);
@@ -187,7 +158,7 @@ schedule_kernel(TcParams p, SchedHdr* hdr, int4* tiles, int* units_gu, int max_t
       start = 0;
     }
     if (n == 0) continue;
-    const int nt = (n + TILE_MAX - 1) / TILE_MAX;
+    const int nt = (n + tile_max - 1) / tile_max;
     const int sz = (n + nt - 1) / nt;
     for (int i = 0; i < nt; ++i) {
       const int rows = min(sz, n - i * sz);
@@ -231,10 +202,44 @@ schedule_kernel(TcParams p, SchedHdr* hdr, int4* tiles, int* units_gu, int max_t
     if (tid == blockDim.x - 1) scan_carry = ub + f;
     __syncthreads();
   }
+  const int n_units_gu = scan_carry;
+  __syncthreads();
+  // padded-row offset of every tile (rows rounded up to 16)
+  if (tid == 0) scan_carry = 0;
+  __syncthreads();
+  for (int base = 0; base < nt_all; base += blockDim.x) {
+    const int i = base + tid;
+    const int f = (i < nt_all) ? (tiles[i].z + 15) & ~15 : 0;
+    int incl = f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int s = warp_sums[lane];
+      int si = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xFFFFFFFFu, si, o);
+        if (lane >= o) si += y;
+      }
+      warp_sums[lane] = si - s;
+    }
+    __syncthreads();
+    const int ub = scan_carry + warp_sums[warp] + incl - f;
+    if (i < nt_all) tiles[i].w = ub;
+    __syncthreads();
+    if (tid == blockDim.x - 1) scan_carry = ub + f;
+    __syncthreads();
+  }
   if (tid == 0) {
     hdr->n_tiles = nt_all;
-    hdr->n_units_gu = scan_carry;
+    hdr->n_units_gu = n_units_gu;
     hdr->n_units_dn = nt_all * (p.h / 128);
+    hdr->pad_rows = scan_carry;
   }
 }
 
@@ -740,6 +745,18 @@ int num_sms() {
 
 }  // namespace
 
+cudaError_t launch_schedule(const TcParams& p, SchedHdr* hdr, int4* tiles, int* units_gu, int max_tiles,
+                            int tile_max, cudaStream_t stream) {
+  MOE_LAUNCH("schedule", stream,
+             schedule_kernel<<<1, 1024, 0, stream>>>(p, hdr, tiles, units_gu, max_tiles, tile_max));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shared_gate(const uint16_t* x, const uint16_t* g, int t, int h, float* out, cudaStream_t stream) {
+  MOE_LAUNCH("shared_gate", stream, shared_gate_kernel<<<(t + 7) / 8, 256, 0, stream>>>(x, g, t, h, out));
+  return cudaGetLastError();
+}
+
 size_t tc_max_tiles(const moe_dims& d) {
   return (size_t)d.t * d.k / TILE_MAX + d.E + d.t / TILE_MAX + 2;
 }
@@ -829,10 +846,9 @@ cudaError_t launch_experts_tc(const ExpertsArgs& a, bool deterministic, cudaStre
     attr_done = true;
   }
 
-  MOE_LAUNCH("schedule", stream, schedule_kernel<<<1, 1024, 0, stream>>>(p, hdr, tiles, units, (int)mt));
-  if (p.gate_vals)
-    MOE_LAUNCH("shared_gate", stream,
-               shared_gate_kernel<<<(a.t + 7) / 8, 256, 0, stream>>>(a.x, a.s_gate, a.t, a.h, gate_vals));
+  if ((err = launch_schedule(p, hdr, tiles, units, (int)mt, TILE_MAX, stream)) != cudaSuccess) return err;
+  if (p.gate_vals && (err = launch_shared_gate(a.x, a.s_gate, a.t, a.h, gate_vals, stream)) != cudaSuccess)
+    return err;
   const int grid = num_sms();
   MOE_LAUNCH("gateup_tc", stream,
              expert_gemm_kernel<true><<<grid, KTHREADS, kernel_smem<true>(), stream>>>(tm_codes_gu, tm_scodes_gu,

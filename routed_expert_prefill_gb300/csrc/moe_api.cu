@@ -15,6 +15,12 @@ cudaError_t launch_build_csr(const int32_t* idx, const float* w, int t, int k, i
                              unsigned char* ws, const WsLayout& L, cudaStream_t stream);
 cudaError_t launch_experts_fast(const ExpertsArgs& a, uint32_t flags, cudaStream_t stream);
 size_t experts_sched_bytes(const moe_dims& d);
+size_t packed_record_bytes(int h, int I);
+size_t packed_pad_rows(const moe_dims& d);
+cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, const uint16_t* biases, int h, int I,
+                        int nrec, uint8_t* dst, cudaStream_t stream);
+cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, const uint8_t* s_packed,
+                                  uint16_t* xg, bool deterministic, cudaStream_t stream);
 
 static thread_local char g_err[512] = "";
 
@@ -41,9 +47,16 @@ WsLayout ws_layout(const moe_dims& d, uint32_t flags) {
   L.csr_counts = take(nchunks * d.E * 4);
   L.csr_base = take(nchunks * d.E * 4);
   L.acc = take((size_t)d.t * d.h * 4);
-  L.hg = take(n * d.inter * 2);
+  const size_t kmax = d.inter > d.shared_inter ? d.inter : d.shared_inter;
+  size_t hg_bytes = n * d.inter * 2;
+  if (flags & MOE_PACKED_WEIGHTS) {
+    const size_t pb = packed_pad_rows(d) * kmax * 2;
+    if (pb > hg_bytes) hg_bytes = pb;
+  }
+  L.hg = take(hg_bytes);
   L.hgs = take((size_t)d.t * d.shared_inter * 2);
   L.ybuf = (flags & MOE_DETERMINISTIC) ? take(n * d.h * 4) : off;
+  L.xg = (flags & MOE_PACKED_WEIGHTS) ? take(packed_pad_rows(d) * d.h * 2) : off;
   L.sched = take(experts_sched_bytes(d));
   L.total = off;
   return L;
@@ -158,10 +171,14 @@ int moe_experts_fwd(const uint16_t* x, const moe_csr* csr, const moe_qweights* e
                     const moe_shared* shared, uint16_t* out, const moe_dims* dims, uint32_t flags, void* ws,
                     size_t ws_bytes, void* stream) {
   TRY(check_dims(dims));
-  const uint32_t known = MOE_DETERMINISTIC | MOE_FORCE_SMALL_T | MOE_FORCE_LARGE_T | MOE_SIMPLE_KERNELS;
+  const uint32_t known =
+      MOE_DETERMINISTIC | MOE_FORCE_SMALL_T | MOE_FORCE_LARGE_T | MOE_SIMPLE_KERNELS | MOE_PACKED_WEIGHTS;
   if (flags & ~known) return set_error(MOE_EINVAL, "unknown flag bits 0x%x", flags & ~known);
   if ((flags & MOE_FORCE_SMALL_T) && (flags & MOE_FORCE_LARGE_T))
     return set_error(MOE_EINVAL, "MOE_FORCE_SMALL_T and MOE_FORCE_LARGE_T are exclusive");
+  if ((flags & MOE_PACKED_WEIGHTS) && (flags & MOE_SIMPLE_KERNELS))
+    return set_error(MOE_EINVAL, "MOE_SIMPLE_KERNELS reads row-major weights, not MOE_PACKED_WEIGHTS");
+  const bool packed = (flags & MOE_PACKED_WEIGHTS) != 0;
   TRY(check_ptr(x, "x", 16));
   TRY(check_ptr(out, "out", 16));
   if (!csr) return set_error(MOE_EINVAL, "csr is NULL");
@@ -171,13 +188,13 @@ int moe_experts_fwd(const uint16_t* x, const moe_csr* csr, const moe_qweights* e
   TRY(check_ptr(csr->slot_of, "csr->slot_of", 4));
   if (!experts) return set_error(MOE_EINVAL, "experts is NULL");
   TRY(check_ptr(experts->codes, "experts->codes", 16));
-  TRY(check_ptr(experts->scales, "experts->scales", 16));
-  TRY(check_ptr(experts->biases, "experts->biases", 16));
+  TRY(check_ptr(experts->scales, "experts->scales", 16, packed));
+  TRY(check_ptr(experts->biases, "experts->biases", 16, packed));
   if (dims->shared_inter > 0) {
     if (!shared) return set_error(MOE_EINVAL, "shared is NULL but shared_inter > 0");
     TRY(check_ptr(shared->codes, "shared->codes", 16));
-    TRY(check_ptr(shared->scales, "shared->scales", 16));
-    TRY(check_ptr(shared->biases, "shared->biases", 16));
+    TRY(check_ptr(shared->scales, "shared->scales", 16, packed));
+    TRY(check_ptr(shared->biases, "shared->biases", 16, packed));
     TRY(check_ptr(shared->gate, "shared->gate", 16, true));
   }
   TRY(check_ws(dims, flags, ws, ws_bytes));
@@ -217,9 +234,36 @@ int moe_experts_fwd(const uint16_t* x, const moe_csr* csr, const moe_qweights* e
   a.out = out;
 
   cudaStream_t s = (cudaStream_t)stream;
+  if (packed)
+    return cuda_status(launch_experts_packed(a, experts->codes, dims->shared_inter > 0 ? shared->codes : nullptr,
+                                             (uint16_t*)(wsb + L.xg), (flags & MOE_DETERMINISTIC) != 0, s),
+                       "moe_experts_fwd launch");
   if (flags & MOE_SIMPLE_KERNELS)
     return cuda_status(launch_experts_simple(a, (flags & MOE_DETERMINISTIC) != 0, s), "moe_experts_fwd launch");
   return cuda_status(launch_experts_fast(a, flags, s), "moe_experts_fwd launch");
+}
+
+size_t moe_packed_bytes(const moe_dims* dims, int shared) {
+  if (check_dims(dims) != MOE_OK) return 0;
+  if (shared) return dims->shared_inter > 0 ? packed_record_bytes(dims->h, dims->shared_inter) : 0;
+  return (size_t)dims->E * packed_record_bytes(dims->h, dims->inter);
+}
+
+int moe_pack_experts(const moe_qweights* src, const moe_dims* dims, int shared, void* dst, size_t dst_bytes,
+                     void* stream) {
+  TRY(check_dims(dims));
+  if (!src) return set_error(MOE_EINVAL, "src is NULL");
+  TRY(check_ptr(src->codes, "src->codes", 16));
+  TRY(check_ptr(src->scales, "src->scales", 2));
+  TRY(check_ptr(src->biases, "src->biases", 2));
+  TRY(check_ptr(dst, "dst", 16));
+  if (shared && dims->shared_inter == 0) return set_error(MOE_ESHAPE, "shared_inter is 0: nothing to pack");
+  const size_t need = moe_packed_bytes(dims, shared);
+  if (dst_bytes < need) return set_error(MOE_EINVAL, "dst has %zu bytes, needs %zu", dst_bytes, need);
+  const int I = shared ? dims->shared_inter : dims->inter;
+  return cuda_status(launch_pack(src->codes, src->scales, src->biases, dims->h, I, shared ? 1 : dims->E,
+                                 (uint8_t*)dst, (cudaStream_t)stream),
+                     "moe_pack_experts launch");
 }
 
 int moe_clear_device_status(void* ws, void* stream) {

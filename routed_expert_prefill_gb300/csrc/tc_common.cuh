@@ -1,0 +1,45 @@
+// Types shared by the tensor-core expert kernels (internal).
+#pragma once
+#include "experts.cuh"
+
+namespace moe {
+
+struct SchedHdr {
+  int n_tiles;
+  int n_units_gu;
+  int n_units_dn;
+  int pad_rows;  // sum over tiles of the row count rounded up to 16
+  int pad[12];
+};
+
+struct TcParams {
+  int t, h, I, Is, E, k;
+  int deterministic;
+  const int32_t* offsets;
+  const int32_t* rows;
+  const float* weights;
+  const uint16_t* scales;
+  const uint16_t* biases;
+  size_t rec_groups;
+  const uint16_t* s_scales;
+  const uint16_t* s_biases;
+  const float* gate_vals;  // per-row shared-expert gate, or null
+  float* acc;
+  uint16_t* hg;
+  uint16_t* hgs;
+  float* ybuf;
+  const SchedHdr* hdr;
+  const int4* tiles;       // {expert (E = shared), start, rows, padded-row offset}
+  const int* units_gu;     // (tile << 8) | feature tile
+  DeviceStatus* status;
+};
+
+
+// Tile schedule: tiles of at most `tile_max` rows per expert (the shared
+// expert: all t rows), largest first, with gate/up units and padded offsets.
+cudaError_t launch_schedule(const TcParams& p, SchedHdr* hdr, int4* tiles, int* units_gu, int max_tiles,
+                            int tile_max, cudaStream_t stream);
+// Per-row shared-expert gate sigmoid(x_r . g) into out[t].
+cudaError_t launch_shared_gate(const uint16_t* x, const uint16_t* g, int t, int h, float* out, cudaStream_t stream);
+
+}  // namespace moe

@@ -27,6 +27,7 @@ MOE_DETERMINISTIC = 0x1
 MOE_FORCE_SMALL_T = 0x2
 MOE_FORCE_LARGE_T = 0x4
 MOE_SIMPLE_KERNELS = 0x8
+MOE_PACKED_WEIGHTS = 0x10
 
 # Every symbol include/moe.h declares.
 EXPORTS = (
@@ -40,6 +41,8 @@ EXPORTS = (
     "moe_read_device_status",
     "moe_profile_enable",
     "moe_profile_read",
+    "moe_packed_bytes",
+    "moe_pack_experts",
 )
 
 
@@ -106,6 +109,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_profile_enable.argtypes = [ctypes.c_int]
     lib.moe_profile_read.restype = ctypes.c_int
     lib.moe_profile_read.argtypes = [ctypes.POINTER(MoeProfileEntry), ctypes.c_int]
+    lib.moe_packed_bytes.restype = sz
+    lib.moe_packed_bytes.argtypes = [ctypes.POINTER(MoeDims), ctypes.c_int]
+    lib.moe_pack_experts.restype = ctypes.c_int
+    lib.moe_pack_experts.argtypes = [ctypes.POINTER(MoeQWeights), ctypes.POINTER(MoeDims), ctypes.c_int, vp, sz, vp]
     _lib = lib
     return lib
 
@@ -208,12 +215,11 @@ def moe_experts_fwd(x: torch.Tensor, csr: Csr, experts: tuple, shared: tuple | N
         ws = new_workspace(dims, flags, x.device, stream)
     if out is None:
         out = torch.empty((dims.t, dims.h), dtype=torch.bfloat16, device=x.device)
-    q = MoeQWeights(experts[0].data_ptr(), experts[1].data_ptr(), experts[2].data_ptr())
+    dp = lambda t_: None if t_ is None else t_.data_ptr()  # noqa: E731
+    q = MoeQWeights(dp(experts[0]), dp(experts[1]), dp(experts[2]))
     sh = None
     if shared is not None:
-        g = shared[3]
-        sh = MoeShared(shared[0].data_ptr(), shared[1].data_ptr(), shared[2].data_ptr(),
-                       None if g is None else g.data_ptr())
+        sh = MoeShared(dp(shared[0]), dp(shared[1]), dp(shared[2]), dp(shared[3]))
     c = csr.c()
     _check(lib.moe_experts_fwd(_ptr(_u16(x)), ctypes.byref(c), ctypes.byref(q),
                                ctypes.byref(sh) if sh is not None else None, _ptr(out), ctypes.byref(dims),
@@ -233,6 +239,20 @@ def profile_read() -> dict:
     if n < 0:
         _check(n)
     return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(n)}
+
+
+def pack_experts(codes: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor, dims: MoeDims,
+                 shared: bool = False, stream=None) -> torch.Tensor:
+    """Tile-contiguous packed copy of the routed (or shared) expert records."""
+    lib = load_library()
+    n = lib.moe_packed_bytes(ctypes.byref(dims), 1 if shared else 0)
+    if n == 0:
+        raise MoeError(-2, "nothing to pack for these dims")
+    dst = torch.empty(n, dtype=torch.uint8, device=codes.device)
+    q = MoeQWeights(codes.data_ptr(), scales.data_ptr(), biases.data_ptr())
+    _check(lib.moe_pack_experts(ctypes.byref(q), ctypes.byref(dims), 1 if shared else 0, _ptr(dst), n,
+                                _stream(stream)))
+    return dst
 
 
 def read_device_status(ws: torch.Tensor, stream=None) -> int:
@@ -266,17 +286,35 @@ def upload_inputs(inp: dict, device="cuda") -> dict:
     return d
 
 
+def add_packed(dev: dict, dims: MoeDims, stream=None) -> dict:
+    """Add packed weight records (dev["packed"], dev["shared_packed"]) to uploaded inputs."""
+    dev["packed"] = pack_experts(dev["codes"], dev["scales"], dev["biases"], dims, False, stream)
+    if dims.shared_inter > 0:
+        dev["shared_packed"] = pack_experts(dev["shared_codes"], dev["shared_scales"], dev["shared_biases"], dims,
+                                            True, stream)
+    return dev
+
+
 def moe_forward(dev: dict, dims: MoeDims, flags: int = 0, ws: torch.Tensor | None = None,
                 out: torch.Tensor | None = None, stream=None, bufs: dict | None = None) -> dict:
-    """Router -> CSR -> experts on one stream; returns the intermediate tensors too."""
+    """Router -> CSR -> experts on one stream; returns the intermediate tensors too.
+
+    With MOE_PACKED_WEIGHTS in `flags` the packed records of add_packed() are used."""
+    if flags & MOE_PACKED_WEIGHTS and "packed" not in dev:
+        add_packed(dev, dims, stream)
     if ws is None:
         ws = new_workspace(dims, flags, dev["x"].device, stream)
     b = bufs or {}
     idx, w = moe_route_topk(dev["x"], dev["wr"], dims.k, dev.get("rbias"), out=b.get("route"), stream=stream)
     csr = moe_build_csr(idx, w, dims.E, ws=ws, out=b.get("csr"), stream=stream)
     shared = None
-    if dims.shared_inter > 0:
-        shared = (dev["shared_codes"], dev["shared_scales"], dev["shared_biases"], dev.get("shared_gate"))
-    y = moe_experts_fwd(dev["x"], csr, (dev["codes"], dev["scales"], dev["biases"]), shared, dims, flags,
-                        out=out, ws=ws, stream=stream)
+    if flags & MOE_PACKED_WEIGHTS:
+        experts = (dev["packed"], None, None)
+        if dims.shared_inter > 0:
+            shared = (dev["shared_packed"], None, None, dev.get("shared_gate"))
+    else:
+        experts = (dev["codes"], dev["scales"], dev["biases"])
+        if dims.shared_inter > 0:
+            shared = (dev["shared_codes"], dev["shared_scales"], dev["shared_biases"], dev.get("shared_gate"))
+    y = moe_experts_fwd(dev["x"], csr, experts, shared, dims, flags, out=out, ws=ws, stream=stream)
     return dict(idx=idx, w=w, csr=csr, out=y, ws=ws)

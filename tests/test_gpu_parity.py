@@ -120,6 +120,32 @@ def test_pipeline_parity(moe, name, flags):
     _check_out(res["out"], ref["out"])
 
 
+@pytest.mark.parametrize("name", SMALL)
+@pytest.mark.parametrize("det", [False, True])
+def test_packed_pipeline_parity(moe, name, det):
+    w = synth.WORKLOADS[name]
+    inp = _inputs(w)
+    ref = _oracle_rows(w, inp, None)
+    flags = moe.MOE_PACKED_WEIGHTS | (moe.MOE_DETERMINISTIC if det else 0)
+    res, status = _run(moe, w, inp, flags)
+    assert status == 0
+    np.testing.assert_array_equal(res["idx"].cpu().numpy(), ref["idx"])
+    _check_csr_against(res["csr"], res["idx"], res["w"], w.E)
+    _check_out(res["out"], ref["out"])
+
+
+def test_packed_matches_rowmajor_path(moe):
+    """Both tensor-core paths agree (deterministic mode) to within bf16 rounding."""
+    w = synth.WORKLOADS["t512_h2048_e128"]
+    inp = _inputs(w)
+    dev = moe.upload_inputs(inp)
+    a, _ = _run(moe, w, inp, moe.MOE_DETERMINISTIC, dev)
+    b, _ = _run(moe, w, inp, moe.MOE_DETERMINISTIC | moe.MOE_PACKED_WEIGHTS, dev)
+    x = a["out"].float().cpu().numpy()
+    y = b["out"].float().cpu().numpy()
+    assert np.abs(x - y).max() <= 1e-2 * np.abs(x).max()
+
+
 def test_simple_kernels_parity(moe):
     w = synth.WORKLOADS["tiny_t16_h256_e8"]
     inp = _inputs(w)
@@ -142,37 +168,41 @@ def test_deterministic_mode_is_bitwise_reproducible(moe):
     np.testing.assert_array_equal(outs[0], outs[1])
 
 
-@pytest.mark.parametrize("t", [1, 3, 13, 37])
-def test_ragged_row_counts(moe, t):
+@pytest.mark.parametrize("t", [1, 3, 13, 37, 300])
+@pytest.mark.parametrize("packed", [False, True])
+def test_ragged_row_counts(moe, t, packed):
     w = synth.WORKLOADS["tiny_t16_h256_e8"].replace(t=t, seed=20 + t)
     inp = synth.make_inputs(w)
     ref = O.moe_forward(inp, w.k, w.h, w.inter, w.shared_inter)
-    res, status = _run(moe, w, inp)
+    res, status = _run(moe, w, inp, moe.MOE_PACKED_WEIGHTS if packed else 0)
     assert status == 0
     np.testing.assert_array_equal(res["idx"].cpu().numpy(), ref["idx"])
     _check_csr_against(res["csr"], res["idx"], res["w"], w.E)
     _check_out(res["out"], ref["out"])
 
 
-def test_all_experts_per_row_and_no_shared(moe):
+@pytest.mark.parametrize("flags", [0, 0x10, 0x11])
+def test_all_experts_per_row_and_no_shared(moe, flags):
     # k = E: every expert takes every row; no shared expert.
     w = synth.Workload("kE", 9, 256, 128, 4, 4, 0, 31)
     inp = synth.make_inputs(w.replace(shared_inter=128))
     ref = O.moe_forward(dict(inp, shared_codes=np.full_like(inp["shared_codes"], 0x88)), w.k, w.h, w.inter, 128)
-    res, status = _run(moe, w, inp)
+    res, status = _run(moe, w, inp, flags)
     assert status == 0
     assert res["csr"].offsets.cpu().numpy().tolist() == [0, 9, 18, 27, 36]
     _check_out(res["out"], ref["out"])
 
 
-def test_one_expert_takes_every_row_and_shared_gate(moe):
+@pytest.mark.parametrize("flags", [0, 0x10, 0x11])
+def test_one_expert_takes_every_row_and_shared_gate(moe, flags):
     # A large router bias sends every row to expert 2 first; E - k experts stay empty.
-    w = synth.Workload("hot", 40, 256, 128, 6, 2, 128, 32, shared_gate=True)
+    # 300 rows: the hot expert spans several tiles.
+    w = synth.Workload("hot", 300, 256, 128, 6, 2, 128, 32, shared_gate=True)
     inp = synth.make_inputs(w)
     inp["rbias"] = np.array([0, 0, 50, 0, 0, 0], np.float32)
     ref = O.moe_forward(inp, w.k, w.h, w.inter, w.shared_inter)
     assert np.all(ref["idx"][:, 0] == 2)
-    res, status = _run(moe, w, inp)
+    res, status = _run(moe, w, inp, flags)
     assert status == 0
     np.testing.assert_array_equal(res["idx"].cpu().numpy(), ref["idx"])
     _check_csr_against(res["csr"], res["idx"], res["w"], w.E)
@@ -207,13 +237,14 @@ BIG = ["t4096_h2048_e128_skewed", "t4096_h4096_e256"]
 
 
 @pytest.mark.parametrize("name", BIG)
-def test_full_size_sampled_rows(moe, name):
+@pytest.mark.parametrize("packed", [False, True])
+def test_full_size_sampled_rows(moe, name, packed):
     """Full-size run in the benchmark's launch configuration; oracle on 96 sampled rows."""
     w = synth.WORKLOADS[name]
     inp = _inputs(w)
     rows = np.sort(np.random.default_rng(99).choice(w.t, 96, replace=False))
     ref = _oracle_rows(w, inp, rows)
-    res, status = _run(moe, w, inp)
+    res, status = _run(moe, w, inp, moe.MOE_PACKED_WEIGHTS if packed else 0)
     assert status == 0
     np.testing.assert_array_equal(res["idx"].cpu().numpy()[rows], ref["idx"])
     _check_csr_against(res["csr"], res["idx"], res["w"], w.E)
