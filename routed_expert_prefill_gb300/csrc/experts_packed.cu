@@ -21,15 +21,21 @@
 //   gather:   the token rows of every tile are copied, chunk by chunk, into
 //     the 128-byte-swizzled K-major image the MMA reads (xg), so one bulk
 //     copy moves a whole B stage.
-//   gateup:   warp 0 streams packed weight blocks (one bulk copy per K
-//     chunk), warp 10 streams xg stages, eight warps dequantise one weight
-//     row each (w = fma(q, s, b) in bf16) straight into TMEM with
-//     tcgen05.st, warp 1 issues tcgen05.mma with A in TMEM and B in shared
-//     memory, and the eight warps read the gate and up accumulators back,
-//     apply silu(gate) * up and write hg, again as swizzled K-major images.
-//   down:     the same pipeline on the down blocks and hg images; the
-//     epilogue scales by the routing weight and adds into the fp32 block
-//     accumulator (atomics) or, deterministic mode, stores per list position.
+//   gateup:   warp 0 streams packed weight blocks (one bulk copy per two K
+//     chunks), warp 10 streams xg stages, two groups of four warps take
+//     alternate stages and dequantise one weight row per thread
+//     (w = fma(q, s, b) in bf16) straight into TMEM with tcgen05.st, warp 1
+//     issues tcgen05.mma with A in TMEM and B in shared memory, and a
+//     four-warp epilogue group drains the gate and up accumulators into
+//     registers (silu(gate) * up), frees TMEM for the next unit, and writes
+//     hg, again as swizzled K-major images.
+//   down:     the same pipeline on the down blocks and hg images, with a
+//     double-buffered accumulator; the epilogue scales by the routing weight
+//     and adds into the fp32 block accumulator (atomics) or, deterministic
+//     mode, stores per list position.
+// Every mbarrier wait is bounded (2 s of global time); a wait that gives up
+// records MOE_ETIMEOUT, raises a CTA-wide abort flag, lets in-flight copies
+// and MMAs land, frees TMEM and returns.
 #include "tc_common.cuh"
 #include "tc_ptx.cuh"
 
@@ -44,21 +50,23 @@ constexpr int KC = 64;      // K per chunk = one quantisation group
 constexpr int QB = 4096 + 256 + 256;  // one packed 128 x 64 block
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
-constexpr int W_CODE = 0, W_MMA = 1, W_DQ0 = 2, W_B = 10;
-constexpr int KWARPS = 11;
+constexpr int W_CODE = 0, W_MMA = 1, W_DQ0 = 2, W_B = 10, W_EPI0 = 11;
+constexpr int KWARPS = 15;            // 0 code, 1 MMA, 2-9 dequant (two groups), 10 B, 11-14 epilogue
 constexpr int KTHREADS = KWARPS * 32;
 constexpr int SB = 4;                 // B stages
 constexpr int B_STAGE = 32768;        // bytes: KPS chunks of Nm rows x 128 B
-constexpr int ACC_UP = 128;           // TMEM column of the up accumulator
+constexpr int CPS = 2;                // K chunks per code stage and per A stage
 constexpr int A_COL = 256;            // TMEM columns 256..511 hold the A ring
 
 template <bool GATEUP>
 struct PCfg {
   static constexpr int NMAT = GATEUP ? 2 : 1;
-  static constexpr int C_STAGE = NMAT * QB;       // one K chunk of packed blocks
-  static constexpr int SC = GATEUP ? 8 : 16;      // code stages
-  static constexpr int SA = GATEUP ? 4 : 8;       // A stages in TMEM
-  static constexpr int A_STRIDE = NMAT * 32;      // TMEM columns per A stage
+  static constexpr int C_STAGE = CPS * NMAT * QB;     // packed blocks of one stage
+  static constexpr int SC = GATEUP ? 4 : 8;           // code stages
+  static constexpr int A_STAGE = CPS * NMAT * 32;     // TMEM columns per A stage
+  static constexpr int SA = 256 / A_STAGE;            // A stages
+  static constexpr int NACC = GATEUP ? 1 : 2;         // accumulator buffers
+  static constexpr int ACC_COLS = GATEUP ? 256 : 128; // TMEM columns per accumulator buffer
 };
 
 __host__ __device__ inline size_t gu_bytes(int h, int I) { return (size_t)(I / 128) * (h / KC) * 2 * QB; }
@@ -119,7 +127,8 @@ pack_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scal
 }
 
 // ----------------------------------------------------------------------------
-// Gather: token rows of every tile -> swizzled K-major images (one block per tile)
+// Gather: token rows of every tile -> swizzled K-major images.  Grid
+// (tile, group of 8 rows); one warp copies one row.
 // ----------------------------------------------------------------------------
 __global__ void __launch_bounds__(256)
 gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ rows, const SchedHdr* hdr,
@@ -128,18 +137,18 @@ gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ rows, 
   const int4 T = tiles[blockIdx.x];
   const int n = T.z, Nm = (n + 15) & ~15;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = blockIdx.y * 8 + warp;
+  if (j >= Nm) return;
   uint8_t* base = reinterpret_cast<uint8_t*>(xg + (size_t)T.w * h);
   const int npieces = h / 8;
-  for (int j = warp; j < Nm; j += 8) {
-    const int jj = min(j, n - 1);
-    int r = (T.x == E) ? T.y + jj : rows[T.y + jj];
-    const bool ok = (r >= 0 && r < t);
-    if (!ok && lane == 0) raise_flag(st, FLAG_BAD_ROW);
-    for (int pc = lane; pc < npieces; pc += 32) {
-      const uint4 v = ok ? reinterpret_cast<const uint4*>(x + (size_t)r * h)[pc] : make_uint4(0, 0, 0, 0);
-      const int kc = pc >> 3, c = pc & 7;
-      *reinterpret_cast<uint4*>(base + (size_t)kc * Nm * 128 + sw128_off(j, c)) = v;
-    }
+  const int jj = min(j, n - 1);
+  const int r = (T.x == E) ? T.y + jj : rows[T.y + jj];
+  const bool ok = (r >= 0 && r < t);
+  if (!ok && lane == 0) raise_flag(st, FLAG_BAD_ROW);
+  for (int pc = lane; pc < npieces; pc += 32) {
+    const uint4 v = ok ? reinterpret_cast<const uint4*>(x + (size_t)r * h)[pc] : make_uint4(0, 0, 0, 0);
+    const int kc = pc >> 3, c = pc & 7;
+    *reinterpret_cast<uint4*>(base + (size_t)kc * Nm * 128 + sw128_off(j, c)) = v;
   }
 }
 
@@ -255,7 +264,8 @@ struct PSmem {
   uint64_t code_full[PCfg<GATEUP>::SC], code_empty[PCfg<GATEUP>::SC];
   uint64_t a_full[PCfg<GATEUP>::SA], a_empty[PCfg<GATEUP>::SA];
   uint64_t b_full[SB], b_empty[SB];
-  uint64_t acc_full, acc_empty, drain;
+  uint64_t acc_full[PCfg<GATEUP>::NACC], acc_empty[PCfg<GATEUP>::NACC];
+  uint64_t drain;
   uint32_t tmem_slot;
   int abort;
 };
@@ -286,18 +296,20 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::SC; ++i) {
       mbar_init(&S.code_full[i], 1);
-      mbar_init(&S.code_empty[i], 8);
+      mbar_init(&S.code_empty[i], 4);
     }
     for (int i = 0; i < C::SA; ++i) {
-      mbar_init(&S.a_full[i], 8);
+      mbar_init(&S.a_full[i], 4);
       mbar_init(&S.a_empty[i], 1);
     }
     for (int i = 0; i < SB; ++i) {
       mbar_init(&S.b_full[i], 1);
       mbar_init(&S.b_empty[i], 1);
     }
-    mbar_init(&S.acc_full, 1);
-    mbar_init(&S.acc_empty, 8);
+    for (int i = 0; i < C::NACC; ++i) {
+      mbar_init(&S.acc_full[i], 1);
+      mbar_init(&S.acc_empty[i], 4);
+    }
     mbar_init(&S.drain, 1);
     S.abort = 0;
     fence_mbar_init();
@@ -311,7 +323,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
   const int n_units = GATEUP ? p.hdr->n_units_gu : p.hdr->n_units_dn;
 
   if (warp == W_CODE) {
-    // ------------------------------------------------------------ packed weight blocks
+    // ------------------------------------------------------------ packed weight blocks, 2 chunks per copy
     if (lane == 0) {
       uint32_t it = 0;
       bool armed[C::SC];
@@ -326,7 +338,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         const uint8_t* src;
         if (GATEUP) src = rec + (size_t)(U.f0 / 128) * (h / KC) * 2 * QB;
         else src = rec + gu_bytes(h, Iu) + (size_t)(U.f0 / 128) * (Iu / KC) * QB;
-        for (int kc = 0; kc < U.nkc; ++kc, ++it) {
+        for (int st = 0; st < U.nkc / CPS; ++st, ++it) {
           const int sc = it % C::SC;
           if (!mbar_wait(&S.code_empty[sc], ((it / C::SC) & 1) ^ 1, abort, WAIT_NS)) {
             note_timeout(p.status, abort, GATEUP ? 31 : 41);
@@ -334,7 +346,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
             break;
           }
           mbar_arrive_expect_tx(&S.code_full[sc], C::C_STAGE);
-          bulk_load(c_s + sc * C::C_STAGE, src + (size_t)kc * C::C_STAGE, C::C_STAGE, &S.code_full[sc]);
+          bulk_load(c_s + sc * C::C_STAGE, src + (size_t)st * C::C_STAGE, C::C_STAGE, &S.code_full[sc]);
           armed[sc] = true;
           par[sc] = (it / C::SC) & 1;
         }
@@ -377,94 +389,96 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
           if (armed[i]) drain_wait(&S.b_full[i], par[i]);
     }
   } else if (warp == W_MMA) {
-    // ------------------------------------------------------------ MMA (A in TMEM)
+    // ------------------------------------------------------------ MMA issuer (A in TMEM)
     if (lane == 0) {
-      uint32_t ait = 0, bit = 0, uit = 0;
+      uint32_t ast = 0, bit = 0, uit = 0;
       for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
         const PUnit U = decode_punit<GATEUP>(p, u);
         const uint32_t idesc = idesc_bf16(128, U.Nm);
-        if (uit > 0 && !mbar_wait(&S.acc_empty, (uit - 1) & 1, abort, WAIT_NS)) {
+        const int ab = uit % C::NACC;
+        if (!mbar_wait(&S.acc_empty[ab], ((uit / C::NACC) & 1) ^ 1, abort, WAIT_NS)) {
           note_timeout(p.status, abort, GATEUP ? 33 : 43);
           break;
         }
         tc_fence_after();
+        const uint32_t acc = tmem + ab * C::ACC_COLS;
         bool ok = true;
-        for (int kc = 0; kc < U.nkc; ++kc) {
-          const int sub = kc % U.kps;
-          const int sb = bit % SB;
-          if (sub == 0 && !mbar_wait(&S.b_full[sb], (bit / SB) & 1, abort, WAIT_NS)) {
-            note_timeout(p.status, abort, GATEUP ? 34 : 44);
-            ok = false;
-            break;
-          }
-          const int sa = ait % C::SA;
-          if (!mbar_wait(&S.a_full[sa], (ait / C::SA) & 1, abort, WAIT_NS)) {
+        for (int st = 0; st < U.nkc / CPS && ok; ++st, ++ast) {
+          const int sa = ast % C::SA;
+          if (!mbar_wait(&S.a_full[sa], (ast / C::SA) & 1, abort, WAIT_NS)) {
             note_timeout(p.status, abort, GATEUP ? 35 : 45);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t bd = desc_sw128(smem_u32(b_s + sb * B_STAGE + sub * U.Nm * 128));
 #pragma unroll
-          for (int m = 0; m < C::NMAT; ++m) {
-            const uint32_t a_tm = tmem + A_COL + sa * C::A_STRIDE + m * 32;
+          for (int c = 0; c < CPS; ++c) {
+            const int kc = st * CPS + c;
+            const int sub = kc % U.kps;
+            const int sb = bit % SB;
+            if (sub == 0) {
+              if (!mbar_wait(&S.b_full[sb], (bit / SB) & 1, abort, WAIT_NS)) {
+                note_timeout(p.status, abort, GATEUP ? 34 : 44);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            const uint64_t bd = desc_sw128(smem_u32(b_s + sb * B_STAGE + sub * U.Nm * 128));
 #pragma unroll
-            for (int kk = 0; kk < KC / 16; ++kk)
-              mma_bf16_ta(tmem + m * ACC_UP, a_tm + 8 * kk, bd + 2 * kk, idesc, (kc | kk) != 0);
+            for (int m = 0; m < C::NMAT; ++m) {
+              const uint32_t a_tm = tmem + A_COL + sa * C::A_STAGE + (c * C::NMAT + m) * 32;
+#pragma unroll
+              for (int kk = 0; kk < KC / 16; ++kk)
+                mma_bf16_ta(acc + m * 128, a_tm + 8 * kk, bd + 2 * kk, idesc, (kc | kk) != 0);
+            }
+            if (sub == U.kps - 1 || kc == U.nkc - 1) {
+              mma_commit(&S.b_empty[sb]);
+              ++bit;
+            }
           }
+          if (!ok) break;
           mma_commit(&S.a_empty[sa]);
-          ++ait;
-          if (sub == U.kps - 1 || kc == U.nkc - 1) {
-            mma_commit(&S.b_empty[sb]);
-            ++bit;
-          }
         }
         if (!ok) break;
-        mma_commit(&S.acc_full);
+        mma_commit(&S.acc_full[ab]);
       }
       if (*abort) {
         mma_commit(&S.drain);
         drain_wait(&S.drain, 0);
       }
     }
-  } else {
-    // ------------------------------------------------------------ dequant + epilogue
-    const int dw = warp - W_DQ0;         // 0..7
-    const int q = warp & 3;              // TMEM lane quarter this warp may access
-    const int o = q * 32 + lane;         // weight row (= TMEM lane) this thread dequantises
-    const int part = dw >> 2;            // gate/up: matrix; down: K half
+  } else if (warp < W_B) {
+    // ------------------------------------------------------------ dequant: two groups alternate stages
+    const int grp = (warp - W_DQ0) >> 2;  // 0: warps 2-5, 1: warps 6-9
+    const int q = warp & 3;               // TMEM lane quarter this warp may access
+    const int o = q * 32 + lane;          // weight row (= TMEM lane)
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-    uint32_t cit = 0, ait = 0, uit = 0;
-    for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
+    uint32_t ast = 0;
+    for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
       const PUnit U = decode_punit<GATEUP>(p, u);
-      const int Iu = U.shared ? p.Is : p.I;
       bool ok = true;
-      for (int kc = 0; kc < U.nkc; ++kc) {
-        const int sc = cit % C::SC, sa = ait % C::SA;
-        if (!mbar_wait(&S.code_full[sc], (cit / C::SC) & 1, abort, WAIT_NS) ||
-            !mbar_wait(&S.a_empty[sa], ((ait / C::SA) & 1) ^ 1, abort, WAIT_NS)) {
+      for (int st = 0; st < U.nkc / CPS; ++st, ++ast) {
+        if ((int)(ast & 1) != grp) continue;
+        const int sc = ast % C::SC, sa = ast % C::SA;
+        if (!mbar_wait(&S.code_full[sc], (ast / C::SC) & 1, abort, WAIT_NS) ||
+            !mbar_wait(&S.a_empty[sa], ((ast / C::SA) & 1) ^ 1, abort, WAIT_NS)) {
           note_timeout(p.status, abort, GATEUP ? 36 : 46);
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint8_t* blk = c_s + sc * C::C_STAGE + (GATEUP ? part * QB : 0);
-        const __nv_bfloat16 sv = reinterpret_cast<const __nv_bfloat16*>(blk + 4096)[o];
-        const __nv_bfloat16 bv = reinterpret_cast<const __nv_bfloat16*>(blk + 4096 + 256)[o];
-        const __nv_bfloat162 s2 = __halves2bfloat162(sv, sv), b2 = __halves2bfloat162(bv, bv);
-        if (GATEUP) {
+#pragma unroll
+        for (int cm = 0; cm < CPS * C::NMAT; ++cm) {
+          const uint8_t* blk = c_s + sc * C::C_STAGE + cm * QB;
+          const __nv_bfloat16 sv = reinterpret_cast<const __nv_bfloat16*>(blk + 4096)[o];
+          const __nv_bfloat16 bv = reinterpret_cast<const __nv_bfloat16*>(blk + 4096 + 256)[o];
           const uint4 c0 = reinterpret_cast<const uint4*>(blk + o * 32)[0];
           const uint4 c1 = reinterpret_cast<const uint4*>(blk + o * 32)[1];
           const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
           uint32_t r[32];
-          dequant_packed<8>(wd, s2, b2, r);
-          tmem_st<32>(lane_base + A_COL + sa * C::A_STRIDE + part * 32, r);
-        } else {
-          const uint4 cw = reinterpret_cast<const uint4*>(blk + o * 32)[part];
-          const uint32_t wd[4] = {cw.x, cw.y, cw.z, cw.w};
-          uint32_t r[16];
-          dequant_packed<4>(wd, s2, b2, r);
-          tmem_st<16>(lane_base + A_COL + sa * C::A_STRIDE + part * 16, r);
+          dequant_packed<8>(wd, __halves2bfloat162(sv, sv), __halves2bfloat162(bv, bv), r);
+          tmem_st<32>(lane_base + A_COL + sa * C::A_STAGE + cm * 32, r);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -473,12 +487,19 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
           mbar_arrive(&S.a_full[sa]);
           mbar_arrive(&S.code_empty[sc]);
         }
-        ++ait;
-        ++cit;
       }
       if (!ok) break;
-      // ---- epilogue: columns split between the two warps of each lane quarter
-      const int ncw = (U.Nm + 31) / 32;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue warpgroup
+    const int q = warp & 3;
+    const int o = q * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    uint32_t uit = 0;
+    for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
+      const PUnit U = decode_punit<GATEUP>(p, u);
+      const int ab = uit % C::NACC;
+      const int feat = U.f0 + o;
       int col_row[4];
       float col_w[4];
 #pragma unroll
@@ -486,7 +507,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         col_row[g] = 0;
         col_w[g] = 1.f;
         const int col = g * 32 + lane;
-        if (!GATEUP && g < ncw && col < U.n) {
+        if (!GATEUP && col < U.n) {
           if (U.shared) {
             col_row[g] = U.start + col;
             col_w[g] = p.gate_vals ? p.gate_vals[U.start + col] : 1.f;
@@ -496,36 +517,53 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
           }
         }
       }
-      if (!mbar_wait(&S.acc_full, uit & 1, abort, WAIT_NS)) {
+      if (!mbar_wait(&S.acc_full[ab], (uit / C::NACC) & 1, abort, WAIT_NS)) {
         note_timeout(p.status, abort, GATEUP ? 37 : 47);
         break;
       }
       tc_fence_after();
-      const int feat = U.f0 + o;  // output feature of this TMEM lane
+      const uint32_t acc = lane_base + ab * C::ACC_COLS;
       if (GATEUP) {
-        // hg image: K chunk feat / 64, 16-byte piece (feat % 64) / 8, element feat % 8
-        uint8_t* img = reinterpret_cast<uint8_t*>(p.hg + (size_t)U.pad * P.kmax) +
-                       (size_t)(feat / 64) * U.Nm * 128;
-        const int c8 = (feat % 64) / 8, e8 = feat % 8;
-        for (int c = part; c * 16 < U.Nm; c += 2) {
-          uint32_t g[16], v[16];
-          tmem_ld16(lane_base + c * 16, g);
-          tmem_ld16(lane_base + ACC_UP + c * 16, v);
-          tmem_ld_wait();
+        // drain TMEM into registers (silu(gate) * up as bf16 pairs), release
+        // the accumulator, then store the hg image
+        uint32_t res[8][8];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = c * 16 + j;
-            const float hv = silu_mul(__uint_as_float(g[j]), __uint_as_float(v[j]));
-            // padding columns get zeros so the down GEMM reads finite values
-            *reinterpret_cast<uint16_t*>(img + sw128_off(col, c8) + e8 * 2) = col < U.n ? f2bf(hv) : (uint16_t)0;
+        for (int c = 0; c < 8; ++c) {
+          if (c * 16 < U.Nm) {
+            uint32_t g[16], v[16];
+            tmem_ld16(acc + c * 16, g);
+            tmem_ld16(acc + 128 + c * 16, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float h0 = c * 16 + 2 * j < U.n ? silu_mul(__uint_as_float(g[2 * j]), __uint_as_float(v[2 * j])) : 0.f;
+              const float h1 =
+                  c * 16 + 2 * j + 1 < U.n ? silu_mul(__uint_as_float(g[2 * j + 1]), __uint_as_float(v[2 * j + 1])) : 0.f;
+              res[c][j] = pack_bf16x2(h0, h1);
+            }
           }
         }
-        (void)Iu;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
+        uint8_t* img = reinterpret_cast<uint8_t*>(p.hg + (size_t)U.pad * P.kmax) + (size_t)(feat / 64) * U.Nm * 128;
+        const int c8 = (feat % 64) / 8, e8 = feat % 8;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          if (c * 16 < U.Nm) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const uint32_t pr = res[c][j >> 1];
+              *reinterpret_cast<uint16_t*>(img + sw128_off(c * 16 + j, c8) + e8 * 2) =
+                  (uint16_t)((j & 1) ? (pr >> 16) : (pr & 0xFFFFu));
+            }
+          }
+        }
       } else {
         bool bad_row = false;
-        for (int c = part; c * 16 < U.Nm; c += 2) {
+        for (int c = 0; c * 16 < U.Nm; ++c) {
           uint32_t y[16];
-          tmem_ld16(lane_base + c * 16, y);
+          tmem_ld16(acc + c * 16, y);
           tmem_ld_wait();
           const int grp = c >> 1;
           int rsel = col_row[0];
@@ -552,10 +590,10 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
           }
         }
         if (bad_row && lane == 0) raise_flag(p.status, FLAG_BAD_ROW);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.acc_empty);
     }
   }
 
@@ -650,7 +688,8 @@ cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, c
   if (p.gate_vals && (err = launch_shared_gate(a.x, a.s_gate, a.t, a.h, gate_vals, stream)) != cudaSuccess)
     return err;
   MOE_LAUNCH("gather", stream,
-             gather_kernel<<<(unsigned)mt, 256, 0, stream>>>(a.x, a.rows, hdr, tiles, a.t, a.h, a.E, xg, a.status));
+             gather_kernel<<<dim3((unsigned)mt, PTILE / 8), 256, 0, stream>>>(a.x, a.rows, hdr, tiles, a.t, a.h, a.E,
+                                                                             xg, a.status));
   const int grid = num_sms();
   MOE_LAUNCH("gateup_packed", stream,
              packed_gemm_kernel<true><<<grid, KTHREADS, psmem_bytes<true>(), stream>>>(P));
