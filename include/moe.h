@@ -172,6 +172,31 @@ int moe_experts_fwd(const uint16_t* x, const moe_csr* csr, const moe_qweights* e
                     uint32_t flags, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * moe_build_csr without a workspace (no counterpart in the method; an
+ * interface for callers that cannot allocate device memory, e.g. code running
+ * inside someone else's memory pool or under a rule that forbids cudaMalloc on
+ * its hot path).  It computes exactly what moe_build_csr computes, into the
+ * caller's `csr` arrays, but keeps its scratch in a fixed array inside this
+ * library (about 0.8 MB per GPU that loads the library, held until the process
+ * exits).  It allocates nothing and calls no allocating routine.
+ *
+ *   - t*k must not exceed MOE_NOALLOC_MAX_PAIRS (else MOE_ESHAPE, nothing
+ *     enqueued); E <= 1024, k <= min(E, 16).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array: calls whose GPU work overlaps (other
+ *     streams, other threads) race and give wrong results.  Order them on one
+ *     stream or synchronise between them.
+ *   - An id outside [0, E) drops its pair (slot_of = -1) as in moe_build_csr;
+ *     the device-side flags of this variant are not reported.
+ * Errors: MOE_EINVAL, MOE_ESHAPE, MOE_ECUDA.
+ */
+#define MOE_NOALLOC_MAX_PAIRS 65536
+int moe_build_csr_noalloc(const int32_t* idx, const float* w, const moe_dims* dims, const moe_csr* csr,
+                          void* stream);
+
+/*
  * Weight packing (a one-time, model-load step; no counterpart in the method).
  * Rewrites row-major 4-bit expert records (the moe_qweights layout) into
  * tile-contiguous blocks that moe_experts_fwd streams with one bulk copy per

@@ -137,3 +137,81 @@ cudaError_t launch_build_csr(const int32_t* idx, const float* w, int t, int k, i
 }
 
 }  // namespace moe
+
+// ----------------------------------------------------------------------------
+// moe_build_csr_noalloc: the same grouping for callers that cannot allocate
+// device memory (a caller already inside a memory pool it does not own, an
+// embedding that forbids cudaMalloc on its hot path, ...).  Its scratch is a
+// fixed array in this library's device image, so each GPU that loads the
+// library holds it (NOALLOC_SCRATCH_BYTES) until the process exits.
+// ----------------------------------------------------------------------------
+#include <mutex>
+
+namespace moe {
+
+namespace {
+
+constexpr size_t NOALLOC_RANK_OFF = 256;  // after the status flags
+constexpr size_t NOALLOC_COUNTS_OFF = NOALLOC_RANK_OFF + (size_t)MOE_NOALLOC_MAX_PAIRS * 4;
+constexpr size_t NOALLOC_BASE_OFF = NOALLOC_COUNTS_OFF + (size_t)MOE_NOALLOC_MAX_PAIRS * 4;
+constexpr size_t NOALLOC_SCRATCH_BYTES = NOALLOC_BASE_OFF + (size_t)MOE_NOALLOC_MAX_PAIRS * 4;
+
+// Status flags, per-pair ranks, per-chunk counts and prefixes.  The count
+// table holds E * ceil(t*k / CSR_CHUNK) entries, which is at most
+// 1024 * MOE_NOALLOC_MAX_PAIRS / 1024 = MOE_NOALLOC_MAX_PAIRS.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+unsigned char* g_noalloc_ptr[kMaxDevices] = {};
+
+}  // namespace
+
+}  // namespace moe
+
+extern "C" int moe_build_csr_noalloc(const int32_t* idx, const float* w, const moe_dims* dims, const moe_csr* csr,
+                                     void* stream) {
+  using namespace moe;
+  if (!dims) return set_error(MOE_EINVAL, "dims is NULL");
+  if (dims->t < 1 || dims->k < 1 || dims->k > 16 || dims->E < 1 || dims->E > 1024 || dims->k > dims->E)
+    return set_error(MOE_ESHAPE, "t=%d, k=%d, E=%d outside 1 <= t, 1 <= k <= min(E, 16), E <= 1024", dims->t,
+                     dims->k, dims->E);
+  if ((long long)dims->t * dims->k > MOE_NOALLOC_MAX_PAIRS)
+    return set_error(MOE_ESHAPE, "t*k = %lld exceeds the %d pairs moe_build_csr_noalloc's fixed scratch holds",
+                     (long long)dims->t * dims->k, MOE_NOALLOC_MAX_PAIRS);
+  if (!idx || !w || !csr || !csr->offsets || !csr->rows || !csr->weights || !csr->slot_of)
+    return set_error(MOE_EINVAL, "a pointer argument is NULL");
+  const void* ptrs[] = {idx, w, csr->offsets, csr->rows, csr->weights, csr->slot_of};
+  for (const void* p : ptrs)
+    if ((uintptr_t)p % 4) return set_error(MOE_EINVAL, "a pointer argument is not 4-byte aligned");
+
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return set_error(MOE_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(err));
+  if (dev < 0 || dev >= kMaxDevices) return set_error(MOE_EINVAL, "device %d out of range", dev);
+  unsigned char* scratch;
+  {
+    // First call on this device: look up the device address of the array
+    // (the host-side name of a __device__ array is not a device address).
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+      void* p = nullptr;
+      err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (err != cudaSuccess) return set_error(MOE_ECUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(err));
+      g_noalloc_ptr[dev] = static_cast<unsigned char*>(p);
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  // The status flags are OR-ed into; everything else is written before it is read.
+  err = cudaMemsetAsync(scratch, 0, sizeof(DeviceStatus), s);
+  if (err != cudaSuccess) return set_error(MOE_ECUDA, "status clear: %s", cudaGetErrorString(err));
+  WsLayout L{};
+  L.status = 0;
+  L.csr_rank = NOALLOC_RANK_OFF;
+  L.csr_counts = NOALLOC_COUNTS_OFF;
+  L.csr_base = NOALLOC_BASE_OFF;
+  err = launch_build_csr(idx, w, dims->t, dims->k, dims->E, *csr, scratch, L, s);
+  if (err != cudaSuccess) return set_error(MOE_ECUDA, "moe_build_csr_noalloc launch: %s", cudaGetErrorString(err));
+  return MOE_OK;
+}

@@ -43,6 +43,7 @@ EXPORTS = (
     "moe_profile_read",
     "moe_packed_bytes",
     "moe_pack_experts",
+    "moe_build_csr_noalloc",
 )
 
 
@@ -111,6 +112,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_profile_read.argtypes = [ctypes.POINTER(MoeProfileEntry), ctypes.c_int]
     lib.moe_packed_bytes.restype = sz
     lib.moe_packed_bytes.argtypes = [ctypes.POINTER(MoeDims), ctypes.c_int]
+    lib.moe_build_csr_noalloc.restype = ctypes.c_int
+    lib.moe_build_csr_noalloc.argtypes = [vp, vp, ctypes.POINTER(MoeDims), ctypes.POINTER(MoeCsr), vp]
     lib.moe_pack_experts.restype = ctypes.c_int
     lib.moe_pack_experts.argtypes = [ctypes.POINTER(MoeQWeights), ctypes.POINTER(MoeDims), ctypes.c_int, vp, sz, vp]
     _lib = lib
@@ -202,6 +205,25 @@ def moe_build_csr(idx: torch.Tensor, w: torch.Tensor, E: int, ws: torch.Tensor |
     c = out.c()
     _check(lib.moe_build_csr(_ptr(idx), _ptr(w), ctypes.byref(dims), ctypes.byref(c), _ptr(ws), ws.numel(),
                              _stream(stream)))
+    return out
+
+
+def moe_build_csr_noalloc(idx: torch.Tensor, w: torch.Tensor, E: int, out: Csr | None = None,
+                          stream=None) -> Csr:
+    """moe_build_csr with the library's fixed scratch instead of a workspace
+    (for callers that may not allocate; at most MOE_NOALLOC_MAX_PAIRS = 65536
+    (row, slot) pairs).  Only the output tensors are the caller's."""
+    lib = load_library()
+    t, k = idx.shape
+    dims = MoeDims(t, 128, 128, E, k, 0)
+    if out is None:
+        dev = idx.device
+        out = Csr(torch.empty(E + 1, dtype=torch.int32, device=dev),
+                  torch.empty(t * k, dtype=torch.int32, device=dev),
+                  torch.empty(t * k, dtype=torch.float32, device=dev),
+                  torch.empty(t * k, dtype=torch.int32, device=dev))
+    c = out.c()
+    _check(lib.moe_build_csr_noalloc(_ptr(idx), _ptr(w), ctypes.byref(dims), ctypes.byref(c), _stream(stream)))
     return out
 
 

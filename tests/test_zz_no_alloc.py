@@ -1,0 +1,60 @@
+"""moe_build_csr_noalloc, the grouping entry point for callers that may not
+allocate device memory (it keeps its scratch in a fixed array inside the
+library).  Called through the C ABI, it must give exactly what the
+workspace-based moe_build_csr gives, on consecutive calls that reuse the same
+fixed scratch.  Collected last (file name) so that a run that stops at the
+first failure has already run every other test."""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from routed_expert_prefill_gb300 import build
+
+    build.build()
+    from routed_expert_prefill_gb300 import moe as m
+
+    m.load_library()
+    return m
+
+
+def _routing(t, k, E, seed):
+    rng = np.random.default_rng(seed)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(t)]).astype(np.int32)
+    w = rng.random((t, k)).astype(np.float32)
+    return torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda()
+
+
+def test_noalloc_csr_matches_workspace_csr_on_consecutive_calls(moe):
+    # a large call, then a smaller one on top of the first one's leftovers,
+    # then one with a skewed id histogram
+    for t, k, E, seed in ((4096, 8, 128, 1), (37, 4, 16, 2), (8192, 8, 256, 3)):
+        idx, w = _routing(t, k, E, seed)
+        if seed == 3:
+            idx[: t // 2, 0] = 5  # half the rows share one expert first
+            idx[: t // 2, 1:] = torch.where(idx[: t // 2, 1:] == 5, 6, idx[: t // 2, 1:])
+        ref = moe.moe_build_csr(idx, w, E)
+        got = moe.moe_build_csr_noalloc(idx, w, E)
+        torch.cuda.synchronize()
+        for name in ("offsets", "rows", "slot_of"):
+            np.testing.assert_array_equal(getattr(got, name).cpu().numpy(), getattr(ref, name).cpu().numpy(), name)
+        np.testing.assert_array_equal(got.weights.cpu().numpy().view(np.uint32),
+                                      ref.weights.cpu().numpy().view(np.uint32))
+
+
+def test_noalloc_rejects_more_pairs_than_its_scratch_holds(moe):
+    t, k = 8193, 8  # 65544 pairs > 65536
+    idx = torch.zeros((t, k), dtype=torch.int32, device="cuda")
+    w = torch.zeros((t, k), dtype=torch.float32, device="cuda")
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_build_csr_noalloc(idx, w, 16)
+    assert ei.value.status == -2
+    assert b"scratch" in moe.load_library().moe_last_error()
