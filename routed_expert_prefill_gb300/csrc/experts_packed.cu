@@ -162,7 +162,9 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   mbar_wait(bar, parity, &never, 100000000ull);
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
+// silu(g) * u with the fast exponential and division (relative error a few
+// ulp, far inside the block-output tolerance).
+__device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.f + __expf(-g)) * u; }
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -390,11 +392,18 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     }
   } else if (warp == W_MMA) {
     // ------------------------------------------------------------ MMA issuer (A in TMEM)
+    // The issue loop is kept lean (no division, descriptors stepped
+    // incrementally): a single thread feeds the tensor pipe, so every
+    // instruction between two MMAs delays the next one.
     if (lane == 0) {
+      uint64_t bstage[SB];
+#pragma unroll
+      for (int i = 0; i < SB; ++i) bstage[i] = desc_sw128(smem_u32(b_s + i * B_STAGE));
       uint32_t ast = 0, bit = 0, uit = 0;
       for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
         const PUnit U = decode_punit<GATEUP>(p, u);
         const uint32_t idesc = idesc_bf16(128, U.Nm);
+        const uint32_t nm8 = (uint32_t)(U.Nm * 128) >> 4;  // descriptor step of one K chunk
         const int ab = uit % C::NACC;
         if (!mbar_wait(&S.acc_empty[ab], ((uit / C::NACC) & 1) ^ 1, abort, WAIT_NS)) {
           note_timeout(p.status, abort, GATEUP ? 33 : 43);
@@ -403,6 +412,8 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         tc_fence_after();
         const uint32_t acc = tmem + ab * C::ACC_COLS;
         bool ok = true;
+        int sub = 0;
+        uint64_t bd = 0;
         for (int st = 0; st < U.nkc / CPS && ok; ++st, ++ast) {
           const int sa = ast % C::SA;
           if (!mbar_wait(&S.a_full[sa], (ast / C::SA) & 1, abort, WAIT_NS)) {
@@ -411,10 +422,10 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
             break;
           }
           tc_fence_after();
+          const uint32_t a_st = tmem + A_COL + sa * C::A_STAGE;
 #pragma unroll
           for (int c = 0; c < CPS; ++c) {
             const int kc = st * CPS + c;
-            const int sub = kc % U.kps;
             const int sb = bit % SB;
             if (sub == 0) {
               if (!mbar_wait(&S.b_full[sb], (bit / SB) & 1, abort, WAIT_NS)) {
@@ -423,18 +434,20 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
                 break;
               }
               tc_fence_after();
+              bd = bstage[sb];
             }
-            const uint64_t bd = desc_sw128(smem_u32(b_s + sb * B_STAGE + sub * U.Nm * 128));
 #pragma unroll
             for (int m = 0; m < C::NMAT; ++m) {
-              const uint32_t a_tm = tmem + A_COL + sa * C::A_STAGE + (c * C::NMAT + m) * 32;
 #pragma unroll
               for (int kk = 0; kk < KC / 16; ++kk)
-                mma_bf16_ta(acc + m * 128, a_tm + 8 * kk, bd + 2 * kk, idesc, (kc | kk) != 0);
+                mma_bf16_ta(acc + m * 128, a_st + (c * C::NMAT + m) * 32 + 8 * kk, bd + 2 * kk, idesc,
+                            (kc | kk) != 0);
             }
-            if (sub == U.kps - 1 || kc == U.nkc - 1) {
+            bd += nm8;
+            if (++sub == U.kps || kc == U.nkc - 1) {
               mma_commit(&S.b_empty[sb]);
               ++bit;
+              sub = 0;
             }
           }
           if (!ok) break;
