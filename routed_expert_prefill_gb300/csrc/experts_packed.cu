@@ -224,6 +224,31 @@ __device__ __forceinline__ void dequant_packed(const uint32_t* w, __nv_bfloat162
   }
 }
 
+// Down epilogue for 16 accumulator columns: column j of the tile goes to
+// row s_row[j] of dcol (a per-feature column of the destination, pitch h),
+// scaled by s_w[j]; plain stores in deterministic mode, fp32 reductions
+// otherwise.
+template <bool DET>
+__device__ __forceinline__ void down_cols16(const uint32_t (&y)[16], const int* s_row, const float* s_w,
+                                            float* dcol, int h) {
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    const int4 r4 = reinterpret_cast<const int4*>(s_row)[jj];
+    const float4 w4 = reinterpret_cast<const float4*>(s_w)[jj];
+    const int rr[4] = {r4.x, r4.y, r4.z, r4.w};
+    const float ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (rr[i] >= 0) {
+        float* d = dcol + (size_t)(uint32_t)rr[i] * (uint32_t)h;
+        const float v = ww[i] * __uint_as_float(y[4 * jj + i]);
+        if (DET) *d = v;
+        else atomicAdd(d, v);
+      }
+    }
+  }
+}
+
 struct PUnit {
   int e, start, n, Nm, f0, nkc, kps, pad;
   bool shared;
@@ -263,6 +288,10 @@ struct PParams {
 
 template <bool GATEUP>
 struct PSmem {
+  // down epilogue: per epilogue warp, the destination row (-1: skip) and
+  // weight of every column of the current tile
+  alignas(16) int col_row[4][PTILE];
+  alignas(16) float col_w[4][PTILE];
   uint64_t code_full[PCfg<GATEUP>::SC], code_empty[PCfg<GATEUP>::SC];
   uint64_t a_full[PCfg<GATEUP>::SA], a_empty[PCfg<GATEUP>::SA];
   uint64_t b_full[SB], b_empty[SB];
@@ -513,22 +542,38 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
       const PUnit U = decode_punit<GATEUP>(p, u);
       const int ab = uit % C::NACC;
       const int feat = U.f0 + o;
-      int col_row[4];
-      float col_w[4];
+      // down: this warp's copy of the tile's destination rows and weights.
+      // Deterministic mode writes routed columns to their own list position
+      // (weights applied when the slots are summed) and the shared expert
+      // straight into the block accumulator.
+      const bool to_list = p.deterministic && !U.shared;
+      if (!GATEUP) {
+        bool bad_row = false;
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        col_row[g] = 0;
-        col_w[g] = 1.f;
-        const int col = g * 32 + lane;
-        if (!GATEUP && col < U.n) {
-          if (U.shared) {
-            col_row[g] = U.start + col;
-            col_w[g] = p.gate_vals ? p.gate_vals[U.start + col] : 1.f;
-          } else {
-            col_row[g] = p.rows[U.start + col];
-            col_w[g] = p.weights[U.start + col];
+        for (int g = 0; g < 4; ++g) {
+          const int col = g * 32 + lane;
+          int r = -1;
+          float wv = 0.f;
+          if (col < U.n) {
+            if (to_list) {
+              r = U.start + col;
+              wv = 1.f;
+            } else {
+              if (U.shared) {
+                r = U.start + col;
+                wv = p.gate_vals ? p.gate_vals[r] : 1.f;
+              } else {
+                r = p.rows[U.start + col];
+                wv = p.weights[U.start + col];
+              }
+              if (r < 0 || r >= p.t) bad_row = true, r = -1;
+            }
           }
+          S.col_row[q][col] = r;
+          S.col_w[q][col] = wv;
         }
+        if (bad_row) raise_flag(p.status, FLAG_BAD_ROW);
+        __syncwarp();
       }
       if (!mbar_wait(&S.acc_full[ab], (uit / C::NACC) & 1, abort, WAIT_NS)) {
         note_timeout(p.status, abort, GATEUP ? 37 : 47);
@@ -573,36 +618,14 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
           }
         }
       } else {
-        bool bad_row = false;
+        float* dcol = (to_list ? p.ybuf : p.acc) + feat;
         for (int c = 0; c * 16 < U.Nm; ++c) {
           uint32_t y[16];
           tmem_ld16(acc + c * 16, y);
           tmem_ld_wait();
-          const int grp = c >> 1;
-          int rsel = col_row[0];
-          float wsel = col_w[0];
-#pragma unroll
-          for (int g = 1; g < 4; ++g)
-            if (g == grp) rsel = col_row[g], wsel = col_w[g];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = c * 16 + j;
-            const int src = (c & 1) * 16 + j;
-            const int r = __shfl_sync(0xFFFFFFFFu, rsel, src);
-            const float wv = __shfl_sync(0xFFFFFFFFu, wsel, src);
-            if (col >= U.n) continue;
-            const float yv = __uint_as_float(y[j]);
-            if (p.deterministic) {
-              if (U.shared) p.acc[(size_t)r * h + feat] = wv * yv;
-              else p.ybuf[(size_t)(U.start + col) * h + feat] = yv;
-            } else if (r >= 0 && r < p.t) {
-              atomicAdd(&p.acc[(size_t)r * h + feat], wv * yv);
-            } else {
-              bad_row = true;
-            }
-          }
+          if (p.deterministic) down_cols16<true>(y, &S.col_row[q][c * 16], &S.col_w[q][c * 16], dcol, h);
+          else down_cols16<false>(y, &S.col_row[q][c * 16], &S.col_w[q][c * 16], dcol, h);
         }
-        if (bad_row && lane == 0) raise_flag(p.status, FLAG_BAD_ROW);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
