@@ -75,14 +75,15 @@ def step_work(w: synth.Workload, counts: np.ndarray) -> dict:
                      + ((Is * h // 2 + 2 * 2 * Is * h // 64) if Is else 0)
                      + (n * I + t * Is) * 2 + 2 * t * h * 4,
                      flops=2 * n * h * I + 2 * t * h * Is),
-        "route_topk": dict(bytes=t * h * 2 + E * h * 2 + t * k * 8, flops=2 * t * h * E),
+        # router (scores + exact refinement): x and router weights in, idx/w out
+        "route": dict(bytes=t * h * 2 + E * h * 2 + t * k * 8, flops=2 * t * h * E),
     }
     return dict(touched=touched, pairs=n, max_rows=int(counts.max()), flops=flops,
                 bytes=wbytes + io, by_kernel=by_kernel)
 
 
 def kernel_family(name: str) -> str:
-    for fam in ("gateup", "down", "route_topk"):
+    for fam in ("gateup", "down", "route"):
         if name.startswith(fam):
             return fam
     return name
@@ -231,28 +232,49 @@ def run_ours(args, w: synth.Workload):
     counts = np.diff(res["csr"].offsets.cpu().numpy())
     work = step_work(w, counts)
 
-    # ---- device-resident timed region (L2 flushed between steps, untimed)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # ---- device-resident timed region (L2 flushed between steps, untimed).
+    # The step is captured once into a CUDA graph and replayed, so the
+    # timing is the GPU's, not the host's launch rate.
+    graph = None
+    if not args.no_graph:
+        side = torch.cuda.Stream(device=dev_name)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        graph.replay()
+        torch.cuda.synchronize()
+
+    def timed(run, n):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for i in range(n):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            run()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
     sampler = ClockSampler(local)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.3)
-    moe.profile_enable(True)
     wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.fill_(float(i))
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
+    step_ms = timed(graph.replay if graph is not None else step, args.steps)
     wall = time.perf_counter() - wall0
+    # per-kernel device time: the same steps launched directly, each launch
+    # bracketed by CUDA events on the launching stream
+    moe.profile_enable(True)
+    eager_ms = timed(step, args.steps)
     moe.profile_enable(False)
     prof = moe.profile_read()
     clocks = sampler.stop()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = sum(step_ms) / len(step_ms)
     if world > 1:
         tt = torch.tensor([ms], device=dev_name)
@@ -343,7 +365,9 @@ def run_ours(args, w: synth.Workload):
                    "step_tflops": work["flops"] / (ms * 1e-3) / 1e12,
                    "step_gbs": work["bytes"] / (ms * 1e-3) / 1e9,
                    "step_roofline_frac": t_star / (ms * 1e-3), "step_bound": step_bound,
-                   "wall_s_timed_region": wall},
+                   "wall_s_timed_region": wall,
+                   "timing": "eager launches" if graph is None else "CUDA graph replay of one captured step",
+                   "eager_ms_per_step": sum(eager_ms) / len(eager_ms)},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": world * w.t / (e2e_ms * 1e-3), "unit": "tokens/s",
@@ -365,7 +389,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--flags", type=int, default=0)
+    ap.add_argument("--flags", type=int, default=16, help="moe_experts_fwd flags (16: packed weights)")
+    ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of graph replays")
     ap.add_argument("--oracle-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -123,11 +123,27 @@ const char* moe_status_string(int status);
  *
  * x      bf16 [t][h]        wr   bf16 [E][h]      rbias  fp32 [E] or NULL
  * idx    int32 [t][k] out   w    fp32 [t][k] out  logits fp32 [t][E] out or NULL
- * Uses no workspace.  Errors: MOE_EINVAL, MOE_ESHAPE, MOE_ECUDA.
+ *
+ * Two implementations, with bit-identical idx and w:
+ *   - ws given and logits NULL: tensor-core scores (bf16 MMA, fp32
+ *     accumulate) bound every logit to within a proven margin of its
+ *     fixed-order value; only the experts that can still reach the top k
+ *     are recomputed in the fixed order.  Needs ws of at least
+ *     moe_workspace_bytes(dims, 0) bytes (dims.inter and dims.shared_inter
+ *     do not change the router's share).  The status block of ws records
+ *     the largest observed |score - logit| / margin (float bits at byte
+ *     offset 8) and the count of recomputed logits (uint32 at offset 12);
+ *     a score outside its margin raises MOE_EDEVICE in
+ *     moe_read_device_status (then idx may differ from the fixed order).
+ *   - ws NULL or logits requested: one pass that evaluates every logit in
+ *     the fixed order (slower; its tile of 8 rows of x, 64 x 256 router
+ *     weights and 8 x E logits must fit in 227 KB of shared memory, which
+ *     holds for h <= 8192 at E <= 1024; MOE_ESHAPE beyond).
+ * Errors: MOE_EINVAL, MOE_ESHAPE, MOE_EWORKSPACE, MOE_ECUDA.
  */
 int moe_route_topk(const uint16_t* x, const uint16_t* wr, const float* rbias,
                    const moe_dims* dims, int32_t* idx, float* w, float* logits,
-                   void* stream);
+                   void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Grouping (prefill/experts.rs, prepare_expert_jobs): the t*k (row, slot)

@@ -17,13 +17,17 @@ enum : uint32_t {
   FLAG_BAD_EXPERT = 1u << 0,  // an expert id outside [0, E)
   FLAG_BAD_ROW = 1u << 1,     // a CSR row index outside [0, t)
   FLAG_BAD_OFFSETS = 1u << 2, // CSR offsets not monotone / out of range
+  FLAG_ROUTE_BOUND = 1u << 3, // a router score left its error bound
   FLAG_TIMEOUT = 1u << 8,     // a bounded device wait gave up
 };
 
 struct DeviceStatus {
   uint32_t flags;
   uint32_t timeout_site;  // which wait gave up (kernel-specific code)
-  uint32_t pad[62];
+  uint32_t route_audit;   // router: largest |score - logit| / bound seen (fp32 bits)
+  uint32_t route_cands;   // router: logits recomputed exactly
+  uint32_t route_done;    // router, small t: CTAs finished (the last one resets it)
+  uint32_t pad[59];
 };
 
 __device__ __forceinline__ void raise_flag(DeviceStatus* st, uint32_t f) {
@@ -81,6 +85,7 @@ struct WsLayout {
   size_t csr_rank;      // int32 [t*k]
   size_t csr_counts;    // int32 [nchunks][E]
   size_t csr_base;      // int32 [nchunks][E]
+  size_t route;         // router scores and norms (tensor-core router)
   size_t acc;           // float [t][h]
   size_t hg;            // bf16 [t*k][inter]
   size_t hgs;           // bf16 [t][shared_inter]

@@ -745,6 +745,11 @@ int num_sms() {
 
 }  // namespace
 
+cudaError_t tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t width, uint64_t height,
+                    uint64_t stride_bytes, uint32_t bw, uint32_t bh, CUtensorMapSwizzle sw) {
+  return make_map(m, base, dt, width, height, stride_bytes, bw, bh, sw);
+}
+
 cudaError_t launch_schedule(const TcParams& p, SchedHdr* hdr, int4* tiles, int* units_gu, int max_tiles,
                             int tile_max, cudaStream_t stream) {
   MOE_LAUNCH("schedule", stream,

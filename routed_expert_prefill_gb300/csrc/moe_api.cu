@@ -11,6 +11,9 @@ namespace moe {
 cudaError_t launch_route_topk(const uint16_t* x, const uint16_t* wr, const float* rbias, int t, int h,
                               int E, int k, int32_t* idx, float* w, float* logits, cudaStream_t stream);
 size_t route_smem_bytes(int h, int E);
+size_t route_ws_bytes(int t, int h, int E);
+cudaError_t launch_route_tc(const uint16_t* x, const uint16_t* wr, const float* rbias, int t, int h, int E, int k,
+                            int32_t* idx, float* w, unsigned char* scratch, DeviceStatus* st, cudaStream_t stream);
 cudaError_t launch_build_csr(const int32_t* idx, const float* w, int t, int k, int E, const moe_csr& csr,
                              unsigned char* ws, const WsLayout& L, cudaStream_t stream);
 cudaError_t launch_experts_fast(const ExpertsArgs& a, uint32_t flags, cudaStream_t stream);
@@ -46,6 +49,7 @@ WsLayout ws_layout(const moe_dims& d, uint32_t flags) {
   L.csr_rank = take(n * 4);
   L.csr_counts = take(nchunks * d.E * 4);
   L.csr_base = take(nchunks * d.E * 4);
+  L.route = take(route_ws_bytes(d.t, d.h, d.E));
   L.acc = take((size_t)d.t * d.h * 4);
   const size_t kmax = d.inter > d.shared_inter ? d.inter : d.shared_inter;
   size_t hg_bytes = n * d.inter * 2;
@@ -135,7 +139,7 @@ size_t moe_workspace_bytes(const moe_dims* dims, uint32_t flags) {
 }
 
 int moe_route_topk(const uint16_t* x, const uint16_t* wr, const float* rbias, const moe_dims* dims,
-                   int32_t* idx, float* w, float* logits, void* stream) {
+                   int32_t* idx, float* w, float* logits, void* ws, size_t ws_bytes, void* stream) {
   TRY(check_dims(dims));
   TRY(check_ptr(x, "x", 16));
   TRY(check_ptr(wr, "wr", 16));
@@ -143,6 +147,14 @@ int moe_route_topk(const uint16_t* x, const uint16_t* wr, const float* rbias, co
   TRY(check_ptr(idx, "idx", 4));
   TRY(check_ptr(w, "w", 4));
   TRY(check_ptr(logits, "logits", 4, true));
+  if (ws && !logits) {
+    TRY(check_ws(dims, 0, ws, ws_bytes));
+    const WsLayout L = ws_layout(*dims, 0);
+    unsigned char* wsb = (unsigned char*)ws;
+    return cuda_status(launch_route_tc(x, wr, rbias, dims->t, dims->h, dims->E, dims->k, idx, w, wsb + L.route,
+                                       (DeviceStatus*)(wsb + L.status), (cudaStream_t)stream),
+                       "moe_route_topk launch");
+  }
   if (route_smem_bytes(dims->h, dims->E) > 227 * 1024)
     return set_error(MOE_ESHAPE, "router tile for h=%d, E=%d exceeds shared memory", dims->h, dims->E);
   return cuda_status(launch_route_topk(x, wr, rbias, dims->t, dims->h, dims->E, dims->k, idx, w, logits,
@@ -282,11 +294,12 @@ int moe_read_device_status(void* ws, void* stream) {
   TRY(cuda_status(cudaStreamSynchronize(s), "status clear sync"));
   if (st.flags & FLAG_TIMEOUT)
     return set_error(MOE_ETIMEOUT, "a bounded device wait gave up (site %u)", st.timeout_site);
-  if (st.flags & (FLAG_BAD_EXPERT | FLAG_BAD_ROW | FLAG_BAD_OFFSETS))
-    return set_error(MOE_EDEVICE, "device-side check failed (flags 0x%x: %s%s%s)", st.flags,
+  if (st.flags & (FLAG_BAD_EXPERT | FLAG_BAD_ROW | FLAG_BAD_OFFSETS | FLAG_ROUTE_BOUND))
+    return set_error(MOE_EDEVICE, "device-side check failed (flags 0x%x: %s%s%s%s)", st.flags,
                      (st.flags & FLAG_BAD_EXPERT) ? "expert id out of range " : "",
                      (st.flags & FLAG_BAD_ROW) ? "row out of range " : "",
-                     (st.flags & FLAG_BAD_OFFSETS) ? "bad offsets" : "");
+                     (st.flags & FLAG_BAD_OFFSETS) ? "bad offsets " : "",
+                     (st.flags & FLAG_ROUTE_BOUND) ? "router score outside its error bound" : "");
   return MOE_OK;
 }
 

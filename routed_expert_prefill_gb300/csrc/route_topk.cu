@@ -10,7 +10,7 @@
 // specifies, so logits are reproducible bit for bit.  x rows stay in shared
 // memory; router weight chunks [64 experts][256 K] are double-buffered with
 // cp.async.  After all passes, warp w selects the top-k of row w.
-#include "common.cuh"
+#include "route_common.cuh"
 
 namespace moe {
 
@@ -31,16 +31,6 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
-
-// Total order on floats as unsigned keys (larger float -> larger key).
-__device__ __forceinline__ uint32_t float_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float key_float(uint32_t k) {
-  uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
-  return __uint_as_float(u);
-}
 
 __global__ void __launch_bounds__(RT_THREADS, 1)
 route_topk_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr,
@@ -160,41 +150,9 @@ route_topk_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w
 #pragma unroll
   for (int q = 0; q < 32; ++q) {
     int e = lane + 32 * q;
-    key[q] = (e < E) ? ((uint64_t)float_key(lr[e]) << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)e) : 0ull;
+    key[q] = (e < E) ? topk_key(lr[e], e) : 0ull;
   }
-  float sel_l[16];
-  int sel_e[16];
-  for (int j = 0; j < k; ++j) {
-    uint64_t best = 0;
-#pragma unroll
-    for (int q = 0; q < 32; ++q) best = key[q] > best ? key[q] : best;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-      best = other > best ? other : best;
-    }
-    const int e = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
-    sel_e[j] = e;
-    sel_l[j] = key_float((uint32_t)(best >> 32));
-    if ((e & 31) == lane) {
-#pragma unroll
-      for (int q = 0; q < 32; ++q)
-        if (q == (e >> 5)) key[q] = 0ull;
-    }
-  }
-  if (lane == 0) {
-    float p[16];
-    float sum = 0.f;
-    for (int j = 0; j < k; ++j) {
-      p[j] = expf(sel_l[j] - sel_l[0]);
-      sum += p[j];
-    }
-    const size_t base = (size_t)(row0 + r) * k;
-    for (int j = 0; j < k; ++j) {
-      idx[base + j] = sel_e[j];
-      wout[base + j] = p[j] / sum;
-    }
-  }
+  warp_topk_softmax<32>(key, k, lane, idx + (size_t)(row0 + r) * k, wout + (size_t)(row0 + r) * k);
 }
 
 }  // namespace

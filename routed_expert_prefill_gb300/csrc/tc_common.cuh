@@ -1,5 +1,7 @@
 // Types shared by the tensor-core expert kernels (internal).
 #pragma once
+#include <cuda.h>
+
 #include "experts.cuh"
 
 namespace moe {
@@ -39,6 +41,10 @@ struct TcParams {
 // expert: all t rows), largest first, with gate/up units and padded offsets.
 cudaError_t launch_schedule(const TcParams& p, SchedHdr* hdr, int4* tiles, int* units_gu, int max_tiles,
                             int tile_max, cudaStream_t stream);
+// 2D tiled tensor map over a row-major matrix: width (elements) x height
+// (rows), row pitch in bytes, box {bw, bh}.
+cudaError_t tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t width, uint64_t height,
+                    uint64_t stride_bytes, uint32_t bw, uint32_t bh, CUtensorMapSwizzle sw);
 // Per-row shared-expert gate sigmoid(x_r . g) into out[t].
 cudaError_t launch_shared_gate(const uint16_t* x, const uint16_t* g, int t, int h, float* out, cudaStream_t stream);
 

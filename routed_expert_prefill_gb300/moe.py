@@ -94,7 +94,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_status_string.restype = ctypes.c_char_p
     lib.moe_status_string.argtypes = [ctypes.c_int]
     lib.moe_route_topk.restype = ctypes.c_int
-    lib.moe_route_topk.argtypes = [vp, vp, vp, ctypes.POINTER(MoeDims), vp, vp, vp, vp]
+    lib.moe_route_topk.argtypes = [vp, vp, vp, ctypes.POINTER(MoeDims), vp, vp, vp, vp, sz, vp]
     lib.moe_build_csr.restype = ctypes.c_int
     lib.moe_build_csr.argtypes = [vp, vp, ctypes.POINTER(MoeDims), ctypes.POINTER(MoeCsr), vp, sz, vp]
     lib.moe_experts_fwd.restype = ctypes.c_int
@@ -171,8 +171,14 @@ def _u16(t: torch.Tensor) -> torch.Tensor:
 
 
 def moe_route_topk(x: torch.Tensor, wr: torch.Tensor, k: int, rbias: torch.Tensor | None = None,
-                   want_logits: bool = False, out=None, stream=None):
-    """Router: x bf16 [t, h], wr bf16 [E, h] -> idx int32 [t, k], w fp32 [t, k] (, logits)."""
+                   want_logits: bool = False, out=None, ws: torch.Tensor | None = None, exact_pass: bool = False,
+                   stream=None):
+    """Router: x bf16 [t, h], wr bf16 [E, h] -> idx int32 [t, k], w fp32 [t, k] (, logits).
+
+    Takes the tensor-core scoring path with exact refinement unless logits
+    are wanted or ``exact_pass`` asks for the single fixed-order pass; both
+    give the same idx and w.
+    """
     lib = load_library()
     t, h = x.shape
     E = wr.shape[0]
@@ -183,8 +189,12 @@ def moe_route_topk(x: torch.Tensor, wr: torch.Tensor, k: int, rbias: torch.Tenso
     else:
         idx, w = out
     logits = torch.empty((t, E), dtype=torch.float32, device=x.device) if want_logits else None
+    use_ws = not (want_logits or exact_pass)
+    if use_ws and ws is None:
+        ws = new_workspace(dims, 0, x.device, stream)
+    wsp, wsn = (_ptr(ws), ws.numel()) if use_ws else (None, 0)
     _check(lib.moe_route_topk(_ptr(_u16(x)), _ptr(_u16(wr)), _ptr(rbias), ctypes.byref(dims), _ptr(idx),
-                              _ptr(w), _ptr(logits), _stream(stream)))
+                              _ptr(w), _ptr(logits), wsp, wsn, _stream(stream)))
     return (idx, w, logits) if want_logits else (idx, w)
 
 
@@ -327,7 +337,8 @@ def moe_forward(dev: dict, dims: MoeDims, flags: int = 0, ws: torch.Tensor | Non
     if ws is None:
         ws = new_workspace(dims, flags, dev["x"].device, stream)
     b = bufs or {}
-    idx, w = moe_route_topk(dev["x"], dev["wr"], dims.k, dev.get("rbias"), out=b.get("route"), stream=stream)
+    idx, w = moe_route_topk(dev["x"], dev["wr"], dims.k, dev.get("rbias"), out=b.get("route"), ws=ws,
+                            stream=stream)
     csr = moe_build_csr(idx, w, dims.E, ws=ws, out=b.get("csr"), stream=stream)
     shared = None
     if flags & MOE_PACKED_WEIGHTS:

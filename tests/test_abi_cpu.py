@@ -58,7 +58,7 @@ def test_bad_dims_rejected(lib, field, val, status):
     d = moe.dims_of(16, 256, 128, 8, 2, 128)
     setattr(d, field, val)
     fake = ctypes.c_void_p(0x10000)
-    rc = lib.moe_route_topk(fake, fake, None, ctypes.byref(d), fake, fake, None, None)
+    rc = lib.moe_route_topk(fake, fake, None, ctypes.byref(d), fake, fake, None, None, 0, None)
     assert rc == status
     assert lib.moe_last_error().decode()
 
@@ -68,10 +68,20 @@ def test_null_and_misaligned_pointers(lib):
 
     d = moe.dims_of(16, 256, 128, 8, 2, 128)
     ok = ctypes.c_void_p(0x10000)
-    assert lib.moe_route_topk(None, ok, None, ctypes.byref(d), ok, ok, None, None) == -1
-    assert lib.moe_route_topk(ctypes.c_void_p(0x10008), ok, None, ctypes.byref(d), ok, ok, None, None) == -1
+    assert lib.moe_route_topk(None, ok, None, ctypes.byref(d), ok, ok, None, None, 0, None) == -1
+    assert lib.moe_route_topk(ctypes.c_void_p(0x10008), ok, None, ctypes.byref(d), ok, ok, None, None, 0, None) == -1
     assert b"aligned" in lib.moe_last_error()
-    assert lib.moe_route_topk(ok, ok, None, None, ok, ok, None, None) == -1
+    assert lib.moe_route_topk(ok, ok, None, None, ok, ok, None, None, 0, None) == -1
+
+
+def test_router_workspace_too_small(lib):
+    from routed_expert_prefill_gb300 import moe
+
+    d = moe.dims_of(16, 256, 128, 8, 2, 128)
+    ok = ctypes.c_void_p(0x10000)
+    need = lib.moe_workspace_bytes(ctypes.byref(d), 0)
+    assert lib.moe_route_topk(ok, ok, None, ctypes.byref(d), ok, ok, None, ok, need - 1, None) == -3
+    assert b"workspace" in lib.moe_last_error()
 
 
 def test_workspace_too_small_and_flags(lib):

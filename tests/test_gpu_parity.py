@@ -107,6 +107,82 @@ def test_router_bitexact(moe, name):
     assert np.abs(wt.cpu().numpy() - ref["w"]).max() <= 2e-6
 
 
+SMALL_T_ROUTER = 16  # up to this many rows the router evaluates every logit in the fixed order
+
+
+def _route_tc(moe, dev, w, t=None, h=None):
+    """Tensor-core router through its workspace; returns idx, w, audit ratio, recomputed count."""
+    ws = moe.new_workspace(moe.dims_of(t or w.t, h or w.h, 128, w.E, w.k, 0))
+    idx, wt = moe.moe_route_topk(dev["x"], dev["wr"], w.k, dev["rbias"], ws=ws)
+    torch.cuda.synchronize()
+    raw = ws[:16].cpu().numpy()
+    audit = float(raw[8:12].view(np.float32)[0])
+    cands = int(raw[12:16].view(np.uint32)[0])
+    assert moe.read_device_status(ws) == 0
+    return idx, wt, audit, cands
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_tc_router_matches_oracle(moe, name):
+    w = synth.WORKLOADS[name]
+    inp = _inputs(w)
+    ref = _oracle_rows(w, inp, None)
+    dev = moe.upload_inputs(inp)
+    idx, wt, audit, cands = _route_tc(moe, dev, w)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref["idx"])
+    assert np.abs(wt.cpu().numpy() - ref["w"]).max() <= 2e-6
+    assert audit <= 0.25, f"score error used {audit:.3g} of its bound"
+    if w.t > SMALL_T_ROUTER:
+        assert w.t * w.k <= cands <= w.t * w.E
+    else:  # every logit evaluated in the fixed order; nothing to refine
+        assert cands == 0
+
+
+@pytest.mark.parametrize("name", ["t4096_h2048_e128_skewed", "t4096_h4096_e256", "t512_h2048_e128"])
+def test_tc_router_equals_exact_pass(moe, name):
+    """Full size: both router implementations agree bit for bit on every row."""
+    w = synth.WORKLOADS[name]
+    dev = moe.upload_inputs(_inputs(w))
+    idx, wt, audit, cands = _route_tc(moe, dev, w)
+    idx0, wt0 = moe.moe_route_topk(dev["x"], dev["wr"], w.k, dev["rbias"], exact_pass=True)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(idx.cpu().numpy(), idx0.cpu().numpy())
+    np.testing.assert_array_equal(wt.cpu().numpy().view(np.uint32), wt0.cpu().numpy().view(np.uint32))
+    assert audit <= 0.25
+    assert cands <= 3 * w.t * w.k, f"{cands / w.t:.1f} logits recomputed per row"
+
+
+@pytest.mark.parametrize("t,h,E,k", [(1, 128, 8, 2), (3, 384, 20, 3), (16, 640, 1000, 16), (17, 256, 40, 8),
+                                     (37, 256, 100, 5), (300, 128, 1000, 16), (129, 640, 33, 4)])
+def test_tc_router_odd_shapes(moe, t, h, E, k):
+    w = synth.Workload("odd", t, h, 128, E, k, 0, 40 + t)
+    inp = synth.make_inputs(w)
+    dev = moe.upload_inputs(inp)
+    idx, wt, audit, _ = _route_tc(moe, dev, w)
+    lg = O.route_logits(inp["x"], inp["wr"], inp.get("rbias"))
+    ref_idx, ref_w = O.route_topk(lg, k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    assert np.abs(wt.cpu().numpy() - ref_w).max() <= 2e-6
+    assert audit <= 0.25
+
+
+@pytest.mark.parametrize("t", [12, 40])
+def test_tc_router_all_ties(moe, t):
+    """Zero rows: every logit equals its bias; equal biases tie and the lower ids win."""
+    w = synth.Workload("ties", t, 256, 128, 64, 6, 0, 7)
+    inp = synth.make_inputs(w)
+    inp["x"][::2] = 0
+    inp["rbias"] = np.zeros(64, np.float32)
+    inp["rbias"][[5, 9, 40]] = 1e-3
+    dev = moe.upload_inputs(inp)
+    idx, wt, _, _ = _route_tc(moe, dev, w)
+    lg = O.route_logits(inp["x"], inp["wr"], inp["rbias"])
+    ref_idx, ref_w = O.route_topk(lg, w.k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    assert idx.cpu().numpy()[0].tolist() == [5, 9, 40, 0, 1, 2]
+    assert np.abs(wt.cpu().numpy() - ref_w).max() <= 2e-6
+
+
 @pytest.mark.parametrize("name", SMALL)
 @pytest.mark.parametrize("flags", [0, 1])
 def test_pipeline_parity(moe, name, flags):
