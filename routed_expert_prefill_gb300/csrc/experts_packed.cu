@@ -162,9 +162,14 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   mbar_wait(bar, parity, &never, 100000000ull);
 }
 
-// silu(g) * u with the fast exponential and division (relative error a few
-// ulp, far inside the block-output tolerance).
-__device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.f + __expf(-g)) * u; }
+// silu(g) * u = g * u * sigmoid(g), sigmoid(g) = (1 + tanh(g / 2)) / 2, with
+// the hardware tanh approximation (one special-function op per element;
+// absolute error of the sigmoid about 2^-12, below the bf16 rounding of hg).
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  float th;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(0.5f * g));
+  return g * u * fmaf(0.5f, th, 0.5f);
+}
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -274,7 +279,9 @@ __device__ __forceinline__ PUnit decode_punit(const TcParams& p, int u) {
   U.pad = T.w;
   U.shared = (T.x == p.E);
   U.nkc = GATEUP ? p.h / KC : (U.shared ? p.Is : p.I) / KC;
-  U.kps = min(B_STAGE / (U.Nm * 128), U.nkc);
+  // K chunks per B stage: a whole number of A stages, so that every A stage
+  // reads a single B stage
+  U.kps = min(B_STAGE / (U.Nm * 128), U.nkc) / CPS * CPS;
   return U;
 }
 
@@ -456,15 +463,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
           for (int c = 0; c < CPS; ++c) {
             const int kc = st * CPS + c;
             const int sb = bit % SB;
-            if (sub == 0) {
-              if (!mbar_wait(&S.b_full[sb], (bit / SB) & 1, abort, WAIT_NS)) {
-                note_timeout(p.status, abort, GATEUP ? 34 : 44);
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              bd = bstage[sb];
-            }
+            if (sub == 0) bd = bstage[sb];  // b_full was observed by the dequant warps before a_full
 #pragma unroll
             for (int m = 0; m < C::NMAT; ++m) {
 #pragma unroll
@@ -479,7 +478,6 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
               sub = 0;
             }
           }
-          if (!ok) break;
           mma_commit(&S.a_empty[sa]);
         }
         if (!ok) break;
@@ -496,7 +494,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     const int q = warp & 3;               // TMEM lane quarter this warp may access
     const int o = q * 32 + lane;          // weight row (= TMEM lane)
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-    uint32_t ast = 0;
+    uint32_t ast = 0, bbase = 0;  // global A stage; global B stage at the unit's start
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
       const PUnit U = decode_punit<GATEUP>(p, u);
       bool ok = true;
@@ -524,6 +522,17 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         }
         tmem_st_wait();
         tc_fence_before();
+        // The MMA issuer waits on a_full only: the B stage this A stage
+        // multiplies must have landed before a_full completes.
+        const uint32_t bst = bbase + (uint32_t)(st * CPS / U.kps);
+        bool b_ok = true;
+        if (lane == 0) b_ok = mbar_wait(&S.b_full[bst % SB], (bst / SB) & 1, abort, WAIT_NS);
+        b_ok = __shfl_sync(0xFFFFFFFFu, b_ok, 0);
+        if (!b_ok) {
+          if (lane == 0) note_timeout(p.status, abort, GATEUP ? 34 : 44);
+          ok = false;
+          break;
+        }
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&S.a_full[sa]);
@@ -531,6 +540,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         }
       }
       if (!ok) break;
+      bbase += (uint32_t)((U.nkc + U.kps - 1) / U.kps);
     }
   } else {
     // ------------------------------------------------------------ epilogue warpgroup
@@ -582,41 +592,28 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
       tc_fence_after();
       const uint32_t acc = lane_base + ab * C::ACC_COLS;
       if (GATEUP) {
-        // drain TMEM into registers (silu(gate) * up as bf16 pairs), release
-        // the accumulator, then store the hg image
-        uint32_t res[8][8];
+        // silu(gate) * up, 16 columns at a time, stored straight into the hg
+        // image (no unit-sized register buffer, so the 16 independent silu
+        // evaluations of a step overlap); the accumulator is released once
+        // the last store has been issued
+        uint8_t* img = reinterpret_cast<uint8_t*>(p.hg + (size_t)U.pad * P.kmax) + (size_t)(feat / 64) * U.Nm * 128;
+        const int c8 = (feat % 64) / 8, e8 = feat % 8;
+        for (int c = 0; c * 16 < U.Nm; ++c) {
+          uint32_t g[16], v[16];
+          tmem_ld16(acc + c * 16, g);
+          tmem_ld16(acc + 128 + c * 16, v);
+          tmem_ld_wait();
+          float hv[16];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          if (c * 16 < U.Nm) {
-            uint32_t g[16], v[16];
-            tmem_ld16(acc + c * 16, g);
-            tmem_ld16(acc + 128 + c * 16, v);
-            tmem_ld_wait();
+          for (int j = 0; j < 16; ++j)
+            hv[j] = c * 16 + j < U.n ? silu_mul(__uint_as_float(g[j]), __uint_as_float(v[j])) : 0.f;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float h0 = c * 16 + 2 * j < U.n ? silu_mul(__uint_as_float(g[2 * j]), __uint_as_float(v[2 * j])) : 0.f;
-              const float h1 =
-                  c * 16 + 2 * j + 1 < U.n ? silu_mul(__uint_as_float(g[2 * j + 1]), __uint_as_float(v[2 * j + 1])) : 0.f;
-              res[c][j] = pack_bf16x2(h0, h1);
-            }
-          }
+          for (int j = 0; j < 16; ++j)
+            *reinterpret_cast<__nv_bfloat16*>(img + sw128_off(c * 16 + j, c8) + e8 * 2) = __float2bfloat16_rn(hv[j]);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
-        uint8_t* img = reinterpret_cast<uint8_t*>(p.hg + (size_t)U.pad * P.kmax) + (size_t)(feat / 64) * U.Nm * 128;
-        const int c8 = (feat % 64) / 8, e8 = feat % 8;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          if (c * 16 < U.Nm) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const uint32_t pr = res[c][j >> 1];
-              *reinterpret_cast<uint16_t*>(img + sw128_off(c * 16 + j, c8) + e8 * 2) =
-                  (uint16_t)((j & 1) ? (pr >> 16) : (pr & 0xFFFFu));
-            }
-          }
-        }
       } else {
         float* dcol = (to_list ? p.ybuf : p.acc) + feat;
         for (int c = 0; c * 16 < U.Nm; ++c) {

@@ -36,19 +36,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is still pending
+// is suspended (issuing nothing) until the phase completes or about
+// `hint_ns` have passed, so waiting warps leave the issue slots to the
+// warps doing work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase of `parity` to complete.  Gives up (returns
-// false) after `limit_ns` of global time or as soon as *abort is set.
+// false) after `limit_ns` of global time or as soon as *abort is set (checked
+// between suspended tries of at most 0.2 ms).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
                                           uint64_t limit_ns) {
   // `abort` may point at a local zero when the caller must not be interrupted.
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 31u) == 0) {
-      if (*abort) return false;
-      if (globaltimer() - t0 > limit_ns) return false;
-    }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > limit_ns) return false;
   }
 }
 
