@@ -77,6 +77,16 @@ __device__ __forceinline__ void dequant8(uint32_t word, __nv_bfloat162 s2, __nv_
   }
 }
 
+// silu(g) * u = g * u * sigmoid(g), sigmoid(g) = (1 + tanh(g / 2)) / 2, with
+// the hardware tanh approximation (one special-function op per element;
+// absolute error of the sigmoid about 2^-12, below the bf16 rounding of the
+// hidden activations it produces).
+__device__ __forceinline__ float silu_mul_fast(float g, float u) {
+  float th;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(0.5f * g));
+  return g * u * fmaf(0.5f, th, 0.5f);
+}
+
 // ---------------------------------------------------------------------------
 // Workspace layout (host side computes it; kernels receive raw pointers)
 // ---------------------------------------------------------------------------
@@ -92,6 +102,7 @@ struct WsLayout {
   size_t ybuf;          // float [t*k][h] (deterministic only)
   size_t xg;            // bf16 gathered token images (packed-weight path only)
   size_t sched;         // scheduler state (counters, tile lists)
+  size_t gvpart;        // small-t gate/up partial sums (t <= 16 only)
   size_t total;
 };
 

@@ -25,9 +25,20 @@ struct ExpertsArgs {
   uint16_t* hgs;           // bf16 [t][Is]
   float* ybuf;             // fp32 [t*k][h] (deterministic only)
   unsigned char* sched;    // scheduler scratch
+  float* gvpart;           // small-t gate/up partial sums [4][t*k + t][2][max(I, Is)] (t <= 16)
   DeviceStatus* status;
   uint16_t* out;           // bf16 [t][h]
 };
+
+// Packed record layout (moe_pack_experts): 128-row x 64-K blocks of 4-bit
+// codes (4096 bytes) + 128 bf16 scales + 128 bf16 biases; per record the
+// gate/up part ([128-row tile][K chunk][gate block][up block]) then the down
+// part ([128-row tile of h][K chunk of inter][block]).
+constexpr int PACK_QB = 4096 + 256 + 256;
+__host__ __device__ inline size_t packed_gu_bytes(int h, int I) { return (size_t)(I / 128) * (h / 64) * 2 * PACK_QB; }
+__host__ __device__ inline size_t packed_rec_bytes(int h, int I) {
+  return packed_gu_bytes(h, I) + (size_t)(h / 128) * (I / 64) * PACK_QB;
+}
 
 cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t stream);
 cudaError_t launch_finalize(const ExpertsArgs& a, bool deterministic, cudaStream_t stream);

@@ -162,14 +162,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   mbar_wait(bar, parity, &never, 100000000ull);
 }
 
-// silu(g) * u = g * u * sigmoid(g), sigmoid(g) = (1 + tanh(g / 2)) / 2, with
-// the hardware tanh approximation (one special-function op per element;
-// absolute error of the sigmoid about 2^-12, below the bf16 rounding of hg).
-__device__ __forceinline__ float silu_mul(float g, float u) {
-  float th;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(0.5f * g));
-  return g * u * fmaf(0.5f, th, 0.5f);
-}
+__device__ __forceinline__ float silu_mul(float g, float u) { return silu_mul_fast(g, u); }
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(

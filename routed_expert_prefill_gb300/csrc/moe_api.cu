@@ -24,6 +24,18 @@ cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, const uint
                         int nrec, uint8_t* dst, cudaStream_t stream);
 cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, const uint8_t* s_packed,
                                   uint16_t* xg, bool deterministic, cudaStream_t stream);
+cudaError_t launch_experts_gemv(const ExpertsArgs& a, bool packed, bool deterministic, cudaStream_t stream);
+size_t gemv_part_bytes(const moe_dims& d);
+
+// Chunks of at most SMALL_T_MAX rows whose (expert, 128-row tile) units are
+// too few to occupy the GPU (t * k * inter / 128 below SMALL_T_UNITS, about
+// one per SM of a GB300) take the weight-streaming small-t kernels, unless
+// MOE_FORCE_LARGE_T.  With more units the tensor-core kernels are faster:
+// their only per-weight work is the dequantisation, where the CUDA-core dot
+// products of the streaming kernels cost several more instructions per
+// weight and row.
+constexpr int SMALL_T_MAX = 16;
+constexpr int SMALL_T_UNITS = 152;
 
 static thread_local char g_err[512] = "";
 
@@ -62,6 +74,7 @@ WsLayout ws_layout(const moe_dims& d, uint32_t flags) {
   L.ybuf = (flags & MOE_DETERMINISTIC) ? take(n * d.h * 4) : off;
   L.xg = (flags & MOE_PACKED_WEIGHTS) ? take(packed_pad_rows(d) * d.h * 2) : off;
   L.sched = take(experts_sched_bytes(d));
+  L.gvpart = take(gemv_part_bytes(d));
   L.total = off;
   return L;
 }
@@ -242,10 +255,17 @@ int moe_experts_fwd(const uint16_t* x, const moe_csr* csr, const moe_qweights* e
   a.hgs = (uint16_t*)(wsb + L.hgs);
   a.ybuf = (flags & MOE_DETERMINISTIC) ? (float*)(wsb + L.ybuf) : nullptr;
   a.sched = wsb + L.sched;
+  a.gvpart = gemv_part_bytes(*dims) ? (float*)(wsb + L.gvpart) : nullptr;
   a.status = (DeviceStatus*)(wsb + L.status);
   a.out = out;
 
   cudaStream_t s = (cudaStream_t)stream;
+  const bool small_t =
+      !(flags & (MOE_FORCE_LARGE_T | MOE_SIMPLE_KERNELS)) &&
+      ((flags & MOE_FORCE_SMALL_T) ||
+       (dims->t <= SMALL_T_MAX && (long)dims->t * dims->k * (dims->inter / 128) < SMALL_T_UNITS));
+  if (small_t)
+    return cuda_status(launch_experts_gemv(a, packed, (flags & MOE_DETERMINISTIC) != 0, s), "moe_experts_fwd launch");
   if (packed)
     return cuda_status(launch_experts_packed(a, experts->codes, dims->shared_inter > 0 ? shared->codes : nullptr,
                                              (uint16_t*)(wsb + L.xg), (flags & MOE_DETERMINISTIC) != 0, s),

@@ -210,6 +210,59 @@ def test_packed_pipeline_parity(moe, name, det):
     _check_out(res["out"], ref["out"])
 
 
+@pytest.mark.parametrize("name", ["decode_t2_h2048_e128", "decode_t8_h2048_e128", "tiny_t16_h256_e8"])
+@pytest.mark.parametrize("flags", [0x2, 0x3, 0x12, 0x13])
+def test_small_t_kernels_forced(moe, name, flags):
+    """The weight-streaming kernels on decode-shaped chunks the dispatch would give the tensor cores."""
+    w = synth.WORKLOADS[name]
+    inp = _inputs(w)
+    ref = _oracle_rows(w, inp, None)
+    res, status = _run(moe, w, inp, flags)
+    assert status == 0
+    _check_out(res["out"], ref["out"])
+
+
+@pytest.mark.parametrize("flags", [0x2, 0x3, 0x12, 0x13])
+def test_small_t_kernels_forced_on_prefill_chunk(moe, flags):
+    """The weight-streaming kernels on a 512-row chunk (rows batched 16 at a time per expert)."""
+    w = synth.WORKLOADS["t512_h2048_e128"]
+    inp = _inputs(w)
+    ref = _oracle_rows(w, inp, None)
+    res, status = _run(moe, w, inp, flags)
+    assert status == 0
+    _check_out(res["out"], ref["out"])
+
+
+@pytest.mark.parametrize("name", ["decode_t1_h2048_e128", "decode_t8_h2048_e128", "tiny_t16_h256_e8"])
+@pytest.mark.parametrize("flags", [0x4, 0x5, 0x14, 0x15])
+def test_large_t_kernels_forced_on_decode(moe, name, flags):
+    """The tensor-core kernels on decode-shaped chunks (tiles of 1-16 rows)."""
+    w = synth.WORKLOADS[name]
+    inp = _inputs(w)
+    ref = _oracle_rows(w, inp, None)
+    res, status = _run(moe, w, inp, flags)
+    assert status == 0
+    _check_out(res["out"], ref["out"])
+
+
+def test_small_t_deterministic_bitwise(moe):
+    """Deterministic small-t runs repeat bit for bit in each weight layout; the layouts agree within bf16 rounding."""
+    w = synth.WORKLOADS["decode_t8_h2048_e128"]
+    inp = _inputs(w)
+    dev = moe.upload_inputs(inp)
+    outs = {}
+    for flags in (0x3, 0x13):
+        runs = []
+        for _ in range(2):
+            res, status = _run(moe, w, inp, flags, dev)
+            assert status == 0
+            runs.append(res["out"].view(torch.int16).cpu().numpy())
+        np.testing.assert_array_equal(runs[0], runs[1])
+        outs[flags] = res["out"].float().cpu().numpy()
+    a, b = outs[0x3], outs[0x13]
+    assert np.abs(a - b).max() <= 1e-2 * np.abs(a).max()
+
+
 def test_packed_matches_rowmajor_path(moe):
     """Both tensor-core paths agree (deterministic mode) to within bf16 rounding."""
     w = synth.WORKLOADS["t512_h2048_e128"]
