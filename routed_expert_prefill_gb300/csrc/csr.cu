@@ -13,6 +13,9 @@
 //   2. csr_scan (one block): per expert, the exclusive prefix of the chunk
 //      counts; then the exclusive prefix over experts gives offsets.
 //   3. csr_scatter: position = offsets[e] + chunk prefix + rank.
+// Up to CSR_SMALL_CHUNKS chunks (decode-shaped chunks) run as one
+// block that walks the chunks in order with running per-expert counts, scans
+// them and scatters: one launch instead of three, the same positions.
 #include "common.cuh"
 
 namespace moe {
@@ -113,6 +116,115 @@ __global__ void csr_scatter_kernel(const int32_t* __restrict__ idx, const float*
   slot_of[p] = pos;
 }
 
+
+constexpr int CSR_SMALL_CHUNKS = 2;
+
+// Exclusive scan over v[0..1023] held one per thread (1024 threads); returns
+// this thread's exclusive prefix and, in *total, the sum.
+__device__ __forceinline__ int block_excl_scan_1024(int v, int* warp_sums, int* total) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int s = warp_sums[lane];
+    int si = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xFFFFFFFFu, si, o);
+      if (lane >= o) si += y;
+    }
+    warp_sums[lane] = si - s;
+    if (lane == 31) warp_sums[32] = si;
+  }
+  __syncthreads();
+  *total = warp_sums[32];
+  return warp_sums[warp] + incl - v;
+}
+
+__global__ void __launch_bounds__(CSR_CHUNK, 1)
+csr_small_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w, int n, int k, int E,
+                 int32_t* __restrict__ offsets, int32_t* __restrict__ rows, float* __restrict__ weights,
+                 int32_t* __restrict__ slot_of, DeviceStatus* st) {
+  extern __shared__ uint32_t sm[];
+  constexpr int W = CSR_CHUNK / 32;
+  uint32_t* bm = sm;                                      // [E][W] chunk bitmap
+  int* run = reinterpret_cast<int*>(sm + E * W);          // [E] pairs seen per expert
+  uint16_t* pre = reinterpret_cast<uint16_t*>(run + E);   // [E][W] bits of the expert in earlier words
+  __shared__ int warp_sums[33];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nch = (n + CSR_CHUNK - 1) / CSR_CHUNK;
+  for (int i = tid; i < E; i += CSR_CHUNK) run[i] = 0;
+  int ee[CSR_SMALL_CHUNKS], pe[CSR_SMALL_CHUNKS];
+#pragma unroll
+  for (int c = 0; c < CSR_SMALL_CHUNKS; ++c) {
+    ee[c] = -1;
+    pe[c] = 0;
+    if (c < nch) {
+      for (int i = tid; i < E * W; i += CSR_CHUNK) bm[i] = 0u;
+      __syncthreads();
+      const int p = c * CSR_CHUNK + tid;
+      int e = -1;
+      if (p < n) {
+        e = idx[p];
+        if (e < 0 || e >= E) {
+          raise_flag(st, FLAG_BAD_EXPERT);
+          e = -1;
+        } else {
+          atomicOr(&bm[e * W + (tid >> 5)], 1u << (tid & 31));
+        }
+      }
+      __syncthreads();
+      // per expert (one warp each): exclusive prefix of its bit counts over the W words
+      for (int ex = warp; ex < E; ex += CSR_CHUNK / 32) {
+        const int cnt = __popc(bm[ex * W + lane]);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        pre[ex * W + lane] = (uint16_t)(incl - cnt);
+      }
+      __syncthreads();
+      if (e >= 0) pe[c] = run[e] + pre[e * W + warp] + __popc(bm[e * W + warp] & ((1u << lane) - 1u));
+      ee[c] = e;
+      __syncthreads();
+      for (int ex = tid; ex < E; ex += CSR_CHUNK) run[ex] += pre[ex * W + W - 1] + __popc(bm[ex * W + W - 1]);
+      __syncthreads();
+    }
+  }
+  // offsets: exclusive prefix of the per-expert totals (E <= 1024 = one per thread)
+  int total;
+  const int excl = block_excl_scan_1024(tid < E ? run[tid] : 0, warp_sums, &total);
+  __syncthreads();
+  if (tid < E) {
+    offsets[tid] = excl;
+    run[tid] = excl;  // reused as the expert's list start
+  }
+  if (tid == 0) offsets[E] = total;
+  __syncthreads();
+#pragma unroll
+  for (int c = 0; c < CSR_SMALL_CHUNKS; ++c) {
+    const int p = c * CSR_CHUNK + tid;
+    if (c < nch && p < n) {
+      if (ee[c] < 0) {
+        slot_of[p] = -1;
+      } else {
+        const int pos = run[ee[c]] + pe[c];
+        rows[pos] = p / k;
+        weights[pos] = w[p];
+        slot_of[p] = pos;
+      }
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_build_csr(const int32_t* idx, const float* w, int t, int k, int E,
@@ -124,6 +236,16 @@ cudaError_t launch_build_csr(const int32_t* idx, const float* w, int t, int k, i
   int32_t* counts = reinterpret_cast<int32_t*>(ws + L.csr_counts);
   int32_t* base = reinterpret_cast<int32_t*>(ws + L.csr_base);
   DeviceStatus* st = reinterpret_cast<DeviceStatus*>(ws + L.status);
+  if (nchunks <= CSR_SMALL_CHUNKS) {
+    const size_t smem = (size_t)E * (CSR_CHUNK / 32) * 6 + (size_t)E * 4;
+    cudaError_t err =
+        cudaFuncSetAttribute(csr_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    MOE_LAUNCH("csr_small", stream,
+               csr_small_kernel<<<1, CSR_CHUNK, smem, stream>>>(idx, w, n, k, E, csr.offsets, csr.rows, csr.weights,
+                                                                csr.slot_of, st));
+    return cudaGetLastError();
+  }
   const size_t smem = (size_t)E * (CSR_CHUNK / 32) * 4;
   cudaError_t err = cudaFuncSetAttribute(csr_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
