@@ -20,6 +20,7 @@ for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
 import argparse
+import hashlib
 import json
 import statistics
 import subprocess
@@ -80,6 +81,49 @@ def step_work(w: synth.Workload, counts: np.ndarray) -> dict:
     }
     return dict(touched=touched, pairs=n, max_rows=int(counts.max()), flops=flops,
                 bytes=wbytes + io, by_kernel=by_kernel)
+
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
+# the packed expert kernels, from one ncu capture of
+# `python bench.py --steps 5 --warmup 3 --no-cpu-baseline` on a GB300; valid
+# while the kernel sources hash to `src` (reported as null otherwise).
+PACKED_SOURCES = ("experts_packed.cu", "tc_ptx.cuh", "tc_common.cuh", "common.cuh", "experts.cuh")
+MEASURED_TRAFFIC = {
+    ("t512_h2048_e128", "gateup", 16): dict(bytes=263.68e6, src="9cb0fc594058ef5c"),
+    ("t512_h2048_e128", "down", 16): dict(bytes=130.08e6, src="9cb0fc594058ef5c"),
+}
+
+
+def packed_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in PACKED_SOURCES:
+        with open(os.path.join(ROOT, "routed_expert_prefill_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str, family: str, flags: int):
+    m = MEASURED_TRAFFIC.get((workload, family, flags))
+    if m is None or m["src"] != packed_source_hash():
+        return None
+    return m["bytes"]
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest x over all ranks of the process group (x itself when alone)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    tt = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_tokens_per_s(world: int, rows_per_rank: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank processes its own chunk of rows_per_rank rows."""
+    return world * rows_per_rank / (max_ms * 1e-3)
 
 
 def kernel_family(name: str) -> str:
@@ -275,11 +319,7 @@ def run_ours(args, w: synth.Workload):
     moe.profile_enable(False)
     prof = moe.profile_read()
     clocks = sampler.stop()
-    ms = sum(step_ms) / len(step_ms)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev_name)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), dev_name)
     gpu_launches = sum(v[0] for v in prof.values())
 
     # ---- end to end through the public API with host buffers
@@ -302,11 +342,7 @@ def run_ours(args, w: synth.Workload):
         out_host.copy_(out, non_blocking=True)
         e_ends[i].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_starts, e_ends)) / args.steps
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev_name)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(e_starts, e_ends)) / args.steps, dev_name)
 
     if rank != 0:
         if world > 1:
@@ -340,8 +376,10 @@ def run_ours(args, w: synth.Workload):
             ach = kf / (per_launch_ms * 1e-3) / 1e12
             roofline = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                         "frac": ach / peaks["bf16_tflops"], "traffic": None}
+        roofline["traffic"] = measured_traffic(w.name, dom, flags)
         roofline.update({"kernel": dom, "peak_source": peak_src,
-                         "kernel_ms_per_launch": per_launch_ms})
+                         "kernel_ms_per_launch": per_launch_ms,
+                         "algorithmic_bytes_per_launch": kb, "algorithmic_flops_per_launch": kf})
     t_star = max(work["flops"] / (peaks["bf16_tflops"] * 1e12), work["bytes"] / (peaks["hbm_gbs"] * 1e9))
     step_bound = "tensor" if work["flops"] / (peaks["bf16_tflops"] * 1e12) > work["bytes"] / (peaks["hbm_gbs"] * 1e9) else "hbm"
 
@@ -352,7 +390,7 @@ def run_ours(args, w: synth.Workload):
         cpu = {"value": rows / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"first {rows} of {w.t} rows, one full oracle pass (router, CSR, experts), 1 thread"}
 
-    value = world * w.t / (ms * 1e-3)
+    value = job_tokens_per_s(world, w.t, ms)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -370,7 +408,7 @@ def run_ours(args, w: synth.Workload):
                    "eager_ms_per_step": sum(eager_ms) / len(eager_ms)},
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": {"value": world * w.t / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_tokens_per_s(world, w.t, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x_host.numel() * 2), "d2h_bytes_per_step": int(out_host.numel() * 2)},
         "gpu_launches": gpu_launches,
         "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in prof.items()},
