@@ -8,7 +8,8 @@
 //     experts, with the K range split into KS slices whose partial sums are
 //     stored side by side (no atomics).  While the MMAs run, the four
 //     epilogue warps compute the squared norms |w_e|^2 of the router rows.
-//   route_refine: one warp per row.  The score a_e (slices summed, bias
+//   route_refine: one warp per row, or two for short chunks (they split the
+//     recomputations, so that a few hundred rows still fill the GPU).  The score a_e (slices summed, bias
 //     added) differs from the canonical fp32 logit c_e by at most
 //       D_e = eps * |x| * |w_e| + 2^-21 |a_e|,
 //     because sum_i |x_i w_ei| <= |x| |w_e| (Cauchy-Schwarz) and eps covers
@@ -39,7 +40,8 @@ constexpr int RS_KC = 64;    // K per stage: one 128-byte swizzled row
 constexpr int RS_A_BYTES = 128 * 128;
 constexpr uint64_t RS_WAIT_NS = 2000000000ull;
 constexpr int RS_TARGET_CTAS = 152;  // about one CTA per SM of a GB300
-constexpr int RF_WARPS = 8;
+constexpr int RS_KS_MAX = 4;         // K slices: each costs the refinement one more load per score
+constexpr int RF_WARPS = 8;  // 4 rows per CTA, two warps each
 constexpr int RF_NB = 4;  // exact logits computed together per warp
 
 struct ScoreParams {
@@ -256,15 +258,16 @@ __device__ __forceinline__ void canonical_dots(const uint16_t* xr, const uint16_
     for (int j = 0; j < NB; ++j) P[j] = P[j] + __shfl_xor_sync(0xFFFFFFFFu, P[j], o);
 }
 
-template <int NQ>
+template <int NQ, int WPR>  // WPR warps per row (1 or 2)
 __global__ void __launch_bounds__(RF_WARPS * 32, 4)
 route_refine_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr, const float* __restrict__ rbias,
                     const float* __restrict__ part, int KS, int Ep, const float* __restrict__ wn2, int t, int h,
                     int E, int k, float eps, int32_t* __restrict__ idx, float* __restrict__ wout,
                     DeviceStatus* st) {
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * RF_WARPS + (threadIdx.x >> 5);
-  if (row >= t) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int pair = warp / WPR, half = warp % WPR;  // the warps of a row
+  const int row = blockIdx.x * (RF_WARPS / WPR) + pair;
+  if (row >= t) return;  // the warps of a row leave together
   const int nm = (h + 255) / 256;
   const uint16_t* xr = x + (size_t)row * h;
 
@@ -283,7 +286,7 @@ route_refine_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__
   // slice sums (any order: the bound allows for it), all loads of a slice in flight together
 #pragma unroll
   for (int q = 0; q < NQ; ++q) av[q] = 0.f;
-#pragma unroll 2
+#pragma unroll 4
   for (int s = 0; s < KS; ++s) {
     const float* ps = part + ((size_t)s * t + row) * Ep + lane;
 #pragma unroll
@@ -329,22 +332,28 @@ route_refine_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__
   }
 
   // Candidate list of this row, then exact logits in batches of RF_NB.
-  __shared__ int cand_s[RF_WARPS][NQ * 32];
-  int* cl = cand_s[threadIdx.x >> 5];
+  // per pair: the second warp's keys [NQ * 32] and the candidate list [NQ * 32]
+  extern __shared__ __align__(16) unsigned char rf_smem[];
+  uint64_t* key_s = reinterpret_cast<uint64_t*>(rf_smem) + (size_t)pair * NQ * 32;
+  int* cl = reinterpret_cast<int*>(reinterpret_cast<uint64_t*>(rf_smem) + (size_t)(RF_WARPS / WPR) * NQ * 32) +
+            (size_t)pair * NQ * 32;
+  __shared__ float audit_s[RF_WARPS];
   int ncand = 0;
 #pragma unroll
   for (int q = 0; q < NQ; ++q) {
     const bool cand = (lane + 32 * q < E) && (!finite || av[q] + dv[q] >= L);
     const uint32_t mask = __ballot_sync(0xFFFFFFFFu, cand);
-    if (cand) cl[ncand + __popc(mask & ((1u << lane) - 1u))] = lane + 32 * q;
+    if (cand && half == 0) cl[ncand + __popc(mask & ((1u << lane) - 1u))] = lane + 32 * q;
     ncand += __popc(mask);
   }
-  __syncwarp();
+  if (WPR == 2) asm volatile("bar.sync %0, 64;" ::"r"(1 + pair) : "memory");  // the list is complete for both warps
+  else __syncwarp();
   uint64_t key[NQ];
 #pragma unroll
   for (int q = 0; q < NQ; ++q) key[q] = 0ull;
   float audit = 0.f;
-  for (int b = 0; b < ncand; b += RF_NB) {
+  // the pair's warps take alternate batches of RF_NB candidates
+  for (int b = half * RF_NB; b < ncand; b += WPR * RF_NB) {
     int e[RF_NB];
     const uint16_t* wrow[RF_NB];
 #pragma unroll
@@ -369,6 +378,19 @@ route_refine_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) audit = fmaxf(audit, __shfl_xor_sync(0xFFFFFFFFu, audit, o));
+  if (WPR == 2) {
+    // merge the second warp's keys (each expert's key is set by exactly one warp)
+    if (half == 1) {
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) key_s[q * 32 + lane] = key[q];
+      if (lane == 0) audit_s[pair] = audit;
+    }
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + pair) : "memory");
+    if (half == 1) return;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) key[q] |= key_s[q * 32 + lane];
+    audit = fmaxf(audit, audit_s[pair]);
+  }
   if (lane == 0) {
     if (audit > 0.f) atomicMax(&st->route_audit, __float_as_uint(audit));
     atomicAdd(&st->route_cands, (uint32_t)ncand);
@@ -470,6 +492,7 @@ RoutePlan route_plan(int t, int h, int E) {
   R.nk = h / RS_KC;
   int ks = RS_TARGET_CTAS / (R.mt * R.ntn);
   ks = ks < R.nk / 2 ? ks : R.nk / 2;
+  ks = ks < RS_KS_MAX ? ks : RS_KS_MAX;
   if (ks < 1) ks = 1;
   R.nkc_split = (R.nk + ks - 1) / ks;
   R.KS = (R.nk + R.nkc_split - 1) / R.nkc_split;
@@ -478,14 +501,32 @@ RoutePlan route_plan(int t, int h, int E) {
 
 size_t score_smem_bytes(int NT) { return 1024 + (size_t)RS_STAGES * (RS_A_BYTES + NT * 128); }
 
+template <int NQ, int WPR>
+cudaError_t launch_refine_w(const uint16_t* x, const uint16_t* wr, const float* rbias, const float* part,
+                            const RoutePlan& R, const float* wn2, int t, int h, int E, int k, float eps, int32_t* idx,
+                            float* w, DeviceStatus* st, cudaStream_t stream) {
+  const size_t smem = (size_t)(RF_WARPS / WPR) * NQ * 32 * 12;
+  static bool attr_set = false;  // one flag per instantiation
+  if (!attr_set) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(route_refine_kernel<NQ, WPR>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int rows_per_cta = RF_WARPS / WPR;
+  MOE_LAUNCH("route_refine", stream,
+             (route_refine_kernel<NQ, WPR><<<(t + rows_per_cta - 1) / rows_per_cta, RF_WARPS * 32, smem, stream>>>(
+                 x, wr, rbias, part, R.KS, R.Ep, wn2, t, h, E, k, eps, idx, w, st)));
+  return cudaGetLastError();
+}
+
+// Two warps per row while one warp per row would leave most SMs idle.
 template <int NQ>
 cudaError_t launch_refine(const uint16_t* x, const uint16_t* wr, const float* rbias, const float* part,
                           const RoutePlan& R, const float* wn2, int t, int h, int E, int k, float eps, int32_t* idx,
                           float* w, DeviceStatus* st, cudaStream_t stream) {
-  MOE_LAUNCH("route_refine", stream,
-             route_refine_kernel<NQ><<<(t + RF_WARPS - 1) / RF_WARPS, RF_WARPS * 32, 0, stream>>>(
-                 x, wr, rbias, part, R.KS, R.Ep, wn2, t, h, E, k, eps, idx, w, st));
-  return cudaGetLastError();
+  if (t <= 1024) return launch_refine_w<NQ, 2>(x, wr, rbias, part, R, wn2, t, h, E, k, eps, idx, w, st, stream);
+  return launch_refine_w<NQ, 1>(x, wr, rbias, part, R, wn2, t, h, E, k, eps, idx, w, st, stream);
 }
 
 template <int TR, int NQ>
