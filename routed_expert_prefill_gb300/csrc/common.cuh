@@ -27,7 +27,8 @@ struct DeviceStatus {
   uint32_t route_audit;   // router: largest |score - logit| / bound seen (fp32 bits)
   uint32_t route_cands;   // router: logits recomputed exactly
   uint32_t route_done;    // router, small t: CTAs finished (the last one resets it)
-  uint32_t pad[59];
+  uint32_t gv_done;       // small-t down kernel: CTAs finished (the last one finalises and resets it)
+  uint32_t pad[58];
 };
 
 __device__ __forceinline__ void raise_flag(DeviceStatus* st, uint32_t f) {

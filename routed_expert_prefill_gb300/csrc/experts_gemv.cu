@@ -73,6 +73,8 @@ struct GvParams {
   float* acc;              // fp32 [t][h]
   float* ybuf;             // fp32 [t*k][h] (deterministic)
   DeviceStatus* status;
+  const int32_t* slot_of;  // [t*k] list position of each (row, slot), -1 if dropped
+  uint16_t* out;           // bf16 [t][h]
 };
 
 // Where one thread finds its 16 weights of each K chunk of one weight row:
@@ -588,8 +590,65 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_gateup(Gv2Params Q) {
   }
 }
 
+// After the last down CTA: out = bf16(acc), or, deterministic mode,
+// bf16(acc + sum over the row's list positions in ascending order of
+// weight * y) -- the finalize pass, run by the last CTA to finish.
+__device__ void gv2_finalize_if_last(const GvParams& P) {
+  __shared__ int s_last;
+  __shared__ int pos[GV_RB][16];
+  __shared__ int npos[GV_RB];
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(&P.status->gv_done, 1u) == gridDim.x * gridDim.y - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int r0 = 0; r0 < P.t; r0 += GV_RB) {
+    const int nr = min(GV_RB, P.t - r0);
+    if (P.deterministic && (int)threadIdx.x < nr) {
+      const int r = r0 + threadIdx.x;
+      int m = 0;
+      for (int j = 0; j < P.k; ++j) {
+        const int p = P.slot_of[(size_t)r * P.k + j];
+        if (p < 0) continue;
+        int i = m++;
+        while (i > 0 && pos[threadIdx.x][i - 1] > p) {
+          pos[threadIdx.x][i] = pos[threadIdx.x][i - 1];
+          --i;
+        }
+        pos[threadIdx.x][i] = p;
+      }
+      npos[threadIdx.x] = m;
+    }
+    __syncthreads();
+    for (int v = threadIdx.x; v < nr * P.h / 4; v += blockDim.x) {
+      const int rr = v / (P.h / 4), f4 = v % (P.h / 4);
+      const int r = r0 + rr;
+      float4 a = __ldcg(reinterpret_cast<const float4*>(P.acc + (size_t)r * P.h) + f4);
+      if (P.deterministic) {
+        for (int j = 0; j < npos[rr]; ++j) {
+          const int p = pos[rr][j];
+          const float w = P.weights[p];
+          const float4 y = __ldcg(reinterpret_cast<const float4*>(P.ybuf + (size_t)p * P.h) + f4);
+          a.x = fmaf(w, y.x, a.x);
+          a.y = fmaf(w, y.y, a.y);
+          a.z = fmaf(w, y.z, a.z);
+          a.w = fmaf(w, y.w, a.w);
+        }
+      }
+      uint2 o;
+      o.x = pack_bf16x2(a.x, a.y);
+      o.y = pack_bf16x2(a.z, a.w);
+      reinterpret_cast<uint2*>(P.out + (size_t)r * P.h)[f4] = o;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) P.status->gv_done = 0;
+}
+
 // down: unit = (expert, 128-row tile of h).  hg of the unit's rows is
-// formed first from the gate/up slices.
+// formed first from the gate/up slices.  Every CTA, with or without a
+// unit, counts itself done; the last one finalises the block output.
 template <int NB>
 __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_down(Gv2Params Q) {
   const GvParams& P = Q.p;
@@ -603,103 +662,105 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_down(Gv2Params Q) {
   const int units_per_e = P.h / 128;
   int e, rt;
   bool shared;
-  if (!gv2_unit<NB>(P, units_per_e, &s_e, R, e, rt, shared)) return;
-  const int nb = R.n, nkc = Iu / GV_KC;
-  uint16_t* hs = reinterpret_cast<uint16_t*>(ring + GV2_RING);  // [NB][Iu] bf16
-  float* xch = reinterpret_cast<float*>(hs + NB * Iu);
-  const size_t pstride = (size_t)(P.t * P.k + P.t) * 2 * Q.kmax;
-  for (int v = threadIdx.x; v < nb * Iu; v += GV2_THREADS) {
-    const int r = v / Iu, c = v % Iu;
-    const float* pp = Q.part + (size_t)R.pos[r] * 2 * Q.kmax + c;
-    float gs = 0.f, us = 0.f;
-    for (int s = 0; s < Q.KS; ++s) {
-      gs += pp[s * pstride];
-      us += pp[s * pstride + Q.kmax];
+  if (gv2_unit<NB>(P, units_per_e, &s_e, R, e, rt, shared)) {
+    const int nb = R.n, nkc = Iu / GV_KC;
+    uint16_t* hs = reinterpret_cast<uint16_t*>(ring + GV2_RING);  // [NB][Iu] bf16
+    float* xch = reinterpret_cast<float*>(hs + NB * Iu);
+    const size_t pstride = (size_t)(P.t * P.k + P.t) * 2 * Q.kmax;
+    for (int v = threadIdx.x; v < nb * Iu; v += GV2_THREADS) {
+      const int r = v / Iu, c = v % Iu;
+      const float* pp = Q.part + (size_t)R.pos[r] * 2 * Q.kmax + c;
+      float gs = 0.f, us = 0.f;
+      for (int s = 0; s < Q.KS; ++s) {
+        gs += pp[s * pstride];
+        us += pp[s * pstride + Q.kmax];
+      }
+      hs[r * Iu + c] = R.row[r] < 0 ? 0 : f2bf(silu_mul_fast(gs, us));
     }
-    hs[r * Iu + c] = R.row[r] < 0 ? 0 : f2bf(silu_mul_fast(gs, us));
-  }
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < ST; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], GV2_CONS / 32);
+    if (threadIdx.x == 0) {
+      for (int i = 0; i < ST; ++i) {
+        mbar_init(&full[i], 1);
+        mbar_init(&empty[i], GV2_CONS / 32);
+      }
+      abort_flag = 0;
+      fence_mbar_init();
     }
-    abort_flag = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  volatile int* abort = &abort_flag;
-  const uint8_t* rec = shared ? P.s_codes : P.codes + (size_t)e * packed_rec_bytes(P.h, P.I);
-  const uint8_t* src = rec + packed_gu_bytes(P.h, Iu) + (size_t)rt * nkc * GV_QB;  // [rt][kc][block]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float y[NB];
+    __syncthreads();
+    volatile int* abort = &abort_flag;
+    const uint8_t* rec = shared ? P.s_codes : P.codes + (size_t)e * packed_rec_bytes(P.h, P.I);
+    const uint8_t* src = rec + packed_gu_bytes(P.h, Iu) + (size_t)rt * nkc * GV_QB;  // [rt][kc][block]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float y[NB];
 #pragma unroll
-  for (int r = 0; r < NB; ++r) y[r] = 0.f;
-  const int o = threadIdx.x & 127, hf = (threadIdx.x >> 7) & 1;
-  if (warp == GV2_CONS / 32) {
-    if (lane == 0) {
-      bool armed[ST];
-      uint32_t par[ST];
+    for (int r = 0; r < NB; ++r) y[r] = 0.f;
+    const int o = threadIdx.x & 127, hf = (threadIdx.x >> 7) & 1;
+    if (warp == GV2_CONS / 32) {
+      if (lane == 0) {
+        bool armed[ST];
+        uint32_t par[ST];
 #pragma unroll
-      for (int i = 0; i < ST; ++i) armed[i] = false, par[i] = 0;
+        for (int i = 0; i < ST; ++i) armed[i] = false, par[i] = 0;
+        for (int i = 0; i < nkc; ++i) {
+          const int s = i % ST;
+          if (!mbar_wait(&empty[s], ((i / ST) & 1) ^ 1, abort, GV2_WAIT_NS)) {
+            gv2_timeout(P.status, abort, 63);
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], GV_QB);
+          bulk_copy_g2s(ring + s * GV_QB, src + (size_t)i * GV_QB, GV_QB, &full[s]);
+          armed[s] = true;
+          par[s] = (i / ST) & 1;
+        }
+        if (*abort)
+          for (int i = 0; i < ST; ++i)
+            if (armed[i]) {
+              const int never = 0;
+              mbar_wait(&full[i], par[i], &never, 100000000ull);
+            }
+      }
+    } else {
       for (int i = 0; i < nkc; ++i) {
         const int s = i % ST;
-        if (!mbar_wait(&empty[s], ((i / ST) & 1) ^ 1, abort, GV2_WAIT_NS)) {
-          gv2_timeout(P.status, abort, 63);
+        // every lane waits (and so observes the copy); the verdict is made
+        // warp-uniform so that a lane giving up cannot leave the others
+        // behind at __syncwarp
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], (i / ST) & 1, abort, GV2_WAIT_NS))) {
+          if (lane == 0) gv2_timeout(P.status, abort, 64);
           break;
         }
-        mbar_arrive_expect_tx(&full[s], GV_QB);
-        bulk_copy_g2s(ring + s * GV_QB, src + (size_t)i * GV_QB, GV_QB, &full[s]);
-        armed[s] = true;
-        par[s] = (i / ST) & 1;
+        uint32_t wd[16];
+        dequant_half(ring + s * GV_QB, o, hf, wd);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        const uint16_t* hk = hs + i * GV_KC + hf * 32;
+#pragma unroll
+        for (int r = 0; r < NB; ++r)
+          if (r < nb) fma32(wd, hk + r * Iu, y[r]);
       }
-      if (*abort)
-        for (int i = 0; i < ST; ++i)
-          if (armed[i]) {
-            const int never = 0;
-            mbar_wait(&full[i], par[i], &never, 100000000ull);
+      if (hf == 1)
+#pragma unroll
+        for (int r = 0; r < NB; ++r)
+          if (r < nb) xch[o * NB + r] = y[r];
+    }
+    __syncthreads();
+    if (threadIdx.x < 128 && !*abort) {
+      const int f = rt * 128 + o;
+#pragma unroll
+      for (int r = 0; r < NB; ++r)
+        if (r < nb) {
+          const float v = y[r] + xch[o * NB + r];
+          const int row = R.row[r];
+          if (P.deterministic && !shared) {
+            P.ybuf[(size_t)R.pos[r] * P.h + f] = v;
+          } else if (row >= 0) {
+            float* d = P.acc + (size_t)row * P.h + f;
+            if (P.deterministic) *d = R.w[r] * v;
+            else atomicAdd(d, R.w[r] * v);
           }
-    }
-  } else {
-    for (int i = 0; i < nkc; ++i) {
-      const int s = i % ST;
-      // every lane waits (and so observes the copy); the verdict is made
-      // warp-uniform so that a lane giving up cannot leave the others
-      // behind at __syncwarp
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], (i / ST) & 1, abort, GV2_WAIT_NS))) {
-        if (lane == 0) gv2_timeout(P.status, abort, 64);
-        break;
-      }
-      uint32_t wd[16];
-      dequant_half(ring + s * GV_QB, o, hf, wd);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-      const uint16_t* hk = hs + i * GV_KC + hf * 32;
-#pragma unroll
-      for (int r = 0; r < NB; ++r)
-        if (r < nb) fma32(wd, hk + r * Iu, y[r]);
-    }
-    if (hf == 1)
-#pragma unroll
-      for (int r = 0; r < NB; ++r)
-        if (r < nb) xch[o * NB + r] = y[r];
-  }
-  __syncthreads();
-  if (threadIdx.x < 128 && !*abort) {
-    const int f = rt * 128 + o;
-#pragma unroll
-    for (int r = 0; r < NB; ++r)
-      if (r < nb) {
-        const float v = y[r] + xch[o * NB + r];
-        const int row = R.row[r];
-        if (P.deterministic && !shared) {
-          P.ybuf[(size_t)R.pos[r] * P.h + f] = v;
-        } else if (row >= 0) {
-          float* d = P.acc + (size_t)row * P.h + f;
-          if (P.deterministic) *d = R.w[r] * v;
-          else atomicAdd(d, R.w[r] * v);
         }
-      }
+    }
   }
+  gv2_finalize_if_last(P);
 }
 
 template <int NB>
@@ -776,6 +837,8 @@ cudaError_t launch_experts_gemv(const ExpertsArgs& a, bool packed, bool determin
   P.acc = a.acc;
   P.ybuf = a.ybuf;
   P.status = a.status;
+  P.slot_of = a.slot_of;
+  P.out = a.out;
   cudaError_t err;
   if (a.Is > 0 && a.s_gate) {
     float* gate_vals = reinterpret_cast<float*>(a.sched);
@@ -802,8 +865,7 @@ cudaError_t launch_experts_gemv(const ExpertsArgs& a, bool packed, bool determin
       else if (NBr == 4) err = launch_gv2<4>(Q, nact, stream);
       else if (NBr == 8) err = launch_gv2<8>(Q, nact, stream);
       else err = launch_gv2<16>(Q, nact, stream);
-      if (err != cudaSuccess) return err;
-      return launch_finalize(a, deterministic, stream);
+      return err;  // gv2_down's last CTA has written out
     }
   }
   if (rows <= 1) err = launch_gemv<1>(P, x_gu, g_gu, nact * g_dn, g_dn, stream);

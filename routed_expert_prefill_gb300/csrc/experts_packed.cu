@@ -494,9 +494,12 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
       for (int st = 0; st < U.nkc / CPS; ++st, ++ast) {
         if ((int)(ast & 1) != grp) continue;
         const int sc = ast % C::SC, sa = ast % C::SA;
-        if (!mbar_wait(&S.code_full[sc], (ast / C::SC) & 1, abort, WAIT_NS) ||
-            !mbar_wait(&S.a_empty[sa], ((ast / C::SA) & 1) ^ 1, abort, WAIT_NS)) {
-          note_timeout(p.status, abort, GATEUP ? 36 : 46);
+        // warp-uniform verdict: the TMEM stores below are .sync.aligned, so
+        // no lane may leave the loop alone when a wait gives up
+        const bool got = mbar_wait(&S.code_full[sc], (ast / C::SC) & 1, abort, WAIT_NS) &&
+                         mbar_wait(&S.a_empty[sa], ((ast / C::SA) & 1) ^ 1, abort, WAIT_NS);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+          if (lane == 0) note_timeout(p.status, abort, GATEUP ? 36 : 46);
           ok = false;
           break;
         }
@@ -578,8 +581,8 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         if (bad_row) raise_flag(p.status, FLAG_BAD_ROW);
         __syncwarp();
       }
-      if (!mbar_wait(&S.acc_full[ab], (uit / C::NACC) & 1, abort, WAIT_NS)) {
-        note_timeout(p.status, abort, GATEUP ? 37 : 47);
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.acc_full[ab], (uit / C::NACC) & 1, abort, WAIT_NS))) {
+        if (lane == 0) note_timeout(p.status, abort, GATEUP ? 37 : 47);
         break;
       }
       tc_fence_after();

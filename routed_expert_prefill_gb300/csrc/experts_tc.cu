@@ -571,9 +571,12 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
           const int sub = kc % C::CPS;
           const int sc = cit % C::SC;
           const int sa = ait % SA;
-          if ((sub == 0 && !mbar_wait(&S.code_full[sc], (cit / C::SC) & 1, abort, WAIT_NS)) ||
-              !mbar_wait(&S.a_empty[sa], ((ait / SA) & 1) ^ 1, abort, WAIT_NS)) {
-            note_timeout(p.status, abort, GATEUP ? 16 : 26);
+          // warp-uniform verdict (the warp's shared-memory A writes and the
+          // arrivals below assume all lanes continue together)
+          const bool got = (sub != 0 || mbar_wait(&S.code_full[sc], (cit / C::SC) & 1, abort, WAIT_NS)) &&
+                           mbar_wait(&S.a_empty[sa], ((ait / SA) & 1) ^ 1, abort, WAIT_NS);
+          if (!__all_sync(0xFFFFFFFFu, got)) {
+            if (lane == 0) note_timeout(p.status, abort, GATEUP ? 16 : 26);
             ok = false;
             break;
           }
@@ -631,8 +634,8 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
           }
         }
       }
-      if (!mbar_wait(&S.acc_full, uit & 1, abort, WAIT_NS)) {
-        note_timeout(p.status, abort, GATEUP ? 17 : 27);
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.acc_full, uit & 1, abort, WAIT_NS))) {
+        if (lane == 0) note_timeout(p.status, abort, GATEUP ? 17 : 27);
         break;
       }
       tc_fence_after();

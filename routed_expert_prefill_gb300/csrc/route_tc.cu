@@ -169,7 +169,8 @@ route_score_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant
       for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xFFFFFFFFu, s2, o);
       if (lane == 0) P.wn2[e0 + r] = s2;
     }
-    if (mbar_wait(&accf, 0, abort, RS_WAIT_NS)) {
+    // warp-uniform verdict: tcgen05.ld below is .sync.aligned
+    if (__all_sync(0xFFFFFFFFu, mbar_wait(&accf, 0, abort, RS_WAIT_NS))) {
       tc_fence_after();
       const int row = row0 + q * 32 + lane;
       float* dst = P.part + ((size_t)ks * P.t + row) * P.Ep + e0;
