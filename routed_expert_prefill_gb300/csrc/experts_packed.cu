@@ -24,8 +24,9 @@
 //   gateup:   warp 0 streams packed weight blocks (one bulk copy per two K
 //     chunks), warp 10 streams xg stages, two groups of four warps take
 //     alternate stages and dequantise one weight row per thread
-//     (w = fma(q, s, b) in bf16) straight into TMEM with tcgen05.st, warp 1
-//     issues tcgen05.mma with A in TMEM and B in shared memory, and a
+//     (w = fma(q, s, b) in bf16) straight into TMEM with tcgen05.st, warps 1
+//     and 15 issue the gate and the up tcgen05.mma streams with A in TMEM
+//     and B in shared memory, and a
 //     four-warp epilogue group drains the gate and up accumulators into
 //     registers (silu(gate) * up), frees TMEM for the next unit, and writes
 //     hg, again as swizzled K-major images.
@@ -45,28 +46,35 @@ namespace {
 
 using namespace tc;
 
-constexpr int PTILE = 128;  // rows per tile: MMA N <= 128
+// Rows per tile (MMA N): 128, or 64 for chunks whose experts see few rows
+// each -- the smaller accumulators then leave room for a deeper A ring.
+constexpr int PTILE = 128;
+constexpr int PTILE_SMALL = 64;
 constexpr int KC = 64;      // K per chunk = one quantisation group
 constexpr int QB = 4096 + 256 + 256;  // one packed 128 x 64 block
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
-constexpr int W_CODE = 0, W_MMA = 1, W_DQ0 = 2, W_B = 10, W_EPI0 = 11;
-constexpr int KWARPS = 15;            // 0 code, 1 MMA, 2-9 dequant (two groups), 10 B, 11-14 epilogue
+constexpr int W_CODE = 0, W_MMA = 1, W_DQ0 = 2, W_B = 10, W_EPI0 = 11, W_MMA2 = 15;
+// 0 code, 1 MMA (gate / down), 2-9 dequant (two groups), 10 B, 11-14 epilogue, 15 MMA (up)
+constexpr int KWARPS = 16;
 constexpr int KTHREADS = KWARPS * 32;
 constexpr int SB = 4;                 // B stages
 constexpr int B_STAGE = 32768;        // bytes: KPS chunks of Nm rows x 128 B
 constexpr int CPS = 2;                // K chunks per code stage and per A stage
-constexpr int A_COL = 256;            // TMEM columns 256..511 hold the A ring
 
-template <bool GATEUP>
+// TMEM (512 columns): NACC accumulator buffers of ACC_COLS columns (gate/up:
+// gate then up, PT columns each), then the A ring of SA stages.
+template <bool GATEUP, int PT>
 struct PCfg {
   static constexpr int NMAT = GATEUP ? 2 : 1;
-  static constexpr int C_STAGE = CPS * NMAT * QB;     // packed blocks of one stage
-  static constexpr int SC = GATEUP ? 4 : 8;           // code stages
-  static constexpr int A_STAGE = CPS * NMAT * 32;     // TMEM columns per A stage
-  static constexpr int SA = 256 / A_STAGE;            // A stages
-  static constexpr int NACC = GATEUP ? 1 : 2;         // accumulator buffers
-  static constexpr int ACC_COLS = GATEUP ? 256 : 128; // TMEM columns per accumulator buffer
+  static constexpr int C_STAGE = CPS * NMAT * QB;        // packed blocks of one stage
+  static constexpr int SC = GATEUP ? 4 : 8;              // code stages
+  static constexpr int A_STAGE = CPS * NMAT * 32;        // TMEM columns per A stage
+  static constexpr int NACC = GATEUP ? 1 : 2;            // accumulator buffers
+  static constexpr int ACC_COLS = GATEUP ? 2 * PT : PT;  // TMEM columns per accumulator buffer
+  static constexpr int A_COL = NACC * ACC_COLS;          // first column of the A ring
+  static constexpr int SA = (512 - A_COL) / A_STAGE;     // A stages: 2 / 4 at PT 128, 3 / 6 at PT 64
+  static constexpr int NISS = GATEUP ? 2 : 1;            // MMA issuing threads (gate and up apart)
 };
 
 __host__ __device__ inline size_t gu_bytes(int h, int I) { return (size_t)(I / 128) * (h / KC) * 2 * QB; }
@@ -286,35 +294,36 @@ struct PParams {
   int kmax;                 // max(I, Is): hg row pitch in the padded space
 };
 
-template <bool GATEUP>
+template <bool GATEUP, int PT>
 struct PSmem {
   // down epilogue: per epilogue warp, the destination row (-1: skip) and
   // weight of every column of the current tile
-  alignas(16) int col_row[4][PTILE];
-  alignas(16) float col_w[4][PTILE];
-  uint64_t code_full[PCfg<GATEUP>::SC], code_empty[PCfg<GATEUP>::SC];
-  uint64_t a_full[PCfg<GATEUP>::SA], a_empty[PCfg<GATEUP>::SA];
+  alignas(16) int col_row[4][PT];
+  alignas(16) float col_w[4][PT];
+  uint64_t code_full[PCfg<GATEUP, PT>::SC], code_empty[PCfg<GATEUP, PT>::SC];
+  uint64_t a_full[PCfg<GATEUP, PT>::SA], a_empty[PCfg<GATEUP, PT>::SA];
   uint64_t b_full[SB], b_empty[SB];
-  uint64_t acc_full[PCfg<GATEUP>::NACC], acc_empty[PCfg<GATEUP>::NACC];
-  uint64_t drain;
+  uint64_t acc_full[PCfg<GATEUP, PT>::NACC], acc_empty[PCfg<GATEUP, PT>::NACC];
+  uint64_t drain[2];
   uint32_t tmem_slot;
   int abort;
 };
 
-template <bool GATEUP>
+template <bool GATEUP, int PT>
 constexpr size_t psmem_bytes() {
-  return 1024 + (size_t)SB * B_STAGE + (size_t)PCfg<GATEUP>::SC * PCfg<GATEUP>::C_STAGE + sizeof(PSmem<GATEUP>);
+  return 1024 + (size_t)SB * B_STAGE + (size_t)PCfg<GATEUP, PT>::SC * PCfg<GATEUP, PT>::C_STAGE +
+         sizeof(PSmem<GATEUP, PT>);
 }
 
-template <bool GATEUP>
+template <bool GATEUP, int PT>
 __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
-  using C = PCfg<GATEUP>;
+  using C = PCfg<GATEUP, PT>;
   const TcParams& p = P.p;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* b_s = base;
   uint8_t* c_s = b_s + SB * B_STAGE;
-  PSmem<GATEUP>& S = *reinterpret_cast<PSmem<GATEUP>*>(c_s + C::SC * C::C_STAGE);
+  PSmem<GATEUP, PT>& S = *reinterpret_cast<PSmem<GATEUP, PT>*>(c_s + C::SC * C::C_STAGE);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = p.h;
 
@@ -331,17 +340,18 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     }
     for (int i = 0; i < C::SA; ++i) {
       mbar_init(&S.a_full[i], 4);
-      mbar_init(&S.a_empty[i], 1);
+      mbar_init(&S.a_empty[i], C::NISS);
     }
     for (int i = 0; i < SB; ++i) {
       mbar_init(&S.b_full[i], 1);
-      mbar_init(&S.b_empty[i], 1);
+      mbar_init(&S.b_empty[i], C::NISS);
     }
     for (int i = 0; i < C::NACC; ++i) {
-      mbar_init(&S.acc_full[i], 1);
+      mbar_init(&S.acc_full[i], C::NISS);
       mbar_init(&S.acc_empty[i], 4);
     }
-    mbar_init(&S.drain, 1);
+    mbar_init(&S.drain[0], 1);
+    mbar_init(&S.drain[1], 1);
     S.abort = 0;
     fence_mbar_init();
   }
@@ -419,12 +429,16 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         for (int i = 0; i < SB; ++i)
           if (armed[i]) drain_wait(&S.b_full[i], par[i]);
     }
-  } else if (warp == W_MMA) {
-    // ------------------------------------------------------------ MMA issuer (A in TMEM)
+  } else if (warp == W_MMA || warp == W_MMA2) {
+    // ------------------------------------------------------------ MMA issuers (A in TMEM)
     // The issue loop is kept lean (no division, descriptors stepped
-    // incrementally): a single thread feeds the tensor pipe, so every
-    // instruction between two MMAs delays the next one.
-    if (lane == 0) {
+    // incrementally): one thread feeds each issue stream, so every
+    // instruction between two MMAs delays the next one.  gate/up: warp W_MMA
+    // issues the gate MMAs and W_MMA2 the up MMAs -- separate accumulators,
+    // so the two streams are independent and each commit barrier counts
+    // both; down: W_MMA alone (one accumulator, one fixed order).
+    const int m = warp == W_MMA ? 0 : 1;
+    if (lane == 0 && (GATEUP || warp == W_MMA)) {
       uint64_t bstage[SB];
 #pragma unroll
       for (int i = 0; i < SB; ++i) bstage[i] = desc_sw128(smem_u32(b_s + i * B_STAGE));
@@ -451,19 +465,16 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
             break;
           }
           tc_fence_after();
-          const uint32_t a_st = tmem + A_COL + sa * C::A_STAGE;
+          const uint32_t a_st = tmem + C::A_COL + sa * C::A_STAGE;
 #pragma unroll
           for (int c = 0; c < CPS; ++c) {
             const int kc = st * CPS + c;
             const int sb = bit % SB;
             if (sub == 0) bd = bstage[sb];  // b_full was observed by the dequant warps before a_full
 #pragma unroll
-            for (int m = 0; m < C::NMAT; ++m) {
-#pragma unroll
-              for (int kk = 0; kk < KC / 16; ++kk)
-                mma_bf16_ta(acc + m * 128, a_st + (c * C::NMAT + m) * 32 + 8 * kk, bd + 2 * kk, idesc,
-                            (kc | kk) != 0);
-            }
+            for (int kk = 0; kk < KC / 16; ++kk)
+              mma_bf16_ta(acc + m * PT, a_st + (c * C::NMAT + m) * 32 + 8 * kk, bd + 2 * kk, idesc,
+                          (kc | kk) != 0);
             bd += nm8;
             if (++sub == U.kps || kc == U.nkc - 1) {
               mma_commit(&S.b_empty[sb]);
@@ -477,8 +488,8 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         mma_commit(&S.acc_full[ab]);
       }
       if (*abort) {
-        mma_commit(&S.drain);
-        drain_wait(&S.drain, 0);
+        mma_commit(&S.drain[m]);
+        drain_wait(&S.drain[m], 0);
       }
     }
   } else if (warp < W_B) {
@@ -514,7 +525,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
           const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
           uint32_t r[32];
           dequant_packed<8>(wd, __halves2bfloat162(sv, sv), __halves2bfloat162(bv, bv), r);
-          tmem_st<32>(lane_base + A_COL + sa * C::A_STAGE + cm * 32, r);
+          tmem_st<32>(lane_base + C::A_COL + sa * C::A_STAGE + cm * 32, r);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -538,7 +549,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
       if (!ok) break;
       bbase += (uint32_t)((U.nkc + U.kps - 1) / U.kps);
     }
-  } else {
+  } else if (warp < W_MMA2) {
     // ------------------------------------------------------------ epilogue warpgroup
     const int q = warp & 3;
     const int o = q * 32 + lane;
@@ -556,7 +567,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
       if (!GATEUP) {
         bool bad_row = false;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
+        for (int g = 0; g < PT / 32; ++g) {
           const int col = g * 32 + lane;
           int r = -1;
           float wv = 0.f;
@@ -597,7 +608,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         for (int c = 0; c * 16 < U.Nm; ++c) {
           uint32_t g[16], v[16];
           tmem_ld16(acc + c * 16, g);
-          tmem_ld16(acc + 128 + c * 16, v);
+          tmem_ld16(acc + PT + c * 16, v);
           tmem_ld_wait();
           float hv[16];
 #pragma unroll
@@ -649,7 +660,10 @@ int num_sms() {
 
 size_t packed_record_bytes(int h, int I) { return rec_bytes(h, I); }
 
-size_t packed_max_tiles(const moe_dims& d) { return (size_t)d.t * d.k / PTILE + d.E + d.t / PTILE + 2; }
+// Tile-list capacity, sized for the smaller tiles.
+size_t packed_max_tiles(const moe_dims& d) {
+  return (size_t)d.t * d.k / PTILE_SMALL + d.E + d.t / PTILE_SMALL + 2;
+}
 
 // Upper bound of the padded row space (rows rounded up to 16 per tile).
 size_t packed_pad_rows(const moe_dims& d) {
@@ -663,6 +677,27 @@ cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, const uint
   MOE_LAUNCH("pack", stream,
              pack_kernel<<<grid, 128, 0, stream>>>(codes, scales, biases, h, I, (size_t)3 * I * h / 2,
                                                    (size_t)3 * I * h / KC, dst));
+  return cudaGetLastError();
+}
+
+template <int PT>
+cudaError_t launch_packed_gemms(const PParams& P, cudaStream_t stream) {
+  static bool attr_done = false;  // one flag per instantiation
+  cudaError_t err;
+  if (!attr_done) {
+    if ((err = cudaFuncSetAttribute(packed_gemm_kernel<true, PT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)psmem_bytes<true, PT>())) != cudaSuccess)
+      return err;
+    if ((err = cudaFuncSetAttribute(packed_gemm_kernel<false, PT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)psmem_bytes<false, PT>())) != cudaSuccess)
+      return err;
+    attr_done = true;
+  }
+  const int grid = num_sms();
+  MOE_LAUNCH("gateup_packed", stream,
+             (packed_gemm_kernel<true, PT><<<grid, KTHREADS, psmem_bytes<true, PT>(), stream>>>(P)));
+  MOE_LAUNCH("down_packed", stream,
+             (packed_gemm_kernel<false, PT><<<grid, KTHREADS, psmem_bytes<false, PT>(), stream>>>(P)));
   return cudaGetLastError();
 }
 
@@ -702,28 +737,19 @@ cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, c
   P.xg = xg;
   P.kmax = a.I > a.Is ? a.I : a.Is;
 
+  // 64-row tiles when the experts see few rows each (at most 40 on average):
+  // a 128-row tile would be mostly padding, and the smaller accumulators
+  // leave TMEM for a deeper A ring.
+  const int pt = (long)a.t * a.k <= 40L * a.E ? PTILE_SMALL : PTILE;
   cudaError_t err;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if ((err = cudaFuncSetAttribute(packed_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)psmem_bytes<true>())) != cudaSuccess)
-      return err;
-    if ((err = cudaFuncSetAttribute(packed_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)psmem_bytes<false>())) != cudaSuccess)
-      return err;
-    attr_done = true;
-  }
-  if ((err = launch_schedule(p, hdr, tiles, units, (int)mt, PTILE, stream)) != cudaSuccess) return err;
+  if ((err = launch_schedule(p, hdr, tiles, units, (int)mt, pt, stream)) != cudaSuccess) return err;
   if (p.gate_vals && (err = launch_shared_gate(a.x, a.s_gate, a.t, a.h, gate_vals, stream)) != cudaSuccess)
     return err;
   MOE_LAUNCH("gather", stream,
-             gather_kernel<<<dim3((unsigned)mt, PTILE / 8), 256, 0, stream>>>(a.x, a.rows, hdr, tiles, a.t, a.h, a.E,
-                                                                             xg, a.status));
-  const int grid = num_sms();
-  MOE_LAUNCH("gateup_packed", stream,
-             packed_gemm_kernel<true><<<grid, KTHREADS, psmem_bytes<true>(), stream>>>(P));
-  MOE_LAUNCH("down_packed", stream,
-             packed_gemm_kernel<false><<<grid, KTHREADS, psmem_bytes<false>(), stream>>>(P));
+             gather_kernel<<<dim3((unsigned)mt, pt / 8), 256, 0, stream>>>(a.x, a.rows, hdr, tiles, a.t, a.h, a.E,
+                                                                          xg, a.status));
+  err = pt == PTILE ? launch_packed_gemms<PTILE>(P, stream) : launch_packed_gemms<PTILE_SMALL>(P, stream);
+  if (err != cudaSuccess) return err;
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   return launch_finalize(a, deterministic, stream);
 }
