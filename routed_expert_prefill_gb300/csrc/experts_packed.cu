@@ -60,20 +60,24 @@ constexpr int KWARPS = 16;
 constexpr int KTHREADS = KWARPS * 32;
 constexpr int SB = 4;                 // B stages
 constexpr int B_STAGE = 32768;        // bytes: KPS chunks of Nm rows x 128 B
-constexpr int CPS = 2;                // K chunks per code stage and per A stage
+constexpr int CPS_DEFAULT = 2;        // K chunks per code stage and per A stage (see PCfg)
 
 // TMEM (512 columns): NACC accumulator buffers of ACC_COLS columns (gate/up:
 // gate then up, PT columns each), then the A ring of SA stages.
-template <bool GATEUP, int PT>
+// CP K chunks per stage: 2, or 4 for the down pass on 64-row tiles (its
+// blocks are half the gate/up stage's, so the per-stage waits and fences
+// would otherwise be spread over only two blocks per warp).
+template <bool GATEUP, int PT, int CP>
 struct PCfg {
+  static constexpr int CPS = CP;
   static constexpr int NMAT = GATEUP ? 2 : 1;
   static constexpr int C_STAGE = CPS * NMAT * QB;        // packed blocks of one stage
-  static constexpr int SC = GATEUP ? 4 : 8;              // code stages
+  static constexpr int SC = 73728 / C_STAGE;             // code stages (72 KB)
   static constexpr int A_STAGE = CPS * NMAT * 32;        // TMEM columns per A stage
   static constexpr int NACC = GATEUP ? 1 : 2;            // accumulator buffers
   static constexpr int ACC_COLS = GATEUP ? 2 * PT : PT;  // TMEM columns per accumulator buffer
   static constexpr int A_COL = NACC * ACC_COLS;          // first column of the A ring
-  static constexpr int SA = (512 - A_COL) / A_STAGE;     // A stages: 2 / 4 at PT 128, 3 / 6 at PT 64
+  static constexpr int SA = (512 - A_COL) / A_STAGE;     // A stages: 2 / 4 at PT 128, 3 / 3 at PT 64
   static constexpr int NISS = GATEUP ? 2 : 1;            // MMA issuing threads (gate and up apart)
 };
 
@@ -260,7 +264,7 @@ struct PUnit {
   bool shared;
 };
 
-template <bool GATEUP>
+template <bool GATEUP, int CPS>
 __device__ __forceinline__ PUnit decode_punit(const TcParams& p, int u) {
   PUnit U;
   int4 T;
@@ -294,36 +298,37 @@ struct PParams {
   int kmax;                 // max(I, Is): hg row pitch in the padded space
 };
 
-template <bool GATEUP, int PT>
+template <bool GATEUP, int PT, int CP>
 struct PSmem {
   // down epilogue: per epilogue warp, the destination row (-1: skip) and
   // weight of every column of the current tile
   alignas(16) int col_row[4][PT];
   alignas(16) float col_w[4][PT];
-  uint64_t code_full[PCfg<GATEUP, PT>::SC], code_empty[PCfg<GATEUP, PT>::SC];
-  uint64_t a_full[PCfg<GATEUP, PT>::SA], a_empty[PCfg<GATEUP, PT>::SA];
+  uint64_t code_full[PCfg<GATEUP, PT, CP>::SC], code_empty[PCfg<GATEUP, PT, CP>::SC];
+  uint64_t a_full[PCfg<GATEUP, PT, CP>::SA], a_empty[PCfg<GATEUP, PT, CP>::SA];
   uint64_t b_full[SB], b_empty[SB];
-  uint64_t acc_full[PCfg<GATEUP, PT>::NACC], acc_empty[PCfg<GATEUP, PT>::NACC];
+  uint64_t acc_full[PCfg<GATEUP, PT, CP>::NACC], acc_empty[PCfg<GATEUP, PT, CP>::NACC];
   uint64_t drain[2];
   uint32_t tmem_slot;
   int abort;
 };
 
-template <bool GATEUP, int PT>
+template <bool GATEUP, int PT, int CP>
 constexpr size_t psmem_bytes() {
-  return 1024 + (size_t)SB * B_STAGE + (size_t)PCfg<GATEUP, PT>::SC * PCfg<GATEUP, PT>::C_STAGE +
-         sizeof(PSmem<GATEUP, PT>);
+  return 1024 + (size_t)SB * B_STAGE + (size_t)PCfg<GATEUP, PT, CP>::SC * PCfg<GATEUP, PT, CP>::C_STAGE +
+         sizeof(PSmem<GATEUP, PT, CP>);
 }
 
-template <bool GATEUP, int PT>
+template <bool GATEUP, int PT, int CP>
 __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
-  using C = PCfg<GATEUP, PT>;
+  using C = PCfg<GATEUP, PT, CP>;
+  constexpr int CPS = CP;
   const TcParams& p = P.p;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* b_s = base;
   uint8_t* c_s = b_s + SB * B_STAGE;
-  PSmem<GATEUP, PT>& S = *reinterpret_cast<PSmem<GATEUP, PT>*>(c_s + C::SC * C::C_STAGE);
+  PSmem<GATEUP, PT, CP>& S = *reinterpret_cast<PSmem<GATEUP, PT, CP>*>(c_s + C::SC * C::C_STAGE);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = p.h;
 
@@ -373,7 +378,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
       for (int i = 0; i < C::SC; ++i) armed[i] = false, par[i] = 0;
       bool stop = false;
       for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
-        const PUnit U = decode_punit<GATEUP>(p, u);
+        const PUnit U = decode_punit<GATEUP, CP>(p, u);
         const int Iu = U.shared ? p.Is : p.I;
         const uint8_t* rec = U.shared ? P.s_packed : P.packed + (size_t)U.e * rec_bytes(h, p.I);
         const uint8_t* src;
@@ -407,7 +412,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
       for (int i = 0; i < SB; ++i) armed[i] = false, par[i] = 0;
       bool stop = false;
       for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
-        const PUnit U = decode_punit<GATEUP>(p, u);
+        const PUnit U = decode_punit<GATEUP, CP>(p, u);
         const uint8_t* src = GATEUP ? reinterpret_cast<const uint8_t*>(P.xg + (size_t)U.pad * h)
                                     : reinterpret_cast<const uint8_t*>(p.hg + (size_t)U.pad * P.kmax);
         for (int kc0 = 0; kc0 < U.nkc; kc0 += U.kps, ++it) {
@@ -444,7 +449,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
       for (int i = 0; i < SB; ++i) bstage[i] = desc_sw128(smem_u32(b_s + i * B_STAGE));
       uint32_t ast = 0, bit = 0, uit = 0;
       for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
-        const PUnit U = decode_punit<GATEUP>(p, u);
+        const PUnit U = decode_punit<GATEUP, CP>(p, u);
         const uint32_t idesc = idesc_bf16(128, U.Nm);
         const uint32_t nm8 = (uint32_t)(U.Nm * 128) >> 4;  // descriptor step of one K chunk
         const int ab = uit % C::NACC;
@@ -500,7 +505,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t ast = 0, bbase = 0;  // global A stage; global B stage at the unit's start
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
-      const PUnit U = decode_punit<GATEUP>(p, u);
+      const PUnit U = decode_punit<GATEUP, CP>(p, u);
       bool ok = true;
       for (int st = 0; st < U.nkc / CPS; ++st, ++ast) {
         if ((int)(ast & 1) != grp) continue;
@@ -556,7 +561,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t uit = 0;
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
-      const PUnit U = decode_punit<GATEUP>(p, u);
+      const PUnit U = decode_punit<GATEUP, CP>(p, u);
       const int ab = uit % C::NACC;
       const int feat = U.f0 + o;
       // down: this warp's copy of the tile's destination rows and weights.
@@ -680,25 +685,28 @@ cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, const uint
   return cudaGetLastError();
 }
 
-template <int PT>
-cudaError_t launch_packed_gemms(const PParams& P, cudaStream_t stream) {
+template <bool GATEUP, int PT, int CP>
+cudaError_t launch_packed_gemm(const PParams& P, cudaStream_t stream) {
   static bool attr_done = false;  // one flag per instantiation
   cudaError_t err;
   if (!attr_done) {
-    if ((err = cudaFuncSetAttribute(packed_gemm_kernel<true, PT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)psmem_bytes<true, PT>())) != cudaSuccess)
-      return err;
-    if ((err = cudaFuncSetAttribute(packed_gemm_kernel<false, PT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)psmem_bytes<false, PT>())) != cudaSuccess)
+    if ((err = cudaFuncSetAttribute(packed_gemm_kernel<GATEUP, PT, CP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)psmem_bytes<GATEUP, PT, CP>())) != cudaSuccess)
       return err;
     attr_done = true;
   }
-  const int grid = num_sms();
-  MOE_LAUNCH("gateup_packed", stream,
-             (packed_gemm_kernel<true, PT><<<grid, KTHREADS, psmem_bytes<true, PT>(), stream>>>(P)));
-  MOE_LAUNCH("down_packed", stream,
-             (packed_gemm_kernel<false, PT><<<grid, KTHREADS, psmem_bytes<false, PT>(), stream>>>(P)));
+  MOE_LAUNCH(GATEUP ? "gateup_packed" : "down_packed", stream,
+             (packed_gemm_kernel<GATEUP, PT, CP><<<num_sms(), KTHREADS, psmem_bytes<GATEUP, PT, CP>(), stream>>>(P)));
   return cudaGetLastError();
+}
+
+template <int PT>
+cudaError_t launch_packed_gemms(const PParams& P, cudaStream_t stream) {
+  cudaError_t err = launch_packed_gemm<true, PT, CPS_DEFAULT>(P, stream);
+  if (err != cudaSuccess) return err;
+  // down on 64-row tiles: four K chunks per stage when every inter is a multiple of 256
+  if (PT == PTILE_SMALL && P.p.I % 256 == 0 && P.p.Is % 256 == 0) return launch_packed_gemm<false, PT, 4>(P, stream);
+  return launch_packed_gemm<false, PT, CPS_DEFAULT>(P, stream);
 }
 
 cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, const uint8_t* s_packed,
