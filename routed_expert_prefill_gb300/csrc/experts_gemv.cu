@@ -36,7 +36,7 @@ namespace moe {
 
 cudaError_t launch_shared_gate(const uint16_t* x, const uint16_t* g, int t, int h, float* out, cudaStream_t stream);
 
-constexpr int GV2_KS_MAX = 4;  // gate/up K slices of the streaming small-t kernels
+constexpr int GV2_KS_MAX = 8;  // gate/up K slices of the streaming small-t kernels
 
 namespace {
 
@@ -393,6 +393,18 @@ __device__ __forceinline__ void dequant_half(const uint8_t* blk, int o, int hf, 
     }
 }
 
+// acc += sum over 32 K of w * a, a = 32 fp32 in shared memory (16-byte aligned).
+__device__ __forceinline__ void fma32f(const uint32_t (&w)[16], const float* a, float& acc) {
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    const float4 x = *reinterpret_cast<const float4*>(a + 4 * v);
+    acc = fmaf(bf16lo(w[2 * v]), x.x, acc);
+    acc = fmaf(bf16hi(w[2 * v]), x.y, acc);
+    acc = fmaf(bf16lo(w[2 * v + 1]), x.z, acc);
+    acc = fmaf(bf16hi(w[2 * v + 1]), x.w, acc);
+  }
+}
+
 // acc += sum over 32 K of w * a, a = 32 bf16 in shared memory (16-byte aligned).
 __device__ __forceinline__ void fma32(const uint32_t (&w)[16], const uint16_t* a, float& acc) {
 #pragma unroll
@@ -493,16 +505,19 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_gateup(Gv2Params Q) {
   if (!gv2_unit<NB>(P, units_per_e, &s_e, R, e, sub, shared)) return;
   const int rt = sub / Q.KS, ks = sub % Q.KS, kc0 = ks * nkc;
   const int nb = R.n;
-  // token rows of this K slice, bf16, [NB][nkc * 64]
-  uint16_t* xs = reinterpret_cast<uint16_t*>(ring + GV2_RING);
-  float* xch = reinterpret_cast<float*>(xs + NB * nkc * GV_KC);  // [128][NB][2] halves exchange
+  // token rows of this K slice as fp32 (converted once, read by both
+  // matrices of every chunk), [NB][nkc * 64]
+  float* xs = reinterpret_cast<float*>(ring + GV2_RING);
+  float* xch = xs + NB * nkc * GV_KC;  // [128][NB][2] halves exchange
   const int kw = nkc * GV_KC;
   for (int v = threadIdx.x; v < nb * kw / 8; v += GV2_THREADS) {
     const int r = v / (kw / 8), c = v % (kw / 8);
     const int row = R.row[r];
     uint4 val = make_uint4(0, 0, 0, 0);
     if (row >= 0) val = __ldg(reinterpret_cast<const uint4*>(P.x + (size_t)row * P.h + kc0 * GV_KC) + c);
-    reinterpret_cast<uint4*>(xs + r * kw)[c] = val;
+    float4* d = reinterpret_cast<float4*>(xs + r * kw + c * 8);
+    d[0] = make_float4(bf16lo(val.x), bf16hi(val.x), bf16lo(val.y), bf16hi(val.y));
+    d[1] = make_float4(bf16lo(val.z), bf16hi(val.z), bf16lo(val.w), bf16hi(val.w));
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < ST; ++i) {
@@ -561,12 +576,12 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_gateup(Gv2Params Q) {
       dequant_half(blk + GV_QB, o, hf, wu);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
-      const uint16_t* xk = xs + i * GV_KC + hf * 32;
+      const float* xk = xs + i * GV_KC + hf * 32;
 #pragma unroll
       for (int r = 0; r < NB; ++r)
         if (r < nb) {
-          fma32(wg, xk + r * kw, g[r]);
-          fma32(wu, xk + r * kw, u[r]);
+          fma32f(wg, xk + r * kw, g[r]);
+          fma32f(wu, xk + r * kw, u[r]);
         }
     }
     if (hf == 1)
@@ -765,7 +780,7 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_down(Gv2Params Q) {
 
 template <int NB>
 size_t gv2_smem_gateup(int h, int KS) {
-  return GV2_RING + (size_t)NB * (h / KS) * 2 + (size_t)128 * NB * 2 * 4;
+  return GV2_RING + (size_t)NB * (h / KS) * 4 + (size_t)128 * NB * 2 * 4;
 }
 template <int NB>
 size_t gv2_smem_down(int kmax) {
@@ -791,8 +806,8 @@ cudaError_t launch_gv2(const Gv2Params& Q, int nact, cudaStream_t stream) {
 
 // The streaming variant fits when the staged rows fit next to the ring.
 bool gv2_fits(int NB, int h, int kmax, int KS) {
-  const size_t lim = 200 * 1024;
-  return (size_t)GV2_RING + (size_t)NB * (h / KS) * 2 + (size_t)128 * NB * 8 <= lim &&
+  const size_t lim = 220 * 1024;
+  return (size_t)GV2_RING + (size_t)NB * (h / KS) * 4 + (size_t)128 * NB * 8 <= lim &&
          (size_t)GV2_RING + (size_t)NB * kmax * 2 + (size_t)128 * NB * 4 <= lim;
 }
 
@@ -856,7 +871,7 @@ cudaError_t launch_experts_gemv(const ExpertsArgs& a, bool packed, bool determin
     // K slices: enough units to occupy the GPU when few experts are active
     const int units = nact * (a.I / 128);
     const int nkc = a.h / GV_KC;
-    int KS = units < 40 ? 4 : units < 80 ? 2 : 1;
+    int KS = units < 20 ? 8 : units < 40 ? 4 : units < 80 ? 2 : 1;
     while (KS > 1 && (nkc % KS || !gv2_fits(NBr, a.h, kmax, KS))) KS >>= 1;
     if (gv2_fits(NBr, a.h, kmax, KS)) {
       Gv2Params Q{P, a.gvpart, KS, kmax};
