@@ -202,18 +202,29 @@ def oracle_sample_seconds(w: synth.Workload, inp: dict, rows: int) -> float:
     return time.perf_counter() - t0
 
 
+def calibrated_rows(w: synth.Workload, inp: dict, budget_s: float) -> int:
+    """Rows of the workload whose oracle pass takes about budget_s (from a timed 4-row probe)."""
+    probe = min(w.t, 4)
+    per_row = oracle_sample_seconds(w, inp, probe) / probe
+    return int(max(probe, min(w.t, budget_s / max(per_row, 1e-9))))
+
+
 def run_reference(args, w: synth.Workload):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     inp = synth.make_inputs(w)
-    rows = min(w.t, args.oracle_rows)
+    # each step a bounded sample: the whole run stays within about 150 s
+    per_step = min(10.0, 150.0 / max(1, args.steps + args.warmup))
+    rows = min(calibrated_rows(w, inp, per_step), args.oracle_rows) if args.oracle_rows else \
+        calibrated_rows(w, inp, per_step)
     for _ in range(args.warmup):
-        oracle_sample_seconds(w, inp, min(rows, 4))
+        oracle_sample_seconds(w, inp, rows)
     secs = [oracle_sample_seconds(w, inp, rows) for _ in range(args.steps)]
     tot = sum(secs)
     value = rows * len(secs) / tot
-    sample = f"first {rows} of the {w.t} rows of the workload per step, full oracle (router, CSR, experts)"
+    sample = (f"first {rows} of the {w.t} rows of the workload per step (about {per_step:.0f} s of oracle work "
+              f"each), full oracle (router, CSR, experts), one thread")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(secs) * w.t / rows,
@@ -385,10 +396,14 @@ def run_ours(args, w: synth.Workload):
 
     cpu = None
     if not args.no_cpu_baseline:
-        rows = min(w.t, args.oracle_rows)
+        # a bounded sample of about 10 s of oracle work
+        rows = calibrated_rows(w, inp, 10.0)
+        if args.oracle_rows:
+            rows = min(rows, args.oracle_rows)
         secs = oracle_sample_seconds(w, inp, rows)
         cpu = {"value": rows / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"first {rows} of {w.t} rows, one full oracle pass (router, CSR, experts), 1 thread"}
+               "sample": f"first {rows} of {w.t} rows (about 10 s of work), one full oracle pass "
+                         f"(router, CSR, experts), 1 thread"}
 
     value = job_tokens_per_s(world, w.t, ms)
     line = {
@@ -429,7 +444,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--flags", type=int, default=16, help="moe_experts_fwd flags (16: packed weights)")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of graph replays")
-    ap.add_argument("--oracle-rows", type=int, default=16)
+    ap.add_argument("--oracle-rows", type=int, default=0, help="cap on the oracle sample's rows (0: time-budgeted)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = synth.WORKLOADS[args.workload]
