@@ -58,8 +58,7 @@ constexpr int W_CODE = 0, W_MMA = 1, W_DQ0 = 2, W_B = 10, W_EPI0 = 11, W_MMA2 = 
 // 0 code, 1 MMA (gate / down), 2-9 dequant (two groups), 10 B, 11-14 epilogue, 15 MMA (up)
 constexpr int KWARPS = 16;
 constexpr int KTHREADS = KWARPS * 32;
-constexpr int SB = 4;                 // B stages
-constexpr int B_STAGE = 32768;        // bytes: KPS chunks of Nm rows x 128 B
+constexpr int B_RING = 131072;        // bytes of token-tile stages (see PCfg::SB, PCfg::B_STAGE)
 constexpr int CPS_DEFAULT = 2;        // K chunks per code stage and per A stage (see PCfg)
 
 // TMEM (512 columns): NACC accumulator buffers of ACC_COLS columns (gate/up:
@@ -79,6 +78,10 @@ struct PCfg {
   static constexpr int A_COL = NACC * ACC_COLS;          // first column of the A ring
   static constexpr int SA = (512 - A_COL) / A_STAGE;     // A stages: 2 / 4 at PT 128, 3 / 3 at PT 64
   static constexpr int NISS = GATEUP ? 2 : 1;            // MMA issuing threads (gate and up apart)
+  // token-tile stages: 4 x 32 KB, or 2 x 64 KB when a stage of CP chunks of
+  // 128 rows needs it (every A stage must read a single B stage)
+  static constexpr int B_STAGE = CP * PT * 128 > 32768 ? 65536 : 32768;
+  static constexpr int SB = B_RING / B_STAGE;
 };
 
 __host__ __device__ inline size_t gu_bytes(int h, int I) { return (size_t)(I / 128) * (h / KC) * 2 * QB; }
@@ -264,7 +267,7 @@ struct PUnit {
   bool shared;
 };
 
-template <bool GATEUP, int CPS>
+template <bool GATEUP, int CPS, int B_STAGE>
 __device__ __forceinline__ PUnit decode_punit(const TcParams& p, int u) {
   PUnit U;
   int4 T;
@@ -306,7 +309,7 @@ struct PSmem {
   alignas(16) float col_w[4][PT];
   uint64_t code_full[PCfg<GATEUP, PT, CP>::SC], code_empty[PCfg<GATEUP, PT, CP>::SC];
   uint64_t a_full[PCfg<GATEUP, PT, CP>::SA], a_empty[PCfg<GATEUP, PT, CP>::SA];
-  uint64_t b_full[SB], b_empty[SB];
+  uint64_t b_full[PCfg<GATEUP, PT, CP>::SB], b_empty[PCfg<GATEUP, PT, CP>::SB];
   uint64_t acc_full[PCfg<GATEUP, PT, CP>::NACC], acc_empty[PCfg<GATEUP, PT, CP>::NACC];
   uint64_t drain[2];
   uint32_t tmem_slot;
@@ -315,7 +318,7 @@ struct PSmem {
 
 template <bool GATEUP, int PT, int CP>
 constexpr size_t psmem_bytes() {
-  return 1024 + (size_t)SB * B_STAGE + (size_t)PCfg<GATEUP, PT, CP>::SC * PCfg<GATEUP, PT, CP>::C_STAGE +
+  return 1024 + (size_t)B_RING + (size_t)PCfg<GATEUP, PT, CP>::SC * PCfg<GATEUP, PT, CP>::C_STAGE +
          sizeof(PSmem<GATEUP, PT, CP>);
 }
 
@@ -323,11 +326,12 @@ template <bool GATEUP, int PT, int CP>
 __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
   using C = PCfg<GATEUP, PT, CP>;
   constexpr int CPS = CP;
+  constexpr int SB = C::SB, B_STAGE = C::B_STAGE;
   const TcParams& p = P.p;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* b_s = base;
-  uint8_t* c_s = b_s + SB * B_STAGE;
+  uint8_t* c_s = b_s + B_RING;
   PSmem<GATEUP, PT, CP>& S = *reinterpret_cast<PSmem<GATEUP, PT, CP>*>(c_s + C::SC * C::C_STAGE);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = p.h;
@@ -378,7 +382,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
       for (int i = 0; i < C::SC; ++i) armed[i] = false, par[i] = 0;
       bool stop = false;
       for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
-        const PUnit U = decode_punit<GATEUP, CP>(p, u);
+        const PUnit U = decode_punit<GATEUP, CP, C::B_STAGE>(p, u);
         const int Iu = U.shared ? p.Is : p.I;
         const uint8_t* rec = U.shared ? P.s_packed : P.packed + (size_t)U.e * rec_bytes(h, p.I);
         const uint8_t* src;
@@ -412,7 +416,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
       for (int i = 0; i < SB; ++i) armed[i] = false, par[i] = 0;
       bool stop = false;
       for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
-        const PUnit U = decode_punit<GATEUP, CP>(p, u);
+        const PUnit U = decode_punit<GATEUP, CP, C::B_STAGE>(p, u);
         const uint8_t* src = GATEUP ? reinterpret_cast<const uint8_t*>(P.xg + (size_t)U.pad * h)
                                     : reinterpret_cast<const uint8_t*>(p.hg + (size_t)U.pad * P.kmax);
         for (int kc0 = 0; kc0 < U.nkc; kc0 += U.kps, ++it) {
@@ -449,7 +453,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
       for (int i = 0; i < SB; ++i) bstage[i] = desc_sw128(smem_u32(b_s + i * B_STAGE));
       uint32_t ast = 0, bit = 0, uit = 0;
       for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
-        const PUnit U = decode_punit<GATEUP, CP>(p, u);
+        const PUnit U = decode_punit<GATEUP, CP, C::B_STAGE>(p, u);
         const uint32_t idesc = idesc_bf16(128, U.Nm);
         const uint32_t nm8 = (uint32_t)(U.Nm * 128) >> 4;  // descriptor step of one K chunk
         const int ab = uit % C::NACC;
@@ -505,7 +509,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t ast = 0, bbase = 0;  // global A stage; global B stage at the unit's start
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
-      const PUnit U = decode_punit<GATEUP, CP>(p, u);
+      const PUnit U = decode_punit<GATEUP, CP, C::B_STAGE>(p, u);
       bool ok = true;
       for (int st = 0; st < U.nkc / CPS; ++st, ++ast) {
         if ((int)(ast & 1) != grp) continue;
@@ -561,7 +565,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t uit = 0;
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
-      const PUnit U = decode_punit<GATEUP, CP>(p, u);
+      const PUnit U = decode_punit<GATEUP, CP, C::B_STAGE>(p, u);
       const int ab = uit % C::NACC;
       const int feat = U.f0 + o;
       // down: this warp's copy of the tile's destination rows and weights.
@@ -704,8 +708,8 @@ template <int PT>
 cudaError_t launch_packed_gemms(const PParams& P, cudaStream_t stream) {
   cudaError_t err = launch_packed_gemm<true, PT, CPS_DEFAULT>(P, stream);
   if (err != cudaSuccess) return err;
-  // down on 64-row tiles: four K chunks per stage when every inter is a multiple of 256
-  if (PT == PTILE_SMALL && P.p.I % 256 == 0 && P.p.Is % 256 == 0) return launch_packed_gemm<false, PT, 4>(P, stream);
+  // down: four K chunks per stage when every inter is a multiple of 256
+  if (P.p.I % 256 == 0 && P.p.Is % 256 == 0) return launch_packed_gemm<false, PT, 4>(P, stream);
   return launch_packed_gemm<false, PT, CPS_DEFAULT>(P, stream);
 }
 
