@@ -177,7 +177,21 @@ int moe_build_csr(const int32_t* idx, const float* w, const moe_dims* dims,
  * the block sum accumulates in fp32 and `out` is rounded once to bf16.
  * Without MOE_DETERMINISTIC the routed terms are added with fp32 atomics
  * (summation order varies run to run); with it every row sums its shared
- * term and its k terms in expert-ascending order.
+ * term and its k terms in expert-ascending order.  The CUDA path computes
+ * silu(z) as z * (1 + tanh(z / 2)) / 2 with the hardware tanh approximation
+ * (absolute error of the sigmoid about 2^-12, below the bf16 rounding of the
+ * result).
+ *
+ * Kernel choice (the result meets the same tolerance either way):
+ *   - weight-streaming small-t kernels when t <= 16 and t * k * inter / 128
+ *     < 152 (too few expert tiles to occupy the GPU), or MOE_FORCE_SMALL_T;
+ *   - otherwise the tensor-core grouped kernels (MOE_FORCE_LARGE_T forces
+ *     them), on packed weights with MOE_PACKED_WEIGHTS, or on the row-major
+ *     records;
+ *   - MOE_SIMPLE_KERNELS: plain CUDA-core kernels (a slow cross-check).
+ * A call whose workspace status block was never cleared (moe_clear_device_
+ * status) may report stale flags; the small-t kernels also keep a completion
+ * counter there, so clear a new workspace once before its first use.
  *
  * x bf16 [t][h] in; out bf16 [t][h] out (no residual is added).
  * ws: at least moe_workspace_bytes(dims, flags) bytes.

@@ -113,6 +113,34 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 WsLayout ws_layout(const moe_dims& d, uint32_t flags);
 
+// Raise a kernel's dynamic shared-memory limit once per device (the attribute
+// is per device; a process may drive several GPUs).  Concurrent first calls
+// from two host threads both set the same value, which is harmless.
+template <typename Kernel>
+cudaError_t set_smem_limit_once(Kernel* kernel, int bytes) {
+  static bool done[128] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev >= 0 && dev < 128 && done[dev]) return cudaSuccess;
+  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err == cudaSuccess && dev >= 0 && dev < 128) done[dev] = true;
+  return err;
+}
+
+// SM count of the current device, queried once per device.
+inline int sm_count() {
+  static int n[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+  if (!n[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    n[dev] = v > 0 ? v : 148;
+  }
+  return n[dev];
+}
+
 // Thread-local error message (moe_api.cu)
 int set_error(int status, const char* fmt, ...);
 

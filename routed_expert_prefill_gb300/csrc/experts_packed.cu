@@ -654,16 +654,6 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
   }
 }
 
-int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
 
 }  // namespace
 
@@ -691,16 +681,10 @@ cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, const uint
 
 template <bool GATEUP, int PT, int CP>
 cudaError_t launch_packed_gemm(const PParams& P, cudaStream_t stream) {
-  static bool attr_done = false;  // one flag per instantiation
-  cudaError_t err;
-  if (!attr_done) {
-    if ((err = cudaFuncSetAttribute(packed_gemm_kernel<GATEUP, PT, CP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)psmem_bytes<GATEUP, PT, CP>())) != cudaSuccess)
-      return err;
-    attr_done = true;
-  }
+  cudaError_t err = set_smem_limit_once(packed_gemm_kernel<GATEUP, PT, CP>, (int)psmem_bytes<GATEUP, PT, CP>());
+  if (err != cudaSuccess) return err;
   MOE_LAUNCH(GATEUP ? "gateup_packed" : "down_packed", stream,
-             (packed_gemm_kernel<GATEUP, PT, CP><<<num_sms(), KTHREADS, psmem_bytes<GATEUP, PT, CP>(), stream>>>(P)));
+             (packed_gemm_kernel<GATEUP, PT, CP><<<sm_count(), KTHREADS, psmem_bytes<GATEUP, PT, CP>(), stream>>>(P)));
   return cudaGetLastError();
 }
 

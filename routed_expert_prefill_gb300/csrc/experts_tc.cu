@@ -735,16 +735,6 @@ cudaError_t make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, u
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
 
 }  // namespace
 
@@ -843,21 +833,13 @@ cudaError_t launch_experts_tc(const ExpertsArgs& a, bool deterministic, cudaStre
     tm_hgs = tm_hg;
   }
 
-  static bool attr_done = false;
-  if (!attr_done) {
-    if ((err = cudaFuncSetAttribute(expert_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)kernel_smem<true>())) != cudaSuccess)
-      return err;
-    if ((err = cudaFuncSetAttribute(expert_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)kernel_smem<false>())) != cudaSuccess)
-      return err;
-    attr_done = true;
-  }
+  if ((err = set_smem_limit_once(expert_gemm_kernel<true>, (int)kernel_smem<true>())) != cudaSuccess) return err;
+  if ((err = set_smem_limit_once(expert_gemm_kernel<false>, (int)kernel_smem<false>())) != cudaSuccess) return err;
 
   if ((err = launch_schedule(p, hdr, tiles, units, (int)mt, TILE_MAX, stream)) != cudaSuccess) return err;
   if (p.gate_vals && (err = launch_shared_gate(a.x, a.s_gate, a.t, a.h, gate_vals, stream)) != cudaSuccess)
     return err;
-  const int grid = num_sms();
+  const int grid = sm_count();
   MOE_LAUNCH("gateup_tc", stream,
              expert_gemm_kernel<true><<<grid, KTHREADS, kernel_smem<true>(), stream>>>(tm_codes_gu, tm_scodes_gu,
                                                                                      tm_x, tm_x, p));

@@ -507,13 +507,8 @@ cudaError_t launch_refine_w(const uint16_t* x, const uint16_t* wr, const float* 
                             const RoutePlan& R, const float* wn2, int t, int h, int E, int k, float eps, int32_t* idx,
                             float* w, DeviceStatus* st, cudaStream_t stream) {
   const size_t smem = (size_t)(RF_WARPS / WPR) * NQ * 32 * 12;
-  static bool attr_set = false;  // one flag per instantiation
-  if (!attr_set) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(route_refine_kernel<NQ, WPR>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const cudaError_t e = set_smem_limit_once(route_refine_kernel<NQ, WPR>, (int)smem);
+  if (e != cudaSuccess) return e;
   const int rows_per_cta = RF_WARPS / WPR;
   MOE_LAUNCH("route_refine", stream,
              (route_refine_kernel<NQ, WPR><<<(t + rows_per_cta - 1) / rows_per_cta, RF_WARPS * 32, smem, stream>>>(
@@ -577,13 +572,7 @@ cudaError_t launch_route_tc(const uint16_t* x, const uint16_t* wr, const float* 
                      CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
     return err;
   const size_t smem = score_smem_bytes(R.NT);
-  static int smem_set = 0;
-  if (smem_set < (int)smem) {
-    if ((err = cudaFuncSetAttribute(route_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)score_smem_bytes(256))) != cudaSuccess)
-      return err;
-    smem_set = (int)score_smem_bytes(256);
-  }
+  if ((err = set_smem_limit_once(route_score_kernel, (int)score_smem_bytes(256))) != cudaSuccess) return err;
   ScoreParams P{t, h, E, R.Ep, R.NT, R.nkc_split, part, wn2, wr, st};
   MOE_LAUNCH("route_score", stream,
              route_score_kernel<<<dim3(R.mt, R.ntn, R.KS), RS_WARPS * 32, smem, stream>>>(tx, tw, P));
