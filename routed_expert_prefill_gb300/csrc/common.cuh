@@ -6,6 +6,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <utility>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -113,19 +116,40 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 WsLayout ws_layout(const moe_dims& d, uint32_t flags);
 
-// Raise a kernel's dynamic shared-memory limit once per device (the attribute
-// is per device; a process may drive several GPUs).  Concurrent first calls
-// from two host threads both set the same value, which is harmless.
-template <typename Kernel>
-cudaError_t set_smem_limit_once(Kernel* kernel, int bytes) {
-  static bool done[128] = {};
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device): the
+// attribute is per device and a process may drive several GPUs.  The table is
+// keyed by the kernel's address, so template instances that share a signature
+// are tracked apart; a later call asking for more bytes sets the limit again.
+inline cudaError_t smem_limit_once(const void* kernel, int bytes) {
+  struct Entry {
+    const void* kernel;
+    int dev;
+    int bytes;
+  };
+  static std::mutex mu;
+  static Entry table[512];
+  static int used = 0;
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if (dev >= 0 && dev < 128 && done[dev]) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(mu);
+  int slot = -1;
+  for (int i = 0; i < used; ++i)
+    if (table[i].kernel == kernel && table[i].dev == dev) {
+      if (table[i].bytes >= bytes) return cudaSuccess;
+      slot = i;
+      break;
+    }
   err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (err == cudaSuccess && dev >= 0 && dev < 128) done[dev] = true;
-  return err;
+  if (err != cudaSuccess) return err;
+  if (slot < 0 && used < 512) slot = used++;
+  if (slot >= 0) table[slot] = Entry{kernel, dev, bytes};
+  return cudaSuccess;
+}
+
+template <typename Kernel>
+cudaError_t set_smem_limit_once(Kernel* kernel, int bytes) {
+  return smem_limit_once(reinterpret_cast<const void*>(kernel), bytes);
 }
 
 // SM count of the current device, queried once per device.
@@ -139,6 +163,37 @@ inline int sm_count() {
     n[dev] = v > 0 ? v : 148;
   }
   return n[dev];
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of the path is launched with
+// programmatic stream serialisation, so it may be launched while the previous
+// kernel on the stream is still running.  Each kernel first waits for the
+// previous grid to complete with its memory visible (pdl_wait), before any
+// other work -- TMEM allocation included, so that a waiting grid never holds
+// columns its predecessor still needs -- and then signals that its own
+// dependents may launch (pdl_trigger).  What overlaps is the launch and CTA
+// rasterisation of the next kernel with the tail of the current one.  Every
+// CTA waits before it can exit, so completion stays transitive along the
+// stream.  Without the launch attribute both are no-ops.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // Thread-local error message (moe_api.cu)

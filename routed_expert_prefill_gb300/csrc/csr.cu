@@ -25,6 +25,8 @@ namespace {
 __global__ void __launch_bounds__(CSR_CHUNK)
 csr_rank_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __restrict__ rank,
                 int32_t* __restrict__ counts, DeviceStatus* st) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint32_t bm[];  // [E][CSR_CHUNK / 32]
   constexpr int W = CSR_CHUNK / 32;
   const int tid = threadIdx.x;
@@ -59,6 +61,8 @@ csr_rank_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __restri
 __global__ void __launch_bounds__(1024)
 csr_scan_kernel(const int32_t* __restrict__ counts, int nchunks, int E, int32_t* __restrict__ base,
                 int32_t* __restrict__ offsets) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int32_t tot[1024];
   __shared__ int32_t warp_sums[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -102,6 +106,8 @@ __global__ void csr_scatter_kernel(const int32_t* __restrict__ idx, const float*
                                    const int32_t* __restrict__ base, const int32_t* __restrict__ offsets,
                                    int32_t* __restrict__ rows, float* __restrict__ weights,
                                    int32_t* __restrict__ slot_of) {
+  pdl_wait();
+  pdl_trigger();
   const int p = blockIdx.x * blockDim.x + threadIdx.x;
   if (p >= n) return;
   const int e = idx[p];
@@ -151,6 +157,8 @@ __global__ void __launch_bounds__(CSR_CHUNK, 1)
 csr_small_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w, int n, int k, int E,
                  int32_t* __restrict__ offsets, int32_t* __restrict__ rows, float* __restrict__ weights,
                  int32_t* __restrict__ slot_of, DeviceStatus* st) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint32_t sm[];
   constexpr int W = CSR_CHUNK / 32;
   uint32_t* bm = sm;                                      // [E][W] chunk bitmap
@@ -242,7 +250,7 @@ cudaError_t launch_build_csr(const int32_t* idx, const float* w, int t, int k, i
         cudaFuncSetAttribute(csr_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     MOE_LAUNCH("csr_small", stream,
-               csr_small_kernel<<<1, CSR_CHUNK, smem, stream>>>(idx, w, n, k, E, csr.offsets, csr.rows, csr.weights,
+               launch_k(csr_small_kernel, 1, CSR_CHUNK, smem, stream, idx, w, n, k, E, csr.offsets, csr.rows, csr.weights,
                                                                 csr.slot_of, st));
     return cudaGetLastError();
   }
@@ -250,10 +258,10 @@ cudaError_t launch_build_csr(const int32_t* idx, const float* w, int t, int k, i
   cudaError_t err = cudaFuncSetAttribute(csr_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   MOE_LAUNCH("csr_rank", stream,
-             csr_rank_kernel<<<nchunks, CSR_CHUNK, smem, stream>>>(idx, n, E, rank, counts, st));
-  MOE_LAUNCH("csr_scan", stream, csr_scan_kernel<<<1, 1024, 0, stream>>>(counts, nchunks, E, base, csr.offsets));
+             launch_k(csr_rank_kernel, nchunks, CSR_CHUNK, smem, stream, idx, n, E, rank, counts, st));
+  MOE_LAUNCH("csr_scan", stream, launch_k(csr_scan_kernel, 1, 1024, 0, stream, counts, nchunks, E, base, csr.offsets));
   MOE_LAUNCH("csr_scatter", stream,
-             csr_scatter_kernel<<<(n + 255) / 256, 256, 0, stream>>>(idx, w, n, k, E, rank, base, csr.offsets,
+             launch_k(csr_scatter_kernel, (n + 255) / 256, 256, 0, stream, idx, w, n, k, E, rank, base, csr.offsets,
                                                                     csr.rows, csr.weights, csr.slot_of));
   return cudaGetLastError();
 }

@@ -6,6 +6,8 @@ namespace moe {
 namespace {
 
 __global__ void zero_f32_kernel(float4* __restrict__ p, size_t n4) {
+  pdl_wait();
+  pdl_trigger();
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x)
     p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
@@ -15,6 +17,8 @@ __global__ void zero_f32_kernel(float4* __restrict__ p, size_t n4) {
 // (= expert-ascending) of weight * y), acc holding the shared term.
 __global__ void __launch_bounds__(256)
 finalize_kernel(ExpertsArgs a, int deterministic) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int pos[16];
   __shared__ int npos;
   const int r = blockIdx.x;
@@ -57,12 +61,12 @@ cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t stream) {
   int blocks = (int)((n4 + 255) / 256);
   if (blocks > 152 * 8) blocks = 152 * 8;
   if (blocks < 1) blocks = 1;
-  MOE_LAUNCH("zero_acc", stream, zero_f32_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<float4*>(p), n4));
+  MOE_LAUNCH("zero_acc", stream, launch_k(zero_f32_kernel, blocks, 256, 0, stream, reinterpret_cast<float4*>(p), n4));
   return cudaGetLastError();
 }
 
 cudaError_t launch_finalize(const ExpertsArgs& a, bool deterministic, cudaStream_t stream) {
-  MOE_LAUNCH("finalize", stream, finalize_kernel<<<a.t, 256, 0, stream>>>(a, deterministic ? 1 : 0));
+  MOE_LAUNCH("finalize", stream, launch_k(finalize_kernel, a.t, 256, 0, stream, a, deterministic ? 1 : 0));
   return cudaGetLastError();
 }
 

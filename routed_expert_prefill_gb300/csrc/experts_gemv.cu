@@ -220,6 +220,8 @@ struct GvRows {
 template <bool GATEUP, int NB>
 __global__ void __launch_bounds__(GV_THREADS)
 gemv_kernel(GvParams P, int groups) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int GV_PF = gv_pf<NB>();
   __shared__ int s_e;
   __shared__ int s_row[NB];
@@ -484,6 +486,8 @@ __device__ bool gv2_unit(const GvParams& P, int units_per_e, int* s_e, Gv2Rows<N
 // gate/up: unit = (expert, 128-row feature tile rt, K slice ks).
 template <int NB>
 __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_gateup(Gv2Params Q) {
+  pdl_wait();
+  pdl_trigger();
   const GvParams& P = Q.p;
   extern __shared__ __align__(16) uint8_t sm[];
   uint8_t* ring = sm;
@@ -666,6 +670,8 @@ __device__ void gv2_finalize_if_last(const GvParams& P) {
 // unit, counts itself done; the last one finalises the block output.
 template <int NB>
 __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_down(Gv2Params Q) {
+  pdl_wait();
+  pdl_trigger();
   const GvParams& P = Q.p;
   extern __shared__ __align__(16) uint8_t sm[];
   uint8_t* ring = sm;
@@ -798,9 +804,9 @@ cudaError_t launch_gv2(const Gv2Params& Q, int nact, cudaStream_t stream) {
     return err;
   const int ug = (P.I / 128) * Q.KS, ugs = (P.Is / 128) * Q.KS;
   const int xg = nact * ug > ugs ? nact * ug : ugs;
-  MOE_LAUNCH("gateup_gemv", stream, (gv2_gateup<NB><<<dim3(xg, 2), GV2_THREADS, sg, stream>>>(Q)));
+  MOE_LAUNCH("gateup_gemv", stream, (launch_k(gv2_gateup<NB>, dim3(xg, 2), GV2_THREADS, sg, stream, Q)));
   MOE_LAUNCH("down_gemv", stream,
-             (gv2_down<NB><<<dim3(nact * (P.h / 128), 2), GV2_THREADS, sd, stream>>>(Q)));
+             (launch_k(gv2_down<NB>, dim3(nact * (P.h / 128), 2), GV2_THREADS, sd, stream, Q)));
   return cudaGetLastError();
 }
 
@@ -814,8 +820,8 @@ bool gv2_fits(int NB, int h, int kmax, int KS) {
 template <int NB>
 cudaError_t launch_gemv(const GvParams& P, int x_gu, int g_gu, int x_dn, int g_dn, cudaStream_t stream) {
   MOE_LAUNCH("gateup_gemv", stream,
-             (gemv_kernel<true, NB><<<dim3(x_gu, 2), GV_THREADS, 0, stream>>>(P, g_gu)));
-  MOE_LAUNCH("down_gemv", stream, (gemv_kernel<false, NB><<<dim3(x_dn, 2), GV_THREADS, 0, stream>>>(P, g_dn)));
+             (launch_k(gemv_kernel<true, NB>, dim3(x_gu, 2), GV_THREADS, 0, stream, P, g_gu)));
+  MOE_LAUNCH("down_gemv", stream, (launch_k(gemv_kernel<false, NB>, dim3(x_dn, 2), GV_THREADS, 0, stream, P, g_dn)));
   return cudaGetLastError();
 }
 

@@ -100,6 +100,8 @@ __global__ void __launch_bounds__(128)
 pack_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
             const uint16_t* __restrict__ biases, int h, int I, size_t src_rec_bytes, size_t src_rec_groups,
             uint8_t* __restrict__ dst) {
+  pdl_wait();
+  pdl_trigger();
   const int rec = blockIdx.y;
   const int nkc_gu = h / KC, nkc_d = I / KC;
   const int nblk_gu = (I / 128) * nkc_gu;  // gate/up block pairs
@@ -148,6 +150,8 @@ pack_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scal
 __global__ void __launch_bounds__(256)
 gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ rows, const SchedHdr* hdr,
               const int4* __restrict__ tiles, int t, int h, int E, uint16_t* __restrict__ xg, DeviceStatus* st) {
+  pdl_wait();
+  pdl_trigger();
   if ((int)blockIdx.x >= hdr->n_tiles) return;
   const int4 T = tiles[blockIdx.x];
   const int n = T.z, Nm = (n + 15) & ~15;
@@ -324,6 +328,8 @@ constexpr size_t psmem_bytes() {
 
 template <bool GATEUP, int PT, int CP>
 __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
+  pdl_wait();
+  pdl_trigger();
   using C = PCfg<GATEUP, PT, CP>;
   constexpr int CPS = CP;
   constexpr int SB = C::SB, B_STAGE = C::B_STAGE;
@@ -684,7 +690,7 @@ cudaError_t launch_packed_gemm(const PParams& P, cudaStream_t stream) {
   cudaError_t err = set_smem_limit_once(packed_gemm_kernel<GATEUP, PT, CP>, (int)psmem_bytes<GATEUP, PT, CP>());
   if (err != cudaSuccess) return err;
   MOE_LAUNCH(GATEUP ? "gateup_packed" : "down_packed", stream,
-             (packed_gemm_kernel<GATEUP, PT, CP><<<sm_count(), KTHREADS, psmem_bytes<GATEUP, PT, CP>(), stream>>>(P)));
+             (launch_k(packed_gemm_kernel<GATEUP, PT, CP>, sm_count(), KTHREADS, psmem_bytes<GATEUP, PT, CP>(), stream, P)));
   return cudaGetLastError();
 }
 
@@ -742,7 +748,7 @@ cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, c
   if (p.gate_vals && (err = launch_shared_gate(a.x, a.s_gate, a.t, a.h, gate_vals, stream)) != cudaSuccess)
     return err;
   MOE_LAUNCH("gather", stream,
-             gather_kernel<<<dim3((unsigned)mt, pt / 8), 256, 0, stream>>>(a.x, a.rows, hdr, tiles, a.t, a.h, a.E,
+             launch_k(gather_kernel, dim3((unsigned)mt, pt / 8), 256, 0, stream, a.x, a.rows, hdr, tiles, a.t, a.h, a.E,
                                                                           xg, a.status));
   err = pt == PTILE ? launch_packed_gemms<PTILE>(P, stream) : launch_packed_gemms<PTILE_SMALL>(P, stream);
   if (err != cudaSuccess) return err;

@@ -56,6 +56,8 @@ __device__ __forceinline__ float qrow_dot(const float* xs, const uint8_t* codes,
 
 __global__ void __launch_bounds__(SB)
 gateup_simple_kernel(ExpertsArgs a, int shared) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ float xs[];
   const int p = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -100,6 +102,8 @@ gateup_simple_kernel(ExpertsArgs a, int shared) {
 // mode 2: shared, store g_r * y into acc.
 __global__ void __launch_bounds__(SB)
 down_simple_kernel(ExpertsArgs a, int mode) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ float hs[];
   __shared__ float gate_r;
   const int p = blockIdx.x;
@@ -167,15 +171,15 @@ cudaError_t launch_experts_simple(const ExpertsArgs& a, bool deterministic, cuda
                                   (a.I > a.Is ? a.I : a.Is) * 4)) != cudaSuccess)
     return err;
   if (a.Is > 0) {
-    MOE_LAUNCH("gateup_simple", stream, gateup_simple_kernel<<<a.t, SB, a.h * 4, stream>>>(a, 1));
-    MOE_LAUNCH("down_simple", stream, down_simple_kernel<<<a.t, SB, a.Is * 4, stream>>>(a, 2));
+    MOE_LAUNCH("gateup_simple", stream, launch_k(gateup_simple_kernel, a.t, SB, a.h * 4, stream, a, 1));
+    MOE_LAUNCH("down_simple", stream, launch_k(down_simple_kernel, a.t, SB, a.Is * 4, stream, a, 2));
   } else {
     err = launch_zero_f32(a.acc, (size_t)a.t * a.h, stream);
     if (err != cudaSuccess) return err;
   }
   if (n > 0) {
-    MOE_LAUNCH("gateup_simple", stream, gateup_simple_kernel<<<n, SB, a.h * 4, stream>>>(a, 0));
-    MOE_LAUNCH("down_simple", stream, down_simple_kernel<<<n, SB, a.I * 4, stream>>>(a, deterministic ? 1 : 0));
+    MOE_LAUNCH("gateup_simple", stream, launch_k(gateup_simple_kernel, n, SB, a.h * 4, stream, a, 0));
+    MOE_LAUNCH("down_simple", stream, launch_k(down_simple_kernel, n, SB, a.I * 4, stream, a, deterministic ? 1 : 0));
   }
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   return launch_finalize(a, deterministic, stream);

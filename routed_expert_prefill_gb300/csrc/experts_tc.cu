@@ -104,6 +104,8 @@ __device__ __forceinline__ __nv_bfloat162 bf2_from_half(uint16_t hb) {
 // ----------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024)
 schedule_kernel(TcParams p, SchedHdr* hdr, int4* tiles, int* units_gu, int max_tiles, int tile_max) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int bucket_cnt[16], bucket_base[16], bucket_fill[16];
   __shared__ int n_tiles_s;
   __shared__ int scan_carry;
@@ -246,6 +248,8 @@ schedule_kernel(TcParams p, SchedHdr* hdr, int4* tiles, int* units_gu, int max_t
 // Per-row shared-expert gate sigmoid(x_r . g): one warp per row.
 __global__ void shared_gate_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ g, int t, int h,
                                    float* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   if (r >= t) return;
@@ -344,6 +348,8 @@ template <bool GATEUP>
 __global__ void __launch_bounds__(KTHREADS, 1)
 expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scodes,
                    const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_sb, TcParams p) {
+  pdl_wait();
+  pdl_trigger();
   using C = Cfg<GATEUP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
@@ -746,12 +752,12 @@ cudaError_t tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, ui
 cudaError_t launch_schedule(const TcParams& p, SchedHdr* hdr, int4* tiles, int* units_gu, int max_tiles,
                             int tile_max, cudaStream_t stream) {
   MOE_LAUNCH("schedule", stream,
-             schedule_kernel<<<1, 1024, 0, stream>>>(p, hdr, tiles, units_gu, max_tiles, tile_max));
+             launch_k(schedule_kernel, 1, 1024, 0, stream, p, hdr, tiles, units_gu, max_tiles, tile_max));
   return cudaGetLastError();
 }
 
 cudaError_t launch_shared_gate(const uint16_t* x, const uint16_t* g, int t, int h, float* out, cudaStream_t stream) {
-  MOE_LAUNCH("shared_gate", stream, shared_gate_kernel<<<(t + 7) / 8, 256, 0, stream>>>(x, g, t, h, out));
+  MOE_LAUNCH("shared_gate", stream, launch_k(shared_gate_kernel, (t + 7) / 8, 256, 0, stream, x, g, t, h, out));
   return cudaGetLastError();
 }
 
@@ -841,10 +847,10 @@ cudaError_t launch_experts_tc(const ExpertsArgs& a, bool deterministic, cudaStre
     return err;
   const int grid = sm_count();
   MOE_LAUNCH("gateup_tc", stream,
-             expert_gemm_kernel<true><<<grid, KTHREADS, kernel_smem<true>(), stream>>>(tm_codes_gu, tm_scodes_gu,
+             launch_k(expert_gemm_kernel<true>, grid, KTHREADS, kernel_smem<true>(), stream, tm_codes_gu, tm_scodes_gu,
                                                                                      tm_x, tm_x, p));
   MOE_LAUNCH("down_tc", stream,
-             expert_gemm_kernel<false><<<grid, KTHREADS, kernel_smem<false>(), stream>>>(tm_codes_dn, tm_scodes_dn,
+             launch_k(expert_gemm_kernel<false>, grid, KTHREADS, kernel_smem<false>(), stream, tm_codes_dn, tm_scodes_dn,
                                                                                        tm_hg, tm_hgs, p));
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   return launch_finalize(a, deterministic, stream);

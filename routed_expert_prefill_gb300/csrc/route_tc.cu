@@ -76,6 +76,8 @@ __device__ __forceinline__ float sumsq8(uint4 u) {
 
 __global__ void __launch_bounds__(RS_WARPS * 32, 1)
 route_score_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tw, ScoreParams P) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t full[RS_STAGES], empty[RS_STAGES], accf, drain;
@@ -265,6 +267,8 @@ route_refine_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__
                     const float* __restrict__ part, int KS, int Ep, const float* __restrict__ wn2, int t, int h,
                     int E, int k, float eps, int32_t* __restrict__ idx, float* __restrict__ wout,
                     DeviceStatus* st) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int pair = warp / WPR, half = warp % WPR;  // the warps of a row
   const int row = blockIdx.x * (RF_WARPS / WPR) + pair;
@@ -412,6 +416,8 @@ __global__ void __launch_bounds__(RSM_WARPS * 32)
 route_small_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr, const float* __restrict__ rbias,
                    int t, int h, int E, int Ep, int k, float* lg, int32_t* __restrict__ idx, float* __restrict__ wout,
                    DeviceStatus* st) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int U = TR <= 2 ? 8 : (TR <= 4 ? 4 : 2);  // K spans per load round
   __shared__ int is_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -511,7 +517,7 @@ cudaError_t launch_refine_w(const uint16_t* x, const uint16_t* wr, const float* 
   if (e != cudaSuccess) return e;
   const int rows_per_cta = RF_WARPS / WPR;
   MOE_LAUNCH("route_refine", stream,
-             (route_refine_kernel<NQ, WPR><<<(t + rows_per_cta - 1) / rows_per_cta, RF_WARPS * 32, smem, stream>>>(
+             (launch_k(route_refine_kernel<NQ, WPR>, (t + rows_per_cta - 1) / rows_per_cta, RF_WARPS * 32, smem, stream, 
                  x, wr, rbias, part, R.KS, R.Ep, wn2, t, h, E, k, eps, idx, w, st)));
   return cudaGetLastError();
 }
@@ -529,7 +535,7 @@ template <int TR, int NQ>
 cudaError_t launch_small_t(const uint16_t* x, const uint16_t* wr, const float* rbias, int t, int h, int E, int k,
                            float* lg, int32_t* idx, float* w, DeviceStatus* st, cudaStream_t stream) {
   MOE_LAUNCH("route_small", stream,
-             route_small_kernel<TR, NQ><<<(E + RSM_WARPS - 1) / RSM_WARPS, RSM_WARPS * 32, 0, stream>>>(
+             launch_k(route_small_kernel<TR, NQ>, (E + RSM_WARPS - 1) / RSM_WARPS, RSM_WARPS * 32, 0, stream, 
                  x, wr, rbias, t, h, E, (E + 15) / 16 * 16, k, lg, idx, w, st));
   return cudaGetLastError();
 }
@@ -575,7 +581,7 @@ cudaError_t launch_route_tc(const uint16_t* x, const uint16_t* wr, const float* 
   if ((err = set_smem_limit_once(route_score_kernel, (int)score_smem_bytes(256))) != cudaSuccess) return err;
   ScoreParams P{t, h, E, R.Ep, R.NT, R.nkc_split, part, wn2, wr, st};
   MOE_LAUNCH("route_score", stream,
-             route_score_kernel<<<dim3(R.mt, R.ntn, R.KS), RS_WARPS * 32, smem, stream>>>(tx, tw, P));
+             launch_k(route_score_kernel, dim3(R.mt, R.ntn, R.KS), RS_WARPS * 32, smem, stream, tx, tw, P));
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   // eps: tensor-core accumulation (h 2^-21), canonical order and slice sums
   // ((h/32 + 8 + KS) 2^-23), norm rounding (factor 1 + h 2^-22).

@@ -37,6 +37,8 @@ route_topk_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w
                   const float* __restrict__ rbias, int t, int h, int E, int k,
                   int32_t* __restrict__ idx, float* __restrict__ wout,
                   float* __restrict__ logits) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) unsigned char smem[];
   const int hp = (h + KSPAN - 1) / KSPAN * KSPAN;
   const int nm = hp / KSPAN;
@@ -171,7 +173,7 @@ cudaError_t launch_route_topk(const uint16_t* x, const uint16_t* wr, const float
   if (err != cudaSuccess) return err;
   dim3 grid((t + RT_ROWS - 1) / RT_ROWS);
   MOE_LAUNCH("route_topk", stream,
-             route_topk_kernel<<<grid, RT_THREADS, smem, stream>>>(x, wr, rbias, t, h, E, k, idx, w, logits));
+             launch_k(route_topk_kernel, grid, RT_THREADS, smem, stream, x, wr, rbias, t, h, E, k, idx, w, logits));
   return cudaGetLastError();
 }
 
