@@ -241,27 +241,35 @@ __device__ __forceinline__ void dequant_packed(const uint32_t* w, __nv_bfloat162
   }
 }
 
-// Down epilogue for 16 accumulator columns: column j of the tile goes to
-// row s_row[j] of dcol (a per-feature column of the destination, pitch h),
-// scaled by s_w[j]; plain stores in deterministic mode, fp32 reductions
+// Down epilogue for 16 accumulator columns of one warp (lane = feature):
+// column j goes to row s_row[j] (-1: none) of the destination, scaled by
+// s_w[j].  The scaled values pass through stg ([16][32] floats) so that lane
+// l then owns features 4 (l % 8) .. +3 of column 4 it + l / 8; dq points at
+// this lane's first feature in destination row 0.  Plain 16-byte stores in
+// deterministic mode (every destination written once), fp32 reductions
 // otherwise.
 template <bool DET>
-__device__ __forceinline__ void down_cols16(const uint32_t (&y)[16], const int* s_row, const float* s_w,
-                                            float* dcol, int h) {
+__device__ __forceinline__ void down_cols16(const uint32_t (&y)[16], const int* s_row, const float* s_w, float* stg,
+                                            float* dq, int lane, int h) {
+  __syncwarp();  // the previous batch's reads of stg are done
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) {
-    const int4 r4 = reinterpret_cast<const int4*>(s_row)[jj];
     const float4 w4 = reinterpret_cast<const float4*>(s_w)[jj];
-    const int rr[4] = {r4.x, r4.y, r4.z, r4.w};
-    const float ww[4] = {w4.x, w4.y, w4.z, w4.w};
+    stg[(4 * jj + 0) * 32 + lane] = w4.x * __uint_as_float(y[4 * jj + 0]);
+    stg[(4 * jj + 1) * 32 + lane] = w4.y * __uint_as_float(y[4 * jj + 1]);
+    stg[(4 * jj + 2) * 32 + lane] = w4.z * __uint_as_float(y[4 * jj + 2]);
+    stg[(4 * jj + 3) * 32 + lane] = w4.w * __uint_as_float(y[4 * jj + 3]);
+  }
+  __syncwarp();
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (rr[i] >= 0) {
-        float* d = dcol + (size_t)(uint32_t)rr[i] * (uint32_t)h;
-        const float v = ww[i] * __uint_as_float(y[4 * jj + i]);
-        if (DET) *d = v;
-        else atomicAdd(d, v);
-      }
+  for (int it = 0; it < 4; ++it) {
+    const int j = it * 4 + (lane >> 3);
+    const float4 v = reinterpret_cast<const float4*>(stg + j * 32)[lane & 7];
+    const int r = s_row[j];
+    if (r >= 0) {
+      float4* d = reinterpret_cast<float4*>(dq + (size_t)(uint32_t)r * (uint32_t)h);
+      if (DET) *d = v;
+      else atomicAdd(d, v);
     }
   }
 }
@@ -311,8 +319,15 @@ struct PSmem {
   // weight of every column of the current tile
   alignas(16) int col_row[4][PT];
   alignas(16) float col_w[4][PT];
+  // epilogue: per epilogue warp, 16 columns x its 32 features (bf16 hg for
+  // gate/up, fp32 for down), the transpose that turns one value per lane
+  // into 16 bytes of consecutive features
+  alignas(16) float stage[4][GATEUP ? 16 * 16 : 16 * 32];
   uint64_t code_full[PCfg<GATEUP, PT, CP>::SC], code_empty[PCfg<GATEUP, PT, CP>::SC];
-  uint64_t a_full[PCfg<GATEUP, PT, CP>::SA], a_empty[PCfg<GATEUP, PT, CP>::SA];
+  // a_empty: per block of the stage, so that a block can be rewritten as
+  // soon as the MMAs reading its previous contents have completed
+  uint64_t a_full[PCfg<GATEUP, PT, CP>::SA];
+  uint64_t a_empty[PCfg<GATEUP, PT, CP>::SA][CP * (GATEUP ? 2 : 1)];
   uint64_t b_full[PCfg<GATEUP, PT, CP>::SB], b_empty[PCfg<GATEUP, PT, CP>::SB];
   uint64_t acc_full[PCfg<GATEUP, PT, CP>::NACC], acc_empty[PCfg<GATEUP, PT, CP>::NACC];
   uint64_t drain[2];
@@ -355,7 +370,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     }
     for (int i = 0; i < C::SA; ++i) {
       mbar_init(&S.a_full[i], 4);
-      mbar_init(&S.a_empty[i], C::NISS);
+      for (int j = 0; j < CPS * C::NMAT; ++j) mbar_init(&S.a_empty[i][j], 1);
     }
     for (int i = 0; i < SB; ++i) {
       mbar_init(&S.b_full[i], 1);
@@ -490,6 +505,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
             for (int kk = 0; kk < KC / 16; ++kk)
               mma_bf16_ta(acc + m * PT, a_st + (c * C::NMAT + m) * 32 + 8 * kk, bd + 2 * kk, idesc,
                           (kc | kk) != 0);
+            mma_commit(&S.a_empty[sa][c * C::NMAT + m]);
             bd += nm8;
             if (++sub == U.kps || kc == U.nkc - 1) {
               mma_commit(&S.b_empty[sb]);
@@ -497,7 +513,6 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
               sub = 0;
             }
           }
-          mma_commit(&S.a_empty[sa]);
         }
         if (!ok) break;
         mma_commit(&S.acc_full[ab]);
@@ -520,11 +535,10 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
       for (int st = 0; st < U.nkc / CPS; ++st, ++ast) {
         if ((int)(ast & 1) != grp) continue;
         const int sc = ast % C::SC, sa = ast % C::SA;
-        // warp-uniform verdict: the TMEM stores below are .sync.aligned, so
+        const uint32_t a_par = ((ast / C::SA) & 1) ^ 1;
+        // warp-uniform verdicts: the TMEM stores below are .sync.aligned, so
         // no lane may leave the loop alone when a wait gives up
-        const bool got = mbar_wait(&S.code_full[sc], (ast / C::SC) & 1, abort, WAIT_NS) &&
-                         mbar_wait(&S.a_empty[sa], ((ast / C::SA) & 1) ^ 1, abort, WAIT_NS);
-        if (!__all_sync(0xFFFFFFFFu, got)) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.code_full[sc], (ast / C::SC) & 1, abort, WAIT_NS))) {
           if (lane == 0) note_timeout(p.status, abort, GATEUP ? 36 : 46);
           ok = false;
           break;
@@ -532,6 +546,12 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         tc_fence_after();
 #pragma unroll
         for (int cm = 0; cm < CPS * C::NMAT; ++cm) {
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.a_empty[sa][cm], a_par, abort, WAIT_NS))) {
+            if (lane == 0) note_timeout(p.status, abort, GATEUP ? 38 : 48);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
           const uint8_t* blk = c_s + sc * C::C_STAGE + cm * QB;
           const __nv_bfloat16 sv = reinterpret_cast<const __nv_bfloat16*>(blk + 4096)[o];
           const __nv_bfloat16 bv = reinterpret_cast<const __nv_bfloat16*>(blk + 4096 + 256)[o];
@@ -541,6 +561,10 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
           uint32_t r[32];
           dequant_packed<8>(wd, __halves2bfloat162(sv, sv), __halves2bfloat162(bv, bv), r);
           tmem_st<32>(lane_base + C::A_COL + sa * C::A_STAGE + cm * 32, r);
+        }
+        if (!ok) {
+          tmem_st_wait();
+          break;
         }
         tmem_st_wait();
         tc_fence_before();
@@ -573,7 +597,6 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
       const PUnit U = decode_punit<GATEUP, CP, C::B_STAGE>(p, u);
       const int ab = uit % C::NACC;
-      const int feat = U.f0 + o;
       // down: this warp's copy of the tile's destination rows and weights.
       // Deterministic mode writes routed columns to their own list position
       // (weights applied when the slots are summed) and the shared expert
@@ -618,36 +641,57 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         // image (no unit-sized register buffer, so the 16 independent silu
         // evaluations of a step overlap); the accumulator is released once
         // the last store has been issued
-        uint8_t* img = reinterpret_cast<uint8_t*>(p.hg + (size_t)U.pad * P.kmax) + (size_t)(feat / 64) * U.Nm * 128;
-        const int c8 = (feat % 64) / 8, e8 = feat % 8;
-        for (int c = 0; c * 16 < U.Nm; ++c) {
+        // The 16 x 32 bf16 values of a step pass through this warp's staging
+        // buffer, after which lane l stores the 16-byte chunk (4 (q % 2) +
+        // l % 4) of image rows l / 4 and 8 + l / 4.
+        uint8_t* img = reinterpret_cast<uint8_t*>(p.hg + (size_t)U.pad * P.kmax) + (size_t)(U.f0 / 64 + q / 2) * U.Nm * 128;
+        __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(S.stage[q]);
+        const int cc = (q & 1) * 4 + (lane & 3);
+        const int nb = U.Nm / 16;
+        for (int c = 0; c < nb; ++c) {
           uint32_t g[16], v[16];
           tmem_ld16(acc + c * 16, g);
           tmem_ld16(acc + PT + c * 16, v);
           tmem_ld_wait();
-          float hv[16];
+          if (c == nb - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
+          }
+          __syncwarp();  // the previous step's reads of the staging buffer are done
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            hv[j] = c * 16 + j < U.n ? silu_mul(__uint_as_float(g[j]), __uint_as_float(v[j])) : 0.f;
+            stg[j * 32 + lane] = __float2bfloat16_rn(
+                c * 16 + j < U.n ? silu_mul(__uint_as_float(g[j]), __uint_as_float(v[j])) : 0.f);
+          __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            *reinterpret_cast<__nv_bfloat16*>(img + sw128_off(c * 16 + j, c8) + e8 * 2) = __float2bfloat16_rn(hv[j]);
+          for (int half = 0; half < 2; ++half) {
+            const int j = half * 8 + (lane >> 2);
+            const uint4 hv = reinterpret_cast<const uint4*>(stg + j * 32)[lane & 3];
+            *reinterpret_cast<uint4*>(img + sw128_off(c * 16 + j, cc)) = hv;
+          }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
       } else {
-        float* dcol = (to_list ? p.ybuf : p.acc) + feat;
-        for (int c = 0; c * 16 < U.Nm; ++c) {
+        // 16 columns at a time, transposed through this warp's staging
+        // buffer: afterwards each lane holds four consecutive features of one
+        // destination row, so the scatter-add issues 16-byte reductions (a
+        // quarter of the requests of one float per lane, each four times
+        // wider).  The accumulator is released after its last load.
+        float* dq = (to_list ? p.ybuf : p.acc) + U.f0 + q * 32 + (lane & 7) * 4;
+        float* stg = S.stage[q];
+        const int nb = U.Nm / 16;
+        for (int c = 0; c < nb; ++c) {
           uint32_t y[16];
           tmem_ld16(acc + c * 16, y);
           tmem_ld_wait();
-          if (p.deterministic) down_cols16<true>(y, &S.col_row[q][c * 16], &S.col_w[q][c * 16], dcol, h);
-          else down_cols16<false>(y, &S.col_row[q][c * 16], &S.col_w[q][c * 16], dcol, h);
+          if (c == nb - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
+          }
+          if (p.deterministic) down_cols16<true>(y, &S.col_row[q][c * 16], &S.col_w[q][c * 16], stg, dq, lane, h);
+          else down_cols16<false>(y, &S.col_row[q][c * 16], &S.col_w[q][c * 16], stg, dq, lane, h);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
       }
     }
   }
