@@ -54,10 +54,16 @@ constexpr int KC = 64;      // K per chunk = one quantisation group
 constexpr int QB = 4096 + 256 + 256;  // one packed 128 x 64 block
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
-constexpr int W_CODE = 0, W_MMA = 1, W_DQ0 = 2, W_B = 10, W_EPI0 = 11, W_MMA2 = 15;
-// 0 code, 1 MMA (gate / down), 2-9 dequant (two groups), 10 B, 11-14 epilogue, 15 MMA (up)
-constexpr int KWARPS = 16;
+constexpr int W_CODE = 0, W_MMA = 1, W_DQ0 = 2, W_B = 10, W_EPI0 = 11, W_MMA2 = 15, W_EPI1 = 16;
+// 0 code, 1 MMA (gate / down), 2-9 dequant (two groups), 10 B, 11-14
+// epilogue, 15 MMA (up); launched with 20 warps, 16-19 form a second
+// epilogue group that takes alternate 16-column steps.  The second group
+// pays where the epilogue of a unit is long against its main loop
+// (128-row tiles; for down, a short inter), and otherwise only takes issue
+// slots from the dequantisation warps.
+constexpr int KWARPS = 20;
 constexpr int KTHREADS = KWARPS * 32;
+constexpr int KTHREADS_1 = 16 * 32;
 constexpr int B_RING = 131072;        // bytes of token-tile stages (see PCfg::SB, PCfg::B_STAGE)
 constexpr int CPS_DEFAULT = 2;        // K chunks per code stage and per A stage (see PCfg)
 
@@ -274,6 +280,14 @@ __device__ __forceinline__ void down_cols16(const uint32_t (&y)[16], const int* 
   }
 }
 
+// This warp has issued its last load of an accumulator buffer: hand it back
+// to the MMA issuer.
+__device__ __forceinline__ void release_acc(uint64_t* bar, int lane) {
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
 struct PUnit {
   int e, start, n, Nm, f0, nkc, kps, pad;
   bool shared;
@@ -317,17 +331,14 @@ template <bool GATEUP, int PT, int CP>
 struct PSmem {
   // down epilogue: per epilogue warp, the destination row (-1: skip) and
   // weight of every column of the current tile
-  alignas(16) int col_row[4][PT];
-  alignas(16) float col_w[4][PT];
+  alignas(16) int col_row[GATEUP ? 1 : 8][PT];
+  alignas(16) float col_w[GATEUP ? 1 : 8][PT];
   // epilogue: per epilogue warp, 16 columns x its 32 features (bf16 hg for
   // gate/up, fp32 for down), the transpose that turns one value per lane
   // into 16 bytes of consecutive features
-  alignas(16) float stage[4][GATEUP ? 16 * 16 : 16 * 32];
+  alignas(16) float stage[8][GATEUP ? 16 * 16 : 16 * 32];
   uint64_t code_full[PCfg<GATEUP, PT, CP>::SC], code_empty[PCfg<GATEUP, PT, CP>::SC];
-  // a_empty: per block of the stage, so that a block can be rewritten as
-  // soon as the MMAs reading its previous contents have completed
-  uint64_t a_full[PCfg<GATEUP, PT, CP>::SA];
-  uint64_t a_empty[PCfg<GATEUP, PT, CP>::SA][CP * (GATEUP ? 2 : 1)];
+  uint64_t a_full[PCfg<GATEUP, PT, CP>::SA], a_empty[PCfg<GATEUP, PT, CP>::SA];
   uint64_t b_full[PCfg<GATEUP, PT, CP>::SB], b_empty[PCfg<GATEUP, PT, CP>::SB];
   uint64_t acc_full[PCfg<GATEUP, PT, CP>::NACC], acc_empty[PCfg<GATEUP, PT, CP>::NACC];
   uint64_t drain[2];
@@ -356,11 +367,12 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
   PSmem<GATEUP, PT, CP>& S = *reinterpret_cast<PSmem<GATEUP, PT, CP>*>(c_s + C::SC * C::C_STAGE);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = p.h;
+  const int egroups = blockDim.x > KTHREADS_1 ? 2 : 1;  // epilogue warpgroups
 
   if (GATEUP && (!p.deterministic || p.Is == 0)) {
     float4* acc4 = reinterpret_cast<float4*>(p.acc);
     const size_t n4 = (size_t)p.t * h / 4;
-    for (size_t i = (size_t)blockIdx.x * KTHREADS + threadIdx.x; i < n4; i += (size_t)gridDim.x * KTHREADS)
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x)
       acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   if (threadIdx.x == 0) {
@@ -370,7 +382,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     }
     for (int i = 0; i < C::SA; ++i) {
       mbar_init(&S.a_full[i], 4);
-      for (int j = 0; j < CPS * C::NMAT; ++j) mbar_init(&S.a_empty[i][j], 1);
+      mbar_init(&S.a_empty[i], C::NISS);
     }
     for (int i = 0; i < SB; ++i) {
       mbar_init(&S.b_full[i], 1);
@@ -378,7 +390,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     }
     for (int i = 0; i < C::NACC; ++i) {
       mbar_init(&S.acc_full[i], C::NISS);
-      mbar_init(&S.acc_empty[i], 4);
+      mbar_init(&S.acc_empty[i], 4 * egroups);
     }
     mbar_init(&S.drain[0], 1);
     mbar_init(&S.drain[1], 1);
@@ -505,7 +517,6 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
             for (int kk = 0; kk < KC / 16; ++kk)
               mma_bf16_ta(acc + m * PT, a_st + (c * C::NMAT + m) * 32 + 8 * kk, bd + 2 * kk, idesc,
                           (kc | kk) != 0);
-            mma_commit(&S.a_empty[sa][c * C::NMAT + m]);
             bd += nm8;
             if (++sub == U.kps || kc == U.nkc - 1) {
               mma_commit(&S.b_empty[sb]);
@@ -513,6 +524,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
               sub = 0;
             }
           }
+          mma_commit(&S.a_empty[sa]);
         }
         if (!ok) break;
         mma_commit(&S.acc_full[ab]);
@@ -535,10 +547,11 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
       for (int st = 0; st < U.nkc / CPS; ++st, ++ast) {
         if ((int)(ast & 1) != grp) continue;
         const int sc = ast % C::SC, sa = ast % C::SA;
-        const uint32_t a_par = ((ast / C::SA) & 1) ^ 1;
-        // warp-uniform verdicts: the TMEM stores below are .sync.aligned, so
+        // warp-uniform verdict: the TMEM stores below are .sync.aligned, so
         // no lane may leave the loop alone when a wait gives up
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.code_full[sc], (ast / C::SC) & 1, abort, WAIT_NS))) {
+        const bool got = mbar_wait(&S.code_full[sc], (ast / C::SC) & 1, abort, WAIT_NS) &&
+                         mbar_wait(&S.a_empty[sa], ((ast / C::SA) & 1) ^ 1, abort, WAIT_NS);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
           if (lane == 0) note_timeout(p.status, abort, GATEUP ? 36 : 46);
           ok = false;
           break;
@@ -546,12 +559,6 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         tc_fence_after();
 #pragma unroll
         for (int cm = 0; cm < CPS * C::NMAT; ++cm) {
-          if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.a_empty[sa][cm], a_par, abort, WAIT_NS))) {
-            if (lane == 0) note_timeout(p.status, abort, GATEUP ? 38 : 48);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
           const uint8_t* blk = c_s + sc * C::C_STAGE + cm * QB;
           const __nv_bfloat16 sv = reinterpret_cast<const __nv_bfloat16*>(blk + 4096)[o];
           const __nv_bfloat16 bv = reinterpret_cast<const __nv_bfloat16*>(blk + 4096 + 256)[o];
@@ -561,10 +568,6 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
           uint32_t r[32];
           dequant_packed<8>(wd, __halves2bfloat162(sv, sv), __halves2bfloat162(bv, bv), r);
           tmem_st<32>(lane_base + C::A_COL + sa * C::A_STAGE + cm * 32, r);
-        }
-        if (!ok) {
-          tmem_st_wait();
-          break;
         }
         tmem_st_wait();
         tc_fence_before();
@@ -588,9 +591,14 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
       if (!ok) break;
       bbase += (uint32_t)((U.nkc + U.kps - 1) / U.kps);
     }
-  } else if (warp < W_MMA2) {
-    // ------------------------------------------------------------ epilogue warpgroup
+  } else if (warp < W_MMA2 || warp >= W_EPI1) {
+    // ------------------------------------------------------------ epilogue: two warpgroups
+    // With two groups, warp pairs share a TMEM lane quarter and group `half`
+    // takes the 16-column steps c = half, half + 2, ...  Each warp releases
+    // the accumulator after its own last load (at once when it has no step).
     const int q = warp & 3;
+    const int half = warp >= W_EPI1 ? 1 : 0;
+    const int ew = half * 4 + q;  // epilogue warp index: staging buffer, row copy
     const int o = q * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t uit = 0;
@@ -624,8 +632,8 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
               if (r < 0 || r >= p.t) bad_row = true, r = -1;
             }
           }
-          S.col_row[q][col] = r;
-          S.col_w[q][col] = wv;
+          S.col_row[ew][col] = r;
+          S.col_w[ew][col] = wv;
         }
         if (bad_row) raise_flag(p.status, FLAG_BAD_ROW);
         __syncwarp();
@@ -645,19 +653,16 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         // buffer, after which lane l stores the 16-byte chunk (4 (q % 2) +
         // l % 4) of image rows l / 4 and 8 + l / 4.
         uint8_t* img = reinterpret_cast<uint8_t*>(p.hg + (size_t)U.pad * P.kmax) + (size_t)(U.f0 / 64 + q / 2) * U.Nm * 128;
-        __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(S.stage[q]);
+        __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(S.stage[ew]);
         const int cc = (q & 1) * 4 + (lane & 3);
         const int nb = U.Nm / 16;
-        for (int c = 0; c < nb; ++c) {
+        if (half >= nb) release_acc(&S.acc_empty[ab], lane);
+        for (int c = half; c < nb; c += egroups) {
           uint32_t g[16], v[16];
           tmem_ld16(acc + c * 16, g);
           tmem_ld16(acc + PT + c * 16, v);
           tmem_ld_wait();
-          if (c == nb - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
-          }
+          if (c + egroups >= nb) release_acc(&S.acc_empty[ab], lane);
           __syncwarp();  // the previous step's reads of the staging buffer are done
 #pragma unroll
           for (int j = 0; j < 16; ++j)
@@ -678,19 +683,16 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         // quarter of the requests of one float per lane, each four times
         // wider).  The accumulator is released after its last load.
         float* dq = (to_list ? p.ybuf : p.acc) + U.f0 + q * 32 + (lane & 7) * 4;
-        float* stg = S.stage[q];
+        float* stg = S.stage[ew];
         const int nb = U.Nm / 16;
-        for (int c = 0; c < nb; ++c) {
+        if (half >= nb) release_acc(&S.acc_empty[ab], lane);
+        for (int c = half; c < nb; c += egroups) {
           uint32_t y[16];
           tmem_ld16(acc + c * 16, y);
           tmem_ld_wait();
-          if (c == nb - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
-          }
-          if (p.deterministic) down_cols16<true>(y, &S.col_row[q][c * 16], &S.col_w[q][c * 16], stg, dq, lane, h);
-          else down_cols16<false>(y, &S.col_row[q][c * 16], &S.col_w[q][c * 16], stg, dq, lane, h);
+          if (c + egroups >= nb) release_acc(&S.acc_empty[ab], lane);
+          if (p.deterministic) down_cols16<true>(y, &S.col_row[ew][c * 16], &S.col_w[ew][c * 16], stg, dq, lane, h);
+          else down_cols16<false>(y, &S.col_row[ew][c * 16], &S.col_w[ew][c * 16], stg, dq, lane, h);
         }
       }
     }
@@ -731,10 +733,12 @@ cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, const uint
 
 template <bool GATEUP, int PT, int CP>
 cudaError_t launch_packed_gemm(const PParams& P, cudaStream_t stream) {
+  const bool two_epi = PT == 128 && (GATEUP || max(P.p.I, P.p.Is) <= 1024);
   cudaError_t err = set_smem_limit_once(packed_gemm_kernel<GATEUP, PT, CP>, (int)psmem_bytes<GATEUP, PT, CP>());
   if (err != cudaSuccess) return err;
   MOE_LAUNCH(GATEUP ? "gateup_packed" : "down_packed", stream,
-             (launch_k(packed_gemm_kernel<GATEUP, PT, CP>, sm_count(), KTHREADS, psmem_bytes<GATEUP, PT, CP>(), stream, P)));
+             (launch_k(packed_gemm_kernel<GATEUP, PT, CP>, sm_count(), two_epi ? KTHREADS : KTHREADS_1,
+                       psmem_bytes<GATEUP, PT, CP>(), stream, P)));
   return cudaGetLastError();
 }
 
