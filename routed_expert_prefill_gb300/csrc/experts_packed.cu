@@ -88,6 +88,13 @@ struct PCfg {
   // 128 rows needs it (every A stage must read a single B stage)
   static constexpr int B_STAGE = CP * PT * 128 > 32768 ? 65536 : 32768;
   static constexpr int SB = B_RING / B_STAGE;
+  // A-ring slots released block by block (an empty barrier per block,
+  // committed after that block's MMAs) rather than per stage: lets a
+  // dequantisation group start rewriting a slot while the tensor pipe still
+  // reads its later blocks.  Pays for the extra waits and commits on the
+  // gate/up pass with 128-row tiles only.
+  static constexpr bool BLK_REL = GATEUP && PT == 128;
+  static constexpr int NREL = BLK_REL ? CPS * NMAT : 1;  // empty barriers per slot
 };
 
 __host__ __device__ inline size_t gu_bytes(int h, int I) { return (size_t)(I / 128) * (h / KC) * 2 * QB; }
@@ -338,7 +345,8 @@ struct PSmem {
   // into 16 bytes of consecutive features
   alignas(16) float stage[8][GATEUP ? 16 * 16 : 16 * 32];
   uint64_t code_full[PCfg<GATEUP, PT, CP>::SC], code_empty[PCfg<GATEUP, PT, CP>::SC];
-  uint64_t a_full[PCfg<GATEUP, PT, CP>::SA], a_empty[PCfg<GATEUP, PT, CP>::SA];
+  uint64_t a_full[PCfg<GATEUP, PT, CP>::SA];
+  uint64_t a_empty[PCfg<GATEUP, PT, CP>::SA][PCfg<GATEUP, PT, CP>::NREL];
   uint64_t b_full[PCfg<GATEUP, PT, CP>::SB], b_empty[PCfg<GATEUP, PT, CP>::SB];
   uint64_t acc_full[PCfg<GATEUP, PT, CP>::NACC], acc_empty[PCfg<GATEUP, PT, CP>::NACC];
   uint64_t drain[2];
@@ -382,7 +390,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     }
     for (int i = 0; i < C::SA; ++i) {
       mbar_init(&S.a_full[i], 4);
-      mbar_init(&S.a_empty[i], C::NISS);
+      for (int j = 0; j < C::NREL; ++j) mbar_init(&S.a_empty[i][j], C::BLK_REL ? 1 : C::NISS);
     }
     for (int i = 0; i < SB; ++i) {
       mbar_init(&S.b_full[i], 1);
@@ -517,6 +525,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
             for (int kk = 0; kk < KC / 16; ++kk)
               mma_bf16_ta(acc + m * PT, a_st + (c * C::NMAT + m) * 32 + 8 * kk, bd + 2 * kk, idesc,
                           (kc | kk) != 0);
+            if constexpr (C::BLK_REL) mma_commit(&S.a_empty[sa][c * C::NMAT + m]);
             bd += nm8;
             if (++sub == U.kps || kc == U.nkc - 1) {
               mma_commit(&S.b_empty[sb]);
@@ -524,7 +533,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
               sub = 0;
             }
           }
-          mma_commit(&S.a_empty[sa]);
+          if constexpr (!C::BLK_REL) mma_commit(&S.a_empty[sa][0]);
         }
         if (!ok) break;
         mma_commit(&S.acc_full[ab]);
@@ -547,10 +556,11 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
       for (int st = 0; st < U.nkc / CPS; ++st, ++ast) {
         if ((int)(ast & 1) != grp) continue;
         const int sc = ast % C::SC, sa = ast % C::SA;
-        // warp-uniform verdict: the TMEM stores below are .sync.aligned, so
+        const uint32_t a_par = ((ast / C::SA) & 1) ^ 1;
+        // warp-uniform verdicts: the TMEM stores below are .sync.aligned, so
         // no lane may leave the loop alone when a wait gives up
         const bool got = mbar_wait(&S.code_full[sc], (ast / C::SC) & 1, abort, WAIT_NS) &&
-                         mbar_wait(&S.a_empty[sa], ((ast / C::SA) & 1) ^ 1, abort, WAIT_NS);
+                         (C::BLK_REL || mbar_wait(&S.a_empty[sa][0], a_par, abort, WAIT_NS));
         if (!__all_sync(0xFFFFFFFFu, got)) {
           if (lane == 0) note_timeout(p.status, abort, GATEUP ? 36 : 46);
           ok = false;
@@ -559,6 +569,14 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         tc_fence_after();
 #pragma unroll
         for (int cm = 0; cm < CPS * C::NMAT; ++cm) {
+          if constexpr (C::BLK_REL) {
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.a_empty[sa][cm], a_par, abort, WAIT_NS))) {
+              if (lane == 0) note_timeout(p.status, abort, 38);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
           const uint8_t* blk = c_s + sc * C::C_STAGE + cm * QB;
           const __nv_bfloat16 sv = reinterpret_cast<const __nv_bfloat16*>(blk + 4096)[o];
           const __nv_bfloat16 bv = reinterpret_cast<const __nv_bfloat16*>(blk + 4096 + 256)[o];
@@ -568,6 +586,10 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
           uint32_t r[32];
           dequant_packed<8>(wd, __halves2bfloat162(sv, sv), __halves2bfloat162(bv, bv), r);
           tmem_st<32>(lane_base + C::A_COL + sa * C::A_STAGE + cm * 32, r);
+        }
+        if (!ok) {
+          tmem_st_wait();
+          break;
         }
         tmem_st_wait();
         tc_fence_before();

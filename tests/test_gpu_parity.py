@@ -338,6 +338,24 @@ def test_one_expert_takes_every_row_and_shared_gate(moe, flags):
     _check_out(res["out"], ref["out"])
 
 
+@pytest.mark.parametrize("inter", [256, 1280])
+@pytest.mark.parametrize("det", [False, True])
+def test_packed_128_row_tiles(moe, inter, det):
+    """About 250 rows per expert: 128-row tiles with ragged last tiles (down
+    runs two epilogue warpgroups at inter 256, one at 1280; gate/up two)."""
+    w = synth.Workload("t128", 1000, 256, inter, 8, 2, 256, 41 + inter)
+    inp = synth.make_inputs(w)
+    ref = O.moe_forward(inp, w.k, w.h, w.inter, w.shared_inter)
+    flags = moe.MOE_PACKED_WEIGHTS | (moe.MOE_DETERMINISTIC if det else 0)
+    res, status = _run(moe, w, inp, flags)
+    assert status == 0
+    np.testing.assert_array_equal(res["idx"].cpu().numpy(), ref["idx"])
+    counts = np.diff(res["csr"].offsets.cpu().numpy())
+    assert counts.max() > 128 and np.any(counts % 128 > 0)
+    _check_csr_against(res["csr"], res["idx"], res["w"], w.E)
+    _check_out(res["out"], ref["out"])
+
+
 def test_bad_expert_ids_are_flagged_and_dropped(moe):
     t, k, E = 8, 2, 4
     idx = torch.tensor([[0, 1], [2, 9], [3, 0], [-1, 2], [1, 2], [0, 3], [1, 0], [2, 3]], dtype=torch.int32,
