@@ -875,9 +875,11 @@ cudaError_t launch_experts_gemv(const ExpertsArgs& a, bool packed, bool determin
   const int kmax = a.I > a.Is ? a.I : a.Is;
   if (packed && a.t <= GV_RB && a.gvpart) {
     // K slices: enough units to occupy the GPU when few experts are active
+    // (measured: 8 slices at 48 gate/up units beat 2; at 96 units one slice
+    // beats four, the per-CTA fixed cost outweighing the better spread)
     const int units = nact * (a.I / 128);
     const int nkc = a.h / GV_KC;
-    int KS = units < 20 ? 8 : units < 40 ? 4 : units < 80 ? 2 : 1;
+    int KS = units < 60 ? 8 : units < 80 ? 2 : 1;
     while (KS > 1 && (nkc % KS || !gv2_fits(NBr, a.h, kmax, KS))) KS >>= 1;
     if (gv2_fits(NBr, a.h, kmax, KS)) {
       Gv2Params Q{P, a.gvpart, KS, kmax};
