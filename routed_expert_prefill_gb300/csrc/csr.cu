@@ -13,9 +13,10 @@
 //   2. csr_scan (one block): per expert, the exclusive prefix of the chunk
 //      counts; then the exclusive prefix over experts gives offsets.
 //   3. csr_scatter: position = offsets[e] + chunk prefix + rank.
-// Up to CSR_SMALL_CHUNKS chunks (decode-shaped chunks) run as one
-// block that walks the chunks in order with running per-expert counts, scans
-// them and scatters: one launch instead of three, the same positions.
+// Up to CSR_SMALL_CHUNKS chunks run as one block that walks the chunks in
+// order with running per-expert counts, scans them and scatters: one launch
+// instead of three, the same positions.  Up to 256 pairs (decode steps) take
+// a lighter one-block kernel (csr_tiny_kernel).
 #include "common.cuh"
 
 namespace moe {
@@ -153,6 +154,89 @@ __device__ __forceinline__ int block_excl_scan_1024(int v, int* warp_sums, int* 
   return warp_sums[warp] + incl - v;
 }
 
+// Up to CSR_TINY pairs (decode steps): one 256-thread block.  Per-expert
+// counts by shared atomics, one exclusive scan over the experts (four per
+// thread), and each pair's rank inside its expert by counting the earlier
+// pairs of the same expert: the same stable order as the chunked kernels.
+constexpr int CSR_TINY = 256;
+
+__global__ void __launch_bounds__(CSR_TINY, 1)
+csr_tiny_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w, int n, int k, int E,
+                int32_t* __restrict__ offsets, int32_t* __restrict__ rows, float* __restrict__ weights,
+                int32_t* __restrict__ slot_of, DeviceStatus* st) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ int start[];  // [E]: the expert's count, then its list start
+  __shared__ int es[CSR_TINY];
+  __shared__ int warp_sums[CSR_TINY / 32 + 1];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < E; i += CSR_TINY) start[i] = 0;
+  int e = -1;
+  if (tid < n) {
+    e = idx[tid];
+    if (e < 0 || e >= E) {
+      raise_flag(st, FLAG_BAD_EXPERT);
+      e = -1;
+    }
+  }
+  es[tid] = e;
+  __syncthreads();
+  if (e >= 0) atomicAdd(&start[e], 1);
+  __syncthreads();
+  // exclusive scan over the experts; thread tid owns experts 4 tid .. 4 tid + 3
+  int c[4], sum = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int ex = 4 * tid + j;
+    c[j] = ex < E ? start[ex] : 0;
+    sum += c[j];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int sv = lane < CSR_TINY / 32 ? warp_sums[lane] : 0;
+    int si = sv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, si, o);
+      if (lane >= o) si += y;
+    }
+    if (lane < CSR_TINY / 32) warp_sums[lane] = si - sv;
+    if (lane == CSR_TINY / 32 - 1) warp_sums[CSR_TINY / 32] = si;
+  }
+  __syncthreads();
+  int run = warp_sums[warp] + incl - sum;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int ex = 4 * tid + j;
+    if (ex < E) {
+      start[ex] = run;
+      offsets[ex] = run;
+    }
+    run += c[j];
+  }
+  if (tid == 0) offsets[E] = warp_sums[CSR_TINY / 32];
+  __syncthreads();
+  if (tid < n) {
+    if (e < 0) {
+      slot_of[tid] = -1;
+    } else {
+      int r = 0;
+      for (int q = 0; q < tid; ++q) r += es[q] == e;
+      const int pos = start[e] + r;
+      rows[pos] = tid / k;
+      weights[pos] = w[tid];
+      slot_of[tid] = pos;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(CSR_CHUNK, 1)
 csr_small_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w, int n, int k, int E,
                  int32_t* __restrict__ offsets, int32_t* __restrict__ rows, float* __restrict__ weights,
@@ -244,6 +328,12 @@ cudaError_t launch_build_csr(const int32_t* idx, const float* w, int t, int k, i
   int32_t* counts = reinterpret_cast<int32_t*>(ws + L.csr_counts);
   int32_t* base = reinterpret_cast<int32_t*>(ws + L.csr_base);
   DeviceStatus* st = reinterpret_cast<DeviceStatus*>(ws + L.status);
+  if (n <= CSR_TINY && E <= 4 * CSR_TINY) {
+    MOE_LAUNCH("csr_tiny", stream,
+               launch_k(csr_tiny_kernel, 1, CSR_TINY, (size_t)E * 4, stream, idx, w, n, k, E, csr.offsets, csr.rows,
+                        csr.weights, csr.slot_of, st));
+    return cudaGetLastError();
+  }
   if (nchunks <= CSR_SMALL_CHUNKS) {
     const size_t smem = (size_t)E * (CSR_CHUNK / 32) * 6 + (size_t)E * 4;
     cudaError_t err =

@@ -514,15 +514,6 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_gateup(Gv2Params Q) {
   float* xs = reinterpret_cast<float*>(ring + GV2_RING);
   float* xch = xs + NB * nkc * GV_KC;  // [128][NB][2] halves exchange
   const int kw = nkc * GV_KC;
-  for (int v = threadIdx.x; v < nb * kw / 8; v += GV2_THREADS) {
-    const int r = v / (kw / 8), c = v % (kw / 8);
-    const int row = R.row[r];
-    uint4 val = make_uint4(0, 0, 0, 0);
-    if (row >= 0) val = __ldg(reinterpret_cast<const uint4*>(P.x + (size_t)row * P.h + kc0 * GV_KC) + c);
-    float4* d = reinterpret_cast<float4*>(xs + r * kw + c * 8);
-    d[0] = make_float4(bf16lo(val.x), bf16hi(val.x), bf16lo(val.y), bf16hi(val.y));
-    d[1] = make_float4(bf16lo(val.z), bf16hi(val.z), bf16lo(val.w), bf16hi(val.w));
-  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < ST; ++i) {
       mbar_init(&full[i], 1);
@@ -540,6 +531,8 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_gateup(Gv2Params Q) {
 #pragma unroll
   for (int r = 0; r < NB; ++r) g[r] = u[r] = 0.f;
   const int o = threadIdx.x & 127, hf = (threadIdx.x >> 7) & 1;
+  // The producer warp starts the weight stream at once; the consumer warps
+  // meanwhile stage the token rows (L2 reads) and meet at a named barrier.
   if (warp == GV2_CONS / 32) {
     if (lane == 0) {
       bool armed[ST];
@@ -565,6 +558,16 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_gateup(Gv2Params Q) {
           }
     }
   } else {
+    for (int v = threadIdx.x; v < nb * kw / 8; v += GV2_CONS) {
+      const int r = v / (kw / 8), c = v % (kw / 8);
+      const int row = R.row[r];
+      uint4 val = make_uint4(0, 0, 0, 0);
+      if (row >= 0) val = __ldg(reinterpret_cast<const uint4*>(P.x + (size_t)row * P.h + kc0 * GV_KC) + c);
+      float4* d = reinterpret_cast<float4*>(xs + r * kw + c * 8);
+      d[0] = make_float4(bf16lo(val.x), bf16hi(val.x), bf16lo(val.y), bf16hi(val.y));
+      d[1] = make_float4(bf16lo(val.z), bf16hi(val.z), bf16lo(val.w), bf16hi(val.w));
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(GV2_CONS) : "memory");  // consumer warps only
     for (int i = 0; i < nkc; ++i) {
       const int s = i % ST;
       // every lane waits (and so observes the copy); the verdict is made
@@ -688,16 +691,6 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_down(Gv2Params Q) {
     uint16_t* hs = reinterpret_cast<uint16_t*>(ring + GV2_RING);  // [NB][Iu] bf16
     float* xch = reinterpret_cast<float*>(hs + NB * Iu);
     const size_t pstride = (size_t)(P.t * P.k + P.t) * 2 * Q.kmax;
-    for (int v = threadIdx.x; v < nb * Iu; v += GV2_THREADS) {
-      const int r = v / Iu, c = v % Iu;
-      const float* pp = Q.part + (size_t)R.pos[r] * 2 * Q.kmax + c;
-      float gs = 0.f, us = 0.f;
-      for (int s = 0; s < Q.KS; ++s) {
-        gs += pp[s * pstride];
-        us += pp[s * pstride + Q.kmax];
-      }
-      hs[r * Iu + c] = R.row[r] < 0 ? 0 : f2bf(silu_mul_fast(gs, us));
-    }
     if (threadIdx.x == 0) {
       for (int i = 0; i < ST; ++i) {
         mbar_init(&full[i], 1);
@@ -715,6 +708,9 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_down(Gv2Params Q) {
 #pragma unroll
     for (int r = 0; r < NB; ++r) y[r] = 0.f;
     const int o = threadIdx.x & 127, hf = (threadIdx.x >> 7) & 1;
+    // The producer warp starts the weight stream at once; the consumer warps
+    // meanwhile form hg from the K-slice partial sums and meet at a named
+    // barrier.
     if (warp == GV2_CONS / 32) {
       if (lane == 0) {
         bool armed[ST];
@@ -740,6 +736,17 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_down(Gv2Params Q) {
             }
       }
     } else {
+      for (int v = threadIdx.x; v < nb * Iu; v += GV2_CONS) {
+        const int r = v / Iu, c = v % Iu;
+        const float* pp = Q.part + (size_t)R.pos[r] * 2 * Q.kmax + c;
+        float gs = 0.f, us = 0.f;
+        for (int s = 0; s < Q.KS; ++s) {
+          gs += pp[s * pstride];
+          us += pp[s * pstride + Q.kmax];
+        }
+        hs[r * Iu + c] = R.row[r] < 0 ? 0 : f2bf(silu_mul_fast(gs, us));
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(GV2_CONS) : "memory");  // consumer warps only
       for (int i = 0; i < nkc; ++i) {
         const int s = i % ST;
         // every lane waits (and so observes the copy); the verdict is made
