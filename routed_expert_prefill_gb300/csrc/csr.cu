@@ -337,7 +337,7 @@ cudaError_t launch_build_csr(const int32_t* idx, const float* w, int t, int k, i
   if (nchunks <= CSR_SMALL_CHUNKS) {
     const size_t smem = (size_t)E * (CSR_CHUNK / 32) * 6 + (size_t)E * 4;
     cudaError_t err =
-        cudaFuncSetAttribute(csr_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        set_smem_limit_once(csr_small_kernel, (int)smem);
     if (err != cudaSuccess) return err;
     MOE_LAUNCH("csr_small", stream,
                launch_k(csr_small_kernel, 1, CSR_CHUNK, smem, stream, idx, w, n, k, E, csr.offsets, csr.rows, csr.weights,
@@ -345,7 +345,7 @@ cudaError_t launch_build_csr(const int32_t* idx, const float* w, int t, int k, i
     return cudaGetLastError();
   }
   const size_t smem = (size_t)E * (CSR_CHUNK / 32) * 4;
-  cudaError_t err = cudaFuncSetAttribute(csr_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t err = set_smem_limit_once(csr_rank_kernel, (int)smem);
   if (err != cudaSuccess) return err;
   MOE_LAUNCH("csr_rank", stream,
              launch_k(csr_rank_kernel, nchunks, CSR_CHUNK, smem, stream, idx, n, E, rank, counts, st));

@@ -805,9 +805,9 @@ cudaError_t launch_gv2(const Gv2Params& Q, int nact, cudaStream_t stream) {
   const GvParams& P = Q.p;
   const size_t sg = gv2_smem_gateup<NB>(P.h, Q.KS), sd = gv2_smem_down<NB>(Q.kmax);
   cudaError_t err;
-  if ((err = cudaFuncSetAttribute(gv2_gateup<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg)) != cudaSuccess)
+  if ((err = set_smem_limit_once(gv2_gateup<NB>, (int)sg)) != cudaSuccess)
     return err;
-  if ((err = cudaFuncSetAttribute(gv2_down<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sd)) != cudaSuccess)
+  if ((err = set_smem_limit_once(gv2_down<NB>, (int)sd)) != cudaSuccess)
     return err;
   const int ug = (P.I / 128) * Q.KS, ugs = (P.Is / 128) * Q.KS;
   const int xg = nact * ug > ugs ? nact * ug : ugs;

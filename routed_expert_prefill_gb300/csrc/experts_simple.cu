@@ -165,10 +165,9 @@ cudaError_t launch_experts_simple(const ExpertsArgs& a, bool deterministic, cuda
   cudaError_t err;
   const int n = a.n_pairs;
   const int smax = (a.h > a.I ? a.h : a.I) * 4;
-  if ((err = cudaFuncSetAttribute(gateup_simple_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smax)) != cudaSuccess)
+  if ((err = set_smem_limit_once(gateup_simple_kernel, smax)) != cudaSuccess)
     return err;
-  if ((err = cudaFuncSetAttribute(down_simple_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (a.I > a.Is ? a.I : a.Is) * 4)) != cudaSuccess)
+  if ((err = set_smem_limit_once(down_simple_kernel, (a.I > a.Is ? a.I : a.Is) * 4)) != cudaSuccess)
     return err;
   if (a.Is > 0) {
     MOE_LAUNCH("gateup_simple", stream, launch_k(gateup_simple_kernel, a.t, SB, a.h * 4, stream, a, 1));

@@ -168,8 +168,7 @@ cudaError_t launch_route_topk(const uint16_t* x, const uint16_t* wr, const float
                               int h, int E, int k, int32_t* idx, float* w, float* logits,
                               cudaStream_t stream) {
   const size_t smem = route_smem_bytes(h, E);
-  cudaError_t err = cudaFuncSetAttribute(route_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+  cudaError_t err = set_smem_limit_once(route_topk_kernel, (int)smem);
   if (err != cudaSuccess) return err;
   dim3 grid((t + RT_ROWS - 1) / RT_ROWS);
   MOE_LAUNCH("route_topk", stream,
