@@ -593,16 +593,22 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         }
         tmem_st_wait();
         tc_fence_before();
-        // The MMA issuer waits on a_full only: the B stage this A stage
-        // multiplies must have landed before a_full completes.
-        const uint32_t bst = bbase + (uint32_t)(st * CPS / U.kps);
-        bool b_ok = true;
-        if (lane == 0) b_ok = mbar_wait(&S.b_full[bst % SB], (bst / SB) & 1, abort, WAIT_NS);
-        b_ok = __shfl_sync(0xFFFFFFFFu, b_ok, 0);
-        if (!b_ok) {
-          if (lane == 0) note_timeout(p.status, abort, GATEUP ? 34 : 44);
-          ok = false;
-          break;
+        // The MMA issuer waits on a_full only, and takes the A stages in
+        // order: the B stage this A stage multiplies must have landed before
+        // the a_full of the first A stage it serves completes.  Later A
+        // stages of the same B stage are ordered after that observation by
+        // the issuer's own earlier wait, so only the first one checks.
+        const int kcs = st * CPS;
+        if (kcs % U.kps == 0) {
+          const uint32_t bst = bbase + (uint32_t)(kcs / U.kps);
+          bool b_ok = true;
+          if (lane == 0) b_ok = mbar_wait(&S.b_full[bst % SB], (bst / SB) & 1, abort, WAIT_NS);
+          b_ok = __shfl_sync(0xFFFFFFFFu, b_ok, 0);
+          if (!b_ok) {
+            if (lane == 0) note_timeout(p.status, abort, GATEUP ? 34 : 44);
+            ok = false;
+            break;
+          }
         }
         __syncwarp();
         if (lane == 0) {
