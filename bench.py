@@ -85,12 +85,15 @@ def step_work(w: synth.Workload, counts: np.ndarray) -> dict:
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
 # the packed expert kernels, from one ncu capture of
-# `python bench.py --steps 5 --warmup 3 --no-cpu-baseline` on a GB300; valid
+# `python bench.py --steps 5 --warmup 3 --no-cpu-baseline [--workload ...]`
+# on a GB300; valid
 # while the kernel sources hash to `src` (reported as null otherwise).
 PACKED_SOURCES = ("experts_packed.cu", "tc_ptx.cuh", "tc_common.cuh", "common.cuh", "experts.cuh")
 MEASURED_TRAFFIC = {
-    ("t512_h2048_e128", "gateup", 16): dict(bytes=263.97e6, src="ccb28b535680ffdb"),
-    ("t512_h2048_e128", "down", 16): dict(bytes=130.25e6, src="ccb28b535680ffdb"),
+    ("t512_h2048_e128", "gateup", 16): dict(bytes=264.25e6, src="bb97e542a014c111"),
+    ("t512_h2048_e128", "down", 16): dict(bytes=130.16e6, src="bb97e542a014c111"),
+    ("t4096_h2048_e128_skewed", "gateup", 16): dict(bytes=301.81e6, src="bb97e542a014c111"),
+    ("t4096_h2048_e128_skewed", "down", 16): dict(bytes=139.19e6, src="bb97e542a014c111"),
 }
 
 
