@@ -164,6 +164,21 @@ int moe_build_csr(const int32_t* idx, const float* w, const moe_dims* dims,
                   const moe_csr* csr, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Router and grouping in one call: exactly the results of moe_route_topk
+ * (with ws, logits NULL) followed by moe_build_csr on the same workspace --
+ * the same idx, w and csr -- with one launch fewer for t <= 16 rows, where
+ * the router's last block also builds the list.  Larger t issue the same
+ * launches as the two calls.
+ *
+ * x, wr, rbias, idx, w as in moe_route_topk; csr as in moe_build_csr; ws of
+ * at least moe_workspace_bytes(dims, 0) bytes (required).
+ * Errors: MOE_EINVAL, MOE_ESHAPE, MOE_EWORKSPACE, MOE_ECUDA.
+ */
+int moe_route_csr(const uint16_t* x, const uint16_t* wr, const float* rbias,
+                  const moe_dims* dims, int32_t* idx, float* w, const moe_csr* csr,
+                  void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Expert FFNs (prefill/experts.rs, pf_experts):
  *
  *   out[r] = g_r * FFN_S(x_r) + sum_j w_rj * FFN_{e_rj}(x_r),

@@ -13,7 +13,9 @@ cudaError_t launch_route_topk(const uint16_t* x, const uint16_t* wr, const float
 size_t route_smem_bytes(int h, int E);
 size_t route_ws_bytes(int t, int h, int E);
 cudaError_t launch_route_tc(const uint16_t* x, const uint16_t* wr, const float* rbias, int t, int h, int E, int k,
-                            int32_t* idx, float* w, unsigned char* scratch, DeviceStatus* st, cudaStream_t stream);
+                            int32_t* idx, float* w, unsigned char* scratch, DeviceStatus* st, cudaStream_t stream,
+                            const moe_csr* co = nullptr);
+bool route_builds_csr(int t);
 cudaError_t launch_build_csr(const int32_t* idx, const float* w, int t, int k, int E, const moe_csr& csr,
                              unsigned char* ws, const WsLayout& L, cudaStream_t stream);
 cudaError_t launch_experts_fast(const ExpertsArgs& a, uint32_t flags, cudaStream_t stream);
@@ -190,6 +192,31 @@ int moe_build_csr(const int32_t* idx, const float* w, const moe_dims* dims, cons
   return cuda_status(launch_build_csr(idx, w, dims->t, dims->k, dims->E, *csr, (unsigned char*)ws, L,
                                       (cudaStream_t)stream),
                      "moe_build_csr launch");
+}
+
+int moe_route_csr(const uint16_t* x, const uint16_t* wr, const float* rbias, const moe_dims* dims, int32_t* idx,
+                  float* w, const moe_csr* csr, void* ws, size_t ws_bytes, void* stream) {
+  TRY(check_dims(dims));
+  TRY(check_ptr(x, "x", 16));
+  TRY(check_ptr(wr, "wr", 16));
+  TRY(check_ptr(rbias, "rbias", 4, true));
+  TRY(check_ptr(idx, "idx", 4));
+  TRY(check_ptr(w, "w", 4));
+  if (!csr) return set_error(MOE_EINVAL, "csr is NULL");
+  TRY(check_ptr(csr->offsets, "csr->offsets", 4));
+  TRY(check_ptr(csr->rows, "csr->rows", 4));
+  TRY(check_ptr(csr->weights, "csr->weights", 4));
+  TRY(check_ptr(csr->slot_of, "csr->slot_of", 4));
+  TRY(check_ws(dims, 0, ws, ws_bytes));
+  const WsLayout L = ws_layout(*dims, 0);
+  unsigned char* wsb = (unsigned char*)ws;
+  const bool fused = route_builds_csr(dims->t);
+  TRY(cuda_status(launch_route_tc(x, wr, rbias, dims->t, dims->h, dims->E, dims->k, idx, w, wsb + L.route,
+                                  (DeviceStatus*)(wsb + L.status), (cudaStream_t)stream, fused ? csr : nullptr),
+                  "moe_route_csr launch"));
+  if (fused) return MOE_OK;
+  return cuda_status(launch_build_csr(idx, w, dims->t, dims->k, dims->E, *csr, wsb, L, (cudaStream_t)stream),
+                     "moe_route_csr launch");
 }
 
 int moe_experts_fwd(const uint16_t* x, const moe_csr* csr, const moe_qweights* experts,

@@ -411,11 +411,88 @@ route_refine_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__
 constexpr int RSM_ROWS = 16;
 constexpr int RSM_WARPS = 4;
 
+// The grouping of moe_build_csr for at most 256 pairs (t <= 16, k <= 16),
+// by the router's last block once every row's top k is written: per-expert
+// counts in shared memory, one scan over the experts (eight per thread), and
+// each pair's rank inside its expert by counting the earlier pairs of the same
+// expert -- the same stable order as the grouping kernels.
+__device__ __forceinline__ void small_csr_block(const int32_t* idx, const float* w, int n, int k, int E,
+                                                const moe_csr& co, DeviceStatus* st) {
+  constexpr int T = RSM_WARPS * 32, PER = 1024 / T;
+  __shared__ int start[1024];
+  __shared__ int es[256];
+  __shared__ int warp_sums[RSM_WARPS + 1];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < E; i += T) start[i] = 0;
+  for (int p = tid; p < n; p += T) {
+    int e = __ldcg(idx + p);  // written by this block before the barrier
+    if (e < 0 || e >= E) {
+      raise_flag(st, FLAG_BAD_EXPERT);
+      e = -1;
+    }
+    es[p] = e;
+  }
+  __syncthreads();
+  for (int p = tid; p < n; p += T)
+    if (es[p] >= 0) atomicAdd(&start[es[p]], 1);
+  __syncthreads();
+  int c[PER], sum = 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int ex = tid * PER + j;
+    c[j] = ex < E ? start[ex] : 0;
+    sum += c[j];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int i = 0; i < RSM_WARPS; ++i) {
+      const int v = warp_sums[i];
+      warp_sums[i] = run;
+      run += v;
+    }
+    warp_sums[RSM_WARPS] = run;
+  }
+  __syncthreads();
+  int run = warp_sums[warp] + incl - sum;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int ex = tid * PER + j;
+    if (ex < E) {
+      start[ex] = run;
+      co.offsets[ex] = run;
+    }
+    run += c[j];
+  }
+  if (tid == 0) co.offsets[E] = warp_sums[RSM_WARPS];
+  __syncthreads();
+  for (int p = tid; p < n; p += T) {
+    const int e = es[p];
+    if (e < 0) {
+      co.slot_of[p] = -1;
+      continue;
+    }
+    int r = 0;
+    for (int q = 0; q < p; ++q) r += es[q] == e;
+    const int pos = start[e] + r;
+    co.rows[pos] = p / k;
+    co.weights[pos] = __ldcg(w + p);
+    co.slot_of[p] = pos;
+  }
+}
+
 template <int TR, int NQ>
 __global__ void __launch_bounds__(RSM_WARPS * 32)
 route_small_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr, const float* __restrict__ rbias,
                    int t, int h, int E, int Ep, int k, float* lg, int32_t* __restrict__ idx, float* __restrict__ wout,
-                   DeviceStatus* st) {
+                   DeviceStatus* st, moe_csr co) {
   pdl_wait();
   pdl_trigger();
   constexpr int U = TR <= 2 ? 8 : (TR <= 4 ? 4 : 2);  // K spans per load round
@@ -482,6 +559,10 @@ route_small_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ 
     }
     warp_topk_softmax<NQ>(key, k, lane, idx + (size_t)r * k, wout + (size_t)r * k);
   }
+  if (co.offsets) {
+    __syncthreads();  // every row's idx and w are written
+    small_csr_block(idx, wout, t * k, k, E, co, st);
+  }
   if (threadIdx.x == 0) st->route_done = 0;
 }
 
@@ -533,21 +614,23 @@ cudaError_t launch_refine(const uint16_t* x, const uint16_t* wr, const float* rb
 
 template <int TR, int NQ>
 cudaError_t launch_small_t(const uint16_t* x, const uint16_t* wr, const float* rbias, int t, int h, int E, int k,
-                           float* lg, int32_t* idx, float* w, DeviceStatus* st, cudaStream_t stream) {
+                           float* lg, int32_t* idx, float* w, DeviceStatus* st, const moe_csr* co,
+                           cudaStream_t stream) {
   MOE_LAUNCH("route_small", stream,
              launch_k(route_small_kernel<TR, NQ>, (E + RSM_WARPS - 1) / RSM_WARPS, RSM_WARPS * 32, 0, stream, 
-                 x, wr, rbias, t, h, E, (E + 15) / 16 * 16, k, lg, idx, w, st));
+                 x, wr, rbias, t, h, E, (E + 15) / 16 * 16, k, lg, idx, w, st, co ? *co : moe_csr{}));
   return cudaGetLastError();
 }
 
 template <int NQ>
 cudaError_t launch_small(const uint16_t* x, const uint16_t* wr, const float* rbias, int t, int h, int E, int k,
-                         float* lg, int32_t* idx, float* w, DeviceStatus* st, cudaStream_t stream) {
-  if (t <= 1) return launch_small_t<1, NQ>(x, wr, rbias, t, h, E, k, lg, idx, w, st, stream);
-  if (t <= 2) return launch_small_t<2, NQ>(x, wr, rbias, t, h, E, k, lg, idx, w, st, stream);
-  if (t <= 4) return launch_small_t<4, NQ>(x, wr, rbias, t, h, E, k, lg, idx, w, st, stream);
-  if (t <= 8) return launch_small_t<8, NQ>(x, wr, rbias, t, h, E, k, lg, idx, w, st, stream);
-  return launch_small_t<16, NQ>(x, wr, rbias, t, h, E, k, lg, idx, w, st, stream);
+                         float* lg, int32_t* idx, float* w, DeviceStatus* st, const moe_csr* co,
+                         cudaStream_t stream) {
+  if (t <= 1) return launch_small_t<1, NQ>(x, wr, rbias, t, h, E, k, lg, idx, w, st, co, stream);
+  if (t <= 2) return launch_small_t<2, NQ>(x, wr, rbias, t, h, E, k, lg, idx, w, st, co, stream);
+  if (t <= 4) return launch_small_t<4, NQ>(x, wr, rbias, t, h, E, k, lg, idx, w, st, co, stream);
+  if (t <= 8) return launch_small_t<8, NQ>(x, wr, rbias, t, h, E, k, lg, idx, w, st, co, stream);
+  return launch_small_t<16, NQ>(x, wr, rbias, t, h, E, k, lg, idx, w, st, co, stream);
 }
 
 }  // namespace
@@ -558,15 +641,20 @@ size_t route_ws_bytes(int t, int h, int E) {
 }
 
 
+// Whether launch_route_tc builds the grouping itself when given one (the
+// small-t router's last block does, for t <= 16 rows).
+bool route_builds_csr(int t) { return t <= RSM_ROWS; }
+
 cudaError_t launch_route_tc(const uint16_t* x, const uint16_t* wr, const float* rbias, int t, int h, int E, int k,
-                            int32_t* idx, float* w, unsigned char* scratch, DeviceStatus* st, cudaStream_t stream) {
+                            int32_t* idx, float* w, unsigned char* scratch, DeviceStatus* st, cudaStream_t stream,
+                            const moe_csr* co) {
   const RoutePlan R = route_plan(t, h, E);
   float* part = reinterpret_cast<float*>(scratch);
   if (t <= RSM_ROWS) {
-    if (E <= 128) return launch_small<4>(x, wr, rbias, t, h, E, k, part, idx, w, st, stream);
-    if (E <= 256) return launch_small<8>(x, wr, rbias, t, h, E, k, part, idx, w, st, stream);
-    if (E <= 512) return launch_small<16>(x, wr, rbias, t, h, E, k, part, idx, w, st, stream);
-    return launch_small<32>(x, wr, rbias, t, h, E, k, part, idx, w, st, stream);
+    if (E <= 128) return launch_small<4>(x, wr, rbias, t, h, E, k, part, idx, w, st, co, stream);
+    if (E <= 256) return launch_small<8>(x, wr, rbias, t, h, E, k, part, idx, w, st, co, stream);
+    if (E <= 512) return launch_small<16>(x, wr, rbias, t, h, E, k, part, idx, w, st, co, stream);
+    return launch_small<32>(x, wr, rbias, t, h, E, k, part, idx, w, st, co, stream);
   }
   float* wn2 = reinterpret_cast<float*>(scratch + align_up((size_t)R.KS * t * R.Ep * 4, 256));
   CUtensorMap tx, tw;

@@ -35,6 +35,7 @@ EXPORTS = (
     "moe_status_string",
     "moe_route_topk",
     "moe_build_csr",
+    "moe_route_csr",
     "moe_experts_fwd",
     "moe_workspace_bytes",
     "moe_clear_device_status",
@@ -97,6 +98,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_route_topk.argtypes = [vp, vp, vp, ctypes.POINTER(MoeDims), vp, vp, vp, vp, sz, vp]
     lib.moe_build_csr.restype = ctypes.c_int
     lib.moe_build_csr.argtypes = [vp, vp, ctypes.POINTER(MoeDims), ctypes.POINTER(MoeCsr), vp, sz, vp]
+    lib.moe_route_csr.restype = ctypes.c_int
+    lib.moe_route_csr.argtypes = [vp, vp, vp, ctypes.POINTER(MoeDims), vp, vp, ctypes.POINTER(MoeCsr), vp, sz, vp]
     lib.moe_experts_fwd.restype = ctypes.c_int
     lib.moe_experts_fwd.argtypes = [vp, ctypes.POINTER(MoeCsr), ctypes.POINTER(MoeQWeights),
                                     ctypes.POINTER(MoeShared), vp, ctypes.POINTER(MoeDims), u32, vp, sz, vp]
@@ -218,6 +221,34 @@ def moe_build_csr(idx: torch.Tensor, w: torch.Tensor, E: int, ws: torch.Tensor |
     return out
 
 
+def moe_route_csr(x: torch.Tensor, wr: torch.Tensor, k: int, rbias: torch.Tensor | None = None,
+                  ws: torch.Tensor | None = None, out_route=None, out_csr: Csr | None = None, stream=None):
+    """Router and grouping in one call: the idx, w and Csr of moe_route_topk
+    (tensor-core path) followed by moe_build_csr, with one launch fewer for
+    t <= 16 rows."""
+    lib = load_library()
+    t, h = x.shape
+    E = wr.shape[0]
+    dims = MoeDims(t, h, 128, E, k, 0)
+    dev = x.device
+    if out_route is None:
+        idx = torch.empty((t, k), dtype=torch.int32, device=dev)
+        w = torch.empty((t, k), dtype=torch.float32, device=dev)
+    else:
+        idx, w = out_route
+    if out_csr is None:
+        out_csr = Csr(torch.empty(E + 1, dtype=torch.int32, device=dev),
+                      torch.empty(t * k, dtype=torch.int32, device=dev),
+                      torch.empty(t * k, dtype=torch.float32, device=dev),
+                      torch.empty(t * k, dtype=torch.int32, device=dev))
+    if ws is None:
+        ws = new_workspace(dims, 0, dev, stream)
+    c = out_csr.c()
+    _check(lib.moe_route_csr(_ptr(_u16(x)), _ptr(_u16(wr)), _ptr(rbias), ctypes.byref(dims), _ptr(idx), _ptr(w),
+                             ctypes.byref(c), _ptr(ws), ws.numel(), _stream(stream)))
+    return idx, w, out_csr
+
+
 def moe_build_csr_noalloc(idx: torch.Tensor, w: torch.Tensor, E: int, out: Csr | None = None,
                           stream=None) -> Csr:
     """moe_build_csr with the library's fixed scratch instead of a workspace
@@ -337,9 +368,8 @@ def moe_forward(dev: dict, dims: MoeDims, flags: int = 0, ws: torch.Tensor | Non
     if ws is None:
         ws = new_workspace(dims, flags, dev["x"].device, stream)
     b = bufs or {}
-    idx, w = moe_route_topk(dev["x"], dev["wr"], dims.k, dev.get("rbias"), out=b.get("route"), ws=ws,
-                            stream=stream)
-    csr = moe_build_csr(idx, w, dims.E, ws=ws, out=b.get("csr"), stream=stream)
+    idx, w, csr = moe_route_csr(dev["x"], dev["wr"], dims.k, dev.get("rbias"), ws=ws, out_route=b.get("route"),
+                                out_csr=b.get("csr"), stream=stream)
     shared = None
     if flags & MOE_PACKED_WEIGHTS:
         experts = (dev["packed"], None, None)

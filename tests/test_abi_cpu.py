@@ -104,6 +104,23 @@ def test_workspace_too_small_and_flags(lib):
     assert rc == -3
 
 
+def test_route_csr_argument_checks(lib):
+    """moe_route_csr validates like the two calls it combines, before any launch."""
+    from routed_expert_prefill_gb300 import moe
+
+    d = moe.dims_of(4, 256, 128, 8, 2, 0)
+    ok = ctypes.c_void_p(0x10000)
+    csr = moe.MoeCsr(0x10000, 0x10000, 0x10000, 0x10000)
+    need = lib.moe_workspace_bytes(ctypes.byref(d), 0)
+    assert lib.moe_route_csr(ok, ok, None, ctypes.byref(d), ok, ok, None, ok, need, None) == -1  # csr NULL
+    assert lib.moe_route_csr(ok, ok, None, ctypes.byref(d), ok, ok, ctypes.byref(csr), None, 0, None) == -3
+    assert lib.moe_route_csr(ok, ok, None, ctypes.byref(d), ok, ok, ctypes.byref(csr), ok, need - 1, None) == -3
+    bad = moe.MoeCsr(0x10000, 0x10002, 0x10000, 0x10000)  # misaligned rows
+    assert lib.moe_route_csr(ok, ok, None, ctypes.byref(d), ok, ok, ctypes.byref(bad), ok, need, None) == -1
+    d.k = 17
+    assert lib.moe_route_csr(ok, ok, None, ctypes.byref(d), ok, ok, ctypes.byref(csr), ok, need, None) == -2
+
+
 def test_status_strings(lib):
     assert lib.moe_status_string(0) == b"MOE_OK"
     assert lib.moe_status_string(-5) == b"MOE_EDEVICE"

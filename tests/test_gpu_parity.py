@@ -356,6 +356,30 @@ def test_packed_128_row_tiles(moe, inter, det):
     _check_out(res["out"], ref["out"])
 
 
+@pytest.mark.parametrize("t,E,k", [(1, 128, 8), (3, 1000, 16), (8, 128, 8), (16, 256, 16), (16, 40, 2),
+                                   (17, 128, 8), (300, 128, 8)])
+def test_route_csr_matches_separate_calls(moe, t, E, k):
+    """The combined call (the router's last block groups the pairs for t <= 16)
+    gives bit for bit the router's and the grouping's outputs."""
+    w = synth.Workload("rc", t, 512, 128, E, k, 0, 60 + t)
+    inp = synth.make_inputs(w)
+    dev = moe.upload_inputs(inp)
+    dims = moe.dims_of(t, 512, 128, E, k, 0)
+    ws = moe.new_workspace(dims, 0)
+    idx0, w0 = moe.moe_route_topk(dev["x"], dev["wr"], k, dev.get("rbias"), ws=ws)
+    csr0 = moe.moe_build_csr(idx0, w0, E, ws=ws)
+    idx1, w1, csr1 = moe.moe_route_csr(dev["x"], dev["wr"], k, dev.get("rbias"), ws=ws)
+    torch.cuda.synchronize()
+    assert moe.read_device_status(ws) == 0
+    np.testing.assert_array_equal(idx1.cpu().numpy(), idx0.cpu().numpy())
+    np.testing.assert_array_equal(w1.cpu().numpy().view(np.uint32), w0.cpu().numpy().view(np.uint32))
+    for a, b in zip((csr1.offsets, csr1.rows, csr1.slot_of), (csr0.offsets, csr0.rows, csr0.slot_of)):
+        np.testing.assert_array_equal(a.cpu().numpy(), b.cpu().numpy())
+    np.testing.assert_array_equal(csr1.weights.cpu().numpy().view(np.uint32),
+                                  csr0.weights.cpu().numpy().view(np.uint32))
+    _check_csr_against(csr1, idx1, w1, E)
+
+
 def test_bad_expert_ids_are_flagged_and_dropped(moe):
     t, k, E = 8, 2, 4
     idx = torch.tensor([[0, 1], [2, 9], [3, 0], [-1, 2], [1, 2], [0, 3], [1, 0], [2, 3]], dtype=torch.int32,
