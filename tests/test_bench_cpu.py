@@ -1,0 +1,74 @@
+"""The benchmark's output contract and its host-side arithmetic, on CPU.
+
+The reference arm times the oracle alone, so it runs without a GPU; its JSON
+line must carry the keys the benchmark contract names.  The GPU arm's helpers
+(work model, whole-job throughput, max over ranks) are plain host code.
+"""
+
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from routed_expert_prefill_gb300 import synth  # noqa: E402
+
+
+def test_reference_arm_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        "tiny_t16_h256_e8", "--steps", "2", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 1 and d["n_gpus"] == 1
+    assert d["unit"] == "tokens/s" and d["higher_is_better"] is True and d["value"] > 0
+    assert d["config"]["workload"] == "tiny_t16_h256_e8"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    e = d["e2e"]
+    assert e["value"] == d["value"] and e["unit"] == d["unit"]
+    assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+    # ms_per_step is the time of one whole step (all t rows), from the sampled rows
+    assert d["ms_per_step"] == pytest.approx(1e3 * d["config"]["t"] / d["value"], rel=1e-6)
+
+
+def test_step_work_counts():
+    """Flops and bytes of the work model on a hand-checked tiny case."""
+    w = synth.Workload("m", 4, 256, 128, 4, 2, 128, 1)
+    counts = np.array([3, 0, 4, 1])  # 8 pairs, 3 experts touched
+    work = bench.step_work(w, counts)
+    n, t, h, inter, si = 8, 4, 256, 128, 128
+    gu = 4 * n * h * inter + 4 * t * h * si
+    dn = 2 * n * h * inter + 2 * t * h * si
+    router = 2 * t * h * w.E
+    assert work["touched"] == 3 and work["pairs"] == 8 and work["max_rows"] == 4
+    assert work["by_kernel"]["gateup"]["flops"] == gu
+    assert work["by_kernel"]["down"]["flops"] == dn
+    assert work["flops"] == gu + dn + router
+    rec = 3 * h * inter * (1 / 2 + 4 / 64)
+    assert work["bytes"] >= 4 * rec  # three touched records and the shared one, plus activations
+
+
+def test_job_throughput_and_single_rank_max():
+    # every rank processes its own chunk: value = world * rows / max time
+    assert bench.job_tokens_per_s(1, 512, 0.2) == pytest.approx(512 / 0.2e-3)
+    assert bench.job_tokens_per_s(4, 512, 0.2) == pytest.approx(4 * 512 / 0.2e-3)
+    assert bench.max_over_ranks(3.5, "cpu") == 3.5
+
+
+def test_measured_traffic_is_tied_to_the_kernel_sources():
+    assert bench.measured_traffic("no_such_workload", "gateup", 16) is None
+    for (wl, fam, fl), m in bench.MEASURED_TRAFFIC.items():
+        got = bench.measured_traffic(wl, fam, fl)
+        assert got is None or got == m["bytes"]
