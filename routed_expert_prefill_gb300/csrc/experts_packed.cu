@@ -26,14 +26,15 @@
 //     alternate stages and dequantise one weight row per thread
 //     (w = fma(q, s, b) in bf16) straight into TMEM with tcgen05.st, warps 1
 //     and 15 issue the gate and the up tcgen05.mma streams with A in TMEM
-//     and B in shared memory, and a
-//     four-warp epilogue group drains the gate and up accumulators into
-//     registers (silu(gate) * up), frees TMEM for the next unit, and writes
-//     hg, again as swizzled K-major images.
+//     and B in shared memory, and one or two four-warp epilogue groups drain
+//     the gate and up accumulators into registers (silu(gate) * up), free
+//     TMEM for the next unit, and write hg, again as swizzled K-major
+//     images, in 16-byte pieces through per-warp staging.
 //   down:     the same pipeline on the down blocks and hg images, with a
 //     double-buffered accumulator; the epilogue scales by the routing weight
-//     and adds into the fp32 block accumulator (atomics) or, deterministic
-//     mode, stores per list position.
+//     and, transposed through per-warp staging, adds 16-byte pieces into the
+//     fp32 block accumulator (reductions) or, deterministic mode, stores per
+//     list position.
 // Every mbarrier wait is bounded (2 s of global time); a wait that gives up
 // records MOE_ETIMEOUT, raises a CTA-wide abort flag, lets in-flight copies
 // and MMAs land, frees TMEM and returns.
