@@ -2,33 +2,47 @@
 
 A step is one pass of the whole path over one chunk: router top-k, CSR
 grouping, and the expert FFNs (shared expert, gate/up + silu*up, down +
-weighted scatter-add), i.e. moe_route_topk -> moe_build_csr ->
-moe_experts_fwd on one stream.  Inputs are synthetic (routed_expert_prefill_gb300.synth)
-and resident in HBM for ``value``; ``e2e`` copies x in from pinned host
-memory and the block output back every step.
+weighted scatter-add), i.e. moe_route_csr -> moe_experts_fwd on one stream.
+Inputs are synthetic (routed_expert_prefill_gb300.synth) and resident in HBM
+for ``value``; ``e2e`` copies x in from pinned host memory and the block
+output back every step.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--workloads LIST|none] [--impl ours|reference]
+
+The headline workload is t=4096, h=4096, inter=1536, E=256, k=8 (the largest
+single-GPU configuration); the same line carries, under ``workloads``, the
+skewed t=4096 chunk, the t=512 chunk and the decode-shaped t=1/2/4/8 chunks,
+each timed the same way.
+
+Timing: W untimed warm-up steps, then exactly K timed steps, each a replay of
+the step captured as a CUDA graph, bracketed by CUDA events on the launching
+stream, with a write larger than L2 between steps (outside the events);
+``ms_per_step`` is the median.  ``sustained`` repeats the same measurement
+for at least one second and 50 runs.
 
 Multi-GPU (torchrun): every rank runs its own chunk (weak scaling, no
-collective on the data path); value = chunks' rows over the max-over-ranks time.
+collective on the data path); value = all ranks' rows over the max-over-ranks
+time.
 """
 
 import os
 
-# The CPU oracle legs run single-threaded (their reported core count is 1).
+# Each oracle worker runs single-threaded; the pool spreads rows over cores.
 for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
-import argparse
-import hashlib
-import json
-import statistics
-import subprocess
-import sys
-import threading
-import time
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import multiprocessing as mp  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import threading  # noqa: E402
+import time  # noqa: E402
 
-import numpy as np
+import numpy as np  # noqa: E402
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -36,9 +50,13 @@ sys.path.insert(0, ROOT)
 from routed_expert_prefill_gb300 import synth  # noqa: E402
 
 METRIC = "prefill tokens/s and % of roofline (tensor or HBM) for routed MoE FFN, 1 GB300"
-DEFAULT_WORKLOAD = "t512_h2048_e128"
+DEFAULT_WORKLOAD = "t4096_h4096_e256"
+EXTRA_WORKLOADS = ("t4096_h2048_e128_skewed", "t512_h2048_e128", "decode_t1_h2048_e128",
+                   "decode_t2_h2048_e128", "decode_t4_h2048_e128", "decode_t8_h2048_e128")
 L2_BYTES = 129 * 2 ** 20
+SUSTAIN_S, SUSTAIN_MIN_RUNS, SUSTAIN_MAX_RUNS = 1.0, 50, 20000
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+MOE_PACKED_WEIGHTS = 0x10
 
 
 def load_peaks():
@@ -47,6 +65,13 @@ def load_peaks():
         d = json.load(open(p))
         return d, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
 # --------------------------------------------------------------------------
@@ -83,11 +108,19 @@ def step_work(w: synth.Workload, counts: np.ndarray) -> dict:
                 bytes=wbytes + io, by_kernel=by_kernel)
 
 
+def step_roofline(work: dict, ms: float, peaks: dict) -> dict:
+    """T* = max(F / bf16 peak, B / HBM peak) against the measured step time."""
+    tf = work["flops"] / (peaks["bf16_tflops"] * 1e12)
+    tb = work["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    return {"frac": max(tf, tb) / (ms * 1e-3), "bound": "tensor" if tf > tb else "hbm",
+            "t_star_us": 1e6 * max(tf, tb), "tflops": work["flops"] / (ms * 1e-3) / 1e12,
+            "gbs": work["bytes"] / (ms * 1e-3) / 1e9}
+
+
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
-# the packed expert kernels, from one ncu capture of
-# `python bench.py --steps 5 --warmup 3 --no-cpu-baseline [--workload ...]`
-# on a GB300; valid
-# while the kernel sources hash to `src` (reported as null otherwise).
+# the packed expert kernels, from one ncu capture of the bench command on a
+# GB300; valid while the kernel sources hash to `src` (reported as null
+# otherwise).
 PACKED_SOURCES = ("experts_packed.cu", "tc_ptx.cuh", "tc_common.cuh", "common.cuh", "experts.cuh")
 MEASURED_TRAFFIC = {
     ("t512_h2048_e128", "gateup", 16): dict(bytes=264.25e6, src="59dce5c721bcb98c"),
@@ -172,7 +205,7 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         for ln in self.lines:
             f = [s.strip() for s in ln.split(",")]
             if len(f) < 9:
@@ -180,6 +213,7 @@ class ClockSampler:
             try:
                 sm.append(float(f[1]))
                 mx.append(float(f[2]))
+                pw.append(float(f[3]))
             except ValueError:
                 continue
             for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
@@ -188,28 +222,90 @@ class ClockSampler:
                     reasons.add(name)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        # "under load": samples drawing more than a third of the peak power seen
+        loaded = [s for s, p in zip(sm, pw) if p > max(pw) / 3] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "samples_under_load": len(loaded), "power_w_max": max(pw)}
 
 
 # --------------------------------------------------------------------------
-# Reference arm: the CPU oracle as it stands
+# The CPU oracle, timed on the host's cores
 # --------------------------------------------------------------------------
 
-def oracle_sample_seconds(w: synth.Workload, inp: dict, rows: int) -> float:
+_POOL_INPUTS = None  # the workload's inputs, set before the pool forks (workers share them)
+
+
+def _oracle_worker(task):
+    """One worker: the oracle as it stands on rows [a, b) of the workload."""
+    a, b, k, h, inter, shared_inter = task
     from oracle import moe_oracle as O
 
-    sub = dict(inp, x=inp["x"][:rows])
+    inp = _POOL_INPUTS
+    O.moe_forward(dict(inp, x=inp["x"][a:b]), k, h, inter, shared_inter)
+    return b - a
+
+
+class OraclePool:
+    """The CPU oracle over a sample of a workload's rows, on every host core.
+
+    A row's output depends on that row alone, so the sample's rows are split
+    into one contiguous range per core and each worker runs the unmodified
+    oracle (router, grouping, experts) on its range.  The pool forks before
+    any CUDA call, so the workers share the inputs without copying them."""
+
+    def __init__(self, w: synth.Workload, inp: dict, cores: int):
+        global _POOL_INPUTS
+        _POOL_INPUTS = inp
+        self.w, self.inp, self.cores = w, inp, cores
+        self.pool = mp.get_context("fork").Pool(cores) if cores > 1 else None
+
+    def seconds(self, rows: int) -> float:
+        w = self.w
+        n = min(self.cores, rows)
+        cuts = np.linspace(0, rows, n + 1).astype(int)
+        tasks = [(int(cuts[i]), int(cuts[i + 1]), w.k, w.h, w.inter, w.shared_inter) for i in range(n)]
+        t0 = time.perf_counter()
+        if self.pool is None:
+            for tk in tasks:
+                _oracle_worker(tk)
+        else:
+            self.pool.map(_oracle_worker, tasks, chunksize=1)
+        return time.perf_counter() - t0
+
+    def rows_for(self, budget_s: float) -> int:
+        """Rows whose pass takes about budget_s (from a timed probe of two rows per core)."""
+        probe = min(self.w.t, 2 * self.cores)
+        s = self.seconds(probe)
+        return int(max(probe, min(self.w.t, probe * budget_s / max(s, 1e-9))))
+
+    def close(self):
+        if self.pool is not None:
+            self.pool.close()
+            self.pool.join()
+
+
+def oracle_one_core_seconds(w: synth.Workload, inp: dict, rows: int) -> float:
+    from oracle import moe_oracle as O
+
     t0 = time.perf_counter()
-    O.moe_forward(sub, w.k, w.h, w.inter, w.shared_inter)
+    O.moe_forward(dict(inp, x=inp["x"][:rows]), w.k, w.h, w.inter, w.shared_inter)
     return time.perf_counter() - t0
 
 
-def calibrated_rows(w: synth.Workload, inp: dict, budget_s: float) -> int:
-    """Rows of the workload whose oracle pass takes about budget_s (from a timed 4-row probe)."""
-    probe = min(w.t, 4)
-    per_row = oracle_sample_seconds(w, inp, probe) / probe
-    return int(max(probe, min(w.t, budget_s / max(per_row, 1e-9))))
+def cpu_baseline(pool: OraclePool, w: synth.Workload, inp: dict, budget_s: float, one_core: bool) -> dict:
+    rows = pool.rows_for(budget_s)
+    secs = pool.seconds(rows)
+    res = {"value": rows / secs, "unit": "tokens/s", "cores": pool.cores, "kind": "oracle",
+           "sample": f"first {rows} of the {w.t} rows, split over {pool.cores} host cores (one oracle "
+                     f"process per core: router, grouping, experts in fp64), {secs:.1f} s"}
+    if one_core:
+        probe = min(w.t, 4)
+        per_row = oracle_one_core_seconds(w, inp, probe) / probe
+        r1 = int(max(probe, min(w.t, budget_s / max(per_row, 1e-9))))
+        s1 = oracle_one_core_seconds(w, inp, r1)
+        res["one_core"] = {"value": r1 / s1, "unit": "tokens/s", "cores": 1,
+                           "sample": f"first {r1} of the {w.t} rows on one core, {s1:.1f} s"}
+    return res
 
 
 def run_reference(args, w: synth.Workload):
@@ -217,24 +313,31 @@ def run_reference(args, w: synth.Workload):
     if rank != 0:
         return
     inp = synth.make_inputs(w)
-    # each step a bounded sample: the whole run stays within about 150 s
-    per_step = min(10.0, 150.0 / max(1, args.steps + args.warmup))
-    rows = min(calibrated_rows(w, inp, per_step), args.oracle_rows) if args.oracle_rows else \
-        calibrated_rows(w, inp, per_step)
-    for _ in range(args.warmup):
-        oracle_sample_seconds(w, inp, rows)
-    secs = [oracle_sample_seconds(w, inp, rows) for _ in range(args.steps)]
-    tot = sum(secs)
-    value = rows * len(secs) / tot
-    sample = (f"first {rows} of the {w.t} rows of the workload per step (about {per_step:.0f} s of oracle work "
-              f"each), full oracle (router, CSR, experts), one thread")
+    pool = OraclePool(w, inp, host_cores())
+    try:
+        # each step a bounded sample: the whole run stays within about 150 s
+        per_step = min(10.0, 150.0 / max(1, args.steps + args.warmup))
+        rows = pool.rows_for(per_step)
+        if args.oracle_rows:
+            rows = min(rows, args.oracle_rows)
+        for _ in range(args.warmup):
+            pool.seconds(rows)
+        secs = [pool.seconds(rows) for _ in range(args.steps)]
+    finally:
+        pool.close()
+    mean_s = sum(secs) / len(secs)
+    value = rows / mean_s
+    sample = (f"first {rows} of the {w.t} rows of the workload per step, split over {pool.cores} host cores "
+              f"(one oracle process per core: router, grouping, experts in fp64)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(secs) * w.t / rows,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * mean_s,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": w.name, "t": w.t, "h": w.h, "inter": w.inter, "E": w.E,
-                                        "k": w.k, "shared_inter": w.shared_inter},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+                                        "k": w.k, "shared_inter": w.shared_inter, "rows_per_step": rows,
+                                        "step": f"the oracle over {rows} of the {w.t} rows"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": pool.cores, "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -244,39 +347,69 @@ def run_reference(args, w: synth.Workload):
 # Our arm
 # --------------------------------------------------------------------------
 
-def run_ours(args, w: synth.Workload):
-    import torch
-    import torch.distributed as dist
+class Ctx:
+    """Per-process state of our arm: torch, the binding, ranks, device buffers."""
 
-    from routed_expert_prefill_gb300 import build as B
+    def __init__(self, args):
+        import torch
+        import torch.distributed as dist
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev_name = f"cuda:{local}"
-    if rank == 0 or not os.path.exists(os.path.join(ROOT, "routed_expert_prefill_gb300", "libmoe_gb300.so")):
-        B.build()
-    if world > 1:
-        dist.barrier()
-    from routed_expert_prefill_gb300 import moe
+        from routed_expert_prefill_gb300 import build as B
 
-    inp = synth.make_inputs(w)
-    dev = moe.upload_inputs(inp, dev_name)
-    dims = moe.dims_of(w.t, w.h, w.inter, w.E, w.k, w.shared_inter)
+        self.torch, self.dist, self.args = torch, dist, args
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        if self.world > 1:
+            dist.init_process_group("nccl")
+        torch.cuda.set_device(self.local)
+        self.dev = f"cuda:{self.local}"
+        if self.rank == 0 or not os.path.exists(os.path.join(ROOT, "routed_expert_prefill_gb300",
+                                                             "libmoe_gb300.so")):
+            B.build()
+        self.barrier()
+        from routed_expert_prefill_gb300 import moe
+
+        self.moe = moe
+        self.flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=self.dev)
+        self.weights = {}  # device weights per weight recipe (the decode workloads share one)
+
+    def barrier(self):
+        if self.world > 1:
+            self.dist.barrier()
+
+    def device_inputs(self, w: synth.Workload, inp: dict, flags: int) -> dict:
+        moe, torch = self.moe, self.torch
+        key = (w.h, w.inter, w.E, w.shared_inter, w.seed, w.skew, w.shared_gate)
+        if key not in self.weights:
+            self.weights.clear()
+            torch.cuda.empty_cache()
+            dev = moe.upload_inputs(inp, self.dev)
+            if flags & MOE_PACKED_WEIGHTS:
+                moe.add_packed(dev, moe.dims_of(w.t, w.h, w.inter, w.E, w.k, w.shared_inter))
+            self.weights[key] = dev
+        dev = dict(self.weights[key])
+        dev["x"] = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).to(self.dev)
+        return dev
+
+
+def measure(ctx: Ctx, w: synth.Workload, inp: dict, headline: bool) -> dict:
+    """Time one workload: graph-replayed steps (value), per-kernel events, the
+    sustained run, and the end-to-end loop through the public API."""
+    torch, moe, args = ctx.torch, ctx.moe, ctx.args
     flags = args.flags
-    ws = moe.new_workspace(dims, flags, dev_name)
-    out = torch.empty((w.t, w.h), dtype=torch.bfloat16, device=dev_name)
+    dev = ctx.device_inputs(w, inp, flags)
+    dims = moe.dims_of(w.t, w.h, w.inter, w.E, w.k, w.shared_inter)
+    ws = moe.new_workspace(dims, flags, ctx.dev)
+    out = torch.empty((w.t, w.h), dtype=torch.bfloat16, device=ctx.dev)
     stream = torch.cuda.current_stream()
-    bufs = dict(route=(torch.empty((w.t, w.k), dtype=torch.int32, device=dev_name),
-                       torch.empty((w.t, w.k), dtype=torch.float32, device=dev_name)),
-                csr=moe.Csr(torch.empty(w.E + 1, dtype=torch.int32, device=dev_name),
-                            torch.empty(w.t * w.k, dtype=torch.int32, device=dev_name),
-                            torch.empty(w.t * w.k, dtype=torch.float32, device=dev_name),
-                            torch.empty(w.t * w.k, dtype=torch.int32, device=dev_name)))
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev_name)
+    bufs = dict(route=(torch.empty((w.t, w.k), dtype=torch.int32, device=ctx.dev),
+                       torch.empty((w.t, w.k), dtype=torch.float32, device=ctx.dev)),
+                csr=moe.Csr(torch.empty(w.E + 1, dtype=torch.int32, device=ctx.dev),
+                            torch.empty(w.t * w.k, dtype=torch.int32, device=ctx.dev),
+                            torch.empty(w.t * w.k, dtype=torch.float32, device=ctx.dev),
+                            torch.empty(w.t * w.k, dtype=torch.int32, device=ctx.dev)))
+    flush = ctx.flush
 
     def step():
         return moe.moe_forward(dev, dims, flags, ws=ws, out=out, bufs=bufs)
@@ -286,16 +419,16 @@ def run_ours(args, w: synth.Workload):
     torch.cuda.synchronize()
     status = moe.read_device_status(ws)
     if status != 0:
-        raise RuntimeError(f"device-side status {status} after warm-up")
+        raise RuntimeError(f"{w.name}: device-side status {status} after warm-up")
     counts = np.diff(res["csr"].offsets.cpu().numpy())
     work = step_work(w, counts)
 
-    # ---- device-resident timed region (L2 flushed between steps, untimed).
-    # The step is captured once into a CUDA graph and replayed, so the
-    # timing is the GPU's, not the host's launch rate.
+    # ---- device-resident timed region: the step captured once into a CUDA
+    # graph and replayed, so the timing is the GPU's, not the host's launch
+    # rate; L2 flushed between steps, outside the events.
     graph = None
     if not args.no_graph:
-        side = torch.cuda.Stream(device=dev_name)
+        side = torch.cuda.Stream(device=ctx.dev)
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
             step()
@@ -305,35 +438,48 @@ def run_ours(args, w: synth.Workload):
             step()
         graph.replay()
         torch.cuda.synchronize()
+    run = graph.replay if graph is not None else step
 
-    def timed(run, n):
+    def timed(fn, n):
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         for i in range(n):
             flush.fill_(float(i))
             starts[i].record(stream)
-            run()
+            fn()
             ends[i].record(stream)
         torch.cuda.synchronize()
         return [a.elapsed_time(b) for a, b in zip(starts, ends)]
 
-    sampler = ClockSampler(local)
-    if world > 1:
-        dist.barrier()
+    sampler = ClockSampler(ctx.local)
+    ctx.barrier()
     torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.3)
     wall0 = time.perf_counter()
-    step_ms = timed(graph.replay if graph is not None else step, args.steps)
+    step_ms = timed(run, args.steps)
     wall = time.perf_counter() - wall0
+    ms = max_over_ranks(statistics.median(step_ms), ctx.dev)
+
+    # sustained: the same measurement repeated for >= 1 s and >= 50 runs
+    sustained = None
+    if not args.no_sustain:
+        per = statistics.median(step_ms) + 0.05  # + the flush
+        n = int(min(SUSTAIN_MAX_RUNS, max(SUSTAIN_MIN_RUNS, 1.0 + SUSTAIN_S * 1e3 / per)))
+        s0 = time.perf_counter()
+        sus_ms = timed(run, n)
+        sus_wall = time.perf_counter() - s0
+        sustained = {"runs": n, "median_ms": statistics.median(sus_ms), "mean_ms": sum(sus_ms) / n,
+                     "p10_ms": float(np.percentile(sus_ms, 10)), "p90_ms": float(np.percentile(sus_ms, 90)),
+                     "wall_s": sus_wall, "device_s": sum(sus_ms) / 1e3}
+    clocks = sampler.stop()
+
     # per-kernel device time: the same steps launched directly, each launch
     # bracketed by CUDA events on the launching stream
     moe.profile_enable(True)
     eager_ms = timed(step, args.steps)
     moe.profile_enable(False)
     prof = moe.profile_read()
-    clocks = sampler.stop()
-    ms = max_over_ranks(sum(step_ms) / len(step_ms), dev_name)
     gpu_launches = sum(v[0] for v in prof.values())
 
     # ---- end to end through the public API with host buffers: every step
@@ -349,7 +495,7 @@ def run_ours(args, w: synth.Workload):
     out_hosts = [torch.empty((w.t, w.h), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     x_devs = [torch.empty_like(dev["x"]) for _ in range(2)]
     outs = [out, torch.empty_like(out)]
-    s_in, s_out = torch.cuda.Stream(device=dev_name), torch.cuda.Stream(device=dev_name)
+    s_in, s_out = torch.cuda.Stream(device=ctx.dev), torch.cuda.Stream(device=ctx.dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]    # x of the buffer copied in
     ev_done = [torch.cuda.Event() for _ in range(2)]  # forward done: x free, output ready
     ev_out = [torch.cuda.Event() for _ in range(2)]   # output copied back: buffer free
@@ -382,7 +528,7 @@ def run_ours(args, w: synth.Workload):
             e2e_step(i)
         e1.record(s_out)
         torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev_name)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ctx.dev)
     else:
         e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         e_ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -395,24 +541,17 @@ def run_ours(args, w: synth.Workload):
             out_hosts[0].copy_(outs[0], non_blocking=True)
             e_ends[i].record(stream)
         torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(e_starts, e_ends)) / args.steps, dev_name)
-    x_host_bytes, out_host_bytes = int(x_host.numel() * 2), int(out_hosts[0].numel() * 2)
-
-    if rank != 0:
-        if world > 1:
-            dist.barrier()
-            dist.destroy_process_group()
-        return
+        e2e_ms = max_over_ranks(statistics.median(s.elapsed_time(e) for s, e in zip(e_starts, e_ends)), ctx.dev)
+    if moe.read_device_status(ws) != 0:
+        raise RuntimeError(f"{w.name}: device-side status set during the timed runs")
 
     peaks, peak_src = load_peaks()
-    # dominant kernel = largest share of device time
-    fam_time = {}
-    fam_launch = {}
+    fam_time, fam_launch = {}, {}
     for name, (n, tms) in prof.items():
         f = kernel_family(name)
         fam_time[f] = fam_time.get(f, 0.0) + tms
         fam_launch[f] = fam_launch.get(f, 0) + n
-    dom = max(fam_time, key=fam_time.get)
+    dom = max(fam_time, key=fam_time.get)  # the dominant kernel: largest share of device time
     per_launch_ms = fam_time[dom] / fam_launch[dom]
     launches_per_step = fam_launch[dom] / args.steps
     kw = work["by_kernel"].get(dom)
@@ -420,64 +559,91 @@ def run_ours(args, w: synth.Workload):
     if kw is not None:
         kb = kw["bytes"] / launches_per_step
         kf = kw["flops"] / launches_per_step
-        hbm_t = kb / (peaks["hbm_gbs"] * 1e9)
-        ten_t = kf / (peaks["bf16_tflops"] * 1e12)
-        if hbm_t >= ten_t:
+        if kb / (peaks["hbm_gbs"] * 1e9) >= kf / (peaks["bf16_tflops"] * 1e12):
             ach = kb / (per_launch_ms * 1e-3) / 1e9
             roofline = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": ach / peaks["hbm_gbs"], "traffic": None}
+                        "frac": ach / peaks["hbm_gbs"]}
         else:
             ach = kf / (per_launch_ms * 1e-3) / 1e12
             roofline = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                        "frac": ach / peaks["bf16_tflops"], "traffic": None}
-        roofline["traffic"] = measured_traffic(w.name, dom, flags)
-        roofline.update({"kernel": dom, "peak_source": peak_src,
-                         "kernel_ms_per_launch": per_launch_ms,
+                        "frac": ach / peaks["bf16_tflops"]}
+        roofline.update({"traffic": measured_traffic(w.name, dom, flags), "kernel": dom,
+                         "peak_source": peak_src + " (burst)", "kernel_ms_per_launch": per_launch_ms,
+                         "kernel_share_of_step": fam_time[dom] / sum(fam_time.values()),
                          "algorithmic_bytes_per_launch": kb, "algorithmic_flops_per_launch": kf})
-    t_star = max(work["flops"] / (peaks["bf16_tflops"] * 1e12), work["bytes"] / (peaks["hbm_gbs"] * 1e9))
-    step_bound = "tensor" if work["flops"] / (peaks["bf16_tflops"] * 1e12) > work["bytes"] / (peaks["hbm_gbs"] * 1e9) else "hbm"
+    sr = step_roofline(work, ms, peaks)
+    return dict(
+        name=w.name, value=job_tokens_per_s(ctx.world, w.t, ms), ms=ms, step_ms=step_ms, wall=wall,
+        work=work, step_roofline=sr, roofline=roofline, sustained=sustained, clocks=clocks,
+        eager_ms=statistics.median(eager_ms), gpu_launches=gpu_launches,
+        kernels={k: {"launches": v[0], "ms": v[1]} for k, v in prof.items()},
+        e2e={"value": job_tokens_per_s(ctx.world, w.t, e2e_ms), "unit": "tokens/s",
+             "h2d_bytes_per_step": int(x_host.numel() * 2), "d2h_bytes_per_step": int(out_hosts[0].numel() * 2),
+             "timing": ("steps back to back, copies overlapping neighbouring steps (step bytes exceed L2)"
+                        if pipelined else "each step alone, copies included, L2 flushed between steps; median")},
+        graph=graph is not None, flags=flags)
+
+
+def workload_config(w: synth.Workload, m: dict) -> dict:
+    work, sr = m["work"], m["step_roofline"]
+    return {"workload": w.name, "t": w.t, "h": w.h, "inter": w.inter, "E": w.E, "k": w.k,
+            "shared_inter": w.shared_inter, "routing": "Zipf-skewed" if w.skew else "near-uniform",
+            "flags": m["flags"], "touched_experts": work["touched"], "max_rows_per_expert": work["max_rows"],
+            "step_flops": work["flops"], "step_bytes": work["bytes"], "step_tflops": sr["tflops"],
+            "step_gbs": sr["gbs"], "step_roofline_frac": sr["frac"], "step_bound": sr["bound"],
+            "step_t_star_us": sr["t_star_us"]}
+
+
+def run_ours(args, w: synth.Workload, pool):
+    ctx = Ctx(args)
+    inp = pool.inp if pool is not None else synth.make_inputs(w)
+    m = measure(ctx, w, inp, True)
+    extras = {}
+    for name in args.extra:
+        wx = synth.WORKLOADS[name]
+        mx = measure(ctx, wx, synth.make_inputs(wx), False)
+        extras[name] = dict(
+            value=mx["value"], unit="tokens/s", ms_per_step=mx["ms"], config=workload_config(wx, mx),
+            roofline=mx["roofline"], e2e=mx["e2e"], gpu_launches=mx["gpu_launches"],
+            sustained=mx["sustained"], clocks=mx["clocks"],
+            kernels=mx["kernels"])
+    if ctx.rank != 0:
+        ctx.barrier()
+        if ctx.world > 1:
+            ctx.dist.destroy_process_group()
+        return
 
     cpu = None
-    if not args.no_cpu_baseline:
-        # a bounded sample of about 10 s of oracle work
-        rows = calibrated_rows(w, inp, 10.0)
-        if args.oracle_rows:
-            rows = min(rows, args.oracle_rows)
-        secs = oracle_sample_seconds(w, inp, rows)
-        cpu = {"value": rows / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"first {rows} of {w.t} rows (about 10 s of work), one full oracle pass "
-                         f"(router, CSR, experts), 1 thread"}
+    if pool is not None:
+        cpu = cpu_baseline(pool, w, inp, 10.0, one_core=w.t * w.h * w.inter <= 512 * 2048 * 768)
+        pool.close()
 
-    value = job_tokens_per_s(world, w.t, ms)
+    cfg = workload_config(w, m)
+    cfg.update({"parallelism": f"replicas{ctx.world}",
+                "l2": "flushed between timed steps (2x L2 write, untimed); expert weights also exceed L2",
+                "timing": ("median of the K timed steps, each a CUDA graph replay of one captured step"
+                           if m["graph"] else "median of the K timed steps, eager launches"),
+                "wall_s_timed_region": m["wall"], "eager_ms_per_step": m["eager_ms"],
+                "step_ms_min": min(m["step_ms"]), "step_ms_max": max(m["step_ms"])})
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": m["value"], "unit": "tokens/s", "n_gpus": ctx.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": m["ms"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "t": w.t, "h": w.h, "inter": w.inter, "E": w.E, "k": w.k,
-                   "shared_inter": w.shared_inter, "flags": flags, "parallelism": f"replicas{world}",
-                   "l2": "flushed between timed steps (2x L2 write, untimed); expert weights also exceed L2",
-                   "touched_experts": work["touched"], "max_rows_per_expert": work["max_rows"],
-                   "step_flops": work["flops"], "step_bytes": work["bytes"],
-                   "step_tflops": work["flops"] / (ms * 1e-3) / 1e12,
-                   "step_gbs": work["bytes"] / (ms * 1e-3) / 1e9,
-                   "step_roofline_frac": t_star / (ms * 1e-3), "step_bound": step_bound,
-                   "wall_s_timed_region": wall,
-                   "timing": "eager launches" if graph is None else "CUDA graph replay of one captured step",
-                   "eager_ms_per_step": sum(eager_ms) / len(eager_ms)},
-        "roofline": roofline,
+        "config": cfg,
+        "step_roofline_frac": m["step_roofline"]["frac"],
+        "roofline": m["roofline"],
         "cpu_baseline": cpu,
-        "e2e": {"value": job_tokens_per_s(world, w.t, e2e_ms), "unit": "tokens/s",
-                "h2d_bytes_per_step": x_host_bytes, "d2h_bytes_per_step": out_host_bytes,
-                "timing": ("steps back to back, copies overlapping neighbouring steps (step bytes exceed L2)"
-                           if pipelined else "each step alone, copies included, L2 flushed between steps")},
-        "gpu_launches": gpu_launches,
-        "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in prof.items()},
-        "clocks": clocks,
+        "e2e": m["e2e"],
+        "gpu_launches": m["gpu_launches"],
+        "sustained": m["sustained"],
+        "kernels": m["kernels"],
+        "clocks": m["clocks"],
+        "workloads": extras,
     }
     print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.barrier()
-        dist.destroy_process_group()
+    ctx.barrier()
+    if ctx.world > 1:
+        ctx.dist.destroy_process_group()
 
 
 def main():
@@ -487,16 +653,36 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--flags", type=int, default=16, help="moe_experts_fwd flags (16: packed weights)")
+    ap.add_argument("--workloads", default="default",
+                    help="extra workloads timed in the same run: comma list, 'none', or 'default' "
+                         "(the other benchmark workloads when the headline one is timed)")
+    ap.add_argument("--flags", type=int, default=MOE_PACKED_WEIGHTS, help="moe_experts_fwd flags (16: packed weights)")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of graph replays")
+    ap.add_argument("--no-sustain", action="store_true", help="skip the >= 1 s sustained measurement")
     ap.add_argument("--oracle-rows", type=int, default=0, help="cap on the oracle sample's rows (0: time-budgeted)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.impl == "ours" and args.warmup < 3:
+        ap.error("--warmup must be at least 3")
     w = synth.WORKLOADS[args.workload]
+    if args.workloads == "default":
+        args.extra = [n for n in EXTRA_WORKLOADS if n != w.name] if w.name == DEFAULT_WORKLOAD else []
+    elif args.workloads == "none":
+        args.extra = []
+    else:
+        args.extra = [n for n in args.workloads.split(",") if n]
+        for n in args.extra:
+            if n not in synth.WORKLOADS:
+                ap.error(f"unknown workload {n}")
     if args.impl == "reference":
         run_reference(args, w)
-    else:
-        run_ours(args, w)
+        return
+    # the oracle pool forks before any CUDA call (rank 0 of a 1-GPU run only)
+    pool = None
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if not args.no_cpu_baseline and world == 1:
+        pool = OraclePool(w, synth.make_inputs(w), host_cores())
+    run_ours(args, w, pool)
 
 
 if __name__ == "__main__":

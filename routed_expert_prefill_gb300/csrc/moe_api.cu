@@ -18,8 +18,9 @@ cudaError_t launch_route_tc(const uint16_t* x, const uint16_t* wr, const float* 
 bool route_builds_csr(int t);
 cudaError_t launch_build_csr(const int32_t* idx, const float* w, int t, int k, int E, const moe_csr& csr,
                              unsigned char* ws, const WsLayout& L, cudaStream_t stream);
-cudaError_t launch_experts_fast(const ExpertsArgs& a, uint32_t flags, cudaStream_t stream);
-size_t experts_sched_bytes(const moe_dims& d);
+cudaError_t launch_experts_tc(const ExpertsArgs& a, bool deterministic, cudaStream_t stream);
+size_t tc_sched_bytes(const moe_dims& d);
+size_t packed_max_tiles(const moe_dims& d);
 size_t packed_record_bytes(int h, int I);
 size_t packed_pad_rows(const moe_dims& d);
 cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, const uint16_t* biases, int h, int I,
@@ -38,6 +39,16 @@ size_t gemv_part_bytes(const moe_dims& d);
 // weight and row.
 constexpr int SMALL_T_MAX = 16;
 constexpr int SMALL_T_UNITS = 152;
+
+// Scheduler scratch: room for the larger of the two tensor-core paths' tile
+// lists (the packed path's, on its smallest tiles, or the row-major path's).
+size_t experts_sched_bytes(const moe_dims& d) {
+  const size_t mt = packed_max_tiles(d);
+  const int fmax = (d.inter > d.shared_inter ? d.inter : d.shared_inter) / 128;
+  const size_t packed = 64 + mt * 16 + mt * fmax * 4 + (size_t)d.t * 4 + 256;
+  const size_t rowmajor = tc_sched_bytes(d);
+  return packed > rowmajor ? packed : rowmajor;
+}
 
 static thread_local char g_err[512] = "";
 
@@ -299,7 +310,7 @@ int moe_experts_fwd(const uint16_t* x, const moe_csr* csr, const moe_qweights* e
                        "moe_experts_fwd launch");
   if (flags & MOE_SIMPLE_KERNELS)
     return cuda_status(launch_experts_simple(a, (flags & MOE_DETERMINISTIC) != 0, s), "moe_experts_fwd launch");
-  return cuda_status(launch_experts_fast(a, flags, s), "moe_experts_fwd launch");
+  return cuda_status(launch_experts_tc(a, (flags & MOE_DETERMINISTIC) != 0, s), "moe_experts_fwd launch");
 }
 
 size_t moe_packed_bytes(const moe_dims* dims, int shared) {

@@ -173,6 +173,61 @@ def _u16(t: torch.Tensor) -> torch.Tensor:
     return t
 
 
+_BF16 = (torch.bfloat16, torch.int16, torch.uint16)  # bf16 values or their bit patterns
+_F16 = (torch.float16, torch.int16, torch.uint16)
+
+
+def _need(t, name: str, dtypes, shape=None, min_numel=None):
+    """Check what the C ABI cannot see: dtype, layout, size and device.
+
+    The library receives bare pointers, so a wrong dtype, a strided view,
+    a short buffer or a tensor on another GPU would otherwise turn into
+    out-of-bounds accesses on the device."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} must have dtype {' or '.join(str(d) for d in dtypes)}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if min_numel is not None and t.numel() < min_numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, needs at least {min_numel}")
+    return t
+
+
+def _on_current_device(**named):
+    """Every tensor must live on the current CUDA device (the library launches there)."""
+    cur = None
+    for name, t in named.items():
+        if t is None:
+            continue
+        if t.device.type != "cuda":
+            raise ValueError(f"{name} must be on a CUDA device, got {t.device}")
+        if cur is None:
+            cur = torch.cuda.current_device()
+        if t.device.index != cur:
+            raise ValueError(f"{name} is on {t.device} but the current device is cuda:{cur}")
+
+
+def _need_csr(c: "Csr", name: str, E: int, n: int):
+    _need(c.offsets, f"{name}.offsets", (torch.int32,), min_numel=E + 1)
+    _need(c.rows, f"{name}.rows", (torch.int32,), min_numel=n)
+    _need(c.weights, f"{name}.weights", (torch.float32,), min_numel=n)
+    _need(c.slot_of, f"{name}.slot_of", (torch.int32,), min_numel=n)
+    return c
+
+
+def _csr_named(c, name: str) -> dict:
+    if c is None:
+        return {}
+    return {f"{name}.{f}": getattr(c, f) for f in ("offsets", "rows", "weights", "slot_of")}
+
+
+def _need_ws(ws, dims: "MoeDims", flags: int):
+    return _need(ws, "ws", (torch.uint8,), min_numel=workspace_bytes(dims, flags))
+
+
 def moe_route_topk(x: torch.Tensor, wr: torch.Tensor, k: int, rbias: torch.Tensor | None = None,
                    want_logits: bool = False, out=None, ws: torch.Tensor | None = None, exact_pass: bool = False,
                    stream=None):
@@ -183,16 +238,27 @@ def moe_route_topk(x: torch.Tensor, wr: torch.Tensor, k: int, rbias: torch.Tenso
     give the same idx and w.
     """
     lib = load_library()
+    if x.dim() != 2 or wr.dim() != 2:
+        raise ValueError("x must be [t, h] and wr [E, h]")
     t, h = x.shape
     E = wr.shape[0]
+    _need(x, "x", _BF16)
+    _need(wr, "wr", _BF16, shape=(E, h))
+    if rbias is not None:
+        _need(rbias, "rbias", (torch.float32,), shape=(E,))
     dims = MoeDims(t, h, 128, E, k, 0)
     if out is None:
         idx = torch.empty((t, k), dtype=torch.int32, device=x.device)
         w = torch.empty((t, k), dtype=torch.float32, device=x.device)
     else:
         idx, w = out
+        _need(idx, "idx", (torch.int32,), shape=(t, k))
+        _need(w, "w", (torch.float32,), shape=(t, k))
     logits = torch.empty((t, E), dtype=torch.float32, device=x.device) if want_logits else None
     use_ws = not (want_logits or exact_pass)
+    if use_ws and ws is not None:
+        _need_ws(ws, dims, 0)
+    _on_current_device(x=x, wr=wr, rbias=rbias, idx=idx, w=w, ws=ws if use_ws else None)
     if use_ws and ws is None:
         ws = new_workspace(dims, 0, x.device, stream)
     wsp, wsn = (_ptr(ws), ws.numel()) if use_ws else (None, 0)
@@ -205,8 +271,17 @@ def moe_build_csr(idx: torch.Tensor, w: torch.Tensor, E: int, ws: torch.Tensor |
                   out: Csr | None = None, stream=None) -> Csr:
     """Group (row, slot) pairs by expert: offsets [E+1], rows/weights/slot_of [t*k]."""
     lib = load_library()
+    if idx.dim() != 2:
+        raise ValueError("idx must be [t, k]")
     t, k = idx.shape
+    _need(idx, "idx", (torch.int32,))
+    _need(w, "w", (torch.float32,), shape=(t, k))
     dims = MoeDims(t, 128, 128, E, k, 0)
+    if ws is not None:
+        _need_ws(ws, dims, 0)
+    if out is not None:
+        _need_csr(out, "out", E, t * k)
+    _on_current_device(idx=idx, w=w, ws=ws, **_csr_named(out, "out"))
     if ws is None:
         ws = new_workspace(dims, 0, idx.device, stream)
     if out is None:
@@ -227,15 +302,29 @@ def moe_route_csr(x: torch.Tensor, wr: torch.Tensor, k: int, rbias: torch.Tensor
     (tensor-core path) followed by moe_build_csr, with one launch fewer for
     t <= 16 rows."""
     lib = load_library()
+    if x.dim() != 2 or wr.dim() != 2:
+        raise ValueError("x must be [t, h] and wr [E, h]")
     t, h = x.shape
     E = wr.shape[0]
+    _need(x, "x", _BF16)
+    _need(wr, "wr", _BF16, shape=(E, h))
+    if rbias is not None:
+        _need(rbias, "rbias", (torch.float32,), shape=(E,))
     dims = MoeDims(t, h, 128, E, k, 0)
     dev = x.device
+    idx = w = None
+    if out_route is not None:
+        idx, w = out_route
+        _need(idx, "idx", (torch.int32,), shape=(t, k))
+        _need(w, "w", (torch.float32,), shape=(t, k))
+    if out_csr is not None:
+        _need_csr(out_csr, "out_csr", E, t * k)
+    if ws is not None:
+        _need_ws(ws, dims, 0)
+    _on_current_device(x=x, wr=wr, rbias=rbias, idx=idx, w=w, ws=ws, **_csr_named(out_csr, "out_csr"))
     if out_route is None:
         idx = torch.empty((t, k), dtype=torch.int32, device=dev)
         w = torch.empty((t, k), dtype=torch.float32, device=dev)
-    else:
-        idx, w = out_route
     if out_csr is None:
         out_csr = Csr(torch.empty(E + 1, dtype=torch.int32, device=dev),
                       torch.empty(t * k, dtype=torch.int32, device=dev),
@@ -255,8 +344,15 @@ def moe_build_csr_noalloc(idx: torch.Tensor, w: torch.Tensor, E: int, out: Csr |
     (for callers that may not allocate; at most MOE_NOALLOC_MAX_PAIRS = 65536
     (row, slot) pairs).  Only the output tensors are the caller's."""
     lib = load_library()
+    if idx.dim() != 2:
+        raise ValueError("idx must be [t, k]")
     t, k = idx.shape
+    _need(idx, "idx", (torch.int32,))
+    _need(w, "w", (torch.float32,), shape=(t, k))
     dims = MoeDims(t, 128, 128, E, k, 0)
+    if out is not None:
+        _need_csr(out, "out", E, t * k)
+    _on_current_device(idx=idx, w=w, **_csr_named(out, "out"))
     if out is None:
         dev = idx.device
         out = Csr(torch.empty(E + 1, dtype=torch.int32, device=dev),
@@ -274,6 +370,35 @@ def moe_experts_fwd(x: torch.Tensor, csr: Csr, experts: tuple, shared: tuple | N
     """Expert FFNs.  experts = (codes u8 [E, rec], scales f16 [E, g], biases f16 [E, g]);
     shared = (codes, scales, biases, gate-or-None) or None."""
     lib = load_library()
+    t, h, I, Is, E, k = dims.t, dims.h, dims.inter, dims.shared_inter, dims.E, dims.k
+    _need(x, "x", _BF16, shape=(t, h))
+    _need_csr(csr, "csr", E, t * k)
+    packed = bool(flags & MOE_PACKED_WEIGHTS)
+
+    def need_record(rec, name, n_rec, inter):
+        if packed:
+            nbytes = lib.moe_packed_bytes(ctypes.byref(MoeDims(t, h, I, E, k, Is)), 1 if name == "shared" else 0)
+            _need(rec[0], f"{name} codes", (torch.uint8,), min_numel=nbytes)
+        else:
+            _need(rec[0], f"{name} codes", (torch.uint8,), min_numel=n_rec * 3 * inter * h // 2)
+            _need(rec[1], f"{name} scales", _F16, min_numel=n_rec * 3 * inter * h // 64)
+            _need(rec[2], f"{name} biases", _F16, min_numel=n_rec * 3 * inter * h // 64)
+
+    need_record(experts, "experts", E, I)
+    if Is > 0:
+        if shared is None:
+            raise ValueError("dims.shared_inter > 0 but no shared expert given")
+        need_record(shared, "shared", 1, Is)
+        if shared[3] is not None:
+            _need(shared[3], "shared gate", _BF16, shape=(h,))
+    if ws is not None:
+        _need_ws(ws, dims, flags)
+    if out is not None:
+        _need(out, "out", _BF16, shape=(t, h))
+    recs = {f"experts[{i}]": experts[i] for i in range(3)}
+    if Is > 0:
+        recs.update({f"shared[{i}]": shared[i] for i in range(4)})
+    _on_current_device(x=x, ws=ws, out=out, **_csr_named(csr, "csr"), **recs)
     if ws is None:
         ws = new_workspace(dims, flags, x.device, stream)
     if out is None:
@@ -311,6 +436,11 @@ def pack_experts(codes: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor
     n = lib.moe_packed_bytes(ctypes.byref(dims), 1 if shared else 0)
     if n == 0:
         raise MoeError(-2, "nothing to pack for these dims")
+    n_rec, inter = (1, dims.shared_inter) if shared else (dims.E, dims.inter)
+    _need(codes, "codes", (torch.uint8,), min_numel=n_rec * 3 * inter * dims.h // 2)
+    _need(scales, "scales", _F16, min_numel=n_rec * 3 * inter * dims.h // 64)
+    _need(biases, "biases", _F16, min_numel=n_rec * 3 * inter * dims.h // 64)
+    _on_current_device(codes=codes, scales=scales, biases=biases)
     dst = torch.empty(n, dtype=torch.uint8, device=codes.device)
     q = MoeQWeights(codes.data_ptr(), scales.data_ptr(), biases.data_ptr())
     _check(lib.moe_pack_experts(ctypes.byref(q), ctypes.byref(dims), 1 if shared else 0, _ptr(dst), n,
@@ -358,11 +488,13 @@ def add_packed(dev: dict, dims: MoeDims, stream=None) -> dict:
     return dev
 
 
-def moe_forward(dev: dict, dims: MoeDims, flags: int = 0, ws: torch.Tensor | None = None,
+def moe_forward(dev: dict, dims: MoeDims, flags: int = MOE_PACKED_WEIGHTS, ws: torch.Tensor | None = None,
                 out: torch.Tensor | None = None, stream=None, bufs: dict | None = None) -> dict:
     """Router -> CSR -> experts on one stream; returns the intermediate tensors too.
 
-    With MOE_PACKED_WEIGHTS in `flags` the packed records of add_packed() are used."""
+    By default (MOE_PACKED_WEIGHTS in `flags`) the packed records of
+    add_packed() are used, made on the first call when absent; flags without
+    it run the row-major records as uploaded."""
     if flags & MOE_PACKED_WEIGHTS and "packed" not in dev:
         add_packed(dev, dims, stream)
     if ws is None:

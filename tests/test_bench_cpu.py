@@ -39,8 +39,11 @@ def test_reference_arm_json_line():
     e = d["e2e"]
     assert e["value"] == d["value"] and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
-    # ms_per_step is the time of one whole step (all t rows), from the sampled rows
-    assert d["ms_per_step"] == pytest.approx(1e3 * d["config"]["t"] / d["value"], rel=1e-6)
+    # ms_per_step is the measured time of one step, the oracle over the rows it ran
+    rows = d["config"]["rows_per_step"]
+    assert 1 <= rows <= d["config"]["t"]
+    assert d["ms_per_step"] == pytest.approx(1e3 * rows / d["value"], rel=1e-6)
+    assert cb["cores"] == bench.host_cores()
 
 
 def test_step_work_counts():
@@ -72,3 +75,22 @@ def test_measured_traffic_is_tied_to_the_kernel_sources():
     for (wl, fam, fl), m in bench.MEASURED_TRAFFIC.items():
         got = bench.measured_traffic(wl, fam, fl)
         assert got is None or got == m["bytes"]
+
+
+def test_oracle_pool_rows_and_time():
+    """The pooled oracle runs the whole sample, split over the cores, in one timed pass."""
+    w = synth.WORKLOADS["tiny_t16_h256_e8"]
+    pool = bench.OraclePool(w, synth.make_inputs(w), 2)
+    try:
+        assert pool.seconds(5) > 0
+        assert 4 <= pool.rows_for(0.01) <= w.t
+    finally:
+        pool.close()
+
+
+def test_step_roofline_picks_the_slower_bound():
+    peaks = {"bf16_tflops": 2000.0, "hbm_gbs": 8000.0}
+    sr = bench.step_roofline({"flops": 2e12, "bytes": 8e9}, 2.0, peaks)  # 1.0 ms tensor, 1.0 ms HBM
+    assert sr["frac"] == pytest.approx(0.5)
+    sr = bench.step_roofline({"flops": 4e12, "bytes": 8e9}, 4.0, peaks)
+    assert sr["bound"] == "tensor" and sr["frac"] == pytest.approx(0.5)

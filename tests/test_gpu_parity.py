@@ -407,17 +407,85 @@ def test_shape_errors_raise(moe):
 BIG = ["t4096_h2048_e128_skewed", "t4096_h4096_e256"]
 
 
+def _oracle_router(w: synth.Workload, inp: dict):
+    """The oracle's logits, ids and weights for every row of a workload."""
+    key = ("router", w)
+    if key not in _cache:
+        lg = O.route_logits(inp["x"], inp["wr"], inp.get("rbias"))
+        idx, wt = O.route_topk(lg, w.k)
+        _cache[key] = (lg, idx, wt)
+    return _cache[key]
+
+
+@pytest.mark.parametrize("name", BIG)
+def test_full_size_router_matches_oracle_every_row(moe, name):
+    """Full size, every row: the fixed-order logits bit-equal the oracle's, and
+    both router implementations give the oracle's ids (weights within 2e-6)."""
+    w = synth.WORKLOADS[name]
+    inp = _inputs(w)
+    lg, ref_idx, ref_w = _oracle_router(w, inp)
+    dev = moe.upload_inputs(inp)
+    idx0, wt0, logits = moe.moe_route_topk(dev["x"], dev["wr"], w.k, dev["rbias"], want_logits=True)
+    idx1, wt1, audit, _ = _route_tc(moe, dev, w)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(logits.cpu().numpy().view(np.uint32), lg.view(np.uint32))
+    for idx, wt in ((idx0, wt0), (idx1, wt1)):
+        np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+        assert np.abs(wt.cpu().numpy() - ref_w).max() <= 2e-6
+    assert audit <= 0.25
+
+
+def _tile_edges(n: int, tile_maxes=(64, 128, 144, 160, 176, 192, 256)) -> set:
+    """List positions of the first and last row of every tile an expert's n
+    rows can be cut into: ceil(n / m) near-equal tiles for each tile height m
+    the kernels use."""
+    edges = {0, n - 1}
+    for m in tile_maxes:
+        nt = -(-n // m)
+        sz = -(-n // nt)
+        for i in range(nt):
+            a = i * sz
+            if a < n:
+                edges |= {a, min(n, a + sz) - 1}
+    return edges
+
+
+def _sample_rows(w: synth.Workload, idx: np.ndarray, n_rows: int = 512) -> np.ndarray:
+    """512 rows of a full-size chunk: the first and last row of every possible
+    tile of the hottest expert, rows of the coldest non-empty experts, the
+    chunk's first and last rows, and random rows for the rest."""
+    offsets, rows, _, _ = O.build_csr(idx, np.zeros(idx.shape, np.float32), w.E)
+    counts = np.diff(offsets)
+    hot = int(np.argmax(counts))
+    pick = {int(rows[offsets[hot] + p]) for p in _tile_edges(int(counts[hot]))}
+    for e in np.argsort(counts, kind="stable"):
+        if counts[e] > 0 and len(pick) < n_rows // 2:
+            pick |= {int(r) for r in rows[offsets[e]:offsets[e + 1]][:4]}
+    pick |= {0, w.t - 1}
+    rng = np.random.default_rng(99)
+    rest = rng.permutation(np.setdiff1d(np.arange(w.t), np.fromiter(pick, int)))
+    pick |= {int(r) for r in rest[: max(0, n_rows - len(pick))]}
+    return np.sort(np.fromiter(pick, int))
+
+
 @pytest.mark.parametrize("name", BIG)
 @pytest.mark.parametrize("packed", [False, True])
 def test_full_size_sampled_rows(moe, name, packed):
-    """Full-size run in the benchmark's launch configuration; oracle on 96 sampled rows."""
+    """Full-size run in the benchmark's launch configuration; the oracle on at
+    least 512 rows, including the first and last row of every tile of the
+    hottest expert.  MOE_FULL_PARITY=1 checks every row instead (slow: the
+    oracle then runs the whole chunk)."""
+    import os
+
     w = synth.WORKLOADS[name]
     inp = _inputs(w)
-    rows = np.sort(np.random.default_rng(99).choice(w.t, 96, replace=False))
+    _, ref_idx, _ = _oracle_router(w, inp)
+    rows = np.arange(w.t) if os.environ.get("MOE_FULL_PARITY") == "1" else _sample_rows(w, ref_idx)
+    assert len(rows) >= 512
     ref = _oracle_rows(w, inp, rows)
     res, status = _run(moe, w, inp, moe.MOE_PACKED_WEIGHTS if packed else 0)
     assert status == 0
-    np.testing.assert_array_equal(res["idx"].cpu().numpy()[rows], ref["idx"])
+    np.testing.assert_array_equal(res["idx"].cpu().numpy(), ref_idx)
     _check_csr_against(res["csr"], res["idx"], res["w"], w.E)
     _check_out(res["out"][torch.from_numpy(rows).cuda()], ref["out"])
     if name.endswith("skewed"):

@@ -285,14 +285,50 @@ def test_shared_gate_closed_form():
         np.testing.assert_allclose(res1["out"][r], res0["out"][r] - (1.0 - sig) * ys[r], rtol=0, atol=1e-12)
 
 
-def test_k1_single_expert_is_dense_ffn():
-    # E = 1, k = 1: every row goes to expert 0 with weight 1.
-    w = synth.Workload("d", 7, 256, 64, 1, 1, 64, 12)
-    inp = synth.make_inputs(w)
-    inp["shared_codes"] = np.full_like(inp["shared_codes"], 0x88)
-    res = O.moe_forward(inp, 1, w.h, w.inter, w.shared_inter)
+def _record_from_dense(rng, h: int, inter: int):
+    """A quantised record built forward from known integer codes: returns the
+    record's bytes (this test's own packing: two codes per byte, low nibble at
+    the even K index), its fp16 scales and biases (b = -8 s), and the three
+    dense matrices W = (q - 8) * s as float64 torch tensors."""
+    import torch
+
+    mats, code_bytes, scales, biases = [], [], [], []
+    for rows, K in ((inter, h), (inter, h), (h, inter)):
+        q = rng.integers(0, 16, size=(rows, K))
+        s = rng.uniform(0.005, 0.02, size=(rows, K // 64)).astype(np.float16)
+        b = (s * np.float16(-8)).astype(np.float16)
+        packed = (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8)
+        code_bytes.append(packed.ravel())
+        scales.append(s.ravel())
+        biases.append(b.ravel())
+        s_full = torch.from_numpy(s.astype(np.float64)).repeat_interleave(64, dim=1)
+        mats.append((torch.from_numpy(q.astype(np.float64)) - 8.0) * s_full)
+    return np.concatenate(code_bytes), np.concatenate(scales), np.concatenate(biases), mats
+
+
+def test_e1_k1_is_a_dense_ffn_chain():
+    """E = 1, k = 1: routing, grouping, gather and weighted scatter reduce to
+    the identity, so the block output is the shared FFN plus one dense FFN.
+    The expected value is a plain float64 torch matmul chain over matrices
+    built from the codes directly (not through the oracle's unpacking)."""
+    import torch
+
+    rng = np.random.default_rng(21)
+    t, h, inter, Is = 9, 256, 128, 64
+    codes, scales, biases, (G, U, D) = _record_from_dense(rng, h, inter)
+    s_codes, s_scales, s_biases, (SG, SU, SD) = _record_from_dense(rng, h, Is)
+    x = _bf16(rng.standard_normal((t, h)))
+    wr = _bf16(rng.standard_normal((1, h)))
+    inp = dict(x=x, wr=wr, rbias=None, codes=codes[None], scales=scales[None], biases=biases[None],
+               shared_codes=s_codes, shared_scales=s_scales, shared_biases=s_biases, shared_gate=None)
+    res = O.moe_forward(inp, 1, h, inter, Is)
     assert np.all(res["idx"] == 0) and np.all(res["w"] == 1.0)
-    assert res["offsets"].tolist() == [0, 7] and res["rows"].tolist() == list(range(7))
+    assert res["offsets"].tolist() == [0, t] and res["rows"].tolist() == list(range(t))
+    X = torch.from_numpy(synth.bf16_bits_to_f32(x).astype(np.float64))
+    silu = torch.nn.functional.silu
+    want = (silu(X @ SG.T) * (X @ SU.T)) @ SD.T + (silu(X @ G.T) * (X @ U.T)) @ D.T
+    err = np.abs(res["out"] - want.numpy()).max()
+    assert err <= 1e-12 * np.abs(want.numpy()).max()
 
 
 def test_skewed_recipe_concentrates_rows():

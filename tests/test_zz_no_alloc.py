@@ -33,10 +33,30 @@ def _routing(t, k, E, seed):
     return torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda()
 
 
+def _same(got, ref, oracle):
+    for name in ("offsets", "rows", "slot_of"):
+        np.testing.assert_array_equal(getattr(got, name).cpu().numpy(), getattr(ref, name).cpu().numpy(), name)
+    np.testing.assert_array_equal(got.weights.cpu().numpy().view(np.uint32),
+                                  ref.weights.cpu().numpy().view(np.uint32))
+    # and the grouping the oracle computes from the same ids and weights
+    offsets, rows, weights, slot_of = oracle
+    np.testing.assert_array_equal(got.offsets.cpu().numpy(), offsets)
+    np.testing.assert_array_equal(got.rows.cpu().numpy(), rows)
+    np.testing.assert_array_equal(got.slot_of.cpu().numpy(), slot_of)
+    np.testing.assert_array_equal(got.weights.cpu().numpy().view(np.uint32), weights.view(np.uint32))
+
+
 def test_noalloc_csr_matches_workspace_csr_on_consecutive_calls(moe):
-    # a large call, then a smaller one on top of the first one's leftovers,
-    # then one with a skewed id histogram
-    for t, k, E, seed in ((4096, 8, 128, 1), (37, 4, 16, 2), (8192, 8, 256, 3)):
+    from oracle import moe_oracle as O
+
+    # A large call; a tiny one (one-block path); a smaller one that still
+    # takes the multi-block path over the first calls' leftovers; one with a
+    # skewed id histogram; and one whose per-chunk count table exactly fills
+    # the fixed scratch (E = 1024, 65536 pairs).  Each is checked against the
+    # workspace variant and against the oracle's grouping.
+    cases = ((4096, 8, 128, 1), (37, 4, 16, 2), (300, 8, 64, 4), (8192, 8, 256, 3), (8192, 8, 1024, 5),
+             (300, 8, 64, 6))
+    for t, k, E, seed in cases:
         idx, w = _routing(t, k, E, seed)
         if seed == 3:
             idx[: t // 2, 0] = 5  # half the rows share one expert first
@@ -44,10 +64,7 @@ def test_noalloc_csr_matches_workspace_csr_on_consecutive_calls(moe):
         ref = moe.moe_build_csr(idx, w, E)
         got = moe.moe_build_csr_noalloc(idx, w, E)
         torch.cuda.synchronize()
-        for name in ("offsets", "rows", "slot_of"):
-            np.testing.assert_array_equal(getattr(got, name).cpu().numpy(), getattr(ref, name).cpu().numpy(), name)
-        np.testing.assert_array_equal(got.weights.cpu().numpy().view(np.uint32),
-                                      ref.weights.cpu().numpy().view(np.uint32))
+        _same(got, ref, O.build_csr(idx.cpu().numpy(), w.cpu().numpy(), E))
 
 
 def test_noalloc_rejects_more_pairs_than_its_scratch_holds(moe):
