@@ -21,9 +21,10 @@
 //   gather:   the token rows of every tile are copied, chunk by chunk, into
 //     the 128-byte-swizzled K-major image the MMA reads (xg), so one bulk
 //     copy moves a whole B stage.
-//   gateup:   warp 0 streams packed weight blocks (one bulk copy per two K
-//     chunks), warp 10 streams xg stages, two groups of four warps take
-//     alternate stages and dequantise one weight row per thread
+//   gateup:   warp 0 streams packed weight blocks (one bulk copy per stage
+//     of one or two K chunks), warp 10 streams xg stages, two groups of
+//     four warps take alternate stages and dequantise one weight row per
+//     thread
 //     (w = fma(q, s, b) in bf16) straight into TMEM with tcgen05.st, warps 1
 //     and 15 issue the gate and the up tcgen05.mma streams with A in TMEM
 //     and B in shared memory, and one or two four-warp epilogue groups drain
@@ -47,10 +48,14 @@ namespace {
 
 using namespace tc;
 
-// Rows per tile (MMA N): 128, or 64 for chunks whose experts see few rows
-// each -- the smaller accumulators then leave room for a deeper A ring.
+// Rows per tile (MMA N): 128; 64 for chunks whose experts see few rows each
+// (the smaller accumulators then leave room for a deeper A ring); 192 for
+// chunks whose experts see about 100 rows or more (one tile per expert
+// instead of two part-empty ones, and each dequantised weight block serves
+// more tokens).
 constexpr int PTILE = 128;
 constexpr int PTILE_SMALL = 64;
+constexpr int PTILE_LARGE = 192;  // experts with ~100 rows or more: one tile for up to 192 rows
 constexpr int KC = 64;      // K per chunk = one quantisation group
 constexpr int QB = 4096 + 256 + 256;  // one packed 128 x 64 block
 constexpr uint64_t WAIT_NS = 2000000000ull;
@@ -65,7 +70,7 @@ constexpr int W_CODE = 0, W_MMA = 1, W_DQ0 = 2, W_B = 10, W_EPI0 = 11, W_MMA2 = 
 constexpr int KWARPS = 20;
 constexpr int KTHREADS = KWARPS * 32;
 constexpr int KTHREADS_1 = 16 * 32;
-constexpr int B_RING = 131072;        // bytes of token-tile stages (see PCfg::SB, PCfg::B_STAGE)
+constexpr int SMEM_MAX = 232448;      // dynamic shared memory of one CTA (227 KB)
 constexpr int CPS_DEFAULT = 2;        // K chunks per code stage and per A stage (see PCfg)
 
 // TMEM (512 columns): NACC accumulator buffers of ACC_COLS columns (gate/up:
@@ -78,24 +83,39 @@ struct PCfg {
   static constexpr int CPS = CP;
   static constexpr int NMAT = GATEUP ? 2 : 1;
   static constexpr int C_STAGE = CPS * NMAT * QB;        // packed blocks of one stage
-  static constexpr int SC = 73728 / C_STAGE;             // code stages (72 KB)
+  // Code stages: four (measured: the code producer stays several stages
+  // ahead of the dequantisation with four; more gave nothing), so that the
+  // token-tile ring gets the rest of shared memory.
+  static constexpr int SC = 4;
   static constexpr int A_STAGE = CPS * NMAT * 32;        // TMEM columns per A stage
   static constexpr int NACC = GATEUP ? 1 : 2;            // accumulator buffers
   static constexpr int ACC_COLS = GATEUP ? 2 * PT : PT;  // TMEM columns per accumulator buffer
   static constexpr int A_COL = NACC * ACC_COLS;          // first column of the A ring
-  static constexpr int SA = (512 - A_COL) / A_STAGE;     // A stages: 2 / 4 at PT 128, 3 / 3 at PT 64
+  static constexpr int SA = (512 - A_COL) / A_STAGE;     // A stages: 2 / 4 at PT 128, 3 / 3 at PT 64, 2 / 2 at PT 192
   static constexpr int NISS = GATEUP ? 2 : 1;            // MMA issuing threads (gate and up apart)
-  // token-tile stages: 4 x 32 KB, or 2 x 64 KB when a stage of CP chunks of
-  // 128 rows needs it (every A stage must read a single B stage)
-  static constexpr int B_STAGE = CP * PT * 128 > 32768 ? 65536 : 32768;
-  static constexpr int SB = B_RING / B_STAGE;
+  // Token-tile stages, and the ring takes all the shared memory the code
+  // ring, the epilogue staging and the barriers leave.  On 192-row tiles a
+  // stage holds CP chunks of a full tile (every A stage reads a single B
+  // stage) and the ring is seven stages deep: the gathered token images
+  // arrive several stage times after they are requested, so the ring's
+  // depth is what hides that latency.  On smaller tiles a stage is 32 or 64
+  // KB and holds as many chunks as fit (fewer, larger stages measured
+  // faster there).
+  static constexpr int B_STAGE =
+      PT > 128 ? CP * PT * 128 : (CP * PT * 128 > 32768 ? 65536 : 32768);
+  static constexpr int EPI_BYTES = (GATEUP ? 1 : 8) * PT * 8 + 8 * (GATEUP ? 16 * 16 : 16 * 32) * 4;
+  static constexpr int SB_FIT = (SMEM_MAX - 1024 - SC * C_STAGE - EPI_BYTES - 1024) / B_STAGE;
+  static constexpr int SB = SB_FIT > 16 ? 16 : SB_FIT;
+  static constexpr int B_RING = SB * B_STAGE;
   // A-ring slots released block by block (an empty barrier per block,
   // committed after that block's MMAs) rather than per stage: lets a
   // dequantisation group start rewriting a slot while the tensor pipe still
   // reads its later blocks.  Pays for the extra waits and commits on the
-  // gate/up pass with 128-row tiles only.
-  static constexpr bool BLK_REL = GATEUP && PT == 128;
+  // gate/up pass with tiles of 128 rows or more only.
+  static constexpr bool BLK_REL = GATEUP && PT >= 128;
   static constexpr int NREL = BLK_REL ? CPS * NMAT : 1;  // empty barriers per slot
+  static_assert(SA >= 2, "the A ring needs a stage per dequantisation group");
+  static_assert(SB >= 2 && B_STAGE % 1024 == 0, "token-tile ring");
 };
 
 __host__ __device__ inline size_t gu_bytes(int h, int I) { return (size_t)(I / 128) * (h / KC) * 2 * QB; }
@@ -288,13 +308,6 @@ __device__ __forceinline__ void down_cols16(const uint32_t (&y)[16], const int* 
   }
 }
 
-// This warp has issued its last load of an accumulator buffer: hand it back
-// to the MMA issuer.
-__device__ __forceinline__ void release_acc(uint64_t* bar, int lane) {
-  tc_fence_before();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(bar);
-}
 
 struct PUnit {
   int e, start, n, Nm, f0, nkc, kps, pad;
@@ -345,11 +358,12 @@ struct PSmem {
   // gate/up, fp32 for down), the transpose that turns one value per lane
   // into 16 bytes of consecutive features
   alignas(16) float stage[8][GATEUP ? 16 * 16 : 16 * 32];
-  uint64_t code_full[PCfg<GATEUP, PT, CP>::SC], code_empty[PCfg<GATEUP, PT, CP>::SC];
-  uint64_t a_full[PCfg<GATEUP, PT, CP>::SA];
-  uint64_t a_empty[PCfg<GATEUP, PT, CP>::SA][PCfg<GATEUP, PT, CP>::NREL];
-  uint64_t b_full[PCfg<GATEUP, PT, CP>::SB], b_empty[PCfg<GATEUP, PT, CP>::SB];
-  uint64_t acc_full[PCfg<GATEUP, PT, CP>::NACC], acc_empty[PCfg<GATEUP, PT, CP>::NACC];
+  using C = PCfg<GATEUP, PT, CP>;
+  uint64_t code_full[C::SC], code_empty[C::SC];
+  uint64_t a_full[C::SA];
+  uint64_t a_empty[C::SA][C::NREL];
+  uint64_t b_full[C::SB], b_empty[C::SB];
+  uint64_t acc_full[C::NACC], acc_empty[C::NACC];
   uint64_t drain[2];
   uint32_t tmem_slot;
   int abort;
@@ -357,8 +371,16 @@ struct PSmem {
 
 template <bool GATEUP, int PT, int CP>
 constexpr size_t psmem_bytes() {
-  return 1024 + (size_t)B_RING + (size_t)PCfg<GATEUP, PT, CP>::SC * PCfg<GATEUP, PT, CP>::C_STAGE +
-         sizeof(PSmem<GATEUP, PT, CP>);
+  using C = PCfg<GATEUP, PT, CP>;
+  return 1024 + (size_t)C::B_RING + (size_t)C::SC * C::C_STAGE + sizeof(PSmem<GATEUP, PT, CP>);
+}
+
+// This warp has issued its last load of an accumulator buffer: hand it back
+// to the MMA issuer.
+__device__ __forceinline__ void release_acc(uint64_t* bar, int lane) {
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
 }
 
 template <bool GATEUP, int PT, int CP>
@@ -372,11 +394,12 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* b_s = base;
-  uint8_t* c_s = b_s + B_RING;
+  uint8_t* c_s = b_s + C::B_RING;
   PSmem<GATEUP, PT, CP>& S = *reinterpret_cast<PSmem<GATEUP, PT, CP>*>(c_s + C::SC * C::C_STAGE);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = p.h;
   const int egroups = blockDim.x > KTHREADS_1 ? 2 : 1;  // epilogue warpgroups
+  const int unit0 = blockIdx.x, ustride = gridDim.x;
 
   if (GATEUP && (!p.deterministic || p.Is == 0)) {
     float4* acc4 = reinterpret_cast<float4*>(p.acc);
@@ -415,7 +438,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
   const int n_units = GATEUP ? p.hdr->n_units_gu : p.hdr->n_units_dn;
 
   if (warp == W_CODE) {
-    // ------------------------------------------------------------ packed weight blocks, 2 chunks per copy
+    // ------------------------------------------------------------ packed weight blocks, CPS chunks per copy
     if (lane == 0) {
       uint32_t it = 0;
       bool armed[C::SC];
@@ -423,14 +446,19 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
 #pragma unroll
       for (int i = 0; i < C::SC; ++i) armed[i] = false, par[i] = 0;
       bool stop = false;
-      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+      // The weight blocks of unit u: nst stages of C_STAGE bytes from the returned address.
+      auto unit_codes = [&](int u, int& nst) -> const uint8_t* {
         const PUnit U = decode_punit<GATEUP, CP, C::B_STAGE>(p, u);
         const int Iu = U.shared ? p.Is : p.I;
         const uint8_t* rec = U.shared ? P.s_packed : P.packed + (size_t)U.e * rec_bytes(h, p.I);
-        const uint8_t* src;
-        if (GATEUP) src = rec + (size_t)(U.f0 / 128) * (h / KC) * 2 * QB;
-        else src = rec + gu_bytes(h, Iu) + (size_t)(U.f0 / 128) * (Iu / KC) * QB;
-        for (int st = 0; st < U.nkc / CPS; ++st, ++it) {
+        nst = U.nkc / CPS;
+        if (GATEUP) return rec + (size_t)(U.f0 / 128) * (h / KC) * 2 * QB;
+        return rec + gu_bytes(h, Iu) + (size_t)(U.f0 / 128) * (Iu / KC) * QB;
+      };
+      for (int u = unit0; u < n_units && !stop; u += ustride) {
+        int nst;
+        const uint8_t* src = unit_codes(u, nst);
+        for (int st = 0; st < nst; ++st, ++it) {
           const int sc = it % C::SC;
           if (!mbar_wait(&S.code_empty[sc], ((it / C::SC) & 1) ^ 1, abort, WAIT_NS)) {
             note_timeout(p.status, abort, GATEUP ? 31 : 41);
@@ -457,7 +485,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
 #pragma unroll
       for (int i = 0; i < SB; ++i) armed[i] = false, par[i] = 0;
       bool stop = false;
-      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+      for (int u = unit0; u < n_units && !stop; u += ustride) {
         const PUnit U = decode_punit<GATEUP, CP, C::B_STAGE>(p, u);
         const uint8_t* src = GATEUP ? reinterpret_cast<const uint8_t*>(P.xg + (size_t)U.pad * h)
                                     : reinterpret_cast<const uint8_t*>(p.hg + (size_t)U.pad * P.kmax);
@@ -494,7 +522,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
 #pragma unroll
       for (int i = 0; i < SB; ++i) bstage[i] = desc_sw128(smem_u32(b_s + i * B_STAGE));
       uint32_t ast = 0, bit = 0, uit = 0;
-      for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
+      for (int u = unit0; u < n_units && !*abort; u += ustride, ++uit) {
         const PUnit U = decode_punit<GATEUP, CP, C::B_STAGE>(p, u);
         const uint32_t idesc = idesc_bf16(128, U.Nm);
         const uint32_t nm8 = (uint32_t)(U.Nm * 128) >> 4;  // descriptor step of one K chunk
@@ -524,8 +552,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
             if (sub == 0) bd = bstage[sb];  // b_full was observed by the dequant warps before a_full
 #pragma unroll
             for (int kk = 0; kk < KC / 16; ++kk)
-              mma_bf16_ta(acc + m * PT, a_st + (c * C::NMAT + m) * 32 + 8 * kk, bd + 2 * kk, idesc,
-                          (kc | kk) != 0);
+              mma_bf16_ta(acc + m * PT, a_st + (c * C::NMAT + m) * 32 + 8 * kk, bd + 2 * kk, idesc, (kc | kk) != 0);
             if constexpr (C::BLK_REL) mma_commit(&S.a_empty[sa][c * C::NMAT + m]);
             bd += nm8;
             if (++sub == U.kps || kc == U.nkc - 1) {
@@ -551,7 +578,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     const int o = q * 32 + lane;          // weight row (= TMEM lane)
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t ast = 0, bbase = 0;  // global A stage; global B stage at the unit's start
-    for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
+    for (int u = unit0; u < n_units && !*abort; u += ustride) {
       const PUnit U = decode_punit<GATEUP, CP, C::B_STAGE>(p, u);
       bool ok = true;
       for (int st = 0; st < U.nkc / CPS; ++st, ++ast) {
@@ -568,8 +595,25 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
           break;
         }
         tc_fence_after();
+        // The codes, scale and bias of block cm + 1 are loaded before block
+        // cm is dequantised and stored (the tensor-memory store is a compiler
+        // barrier), so their shared-memory latency overlaps the arithmetic.
+        const uint8_t* stage_c = c_s + sc * C::C_STAGE;
+        uint4 c0 = reinterpret_cast<const uint4*>(stage_c + o * 32)[0];
+        uint4 c1 = reinterpret_cast<const uint4*>(stage_c + o * 32)[1];
+        __nv_bfloat16 sv = reinterpret_cast<const __nv_bfloat16*>(stage_c + 4096)[o];
+        __nv_bfloat16 bv = reinterpret_cast<const __nv_bfloat16*>(stage_c + 4096 + 256)[o];
 #pragma unroll
         for (int cm = 0; cm < CPS * C::NMAT; ++cm) {
+          uint4 n0 = c0, n1 = c1;
+          __nv_bfloat16 ns = sv, nbv = bv;
+          if (cm + 1 < CPS * C::NMAT) {
+            const uint8_t* nb = stage_c + (cm + 1) * QB;
+            n0 = reinterpret_cast<const uint4*>(nb + o * 32)[0];
+            n1 = reinterpret_cast<const uint4*>(nb + o * 32)[1];
+            ns = reinterpret_cast<const __nv_bfloat16*>(nb + 4096)[o];
+            nbv = reinterpret_cast<const __nv_bfloat16*>(nb + 4096 + 256)[o];
+          }
           if constexpr (C::BLK_REL) {
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.a_empty[sa][cm], a_par, abort, WAIT_NS))) {
               if (lane == 0) note_timeout(p.status, abort, 38);
@@ -578,15 +622,11 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
             }
             tc_fence_after();
           }
-          const uint8_t* blk = c_s + sc * C::C_STAGE + cm * QB;
-          const __nv_bfloat16 sv = reinterpret_cast<const __nv_bfloat16*>(blk + 4096)[o];
-          const __nv_bfloat16 bv = reinterpret_cast<const __nv_bfloat16*>(blk + 4096 + 256)[o];
-          const uint4 c0 = reinterpret_cast<const uint4*>(blk + o * 32)[0];
-          const uint4 c1 = reinterpret_cast<const uint4*>(blk + o * 32)[1];
           const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
           uint32_t r[32];
           dequant_packed<8>(wd, __halves2bfloat162(sv, sv), __halves2bfloat162(bv, bv), r);
           tmem_st<32>(lane_base + C::A_COL + sa * C::A_STAGE + cm * 32, r);
+          c0 = n0, c1 = n1, sv = ns, bv = nbv;
         }
         if (!ok) {
           tmem_st_wait();
@@ -631,7 +671,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     const int o = q * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t uit = 0;
-    for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
+    for (int u = unit0; u < n_units && !*abort; u += ustride, ++uit) {
       const PUnit U = decode_punit<GATEUP, CP, C::B_STAGE>(p, u);
       const int ab = uit % C::NACC;
       // down: this warp's copy of the tile's destination rows and weights.
@@ -762,7 +802,8 @@ cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, const uint
 
 template <bool GATEUP, int PT, int CP>
 cudaError_t launch_packed_gemm(const PParams& P, cudaStream_t stream) {
-  const bool two_epi = PT == 128 && (GATEUP || max(P.p.I, P.p.Is) <= 1024);
+  static_assert(psmem_bytes<GATEUP, PT, CP>() <= SMEM_MAX, "shared memory of one CTA");
+  const bool two_epi = PT >= 128 && (GATEUP || max(P.p.I, P.p.Is) <= 1024);
   cudaError_t err = set_smem_limit_once(packed_gemm_kernel<GATEUP, PT, CP>, (int)psmem_bytes<GATEUP, PT, CP>());
   if (err != cudaSuccess) return err;
   MOE_LAUNCH(GATEUP ? "gateup_packed" : "down_packed", stream,
@@ -771,12 +812,16 @@ cudaError_t launch_packed_gemm(const PParams& P, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// K chunks per stage: gate/up two (one on 192-row tiles, whose 384
+// accumulator columns leave 128 for the A ring); down four when every inter
+// is a multiple of 256 on tiles of up to 128 rows, else two.
 template <int PT>
 cudaError_t launch_packed_gemms(const PParams& P, cudaStream_t stream) {
-  cudaError_t err = launch_packed_gemm<true, PT, CPS_DEFAULT>(P, stream);
+  constexpr int GU_CP = PT > 128 ? 1 : CPS_DEFAULT;
+  cudaError_t err = launch_packed_gemm<true, PT, GU_CP>(P, stream);
   if (err != cudaSuccess) return err;
-  // down: four K chunks per stage when every inter is a multiple of 256
-  if (P.p.I % 256 == 0 && P.p.Is % 256 == 0) return launch_packed_gemm<false, PT, 4>(P, stream);
+  if constexpr (PT <= 128)
+    if (P.p.I % 256 == 0 && P.p.Is % 256 == 0) return launch_packed_gemm<false, PT, 4>(P, stream);
   return launch_packed_gemm<false, PT, CPS_DEFAULT>(P, stream);
 }
 
@@ -816,10 +861,13 @@ cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, c
   P.xg = xg;
   P.kmax = a.I > a.Is ? a.I : a.Is;
 
-  // 64-row tiles when the experts see few rows each (at most 40 on average):
-  // a 128-row tile would be mostly padding, and the smaller accumulators
-  // leave TMEM for a deeper A ring.
-  const int pt = (long)a.t * a.k <= 40L * a.E ? PTILE_SMALL : PTILE;
+  // Tile height by the rows an expert sees on average: 64 up to 40 rows (a
+  // larger tile would be mostly padding, and the smaller accumulators leave
+  // TMEM for a deeper A ring), 128 up to 96, else 192, so that experts of
+  // 100-190 rows (the near-uniform t = 4096 chunks) take one tile each
+  // instead of two half-empty ones.
+  const long pairs = (long)a.t * a.k;
+  const int pt = pairs <= 40L * a.E ? PTILE_SMALL : pairs <= 96L * a.E ? PTILE : PTILE_LARGE;
   cudaError_t err;
   if ((err = launch_schedule(p, hdr, tiles, units, (int)mt, pt, stream)) != cudaSuccess) return err;
   if (p.gate_vals && (err = launch_shared_gate(a.x, a.s_gate, a.t, a.h, gate_vals, stream)) != cudaSuccess)
@@ -827,7 +875,9 @@ cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, c
   MOE_LAUNCH("gather", stream,
              launch_k(gather_kernel, dim3((unsigned)mt, pt / 8), 256, 0, stream, a.x, a.rows, hdr, tiles, a.t, a.h, a.E,
                                                                           xg, a.status));
-  err = pt == PTILE ? launch_packed_gemms<PTILE>(P, stream) : launch_packed_gemms<PTILE_SMALL>(P, stream);
+  err = pt == PTILE_LARGE ? launch_packed_gemms<PTILE_LARGE>(P, stream)
+        : pt == PTILE     ? launch_packed_gemms<PTILE>(P, stream)
+                          : launch_packed_gemms<PTILE_SMALL>(P, stream);
   if (err != cudaSuccess) return err;
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   return launch_finalize(a, deterministic, stream);

@@ -338,20 +338,26 @@ def test_one_expert_takes_every_row_and_shared_gate(moe, flags):
     _check_out(res["out"], ref["out"])
 
 
+@pytest.mark.parametrize("t,E,tile", [(1000, 8, 192), (410, 10, 128)])
 @pytest.mark.parametrize("inter", [256, 1280])
 @pytest.mark.parametrize("det", [False, True])
-def test_packed_128_row_tiles(moe, inter, det):
-    """About 250 rows per expert: 128-row tiles with ragged last tiles (down
-    runs two epilogue warpgroups at inter 256, one at 1280; gate/up two)."""
-    w = synth.Workload("t128", 1000, 256, inter, 8, 2, 256, 41 + inter)
+def test_packed_large_tiles(moe, t, E, tile, inter, det):
+    """Tiles of up to 192 rows (experts see 250 rows on average) and of up to
+    128 rows (80 on average); a router bias sends every row to expert 0 first,
+    so it spans several tiles with a ragged last one.  Down runs two epilogue
+    warpgroups at inter 256 and one at 1280; gate/up two."""
+    w = synth.Workload("tl", t, 256, inter, E, 2, 256, 41 + inter + t)
     inp = synth.make_inputs(w)
+    inp["rbias"] = np.zeros(E, np.float32)
+    inp["rbias"][0] = 3.0
     ref = O.moe_forward(inp, w.k, w.h, w.inter, w.shared_inter)
     flags = moe.MOE_PACKED_WEIGHTS | (moe.MOE_DETERMINISTIC if det else 0)
     res, status = _run(moe, w, inp, flags)
     assert status == 0
     np.testing.assert_array_equal(res["idx"].cpu().numpy(), ref["idx"])
     counts = np.diff(res["csr"].offsets.cpu().numpy())
-    assert counts.max() > 128 and np.any(counts % 128 > 0)
+    n0 = int(counts[0])
+    assert n0 > tile and n0 % -(-n0 // -(-n0 // tile)) != 0  # several tiles, the last one ragged
     _check_csr_against(res["csr"], res["idx"], res["w"], w.E)
     _check_out(res["out"], ref["out"])
 
