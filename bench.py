@@ -103,6 +103,8 @@ def step_work(w: synth.Workload, counts: np.ndarray) -> dict:
                      flops=2 * n * h * I + 2 * t * h * Is),
         # router (scores + exact refinement): x and router weights in, idx/w out
         "route": dict(bytes=t * h * 2 + E * h * 2 + t * k * 8, flops=2 * t * h * E),
+        # the fused decode launch: the whole step
+        "decode_fused": dict(bytes=wbytes + io, flops=flops),
     }
     return dict(touched=touched, pairs=n, max_rows=int(counts.max()), flops=flops,
                 bytes=wbytes + io, by_kernel=by_kernel)
@@ -163,7 +165,7 @@ def job_tokens_per_s(world: int, rows_per_rank: int, max_ms: float) -> float:
 
 
 def kernel_family(name: str) -> str:
-    for fam in ("gateup", "down", "route"):
+    for fam in ("gateup", "down", "route", "decode_fused"):
         if name.startswith(fam):
             return fam
     return name

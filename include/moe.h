@@ -102,6 +102,7 @@ typedef struct {
 #define MOE_FORCE_LARGE_T 0x4u /* force the tensor-core grouped GEMM kernels */
 #define MOE_SIMPLE_KERNELS 0x8u /* plain CUDA-core kernels (slow; a cross-check path) */
 #define MOE_PACKED_WEIGHTS 0x10u /* experts->codes and shared->codes hold moe_pack_experts output */
+#define MOE_FUSED_DECODE 0x20u /* moe_forward: one cooperative launch for decode-shaped chunks */
 
 /* Thread-local message of the last failed call on this thread ("" if none). */
 const char* moe_last_error(void);
@@ -206,7 +207,10 @@ int moe_route_csr(const uint16_t* x, const uint16_t* wr, const float* rbias,
  *   - MOE_SIMPLE_KERNELS: plain CUDA-core kernels (a slow cross-check).
  * A call whose workspace status block was never cleared (moe_clear_device_
  * status) may report stale flags; the small-t kernels also keep a completion
- * counter there, so clear a new workspace once before its first use.
+ * counter there, so clear a new workspace once before its first use.  After a
+ * call that gave up (MOE_ETIMEOUT), the moe_read_device_status that reports
+ * it clears the status block, counters included, so the next call starts
+ * clean.
  *
  * x bf16 [t][h] in; out bf16 [t][h] out (no residual is added).
  * ws: at least moe_workspace_bytes(dims, flags) bytes.
@@ -215,6 +219,35 @@ int moe_route_csr(const uint16_t* x, const uint16_t* wr, const float* rbias,
 int moe_experts_fwd(const uint16_t* x, const moe_csr* csr, const moe_qweights* experts,
                     const moe_shared* shared, uint16_t* out, const moe_dims* dims,
                     uint32_t flags, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The whole block in one call: exactly moe_route_csr followed by
+ * moe_experts_fwd on the same workspace and stream -- the same idx, w and
+ * csr bit for bit, and `out` within the same tolerance (the fp32 block
+ * accumulator is summed in another order).  Arguments as in those two calls.
+ *
+ * Decode-shaped chunks (decode.rs, step_rows: the MoE block over a verify
+ * batch of a few rows) take one launch instead of three with
+ * MOE_FUSED_DECODE: when t <= 8, E <= 256, h <= 2048 (x is staged in shared
+ * memory), the weights are packed (MOE_PACKED_WEIGHTS) and none of
+ * MOE_DETERMINISTIC, MOE_FORCE_SMALL_T, MOE_FORCE_LARGE_T, MOE_SIMPLE_KERNELS
+ * is set, a cooperative grid of one CTA per SM computes the router logits,
+ * meets at a grid-wide barrier, groups the rows in every CTA, and streams
+ * each CTA's share of the touched experts' weight blocks once through the
+ * tensor cores (gate/up, then down, with counters in the workspace in place
+ * of kernel boundaries).  Without the flag, or for other chunks, the call
+ * issues the launches of the two calls.  MOE_FUSED_DECODE is ignored by
+ * moe_route_csr and moe_experts_fwd.
+ *
+ * The grid barrier counts arrivals in the workspace's status block: clear a
+ * fresh workspace once (moe_clear_device_status).  Every wait is bounded;
+ * after a call that gave up (MOE_ETIMEOUT from moe_read_device_status),
+ * that read has cleared the status block and the next call starts clean.
+ * Errors: MOE_EINVAL, MOE_ESHAPE, MOE_EWORKSPACE, MOE_ECUDA.
+ */
+int moe_forward(const uint16_t* x, const uint16_t* wr, const float* rbias, const moe_qweights* experts,
+                const moe_shared* shared, const moe_dims* dims, uint32_t flags, int32_t* idx, float* w,
+                const moe_csr* csr, uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * moe_build_csr without a workspace (no counterpart in the method; an

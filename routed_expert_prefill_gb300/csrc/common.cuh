@@ -31,7 +31,8 @@ struct DeviceStatus {
   uint32_t route_cands;   // router: logits recomputed exactly
   uint32_t route_done;    // router, small t: CTAs finished (the last one resets it)
   uint32_t gv_done;       // small-t down kernel: CTAs finished (the last one finalises and resets it)
-  uint32_t pad[58];
+  uint32_t fused_bar;     // fused decode launch: grid-barrier arrivals (every call adds the grid size)
+  uint32_t pad[57];
 };
 
 __device__ __forceinline__ void raise_flag(DeviceStatus* st, uint32_t f) {
@@ -107,6 +108,7 @@ struct WsLayout {
   size_t xg;            // bf16 gathered token images (packed-weight path only)
   size_t sched;         // scheduler state (counters, tile lists)
   size_t gvpart;        // small-t gate/up partial sums (t <= 16 only)
+  size_t fused;         // fused decode launch: logits, gate/up sums, accumulator, counters (t <= 16 only)
   size_t total;
 };
 

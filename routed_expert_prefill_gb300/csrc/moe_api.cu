@@ -29,6 +29,12 @@ cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, c
                                   uint16_t* xg, bool deterministic, cudaStream_t stream);
 cudaError_t launch_experts_gemv(const ExpertsArgs& a, bool packed, bool deterministic, cudaStream_t stream);
 size_t gemv_part_bytes(const moe_dims& d);
+bool decode_fused_ok(const moe_dims& d, uint32_t flags);
+size_t decode_fused_ws_bytes(const moe_dims& d);
+cudaError_t launch_decode_fused(const uint16_t* x, const uint16_t* wr, const float* rbias, const moe_dims& d,
+                                const uint8_t* packed, const uint8_t* s_packed, const uint16_t* s_gate, int32_t* idx,
+                                float* w, const moe_csr& csr, uint16_t* out, unsigned char* scratch,
+                                DeviceStatus* st, cudaStream_t stream);
 
 // Chunks of at most SMALL_T_MAX rows whose (expert, 128-row tile) units are
 // too few to occupy the GPU (t * k * inter / 128 below SMALL_T_UNITS, about
@@ -88,6 +94,7 @@ WsLayout ws_layout(const moe_dims& d, uint32_t flags) {
   L.xg = (flags & MOE_PACKED_WEIGHTS) ? take(packed_pad_rows(d) * d.h * 2) : off;
   L.sched = take(experts_sched_bytes(d));
   L.gvpart = take(gemv_part_bytes(d));
+  L.fused = take(d.t <= SMALL_T_MAX ? decode_fused_ws_bytes(d) : 0);
   L.total = off;
   return L;
 }
@@ -230,17 +237,23 @@ int moe_route_csr(const uint16_t* x, const uint16_t* wr, const float* rbias, con
                      "moe_route_csr launch");
 }
 
-int moe_experts_fwd(const uint16_t* x, const moe_csr* csr, const moe_qweights* experts,
-                    const moe_shared* shared, uint16_t* out, const moe_dims* dims, uint32_t flags, void* ws,
-                    size_t ws_bytes, void* stream) {
-  TRY(check_dims(dims));
+static int check_flags(uint32_t flags) {
   const uint32_t known =
-      MOE_DETERMINISTIC | MOE_FORCE_SMALL_T | MOE_FORCE_LARGE_T | MOE_SIMPLE_KERNELS | MOE_PACKED_WEIGHTS;
+      MOE_DETERMINISTIC | MOE_FORCE_SMALL_T | MOE_FORCE_LARGE_T | MOE_SIMPLE_KERNELS | MOE_PACKED_WEIGHTS |
+      MOE_FUSED_DECODE;
   if (flags & ~known) return set_error(MOE_EINVAL, "unknown flag bits 0x%x", flags & ~known);
   if ((flags & MOE_FORCE_SMALL_T) && (flags & MOE_FORCE_LARGE_T))
     return set_error(MOE_EINVAL, "MOE_FORCE_SMALL_T and MOE_FORCE_LARGE_T are exclusive");
   if ((flags & MOE_PACKED_WEIGHTS) && (flags & MOE_SIMPLE_KERNELS))
     return set_error(MOE_EINVAL, "MOE_SIMPLE_KERNELS reads row-major weights, not MOE_PACKED_WEIGHTS");
+  return MOE_OK;
+}
+
+int moe_experts_fwd(const uint16_t* x, const moe_csr* csr, const moe_qweights* experts,
+                    const moe_shared* shared, uint16_t* out, const moe_dims* dims, uint32_t flags, void* ws,
+                    size_t ws_bytes, void* stream) {
+  TRY(check_dims(dims));
+  TRY(check_flags(flags));
   const bool packed = (flags & MOE_PACKED_WEIGHTS) != 0;
   TRY(check_ptr(x, "x", 16));
   TRY(check_ptr(out, "out", 16));
@@ -311,6 +324,44 @@ int moe_experts_fwd(const uint16_t* x, const moe_csr* csr, const moe_qweights* e
   if (flags & MOE_SIMPLE_KERNELS)
     return cuda_status(launch_experts_simple(a, (flags & MOE_DETERMINISTIC) != 0, s), "moe_experts_fwd launch");
   return cuda_status(launch_experts_tc(a, (flags & MOE_DETERMINISTIC) != 0, s), "moe_experts_fwd launch");
+}
+
+int moe_forward(const uint16_t* x, const uint16_t* wr, const float* rbias, const moe_qweights* experts,
+                const moe_shared* shared, const moe_dims* dims, uint32_t flags, int32_t* idx, float* w,
+                const moe_csr* csr, uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+  TRY(check_dims(dims));
+  TRY(check_flags(flags));
+  if (!(decode_fused_ok(*dims, flags))) {
+    TRY(moe_route_csr(x, wr, rbias, dims, idx, w, csr, ws, ws_bytes, stream));
+    return moe_experts_fwd(x, csr, experts, shared, out, dims, flags, ws, ws_bytes, stream);
+  }
+  // the fused decode launch: the same argument checks as the two calls
+  TRY(check_ptr(x, "x", 16));
+  TRY(check_ptr(wr, "wr", 16));
+  TRY(check_ptr(rbias, "rbias", 4, true));
+  TRY(check_ptr(idx, "idx", 4));
+  TRY(check_ptr(w, "w", 4));
+  TRY(check_ptr(out, "out", 16));
+  if (!csr) return set_error(MOE_EINVAL, "csr is NULL");
+  TRY(check_ptr(csr->offsets, "csr->offsets", 4));
+  TRY(check_ptr(csr->rows, "csr->rows", 4));
+  TRY(check_ptr(csr->weights, "csr->weights", 4));
+  TRY(check_ptr(csr->slot_of, "csr->slot_of", 4));
+  if (!experts) return set_error(MOE_EINVAL, "experts is NULL");
+  TRY(check_ptr(experts->codes, "experts->codes", 16));
+  if (dims->shared_inter > 0) {
+    if (!shared) return set_error(MOE_EINVAL, "shared is NULL but shared_inter > 0");
+    TRY(check_ptr(shared->codes, "shared->codes", 16));
+    TRY(check_ptr(shared->gate, "shared->gate", 16, true));
+  }
+  TRY(check_ws(dims, flags, ws, ws_bytes));
+  const WsLayout L = ws_layout(*dims, flags);
+  unsigned char* wsb = (unsigned char*)ws;
+  return cuda_status(
+      launch_decode_fused(x, wr, rbias, *dims, experts->codes, dims->shared_inter > 0 ? shared->codes : nullptr,
+                          dims->shared_inter > 0 ? shared->gate : nullptr, idx, w, *csr, out, wsb + L.fused,
+                          (DeviceStatus*)(wsb + L.status), (cudaStream_t)stream),
+      "moe_forward launch");
 }
 
 size_t moe_packed_bytes(const moe_dims* dims, int shared) {

@@ -28,6 +28,7 @@ MOE_FORCE_SMALL_T = 0x2
 MOE_FORCE_LARGE_T = 0x4
 MOE_SIMPLE_KERNELS = 0x8
 MOE_PACKED_WEIGHTS = 0x10
+MOE_FUSED_DECODE = 0x20
 
 # Every symbol include/moe.h declares.
 EXPORTS = (
@@ -45,6 +46,7 @@ EXPORTS = (
     "moe_packed_bytes",
     "moe_pack_experts",
     "moe_build_csr_noalloc",
+    "moe_forward",
 )
 
 
@@ -117,6 +119,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_packed_bytes.argtypes = [ctypes.POINTER(MoeDims), ctypes.c_int]
     lib.moe_build_csr_noalloc.restype = ctypes.c_int
     lib.moe_build_csr_noalloc.argtypes = [vp, vp, ctypes.POINTER(MoeDims), ctypes.POINTER(MoeCsr), vp]
+    lib.moe_forward.restype = ctypes.c_int
+    lib.moe_forward.argtypes = [vp, vp, vp, ctypes.POINTER(MoeQWeights), ctypes.POINTER(MoeShared),
+                                ctypes.POINTER(MoeDims), u32, vp, vp, ctypes.POINTER(MoeCsr), vp, vp, sz, vp]
     lib.moe_pack_experts.restype = ctypes.c_int
     lib.moe_pack_experts.argtypes = [ctypes.POINTER(MoeQWeights), ctypes.POINTER(MoeDims), ctypes.c_int, vp, sz, vp]
     _lib = lib
@@ -490,26 +495,61 @@ def add_packed(dev: dict, dims: MoeDims, stream=None) -> dict:
 
 def moe_forward(dev: dict, dims: MoeDims, flags: int = MOE_PACKED_WEIGHTS, ws: torch.Tensor | None = None,
                 out: torch.Tensor | None = None, stream=None, bufs: dict | None = None) -> dict:
-    """Router -> CSR -> experts on one stream; returns the intermediate tensors too.
+    """The whole block through the C entry point moe_forward (router, grouping
+    and expert FFNs in one call; one launch for decode-shaped chunks);
+    returns the intermediate tensors too.
 
     By default (MOE_PACKED_WEIGHTS in `flags`) the packed records of
     add_packed() are used, made on the first call when absent; flags without
     it run the row-major records as uploaded."""
     if flags & MOE_PACKED_WEIGHTS and "packed" not in dev:
         add_packed(dev, dims, stream)
-    if ws is None:
-        ws = new_workspace(dims, flags, dev["x"].device, stream)
-    b = bufs or {}
-    idx, w, csr = moe_route_csr(dev["x"], dev["wr"], dims.k, dev.get("rbias"), ws=ws, out_route=b.get("route"),
-                                out_csr=b.get("csr"), stream=stream)
-    shared = None
-    if flags & MOE_PACKED_WEIGHTS:
+    lib = load_library()
+    x, wr, rbias = dev["x"], dev["wr"], dev.get("rbias")
+    t, h, I, Is, E, k = dims.t, dims.h, dims.inter, dims.shared_inter, dims.E, dims.k
+    _need(x, "x", _BF16, shape=(t, h))
+    _need(wr, "wr", _BF16, shape=(E, h))
+    if rbias is not None:
+        _need(rbias, "rbias", (torch.float32,), shape=(E,))
+    packed = bool(flags & MOE_PACKED_WEIGHTS)
+    if packed:
         experts = (dev["packed"], None, None)
-        if dims.shared_inter > 0:
-            shared = (dev["shared_packed"], None, None, dev.get("shared_gate"))
+        shared = (dev["shared_packed"], None, None, dev.get("shared_gate")) if Is > 0 else None
     else:
         experts = (dev["codes"], dev["scales"], dev["biases"])
-        if dims.shared_inter > 0:
-            shared = (dev["shared_codes"], dev["shared_scales"], dev["shared_biases"], dev.get("shared_gate"))
-    y = moe_experts_fwd(dev["x"], csr, experts, shared, dims, flags, out=out, ws=ws, stream=stream)
-    return dict(idx=idx, w=w, csr=csr, out=y, ws=ws)
+        shared = ((dev["shared_codes"], dev["shared_scales"], dev["shared_biases"], dev.get("shared_gate"))
+                  if Is > 0 else None)
+    b = bufs or {}
+    dev_ = x.device
+    idx, w = b.get("route") or (torch.empty((t, k), dtype=torch.int32, device=dev_),
+                                torch.empty((t, k), dtype=torch.float32, device=dev_))
+    csr = b.get("csr") or Csr(torch.empty(E + 1, dtype=torch.int32, device=dev_),
+                              torch.empty(t * k, dtype=torch.int32, device=dev_),
+                              torch.empty(t * k, dtype=torch.float32, device=dev_),
+                              torch.empty(t * k, dtype=torch.int32, device=dev_))
+    _need(idx, "idx", (torch.int32,), shape=(t, k))
+    _need(w, "w", (torch.float32,), shape=(t, k))
+    _need_csr(csr, "csr", E, t * k)
+    for i, name in enumerate(("codes", "scales", "biases")):
+        if experts[i] is not None:
+            _need(experts[i], f"experts {name}", (torch.uint8,) if i == 0 else _F16)
+    if ws is None:
+        ws = new_workspace(dims, flags, dev_, stream)
+    else:
+        _need_ws(ws, dims, flags)
+    if out is None:
+        out = torch.empty((t, h), dtype=torch.bfloat16, device=dev_)
+    else:
+        _need(out, "out", _BF16, shape=(t, h))
+    recs = {f"experts[{i}]": experts[i] for i in range(3)}
+    if shared is not None:
+        recs.update({f"shared[{i}]": shared[i] for i in range(4)})
+    _on_current_device(x=x, wr=wr, rbias=rbias, idx=idx, w=w, ws=ws, out=out, **_csr_named(csr, "csr"), **recs)
+    dp = lambda t_: None if t_ is None else t_.data_ptr()  # noqa: E731
+    q = MoeQWeights(dp(experts[0]), dp(experts[1]), dp(experts[2]))
+    sh = MoeShared(dp(shared[0]), dp(shared[1]), dp(shared[2]), dp(shared[3])) if shared is not None else None
+    c = csr.c()
+    _check(lib.moe_forward(_ptr(x), _ptr(wr), _ptr(rbias), ctypes.byref(q), ctypes.byref(sh) if sh else None,
+                           ctypes.byref(dims), flags, _ptr(idx), _ptr(w), ctypes.byref(c), _ptr(out), _ptr(ws),
+                           ws.numel(), _stream(stream)))
+    return dict(idx=idx, w=w, csr=csr, out=out, ws=ws)

@@ -497,3 +497,59 @@ def test_full_size_sampled_rows(moe, name, packed):
     if name.endswith("skewed"):
         counts = np.diff(res["csr"].offsets.cpu().numpy())
         assert counts.max() >= 0.5 * w.t and (counts <= 3).sum() >= w.E // 3
+
+
+FUSED_CASES = [
+    # t, h, inter, E, k, shared_inter, shared gate
+    (1, 2048, 768, 128, 8, 768, False),
+    (8, 2048, 768, 128, 8, 768, False),
+    (8, 256, 128, 8, 2, 128, True),     # shared gate; every expert sees several rows
+    (5, 512, 256, 40, 8, 0, False),     # no shared expert, E not a multiple of 32
+    (8, 640, 256, 256, 16, 256, True),  # k = 16, E = 256, h not a multiple of 256
+    (3, 256, 128, 4, 4, 128, False),    # k = E: every expert takes every row
+]
+
+
+@pytest.mark.parametrize("t,h,inter,E,k,Is,gate", FUSED_CASES)
+def test_fused_decode_launch(moe, t, h, inter, E, k, Is, gate):
+    """moe_forward on a decode-shaped chunk is one launch, and gives the
+    oracle's idx and grouping bit for bit, the separate calls' idx, w and
+    grouping bit for bit, and outputs within the tolerance; three calls in a
+    row (the grid barrier's counter advancing) agree."""
+    w = synth.Workload("fd", t, h, inter, E, k, Is, 70 + t + E, shared_gate=gate)
+    inp = synth.make_inputs(w)
+    ref = O.moe_forward(inp, k, h, inter, Is)
+    dev = moe.upload_inputs(inp)
+    dims = _dims(moe, w)
+    moe.add_packed(dev, dims)
+    flags = moe.MOE_PACKED_WEIGHTS | moe.MOE_FUSED_DECODE
+    ws = moe.new_workspace(dims, flags)
+    outs = []
+    for rep in range(3):
+        moe.profile_enable(True)
+        res = moe.moe_forward(dev, dims, flags, ws=ws)
+        prof = moe.profile_read()
+        moe.profile_enable(False)
+        assert list(prof) == ["decode_fused"] and prof["decode_fused"][0] == 1, prof
+        assert moe.read_device_status(ws) == 0
+        np.testing.assert_array_equal(res["idx"].cpu().numpy(), ref["idx"])
+        assert np.abs(res["w"].cpu().numpy() - ref["w"]).max() <= 2e-6
+        _check_csr_against(res["csr"], res["idx"], res["w"], E)
+        _check_out(res["out"], ref["out"])
+        outs.append(res["out"].float().cpu().numpy())
+    assert np.abs(outs[0] - outs[2]).max() <= 1e-2 * np.abs(outs[0]).max()
+    # the separate calls on the same inputs
+    idx1, w1, csr1 = moe.moe_route_csr(dev["x"], dev["wr"], k, dev.get("rbias"))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(res["idx"].cpu().numpy(), idx1.cpu().numpy())
+    np.testing.assert_array_equal(res["w"].cpu().numpy().view(np.uint32), w1.cpu().numpy().view(np.uint32))
+    for a, b in zip(res["csr"], csr1):
+        np.testing.assert_array_equal(a.cpu().numpy().view(np.uint32), b.cpu().numpy().view(np.uint32))
+    # without MOE_FUSED_DECODE the same call issues the separate launches
+    moe.profile_enable(True)
+    res2 = moe.moe_forward(dev, dims, moe.MOE_PACKED_WEIGHTS, ws=ws)
+    prof = moe.profile_read()
+    moe.profile_enable(False)
+    assert "decode_fused" not in prof and prof, prof
+    np.testing.assert_array_equal(res2["idx"].cpu().numpy(), ref["idx"])
+    _check_out(res2["out"], ref["out"])
