@@ -19,34 +19,44 @@
 //   B. its share of the touched experts' gate/up pairs,
 //   C. its share of the shared expert's down blocks,
 //   D. its share of the touched experts' down blocks.
+// Gate/up pairs run [expert][feature tile][K chunk of h], down blocks
+// [expert][output tile][K chunk of inter], so consecutive items of a CTA
+// accumulate into one tensor-memory accumulator (a "segment") that is read
+// out once, when the segment closes.  The CTA's list is written once into
+// shared memory as packed (expert slot, tile, K chunk, open/close) entries:
+// part A in the prologue, parts B to D as soon as the routing is known.
 //
 // Warp roles (14 warps):
 //   0      producer: one thread bulk-copies the blocks of the CTA's items
 //          into a ring in shared memory, starting with part A at once;
-//   1      MMA issuer: one thread issues tcgen05.mma (M = 128 weight rows,
-//          N = 16 token columns, A in tensor memory, B in shared memory);
-//   2-9    two dequantisation groups taking alternate items: one weight row
-//          per thread, w = fma(q, s, b) in bf16 (one rounding) straight into
-//          tensor memory (tcgen05.st);
+//   1      MMA issuer: the warp walks the list in step, one elected lane
+//          issues tcgen05.mma (M = 128 weight rows, N = 16 token columns, A in
+//          tensor memory, B in shared memory);
+//   2-9    first x into shared memory, then two dequantisation groups taking
+//          alternate items: one weight row per thread, w = fma(q, s, b) in
+//          bf16 (one rounding) straight into tensor memory (tcgen05.st);
 //   10-13  first the router: the logits of experts b, b + G, ... in the
 //          fixed summation order of moe_route_topk (lane l owns
 //          K = 256 m + 8 l + c, m then c ascending from +0, lane sums
 //          combined by the xor butterfly 16..1, bias last), zeroing of the
 //          accumulators, a grid-wide barrier (a generation counter every call
 //          advances by the grid size), top-k and grouping (identical in every
-//          CTA; CTA 0 writes idx, w and the CSR arrays); then the epilogue:
-//          tcgen05.ld of the accumulators and fp32 atomics into the
-//          per-expert gate/up sums and into the block accumulator.
+//          CTA; CTA 0 writes idx, w and the CSR arrays), the rest of the list;
+//          then the epilogue: tcgen05.ld of each closed segment and fp32
+//          atomics into the per-expert gate/up sums or the block accumulator.
 //
 // Operands.  Gate/up: B is x, staged once as 64-wide K chunks of 16 rows
 // (128-byte swizzled, rows past t zero), so every expert is multiplied with
 // all t rows -- at N = 16 the MMA costs the same -- and the epilogue keeps
 // the columns of the expert's own rows.  Down: B is silu(gate) * up of one
 // 64-wide chunk for the expert's rows (rounded to bf16, as the hidden
-// activations are everywhere else), built by the epilogue warps once the
-// chunk's gate/up sums are complete: a counter per (expert, 128-row feature
-// tile) counts the K chunks added.  A counter per 128-column output tile lets
-// the last contributor round the tile to bf16.
+// activations are everywhere else).  A counter per (expert, 128-row feature
+// tile) counts the K chunks added; the CTA whose addition completes the tile
+// writes its two B tiles to the workspace, already in the swizzled layout,
+// and raises the tile's flag; the producer waits for the flag before it
+// bulk-copies a down block together with its B tile into one ring slot.  A
+// counter per 128-column output tile lets the last contributor round the
+// tile to bf16.
 //
 // Every wait is bounded (2 s of global time): a wait that gives up records
 // MOE_ETIMEOUT, the CTA stops, lets its in-flight copies and MMAs land, frees
@@ -65,19 +75,22 @@ using namespace tc;
 constexpr int D_WARPS = 14;
 constexpr int D_THREADS = D_WARPS * 32;
 constexpr int W_PROD = 0, W_ISSUE = 1, W_DQ0 = 2, W_EPI0 = 10;
-constexpr int D_SLOT = 2 * PACK_QB;  // ring slot: a gate/up block pair (a down block uses half)
+constexpr int D_SLOT = 2 * PACK_QB;  // ring slot: a gate/up block pair, or a down block and its B tile
+constexpr int D_HG_OFF = 5 * 1024;   // the B tile of a down item within its slot (1024-byte aligned)
 constexpr int D_NSLOT = 12;
 constexpr int D_NA = 4;              // tensor-memory A slots of 64 columns (a gate/up pair, or a down block)
 constexpr int D_NACC = 8;            // accumulator buffers of 32 columns (gate 16 + up 16, or down 16)
 constexpr int D_ACC_COL = D_NA * 64;
-constexpr int D_NHG = 4;             // silu(gate) * up tiles of the down pass
 constexpr int D_TILE = 2048;         // 16 rows x 128 bytes, swizzled
 constexpr int D_MAX_H = 2048;        // x is staged as h / 64 tiles
 constexpr int D_MAX_T = 8;
 constexpr int D_MAX_E = 256;
 constexpr int D_MAX_PAIRS = D_MAX_T * 16;
+constexpr int D_MAX_ITEMS = 2048;    // entries of a CTA's list
 constexpr int D_KC = 64;
 constexpr uint64_t D_WAIT_NS = 2000000000ull;
+static_assert(PACK_QB <= D_HG_OFF && D_HG_OFF + D_TILE <= D_SLOT, "down item layout in a ring slot");
+static_assert(D_SLOT % 1024 == 0, "ring slots keep the 1024-byte alignment of the swizzled tiles");
 
 struct DfParams {
   int t, h, I, Is, E, Ep, k;
@@ -93,9 +106,11 @@ struct DfParams {
   uint16_t* out;            // bf16 [t][h] out
   float* logits;            // ws: [t][Ep]
   float* gate_vals;         // ws: [t]
-  float* gu;                // ws: [slots][2][Imax][t] gate / up sums (slot 0: the shared expert)
+  float* gu;                // ws: [t + t * k][2][Imax] gate / up sums: rows of the shared expert, then list positions
   float* acc;               // ws: [t][h] block accumulator
   uint32_t* ftcount;        // ws: [slots][Imax / 128] K chunks added per feature tile
+  uint32_t* hgready;        // ws: [slots] feature tiles whose B tiles are written
+  uint8_t* hg;              // ws: [slots][Imax / 64] swizzled bf16 B tiles of the down pass
   uint32_t* hcount;         // ws: [h / 128] down blocks added per output tile
   DeviceStatus* st;
   int imax;                 // max(I, Is)
@@ -106,13 +121,14 @@ struct DfSmem {
   uint64_t full[D_NSLOT], empty[D_NSLOT];
   uint64_t a_full[D_NA], a_empty[D_NA];
   uint64_t acc_full[D_NACC], acc_empty[D_NACC];
-  uint64_t hg_full[D_NHG], hg_empty[D_NHG];
-  uint64_t ready;  // the routing is known (parts B, C, D)
-  uint64_t esync;  // barrier of the four epilogue warps
+  uint64_t x_ready;  // x is in its B tiles
+  uint64_t ready;    // the routing is known: parts B, C, D are in the list
+  uint64_t esync;    // barrier of the four epilogue warps
   uint64_t drain;
+  uint32_t items[D_MAX_ITEMS];
   int32_t idx[D_MAX_PAIRS];
   float w[D_MAX_PAIRS];
-  int32_t cnt[D_MAX_E + 1];
+  int32_t cnt[D_MAX_E];
   int32_t off[D_MAX_E + 1];
   int32_t rows[D_MAX_PAIRS];
   float wts[D_MAX_PAIRS];
@@ -121,16 +137,15 @@ struct DfSmem {
   int32_t slot_n[D_MAX_PAIRS + 1];     // rows of slot s
   int32_t htcnt[D_MAX_H / 128];
   int32_t htlast[D_MAX_H / 128];
-  int32_t wsum[4];
+  int32_t n_items;  // entries in the list (part A alone until `ready`)
   int32_t n_touched;
+  int32_t last;     // this CTA completed the feature tile just drained
   uint32_t tmem_slot;
   int abort;
 };
 
 constexpr size_t D_XT_BYTES = (size_t)(D_MAX_H / D_KC) * D_TILE;
-constexpr size_t df_smem_bytes() {
-  return 1024 + (size_t)D_NSLOT * D_SLOT + D_XT_BYTES + (size_t)D_NHG * D_TILE + sizeof(DfSmem);
-}
+constexpr size_t df_smem_bytes() { return 1024 + (size_t)D_NSLOT * D_SLOT + D_XT_BYTES + sizeof(DfSmem); }
 
 __device__ __forceinline__ void df_timeout(DeviceStatus* st, volatile int* abort, uint32_t site) {
   if (atomicOr(&st->flags, FLAG_TIMEOUT) == 0) st->timeout_site = site;
@@ -142,6 +157,8 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+// Orders this thread's generic-proxy global accesses with its bulk copies.
+__device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // Spin (bounded) until *p >= target; false when it gave up or *abort is set.
 __device__ __forceinline__ bool spin_until(const uint32_t* p, uint32_t target, const volatile int* abort) {
@@ -161,50 +178,50 @@ __device__ __forceinline__ void df_bulk(void* dst, const void* src, uint32_t byt
                : "memory");
 }
 
-// One item of this CTA's list: a gate/up block pair (a = feature tile, b =
-// K chunk) or a down block (a = K chunk of inter, b = 128-row tile of h).
+// A list entry: expert slot (0: the shared expert), tile (gate/up: 128-row
+// feature tile; down: 128-column output tile), K chunk (gate/up: of h; down:
+// of inter), and whether the item opens / closes its segment.
 struct Item {
-  int slot, a, b;
-  bool gu;
+  int slot, tile, kc;
+  bool gu, opens, closes;
 };
+__device__ __forceinline__ Item item_unpack(uint32_t v) {
+  Item it;
+  it.slot = (int)(v & 0xFFu), it.tile = (int)((v >> 8) & 0xFFu), it.kc = (int)((v >> 16) & 0xFFu);
+  it.gu = (v >> 24) & 1u, it.opens = (v >> 25) & 1u, it.closes = (v >> 26) & 1u;
+  return it;
+}
 
-// The CTA's list: A [0, nA) shared gate/up, B routed gate/up, C shared down,
-// D routed down.  Routed slots are 1.. in expert order and all the same size.
+// The CTA's ranges of the four parts.  Routed slots are 1.. in expert order
+// and all the same size.
 struct Plan {
-  int nkc, nht;
+  int nkc, nht;        // K chunks of h, 128-column tiles of h
+  int nkd_s, nkd_r;    // K chunks of the down pass: Is / 64, I / 64
+  int per_gu, per_dn;  // items of one routed slot
   int sa0, nA, rb0, nB, sc0, nC, rd0, nD;
-  int per_gu, per_dn;  // blocks of one routed slot
   __device__ __forceinline__ int total() const { return nA + nB + nC + nD; }
-  __device__ __forceinline__ Item at(int i) const {
-    Item it;
+  // Entry of item i.  Within a part, item g covers (slot base + g / per,
+  // tile (g % per) / n, K chunk g % n); a segment is a run of K chunks of one
+  // (slot, tile), so it opens at K chunk 0 or at the part's first item and
+  // closes at K chunk n - 1 or at the part's last item.  Neighbours from
+  // different parts are always in different segments (the pass or the slot
+  // differs), so the close of part A is known before the routing.
+  __device__ __forceinline__ uint32_t entry(int i) const {
+    int gu, s0, per, n, g0, cnt;
     if (i < nA) {
-      const int g = sa0 + i;
-      it.slot = 0, it.a = g / nkc, it.b = g % nkc, it.gu = true;
-    } else if (i < nA + nB) {
-      const int g = rb0 + (i - nA);
-      const int rel = g % per_gu;
-      it.slot = 1 + g / per_gu, it.a = rel / nkc, it.b = rel % nkc, it.gu = true;
-    } else if (i < nA + nB + nC) {
-      const int g = sc0 + (i - nA - nB);
-      it.slot = 0, it.a = g / nht, it.b = g % nht, it.gu = false;
+      gu = 1, s0 = 0, per = 0x7FFFFFFF, n = nkc, g0 = sa0, cnt = nA;
+    } else if ((i -= nA) < nB) {
+      gu = 1, s0 = 1, per = per_gu, n = nkc, g0 = rb0, cnt = nB;
+    } else if ((i -= nB) < nC) {
+      gu = 0, s0 = 0, per = 0x7FFFFFFF, n = nkd_s, g0 = sc0, cnt = nC;
     } else {
-      const int g = rd0 + (i - nA - nB - nC);
-      const int rel = g % per_dn;
-      it.slot = 1 + g / per_dn, it.a = rel / nht, it.b = rel % nht, it.gu = false;
+      i -= nC;
+      gu = 0, s0 = 1, per = per_dn, n = nkd_r, g0 = rd0, cnt = nD;
     }
-    return it;
-  }
-  // Whether item i closes its gate/up segment (the next item is not a
-  // gate/up pair of the same slot and feature tile) or its down chunk.
-  __device__ __forceinline__ bool closes(int i) const {
-    if (i + 1 >= total()) return true;
-    const Item a = at(i), b = at(i + 1);
-    return a.gu != b.gu || a.slot != b.slot || a.a != b.a;
-  }
-  __device__ __forceinline__ bool opens(int i) const {
-    if (i == 0) return true;
-    const Item a = at(i - 1), b = at(i);
-    return a.gu != b.gu || a.slot != b.slot || a.a != b.a;
+    const int g = g0 + i, sl = g / per, rel = g - sl * per, tile = rel / n, kc = rel - tile * n;
+    const bool opens = kc == 0 || i == 0, closes = kc == n - 1 || i == cnt - 1;
+    return (uint32_t)(s0 + sl) | ((uint32_t)tile << 8) | ((uint32_t)kc << 16) | ((uint32_t)gu << 24) |
+           ((uint32_t)opens << 25) | ((uint32_t)closes << 26);
   }
 };
 
@@ -215,8 +232,7 @@ __global__ void __launch_bounds__(D_THREADS, 1) decode_fused_kernel(DfParams P) 
   extern __shared__ uint8_t df_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(df_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* xt = ring + (size_t)D_NSLOT * D_SLOT;  // x: h / 64 swizzled 16-row tiles
-  uint8_t* hgt = xt + D_XT_BYTES;                 // silu(gate) * up tiles
-  DfSmem& S = *reinterpret_cast<DfSmem*>(hgt + (size_t)D_NHG * D_TILE);
+  DfSmem& S = *reinterpret_cast<DfSmem*>(xt + D_XT_BYTES);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = gridDim.x, b = blockIdx.x;
   const int t = P.t, h = P.h, E = P.E, k = P.k;
@@ -224,81 +240,80 @@ __global__ void __launch_bounds__(D_THREADS, 1) decode_fused_kernel(DfParams P) 
 
   Plan L{};
   L.nkc = h / D_KC, L.nht = h / 128;
-  L.per_gu = (P.I / 128) * L.nkc, L.per_dn = (P.I / D_KC) * L.nht;
+  L.nkd_s = P.Is / D_KC, L.nkd_r = P.I / D_KC;
+  L.per_gu = (P.I / 128) * L.nkc, L.per_dn = L.nht * L.nkd_r;
   {
-    const int sg = P.Is > 0 ? (P.Is / 128) * L.nkc : 0, sd = P.Is > 0 ? (P.Is / D_KC) * L.nht : 0;
+    const int sg = (P.Is / 128) * L.nkc, sd = L.nht * L.nkd_s;
     L.sa0 = split(sg, b, G), L.nA = split(sg, b + 1, G) - L.sa0;
     L.sc0 = split(sd, b, G), L.nC = split(sd, b + 1, G) - L.sc0;
     L.nB = 0, L.nD = 0, L.rb0 = 0, L.rd0 = 0;  // known after the routing
   }
-
   if (tid == 0) {
-    for (int i = 0; i < D_NSLOT; ++i) mbar_init(&S.full[i], 1), mbar_init(&S.empty[i], 4);
+    for (int i = 0; i < D_NSLOT; ++i) mbar_init(&S.full[i], 1), mbar_init(&S.empty[i], 1);
     for (int i = 0; i < D_NA; ++i) mbar_init(&S.a_full[i], 4), mbar_init(&S.a_empty[i], 1);
     for (int i = 0; i < D_NACC; ++i) mbar_init(&S.acc_full[i], 1), mbar_init(&S.acc_empty[i], 4);
-    for (int i = 0; i < D_NHG; ++i) mbar_init(&S.hg_full[i], 4), mbar_init(&S.hg_empty[i], 1);
+    mbar_init(&S.x_ready, 8);
     mbar_init(&S.ready, 1);
     mbar_init(&S.esync, 4);
     mbar_init(&S.drain, 1);
     S.abort = 0;
+    S.n_items = L.nA;
     fence_mbar_init();
   }
-  // x into the swizzled B tiles (rows past t are zero)
-  for (int q = tid; q < 16 * (h / 8); q += blockDim.x) {
-    const int r = q / (h / 8), p = q % (h / 8);
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < t) v = __ldg(reinterpret_cast<const uint4*>(P.x + (size_t)r * h) + p);
-    *reinterpret_cast<uint4*>(xt + (size_t)(p >> 3) * D_TILE + sw128_off(r, p & 7)) = v;
-  }
-  fence_async_smem();
+  for (int i = tid; i < L.nA; i += D_THREADS) S.items[i] = L.entry(i);
   if (warp == W_ISSUE) tmem_alloc(&S.tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_slot;
 
-  // The roles that start on part A wait here for parts B, C, D.
-  auto await_plan = [&]() -> bool {
-    if (!mbar_wait(&S.ready, 0, abort, D_WAIT_NS)) return false;
-    if (*abort) return false;
-    const int n = S.n_touched;
-    const int rg = n * L.per_gu, rd = n * L.per_dn;
-    L.rb0 = split(rg, b, G), L.nB = split(rg, b + 1, G) - L.rb0;
-    L.rd0 = split(rd, b, G), L.nD = split(rd, b + 1, G) - L.rd0;
-    return true;
+  // The roles that start on part A wait here for parts B, C, D; the list's
+  // length comes back (0 after an abort).
+  auto await_plan = [&]() -> int {
+    if (!mbar_wait(&S.ready, 0, abort, D_WAIT_NS)) return 0;
+    return *abort ? 0 : S.n_items;
   };
 
   if (warp == W_PROD) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
+      int total = L.nA, issued = 0;
       bool planned = false;
-      int issued = 0;
+      int hg_slot = -1;
+      const size_t rec_bytes = packed_rec_bytes(h, P.I);
+      const int kd_per_slot = P.imax / D_KC;
       for (int i = 0; !*abort; ++i) {
-        if (i == L.nA && !planned) {
-          if (!await_plan()) break;
+        if (i == total && !planned) {
+          total = await_plan();
           planned = true;
         }
-        if (i >= L.total()) break;
-        const Item it = L.at(i);
+        if (i >= total) break;
+        const Item it = item_unpack(S.items[i]);
         const int sl = i % D_NSLOT;
         if (!mbar_wait(&S.empty[sl], ((i / D_NSLOT) & 1) ^ 1, abort, D_WAIT_NS)) {
           df_timeout(P.st, abort, 71);
           break;
         }
-        const int Iu = it.slot == 0 ? P.Is : P.I;
-        const uint8_t* rec =
-            it.slot == 0 ? P.s_packed : P.packed + (size_t)S.slot_e[it.slot] * packed_rec_bytes(h, P.I);
-        const uint8_t* src;
-        uint32_t bytes;
+        const uint8_t* rec = it.slot == 0 ? P.s_packed : P.packed + (size_t)S.slot_e[it.slot] * rec_bytes;
+        uint8_t* dst = ring + (size_t)sl * D_SLOT;
         if (it.gu) {
-          src = rec + ((size_t)it.a * L.nkc + it.b) * D_SLOT;  // [feature tile][chunk][gate][up]
-          bytes = D_SLOT;
+          mbar_arrive_expect_tx(&S.full[sl], D_SLOT);
+          df_bulk(dst, rec + ((size_t)it.tile * L.nkc + it.kc) * D_SLOT, D_SLOT, &S.full[sl]);  // [ftile][chunk][g][u]
         } else {
-          src = rec + packed_gu_bytes(h, Iu) + ((size_t)it.b * (Iu / D_KC) + it.a) * PACK_QB;  // [out tile][chunk]
-          bytes = PACK_QB;
+          const int Iu = it.slot == 0 ? P.Is : P.I;
+          if (it.slot != hg_slot) {  // every B tile of the slot is written once all its feature tiles are complete
+            if (!spin_until(P.hgready + it.slot, (uint32_t)(Iu / 128), abort)) {
+              df_timeout(P.st, abort, 70);
+              break;
+            }
+            fence_async_global();
+            hg_slot = it.slot;
+          }
+          mbar_arrive_expect_tx(&S.full[sl], PACK_QB + D_TILE);
+          df_bulk(dst, rec + packed_gu_bytes(h, Iu) + ((size_t)it.tile * (Iu / D_KC) + it.kc) * PACK_QB, PACK_QB,
+                  &S.full[sl]);  // [out tile][chunk]
+          df_bulk(dst + D_HG_OFF, P.hg + ((size_t)it.slot * kd_per_slot + it.kc) * D_TILE, D_TILE, &S.full[sl]);
         }
-        mbar_arrive_expect_tx(&S.full[sl], bytes);
-        df_bulk(ring + (size_t)sl * D_SLOT, src, bytes, &S.full[sl]);
         issued = i + 1;
       }
       if (*abort) {
@@ -308,85 +323,97 @@ __global__ void __launch_bounds__(D_THREADS, 1) decode_fused_kernel(DfParams P) 
       }
     }
   } else if (warp == W_ISSUE) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(128, 16);
-      bool planned = false;
-      uint32_t u = 0, hgi = 0;  // accumulation units (segments, down items), down chunks
-      for (int i = 0; !*abort; ++i) {
-        if (i == L.nA && !planned) {
-          if (!await_plan()) break;
-          planned = true;
-        }
-        if (i >= L.total()) break;
-        const Item it = L.at(i);
-        const int as = i % D_NA, ab = (int)(u % D_NACC);
-        // the segment after part A always opens anew (another slot, or a down
-        // block), so the close of part A is known before the routing
-        const bool closes = (i + 1 == L.nA && !planned) ? true : L.closes(i);
-        const bool opens = L.opens(i);
-        if (opens || !it.gu) {
-          if (!mbar_wait(&S.acc_empty[ab], ((u / D_NACC) & 1) ^ 1, abort, D_WAIT_NS)) {
-            df_timeout(P.st, abort, 72);
-            break;
-          }
-        }
-        const int hs = (int)(hgi % D_NHG);
-        if (!it.gu && opens) {
-          if (!mbar_wait(&S.hg_full[hs], (hgi / D_NHG) & 1, abort, D_WAIT_NS)) {
-            df_timeout(P.st, abort, 73);
-            break;
-          }
-        }
-        if (!mbar_wait(&S.a_full[as], (i / D_NA) & 1, abort, D_WAIT_NS)) {
-          df_timeout(P.st, abort, 74);
-          break;
-        }
+    // ---------------------------------------------------------------- MMA issuer (warp-uniform)
+    const uint32_t idesc = idesc_bf16(128, 16);
+    int total = L.nA;
+    bool planned = false, live = true;
+    uint32_t u = 0;  // segments
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.x_ready, 0, abort, D_WAIT_NS))) {
+      if (lane == 0) df_timeout(P.st, abort, 69);
+      live = false;
+    }
+    for (int i = 0; live && !__any_sync(0xFFFFFFFFu, *abort); ++i) {  // warp-uniform exit
+      if (i == total && !planned) {
+        total = __shfl_sync(0xFFFFFFFFu, await_plan(), 0);
+        planned = true;
+      }
+      if (i >= total) break;
+      const Item it = item_unpack(S.items[i]);
+      const int as = i % D_NA, sl = i % D_NSLOT, ab = (int)(u % D_NACC);
+      bool got = true;
+      if (it.opens) got = mbar_wait(&S.acc_empty[ab], ((u / D_NACC) & 1) ^ 1, abort, D_WAIT_NS);
+      got = got && mbar_wait(&S.a_full[as], (i / D_NA) & 1, abort, D_WAIT_NS);
+      if (!__all_sync(0xFFFFFFFFu, got)) {
+        if (lane == 0) df_timeout(P.st, abort, 74);
+        break;
+      }
+      if (elect_one()) {
         tc_fence_after();
         const uint32_t acc = tmem + D_ACC_COL + ab * 32, a_st = tmem + as * 64;
         if (it.gu) {
-          const uint64_t bd = desc_sw128(smem_u32(xt + (size_t)it.b * D_TILE));
+          const uint64_t bd = desc_sw128(smem_u32(xt + (size_t)it.kc * D_TILE));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t accum = (opens && kk == 0) ? 0u : 1u;
+            const uint32_t accum = (it.opens && kk == 0) ? 0u : 1u;
             mma_bf16_ta(acc, a_st + 8 * kk, bd + 2 * kk, idesc, accum);
             mma_bf16_ta(acc + 16, a_st + 32 + 8 * kk, bd + 2 * kk, idesc, accum);
           }
         } else {
-          const uint64_t bd = desc_sw128(smem_u32(hgt + (size_t)hs * D_TILE));
+          const uint64_t bd = desc_sw128(smem_u32(ring + (size_t)sl * D_SLOT + D_HG_OFF));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) mma_bf16_ta(acc, a_st + 8 * kk, bd + 2 * kk, idesc, kk != 0);
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ta(acc, a_st + 8 * kk, bd + 2 * kk, idesc, (it.opens && kk == 0) ? 0u : 1u);
         }
         mma_commit(&S.a_empty[as]);
-        if (closes || !it.gu) {
-          mma_commit(&S.acc_full[ab]);
-          ++u;
-        }
-        if (!it.gu && closes) {
-          mma_commit(&S.hg_empty[hs]);
-          ++hgi;
-        }
+        mma_commit(&S.empty[sl]);  // the codes (and a down item's B tile) are consumed
+        if (it.closes) mma_commit(&S.acc_full[ab]);
       }
-      if (*abort) {
-        mma_commit(&S.drain);
-        const int never = 0;
-        mbar_wait(&S.drain, 0, &never, 100000000ull);
-      }
+      __syncwarp();
+      if (it.closes) ++u;
     }
+    if (__any_sync(0xFFFFFFFFu, *abort) && elect_one()) {
+      mma_commit(&S.drain);
+      const int never = 0;
+      mbar_wait(&S.drain, 0, &never, 100000000ull);
+    }
+    __syncwarp();
   } else if (warp < W_EPI0) {
-    // ---------------------------------------------------------------- dequantisation (two groups, alternate items)
+    // ---------------------------------------------------------------- x, then dequantisation
+    {
+      // x into the swizzled B tiles (rows past t are zero), the loads of a
+      // batch in flight together
+      const int dtid = tid - W_DQ0 * 32, hp = h / 8, nq = 16 * hp;
+      for (int q0 = dtid; q0 < nq; q0 += 256 * 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int q = q0 + j * 256, r = q / hp, p = q - r * hp;
+          v[j] = (q < nq && r < t) ? __ldg(reinterpret_cast<const uint4*>(P.x + (size_t)r * h) + p)
+                                   : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int q = q0 + j * 256, r = q / hp, p = q - r * hp;
+          if (q < nq) *reinterpret_cast<uint4*>(xt + (size_t)(p >> 3) * D_TILE + sw128_off(r, p & 7)) = v[j];
+        }
+      }
+      fence_async_smem();  // the tensor core reads the tiles through the async proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.x_ready);
+    }
     const int grp = (warp - W_DQ0) >> 2;
     const int q = warp & 3;       // tensor-memory lane quarter of this warp
     const int o = q * 32 + lane;  // weight row = tensor-memory lane
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    int total = L.nA;
     bool planned = false;
-    for (int i = grp; !*abort; i += 2) {
-      if (i >= L.nA && !planned) {
-        if (!__all_sync(0xFFFFFFFFu, await_plan())) break;
+    for (int i = grp; !__any_sync(0xFFFFFFFFu, *abort); i += 2) {  // warp-uniform exit
+      if (i >= total && !planned) {
+        total = __shfl_sync(0xFFFFFFFFu, await_plan(), 0);
         planned = true;
       }
-      if (i >= L.total()) break;
-      const Item it = L.at(i);
+      if (i >= total) break;
+      const Item it = item_unpack(S.items[i]);
       const int sl = i % D_NSLOT, as = i % D_NA;
       const bool got = mbar_wait(&S.full[sl], (i / D_NSLOT) & 1, abort, D_WAIT_NS) &&
                        mbar_wait(&S.a_empty[as], ((i / D_NA) & 1) ^ 1, abort, D_WAIT_NS);
@@ -411,10 +438,7 @@ __global__ void __launch_bounds__(D_THREADS, 1) decode_fused_kernel(DfParams P) 
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&S.a_full[as]);
-        mbar_arrive(&S.empty[sl]);  // the codes are in tensor memory: the ring slot is free
-      }
+      if (lane == 0) mbar_arrive(&S.a_full[as]);
     }
   } else {
     // ---------------------------------------------------------------- router, grouping, epilogue
@@ -442,18 +466,18 @@ __global__ void __launch_bounds__(D_THREADS, 1) decode_fused_kernel(DfParams P) 
           for (int m0 = 0; m0 < nm; m0 += 8) {
             uint4 wv[8], xv[8];  // every load of the batch in flight together
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int k0 = (m0 + u) * 256 + lane * 8;
-              const bool in = m0 + u < nm && k0 < h;
-              wv[u] = in ? __ldg(reinterpret_cast<const uint4*>(wrow + k0)) : make_uint4(0, 0, 0, 0);
-              xv[u] = in ? __ldg(reinterpret_cast<const uint4*>(xr + k0)) : make_uint4(0, 0, 0, 0);
+            for (int j = 0; j < 8; ++j) {
+              const int k0 = (m0 + j) * 256 + lane * 8;
+              const bool in = m0 + j < nm && k0 < h;
+              wv[j] = in ? __ldg(reinterpret_cast<const uint4*>(wrow + k0)) : make_uint4(0, 0, 0, 0);
+              xv[j] = in ? __ldg(reinterpret_cast<const uint4*>(xr + k0)) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              if (m0 + u >= nm || (m0 + u) * 256 + lane * 8 >= h) continue;
+            for (int j = 0; j < 8; ++j) {
+              if (m0 + j >= nm || (m0 + j) * 256 + lane * 8 >= h) continue;
 #pragma unroll
               for (int cc = 0; cc < 8; ++cc) {
-                const uint32_t ww = (&wv[u].x)[cc >> 1], xw = (&xv[u].x)[cc >> 1];
+                const uint32_t ww = (&wv[j].x)[cc >> 1], xw = (&xv[j].x)[cc >> 1];
                 a = fmaf((cc & 1) ? bf16hi(xw) : bf16lo(xw), (cc & 1) ? bf16hi(ww) : bf16lo(ww), a);
               }
             }
@@ -467,20 +491,39 @@ __global__ void __launch_bounds__(D_THREADS, 1) decode_fused_kernel(DfParams P) 
         }
       }
       if (P.s_gate && b == G - 1) {
+        const int hp = h / 8;
         for (int r = ew; r < t; r += 4) {
           float s = 0.f;
-          for (int i = lane; i < h; i += 32) s = fmaf(bf16f(P.x[(size_t)r * h + i]), bf16f(P.s_gate[i]), s);
+          for (int p0 = lane; p0 < hp; p0 += 32 * 8) {
+            uint4 xv[8], gv[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int p = p0 + 32 * j;
+              xv[j] = p < hp ? __ldg(reinterpret_cast<const uint4*>(P.x + (size_t)r * h) + p) : make_uint4(0, 0, 0, 0);
+              gv[j] = p < hp ? __ldg(reinterpret_cast<const uint4*>(P.s_gate) + p) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc) {
+                const uint32_t xw = (&xv[j].x)[cc], gw = (&gv[j].x)[cc];
+                s = fmaf(bf16lo(xw), bf16lo(gw), s);
+                s = fmaf(bf16hi(xw), bf16hi(gw), s);
+              }
+          }
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
           if (lane == 0) P.gate_vals[r] = 1.f / (1.f + __expf(-s));
         }
       }
-      const size_t n_gu = (size_t)P.max_slots * 2 * P.imax * t, n_acc = (size_t)t * h;
+      const size_t n_gu4 = (size_t)(t + t * k) * 2 * P.imax / 4, n_acc4 = (size_t)t * h / 4;
       const size_t n_ft = (size_t)P.max_slots * (P.imax / 128), n_h = (size_t)h / 128;
       const size_t gt = (size_t)b * 128 + etid, gs = (size_t)G * 128;
-      for (size_t i = gt; i < n_gu; i += gs) P.gu[i] = 0.f;
-      for (size_t i = gt; i < n_acc; i += gs) P.acc[i] = 0.f;
+      const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (size_t i = gt; i < n_gu4; i += gs) reinterpret_cast<float4*>(P.gu)[i] = z4;
+      for (size_t i = gt; i < n_acc4; i += gs) reinterpret_cast<float4*>(P.acc)[i] = z4;
       for (size_t i = gt; i < n_ft; i += gs) P.ftcount[i] = 0u;
+      for (size_t i = gt; i < (size_t)P.max_slots; i += gs) P.hgready[i] = 0u;
       for (size_t i = gt; i < n_h; i += gs) P.hcount[i] = 0u;
     }
     // grid-wide barrier: every call advances the counter by G, so the target
@@ -494,107 +537,124 @@ __global__ void __launch_bounds__(D_THREADS, 1) decode_fused_kernel(DfParams P) 
     }
     ok = esync() && !*abort;
 
-    // 2. selection and grouping (every CTA; E <= 256, t * k <= 128)
-    if (ok) {
-      for (int r = ew; r < t; r += 4) {
-        uint64_t key[NQ];
-#pragma unroll
-        for (int qq = 0; qq < NQ; ++qq) {
-          const int e = lane + 32 * qq;
-          key[qq] = e < E ? topk_key(__ldcg(P.logits + (size_t)r * P.Ep + e), e) : 0ull;
-        }
-        warp_topk_softmax<NQ>(key, k, lane, S.idx + r * k, S.w + r * k);
-      }
-      for (int e = etid; e <= E; e += 128) S.cnt[e] = 0;
-      ok = esync();
-    }
+    // 2. selection (rows over the four warps), then grouping in one warp
+    // (every CTA; E <= 256, t * k <= 128)
     const int npairs = t * k;
     if (ok) {
-      for (int p = etid; p < npairs; p += 128) atomicAdd(&S.cnt[S.idx[p]], 1);
+      // rows ew and ew + 4 (t <= 8): both rows' logits in flight together
+      uint64_t key0[NQ], key1[NQ];
+      const int r0 = ew, r1 = ew + 4;
+#pragma unroll
+      for (int qq = 0; qq < NQ; ++qq) {
+        const int e = lane + 32 * qq;
+        key0[qq] = e < E && r0 < t ? topk_key(__ldcg(P.logits + (size_t)r0 * P.Ep + e), e) : 0ull;
+        key1[qq] = e < E && r1 < t ? topk_key(__ldcg(P.logits + (size_t)r1 * P.Ep + e), e) : 0ull;
+      }
+      if (r0 < t) warp_topk_softmax<NQ>(key0, k, lane, S.idx + r0 * k, S.w + r0 * k);
+      if (r1 < t) warp_topk_softmax<NQ>(key1, k, lane, S.idx + r1 * k, S.w + r1 * k);
       ok = esync();
     }
-    if (ok) {
-      // scan over the experts, two per thread: list offsets and the slot of
-      // every touched expert
-      const int e0 = 2 * etid, e1 = e0 + 1;
-      const int n0 = e0 < E ? S.cnt[e0] : 0, n1 = e1 < E ? S.cnt[e1] : 0;
-      const int u0 = n0 > 0, u1 = n1 > 0;
-      int sn = n0 + n1, su = u0 + u1;
+    if (ok && ew == 0) {
+      for (int e = lane; e < E; e += 32) S.cnt[e] = 0;
+      __syncwarp();
+      for (int p = lane; p < npairs; p += 32) atomicAdd(&S.cnt[S.idx[p]], 1);
+      __syncwarp();
+      // lane l owns experts [l * epl, l * epl + epl): list offsets and the
+      // slot of every touched expert, by a scan over the lanes
+      const int epl = (E + 31) / 32, e0 = lane * epl;
+      int sn = 0, su = 0;
+      for (int j = 0; j < epl; ++j) {
+        const int e = e0 + j;
+        const int c = e < E ? S.cnt[e] : 0;
+        sn += c, su += c > 0;
+      }
+      int in = sn, iu = su;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int yn = __shfl_up_sync(0xFFFFFFFFu, sn, o), yu = __shfl_up_sync(0xFFFFFFFFu, su, o);
-        if (lane >= o) sn += yn, su += yu;
+        const int yn = __shfl_up_sync(0xFFFFFFFFu, in, o), yu = __shfl_up_sync(0xFFFFFFFFu, iu, o);
+        if (lane >= o) in += yn, iu += yu;
       }
-      if (lane == 31) S.wsum[ew] = (sn << 16) | su;
-      ok = esync();
-      if (ok) {
-        int bn = 0, bu = 0;
-        for (int qq = 0; qq < ew; ++qq) bn += S.wsum[qq] >> 16, bu += S.wsum[qq] & 0xFFFF;
-        const int off0 = bn + sn - n0 - n1, s0 = bu + su - u0 - u1;
-        if (e0 < E) {
-          S.off[e0] = off0;
-          if (u0) S.slot_e[1 + s0] = e0, S.slot_row0[1 + s0] = off0, S.slot_n[1 + s0] = n0;
+      int pos = in - sn, slot = iu - su;
+      for (int j = 0; j < epl; ++j) {
+        const int e = e0 + j;
+        if (e >= E) break;
+        const int c = S.cnt[e];
+        S.off[e] = pos;
+        if (c > 0) {
+          ++slot;
+          S.slot_e[slot] = e, S.slot_row0[slot] = pos, S.slot_n[slot] = c;
         }
-        if (e1 < E) {
-          S.off[e1] = off0 + n0;
-          if (u1) S.slot_e[1 + s0 + u0] = e1, S.slot_row0[1 + s0 + u0] = off0 + n0, S.slot_n[1 + s0 + u0] = n1;
+        pos += c;
+        S.cnt[e] = 0;  // from here: rows placed per expert
+      }
+      if (lane == 31) S.off[E] = in, S.n_touched = iu;
+      if (lane == 0) S.slot_n[0] = t;
+      __syncwarp();
+      // stable placement, row by row (a row names an expert once, so the
+      // lanes of one row touch distinct experts)
+      for (int r = 0; r < t; ++r) {
+        if (lane < k) {
+          const int p = r * k + lane, e = S.idx[p];
+          const int at = S.off[e] + S.cnt[e];
+          S.cnt[e] += 1;
+          S.rows[at] = r;
+          S.wts[at] = S.w[p];
+          if (b == 0) P.csr.slot_of[p] = at;
         }
-        if (etid == 127) {
-          S.off[E] = bn + sn;
-          S.n_touched = bu + su;
-          S.slot_n[0] = t;
-        }
-        ok = esync();
+        __syncwarp();
       }
     }
+    if (ok) ok = esync();
     if (ok) {
-      // stable placement: within an expert, rows ascend (a row names an expert once)
-      for (int p = etid; p < npairs; p += 128) {
-        const int e = S.idx[p], r = p / k;
-        int rank = 0;
-        for (int qq = 0; qq < r * k; ++qq) rank += S.idx[qq] == e;
-        const int pos = S.off[e] + rank;
-        S.rows[pos] = r;
-        S.wts[pos] = S.w[p];
-        if (b == 0) P.csr.slot_of[p] = pos;
+      // the rest of the list
+      const int n = S.n_touched;
+      const int rg = n * L.per_gu, rd = n * L.per_dn;
+      L.rb0 = split(rg, b, G), L.nB = split(rg, b + 1, G) - L.rb0;
+      L.rd0 = split(rd, b, G), L.nD = split(rd, b + 1, G) - L.rd0;
+      const int total = L.total();
+      if (total > D_MAX_ITEMS) {  // excluded by decode_fused_ok
+        if (etid == 0) df_timeout(P.st, abort, 68);
+        ok = false;
+      } else {
+        for (int i = L.nA + etid; i < total; i += 128) S.items[i] = L.entry(i);
+        if (etid == 0) S.n_items = total;
       }
-      for (int i = etid; i < h / 128; i += 128) S.htcnt[i] = 0;
-      ok = esync();
-    }
-    if (ok && b == 0) {
-      for (int p = etid; p < npairs; p += 128) {
-        P.idx[p] = S.idx[p];
-        P.w[p] = S.w[p];
-        P.csr.rows[p] = S.rows[p];
-        P.csr.weights[p] = S.wts[p];
+      for (int i = etid; i < L.nht; i += 128) S.htcnt[i] = 0;
+      if (b == 0) {
+        for (int p = etid; p < npairs; p += 128) {
+          P.idx[p] = S.idx[p];
+          P.w[p] = S.w[p];
+          P.csr.rows[p] = S.rows[p];
+          P.csr.weights[p] = S.wts[p];
+        }
+        for (int e = etid; e <= E; e += 128) P.csr.offsets[e] = S.off[e];
       }
-      for (int e = etid; e <= E; e += 128) P.csr.offsets[e] = S.off[e];
+      ok = esync() && ok;
     }
     // parts B, C, D are known: release the other roles (an abort releases
     // them too; they read the flag)
     if (etid == 0) mbar_arrive(&S.ready);
-    ok = ok && __all_sync(0xFFFFFFFFu, await_plan());
 
-    // 3. epilogue: drain the accumulators in item order
+    // 3. epilogue: drain the segments in list order
     const int qd = warp & 3;  // tensor-memory lane quarter of this warp
     const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
-    uint32_t u = 0, hgi = 0;
+    const int total = ok ? S.n_items : 0;
+    uint32_t u = 0;
     int seg_n = 0;
-    for (int i = 0; ok && i < L.total(); ++i) {
-      const Item it = L.at(i);
-      const bool closes = L.closes(i), opens = L.opens(i);
+    for (int i = 0; ok && i < total; ++i) {
+      const Item it = item_unpack(S.items[i]);
+      ++seg_n;
+      if (!it.closes) continue;
+      const int ab = (int)(u % D_NACC);
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.acc_full[ab], (u / D_NACC) & 1, abort, D_WAIT_NS))) {
+        if (lane == 0) df_timeout(P.st, abort, 78);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
       const int n_tok = S.slot_n[it.slot];
       const int row0 = it.slot == 0 ? -1 : S.slot_row0[it.slot];
       if (it.gu) {
-        ++seg_n;
-        if (!closes) continue;
-        const int ab = (int)(u % D_NACC);
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.acc_full[ab], (u / D_NACC) & 1, abort, D_WAIT_NS))) {
-          if (lane == 0) df_timeout(P.st, abort, 78);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
         uint32_t gv[16], uv[16];
         tmem_ld16(lane_base + D_ACC_COL + ab * 32, gv);
         tmem_ld16(lane_base + D_ACC_COL + ab * 32 + 16, uv);
@@ -603,69 +663,61 @@ __global__ void __launch_bounds__(D_THREADS, 1) decode_fused_kernel(DfParams P) 
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
         // column j of the accumulator is x row j; keep the slot's rows
-        const int f = it.a * 128 + qd * 32 + lane;
-        float* gb = P.gu + (size_t)it.slot * 2 * P.imax * t;
+        const int f = it.tile * 128 + qd * 32 + lane;
+        float* gb = P.gu + (size_t)(row0 < 0 ? 0 : t + row0) * 2 * P.imax;  // [row][gate, up][feature]
         for (int n = 0; n < n_tok; ++n) {
           const int r = row0 < 0 ? n : S.rows[row0 + n];
           float gval = 0.f, uval = 0.f;
 #pragma unroll
           for (int j = 0; j < D_MAX_T; ++j)
             if (j == r) gval = __uint_as_float(gv[j]), uval = __uint_as_float(uv[j]);
-          atomicAdd(gb + (size_t)f * t + n, gval);
-          atomicAdd(gb + (size_t)(P.imax + f) * t + n, uval);
+          atomicAdd(gb + (size_t)(2 * n) * P.imax + f, gval);
+          atomicAdd(gb + (size_t)(2 * n + 1) * P.imax + f, uval);
         }
         __threadfence();
         if (!esync()) {
           ok = false;
           break;
         }
-        if (etid == 0) atomicAdd(&P.ftcount[(size_t)it.slot * (P.imax / 128) + it.a], (uint32_t)seg_n);
-        seg_n = 0;
-        ++u;
-      } else {
-        const int hs = (int)(hgi % D_NHG);
-        if (opens) {
-          // silu(gate) * up of this chunk for the slot's rows, once its
-          // feature tile is complete
-          bool got = true;
-          if (lane == 0) got = mbar_wait(&S.hg_empty[hs], ((hgi / D_NHG) & 1) ^ 1, abort, D_WAIT_NS);
-          if (etid == 0 && got) {
-            got = spin_until(P.ftcount + (size_t)it.slot * (P.imax / 128) + it.a / 2, (uint32_t)L.nkc, abort);
-            if (!got) df_timeout(P.st, abort, 79);
-          }
-          got = __shfl_sync(0xFFFFFFFFu, got, 0);
-          if (!esync() || !got || *abort) {
-            ok = false;
-            break;
-          }
-          const float* gb = P.gu + (size_t)it.slot * 2 * P.imax * t;
-          const int n = etid >> 3, pc = etid & 7;  // token row n of the tile, 16-byte piece pc
-          uint32_t pk[4] = {0u, 0u, 0u, 0u};
-          if (n < n_tok) {
-#pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-              const int f = it.a * D_KC + pc * 8 + 2 * e2;
-              const float v0 =
-                  silu_mul_fast(__ldcg(gb + (size_t)f * t + n), __ldcg(gb + (size_t)(P.imax + f) * t + n));
-              const float v1 = silu_mul_fast(__ldcg(gb + (size_t)(f + 1) * t + n),
-                                             __ldcg(gb + (size_t)(P.imax + f + 1) * t + n));
-              pk[e2] = ((uint32_t)f2bf(v1) << 16) | f2bf(v0);
-            }
-          }
-          *reinterpret_cast<uint4*>(hgt + (size_t)hs * D_TILE + sw128_off(n, pc)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          fence_async_smem();  // the tensor core reads the tile through the async proxy
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&S.hg_full[hs]);
+        const size_t ft = (size_t)it.slot * (P.imax / 128) + it.tile;
+        if (etid == 0) {
+          const uint32_t before = atomicAdd(&P.ftcount[ft], (uint32_t)seg_n);
+          S.last = before + (uint32_t)seg_n == (uint32_t)L.nkc;
+          __threadfence();
         }
-        if (closes) ++hgi;
-        const int ab = (int)(u % D_NACC);
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.acc_full[ab], (u / D_NACC) & 1, abort, D_WAIT_NS))) {
-          if (lane == 0) df_timeout(P.st, abort, 80);
+        if (!esync()) {
           ok = false;
           break;
         }
-        tc_fence_after();
+        if (S.last) {
+          // this CTA completed the feature tile: silu(gate) * up of its 128
+          // features for the slot's rows, as the two B tiles of the down pass
+          for (int qq = etid; qq < 2 * 16 * 8; qq += 128) {
+            const int c = qq >> 7, n = (qq >> 3) & 15, pc = qq & 7;
+            uint32_t pk[4] = {0u, 0u, 0u, 0u};
+            if (n < n_tok) {
+#pragma unroll
+              for (int e2 = 0; e2 < 4; ++e2) {
+                const int fj = it.tile * 128 + c * 64 + pc * 8 + 2 * e2;
+                const float* gr = gb + (size_t)(2 * n) * P.imax + fj;
+                const float2 g2 = __ldcg(reinterpret_cast<const float2*>(gr));
+                const float2 u2 = __ldcg(reinterpret_cast<const float2*>(gr + P.imax));
+                const float v0 = silu_mul_fast(g2.x, u2.x), v1 = silu_mul_fast(g2.y, u2.y);
+                pk[e2] = ((uint32_t)f2bf(v1) << 16) | f2bf(v0);
+              }
+            }
+            uint8_t* tile = P.hg + ((size_t)it.slot * (P.imax / D_KC) + it.tile * 2 + c) * D_TILE;
+            *reinterpret_cast<uint4*>(tile + sw128_off(n, pc)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+          fence_async_global();  // bulk copies read the tiles
+          __threadfence();
+          if (!esync()) {
+            ok = false;
+            break;
+          }
+          if (etid == 0) atomicAdd(P.hgready + it.slot, 1u);
+        }
+      } else {
         uint32_t yv[16];
         tmem_ld16(lane_base + D_ACC_COL + ab * 32, yv);
         tmem_ld_wait();
@@ -673,7 +725,7 @@ __global__ void __launch_bounds__(D_THREADS, 1) decode_fused_kernel(DfParams P) 
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
         // column n is the slot's n-th row: weight * y into the block accumulator
-        const int col = it.b * 128 + qd * 32 + lane;
+        const int col = it.tile * 128 + qd * 32 + lane;
 #pragma unroll
         for (int n = 0; n < D_MAX_T; ++n) {
           if (n < n_tok) {
@@ -689,16 +741,17 @@ __global__ void __launch_bounds__(D_THREADS, 1) decode_fused_kernel(DfParams P) 
             atomicAdd(P.acc + (size_t)r * h + col, wt * __uint_as_float(yv[n]));
           }
         }
-        if (etid == 0) S.htcnt[it.b] += 1;
-        ++u;
+        if (etid == 0) S.htcnt[it.tile] += seg_n;
       }
+      seg_n = 0;
+      ++u;
     }
 
     // 4. output tiles this CTA completes (after every epilogue thread's additions)
     __threadfence();
     ok = esync() && ok && !*abort;
     if (ok) {
-      const uint32_t per_tile = (uint32_t)(S.n_touched * (P.I / D_KC) + (P.Is > 0 ? P.Is / D_KC : 0));
+      const uint32_t per_tile = (uint32_t)(S.n_touched * L.nkd_r + L.nkd_s);
       for (int ht = etid; ht < L.nht; ht += 128) {
         const int mine = S.htcnt[ht];
         S.htlast[ht] = mine > 0 && atomicAdd(&P.hcount[ht], (uint32_t)mine) + (uint32_t)mine == per_tile;
@@ -745,12 +798,21 @@ cudaError_t launch_df(const DfParams& P, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+size_t cdiv(size_t a, size_t b) { return (a + b - 1) / b; }
+
 }  // namespace
 
 bool decode_fused_ok(const moe_dims& d, uint32_t flags) {
-  return d.t <= D_MAX_T && d.E <= D_MAX_E && d.h <= D_MAX_H && (flags & MOE_PACKED_WEIGHTS) &&
-         (flags & MOE_FUSED_DECODE) &&
-         !(flags & (MOE_DETERMINISTIC | MOE_FORCE_SMALL_T | MOE_FORCE_LARGE_T | MOE_SIMPLE_KERNELS));
+  if (!(d.t <= D_MAX_T && d.E <= D_MAX_E && d.h <= D_MAX_H && (flags & MOE_PACKED_WEIGHTS) &&
+        (flags & MOE_FUSED_DECODE) &&
+        !(flags & (MOE_DETERMINISTIC | MOE_FORCE_SMALL_T | MOE_FORCE_LARGE_T | MOE_SIMPLE_KERNELS))))
+    return false;
+  // the longest list a CTA can get must fit its table
+  const size_t G = (size_t)sm_count(), nkc = d.h / D_KC, nht = d.h / 128;
+  const size_t slots_r = (size_t)(d.E < d.t * d.k ? d.E : d.t * d.k);
+  const size_t most = cdiv((size_t)(d.shared_inter / 128) * nkc, G) + cdiv(nht * (d.shared_inter / D_KC), G) +
+                      cdiv(slots_r * (d.inter / 128) * nkc, G) + cdiv(slots_r * nht * (d.inter / D_KC), G);
+  return G > 0 && most <= (size_t)D_MAX_ITEMS;
 }
 
 size_t decode_fused_ws_bytes(const moe_dims& d) {
@@ -758,8 +820,9 @@ size_t decode_fused_ws_bytes(const moe_dims& d) {
   const int slots = 1 + (d.E < d.t * d.k ? d.E : d.t * d.k);
   const int Ep = (d.E + 15) / 16 * 16;
   return align_up((size_t)d.t * Ep * 4, 256) + align_up((size_t)d.t * 4, 256) +
-         align_up((size_t)slots * 2 * imax * d.t * 4, 256) + align_up((size_t)d.t * d.h * 4, 256) +
-         align_up((size_t)slots * (imax / 128) * 4, 256) + align_up((size_t)(d.h / 128) * 4, 256);
+         align_up((size_t)(d.t + d.t * d.k) * 2 * imax * 4, 256) + align_up((size_t)d.t * d.h * 4, 256) +
+         align_up((size_t)slots * (imax / 128) * 4, 256) + align_up((size_t)slots * 4, 256) +
+         align_up((size_t)slots * (imax / D_KC) * D_TILE, 256) + align_up((size_t)(d.h / 128) * 4, 256);
 }
 
 cudaError_t launch_decode_fused(const uint16_t* x, const uint16_t* wr, const float* rbias, const moe_dims& d,
@@ -781,9 +844,11 @@ cudaError_t launch_decode_fused(const uint16_t* x, const uint16_t* wr, const flo
   };
   P.logits = reinterpret_cast<float*>(take((size_t)d.t * P.Ep * 4));
   P.gate_vals = reinterpret_cast<float*>(take((size_t)d.t * 4));
-  P.gu = reinterpret_cast<float*>(take((size_t)P.max_slots * 2 * P.imax * d.t * 4));
+  P.gu = reinterpret_cast<float*>(take((size_t)(d.t + d.t * d.k) * 2 * P.imax * 4));
   P.acc = reinterpret_cast<float*>(take((size_t)d.t * d.h * 4));
   P.ftcount = reinterpret_cast<uint32_t*>(take((size_t)P.max_slots * (P.imax / 128) * 4));
+  P.hgready = reinterpret_cast<uint32_t*>(take((size_t)P.max_slots * 4));
+  P.hg = reinterpret_cast<uint8_t*>(take((size_t)P.max_slots * (P.imax / D_KC) * D_TILE));
   P.hcount = reinterpret_cast<uint32_t*>(take((size_t)(d.h / 128) * 4));
   P.st = st;
   const int NQ = (d.E + 31) / 32;

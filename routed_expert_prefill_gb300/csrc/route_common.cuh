@@ -35,15 +35,14 @@ __device__ __forceinline__ void warp_topk_softmax(uint64_t (&key)[NQ], int k, in
     uint64_t best = 0;
 #pragma unroll
     for (int q = 0; q < NQ; ++q) best = key[q] > best ? key[q] : best;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-      best = other > best ? other : best;
-    }
-    const int e = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
+    // the warp's largest key, in two 32-bit reductions: the logit part,
+    // then the expert part among the lanes that hold that logit
+    const uint32_t hi = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(best >> 32));
+    const uint32_t lo = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(best >> 32) == hi ? (uint32_t)best : 0u);
+    const int e = (int)(0xFFFFFFFFu - lo);
     if (lane == j) {
       my_e = e;
-      my_l = key_float((uint32_t)(best >> 32));
+      my_l = key_float(hi);
     }
     if ((e & 31) == lane) {
 #pragma unroll

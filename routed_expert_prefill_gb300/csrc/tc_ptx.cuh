@@ -66,6 +66,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// One lane of the (fully active) warp is elected: the lowest, so the same
+// lane every time.  The code around it stays warp-uniform, which keeps the
+// operands of the tensor-core instructions it issues in uniform registers.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile("{\n.reg .pred q;\n.reg .b32 r;\nelect.sync r|q, 0xffffffff;\nselp.u32 %0, 1, 0, q;\n}" : "=r"(p));
+  return p != 0;
+}
+
 // ----------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
   asm volatile(
