@@ -312,6 +312,26 @@ int moe_clear_device_status(void* ws, void* stream);
 int moe_read_device_status(void* ws, void* stream);
 
 /*
+ * Test hook for the bounded device waits (no counterpart in the method).
+ * Sets `what` in the status block of `ws` (enqueued on `stream`); until
+ * moe_read_device_status clears it, the calls on this workspace make one
+ * kind of wait run out instead of completing:
+ *   MOE_STALL_WEIGHT_COPIES: the weight producer of the tensor-core expert
+ *     kernels (packed and row-major) and of the small-t kernels issues no
+ *     copy, so their consumers' waits give up;
+ *   MOE_STALL_GRID_BARRIER: the grid barrier of the fused decode launch
+ *     waits for one arrival more than the grid has.
+ * Each such wait gives up after its limit (2 s of device time), records
+ * MOE_ETIMEOUT, and its CTA lets the copies and MMAs in flight land, frees
+ * its tensor memory and returns; later calls on a cleared workspace run
+ * normally.  Nothing else reads the hook.  Errors: MOE_EWORKSPACE,
+ * MOE_EINVAL (unknown bits), MOE_ECUDA.
+ */
+#define MOE_STALL_WEIGHT_COPIES 0x1u
+#define MOE_STALL_GRID_BARRIER 0x2u
+int moe_debug_stall(void* ws, uint32_t what, void* stream);
+
+/*
  * Launch accounting (benchmark support; no counterpart in the method).
  * While enabled, every kernel the library launches is counted and
  * bracketed by a pair of CUDA events on the stream it is launched on, so a

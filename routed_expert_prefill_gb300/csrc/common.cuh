@@ -32,7 +32,8 @@ struct DeviceStatus {
   uint32_t route_done;    // router, small t: CTAs finished (the last one resets it)
   uint32_t gv_done;       // small-t down kernel: CTAs finished (the last one finalises and resets it)
   uint32_t fused_bar;     // fused decode launch: grid-barrier arrivals (every call adds the grid size)
-  uint32_t pad[57];
+  uint32_t stall;         // test hook (moe_debug_stall): MOE_STALL_* bits of waits that must run out
+  uint32_t pad[56];
 };
 
 __device__ __forceinline__ void raise_flag(DeviceStatus* st, uint32_t f) {

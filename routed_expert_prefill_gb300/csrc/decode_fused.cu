@@ -532,7 +532,8 @@ __global__ void __launch_bounds__(D_THREADS, 1) decode_fused_kernel(DfParams P) 
     bool ok = esync();
     if (ok && etid == 0) {
       const uint32_t arrival = atomicAdd(&P.st->fused_bar, 1u);
-      const uint32_t target = (arrival / (uint32_t)G + 1u) * (uint32_t)G;
+      // (one arrival more under the MOE_STALL_GRID_BARRIER test hook: the wait runs out)
+      const uint32_t target = (arrival / (uint32_t)G + 1u) * (uint32_t)G + ((P.st->stall & MOE_STALL_GRID_BARRIER) ? 1u : 0u);
       if (!spin_until(&P.st->fused_bar, target, abort)) df_timeout(P.st, abort, 77);
     }
     ok = esync() && !*abort;

@@ -534,7 +534,8 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_gateup(Gv2Params Q) {
   // The producer warp starts the weight stream at once; the consumer warps
   // meanwhile stage the token rows (L2 reads) and meet at a named barrier.
   if (warp == GV2_CONS / 32) {
-    if (lane == 0) {
+    // no copy under the MOE_STALL_WEIGHT_COPIES test hook: the consumers' waits run out
+    if (lane == 0 && !(P.status && (P.status->stall & MOE_STALL_WEIGHT_COPIES))) {
       bool armed[ST];
       uint32_t par[ST];
 #pragma unroll
@@ -712,7 +713,8 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_down(Gv2Params Q) {
     // meanwhile form hg from the K-slice partial sums and meet at a named
     // barrier.
     if (warp == GV2_CONS / 32) {
-      if (lane == 0) {
+      // no copy under the MOE_STALL_WEIGHT_COPIES test hook: the consumers' waits run out
+      if (lane == 0 && !(P.status && (P.status->stall & MOE_STALL_WEIGHT_COPIES))) {
         bool armed[ST];
         uint32_t par[ST];
 #pragma unroll

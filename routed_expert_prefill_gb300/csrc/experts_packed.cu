@@ -388,7 +388,8 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
 
   if (warp == W_CODE) {
     // ------------------------------------------------------------ packed weight blocks, CPS chunks per copy
-    if (lane == 0) {
+    // (none under the MOE_STALL_WEIGHT_COPIES test hook: the consumers' waits run out)
+    if (lane == 0 && !(p.status && (p.status->stall & MOE_STALL_WEIGHT_COPIES))) {
       uint32_t it = 0;
       bool armed[C::SC];
       uint32_t par[C::SC];

@@ -398,7 +398,8 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
 
   if (warp == W_CODE) {
     // ------------------------------------------------------------ code producer
-    if (lane == 0) {
+    // (no copy under the MOE_STALL_WEIGHT_COPIES test hook: the consumers' waits run out)
+    if (lane == 0 && !(p.status && (p.status->stall & MOE_STALL_WEIGHT_COPIES))) {
       prefetch_tmap(&tm_codes);
       if (p.Is > 0) prefetch_tmap(&tm_scodes);
       uint32_t it = 0;

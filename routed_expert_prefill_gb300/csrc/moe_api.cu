@@ -149,6 +149,8 @@ int cuda_status(cudaError_t e, const char* what) {
 
 }  // namespace
 
+__global__ void set_stall_kernel(DeviceStatus* st, uint32_t what) { st->stall = what; }
+
 extern "C" {
 
 const char* moe_last_error(void) { return g_err; }
@@ -391,6 +393,14 @@ int moe_clear_device_status(void* ws, void* stream) {
   if (!ws) return set_error(MOE_EWORKSPACE, "workspace is NULL");
   return cuda_status(cudaMemsetAsync(ws, 0, sizeof(DeviceStatus), (cudaStream_t)stream),
                      "moe_clear_device_status");
+}
+
+int moe_debug_stall(void* ws, uint32_t what, void* stream) {
+  if (!ws) return set_error(MOE_EWORKSPACE, "workspace is NULL");
+  if (what & ~(MOE_STALL_WEIGHT_COPIES | MOE_STALL_GRID_BARRIER))
+    return set_error(MOE_EINVAL, "unknown stall bits 0x%x", what & ~(MOE_STALL_WEIGHT_COPIES | MOE_STALL_GRID_BARRIER));
+  set_stall_kernel<<<1, 1, 0, (cudaStream_t)stream>>>((DeviceStatus*)ws, what);
+  return cuda_status(cudaGetLastError(), "moe_debug_stall");
 }
 
 int moe_read_device_status(void* ws, void* stream) {

@@ -29,6 +29,8 @@ MOE_FORCE_LARGE_T = 0x4
 MOE_SIMPLE_KERNELS = 0x8
 MOE_PACKED_WEIGHTS = 0x10
 MOE_FUSED_DECODE = 0x20
+MOE_STALL_WEIGHT_COPIES = 0x1
+MOE_STALL_GRID_BARRIER = 0x2
 
 # Every symbol include/moe.h declares.
 EXPORTS = (
@@ -47,6 +49,7 @@ EXPORTS = (
     "moe_pack_experts",
     "moe_build_csr_noalloc",
     "moe_forward",
+    "moe_debug_stall",
 )
 
 
@@ -111,6 +114,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_clear_device_status.argtypes = [vp, vp]
     lib.moe_read_device_status.restype = ctypes.c_int
     lib.moe_read_device_status.argtypes = [vp, vp]
+    lib.moe_debug_stall.restype = ctypes.c_int
+    lib.moe_debug_stall.argtypes = [vp, u32, vp]
     lib.moe_profile_enable.restype = ctypes.c_int
     lib.moe_profile_enable.argtypes = [ctypes.c_int]
     lib.moe_profile_read.restype = ctypes.c_int
@@ -451,6 +456,13 @@ def pack_experts(codes: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor
     _check(lib.moe_pack_experts(ctypes.byref(q), ctypes.byref(dims), 1 if shared else 0, _ptr(dst), n,
                                 _stream(stream)))
     return dst
+
+
+def debug_stall(ws: torch.Tensor, what: int, stream=None) -> None:
+    """Test hook: make one kind of bounded device wait run out on the calls
+    that use ``ws`` until read_device_status clears it (MOE_STALL_* bits)."""
+    _need(ws, "ws", (torch.uint8,))
+    _check(load_library().moe_debug_stall(_ptr(ws), what, _stream(stream)))
 
 
 def read_device_status(ws: torch.Tensor, stream=None) -> int:
