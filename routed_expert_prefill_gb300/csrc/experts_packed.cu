@@ -55,7 +55,7 @@ using namespace tc;
 // more tokens).
 constexpr int PTILE = 128;
 constexpr int PTILE_SMALL = 64;
-constexpr int PTILE_LARGE = 192;  // experts with ~100 rows or more: one tile for up to 192 rows
+constexpr int PTILE_LARGE = 160;  // experts with ~100 rows or more: one tile for up to 160 rows
 constexpr int KC = 64;      // K per chunk = one quantisation group
 constexpr int QB = 4096 + 256 + 256;  // one packed 128 x 64 block
 constexpr uint64_t WAIT_NS = 2000000000ull;
