@@ -531,7 +531,15 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     for (int u = unit0; u < n_units && !*abort; u += ustride) {
       const PUnit U = decode_punit<GATEUP, CP, C::B_STAGE>(p, u);
       bool ok = true;
+      // the token stage of each A stage, counted without a division: a B
+      // stage spans spb whole A stages
+      const int spb = U.kps / CPS;
+      int bsub = 0;
+      uint32_t bcur = bbase;
       for (int st = 0; st < U.nkc / CPS; ++st, ++ast) {
+        const bool b_first = bsub == 0;
+        const uint32_t bst = bcur;
+        if (++bsub == spb) bsub = 0, ++bcur;
         if ((int)(ast & 1) != grp) continue;
         const int sc = ast % C::SC, sa = ast % C::SA;
         const uint32_t a_par = ((ast / C::SA) & 1) ^ 1;
@@ -589,11 +597,10 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         // the a_full of the first A stage it serves completes.  Later A
         // stages of the same B stage are ordered after that observation by
         // the issuer's own earlier wait, so only the first one checks.
-        const int kcs = st * CPS;
-        if (kcs % U.kps == 0) {
-          const uint32_t bst = bbase + (uint32_t)(kcs / U.kps);
+        if (b_first) {
           bool b_ok = true;
-          if (lane == 0) b_ok = mbar_wait(&S.b_full[bst % SB], (bst / SB) & 1, abort, WAIT_NS);
+          if (lane == 0 && !mbar_test(&S.b_full[bst % SB], (bst / SB) & 1))
+            b_ok = mbar_wait(&S.b_full[bst % SB], (bst / SB) & 1, abort, WAIT_NS);
           b_ok = __shfl_sync(0xFFFFFFFFu, b_ok, 0);
           if (!b_ok) {
             if (lane == 0) note_timeout(p.status, abort, GATEUP ? 34 : 44);
