@@ -49,10 +49,14 @@ namespace {
 using namespace tc;
 
 // Rows per tile (MMA N): 128; 64 for chunks whose experts see few rows each
-// (the smaller accumulators then leave room for a deeper A ring); 192 for
+// (the smaller accumulators then leave room for a deeper A ring); 160 for
 // chunks whose experts see about 100 rows or more (one tile per expert
 // instead of two part-empty ones, and each dequantised weight block serves
-// more tokens).
+// more tokens).  160 rather than 192: the gate and up accumulators of a
+// 160-row tile leave three A stages in tensor memory instead of two, and
+// with two the dequantisation of stage s + 2 waited for stage s's MMAs and
+// the tensor pipe idled; at t = 4096, E = 256 hardly any expert sees more
+// than 160 rows.
 constexpr int PTILE = 128;
 constexpr int PTILE_SMALL = 64;
 constexpr int PTILE_LARGE = 160;  // experts with ~100 rows or more: one tile for up to 160 rows
@@ -91,10 +95,10 @@ struct PCfg {
   static constexpr int NACC = GATEUP ? 1 : 2;            // accumulator buffers
   static constexpr int ACC_COLS = GATEUP ? 2 * PT : PT;  // TMEM columns per accumulator buffer
   static constexpr int A_COL = NACC * ACC_COLS;          // first column of the A ring
-  static constexpr int SA = (512 - A_COL) / A_STAGE;     // A stages: 2 / 4 at PT 128, 3 / 3 at PT 64, 2 / 2 at PT 192
+  static constexpr int SA = (512 - A_COL) / A_STAGE;     // A stages: 2 / 4 at PT 128, 3 / 3 at PT 64, 3 / 3 at PT 160
   static constexpr int NISS = GATEUP ? 2 : 1;            // MMA issuing threads (gate and up apart)
   // Token-tile stages, and the ring takes all the shared memory the code
-  // ring, the epilogue staging and the barriers leave.  On 192-row tiles a
+  // ring, the epilogue staging and the barriers leave.  On 160-row tiles a
   // stage holds CP chunks of a full tile (every A stage reads a single B
   // stage) and the ring is seven stages deep: the gathered token images
   // arrive several stage times after they are requested, so the ring's
@@ -769,8 +773,8 @@ cudaError_t launch_packed_gemm(const PParams& P, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-// K chunks per stage: gate/up two (one on 192-row tiles, whose 384
-// accumulator columns leave 128 for the A ring); down four when every inter
+// K chunks per stage: gate/up two (one on 160-row tiles, whose 320
+// accumulator columns leave 192 for the A ring); down four when every inter
 // is a multiple of 256 on tiles of up to 128 rows, else two.
 template <int PT>
 cudaError_t launch_packed_gemms(const PParams& P, cudaStream_t stream) {
@@ -820,8 +824,8 @@ cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, c
 
   // Tile height by the rows an expert sees on average: 64 up to 40 rows (a
   // larger tile would be mostly padding, and the smaller accumulators leave
-  // TMEM for a deeper A ring), 128 up to 96, else 192, so that experts of
-  // 100-190 rows (the near-uniform t = 4096 chunks) take one tile each
+  // TMEM for a deeper A ring), 128 up to 96, else 160, so that experts of
+  // 100-160 rows (the near-uniform t = 4096 chunks) take one tile each
   // instead of two half-empty ones.
   const long pairs = (long)a.t * a.k;
   const int pt = pairs <= 40L * a.E ? PTILE_SMALL : pairs <= 96L * a.E ? PTILE : PTILE_LARGE;
