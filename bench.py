@@ -125,10 +125,8 @@ def step_roofline(work: dict, ms: float, peaks: dict) -> dict:
 # otherwise).
 PACKED_SOURCES = ("experts_packed.cu", "tc_ptx.cuh", "tc_common.cuh", "common.cuh", "experts.cuh")
 MEASURED_TRAFFIC = {
-    ("t512_h2048_e128", "gateup", 16): dict(bytes=264.25e6, src="59dce5c721bcb98c"),
-    ("t512_h2048_e128", "down", 16): dict(bytes=130.16e6, src="59dce5c721bcb98c"),
-    ("t4096_h2048_e128_skewed", "gateup", 16): dict(bytes=301.81e6, src="59dce5c721bcb98c"),
-    ("t4096_h2048_e128_skewed", "down", 16): dict(bytes=139.19e6, src="59dce5c721bcb98c"),
+    ("t4096_h4096_e256", "gateup", 16): dict(bytes=2346.92e6, src="93f74e72d52a31a9"),
+    ("t4096_h4096_e256", "down", 16): dict(bytes=1731.46e6, src="93f74e72d52a31a9"),
 }
 
 
