@@ -260,9 +260,10 @@ int moe_forward(const uint16_t* x, const uint16_t* wr, const float* rbias, const
  *
  *   - t*k must not exceed MOE_NOALLOC_MAX_PAIRS (else MOE_ESHAPE, nothing
  *     enqueued); E <= 1024, k <= min(E, 16).
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *   - Every call looks up the array's device address (cudaGetSymbolAddress)
+ *     for the current device, so a device reset or a re-created context
+ *     leaves no stale address behind.  The first call on a device may load
+ *     the library's module: make it before any stream capture.
  *   - All calls share the one array: calls whose GPU work overlaps (other
  *     streams, other threads) race and give wrong results.  Order them on one
  *     stream or synchronise between them.

@@ -365,8 +365,6 @@ cudaError_t launch_build_csr(const int32_t* idx, const float* w, int t, int k, i
 // fixed array in this library's device image, so each GPU that loads the
 // library holds it (NOALLOC_SCRATCH_BYTES) until the process exits.
 // ----------------------------------------------------------------------------
-#include <mutex>
-
 namespace moe {
 
 namespace {
@@ -380,10 +378,6 @@ constexpr size_t NOALLOC_SCRATCH_BYTES = NOALLOC_BASE_OFF + (size_t)MOE_NOALLOC_
 // table holds E * ceil(t*k / CSR_CHUNK) entries, which is at most
 // 1024 * MOE_NOALLOC_MAX_PAIRS / 1024 = MOE_NOALLOC_MAX_PAIRS.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
-
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-unsigned char* g_noalloc_ptr[kMaxDevices] = {};
 
 }  // namespace
 
@@ -405,23 +399,17 @@ extern "C" int moe_build_csr_noalloc(const int32_t* idx, const float* w, const m
   for (const void* p : ptrs)
     if ((uintptr_t)p % 4) return set_error(MOE_EINVAL, "a pointer argument is not 4-byte aligned");
 
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return set_error(MOE_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(err));
-  if (dev < 0 || dev >= kMaxDevices) return set_error(MOE_EINVAL, "device %d out of range", dev);
+  // The device address of the array, looked up on every call: after a
+  // device reset or a re-created primary context the module is loaded anew
+  // and a cached address would be stale (the lookup is cheap once loaded).
   unsigned char* scratch;
   {
-    // First call on this device: look up the device address of the array
-    // (the host-side name of a __device__ array is not a device address).
-    std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-      void* p = nullptr;
-      err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-      if (err != cudaSuccess) return set_error(MOE_ECUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(err));
-      g_noalloc_ptr[dev] = static_cast<unsigned char*>(p);
-    }
-    scratch = g_noalloc_ptr[dev];
+    void* p = nullptr;
+    cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (err != cudaSuccess) return set_error(MOE_ECUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(err));
+    scratch = static_cast<unsigned char*>(p);
   }
+  cudaError_t err;
   cudaStream_t s = (cudaStream_t)stream;
   // The status flags are OR-ed into; everything else is written before it is read.
   err = cudaMemsetAsync(scratch, 0, sizeof(DeviceStatus), s);
