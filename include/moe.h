@@ -267,11 +267,19 @@ int moe_forward(const uint16_t* x, const uint16_t* wr, const float* rbias, const
  *   - All calls share the one array: calls whose GPU work overlaps (other
  *     streams, other threads) race and give wrong results.  Order them on one
  *     stream or synchronise between them.
- *   - An id outside [0, E) drops its pair (slot_of = -1) as in moe_build_csr;
- *     the device-side flags of this variant are not reported.
+ *   - An id outside [0, E) drops its pair (slot_of = -1) as in moe_build_csr
+ *     and raises a device-side flag in the array's status block, which
+ *     moe_noalloc_read_status reports.
  * Errors: MOE_EINVAL, MOE_ESHAPE, MOE_ECUDA.
  */
 #define MOE_NOALLOC_MAX_PAIRS 65536
+/* Synchronise `stream`, read the status flags of moe_build_csr_noalloc's
+ * scratch on the current device and clear them: MOE_OK, MOE_EDEVICE (an id
+ * outside [0, E) was dropped since the last read) or MOE_ECUDA.  Reads
+ * nothing else; calls on other streams race with it as with the grouping
+ * itself. */
+int moe_noalloc_read_status(void* stream);
+
 int moe_build_csr_noalloc(const int32_t* idx, const float* w, const moe_dims* dims, const moe_csr* csr,
                           void* stream);
 

@@ -383,6 +383,23 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH
 
 }  // namespace moe
 
+extern "C" int moe_noalloc_read_status(void* stream) {
+  using namespace moe;
+  void* p = nullptr;
+  cudaError_t err = cudaGetSymbolAddress(&p, moe::g_noalloc_scratch);
+  if (err != cudaSuccess) return set_error(MOE_ECUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(err));
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t flags = 0;
+  if ((err = cudaMemcpyAsync(&flags, p, sizeof(flags), cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
+      (err = cudaStreamSynchronize(s)) != cudaSuccess ||
+      (err = cudaMemsetAsync(p, 0, sizeof(DeviceStatus), s)) != cudaSuccess ||
+      (err = cudaStreamSynchronize(s)) != cudaSuccess)
+    return set_error(MOE_ECUDA, "moe_noalloc_read_status: %s", cudaGetErrorString(err));
+  if (flags & (FLAG_BAD_EXPERT | FLAG_BAD_ROW | FLAG_BAD_OFFSETS))
+    return set_error(MOE_EDEVICE, "moe_build_csr_noalloc: expert id out of range (flags 0x%x)", flags);
+  return MOE_OK;
+}
+
 extern "C" int moe_build_csr_noalloc(const int32_t* idx, const float* w, const moe_dims* dims, const moe_csr* csr,
                                      void* stream) {
   using namespace moe;
@@ -411,9 +428,8 @@ extern "C" int moe_build_csr_noalloc(const int32_t* idx, const float* w, const m
   }
   cudaError_t err;
   cudaStream_t s = (cudaStream_t)stream;
-  // The status flags are OR-ed into; everything else is written before it is read.
-  err = cudaMemsetAsync(scratch, 0, sizeof(DeviceStatus), s);
-  if (err != cudaSuccess) return set_error(MOE_ECUDA, "status clear: %s", cudaGetErrorString(err));
+  // The status flags are OR-ed into and kept until moe_noalloc_read_status
+  // clears them; everything else is written before it is read.
   WsLayout L{};
   L.status = 0;
   L.csr_rank = NOALLOC_RANK_OFF;

@@ -48,6 +48,7 @@ EXPORTS = (
     "moe_packed_bytes",
     "moe_pack_experts",
     "moe_build_csr_noalloc",
+    "moe_noalloc_read_status",
     "moe_forward",
     "moe_debug_stall",
 )
@@ -114,6 +115,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_clear_device_status.argtypes = [vp, vp]
     lib.moe_read_device_status.restype = ctypes.c_int
     lib.moe_read_device_status.argtypes = [vp, vp]
+    lib.moe_noalloc_read_status.restype = ctypes.c_int
+    lib.moe_noalloc_read_status.argtypes = [vp]
     lib.moe_debug_stall.restype = ctypes.c_int
     lib.moe_debug_stall.argtypes = [vp, u32, vp]
     lib.moe_profile_enable.restype = ctypes.c_int
@@ -372,6 +375,13 @@ def moe_build_csr_noalloc(idx: torch.Tensor, w: torch.Tensor, E: int, out: Csr |
     c = out.c()
     _check(lib.moe_build_csr_noalloc(_ptr(idx), _ptr(w), ctypes.byref(dims), ctypes.byref(c), _stream(stream)))
     return out
+
+
+def noalloc_read_status(stream=None) -> int:
+    """Synchronise and return the status of moe_build_csr_noalloc's scratch on
+    the current device (0 = clean, MOE_EDEVICE = an id out of range was
+    dropped since the last read); clears it."""
+    return load_library().moe_noalloc_read_status(_stream(stream))
 
 
 def moe_experts_fwd(x: torch.Tensor, csr: Csr, experts: tuple, shared: tuple | None, dims: MoeDims,

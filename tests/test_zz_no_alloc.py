@@ -75,3 +75,23 @@ def test_noalloc_rejects_more_pairs_than_its_scratch_holds(moe):
         moe.moe_build_csr_noalloc(idx, w, 16)
     assert ei.value.status == -2
     assert b"scratch" in moe.load_library().moe_last_error()
+
+
+@pytest.mark.parametrize("t,k,E", [(37, 4, 16), (300, 8, 64)])  # the one-block path and the three-kernel path
+def test_noalloc_reports_dropped_ids(moe, t, k, E):
+    """An id outside [0, E) drops its pair (slot_of = -1), and the scratch's
+    status block reports it to moe_noalloc_read_status until that read clears
+    it; a later clean call leaves the status clean."""
+    moe.noalloc_read_status()  # clears whatever earlier calls left
+    idx, w = _routing(t, k, E, 11)
+    idx[3, 1] = E + 7
+    got = moe.moe_build_csr_noalloc(idx, w, E)
+    ref = moe.moe_build_csr(idx, w, E)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(got.slot_of.cpu().numpy(), ref.slot_of.cpu().numpy())
+    assert int(got.slot_of.cpu()[3 * k + 1]) == -1
+    assert moe.noalloc_read_status() == -5  # MOE_EDEVICE
+    assert moe.noalloc_read_status() == 0
+    idx2, w2 = _routing(t, k, E, 12)
+    moe.moe_build_csr_noalloc(idx2, w2, E)
+    assert moe.noalloc_read_status() == 0
