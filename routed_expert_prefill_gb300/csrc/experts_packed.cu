@@ -82,21 +82,31 @@ constexpr int CPS_DEFAULT = 2;        // K chunks per code stage and per A stage
 // CP K chunks per stage: 2, or 4 for the down pass on 64-row tiles (its
 // blocks are half the gate/up stage's, so the per-stage waits and fences
 // would otherwise be spread over only two blocks per warp).
-template <bool GATEUP, int PT, int CP>
+// Kernel modes: the down pass on one 128-row output tile per unit, the
+// gate/up pass, and the down pass on two adjacent output tiles per unit.  In
+// the paired modes two weight matrices (gate and up, or two output tiles)
+// share every token stage: two MMA issuers, two accumulators, one token
+// image read for both, which halves the down pass's token-image ingest per
+// weight block.
+constexpr int MODE_DN = 0, MODE_GU = 1, MODE_DN2 = 2;
+
+template <int MODE, int PT, int CP>
 struct PCfg {
+  static constexpr bool GATEUP = MODE == MODE_GU;
+  static constexpr bool PAIRED = MODE != MODE_DN;
   static constexpr int CPS = CP;
-  static constexpr int NMAT = GATEUP ? 2 : 1;
+  static constexpr int NMAT = PAIRED ? 2 : 1;
   static constexpr int C_STAGE = CPS * NMAT * QB;        // packed blocks of one stage
   // Code stages: four (measured: the code producer stays several stages
   // ahead of the dequantisation with four; more gave nothing), so that the
   // token-tile ring gets the rest of shared memory.
   static constexpr int SC = 4;
   static constexpr int A_STAGE = CPS * NMAT * 32;        // TMEM columns per A stage
-  static constexpr int NACC = GATEUP ? 1 : 2;            // accumulator buffers
-  static constexpr int ACC_COLS = GATEUP ? 2 * PT : PT;  // TMEM columns per accumulator buffer
+  static constexpr int NACC = PAIRED ? 1 : 2;            // accumulator buffers
+  static constexpr int ACC_COLS = PAIRED ? 2 * PT : PT;  // TMEM columns per accumulator buffer
   static constexpr int A_COL = NACC * ACC_COLS;          // first column of the A ring
   static constexpr int SA = (512 - A_COL) / A_STAGE;     // A stages: 2 / 4 at PT 128, 3 / 3 at PT 64, 3 / 3 at PT 160
-  static constexpr int NISS = GATEUP ? 2 : 1;            // MMA issuing threads (gate and up apart)
+  static constexpr int NISS = PAIRED ? 2 : 1;            // MMA issuing threads (one per matrix)
   // Token-tile stages, and the ring takes all the shared memory the code
   // ring, the epilogue staging and the barriers leave.  On 160-row tiles a
   // stage holds CP chunks of a full tile (every A stage reads a single B
@@ -116,7 +126,7 @@ struct PCfg {
   // dequantisation group start rewriting a slot while the tensor pipe still
   // reads its later blocks.  Pays for the extra waits and commits on the
   // gate/up pass with tiles of 128 rows or more only.
-  static constexpr bool BLK_REL = GATEUP && PT >= 128;
+  static constexpr bool BLK_REL = PAIRED && PT >= 128;
   static constexpr int NREL = BLK_REL ? CPS * NMAT : 1;  // empty barriers per slot
   static_assert(SA >= 2, "the A ring needs a stage per dequantisation group");
   static_assert(SB >= 2 && B_STAGE % 1024 == 0, "token-tile ring");
@@ -267,8 +277,9 @@ struct PUnit {
   bool shared;
 };
 
-template <bool GATEUP, int CPS, int B_STAGE>
+template <int MODE, int CPS, int B_STAGE>
 __device__ __forceinline__ PUnit decode_punit(const TcParams& p, int u) {
+  constexpr bool GATEUP = MODE == MODE_GU;
   PUnit U;
   int4 T;
   if (GATEUP) {
@@ -276,9 +287,10 @@ __device__ __forceinline__ PUnit decode_punit(const TcParams& p, int u) {
     T = p.tiles[code >> 8];
     U.f0 = (code & 255) * 128;
   } else {
-    const int nmt = p.h / 128;
+    constexpr int W = MODE == MODE_DN2 ? 256 : 128;  // output features of one unit
+    const int nmt = p.h / W;
     T = p.tiles[u / nmt];
-    U.f0 = (u % nmt) * 128;
+    U.f0 = (u % nmt) * W;
   }
   U.e = T.x;
   U.start = T.y;
@@ -301,8 +313,9 @@ struct PParams {
   int kmax;                 // max(I, Is): hg row pitch in the padded space
 };
 
-template <bool GATEUP, int PT, int CP>
+template <int MODE, int PT, int CP>
 struct PSmem {
+  static constexpr bool GATEUP = MODE == MODE_GU;
   // down epilogue: per epilogue warp, the destination row (-1: skip) and
   // weight of every column of the current tile
   alignas(16) int col_row[GATEUP ? 1 : 8][PT];
@@ -311,7 +324,7 @@ struct PSmem {
   // gate/up, fp32 for down), the transpose that turns one value per lane
   // into 16 bytes of consecutive features
   alignas(16) float stage[8][GATEUP ? 16 * 16 : 16 * 32];
-  using C = PCfg<GATEUP, PT, CP>;
+  using C = PCfg<MODE, PT, CP>;
   uint64_t code_full[C::SC], code_empty[C::SC];
   uint64_t a_full[C::SA];
   uint64_t a_empty[C::SA][C::NREL];
@@ -322,10 +335,10 @@ struct PSmem {
   int abort;
 };
 
-template <bool GATEUP, int PT, int CP>
+template <int MODE, int PT, int CP>
 constexpr size_t psmem_bytes() {
-  using C = PCfg<GATEUP, PT, CP>;
-  return 1024 + (size_t)C::B_RING + (size_t)C::SC * C::C_STAGE + sizeof(PSmem<GATEUP, PT, CP>);
+  using C = PCfg<MODE, PT, CP>;
+  return 1024 + (size_t)C::B_RING + (size_t)C::SC * C::C_STAGE + sizeof(PSmem<MODE, PT, CP>);
 }
 
 // This warp has issued its last load of an accumulator buffer: hand it back
@@ -336,11 +349,12 @@ __device__ __forceinline__ void release_acc(uint64_t* bar, int lane) {
   if (lane == 0) mbar_arrive(bar);
 }
 
-template <bool GATEUP, int PT, int CP>
+template <int MODE, int PT, int CP>
 __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
   pdl_wait();
   pdl_trigger();
-  using C = PCfg<GATEUP, PT, CP>;
+  using C = PCfg<MODE, PT, CP>;
+  constexpr bool GATEUP = C::GATEUP, PAIRED = C::PAIRED;
   constexpr int CPS = CP;
   constexpr int SB = C::SB, B_STAGE = C::B_STAGE;
   const TcParams& p = P.p;
@@ -348,7 +362,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* b_s = base;
   uint8_t* c_s = b_s + C::B_RING;
-  PSmem<GATEUP, PT, CP>& S = *reinterpret_cast<PSmem<GATEUP, PT, CP>*>(c_s + C::SC * C::C_STAGE);
+  PSmem<MODE, PT, CP>& S = *reinterpret_cast<PSmem<MODE, PT, CP>*>(c_s + C::SC * C::C_STAGE);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = p.h;
   const int egroups = blockDim.x > KTHREADS_1 ? 2 : 1;  // epilogue warpgroups
@@ -388,7 +402,8 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
   tc_fence_after();
   const uint32_t tmem = S.tmem_slot;
   volatile int* abort = &S.abort;
-  const int n_units = GATEUP ? p.hdr->n_units_gu : p.hdr->n_units_dn;
+  const int n_units =
+      GATEUP ? p.hdr->n_units_gu : (MODE == MODE_DN2 ? p.hdr->n_units_dn / 2 : p.hdr->n_units_dn);
 
   if (warp == W_CODE) {
     // ------------------------------------------------------------ packed weight blocks, CPS chunks per copy
@@ -400,12 +415,16 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
 #pragma unroll
       for (int i = 0; i < C::SC; ++i) armed[i] = false, par[i] = 0;
       bool stop = false;
-      // The weight blocks of unit u: nst stages of C_STAGE bytes from the returned address.
+      // The weight blocks of unit u: nst stages of C_STAGE bytes from the
+      // returned address (paired down: blocks of the second output tile
+      // `m2` bytes further on, copied block by block into [chunk][tile]).
+      size_t m2 = 0;
       auto unit_codes = [&](int u, int& nst) -> const uint8_t* {
-        const PUnit U = decode_punit<GATEUP, CP, C::B_STAGE>(p, u);
+        const PUnit U = decode_punit<MODE, CP, C::B_STAGE>(p, u);
         const int Iu = U.shared ? p.Is : p.I;
         const uint8_t* rec = U.shared ? P.s_packed : P.packed + (size_t)U.e * rec_bytes(h, p.I);
         nst = U.nkc / CPS;
+        m2 = (size_t)(Iu / KC) * QB;
         if (GATEUP) return rec + (size_t)(U.f0 / 128) * (h / KC) * 2 * QB;
         return rec + gu_bytes(h, Iu) + (size_t)(U.f0 / 128) * (Iu / KC) * QB;
       };
@@ -420,7 +439,16 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
             break;
           }
           mbar_arrive_expect_tx(&S.code_full[sc], C::C_STAGE);
-          bulk_load(c_s + sc * C::C_STAGE, src + (size_t)st * C::C_STAGE, C::C_STAGE, &S.code_full[sc]);
+          if constexpr (MODE == MODE_DN2) {
+#pragma unroll
+            for (int c = 0; c < CPS; ++c)
+#pragma unroll
+              for (int m = 0; m < 2; ++m)
+                bulk_load(c_s + sc * C::C_STAGE + (c * 2 + m) * QB, src + m * m2 + (size_t)(st * CPS + c) * QB, QB,
+                          &S.code_full[sc]);
+          } else {
+            bulk_load(c_s + sc * C::C_STAGE, src + (size_t)st * C::C_STAGE, C::C_STAGE, &S.code_full[sc]);
+          }
           armed[sc] = true;
           par[sc] = (it / C::SC) & 1;
         }
@@ -440,7 +468,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
       for (int i = 0; i < SB; ++i) armed[i] = false, par[i] = 0;
       bool stop = false;
       for (int u = unit0; u < n_units && !stop; u += ustride) {
-        const PUnit U = decode_punit<GATEUP, CP, C::B_STAGE>(p, u);
+        const PUnit U = decode_punit<MODE, CP, C::B_STAGE>(p, u);
         const uint8_t* src = GATEUP ? reinterpret_cast<const uint8_t*>(P.xg + (size_t)U.pad * h)
                                     : reinterpret_cast<const uint8_t*>(p.hg + (size_t)U.pad * P.kmax);
         for (int kc0 = 0; kc0 < U.nkc; kc0 += U.kps, ++it) {
@@ -471,13 +499,13 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     // so the two streams are independent and each commit barrier counts
     // both; down: W_MMA alone (one accumulator, one fixed order).
     const int m = warp == W_MMA ? 0 : 1;
-    if (lane == 0 && (GATEUP || warp == W_MMA)) {
+    if (lane == 0 && (PAIRED || warp == W_MMA)) {
       uint64_t bstage[SB];
 #pragma unroll
       for (int i = 0; i < SB; ++i) bstage[i] = desc_sw128(smem_u32(b_s + i * B_STAGE));
       uint32_t ast = 0, bit = 0, uit = 0;
       for (int u = unit0; u < n_units && !*abort; u += ustride, ++uit) {
-        const PUnit U = decode_punit<GATEUP, CP, C::B_STAGE>(p, u);
+        const PUnit U = decode_punit<MODE, CP, C::B_STAGE>(p, u);
         const uint32_t idesc = idesc_bf16(128, U.Nm);
         const uint32_t nm8 = (uint32_t)(U.Nm * 128) >> 4;  // descriptor step of one K chunk
         const int ab = uit % C::NACC;
@@ -533,7 +561,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t ast = 0, bbase = 0;  // global A stage; global B stage at the unit's start
     for (int u = unit0; u < n_units && !*abort; u += ustride) {
-      const PUnit U = decode_punit<GATEUP, CP, C::B_STAGE>(p, u);
+      const PUnit U = decode_punit<MODE, CP, C::B_STAGE>(p, u);
       bool ok = true;
       // the token stage of each A stage, counted without a division: a B
       // stage spans spb whole A stages
@@ -633,7 +661,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t uit = 0;
     for (int u = unit0; u < n_units && !*abort; u += ustride, ++uit) {
-      const PUnit U = decode_punit<GATEUP, CP, C::B_STAGE>(p, u);
+      const PUnit U = decode_punit<MODE, CP, C::B_STAGE>(p, u);
       const int ab = uit % C::NACC;
       // down: this warp's copy of the tile's destination rows and weights.
       // Deterministic mode writes routed columns to their own list position
@@ -712,17 +740,22 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         // destination row, so the scatter-add issues 16-byte reductions (a
         // quarter of the requests of one float per lane, each four times
         // wider).  The accumulator is released after its last load.
+        // Paired mode: the steps of both output tiles (accumulator m at
+        // columns m PT, features f0 + 128 m), in one sequence.
         float* dq = (to_list ? p.ybuf : p.acc) + U.f0 + q * 32 + (lane & 7) * 4;
         float* stg = S.stage[ew];
-        const int nb = U.Nm / 16;
-        if (half >= nb) release_acc(&S.acc_empty[ab], lane);
-        for (int c = half; c < nb; c += egroups) {
+        const int nb = U.Nm / 16, nsteps = C::NMAT * nb;
+        if (half >= nsteps) release_acc(&S.acc_empty[ab], lane);
+        for (int cs = half; cs < nsteps; cs += egroups) {
+          const int m = cs >= nb ? 1 : 0, c = cs - m * nb;
           uint32_t y[16];
-          tmem_ld16(acc + c * 16, y);
+          tmem_ld16(acc + m * PT + c * 16, y);
           tmem_ld_wait();
-          if (c + egroups >= nb) release_acc(&S.acc_empty[ab], lane);
-          if (p.deterministic) down_cols16<true>(y, &S.col_row[ew][c * 16], &S.col_w[ew][c * 16], stg, dq, lane, h);
-          else down_cols16<false>(y, &S.col_row[ew][c * 16], &S.col_w[ew][c * 16], stg, dq, lane, h);
+          if (cs + egroups >= nsteps) release_acc(&S.acc_empty[ab], lane);
+          if (p.deterministic)
+            down_cols16<true>(y, &S.col_row[ew][c * 16], &S.col_w[ew][c * 16], stg, dq + m * 128, lane, h);
+          else
+            down_cols16<false>(y, &S.col_row[ew][c * 16], &S.col_w[ew][c * 16], stg, dq + m * 128, lane, h);
         }
       }
     }
@@ -761,15 +794,15 @@ cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, const uint
   return cudaGetLastError();
 }
 
-template <bool GATEUP, int PT, int CP>
+template <int MODE, int PT, int CP>
 cudaError_t launch_packed_gemm(const PParams& P, cudaStream_t stream) {
-  static_assert(psmem_bytes<GATEUP, PT, CP>() <= SMEM_MAX, "shared memory of one CTA");
-  const bool two_epi = PT >= 128 && (GATEUP || max(P.p.I, P.p.Is) <= 1024);
-  cudaError_t err = set_smem_limit_once(packed_gemm_kernel<GATEUP, PT, CP>, (int)psmem_bytes<GATEUP, PT, CP>());
+  static_assert(psmem_bytes<MODE, PT, CP>() <= SMEM_MAX, "shared memory of one CTA");
+  const bool two_epi = PT >= 128 && (MODE != MODE_DN || max(P.p.I, P.p.Is) <= 1024);
+  cudaError_t err = set_smem_limit_once(packed_gemm_kernel<MODE, PT, CP>, (int)psmem_bytes<MODE, PT, CP>());
   if (err != cudaSuccess) return err;
-  MOE_LAUNCH(GATEUP ? "gateup_packed" : "down_packed", stream,
-             (launch_k(packed_gemm_kernel<GATEUP, PT, CP>, sm_count(), two_epi ? KTHREADS : KTHREADS_1,
-                       psmem_bytes<GATEUP, PT, CP>(), stream, P)));
+  MOE_LAUNCH(MODE == MODE_GU ? "gateup_packed" : "down_packed", stream,
+             (launch_k(packed_gemm_kernel<MODE, PT, CP>, sm_count(), two_epi ? KTHREADS : KTHREADS_1,
+                       psmem_bytes<MODE, PT, CP>(), stream, P)));
   return cudaGetLastError();
 }
 
@@ -779,11 +812,19 @@ cudaError_t launch_packed_gemm(const PParams& P, cudaStream_t stream) {
 template <int PT>
 cudaError_t launch_packed_gemms(const PParams& P, cudaStream_t stream) {
   constexpr int GU_CP = PT > 128 ? 1 : CPS_DEFAULT;
-  cudaError_t err = launch_packed_gemm<true, PT, GU_CP>(P, stream);
+  cudaError_t err = launch_packed_gemm<MODE_GU, PT, GU_CP>(P, stream);
   if (err != cudaSuccess) return err;
+  // down on tiles of 128 rows or more and a long inner dimension: two output
+  // tiles per unit (the token image is read once for both), staged like
+  // gate/up.  Its accumulators then take the TMEM of the double buffer, so
+  // each unit's drain is exposed: with inter 768 that cost more than the
+  // halved ingest saved (t4096 skewed: 150 -> 162 us), with 1536 less (t4096
+  // h4096: 517 -> 499 us).
+  if constexpr (PT >= 128)
+    if (P.p.h % 256 == 0 && max(P.p.I, P.p.Is) >= 1024) return launch_packed_gemm<MODE_DN2, PT, GU_CP>(P, stream);
   if constexpr (PT <= 128)
-    if (P.p.I % 256 == 0 && P.p.Is % 256 == 0) return launch_packed_gemm<false, PT, 4>(P, stream);
-  return launch_packed_gemm<false, PT, CPS_DEFAULT>(P, stream);
+    if (P.p.I % 256 == 0 && P.p.Is % 256 == 0) return launch_packed_gemm<MODE_DN, PT, 4>(P, stream);
+  return launch_packed_gemm<MODE_DN, PT, CPS_DEFAULT>(P, stream);
 }
 
 cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, const uint8_t* s_packed,
