@@ -23,7 +23,9 @@ engine, rustdoc source pages):
   matmuls, ``silu_mul``, the down quantised matmul, and scatter-adds the
   result times the routing weight (``scatter_add_rows``).
 * ``prefill/experts.rs``, ``Q { w, s, b, out, inp }``: affine quantisation,
-  ``W[o, i] = q[o, i] * s[o, i // 64] + b[o, i // 64]``.
+  ``W[o, i] = q[o, i] * s[o, i // 64] + b[o, i // 64]``, with codes of
+  ``l.bits`` bits (``pf_experts`` passes the layout's ``bits`` to every
+  quantised matmul; 4 for the base layout, lower for the low-bit stores).
 
 Floating point: everything after the router is fp64 with the exact
 dequantised weights and no intermediate rounding; the output is returned in
@@ -39,6 +41,10 @@ Readings where the pages are silent (the kernels' bodies are not printed):
   renormalising the top k).
 * shared gate (``shared_add_rows`` binds the rows and a dense gate vector):
   a per-row scalar ``sigmoid(x_r . g)``; absent means 1.
+* code packing at ``bits`` bits (not printed): each row K-contiguous, least
+  significant bit first, code k in bits ``[k*bits, k*bits + bits)`` of the
+  row's little-endian bit string; at 4 bits this is two codes per byte with
+  the low nibble at the even K index.
 """
 
 from __future__ import annotations
@@ -89,29 +95,43 @@ def f64_to_bf16(a: np.ndarray) -> np.ndarray:
     return bits.astype(np.uint16)
 
 
-def dequant(codes: np.ndarray, scales: np.ndarray, biases: np.ndarray, rows: int, K: int) -> np.ndarray:
-    """Affine 4-bit dequantisation, exact in float64.
+def unpack_codes(codes: np.ndarray, rows: int, K: int, bits: int = 4) -> np.ndarray:
+    """Integer codes q [rows, K] from a row-major record of ``bits``-bit codes:
+    each row's bytes read as one little-endian bit string, code k in bits
+    [k*bits, k*bits + bits)."""
+    c = np.asarray(codes, np.uint8).reshape(rows, K * bits // 8)
+    if bits == 4:  # the same bit string read a byte at a time: low nibble first
+        q = np.empty((rows, K), np.int64)
+        q[:, 0::2] = c & 0x0F
+        q[:, 1::2] = c >> 4
+        return q
+    if bits == 8:
+        return c.astype(np.int64)
+    bit = np.unpackbits(c, axis=1, bitorder="little").reshape(rows, K, bits).astype(np.int64)
+    return (bit << np.arange(bits, dtype=np.int64)).sum(axis=2)
 
-    ``codes``: uint8 [rows, K/2], low nibble = even K index.
+
+def dequant(codes: np.ndarray, scales: np.ndarray, biases: np.ndarray, rows: int, K: int,
+            bits: int = 4) -> np.ndarray:
+    """Affine dequantisation of ``bits``-bit codes, exact in float64.
+
+    ``codes``: uint8 [rows, K*bits/8] (see unpack_codes).
     ``scales``/``biases``: float16 [rows, K/64].
     Returns W[o, i] = q[o, i] * s[o, i // 64] + b[o, i // 64]   (experts.rs, ``Q``).
     """
-    c = np.asarray(codes, np.uint8).reshape(rows, K // 2)
-    q = np.empty((rows, K), np.float64)
-    q[:, 0::2] = c & 0x0F
-    q[:, 1::2] = c >> 4
+    q = unpack_codes(codes, rows, K, bits).astype(np.float64)
     s = np.asarray(scales, np.float16).reshape(rows, K // GROUP).astype(np.float64)
     b = np.asarray(biases, np.float16).reshape(rows, K // GROUP).astype(np.float64)
     return q * np.repeat(s, GROUP, axis=1) + np.repeat(b, GROUP, axis=1)
 
 
-def expert_matrices(codes, scales, biases, h: int, inter: int):
+def expert_matrices(codes, scales, biases, h: int, inter: int, bits: int = 4):
     """Split one expert record into dequantised gate [I,h], up [I,h], down [h,I]."""
-    nb = inter * h // 2
+    nb = inter * h * bits // 8
     ng = inter * h // GROUP
-    gate = dequant(codes[0:nb], scales[0:ng], biases[0:ng], inter, h)
-    up = dequant(codes[nb:2 * nb], scales[ng:2 * ng], biases[ng:2 * ng], inter, h)
-    down = dequant(codes[2 * nb:3 * nb], scales[2 * ng:3 * ng], biases[2 * ng:3 * ng], h, inter)
+    gate = dequant(codes[0:nb], scales[0:ng], biases[0:ng], inter, h, bits)
+    up = dequant(codes[nb:2 * nb], scales[ng:2 * ng], biases[ng:2 * ng], inter, h, bits)
+    down = dequant(codes[2 * nb:3 * nb], scales[2 * ng:3 * ng], biases[2 * ng:3 * ng], h, inter, bits)
     return gate, up, down
 
 
@@ -235,7 +255,7 @@ def ffn(X: np.ndarray, gate: np.ndarray, up: np.ndarray, down: np.ndarray) -> np
 
 def experts_fwd(x_bits, offsets, rows, weights, codes, scales, biases,
                 shared_codes, shared_scales, shared_biases, h: int, inter: int,
-                shared_inter: int, shared_gate_bits=None) -> np.ndarray:
+                shared_inter: int, shared_gate_bits=None, bits: int = 4) -> np.ndarray:
     """Block output [t, h] in float64.
 
     Zeroed output; the shared expert over all rows (times the optional
@@ -246,7 +266,7 @@ def experts_fwd(x_bits, offsets, rows, weights, codes, scales, biases,
     t = X.shape[0]
     E = len(offsets) - 1
     out = np.zeros((t, h), np.float64)
-    sg, su, sd = expert_matrices(shared_codes, shared_scales, shared_biases, h, shared_inter)
+    sg, su, sd = expert_matrices(shared_codes, shared_scales, shared_biases, h, shared_inter, bits)
     ys = ffn(X, sg, su, sd)
     if shared_gate_bits is not None:
         gvec = bf16_to_f64(shared_gate_bits)
@@ -257,7 +277,7 @@ def experts_fwd(x_bits, offsets, rows, weights, codes, scales, biases,
         if a == b:
             continue
         r = np.asarray(rows[a:b], np.int64)
-        G, U, D = expert_matrices(codes[e], scales[e], biases[e], h, inter)
+        G, U, D = expert_matrices(codes[e], scales[e], biases[e], h, inter, bits)
         y = ffn(X[r], G, U, D)
         out[r] += np.asarray(weights[a:b], np.float64)[:, None] * y
     return out
@@ -275,6 +295,7 @@ def moe_forward(inp: dict, k: int, h: int, inter: int, shared_inter: int):
     offsets, rows, weights, slot_of = build_csr(idx, w, E)
     out = experts_fwd(inp["x"], offsets, rows, weights, inp["codes"], inp["scales"],
                       inp["biases"], inp["shared_codes"], inp["shared_scales"],
-                      inp["shared_biases"], h, inter, shared_inter, inp.get("shared_gate"))
+                      inp["shared_biases"], h, inter, shared_inter, inp.get("shared_gate"),
+                      inp.get("bits", 4))
     return dict(logits=logits, idx=idx, w=w, offsets=offsets, rows=rows, weights=weights,
                 slot_of=slot_of, out=out, out_bf16=f64_to_bf16(out))

@@ -12,10 +12,13 @@ Layouts (shared by every consumer):
   ``e`` of row ``r`` is the dot product of ``x[r, :]`` and ``wr[e, :]``).
 * ``rbias``   float32 ``[E]`` or ``None``: per-expert logit bias (only the
   skewed workload has one).
-* ``codes``   uint8 ``[E, 3*inter*h/2]``: one record per expert holding, in
-  order, gate ``[inter, h]``, up ``[inter, h]`` and down ``[h, inter]``
-  4-bit codes, each K-contiguous with two codes per byte, the low nibble at
-  the even K index.
+* ``codes``   uint8 ``[E, 3*inter*h*bits/8]``: one record per expert holding,
+  in order, gate ``[inter, h]``, up ``[inter, h]`` and down ``[h, inter]``
+  codes of ``bits`` bits (4 unless the workload says otherwise), each row
+  K-contiguous and packed least significant bit first: code k of a row
+  occupies bits ``[k*bits, k*bits + bits)`` of the row's bytes read as one
+  little-endian bit string (at 4 bits: two codes per byte, the low nibble at
+  the even K index).
 * ``scales``/``biases`` float16 ``[E, 3*inter*h/64]``: per output row and
   per 64-wide K group, same matrix order and row-major ``[rows, K/64]``.
 * the shared expert uses the same record layout with ``shared_inter``.
@@ -47,6 +50,7 @@ class Workload:
     seed: int
     skew: bool = False
     shared_gate: bool = False
+    bits: int = 4  # code width of the expert records (2, 3, 4 or 8)
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -79,9 +83,9 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
-def record_bytes(h: int, inter: int) -> int:
-    """Bytes of 4-bit codes in one expert record (gate, up, down)."""
-    return 3 * inter * h // 2
+def record_bytes(h: int, inter: int, bits: int = 4) -> int:
+    """Bytes of codes in one expert record (gate, up, down)."""
+    return 3 * inter * h * bits // 8
 
 
 def record_groups(h: int, inter: int) -> int:
@@ -89,11 +93,14 @@ def record_groups(h: int, inter: int) -> int:
     return 3 * inter * h // GROUP
 
 
-def _quant_record(rng_codes, rng_scales, n: int, h: int, inter: int):
-    codes = rng_codes.integers(0, 256, size=(n, record_bytes(h, inter)), dtype=np.uint8)
-    scales = rng_scales.uniform(0.005, 0.02, size=(n, record_groups(h, inter))).astype(np.float16)
-    # bias = -8 * scale: exact in fp16 (a power-of-two multiple).
-    biases = (scales * np.float16(-8.0)).astype(np.float16)
+def _quant_record(rng_codes, rng_scales, n: int, h: int, inter: int, bits: int = 4):
+    codes = rng_codes.integers(0, 256, size=(n, record_bytes(h, inter, bits)), dtype=np.uint8)
+    # scales 2^(4 - bits) times those of the 4-bit records, so the weights
+    # span about the same range at every width
+    scales = (rng_scales.uniform(0.005, 0.02, size=(n, record_groups(h, inter))) * 2.0 ** (4 - bits)).astype(
+        np.float16)
+    # bias = -2^(bits-1) * scale: exact in fp16 (a power-of-two multiple).
+    biases = (scales * np.float16(-(2.0 ** (bits - 1)))).astype(np.float16)
     return codes, scales, biases
 
 
@@ -115,9 +122,9 @@ def make_inputs(w: Workload, t: int | None = None) -> dict:
     g = lambda s: np.random.default_rng([w.seed, s])  # noqa: E731
     x = f32_to_bf16_bits(g(_S_X).standard_normal((t, w.h)).astype(np.float32))
     wr = f32_to_bf16_bits((g(_S_WR).standard_normal((w.E, w.h)) * 0.02).astype(np.float32))
-    codes, scales, biases = _quant_record(g(_S_CODES), g(_S_SCALES), w.E, w.h, w.inter)
+    codes, scales, biases = _quant_record(g(_S_CODES), g(_S_SCALES), w.E, w.h, w.inter, w.bits)
     s_codes, s_scales, s_biases = _quant_record(
-        g(_S_SH_CODES), g(_S_SH_SCALES), 1, w.h, w.shared_inter
+        g(_S_SH_CODES), g(_S_SH_SCALES), 1, w.h, w.shared_inter, w.bits
     )
     out = dict(
         x=x,
@@ -130,6 +137,7 @@ def make_inputs(w: Workload, t: int | None = None) -> dict:
         shared_scales=s_scales[0],
         shared_biases=s_biases[0],
         shared_gate=None,
+        bits=w.bits,
     )
     if w.shared_gate:
         out["shared_gate"] = f32_to_bf16_bits(

@@ -341,3 +341,69 @@ def test_skewed_recipe_concentrates_rows():
     top8 = np.sort(counts)[::-1][:8].sum()
     assert top8 >= 0.6 * w.t * w.k
     assert (counts <= 3).sum() >= w.E // 2
+
+
+# ---------------------------------------------------------------------------
+# Low-bit layouts (prefill/experts.rs, pf_experts: the quantised matmuls take
+# the layout's bits): code k of a row in bits [k*bits, k*bits + bits) of the
+# row's little-endian bit string.
+# ---------------------------------------------------------------------------
+
+def _pack_bit_by_bit(q: np.ndarray, bits: int) -> np.ndarray:
+    """Pack integer codes [rows, K] one bit at a time into bytes, least
+    significant bit first (written without numpy's bit routines)."""
+    rows, K = q.shape
+    out = np.zeros((rows, K * bits // 8), np.uint8)
+    for r in range(rows):
+        for k in range(K):
+            for j in range(bits):
+                pos = k * bits + j
+                if (int(q[r, k]) >> j) & 1:
+                    out[r, pos // 8] |= np.uint8(1 << (pos % 8))
+    return out
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
+def test_unpack_codes_inverts_a_bit_by_bit_packer(bits):
+    rng = np.random.default_rng(bits)
+    q = rng.integers(0, 1 << bits, size=(3, 128))
+    np.testing.assert_array_equal(O.unpack_codes(_pack_bit_by_bit(q, bits), 3, 128, bits), q)
+
+
+def test_low_bit_worked_examples():
+    # 2 bits: 0xE4 = 0b11100100 holds, from the least significant bit up, 0, 1, 2, 3
+    np.testing.assert_array_equal(O.unpack_codes(np.full(16, 0xE4, np.uint8), 1, 64, 2)[0],
+                                  np.tile([0, 1, 2, 3], 16))
+    # 3 bits: the codes 0..7 occupy bits 0-23; the set bits are 3, 7 | 9, 10,
+    # 14, 15 | 17, 19, 20, 21, 22, 23, i.e. the bytes 0x88, 0xC6, 0xFA
+    np.testing.assert_array_equal(O.unpack_codes(np.tile(np.array([0x88, 0xC6, 0xFA], np.uint8), 8), 1, 64, 3)[0],
+                                  np.tile(np.arange(8), 8))
+    # 4 bits: the same string read a byte at a time, low nibble first
+    np.testing.assert_array_equal(O.unpack_codes(np.full(32, 0x5A, np.uint8), 1, 64, 4)[0], np.tile([10, 5], 32))
+
+
+def test_eight_bit_dequant_closed_form():
+    rng = np.random.default_rng(8)
+    codes = rng.integers(0, 256, size=(2, 128)).astype(np.uint8)
+    s = rng.uniform(0.001, 0.002, size=(2, 2)).astype(np.float16)
+    b = (s * np.float16(-128)).astype(np.float16)
+    w = O.dequant(codes, s, b, 2, 128, 8)
+    for r in range(2):
+        for i in range(128):
+            assert w[r, i] == float(codes[r, i]) * float(s[r, i // 64]) + float(b[r, i // 64])
+
+
+@pytest.mark.parametrize("bits", [2, 3, 8])
+def test_low_bit_record_has_the_width_of_its_codes(bits):
+    """A record of a low-bit workload holds 3 * inter * h * bits / 8 bytes of
+    codes and dequantises to weights centred like the 4-bit ones."""
+    w = synth.Workload("lb", 4, 256, 128, 4, 2, 128, 3, bits=bits)
+    inp = synth.make_inputs(w)
+    assert inp["codes"].shape == (4, 3 * 128 * 256 * bits // 8) and inp["bits"] == bits
+    G, U, D = O.expert_matrices(inp["codes"][0], inp["scales"][0], inp["biases"][0], 256, 128, bits)
+    assert G.shape == (128, 256) and U.shape == (128, 256) and D.shape == (256, 128)
+    # codes uniform on [0, 2^bits): the mean weight is half a step below
+    # zero, within four standard errors of a mean over the G.size weights
+    s = inp["scales"][0].astype(np.float64)
+    tol = 4 * (2 ** bits / math.sqrt(12)) / math.sqrt(G.size)
+    assert abs(G.mean() / s.mean() + 0.5) < tol
