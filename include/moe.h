@@ -62,6 +62,7 @@ typedef struct {
   int32_t E;            /* number of routed experts */
   int32_t k;            /* experts per row */
   int32_t shared_inter; /* shared expert intermediate size; 0 = none */
+  int32_t bits;         /* code width of the expert records: 2, 4 or 8 (0 means 4) */
 } moe_dims;
 
 /* The expert-grouped list produced by moe_build_csr (all device, caller-owned). */
@@ -74,8 +75,12 @@ typedef struct {
 
 /* Quantised expert weights.  One record per expert, each holding three
  * matrices in this order: gate [inter][h], up [inter][h], down [h][inter].
- * codes:  uint8 [E][3*inter*h/2], each matrix row-major and K-contiguous,
- *         two 4-bit codes per byte, the low nibble at the even K index.
+ * codes:  uint8 [E][3*inter*h*bits/8], each matrix row-major and
+ *         K-contiguous; a row's bytes form one little-endian bit string and
+ *         code k occupies its bits [k*bits, k*bits + bits) (4 bits: two codes
+ *         per byte, the low nibble at the even K index).  bits = dims->bits
+ *         (0 means 4); records of 2 or 8 bits go through moe_pack_experts and
+ *         the tensor-core kernels (MOE_PACKED_WEIGHTS) only.
  * scales, biases: fp16 [E][3*inter*h/64], per output row and 64-wide K
  *         group, row-major [rows][K/64] per matrix, same matrix order. */
 typedef struct {

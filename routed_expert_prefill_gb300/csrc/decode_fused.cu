@@ -821,6 +821,7 @@ size_t cdiv(size_t a, size_t b) { return (a + b - 1) / b; }
 
 bool decode_fused_ok(const moe_dims& d, uint32_t flags) {
   if (!(d.t <= D_MAX_T && d.E <= D_MAX_E && d.h <= D_MAX_H && (flags & MOE_PACKED_WEIGHTS) &&
+        (d.bits == 0 || d.bits == 4) &&
         (flags & MOE_FUSED_DECODE) &&
         !(flags & (MOE_DETERMINISTIC | MOE_FORCE_SMALL_T | MOE_FORCE_LARGE_T | MOE_SIMPLE_KERNELS))))
     return false;

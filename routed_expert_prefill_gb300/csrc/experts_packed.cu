@@ -61,7 +61,10 @@ constexpr int PTILE = 128;
 constexpr int PTILE_SMALL = 64;
 constexpr int PTILE_LARGE = 160;  // experts with ~100 rows or more: one tile for up to 160 rows
 constexpr int KC = 64;      // K per chunk = one quantisation group
-constexpr int QB = 4096 + 256 + 256;  // one packed 128 x 64 block
+// One packed 128 x 64 block at BITS bits per code: 128 rows of 8 * BITS
+// code bytes, then 128 bf16 scales and 128 bf16 biases.
+__host__ __device__ constexpr int qb_bytes(int bits) { return 1024 * bits + 512; }
+constexpr int QB = qb_bytes(4);  // the 4-bit block
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
 constexpr int W_CODE = 0, W_MMA = 1, W_DQ0 = 2, W_B = 10, W_EPI0 = 11, W_MMA2 = 15, W_EPI1 = 16;
@@ -90,13 +93,15 @@ constexpr int CPS_DEFAULT = 2;        // K chunks per code stage and per A stage
 // weight block.
 constexpr int MODE_DN = 0, MODE_GU = 1, MODE_DN2 = 2;
 
-template <int MODE, int PT, int CP>
+template <int MODE, int PT, int CP, int BITS>
 struct PCfg {
+  static constexpr int QB = qb_bytes(BITS);               // bytes of one packed block
+  static constexpr int ROWB = 8 * BITS;                   // code bytes of one row of a block
   static constexpr bool GATEUP = MODE == MODE_GU;
   static constexpr bool PAIRED = MODE != MODE_DN;
   static constexpr int CPS = CP;
   static constexpr int NMAT = PAIRED ? 2 : 1;
-  static constexpr int C_STAGE = CPS * NMAT * QB;        // packed blocks of one stage
+  static constexpr int C_STAGE = CPS * NMAT * QB;        // packed blocks of one stage (QB at BITS)
   // Code stages: four (measured: the code producer stays several stages
   // ahead of the dequantisation with four; more gave nothing), so that the
   // token-tile ring gets the rest of shared memory.
@@ -132,8 +137,12 @@ struct PCfg {
   static_assert(SB >= 2 && B_STAGE % 1024 == 0, "token-tile ring");
 };
 
-__host__ __device__ inline size_t gu_bytes(int h, int I) { return (size_t)(I / 128) * (h / KC) * 2 * QB; }
-__host__ __device__ inline size_t rec_bytes(int h, int I) { return gu_bytes(h, I) + (size_t)(h / 128) * (I / KC) * QB; }
+__host__ __device__ inline size_t gu_bytes(int h, int I, int bits = 4) {
+  return (size_t)(I / 128) * (h / KC) * 2 * qb_bytes(bits);
+}
+__host__ __device__ inline size_t rec_bytes(int h, int I, int bits = 4) {
+  return gu_bytes(h, I, bits) + (size_t)(h / 128) * (I / KC) * qb_bytes(bits);
+}
 
 __device__ __forceinline__ uint32_t pack_word(uint32_t w) {
   return (w & 0xFu) | (((w >> 4) & 0xFu) << 16) | (((w >> 8) & 0xFu) << 4) | (((w >> 12) & 0xFu) << 20) |
@@ -141,13 +150,29 @@ __device__ __forceinline__ uint32_t pack_word(uint32_t w) {
          (((w >> 28) & 0xFu) << 28);
 }
 
+// 2 bits: a word of 16 codes (code m at bits 2m) becomes pairs (K2i,
+// K2i+1) at (w >> 2i) & 0x00030003.
+__device__ __forceinline__ uint32_t pack_word2(uint32_t w) {
+  uint32_t r = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    r |= (((w >> (4 * i)) & 3u) << (2 * i)) | (((w >> (4 * i + 2)) & 3u) << (16 + 2 * i));
+  return r;
+}
+// 8 bits: a word of 4 codes (code m at bits 8m) becomes pairs (K2i, K2i+1)
+// at (w >> 8i) & 0x00FF00FF.
+__device__ __forceinline__ uint32_t pack_word8(uint32_t w) { return __byte_perm(w, 0, 0x3120); }
+
 // ----------------------------------------------------------------------------
-// Packing: one 128-thread block per packed block (thread = weight row)
+// Packing: one 128-thread block per packed block (thread = weight row).
+// Source records hold BITS-bit codes, each row least significant bit first.
 // ----------------------------------------------------------------------------
+template <int BITS>
 __global__ void __launch_bounds__(128)
 pack_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
             const uint16_t* __restrict__ biases, int h, int I, size_t src_rec_bytes, size_t src_rec_groups,
             uint8_t* __restrict__ dst) {
+  constexpr int QBB = qb_bytes(BITS), ROWB = 8 * BITS;  // block bytes; code bytes of a row's 64 K
   pdl_wait();
   pdl_trigger();
   const int rec = blockIdx.y;
@@ -163,7 +188,7 @@ pack_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scal
     kc = pair % nkc_gu;
     K = h;
     rows = I;
-    dst_off = (size_t)pair * 2 * QB + (size_t)mat * QB;
+    dst_off = (size_t)pair * 2 * QBB + (size_t)mat * QBB;
   } else {
     blk -= 2 * nblk_gu;
     mat = 2;
@@ -171,23 +196,25 @@ pack_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scal
     kc = blk % nkc_d;
     K = I;
     rows = h;
-    dst_off = gu_bytes(h, I) + (size_t)blk * QB;
+    dst_off = gu_bytes(h, I, BITS) + (size_t)blk * QBB;
   }
   const int o = threadIdx.x;
-  const size_t mat_bytes = (size_t)I * h / 2, mat_groups = (size_t)I * h / KC;
-  const uint8_t* src = codes + rec * src_rec_bytes + mat * mat_bytes + (size_t)(rt * 128 + o) * (K / 2) + kc * 32;
+  const size_t mat_bytes = (size_t)I * h * BITS / 8, mat_groups = (size_t)I * h / KC;
+  const uint8_t* src =
+      codes + rec * src_rec_bytes + mat * mat_bytes + (size_t)(rt * 128 + o) * (K * BITS / 8) + kc * ROWB;
   const size_t g = rec * src_rec_groups + mat * mat_groups + (size_t)(rt * 128 + o) * (K / KC) + kc;
-  uint8_t* d = dst + rec * rec_bytes(h, I) + dst_off;
-  const uint4 c0 = reinterpret_cast<const uint4*>(src)[0];
-  const uint4 c1 = reinterpret_cast<const uint4*>(src)[1];
-  uint4 p0, p1;
-  p0.x = pack_word(c0.x), p0.y = pack_word(c0.y), p0.z = pack_word(c0.z), p0.w = pack_word(c0.w);
-  p1.x = pack_word(c1.x), p1.y = pack_word(c1.y), p1.z = pack_word(c1.z), p1.w = pack_word(c1.w);
-  reinterpret_cast<uint4*>(d + o * 32)[0] = p0;
-  reinterpret_cast<uint4*>(d + o * 32)[1] = p1;
+  uint8_t* d = dst + rec * rec_bytes(h, I, BITS) + dst_off;
+#pragma unroll
+  for (int v = 0; v < ROWB / 16; ++v) {
+    uint4 c = reinterpret_cast<const uint4*>(src)[v];
+    if (BITS == 2) c.x = pack_word2(c.x), c.y = pack_word2(c.y), c.z = pack_word2(c.z), c.w = pack_word2(c.w);
+    if (BITS == 4) c.x = pack_word(c.x), c.y = pack_word(c.y), c.z = pack_word(c.z), c.w = pack_word(c.w);
+    if (BITS == 8) c.x = pack_word8(c.x), c.y = pack_word8(c.y), c.z = pack_word8(c.z), c.w = pack_word8(c.w);
+    reinterpret_cast<uint4*>(d + o * ROWB)[v] = c;
+  }
   __nv_bfloat16 sb = h2bf(scales[g]), bb = h2bf(biases[g]);
-  reinterpret_cast<__nv_bfloat16*>(d + 4096)[o] = sb;
-  reinterpret_cast<__nv_bfloat16*>(d + 4096 + 256)[o] = bb;
+  reinterpret_cast<__nv_bfloat16*>(d + 128 * ROWB)[o] = sb;
+  reinterpret_cast<__nv_bfloat16*>(d + 128 * ROWB + 256)[o] = bb;
   (void)rows;
 }
 
@@ -272,6 +299,45 @@ __device__ __forceinline__ void down_cols16(const uint32_t (&y)[16], const int* 
 }
 
 
+// Dequantise one row of a packed block (64 K) into 32 bf16 pairs in K order,
+// w = fma(q, s, b) in bf16.  The in-word layouts are those of pack_kernel.
+template <int BITS>
+__device__ __forceinline__ void dequant_bits(const uint32_t* w, __nv_bfloat162 s2, __nv_bfloat162 b2, uint32_t* out) {
+  if constexpr (BITS == 4) {
+    dequant_packed<8>(w, s2, b2, out);
+  } else if constexpr (BITS == 2) {
+    // word j: pairs (K 16j + 2i, K 16j + 2i + 1) at (w >> 2i) & 0x00030003
+    const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.f, 128.f);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t v = ((w[j] >> (2 * i)) & 0x00030003u) | 0x43004300u;
+        const __nv_bfloat162 q = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&v), k128);
+        const __nv_bfloat162 r = __hfma2(q, s2, b2);
+        out[8 * j + i] = *reinterpret_cast<const uint32_t*>(&r);
+      }
+  } else {
+    static_assert(BITS == 8, "2, 4 or 8 bits");
+    // word j: pairs (K 4j + 2i, K 4j + 2i + 1) at (w >> 8i) & 0x00FF00FF.  The
+    // low seven bits go through the bf16 magic number (128 + q, exact), bit
+    // 7 adds 128 (0x4300 per half where set): q exact up to 255.
+    const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.f, 128.f);
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint32_t t = w[j] >> (8 * i);
+        uint32_t v = (t & 0x007F007Fu) | 0x43004300u;
+        uint32_t hv = ((t >> 7) & 0x00010001u) * 0x4300u;
+        const __nv_bfloat162 q = __hadd2(__hsub2(*reinterpret_cast<__nv_bfloat162*>(&v), k128),
+                                         *reinterpret_cast<__nv_bfloat162*>(&hv));
+        const __nv_bfloat162 r = __hfma2(q, s2, b2);
+        out[2 * j + i] = *reinterpret_cast<const uint32_t*>(&r);
+      }
+  }
+}
+
 struct PUnit {
   int e, start, n, Nm, f0, nkc, kps, pad;
   bool shared;
@@ -313,7 +379,7 @@ struct PParams {
   int kmax;                 // max(I, Is): hg row pitch in the padded space
 };
 
-template <int MODE, int PT, int CP>
+template <int MODE, int PT, int CP, int BITS>
 struct PSmem {
   static constexpr bool GATEUP = MODE == MODE_GU;
   // down epilogue: per epilogue warp, the destination row (-1: skip) and
@@ -324,7 +390,7 @@ struct PSmem {
   // gate/up, fp32 for down), the transpose that turns one value per lane
   // into 16 bytes of consecutive features
   alignas(16) float stage[8][GATEUP ? 16 * 16 : 16 * 32];
-  using C = PCfg<MODE, PT, CP>;
+  using C = PCfg<MODE, PT, CP, BITS>;
   uint64_t code_full[C::SC], code_empty[C::SC];
   uint64_t a_full[C::SA];
   uint64_t a_empty[C::SA][C::NREL];
@@ -335,10 +401,10 @@ struct PSmem {
   int abort;
 };
 
-template <int MODE, int PT, int CP>
+template <int MODE, int PT, int CP, int BITS>
 constexpr size_t psmem_bytes() {
-  using C = PCfg<MODE, PT, CP>;
-  return 1024 + (size_t)C::B_RING + (size_t)C::SC * C::C_STAGE + sizeof(PSmem<MODE, PT, CP>);
+  using C = PCfg<MODE, PT, CP, BITS>;
+  return 1024 + (size_t)C::B_RING + (size_t)C::SC * C::C_STAGE + sizeof(PSmem<MODE, PT, CP, BITS>);
 }
 
 // This warp has issued its last load of an accumulator buffer: hand it back
@@ -349,11 +415,12 @@ __device__ __forceinline__ void release_acc(uint64_t* bar, int lane) {
   if (lane == 0) mbar_arrive(bar);
 }
 
-template <int MODE, int PT, int CP>
+template <int MODE, int PT, int CP, int BITS>
 __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
   pdl_wait();
   pdl_trigger();
-  using C = PCfg<MODE, PT, CP>;
+  using C = PCfg<MODE, PT, CP, BITS>;
+  constexpr int QB = C::QB;
   constexpr bool GATEUP = C::GATEUP, PAIRED = C::PAIRED;
   constexpr int CPS = CP;
   constexpr int SB = C::SB, B_STAGE = C::B_STAGE;
@@ -362,7 +429,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* b_s = base;
   uint8_t* c_s = b_s + C::B_RING;
-  PSmem<MODE, PT, CP>& S = *reinterpret_cast<PSmem<MODE, PT, CP>*>(c_s + C::SC * C::C_STAGE);
+  PSmem<MODE, PT, CP, BITS>& S = *reinterpret_cast<PSmem<MODE, PT, CP, BITS>*>(c_s + C::SC * C::C_STAGE);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = p.h;
   const int egroups = blockDim.x > KTHREADS_1 ? 2 : 1;  // epilogue warpgroups
@@ -422,11 +489,11 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
       auto unit_codes = [&](int u, int& nst) -> const uint8_t* {
         const PUnit U = decode_punit<MODE, CP, C::B_STAGE>(p, u);
         const int Iu = U.shared ? p.Is : p.I;
-        const uint8_t* rec = U.shared ? P.s_packed : P.packed + (size_t)U.e * rec_bytes(h, p.I);
+        const uint8_t* rec = U.shared ? P.s_packed : P.packed + (size_t)U.e * rec_bytes(h, p.I, BITS);
         nst = U.nkc / CPS;
         m2 = (size_t)(Iu / KC) * QB;
         if (GATEUP) return rec + (size_t)(U.f0 / 128) * (h / KC) * 2 * QB;
-        return rec + gu_bytes(h, Iu) + (size_t)(U.f0 / 128) * (Iu / KC) * QB;
+        return rec + gu_bytes(h, Iu, BITS) + (size_t)(U.f0 / 128) * (Iu / KC) * QB;
       };
       for (int u = unit0; u < n_units && !stop; u += ustride) {
         int nst;
@@ -589,20 +656,24 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         // cm is dequantised and stored (the tensor-memory store is a compiler
         // barrier), so their shared-memory latency overlaps the arithmetic.
         const uint8_t* stage_c = c_s + sc * C::C_STAGE;
-        uint4 c0 = reinterpret_cast<const uint4*>(stage_c + o * 32)[0];
-        uint4 c1 = reinterpret_cast<const uint4*>(stage_c + o * 32)[1];
-        __nv_bfloat16 sv = reinterpret_cast<const __nv_bfloat16*>(stage_c + 4096)[o];
-        __nv_bfloat16 bv = reinterpret_cast<const __nv_bfloat16*>(stage_c + 4096 + 256)[o];
+        constexpr int NV = C::ROWB / 16;  // 16-byte code words of a row
+        uint4 cw[NV];
+#pragma unroll
+        for (int v = 0; v < NV; ++v) cw[v] = reinterpret_cast<const uint4*>(stage_c + o * C::ROWB)[v];
+        __nv_bfloat16 sv = reinterpret_cast<const __nv_bfloat16*>(stage_c + 128 * C::ROWB)[o];
+        __nv_bfloat16 bv = reinterpret_cast<const __nv_bfloat16*>(stage_c + 128 * C::ROWB + 256)[o];
 #pragma unroll
         for (int cm = 0; cm < CPS * C::NMAT; ++cm) {
-          uint4 n0 = c0, n1 = c1;
+          uint4 nw[NV];
+#pragma unroll
+          for (int v = 0; v < NV; ++v) nw[v] = cw[v];
           __nv_bfloat16 ns = sv, nbv = bv;
           if (cm + 1 < CPS * C::NMAT) {
             const uint8_t* nb = stage_c + (cm + 1) * QB;
-            n0 = reinterpret_cast<const uint4*>(nb + o * 32)[0];
-            n1 = reinterpret_cast<const uint4*>(nb + o * 32)[1];
-            ns = reinterpret_cast<const __nv_bfloat16*>(nb + 4096)[o];
-            nbv = reinterpret_cast<const __nv_bfloat16*>(nb + 4096 + 256)[o];
+#pragma unroll
+            for (int v = 0; v < NV; ++v) nw[v] = reinterpret_cast<const uint4*>(nb + o * C::ROWB)[v];
+            ns = reinterpret_cast<const __nv_bfloat16*>(nb + 128 * C::ROWB)[o];
+            nbv = reinterpret_cast<const __nv_bfloat16*>(nb + 128 * C::ROWB + 256)[o];
           }
           if constexpr (C::BLK_REL) {
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.a_empty[sa][cm], a_par, abort, WAIT_NS))) {
@@ -612,11 +683,13 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
             }
             tc_fence_after();
           }
-          const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
           uint32_t r[32];
-          dequant_packed<8>(wd, __halves2bfloat162(sv, sv), __halves2bfloat162(bv, bv), r);
+          dequant_bits<BITS>(reinterpret_cast<const uint32_t*>(cw), __halves2bfloat162(sv, sv),
+                             __halves2bfloat162(bv, bv), r);
           tmem_st<32>(lane_base + C::A_COL + sa * C::A_STAGE + cm * 32, r);
-          c0 = n0, c1 = n1, sv = ns, bv = nbv;
+#pragma unroll
+          for (int v = 0; v < NV; ++v) cw[v] = nw[v];
+          sv = ns, bv = nbv;
         }
         if (!ok) {
           tmem_st_wait();
@@ -772,7 +845,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
 
 }  // namespace
 
-size_t packed_record_bytes(int h, int I) { return rec_bytes(h, I); }
+size_t packed_record_bytes(int h, int I, int bits) { return rec_bytes(h, I, bits); }
 
 // Tile-list capacity, sized for the smaller tiles.
 size_t packed_max_tiles(const moe_dims& d) {
@@ -785,34 +858,42 @@ size_t packed_pad_rows(const moe_dims& d) {
 }
 
 cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, const uint16_t* biases, int h, int I,
-                        int nrec, uint8_t* dst, cudaStream_t stream) {
+                        int nrec, int bits, uint8_t* dst, cudaStream_t stream) {
   const int nblk = 2 * (I / 128) * (h / KC) + (h / 128) * (I / KC);
   dim3 grid(nblk, nrec);
-  MOE_LAUNCH("pack", stream,
-             pack_kernel<<<grid, 128, 0, stream>>>(codes, scales, biases, h, I, (size_t)3 * I * h / 2,
-                                                   (size_t)3 * I * h / KC, dst));
+  const size_t src_bytes = (size_t)3 * I * h * bits / 8, src_groups = (size_t)3 * I * h / KC;
+  if (bits == 2)
+    MOE_LAUNCH("pack", stream,
+               pack_kernel<2><<<grid, 128, 0, stream>>>(codes, scales, biases, h, I, src_bytes, src_groups, dst));
+  else if (bits == 8)
+    MOE_LAUNCH("pack", stream,
+               pack_kernel<8><<<grid, 128, 0, stream>>>(codes, scales, biases, h, I, src_bytes, src_groups, dst));
+  else
+    MOE_LAUNCH("pack", stream,
+               pack_kernel<4><<<grid, 128, 0, stream>>>(codes, scales, biases, h, I, src_bytes, src_groups, dst));
   return cudaGetLastError();
 }
 
-template <int MODE, int PT, int CP>
+template <int MODE, int PT, int CP, int BITS>
 cudaError_t launch_packed_gemm(const PParams& P, cudaStream_t stream) {
-  static_assert(psmem_bytes<MODE, PT, CP>() <= SMEM_MAX, "shared memory of one CTA");
+  static_assert(psmem_bytes<MODE, PT, CP, BITS>() <= SMEM_MAX, "shared memory of one CTA");
   const bool two_epi = PT >= 128 && (MODE != MODE_DN || max(P.p.I, P.p.Is) <= 1024);
-  cudaError_t err = set_smem_limit_once(packed_gemm_kernel<MODE, PT, CP>, (int)psmem_bytes<MODE, PT, CP>());
+  cudaError_t err =
+      set_smem_limit_once(packed_gemm_kernel<MODE, PT, CP, BITS>, (int)psmem_bytes<MODE, PT, CP, BITS>());
   if (err != cudaSuccess) return err;
   MOE_LAUNCH(MODE == MODE_GU ? "gateup_packed" : "down_packed", stream,
-             (launch_k(packed_gemm_kernel<MODE, PT, CP>, sm_count(), two_epi ? KTHREADS : KTHREADS_1,
-                       psmem_bytes<MODE, PT, CP>(), stream, P)));
+             (launch_k(packed_gemm_kernel<MODE, PT, CP, BITS>, sm_count(), two_epi ? KTHREADS : KTHREADS_1,
+                       psmem_bytes<MODE, PT, CP, BITS>(), stream, P)));
   return cudaGetLastError();
 }
 
 // K chunks per stage: gate/up two (one on 160-row tiles, whose 320
 // accumulator columns leave 192 for the A ring); down four when every inter
 // is a multiple of 256 on tiles of up to 128 rows, else two.
-template <int PT>
+template <int PT, int BITS>
 cudaError_t launch_packed_gemms(const PParams& P, cudaStream_t stream) {
   constexpr int GU_CP = PT > 128 ? 1 : CPS_DEFAULT;
-  cudaError_t err = launch_packed_gemm<MODE_GU, PT, GU_CP>(P, stream);
+  cudaError_t err = launch_packed_gemm<MODE_GU, PT, GU_CP, BITS>(P, stream);
   if (err != cudaSuccess) return err;
   // down on tiles of 128 rows or more and a long inner dimension: two output
   // tiles per unit (the token image is read once for both), staged like
@@ -821,10 +902,18 @@ cudaError_t launch_packed_gemms(const PParams& P, cudaStream_t stream) {
   // halved ingest saved (t4096 skewed: 150 -> 162 us), with 1536 less (t4096
   // h4096: 517 -> 499 us).
   if constexpr (PT >= 128)
-    if (P.p.h % 256 == 0 && max(P.p.I, P.p.Is) >= 1024) return launch_packed_gemm<MODE_DN2, PT, GU_CP>(P, stream);
-  if constexpr (PT <= 128)
-    if (P.p.I % 256 == 0 && P.p.Is % 256 == 0) return launch_packed_gemm<MODE_DN, PT, 4>(P, stream);
-  return launch_packed_gemm<MODE_DN, PT, CPS_DEFAULT>(P, stream);
+    if (P.p.h % 256 == 0 && max(P.p.I, P.p.Is) >= 1024)
+      return launch_packed_gemm<MODE_DN2, PT, GU_CP, BITS>(P, stream);
+  if constexpr (PT <= 128 && BITS <= 4)
+    if (P.p.I % 256 == 0 && P.p.Is % 256 == 0) return launch_packed_gemm<MODE_DN, PT, 4, BITS>(P, stream);
+  return launch_packed_gemm<MODE_DN, PT, CPS_DEFAULT, BITS>(P, stream);
+}
+
+template <int BITS>
+cudaError_t launch_packed_pt(const PParams& P, int pt, cudaStream_t stream) {
+  return pt == PTILE_LARGE ? launch_packed_gemms<PTILE_LARGE, BITS>(P, stream)
+         : pt == PTILE     ? launch_packed_gemms<PTILE, BITS>(P, stream)
+                           : launch_packed_gemms<PTILE_SMALL, BITS>(P, stream);
 }
 
 cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, const uint8_t* s_packed,
@@ -877,9 +966,9 @@ cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, c
   MOE_LAUNCH("gather", stream,
              launch_k(gather_kernel, dim3((unsigned)mt, pt / 8), 256, 0, stream, a.x, a.rows, hdr, tiles, a.t, a.h, a.E,
                                                                           xg, a.status));
-  err = pt == PTILE_LARGE ? launch_packed_gemms<PTILE_LARGE>(P, stream)
-        : pt == PTILE     ? launch_packed_gemms<PTILE>(P, stream)
-                          : launch_packed_gemms<PTILE_SMALL>(P, stream);
+  err = a.bits == 2   ? launch_packed_pt<2>(P, pt, stream)
+        : a.bits == 8 ? launch_packed_pt<8>(P, pt, stream)
+                      : launch_packed_pt<4>(P, pt, stream);
   if (err != cudaSuccess) return err;
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   return launch_finalize(a, deterministic, stream);

@@ -21,10 +21,10 @@ cudaError_t launch_build_csr(const int32_t* idx, const float* w, int t, int k, i
 cudaError_t launch_experts_tc(const ExpertsArgs& a, bool deterministic, cudaStream_t stream);
 size_t tc_sched_bytes(const moe_dims& d);
 size_t packed_max_tiles(const moe_dims& d);
-size_t packed_record_bytes(int h, int I);
+size_t packed_record_bytes(int h, int I, int bits);
 size_t packed_pad_rows(const moe_dims& d);
 cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, const uint16_t* biases, int h, int I,
-                        int nrec, uint8_t* dst, cudaStream_t stream);
+                        int nrec, int bits, uint8_t* dst, cudaStream_t stream);
 cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, const uint8_t* s_packed,
                                   uint16_t* xg, bool deterministic, cudaStream_t stream);
 cudaError_t launch_experts_gemv(const ExpertsArgs& a, bool packed, bool deterministic, cudaStream_t stream);
@@ -105,6 +105,8 @@ using namespace moe;
 
 namespace {
 
+int dims_bits(const moe_dims* d) { return d->bits ? d->bits : 4; }
+
 int check_dims(const moe_dims* d) {
   if (!d) return set_error(MOE_EINVAL, "dims is NULL");
   if (d->t < 1 || d->t > 65536) return set_error(MOE_ESHAPE, "t=%d outside [1, 65536]", d->t);
@@ -118,6 +120,8 @@ int check_dims(const moe_dims* d) {
   if (d->E < 1 || d->E > 1024) return set_error(MOE_ESHAPE, "E=%d outside [1, 1024]", d->E);
   if (d->k < 1 || d->k > 16 || d->k > d->E)
     return set_error(MOE_ESHAPE, "k=%d outside [1, min(E, 16)]", d->k);
+  if (d->bits != 0 && d->bits != 2 && d->bits != 4 && d->bits != 8)
+    return set_error(MOE_ESHAPE, "bits=%d: the expert records hold 2-, 4- or 8-bit codes (0 means 4)", d->bits);
   return MOE_OK;
 }
 
@@ -295,7 +299,8 @@ int moe_experts_fwd(const uint16_t* x, const moe_csr* csr, const moe_qweights* e
   a.codes = experts->codes;
   a.scales = experts->scales;
   a.biases = experts->biases;
-  a.rec_bytes = (size_t)3 * dims->inter * dims->h / 2;
+  a.bits = dims_bits(dims);
+  a.rec_bytes = (size_t)3 * dims->inter * dims->h * a.bits / 8;
   a.rec_groups = (size_t)3 * dims->inter * dims->h / 64;
   if (dims->shared_inter > 0) {
     a.s_codes = shared->codes;
@@ -313,8 +318,11 @@ int moe_experts_fwd(const uint16_t* x, const moe_csr* csr, const moe_qweights* e
   a.out = out;
 
   cudaStream_t s = (cudaStream_t)stream;
+  if (a.bits != 4 && (!packed || (flags & MOE_FORCE_SMALL_T)))
+    return set_error(MOE_EINVAL, "%d-bit records need MOE_PACKED_WEIGHTS and the tensor-core kernels "
+                     "(not MOE_FORCE_SMALL_T)", a.bits);
   const bool small_t =
-      !(flags & (MOE_FORCE_LARGE_T | MOE_SIMPLE_KERNELS)) &&
+      a.bits == 4 && !(flags & (MOE_FORCE_LARGE_T | MOE_SIMPLE_KERNELS)) &&
       ((flags & MOE_FORCE_SMALL_T) ||
        (dims->t <= SMALL_T_MAX && (long)dims->t * dims->k * (dims->inter / 128) < SMALL_T_UNITS));
   if (small_t)
@@ -368,8 +376,8 @@ int moe_forward(const uint16_t* x, const uint16_t* wr, const float* rbias, const
 
 size_t moe_packed_bytes(const moe_dims* dims, int shared) {
   if (check_dims(dims) != MOE_OK) return 0;
-  if (shared) return dims->shared_inter > 0 ? packed_record_bytes(dims->h, dims->shared_inter) : 0;
-  return (size_t)dims->E * packed_record_bytes(dims->h, dims->inter);
+  if (shared) return dims->shared_inter > 0 ? packed_record_bytes(dims->h, dims->shared_inter, dims_bits(dims)) : 0;
+  return (size_t)dims->E * packed_record_bytes(dims->h, dims->inter, dims_bits(dims));
 }
 
 int moe_pack_experts(const moe_qweights* src, const moe_dims* dims, int shared, void* dst, size_t dst_bytes,
@@ -384,7 +392,7 @@ int moe_pack_experts(const moe_qweights* src, const moe_dims* dims, int shared, 
   const size_t need = moe_packed_bytes(dims, shared);
   if (dst_bytes < need) return set_error(MOE_EINVAL, "dst has %zu bytes, needs %zu", dst_bytes, need);
   const int I = shared ? dims->shared_inter : dims->inter;
-  return cuda_status(launch_pack(src->codes, src->scales, src->biases, dims->h, I, shared ? 1 : dims->E,
+  return cuda_status(launch_pack(src->codes, src->scales, src->biases, dims->h, I, shared ? 1 : dims->E, dims_bits(dims),
                                  (uint8_t*)dst, (cudaStream_t)stream),
                      "moe_pack_experts launch");
 }

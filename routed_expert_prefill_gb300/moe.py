@@ -56,7 +56,8 @@ EXPORTS = (
 
 class MoeDims(ctypes.Structure):
     _fields_ = [("t", ctypes.c_int32), ("h", ctypes.c_int32), ("inter", ctypes.c_int32),
-                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("shared_inter", ctypes.c_int32)]
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("shared_inter", ctypes.c_int32),
+                ("bits", ctypes.c_int32)]
 
 
 class MoeCsr(ctypes.Structure):
@@ -151,8 +152,12 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def dims_of(t: int, h: int, inter: int, E: int, k: int, shared_inter: int) -> MoeDims:
-    return MoeDims(t, h, inter, E, k, shared_inter)
+def dims_of(t: int, h: int, inter: int, E: int, k: int, shared_inter: int, bits: int = 4) -> MoeDims:
+    return MoeDims(t, h, inter, E, k, shared_inter, bits)
+
+
+def _code_bits(dims: MoeDims) -> int:
+    return dims.bits or 4
 
 
 class Csr(NamedTuple):
@@ -397,10 +402,11 @@ def moe_experts_fwd(x: torch.Tensor, csr: Csr, experts: tuple, shared: tuple | N
 
     def need_record(rec, name, n_rec, inter):
         if packed:
-            nbytes = lib.moe_packed_bytes(ctypes.byref(MoeDims(t, h, I, E, k, Is)), 1 if name == "shared" else 0)
+            nbytes = lib.moe_packed_bytes(ctypes.byref(MoeDims(t, h, I, E, k, Is, dims.bits)),
+                                          1 if name == "shared" else 0)
             _need(rec[0], f"{name} codes", (torch.uint8,), min_numel=nbytes)
         else:
-            _need(rec[0], f"{name} codes", (torch.uint8,), min_numel=n_rec * 3 * inter * h // 2)
+            _need(rec[0], f"{name} codes", (torch.uint8,), min_numel=n_rec * 3 * inter * h * _code_bits(dims) // 8)
             _need(rec[1], f"{name} scales", _F16, min_numel=n_rec * 3 * inter * h // 64)
             _need(rec[2], f"{name} biases", _F16, min_numel=n_rec * 3 * inter * h // 64)
 
@@ -457,7 +463,7 @@ def pack_experts(codes: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor
     if n == 0:
         raise MoeError(-2, "nothing to pack for these dims")
     n_rec, inter = (1, dims.shared_inter) if shared else (dims.E, dims.inter)
-    _need(codes, "codes", (torch.uint8,), min_numel=n_rec * 3 * inter * dims.h // 2)
+    _need(codes, "codes", (torch.uint8,), min_numel=n_rec * 3 * inter * dims.h * _code_bits(dims) // 8)
     _need(scales, "scales", _F16, min_numel=n_rec * 3 * inter * dims.h // 64)
     _need(biases, "biases", _F16, min_numel=n_rec * 3 * inter * dims.h // 64)
     _on_current_device(codes=codes, scales=scales, biases=biases)

@@ -553,3 +553,49 @@ def test_fused_decode_launch(moe, t, h, inter, E, k, Is, gate):
     assert "decode_fused" not in prof and prof, prof
     np.testing.assert_array_equal(res2["idx"].cpu().numpy(), ref["idx"])
     _check_out(res2["out"], ref["out"])
+
+
+# Low-bit expert records (prefill/experts.rs, pf_experts: the quantised
+# matmuls take the layout's bits): 2- and 8-bit codes through the packed
+# tensor-core kernels, on 64-, 128- and 160-row tiles, the paired down pass
+# (inter >= 1024) and a ragged multi-tile expert.
+LOWBIT_CASES = [
+    ("lb_tiny", 16, 256, 128, 8, 2, 128, False),     # 64-row tiles
+    ("lb_mid", 300, 512, 256, 16, 4, 256, False),    # 128-row tiles
+    ("lb_big", 1000, 256, 1280, 8, 2, 256, True),    # 160-row tiles, paired down, expert 0 takes every row
+]
+
+
+@pytest.mark.parametrize("bits", [2, 8])
+@pytest.mark.parametrize("case", LOWBIT_CASES, ids=[c[0] for c in LOWBIT_CASES])
+@pytest.mark.parametrize("det", [False, True])
+def test_low_bit_packed_parity(moe, bits, case, det):
+    name, t, h, inter, E, k, Is, skew0 = case
+    w = synth.Workload(name, t, h, inter, E, k, Is, 90 + t + bits, bits=bits)
+    inp = synth.make_inputs(w)
+    if skew0:
+        inp["rbias"] = np.zeros(E, np.float32)
+        inp["rbias"][0] = 3.0
+    ref = O.moe_forward(inp, k, h, inter, Is)
+    dev = moe.upload_inputs(inp)
+    dims = moe.dims_of(t, h, inter, E, k, Is, bits=bits)
+    flags = moe.MOE_PACKED_WEIGHTS | (moe.MOE_DETERMINISTIC if det else 0)
+    res = moe.moe_forward(dev, dims, flags)
+    torch.cuda.synchronize()
+    assert moe.read_device_status(res["ws"]) == 0
+    np.testing.assert_array_equal(res["idx"].cpu().numpy(), ref["idx"])
+    _check_csr_against(res["csr"], res["idx"], res["w"], E)
+    _check_out(res["out"], ref["out"])
+
+
+def test_low_bit_needs_packed_tensor_core_kernels(moe):
+    w = synth.Workload("lb_err", 16, 256, 128, 8, 2, 128, 5, bits=8)
+    inp = synth.make_inputs(w)
+    dev = moe.upload_inputs(inp)
+    dims = moe.dims_of(16, 256, 128, 8, 2, 128, bits=8)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_forward(dev, dims, 0)  # row-major records
+    assert ei.value.status == -1
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_forward(dev, moe.dims_of(16, 256, 128, 8, 2, 128, bits=3), moe.MOE_PACKED_WEIGHTS)
+    assert ei.value.status == -2
