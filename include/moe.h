@@ -62,7 +62,7 @@ typedef struct {
   int32_t E;            /* number of routed experts */
   int32_t k;            /* experts per row */
   int32_t shared_inter; /* shared expert intermediate size; 0 = none */
-  int32_t bits;         /* code width of the expert records: 2, 4 or 8 (0 means 4) */
+  int32_t bits;         /* code width of the expert records: 2, 3, 4 or 8 (0 means 4) */
 } moe_dims;
 
 /* The expert-grouped list produced by moe_build_csr (all device, caller-owned). */
@@ -79,7 +79,7 @@ typedef struct {
  *         K-contiguous; a row's bytes form one little-endian bit string and
  *         code k occupies its bits [k*bits, k*bits + bits) (4 bits: two codes
  *         per byte, the low nibble at the even K index).  bits = dims->bits
- *         (0 means 4); records of 2 or 8 bits go through moe_pack_experts and
+ *         (0 means 4); records of 2, 3 or 8 bits go through moe_pack_experts and
  *         the tensor-core kernels (MOE_PACKED_WEIGHTS) only.
  * scales, biases: fp16 [E][3*inter*h/64], per output row and 64-wide K
  *         group, row-major [rows][K/64] per matrix, same matrix order. */

@@ -28,7 +28,7 @@ struct ExpertsArgs {
   float* gvpart;           // small-t gate/up partial sums [4][t*k + t][2][max(I, Is)] (t <= 16)
   DeviceStatus* status;
   uint16_t* out;           // bf16 [t][h]
-  int bits;                // code width of the records: 2, 4 or 8 (packed kernels; the others take 4)
+  int bits;                // code width of the records: 2, 3, 4 or 8 (packed kernels; the others take 4)
 };
 
 // Packed record layout (moe_pack_experts): 128-row x 64-K blocks of 4-bit

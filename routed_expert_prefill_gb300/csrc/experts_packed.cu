@@ -39,6 +39,7 @@
 // Every mbarrier wait is bounded (2 s of global time); a wait that gives up
 // records MOE_ETIMEOUT, raises a CTA-wide abort flag, lets in-flight copies
 // and MMAs land, frees TMEM and returns.
+#include <type_traits>
 #include "tc_common.cuh"
 #include "tc_ptx.cuh"
 
@@ -163,6 +164,27 @@ __device__ __forceinline__ uint32_t pack_word2(uint32_t w) {
 // at (w >> 8i) & 0x00FF00FF.
 __device__ __forceinline__ uint32_t pack_word8(uint32_t w) { return __byte_perm(w, 0, 0x3120); }
 
+// 3 bits: a row's 64 codes (24 source bytes, code k at bits [3k, 3k + 3))
+// become two planes.  The low two bits of each code form four words in the
+// 2-bit pair layout; the high bit of pair p = 8j + i (codes K 2p, K 2p + 1)
+// goes to bits p % 16 (even code) and 16 + p % 16 (odd code) of word
+// p / 16 of the high plane.
+__device__ __forceinline__ void pack_row3(const uint32_t (&src)[6], uint32_t (&lo)[4], uint32_t (&hi)[2]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) lo[j] = 0;
+  hi[0] = hi[1] = 0;
+#pragma unroll
+  for (int k = 0; k < 64; ++k) {
+    const int bit = 3 * k, wi = bit >> 5, off = bit & 31;
+    uint32_t v = src[wi] >> off;
+    if (off > 29) v |= src[wi + 1] << (32 - off);
+    const uint32_t q = v & 7u;
+    const int pr = k >> 1, j = pr >> 3, i = pr & 7, half = (k & 1) * 16;
+    lo[j] |= (q & 3u) << (half + 2 * i);
+    hi[pr >> 4] |= (q >> 2) << (half + (pr & 15));
+  }
+}
+
 // ----------------------------------------------------------------------------
 // Packing: one 128-thread block per packed block (thread = weight row).
 // Source records hold BITS-bit codes, each row least significant bit first.
@@ -204,13 +226,27 @@ pack_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scal
       codes + rec * src_rec_bytes + mat * mat_bytes + (size_t)(rt * 128 + o) * (K * BITS / 8) + kc * ROWB;
   const size_t g = rec * src_rec_groups + mat * mat_groups + (size_t)(rt * 128 + o) * (K / KC) + kc;
   uint8_t* d = dst + rec * rec_bytes(h, I, BITS) + dst_off;
+  if constexpr (BITS == 3) {
+    uint32_t w[6], lo[4], hi[2];
 #pragma unroll
-  for (int v = 0; v < ROWB / 16; ++v) {
-    uint4 c = reinterpret_cast<const uint4*>(src)[v];
-    if (BITS == 2) c.x = pack_word2(c.x), c.y = pack_word2(c.y), c.z = pack_word2(c.z), c.w = pack_word2(c.w);
-    if (BITS == 4) c.x = pack_word(c.x), c.y = pack_word(c.y), c.z = pack_word(c.z), c.w = pack_word(c.w);
-    if (BITS == 8) c.x = pack_word8(c.x), c.y = pack_word8(c.y), c.z = pack_word8(c.z), c.w = pack_word8(c.w);
-    reinterpret_cast<uint4*>(d + o * ROWB)[v] = c;
+    for (int v = 0; v < 3; ++v) {
+      const uint2 c = reinterpret_cast<const uint2*>(src)[v];
+      w[2 * v] = c.x, w[2 * v + 1] = c.y;
+    }
+    pack_row3(w, lo, hi);
+    uint2* dr = reinterpret_cast<uint2*>(d + o * ROWB);
+    dr[0] = make_uint2(lo[0], lo[1]);
+    dr[1] = make_uint2(lo[2], lo[3]);
+    dr[2] = make_uint2(hi[0], hi[1]);
+  } else {
+#pragma unroll
+    for (int v = 0; v < ROWB / 16; ++v) {
+      uint4 c = reinterpret_cast<const uint4*>(src)[v];
+      if (BITS == 2) c.x = pack_word2(c.x), c.y = pack_word2(c.y), c.z = pack_word2(c.z), c.w = pack_word2(c.w);
+      if (BITS == 4) c.x = pack_word(c.x), c.y = pack_word(c.y), c.z = pack_word(c.z), c.w = pack_word(c.w);
+      if (BITS == 8) c.x = pack_word8(c.x), c.y = pack_word8(c.y), c.z = pack_word8(c.z), c.w = pack_word8(c.w);
+      reinterpret_cast<uint4*>(d + o * ROWB)[v] = c;
+    }
   }
   __nv_bfloat16 sb = h2bf(scales[g]), bb = h2bf(biases[g]);
   reinterpret_cast<__nv_bfloat16*>(d + 128 * ROWB)[o] = sb;
@@ -317,8 +353,22 @@ __device__ __forceinline__ void dequant_bits(const uint32_t* w, __nv_bfloat162 s
         const __nv_bfloat162 r = __hfma2(q, s2, b2);
         out[8 * j + i] = *reinterpret_cast<const uint32_t*>(&r);
       }
+  } else if constexpr (BITS == 3) {
+    // w[0..3]: the low two bits in the 2-bit pair layout; w[4..5]: the high
+    // bits, pair p = 8j + i at bit p % 16 of each half of word 4 + p / 16
+    const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.f, 128.f);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t hb = (w[4 + (j >> 1)] >> (8 * (j & 1) + i)) & 0x00010001u;
+        uint32_t v = ((w[j] >> (2 * i)) & 0x00030003u) | (hb << 2) | 0x43004300u;
+        const __nv_bfloat162 q = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&v), k128);
+        const __nv_bfloat162 r = __hfma2(q, s2, b2);
+        out[8 * j + i] = *reinterpret_cast<const uint32_t*>(&r);
+      }
   } else {
-    static_assert(BITS == 8, "2, 4 or 8 bits");
+    static_assert(BITS == 8, "2, 3, 4 or 8 bits");
     // word j: pairs (K 4j + 2i, K 4j + 2i + 1) at (w >> 8i) & 0x00FF00FF.  The
     // low seven bits go through the bf16 magic number (128 + q, exact), bit
     // 7 adds 128 (0x4300 per half where set): q exact up to 255.
@@ -656,22 +706,24 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         // cm is dequantised and stored (the tensor-memory store is a compiler
         // barrier), so their shared-memory latency overlaps the arithmetic.
         const uint8_t* stage_c = c_s + sc * C::C_STAGE;
-        constexpr int NV = C::ROWB / 16;  // 16-byte code words of a row
-        uint4 cw[NV];
+        // a row's codes in 16-byte words (rows of 16, 32 or 64 bytes) or 8-byte words (3 bits, 24 bytes)
+        using CW = std::conditional_t<C::ROWB % 16 == 0, uint4, uint2>;
+        constexpr int NV = C::ROWB / (int)sizeof(CW);
+        CW cw[NV];
 #pragma unroll
-        for (int v = 0; v < NV; ++v) cw[v] = reinterpret_cast<const uint4*>(stage_c + o * C::ROWB)[v];
+        for (int v = 0; v < NV; ++v) cw[v] = reinterpret_cast<const CW*>(stage_c + o * C::ROWB)[v];
         __nv_bfloat16 sv = reinterpret_cast<const __nv_bfloat16*>(stage_c + 128 * C::ROWB)[o];
         __nv_bfloat16 bv = reinterpret_cast<const __nv_bfloat16*>(stage_c + 128 * C::ROWB + 256)[o];
 #pragma unroll
         for (int cm = 0; cm < CPS * C::NMAT; ++cm) {
-          uint4 nw[NV];
+          CW nw[NV];
 #pragma unroll
           for (int v = 0; v < NV; ++v) nw[v] = cw[v];
           __nv_bfloat16 ns = sv, nbv = bv;
           if (cm + 1 < CPS * C::NMAT) {
             const uint8_t* nb = stage_c + (cm + 1) * QB;
 #pragma unroll
-            for (int v = 0; v < NV; ++v) nw[v] = reinterpret_cast<const uint4*>(nb + o * C::ROWB)[v];
+            for (int v = 0; v < NV; ++v) nw[v] = reinterpret_cast<const CW*>(nb + o * C::ROWB)[v];
             ns = reinterpret_cast<const __nv_bfloat16*>(nb + 128 * C::ROWB)[o];
             nbv = reinterpret_cast<const __nv_bfloat16*>(nb + 128 * C::ROWB + 256)[o];
           }
@@ -865,6 +917,9 @@ cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, const uint
   if (bits == 2)
     MOE_LAUNCH("pack", stream,
                pack_kernel<2><<<grid, 128, 0, stream>>>(codes, scales, biases, h, I, src_bytes, src_groups, dst));
+  else if (bits == 3)
+    MOE_LAUNCH("pack", stream,
+               pack_kernel<3><<<grid, 128, 0, stream>>>(codes, scales, biases, h, I, src_bytes, src_groups, dst));
   else if (bits == 8)
     MOE_LAUNCH("pack", stream,
                pack_kernel<8><<<grid, 128, 0, stream>>>(codes, scales, biases, h, I, src_bytes, src_groups, dst));
@@ -967,6 +1022,7 @@ cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, c
              launch_k(gather_kernel, dim3((unsigned)mt, pt / 8), 256, 0, stream, a.x, a.rows, hdr, tiles, a.t, a.h, a.E,
                                                                           xg, a.status));
   err = a.bits == 2   ? launch_packed_pt<2>(P, pt, stream)
+        : a.bits == 3 ? launch_packed_pt<3>(P, pt, stream)
         : a.bits == 8 ? launch_packed_pt<8>(P, pt, stream)
                       : launch_packed_pt<4>(P, pt, stream);
   if (err != cudaSuccess) return err;

@@ -120,8 +120,8 @@ int check_dims(const moe_dims* d) {
   if (d->E < 1 || d->E > 1024) return set_error(MOE_ESHAPE, "E=%d outside [1, 1024]", d->E);
   if (d->k < 1 || d->k > 16 || d->k > d->E)
     return set_error(MOE_ESHAPE, "k=%d outside [1, min(E, 16)]", d->k);
-  if (d->bits != 0 && d->bits != 2 && d->bits != 4 && d->bits != 8)
-    return set_error(MOE_ESHAPE, "bits=%d: the expert records hold 2-, 4- or 8-bit codes (0 means 4)", d->bits);
+  if (d->bits != 0 && d->bits != 2 && d->bits != 3 && d->bits != 4 && d->bits != 8)
+    return set_error(MOE_ESHAPE, "bits=%d: the expert records hold 2-, 3-, 4- or 8-bit codes (0 means 4)", d->bits);
   return MOE_OK;
 }
 

@@ -556,7 +556,7 @@ def test_fused_decode_launch(moe, t, h, inter, E, k, Is, gate):
 
 
 # Low-bit expert records (prefill/experts.rs, pf_experts: the quantised
-# matmuls take the layout's bits): 2- and 8-bit codes through the packed
+# matmuls take the layout's bits): 2-, 3- and 8-bit codes through the packed
 # tensor-core kernels, on 64-, 128- and 160-row tiles, the paired down pass
 # (inter >= 1024) and a ragged multi-tile expert.
 LOWBIT_CASES = [
@@ -566,7 +566,7 @@ LOWBIT_CASES = [
 ]
 
 
-@pytest.mark.parametrize("bits", [2, 8])
+@pytest.mark.parametrize("bits", [2, 3, 8])
 @pytest.mark.parametrize("case", LOWBIT_CASES, ids=[c[0] for c in LOWBIT_CASES])
 @pytest.mark.parametrize("det", [False, True])
 def test_low_bit_packed_parity(moe, bits, case, det):
@@ -597,5 +597,5 @@ def test_low_bit_needs_packed_tensor_core_kernels(moe):
         moe.moe_forward(dev, dims, 0)  # row-major records
     assert ei.value.status == -1
     with pytest.raises(moe.MoeError) as ei:
-        moe.moe_forward(dev, moe.dims_of(16, 256, 128, 8, 2, 128, bits=3), moe.MOE_PACKED_WEIGHTS)
+        moe.moe_forward(dev, moe.dims_of(16, 256, 128, 8, 2, 128, bits=5), moe.MOE_PACKED_WEIGHTS)
     assert ei.value.status == -2
