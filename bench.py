@@ -52,7 +52,8 @@ from routed_expert_prefill_gb300 import synth  # noqa: E402
 METRIC = "prefill tokens/s and % of roofline (tensor or HBM) for routed MoE FFN, 1 GB300"
 DEFAULT_WORKLOAD = "t4096_h4096_e256"
 EXTRA_WORKLOADS = ("t4096_h2048_e128_skewed", "t512_h2048_e128", "decode_t1_h2048_e128",
-                   "decode_t2_h2048_e128", "decode_t4_h2048_e128", "decode_t8_h2048_e128")
+                   "decode_t2_h2048_e128", "decode_t4_h2048_e128", "decode_t8_h2048_e128",
+                   "t4096_h4096_e256_b2", "t4096_h4096_e256_b3", "t4096_h4096_e256_b8")
 L2_BYTES = 129 * 2 ** 20
 SUSTAIN_S, SUSTAIN_MIN_RUNS, SUSTAIN_MAX_RUNS = 1.0, 50, 20000
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -78,27 +79,32 @@ def host_cores() -> int:
 # Algorithmic work of one step (from the step's actual routing)
 # --------------------------------------------------------------------------
 
-def record_bytes(h, inter):
-    """Bytes of one quantised expert record: 4-bit codes + fp16 scale and bias per 64."""
-    return 3 * inter * h // 2 + 2 * 2 * (3 * inter * h // 64)
+def matrix_bytes(rows, K, bits=4):
+    """Bytes of one quantised matrix: codes of `bits` bits + fp16 scale and bias per 64."""
+    return rows * K * bits // 8 + 2 * 2 * (rows * K // 64)
+
+
+def record_bytes(h, inter, bits=4):
+    """Bytes of one quantised expert record (gate, up, down)."""
+    return 3 * matrix_bytes(inter, h, bits)
 
 
 def step_work(w: synth.Workload, counts: np.ndarray) -> dict:
     touched = int((counts > 0).sum())
     n = int(counts.sum())
-    t, h, I, Is, E, k = w.t, w.h, w.inter, w.shared_inter, w.E, w.k
+    t, h, I, Is, E, k, bits = w.t, w.h, w.inter, w.shared_inter, w.E, w.k, w.bits
     flops = 2 * t * h * E + 6 * n * h * I + 6 * t * h * Is
-    wbytes = touched * record_bytes(h, I) + (record_bytes(h, Is) if Is else 0)
+    wbytes = touched * record_bytes(h, I, bits) + (record_bytes(h, Is, bits) if Is else 0)
     io = 2 * t * h * 2 + E * h * 2 + t * k * 8
     by_kernel = {
         # gate+up weights of touched experts (and the shared expert) + x in + hg out
-        "gateup": dict(bytes=touched * 2 * (I * h // 2 + 2 * 2 * I * h // 64)
-                       + (2 * (Is * h // 2 + 2 * 2 * Is * h // 64) if Is else 0)
+        "gateup": dict(bytes=touched * 2 * matrix_bytes(I, h, bits)
+                       + (2 * matrix_bytes(Is, h, bits) if Is else 0)
                        + t * h * 2 + (n * I + t * Is) * 2,
                        flops=4 * n * h * I + 4 * t * h * Is),
         # down weights + hg in + fp32 block accumulator in/out
-        "down": dict(bytes=touched * (I * h // 2 + 2 * 2 * I * h // 64)
-                     + ((Is * h // 2 + 2 * 2 * Is * h // 64) if Is else 0)
+        "down": dict(bytes=touched * matrix_bytes(h, I, bits)
+                     + (matrix_bytes(h, Is, bits) if Is else 0)
                      + (n * I + t * Is) * 2 + 2 * t * h * 4,
                      flops=2 * n * h * I + 2 * t * h * Is),
         # router (scores + exact refinement): x and router weights in, idx/w out
@@ -380,13 +386,13 @@ class Ctx:
 
     def device_inputs(self, w: synth.Workload, inp: dict, flags: int) -> dict:
         moe, torch = self.moe, self.torch
-        key = (w.h, w.inter, w.E, w.shared_inter, w.seed, w.skew, w.shared_gate)
+        key = (w.h, w.inter, w.E, w.shared_inter, w.seed, w.skew, w.shared_gate, w.bits)
         if key not in self.weights:
             self.weights.clear()
             torch.cuda.empty_cache()
             dev = moe.upload_inputs(inp, self.dev)
             if flags & MOE_PACKED_WEIGHTS:
-                moe.add_packed(dev, moe.dims_of(w.t, w.h, w.inter, w.E, w.k, w.shared_inter))
+                moe.add_packed(dev, moe.dims_of(w.t, w.h, w.inter, w.E, w.k, w.shared_inter, w.bits))
             self.weights[key] = dev
         dev = dict(self.weights[key])
         dev["x"] = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).to(self.dev)
@@ -399,7 +405,7 @@ def measure(ctx: Ctx, w: synth.Workload, inp: dict, headline: bool) -> dict:
     torch, moe, args = ctx.torch, ctx.moe, ctx.args
     flags = args.flags
     dev = ctx.device_inputs(w, inp, flags)
-    dims = moe.dims_of(w.t, w.h, w.inter, w.E, w.k, w.shared_inter)
+    dims = moe.dims_of(w.t, w.h, w.inter, w.E, w.k, w.shared_inter, w.bits)
     ws = moe.new_workspace(dims, flags, ctx.dev)
     out = torch.empty((w.t, w.h), dtype=torch.bfloat16, device=ctx.dev)
     stream = torch.cuda.current_stream()
@@ -587,7 +593,8 @@ def measure(ctx: Ctx, w: synth.Workload, inp: dict, headline: bool) -> dict:
 def workload_config(w: synth.Workload, m: dict) -> dict:
     work, sr = m["work"], m["step_roofline"]
     return {"workload": w.name, "t": w.t, "h": w.h, "inter": w.inter, "E": w.E, "k": w.k,
-            "shared_inter": w.shared_inter, "routing": "Zipf-skewed" if w.skew else "near-uniform",
+            "shared_inter": w.shared_inter, "bits": w.bits,
+            "routing": "Zipf-skewed" if w.skew else "near-uniform",
             "flags": m["flags"], "touched_experts": work["touched"], "max_rows_per_expert": work["max_rows"],
             "step_flops": work["flops"], "step_bytes": work["bytes"], "step_tflops": sr["tflops"],
             "step_gbs": sr["gbs"], "step_roofline_frac": sr["frac"], "step_bound": sr["bound"],

@@ -292,8 +292,6 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   mbar_wait(bar, parity, &never, 100000000ull);
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return silu_mul_fast(g, u); }
-
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                    smem_u32(dst)),
@@ -335,57 +333,86 @@ __device__ __forceinline__ void down_cols16(const uint32_t (&y)[16], const int* 
 }
 
 
-// Dequantise one row of a packed block (64 K) into 32 bf16 pairs in K order,
-// w = fma(q, s, b) in bf16.  The in-word layouts are those of pack_kernel.
+// Dequantise one row of a packed block (64 K) into 32 bf16 pairs in K order.
+// The in-word layouts are those of pack_kernel.
+//
+// A code's bits, masked in place and read as a bf16 number, are a subnormal
+// (or, from 128 to 255, a number of the smallest normal binade); either way
+// the bf16 number with bits r has the value r * 2^-133 exactly.  So
+//   fma(r, s * 2^109, b * 2^-24) = (q s + b) * 2^-24, rounded once,
+// the same rounding as fma(q, s, b) scaled by a power of two (exact while
+// the result stays normal, |q s + b| >= 2^-102), with neither a magic
+// exponent nor a subtraction.  A code masked 4 bits up reads as 16 q and
+// takes s * 2^109 / 16, so one shift serves four pairs.  The accumulators
+// then carry the factor 2^-24, which the epilogues multiply out (exact).
+// s * 2^109 stays finite for every fp16 scale (< 2^16).
+constexpr float DQ_SCALE_UP = 0x1p109f, DQ_BIAS_DOWN = 0x1p-24f, ACC_UP = 0x1p24f;
+
 template <int BITS>
 __device__ __forceinline__ void dequant_bits(const uint32_t* w, __nv_bfloat162 s2, __nv_bfloat162 b2, uint32_t* out) {
+  const __nv_bfloat162 sA = __hmul2(s2, __float2bfloat162_rn(DQ_SCALE_UP));
+  const __nv_bfloat162 bb = __hmul2(b2, __float2bfloat162_rn(DQ_BIAS_DOWN));
+  auto fma_raw = [&](uint32_t raw, __nv_bfloat162 sc) {
+    const __nv_bfloat162 r = __hfma2(*reinterpret_cast<const __nv_bfloat162*>(&raw), sc, bb);
+    return *reinterpret_cast<const uint32_t*>(&r);
+  };
   if constexpr (BITS == 4) {
-    dequant_packed<8>(w, s2, b2, out);
+    // word j: pairs (K 8j + 2i, K 8j + 2i + 1) at (w >> 4i) & 0x000F000F
+    const __nv_bfloat162 s16 = __hmul2(sA, __float2bfloat162_rn(0.0625f));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t lo = w[j], hi = w[j] >> 8;
+      out[4 * j + 0] = fma_raw(lo & 0x000F000Fu, sA);
+      out[4 * j + 1] = fma_raw(lo & 0x00F000F0u, s16);
+      out[4 * j + 2] = fma_raw(hi & 0x000F000Fu, sA);
+      out[4 * j + 3] = fma_raw(hi & 0x00F000F0u, s16);
+    }
   } else if constexpr (BITS == 2) {
     // word j: pairs (K 16j + 2i, K 16j + 2i + 1) at (w >> 2i) & 0x00030003
-    const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.f, 128.f);
+    __nv_bfloat162 sc[4];
+    sc[0] = sA;
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int i = 1; i < 4; ++i) sc[i] = __hmul2(sc[i - 1], __float2bfloat162_rn(0.25f));
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        uint32_t v = ((w[j] >> (2 * i)) & 0x00030003u) | 0x43004300u;
-        const __nv_bfloat162 q = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&v), k128);
-        const __nv_bfloat162 r = __hfma2(q, s2, b2);
-        out[8 * j + i] = *reinterpret_cast<const uint32_t*>(&r);
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t lo = w[j], hi = w[j] >> 8;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        out[8 * j + i] = fma_raw(lo & (0x00030003u << (2 * i)), sc[i]);
+        out[8 * j + 4 + i] = fma_raw(hi & (0x00030003u << (2 * i)), sc[i]);
       }
+    }
   } else if constexpr (BITS == 3) {
     // w[0..3]: the low two bits in the 2-bit pair layout; w[4..5]: the high
-    // bits, pair p = 8j + i at bit p % 16 of each half of word 4 + p / 16
-    const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.f, 128.f);
+    // bits, pair p = 8j + i at bit p % 16 of each half of word 4 + p / 16.
+    // The code is assembled at bits 0-2 of each half.
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const uint32_t hb = (w[4 + (j >> 1)] >> (8 * (j & 1) + i)) & 0x00010001u;
-        uint32_t v = ((w[j] >> (2 * i)) & 0x00030003u) | (hb << 2) | 0x43004300u;
-        const __nv_bfloat162 q = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&v), k128);
-        const __nv_bfloat162 r = __hfma2(q, s2, b2);
-        out[8 * j + i] = *reinterpret_cast<const uint32_t*>(&r);
+        const int hs = 8 * (j & 1) + i;  // the high bit's position in its half
+        const uint32_t hw = w[4 + (j >> 1)];
+        const uint32_t hb = (hs >= 2 ? hw >> (hs - 2) : hw << (2 - hs)) & 0x00040004u;
+        out[8 * j + i] = fma_raw(((w[j] >> (2 * i)) & 0x00030003u) | hb, sA);
       }
   } else {
     static_assert(BITS == 8, "2, 3, 4 or 8 bits");
-    // word j: pairs (K 4j + 2i, K 4j + 2i + 1) at (w >> 8i) & 0x00FF00FF.  The
-    // low seven bits go through the bf16 magic number (128 + q, exact), bit
-    // 7 adds 128 (0x4300 per half where set): q exact up to 255.
-    const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.f, 128.f);
+    // word j: pairs (K 4j + 2i, K 4j + 2i + 1) at (w >> 8i) & 0x00FF00FF
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const uint32_t t = w[j] >> (8 * i);
-        uint32_t v = (t & 0x007F007Fu) | 0x43004300u;
-        uint32_t hv = ((t >> 7) & 0x00010001u) * 0x4300u;
-        const __nv_bfloat162 q = __hadd2(__hsub2(*reinterpret_cast<__nv_bfloat162*>(&v), k128),
-                                         *reinterpret_cast<__nv_bfloat162*>(&hv));
-        const __nv_bfloat162 r = __hfma2(q, s2, b2);
-        out[2 * j + i] = *reinterpret_cast<const uint32_t*>(&r);
-      }
+    for (int j = 0; j < 16; ++j) {
+      out[2 * j + 0] = fma_raw(w[j] & 0x00FF00FFu, sA);
+      out[2 * j + 1] = fma_raw((w[j] >> 8) & 0x00FF00FFu, sA);
+    }
   }
+}
+
+// silu(g) * u of accumulators carrying the factor 2^-24 of dequant_bits: the
+// same arithmetic as silu_mul_fast on (2^24 G, 2^24 U), with the powers of
+// two folded into its constants (bit-identical while G U stays normal).
+__device__ __forceinline__ float silu_mul_acc(float G, float U) {
+  float th;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(0x1p23f * G));
+  return G * U * fmaf(0x1p47f, th, 0x1p47f);
 }
 
 struct PUnit {
@@ -816,7 +843,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
             }
           }
           S.col_row[ew][col] = r;
-          S.col_w[ew][col] = wv;
+          S.col_w[ew][col] = wv * ACC_UP;  // the accumulators carry 2^-24 (dequant_bits)
         }
         if (bad_row) raise_flag(p.status, FLAG_BAD_ROW);
         __syncwarp();
@@ -850,7 +877,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             stg[j * 32 + lane] = __float2bfloat16_rn(
-                c * 16 + j < U.n ? silu_mul(__uint_as_float(g[j]), __uint_as_float(v[j])) : 0.f);
+                c * 16 + j < U.n ? silu_mul_acc(__uint_as_float(g[j]), __uint_as_float(v[j])) : 0.f);
           __syncwarp();
 #pragma unroll
           for (int half = 0; half < 2; ++half) {

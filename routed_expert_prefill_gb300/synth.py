@@ -65,6 +65,10 @@ WORKLOADS = {
     ),
     "t4096_h4096_e256": Workload("t4096_h4096_e256", 4096, 4096, 1536, 256, 8, 1536, 3),
 }
+# the headline workload with 2-, 3- and 8-bit expert records (same seed)
+for _b in (2, 3, 8):
+    WORKLOADS[f"t4096_h4096_e256_b{_b}"] = WORKLOADS["t4096_h4096_e256"].replace(
+        name=f"t4096_h4096_e256_b{_b}", bits=_b)
 for _t in (1, 2, 4, 8):
     WORKLOADS[f"decode_t{_t}_h2048_e128"] = Workload(
         f"decode_t{_t}_h2048_e128", _t, 2048, 768, 128, 8, 768, 4
