@@ -305,33 +305,34 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // l then owns features 4 (l % 8) .. +3 of column 4 it + l / 8; dq points at
 // this lane's first feature in destination row 0.  Plain 16-byte stores in
 // deterministic mode (every destination written once), fp32 reductions
-// otherwise.
+// otherwise.  The column weights w4 and this lane's destination rows rr are
+// loaded by the caller before it waits for the accumulator load, and the
+// four staged vectors are read before the first reduction is issued, so the
+// shared-memory latencies overlap instead of adding up.
 template <bool DET>
-__device__ __forceinline__ void down_cols16(const uint32_t (&y)[16], const int* s_row, const float* s_w, float* stg,
-                                            float* dq, int lane, int h) {
+__device__ __forceinline__ void down_cols16(const uint32_t (&y)[16], const float4 (&w4)[4], const int (&rr)[4],
+                                            float* stg, float* dq, int lane, int h) {
   __syncwarp();  // the previous batch's reads of stg are done
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) {
-    const float4 w4 = reinterpret_cast<const float4*>(s_w)[jj];
-    stg[(4 * jj + 0) * 32 + lane] = w4.x * __uint_as_float(y[4 * jj + 0]);
-    stg[(4 * jj + 1) * 32 + lane] = w4.y * __uint_as_float(y[4 * jj + 1]);
-    stg[(4 * jj + 2) * 32 + lane] = w4.z * __uint_as_float(y[4 * jj + 2]);
-    stg[(4 * jj + 3) * 32 + lane] = w4.w * __uint_as_float(y[4 * jj + 3]);
+    stg[(4 * jj + 0) * 32 + lane] = w4[jj].x * __uint_as_float(y[4 * jj + 0]);
+    stg[(4 * jj + 1) * 32 + lane] = w4[jj].y * __uint_as_float(y[4 * jj + 1]);
+    stg[(4 * jj + 2) * 32 + lane] = w4[jj].z * __uint_as_float(y[4 * jj + 2]);
+    stg[(4 * jj + 3) * 32 + lane] = w4[jj].w * __uint_as_float(y[4 * jj + 3]);
   }
   __syncwarp();
+  float4 v[4];
+#pragma unroll
+  for (int it = 0; it < 4; ++it) v[it] = reinterpret_cast<const float4*>(stg + (it * 4 + (lane >> 3)) * 32)[lane & 7];
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
-    const int j = it * 4 + (lane >> 3);
-    const float4 v = reinterpret_cast<const float4*>(stg + j * 32)[lane & 7];
-    const int r = s_row[j];
-    if (r >= 0) {
-      float4* d = reinterpret_cast<float4*>(dq + (size_t)(uint32_t)r * (uint32_t)h);
-      if (DET) *d = v;
-      else atomicAdd(d, v);
+    if (rr[it] >= 0) {
+      float4* d = reinterpret_cast<float4*>(dq + (size_t)(uint32_t)rr[it] * (uint32_t)h);
+      if (DET) *d = v[it];
+      else atomicAdd(d, v[it]);
     }
   }
 }
-
 
 // Dequantise one row of a packed block (64 K) into 32 bf16 pairs in K order.
 // The in-word layouts are those of pack_kernel.
@@ -902,12 +903,18 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
           const int m = cs >= nb ? 1 : 0, c = cs - m * nb;
           uint32_t y[16];
           tmem_ld16(acc + m * PT + c * 16, y);
+          float4 w4[4];
+          int rr[4];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) w4[jj] = reinterpret_cast<const float4*>(&S.col_w[ew][c * 16])[jj];
+#pragma unroll
+          for (int it = 0; it < 4; ++it) rr[it] = S.col_row[ew][c * 16 + it * 4 + (lane >> 3)];
           tmem_ld_wait();
           if (cs + egroups >= nsteps) release_acc(&S.acc_empty[ab], lane);
           if (p.deterministic)
-            down_cols16<true>(y, &S.col_row[ew][c * 16], &S.col_w[ew][c * 16], stg, dq + m * 128, lane, h);
+            down_cols16<true>(y, w4, rr, stg, dq + m * 128, lane, h);
           else
-            down_cols16<false>(y, &S.col_row[ew][c * 16], &S.col_w[ew][c * 16], stg, dq + m * 128, lane, h);
+            down_cols16<false>(y, w4, rr, stg, dq + m * 128, lane, h);
         }
       }
     }
