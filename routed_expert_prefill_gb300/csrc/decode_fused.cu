@@ -676,6 +676,8 @@ __global__ void __launch_bounds__(D_THREADS, 1) decode_fused_kernel(DfParams P) 
         tmem_ld16(lane_base + D_ACC_COL + ab * 32, gv);
         tmem_ld16(lane_base + D_ACC_COL + ab * 32 + 16, uv);
         tmem_ld_wait();
+        tmem_ld_fence(gv);
+        tmem_ld_fence(uv);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
@@ -738,6 +740,7 @@ __global__ void __launch_bounds__(D_THREADS, 1) decode_fused_kernel(DfParams P) 
         uint32_t yv[16];
         tmem_ld16(lane_base + D_ACC_COL + ab * 32, yv);
         tmem_ld_wait();
+        tmem_ld_fence(yv);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.acc_empty[ab]);

@@ -134,6 +134,14 @@ struct PCfg {
   // gate/up pass with tiles of 128 rows or more only.
   static constexpr bool BLK_REL = PAIRED && PT >= 128;
   static constexpr int NREL = BLK_REL ? CPS * NMAT : 1;  // empty barriers per slot
+  // Paired down pass: each output tile's accumulator has its own full and
+  // empty barriers, and the epilogue drains tile 0 first, so tile 0's
+  // issuer starts the next unit while tile 1 is still drained (as far as
+  // the shared A slots let it run ahead).  (Measured: giving each
+  // dequantisation group one matrix of every stage instead, so that the two
+  // matrices' pipelines decouple fully, was slower on both paired passes:
+  // every group then pays the per-stage waits twice as often.)
+  static constexpr bool ACC_SPLIT = MODE == MODE_DN2;
   static_assert(SA >= 2, "the A ring needs a stage per dequantisation group");
   static_assert(SB >= 2 && B_STAGE % 1024 == 0, "token-tile ring");
 };
@@ -473,7 +481,7 @@ struct PSmem {
   uint64_t a_full[C::SA];
   uint64_t a_empty[C::SA][C::NREL];
   uint64_t b_full[C::SB], b_empty[C::SB];
-  uint64_t acc_full[C::NACC], acc_empty[C::NACC];
+  uint64_t acc_full[2], acc_empty[2];  // per buffer, or per matrix (ACC_SPLIT)
   uint64_t drain[2];
   uint32_t tmem_slot;
   int abort;
@@ -532,8 +540,8 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
       mbar_init(&S.b_full[i], 1);
       mbar_init(&S.b_empty[i], C::NISS);
     }
-    for (int i = 0; i < C::NACC; ++i) {
-      mbar_init(&S.acc_full[i], C::NISS);
+    for (int i = 0; i < (C::ACC_SPLIT ? 2 : C::NACC); ++i) {
+      mbar_init(&S.acc_full[i], C::ACC_SPLIT ? 1 : C::NISS);
       mbar_init(&S.acc_empty[i], 4 * egroups);
     }
     mbar_init(&S.drain[0], 1);
@@ -654,7 +662,8 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         const uint32_t idesc = idesc_bf16(128, U.Nm);
         const uint32_t nm8 = (uint32_t)(U.Nm * 128) >> 4;  // descriptor step of one K chunk
         const int ab = uit % C::NACC;
-        if (!mbar_wait(&S.acc_empty[ab], ((uit / C::NACC) & 1) ^ 1, abort, WAIT_NS)) {
+        const int ai = C::ACC_SPLIT ? m : ab;  // accumulator barrier
+        if (!mbar_wait(&S.acc_empty[ai], ((uit / C::NACC) & 1) ^ 1, abort, WAIT_NS)) {
           note_timeout(p.status, abort, GATEUP ? 33 : 43);
           break;
         }
@@ -691,7 +700,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
           if constexpr (!C::BLK_REL) mma_commit(&S.a_empty[sa][0]);
         }
         if (!ok) break;
-        mma_commit(&S.acc_full[ab]);
+        mma_commit(&S.acc_full[ai]);
       }
       if (*abort) {
         mma_commit(&S.drain[m]);
@@ -873,6 +882,8 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
           tmem_ld16(acc + c * 16, g);
           tmem_ld16(acc + PT + c * 16, v);
           tmem_ld_wait();
+          tmem_ld_fence(g);
+          tmem_ld_fence(v);
           if (c + egroups >= nb) release_acc(&S.acc_empty[ab], lane);
           __syncwarp();  // the previous step's reads of the staging buffer are done
 #pragma unroll
@@ -893,29 +904,44 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         // destination row, so the scatter-add issues 16-byte reductions (a
         // quarter of the requests of one float per lane, each four times
         // wider).  The accumulator is released after its last load.
-        // Paired mode: the steps of both output tiles (accumulator m at
-        // columns m PT, features f0 + 128 m), in one sequence.
+        // Paired mode: output tile m's accumulator at columns m PT (features
+        // f0 + 128 m); each tile has its own barriers (ACC_SPLIT), tile 0 is
+        // drained and handed back first.
         float* dq = (to_list ? p.ybuf : p.acc) + U.f0 + q * 32 + (lane & 7) * 4;
         float* stg = S.stage[ew];
-        const int nb = U.Nm / 16, nsteps = C::NMAT * nb;
-        if (half >= nsteps) release_acc(&S.acc_empty[ab], lane);
-        for (int cs = half; cs < nsteps; cs += egroups) {
-          const int m = cs >= nb ? 1 : 0, c = cs - m * nb;
-          uint32_t y[16];
-          tmem_ld16(acc + m * PT + c * 16, y);
-          float4 w4[4];
-          int rr[4];
+        const int nb = U.Nm / 16;
+        bool fail = false;
+        for (int m = 0; m < C::NMAT && !fail; ++m) {
+          if (C::ACC_SPLIT && m > 0) {
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.acc_full[m], uit & 1, abort, WAIT_NS))) {
+              if (lane == 0) note_timeout(p.status, abort, 48);
+              fail = true;
+              break;
+            }
+            tc_fence_after();
+          }
+          const bool rel = C::ACC_SPLIT || m == C::NMAT - 1;  // this pass ends with a hand-back
+          uint64_t* ebar = &S.acc_empty[C::ACC_SPLIT ? m : ab];
+          if (rel && half >= nb) release_acc(ebar, lane);
+          for (int c = half; c < nb; c += egroups) {
+            uint32_t y[16];
+            tmem_ld16(acc + m * PT + c * 16, y);
+            float4 w4[4];
+            int rr[4];
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) w4[jj] = reinterpret_cast<const float4*>(&S.col_w[ew][c * 16])[jj];
+            for (int jj = 0; jj < 4; ++jj) w4[jj] = reinterpret_cast<const float4*>(&S.col_w[ew][c * 16])[jj];
 #pragma unroll
-          for (int it = 0; it < 4; ++it) rr[it] = S.col_row[ew][c * 16 + it * 4 + (lane >> 3)];
-          tmem_ld_wait();
-          if (cs + egroups >= nsteps) release_acc(&S.acc_empty[ab], lane);
-          if (p.deterministic)
-            down_cols16<true>(y, w4, rr, stg, dq + m * 128, lane, h);
-          else
-            down_cols16<false>(y, w4, rr, stg, dq + m * 128, lane, h);
+            for (int it = 0; it < 4; ++it) rr[it] = S.col_row[ew][c * 16 + it * 4 + (lane >> 3)];
+            tmem_ld_wait();
+            tmem_ld_fence(y);
+            if (rel && c + egroups >= nb) release_acc(ebar, lane);
+            if (p.deterministic)
+              down_cols16<true>(y, w4, rr, stg, dq + m * 128, lane, h);
+            else
+              down_cols16<false>(y, w4, rr, stg, dq + m * 128, lane, h);
+          }
         }
+        if (fail) break;
       }
     }
   }

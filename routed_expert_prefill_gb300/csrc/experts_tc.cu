@@ -655,6 +655,8 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
           tmem_ld16(lane_base + c * 16, g);
           tmem_ld16(lane_base + 256 + c * 16, v);
           tmem_ld_wait();
+          tmem_ld_fence(g);
+          tmem_ld_fence(v);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = c * 16 + j;
@@ -668,6 +670,7 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
           uint32_t y[16];
           tmem_ld16(lane_base + c * 16, y);
           tmem_ld_wait();
+          tmem_ld_fence(y);
           const int grp = c >> 1;  // 32-column group holding columns c*16 .. c*16+15
           int rsel = col_row[0];
           float wsel = col_w[0];

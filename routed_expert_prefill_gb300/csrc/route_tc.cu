@@ -180,6 +180,7 @@ route_score_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant
         uint32_t y[16];
         tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c * 16, y);
         tmem_ld_wait();
+        tmem_ld_fence(y);
         if (row < P.t && e0 + c * 16 < P.Ep) {
           float4* d4 = reinterpret_cast<float4*>(dst + c * 16);
 #pragma unroll
