@@ -103,10 +103,6 @@ struct PCfg {
   static constexpr int CPS = CP;
   static constexpr int NMAT = PAIRED ? 2 : 1;
   static constexpr int C_STAGE = CPS * NMAT * QB;        // packed blocks of one stage (QB at BITS)
-  // Code stages: four (measured: the code producer stays several stages
-  // ahead of the dequantisation with four; more gave nothing), so that the
-  // token-tile ring gets the rest of shared memory.
-  static constexpr int SC = 4;
   static constexpr int A_STAGE = CPS * NMAT * 32;        // TMEM columns per A stage
   static constexpr int NACC = PAIRED ? 1 : 2;            // accumulator buffers
   static constexpr int ACC_COLS = PAIRED ? 2 * PT : PT;  // TMEM columns per accumulator buffer
@@ -124,6 +120,15 @@ struct PCfg {
   static constexpr int B_STAGE =
       PT > 128 ? CP * PT * 128 : (CP * PT * 128 > 32768 ? 65536 : 32768);
   static constexpr int EPI_BYTES = (GATEUP ? 1 : 8) * PT * 8 + 8 * (GATEUP ? 16 * 16 : 16 * 32) * 4;
+  // Code stages: four on the larger tiles (the code producer stays several
+  // stages ahead of the dequantisation with four; more gave nothing there,
+  // and the token-tile ring gets the rest of shared memory).  On 64-row
+  // tiles the token stages are small and the weight stream is what the
+  // kernel waits for: up to eight code stages there, as many as leave two
+  // token stages, so that more weight bytes are in flight per SM.
+  static constexpr int SC_FIT = (SMEM_MAX - 2048 - EPI_BYTES - 2 * B_STAGE) / C_STAGE;
+  static constexpr int SC_WANT = PT <= 64 ? 8 : 4;
+  static constexpr int SC = SC_WANT < SC_FIT ? SC_WANT : (SC_FIT < 4 ? 4 : SC_FIT);
   static constexpr int SB_FIT = (SMEM_MAX - 1024 - SC * C_STAGE - EPI_BYTES - 1024) / B_STAGE;
   static constexpr int SB = SB_FIT > 16 ? 16 : SB_FIT;
   static constexpr int B_RING = SB * B_STAGE;
