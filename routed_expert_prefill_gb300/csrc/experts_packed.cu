@@ -568,10 +568,10 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     // (none under the MOE_STALL_WEIGHT_COPIES test hook: the consumers' waits run out)
     if (lane == 0 && !(p.status && (p.status->stall & MOE_STALL_WEIGHT_COPIES))) {
       uint32_t it = 0;
-      bool armed[C::SC];
-      uint32_t par[C::SC];
-#pragma unroll
-      for (int i = 0; i < C::SC; ++i) armed[i] = false, par[i] = 0;
+      // stages with a copy issued, and the phase parity each was armed for
+      // (bit masks: a per-thread array indexed by the stage would live in
+      // local memory)
+      uint32_t armed = 0, par = 0;
       bool stop = false;
       // The weight blocks of unit u: nst stages of C_STAGE bytes from the
       // returned address (paired down: blocks of the second output tile
@@ -607,23 +607,20 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
           } else {
             bulk_load(c_s + sc * C::C_STAGE, src + (size_t)st * C::C_STAGE, C::C_STAGE, &S.code_full[sc]);
           }
-          armed[sc] = true;
-          par[sc] = (it / C::SC) & 1;
+          armed |= 1u << sc;
+          par = (par & ~(1u << sc)) | (((it / C::SC) & 1u) << sc);
         }
         if (*abort) stop = true;
       }
       if (*abort)
         for (int i = 0; i < C::SC; ++i)
-          if (armed[i]) drain_wait(&S.code_full[i], par[i]);
+          if ((armed >> i) & 1u) drain_wait(&S.code_full[i], (par >> i) & 1u);
     }
   } else if (warp == W_B) {
     // ------------------------------------------------------------ token images
     if (lane == 0) {
       uint32_t it = 0;
-      bool armed[SB];
-      uint32_t par[SB];
-#pragma unroll
-      for (int i = 0; i < SB; ++i) armed[i] = false, par[i] = 0;
+      uint32_t armed = 0, par = 0;  // as for the code stages
       bool stop = false;
       for (int u = unit0; u < n_units && !stop; u += ustride) {
         const PUnit U = decode_punit<MODE, CP, C::B_STAGE>(p, u);
@@ -639,14 +636,14 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
           const uint32_t bytes = (uint32_t)(min(U.kps, U.nkc - kc0) * U.Nm * 128);
           mbar_arrive_expect_tx(&S.b_full[sb], bytes);
           bulk_load(b_s + sb * B_STAGE, src + (size_t)kc0 * U.Nm * 128, bytes, &S.b_full[sb]);
-          armed[sb] = true;
-          par[sb] = (it / SB) & 1;
+          armed |= 1u << sb;
+          par = (par & ~(1u << sb)) | (((it / SB) & 1u) << sb);
         }
         if (*abort) stop = true;
       }
       if (*abort)
         for (int i = 0; i < SB; ++i)
-          if (armed[i]) drain_wait(&S.b_full[i], par[i]);
+          if ((armed >> i) & 1u) drain_wait(&S.b_full[i], (par >> i) & 1u);
     }
   } else if (warp == W_MMA || warp == W_MMA2) {
     // ------------------------------------------------------------ MMA issuers (A in TMEM)
@@ -658,9 +655,11 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     // both; down: W_MMA alone (one accumulator, one fixed order).
     const int m = warp == W_MMA ? 0 : 1;
     if (lane == 0 && (PAIRED || warp == W_MMA)) {
-      uint64_t bstage[SB];
-#pragma unroll
-      for (int i = 0; i < SB; ++i) bstage[i] = desc_sw128(smem_u32(b_s + i * B_STAGE));
+      // descriptor of token stage 0; stage sb's differs by its offset in
+      // the start-address field (16-byte units; shared memory < 256 KB
+      // keeps the field from overflowing), computed rather than looked up
+      // in a per-thread table, which would live in local memory
+      const uint64_t bstage0 = desc_sw128(smem_u32(b_s));
       uint32_t ast = 0, bit = 0, uit = 0;
       for (int u = unit0; u < n_units && !*abort; u += ustride, ++uit) {
         const PUnit U = decode_punit<MODE, CP, C::B_STAGE>(p, u);
@@ -690,7 +689,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
           for (int c = 0; c < CPS; ++c) {
             const int kc = st * CPS + c;
             const int sb = bit % SB;
-            if (sub == 0) bd = bstage[sb];  // b_full was observed by the dequant warps before a_full
+            if (sub == 0) bd = bstage0 + (uint64_t)((uint32_t)(sb * B_STAGE) >> 4);  // b_full was observed by the dequant warps before a_full
 #pragma unroll
             for (int kk = 0; kk < KC / 16; ++kk)
               mma_bf16_ta(acc + m * PT, a_st + (c * C::NMAT + m) * 32 + 8 * kk, bd + 2 * kk, idesc, (kc | kk) != 0);
