@@ -492,6 +492,7 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_gateup(Gv2Params Q) {
   extern __shared__ __align__(16) uint8_t sm[];
   uint8_t* ring = sm;
   constexpr int ST = GV2_RING / (2 * GV_QB);  // 8 stages of one gate+up block pair
+  static_assert(ST <= 32, "stage bit masks");
   __shared__ uint64_t full[ST], empty[ST];
   __shared__ int s_e, abort_flag;
   __shared__ Gv2Rows<NB> R;
@@ -536,10 +537,7 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_gateup(Gv2Params Q) {
   if (warp == GV2_CONS / 32) {
     // no copy under the MOE_STALL_WEIGHT_COPIES test hook: the consumers' waits run out
     if (lane == 0 && !(P.status && (P.status->stall & MOE_STALL_WEIGHT_COPIES))) {
-      bool armed[ST];
-      uint32_t par[ST];
-#pragma unroll
-      for (int i = 0; i < ST; ++i) armed[i] = false, par[i] = 0;
+      uint32_t armed = 0, par = 0;  // per stage: copy issued, its phase parity (bit masks, not local memory)
       for (int i = 0; i < nkc; ++i) {
         const int s = i % ST;
         if (!mbar_wait(&empty[s], ((i / ST) & 1) ^ 1, abort, GV2_WAIT_NS)) {
@@ -548,14 +546,14 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_gateup(Gv2Params Q) {
         }
         mbar_arrive_expect_tx(&full[s], 2 * GV_QB);
         bulk_copy_g2s(ring + s * 2 * GV_QB, src + (size_t)i * 2 * GV_QB, 2 * GV_QB, &full[s]);
-        armed[s] = true;
-        par[s] = (i / ST) & 1;
+        armed |= 1u << s;
+        par = (par & ~(1u << s)) | (((i / ST) & 1u) << s);
       }
       if (*abort)
         for (int i = 0; i < ST; ++i)
-          if (armed[i]) {
+          if ((armed >> i) & 1u) {
             const int never = 0;
-            mbar_wait(&full[i], par[i], &never, 100000000ull);
+            mbar_wait(&full[i], (par >> i) & 1u, &never, 100000000ull);
           }
     }
   } else {
@@ -680,6 +678,7 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_down(Gv2Params Q) {
   extern __shared__ __align__(16) uint8_t sm[];
   uint8_t* ring = sm;
   constexpr int ST = GV2_RING / GV_QB;  // 16 stages of one block
+  static_assert(ST <= 32, "stage bit masks");
   __shared__ uint64_t full[ST], empty[ST];
   __shared__ int s_e, abort_flag;
   __shared__ Gv2Rows<NB> R;
@@ -715,10 +714,7 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_down(Gv2Params Q) {
     if (warp == GV2_CONS / 32) {
       // no copy under the MOE_STALL_WEIGHT_COPIES test hook: the consumers' waits run out
       if (lane == 0 && !(P.status && (P.status->stall & MOE_STALL_WEIGHT_COPIES))) {
-        bool armed[ST];
-        uint32_t par[ST];
-#pragma unroll
-        for (int i = 0; i < ST; ++i) armed[i] = false, par[i] = 0;
+        uint32_t armed = 0, par = 0;  // per stage: copy issued, its phase parity (bit masks, not local memory)
         for (int i = 0; i < nkc; ++i) {
           const int s = i % ST;
           if (!mbar_wait(&empty[s], ((i / ST) & 1) ^ 1, abort, GV2_WAIT_NS)) {
@@ -727,14 +723,14 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_down(Gv2Params Q) {
           }
           mbar_arrive_expect_tx(&full[s], GV_QB);
           bulk_copy_g2s(ring + s * GV_QB, src + (size_t)i * GV_QB, GV_QB, &full[s]);
-          armed[s] = true;
-          par[s] = (i / ST) & 1;
+          armed |= 1u << s;
+          par = (par & ~(1u << s)) | (((i / ST) & 1u) << s);
         }
         if (*abort)
           for (int i = 0; i < ST; ++i)
-            if (armed[i]) {
+            if ((armed >> i) & 1u) {
               const int never = 0;
-              mbar_wait(&full[i], par[i], &never, 100000000ull);
+              mbar_wait(&full[i], (par >> i) & 1u, &never, 100000000ull);
             }
       }
     } else {

@@ -149,6 +149,7 @@ struct PCfg {
   static constexpr bool ACC_SPLIT = MODE == MODE_DN2;
   static_assert(SA >= 2, "the A ring needs a stage per dequantisation group");
   static_assert(SB >= 2 && B_STAGE % 1024 == 0, "token-tile ring");
+  static_assert(SB <= 32 && SC <= 32, "stage bit masks");
 };
 
 __host__ __device__ inline size_t gu_bytes(int h, int I, int bits = 4) {

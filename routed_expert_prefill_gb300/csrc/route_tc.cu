@@ -112,10 +112,7 @@ route_score_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant
     if (lane == 0) {
       prefetch_tmap(&tx);
       prefetch_tmap(&tw);
-      bool armed[RS_STAGES];
-      uint32_t par[RS_STAGES];
-#pragma unroll
-      for (int i = 0; i < RS_STAGES; ++i) armed[i] = false, par[i] = 0;
+      uint32_t armed = 0, par = 0;  // per stage: copy issued, its phase parity (bit masks, not local memory)
       for (int i = 0; i < nkc; ++i) {
         const int s = i % RS_STAGES;
         if (!mbar_wait(&empty[s], ((i / RS_STAGES) & 1) ^ 1, abort, RS_WAIT_NS)) {
@@ -126,12 +123,12 @@ route_score_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant
         mbar_arrive_expect_tx(&full[s], st_bytes);
         tma_load_2d(sa, &tx, (kc0 + i) * RS_KC, row0, &full[s]);
         tma_load_2d(sa + RS_A_BYTES, &tw, (kc0 + i) * RS_KC, e0, &full[s]);
-        armed[s] = true;
-        par[s] = (i / RS_STAGES) & 1;
+        armed |= 1u << s;
+        par = (par & ~(1u << s)) | (((i / RS_STAGES) & 1u) << s);
       }
       if (*abort)
         for (int i = 0; i < RS_STAGES; ++i)
-          if (armed[i]) rs_drain_wait(&full[i], par[i]);
+          if ((armed >> i) & 1u) rs_drain_wait(&full[i], (par >> i) & 1u);
     }
   } else if (warp == 1) {
     if (lane == 0) {
