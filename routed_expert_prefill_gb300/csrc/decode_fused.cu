@@ -432,7 +432,8 @@ __global__ void __launch_bounds__(D_THREADS, 1) decode_fused_kernel(DfParams P) 
         const uint4 c1 = reinterpret_cast<const uint4*>(bm + o * 32)[1];
         const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
         uint32_t r[32];
-        dequant_packed<8>(wd, __halves2bfloat162(sv, sv), __halves2bfloat162(bv, bv), r);
+        // weights times 2^-24 (subnormal form); the drains multiply it out
+        dequant_packed_sub<8>(wd, __halves2bfloat162(sv, sv), __halves2bfloat162(bv, bv), r);
         tmem_st<32>(lane_base + as * 64 + m * 32, r);
       }
       tmem_st_wait();
@@ -690,8 +691,8 @@ __global__ void __launch_bounds__(D_THREADS, 1) decode_fused_kernel(DfParams P) 
 #pragma unroll
           for (int j = 0; j < D_MAX_T; ++j)
             if (j == r) gval = __uint_as_float(gv[j]), uval = __uint_as_float(uv[j]);
-          atomicAdd(gb + (size_t)(2 * n) * P.imax + f, gval);
-          atomicAdd(gb + (size_t)(2 * n + 1) * P.imax + f, uval);
+          atomicAdd(gb + (size_t)(2 * n) * P.imax + f, gval * 0x1p24f);  // the weights' 2^-24 out (exact)
+          atomicAdd(gb + (size_t)(2 * n + 1) * P.imax + f, uval * 0x1p24f);
         }
         __threadfence();
         if (!esync()) {
@@ -758,7 +759,7 @@ __global__ void __launch_bounds__(D_THREADS, 1) decode_fused_kernel(DfParams P) 
               r = S.rows[row0 + n];
               wt = S.wts[row0 + n];
             }
-            atomicAdd(P.acc + (size_t)r * h + col, wt * __uint_as_float(yv[n]));
+            atomicAdd(P.acc + (size_t)r * h + col, (wt * 0x1p24f) * __uint_as_float(yv[n]));  // 2^-24 out
           }
         }
         if (etid == 0) S.htcnt[it.tile] += seg_n;

@@ -349,18 +349,12 @@ __device__ __forceinline__ void down_cols16(const uint32_t (&y)[16], const float
 }
 
 // Dequantise one row of a packed block (64 K) into 32 bf16 pairs in K order.
-// The in-word layouts are those of pack_kernel.
-//
-// A code's bits, masked in place and read as a bf16 number, are a subnormal
-// (or, from 128 to 255, a number of the smallest normal binade); either way
-// the bf16 number with bits r has the value r * 2^-133 exactly.  So
-//   fma(r, s * 2^109, b * 2^-24) = (q s + b) * 2^-24, rounded once,
-// the same rounding as fma(q, s, b) scaled by a power of two (exact while
-// the result stays normal, |q s + b| >= 2^-102), with neither a magic
-// exponent nor a subtraction.  A code masked 4 bits up reads as 16 q and
-// takes s * 2^109 / 16, so one shift serves four pairs.  The accumulators
-// then carry the factor 2^-24, which the epilogues multiply out (exact).
-// s * 2^109 stays finite for every fp16 scale (< 2^16).
+// The in-word layouts are those of pack_kernel.  Every width uses the
+// subnormal form of dequant_packed_sub: the code's bits read as a bf16
+// number of value r * 2^-133 times s * 2^109, plus b * 2^-24, rounded once,
+// which is (q s + b) * 2^-24; a code masked 2, 4 or 6 bits up reads as 4 q,
+// 16 q or 64 q and takes the scale divided by that.  The accumulators then
+// carry the factor 2^-24, which the epilogues multiply out (exact).
 constexpr float DQ_SCALE_UP = 0x1p109f, DQ_BIAS_DOWN = 0x1p-24f, ACC_UP = 0x1p24f;
 
 template <int BITS>
@@ -373,15 +367,7 @@ __device__ __forceinline__ void dequant_bits(const uint32_t* w, __nv_bfloat162 s
   };
   if constexpr (BITS == 4) {
     // word j: pairs (K 8j + 2i, K 8j + 2i + 1) at (w >> 4i) & 0x000F000F
-    const __nv_bfloat162 s16 = __hmul2(sA, __float2bfloat162_rn(0.0625f));
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t lo = w[j], hi = w[j] >> 8;
-      out[4 * j + 0] = fma_raw(lo & 0x000F000Fu, sA);
-      out[4 * j + 1] = fma_raw(lo & 0x00F000F0u, s16);
-      out[4 * j + 2] = fma_raw(hi & 0x000F000Fu, sA);
-      out[4 * j + 3] = fma_raw(hi & 0x00F000F0u, s16);
-    }
+    dequant_packed_sub<8>(w, s2, b2, out);
   } else if constexpr (BITS == 2) {
     // word j: pairs (K 16j + 2i, K 16j + 2i + 1) at (w >> 2i) & 0x00030003
     __nv_bfloat162 sc[4];

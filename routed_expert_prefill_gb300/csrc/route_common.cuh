@@ -44,11 +44,12 @@ __device__ __forceinline__ void warp_topk_softmax(uint64_t (&key)[NQ], int k, in
       my_e = e;
       my_l = key_float(hi);
     }
-    if ((e & 31) == lane) {
+    // the chosen key leaves the set: a select on every word (a conditional
+    // store here would be turned back into an indexed store, which puts
+    // the whole array in local memory)
+    const int qe = (e & 31) == lane ? (e >> 5) : -1;
 #pragma unroll
-      for (int q = 0; q < NQ; ++q)
-        if (q == (e >> 5)) key[q] = 0ull;
-    }
+    for (int q = 0; q < NQ; ++q) key[q] = q == qe ? 0ull : key[q];
   }
   const float l0 = __shfl_sync(0xFFFFFFFFu, my_l, 0);
   const float p = lane < k ? expf(my_l - l0) : 0.f;

@@ -226,6 +226,35 @@ __device__ __forceinline__ void dequant_packed(const uint32_t* w, __nv_bfloat162
   }
 }
 
+// The same pairs dequantised to (q s + b) * 2^-24, the single rounding of
+// fma(q, s, b) scaled by a power of two: a code's bits masked in place and
+// read as a bf16 number are a subnormal of value r * 2^-133 (r < 128) or a
+// number of the smallest normal binade of the same value (r < 256), so
+// fma(r, s * 2^109, b * 2^-24) needs neither a magic exponent nor a
+// subtraction, and a code 4 bits up (r = 16 q) takes s * 2^109 / 16: one
+// shift serves four pairs.  The result stays exact up to that scaling while
+// |q s + b| >= 2^-102; products with it carry 2^-24, which the caller
+// multiplies out.  s * 2^109 is finite for every fp16 scale.
+template <int NW>
+__device__ __forceinline__ void dequant_packed_sub(const uint32_t* w, __nv_bfloat162 s2, __nv_bfloat162 b2,
+                                                   uint32_t* out) {
+  const __nv_bfloat162 sA = __hmul2(s2, __float2bfloat162_rn(0x1p109f));
+  const __nv_bfloat162 s16 = __hmul2(sA, __float2bfloat162_rn(0.0625f));
+  const __nv_bfloat162 bb = __hmul2(b2, __float2bfloat162_rn(0x1p-24f));
+  auto fma_raw = [&](uint32_t raw, __nv_bfloat162 sc) {
+    const __nv_bfloat162 r = __hfma2(*reinterpret_cast<const __nv_bfloat162*>(&raw), sc, bb);
+    return *reinterpret_cast<const uint32_t*>(&r);
+  };
+#pragma unroll
+  for (int j = 0; j < NW; ++j) {
+    const uint32_t lo = w[j], hi = w[j] >> 8;
+    out[4 * j + 0] = fma_raw(lo & 0x000F000Fu, sA);
+    out[4 * j + 1] = fma_raw(lo & 0x00F000F0u, s16);
+    out[4 * j + 2] = fma_raw(hi & 0x000F000Fu, sA);
+    out[4 * j + 3] = fma_raw(hi & 0x00F000F0u, s16);
+  }
+}
+
 // Byte offset of the 16-byte chunk c (0..7) of row r in a 128B-swizzled tile.
 __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c) {
   return (r >> 3) * 1024u + (r & 7u) * 128u + ((c ^ (r & 7u)) << 4);
