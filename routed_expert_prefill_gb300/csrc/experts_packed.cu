@@ -641,60 +641,71 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     // so the two streams are independent and each commit barrier counts
     // both; down: W_MMA alone (one accumulator, one fixed order).
     const int m = warp == W_MMA ? 0 : 1;
-    if (lane == 0 && (PAIRED || warp == W_MMA)) {
+    // The whole warp walks the loop (its waits and bookkeeping stay
+    // warp-uniform) and one elected lane issues: the same lane every time,
+    // so its commits track its own MMAs.  Issued this way an MMA costs
+    // about half the cycles of a lone lane-0 loop.
+    if (PAIRED || warp == W_MMA) {
       // descriptor of token stage 0; stage sb's differs by its offset in
       // the start-address field (16-byte units; shared memory < 256 KB
       // keeps the field from overflowing), computed rather than looked up
       // in a per-thread table, which would live in local memory
       const uint64_t bstage0 = desc_sw128(smem_u32(b_s));
       uint32_t ast = 0, bit = 0, uit = 0;
-      for (int u = unit0; u < n_units && !*abort; u += ustride, ++uit) {
+      for (int u = unit0; u < n_units && !__any_sync(0xFFFFFFFFu, *abort); u += ustride, ++uit) {
         const PUnit U = decode_punit<MODE, CP, C::B_STAGE>(p, u);
         const uint32_t idesc = idesc_bf16(128, U.Nm);
         const uint32_t nm8 = (uint32_t)(U.Nm * 128) >> 4;  // descriptor step of one K chunk
         const int ab = uit % C::NACC;
         const int ai = C::ACC_SPLIT ? m : ab;  // accumulator barrier
-        if (!mbar_wait(&S.acc_empty[ai], ((uit / C::NACC) & 1) ^ 1, abort, WAIT_NS)) {
-          note_timeout(p.status, abort, GATEUP ? 33 : 43);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.acc_empty[ai], ((uit / C::NACC) & 1) ^ 1, abort, WAIT_NS))) {
+          if (lane == 0) note_timeout(p.status, abort, GATEUP ? 33 : 43);
           break;
         }
-        tc_fence_after();
         const uint32_t acc = tmem + ab * C::ACC_COLS;
         bool ok = true;
         int sub = 0;
         uint64_t bd = 0;
-        for (int st = 0; st < U.nkc / CPS && ok; ++st, ++ast) {
+        for (int st = 0; st < U.nkc / CPS; ++st, ++ast) {
           const int sa = ast % C::SA;
-          if (!mbar_wait(&S.a_full[sa], (ast / C::SA) & 1, abort, WAIT_NS)) {
-            note_timeout(p.status, abort, GATEUP ? 35 : 45);
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.a_full[sa], (ast / C::SA) & 1, abort, WAIT_NS))) {
+            if (lane == 0) note_timeout(p.status, abort, GATEUP ? 35 : 45);
             ok = false;
             break;
           }
-          tc_fence_after();
           const uint32_t a_st = tmem + C::A_COL + sa * C::A_STAGE;
+          const bool leader = elect_one();
+          if (leader) tc_fence_after();
 #pragma unroll
           for (int c = 0; c < CPS; ++c) {
             const int kc = st * CPS + c;
             const int sb = bit % SB;
             if (sub == 0) bd = bstage0 + (uint64_t)((uint32_t)(sb * B_STAGE) >> 4);  // b_full was observed by the dequant warps before a_full
+            if (leader) {
 #pragma unroll
-            for (int kk = 0; kk < KC / 16; ++kk)
-              mma_bf16_ta(acc + m * PT, a_st + (c * C::NMAT + m) * 32 + 8 * kk, bd + 2 * kk, idesc, (kc | kk) != 0);
-            if constexpr (C::BLK_REL) mma_commit(&S.a_empty[sa][c * C::NMAT + m]);
+              for (int kk = 0; kk < KC / 16; ++kk)
+                mma_bf16_ta(acc + m * PT, a_st + (c * C::NMAT + m) * 32 + 8 * kk, bd + 2 * kk, idesc, (kc | kk) != 0);
+              if constexpr (C::BLK_REL) mma_commit(&S.a_empty[sa][c * C::NMAT + m]);
+            }
             bd += nm8;
             if (++sub == U.kps || kc == U.nkc - 1) {
-              mma_commit(&S.b_empty[sb]);
+              if (leader) mma_commit(&S.b_empty[sb]);
               ++bit;
               sub = 0;
             }
           }
-          if constexpr (!C::BLK_REL) mma_commit(&S.a_empty[sa][0]);
+          if constexpr (!C::BLK_REL) {
+            if (leader) mma_commit(&S.a_empty[sa][0]);
+          }
+          __syncwarp();
         }
         if (!ok) break;
-        mma_commit(&S.acc_full[ai]);
+        if (elect_one()) mma_commit(&S.acc_full[ai]);
+        __syncwarp();
       }
-      if (*abort) {
-        mma_commit(&S.drain[m]);
+      if (__any_sync(0xFFFFFFFFu, *abort)) {
+        if (elect_one()) mma_commit(&S.drain[m]);
+        __syncwarp();
         drain_wait(&S.drain[m], 0);
       }
     }
