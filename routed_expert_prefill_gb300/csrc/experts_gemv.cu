@@ -536,20 +536,24 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_gateup(Gv2Params Q) {
   // meanwhile stage the token rows (L2 reads) and meet at a named barrier.
   if (warp == GV2_CONS / 32) {
     // no copy under the MOE_STALL_WEIGHT_COPIES test hook: the consumers' waits run out
-    if (lane == 0 && !(P.status && (P.status->stall & MOE_STALL_WEIGHT_COPIES))) {
+    // the whole warp walks the loop, one elected lane issues the copies
+    if (!(P.status && (P.status->stall & MOE_STALL_WEIGHT_COPIES))) {
       uint32_t armed = 0, par = 0;  // per stage: copy issued, its phase parity (bit masks, not local memory)
       for (int i = 0; i < nkc; ++i) {
         const int s = i % ST;
-        if (!mbar_wait(&empty[s], ((i / ST) & 1) ^ 1, abort, GV2_WAIT_NS)) {
-          gv2_timeout(P.status, abort, 61);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&empty[s], ((i / ST) & 1) ^ 1, abort, GV2_WAIT_NS))) {
+          if (lane == 0) gv2_timeout(P.status, abort, 61);
           break;
         }
-        mbar_arrive_expect_tx(&full[s], 2 * GV_QB);
-        bulk_copy_g2s(ring + s * 2 * GV_QB, src + (size_t)i * 2 * GV_QB, 2 * GV_QB, &full[s]);
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&full[s], 2 * GV_QB);
+          bulk_copy_g2s(ring + s * 2 * GV_QB, src + (size_t)i * 2 * GV_QB, 2 * GV_QB, &full[s]);
+        }
+        __syncwarp();
         armed |= 1u << s;
         par = (par & ~(1u << s)) | (((i / ST) & 1u) << s);
       }
-      if (*abort)
+      if (__any_sync(0xFFFFFFFFu, *abort))
         for (int i = 0; i < ST; ++i)
           if ((armed >> i) & 1u) {
             const int never = 0;
@@ -713,20 +717,24 @@ __global__ void __launch_bounds__(GV2_THREADS, 1) gv2_down(Gv2Params Q) {
     // barrier.
     if (warp == GV2_CONS / 32) {
       // no copy under the MOE_STALL_WEIGHT_COPIES test hook: the consumers' waits run out
-      if (lane == 0 && !(P.status && (P.status->stall & MOE_STALL_WEIGHT_COPIES))) {
+      // the whole warp walks the loop, one elected lane issues the copies
+      if (!(P.status && (P.status->stall & MOE_STALL_WEIGHT_COPIES))) {
         uint32_t armed = 0, par = 0;  // per stage: copy issued, its phase parity (bit masks, not local memory)
         for (int i = 0; i < nkc; ++i) {
           const int s = i % ST;
-          if (!mbar_wait(&empty[s], ((i / ST) & 1) ^ 1, abort, GV2_WAIT_NS)) {
-            gv2_timeout(P.status, abort, 63);
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(&empty[s], ((i / ST) & 1) ^ 1, abort, GV2_WAIT_NS))) {
+            if (lane == 0) gv2_timeout(P.status, abort, 63);
             break;
           }
-          mbar_arrive_expect_tx(&full[s], GV_QB);
-          bulk_copy_g2s(ring + s * GV_QB, src + (size_t)i * GV_QB, GV_QB, &full[s]);
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&full[s], GV_QB);
+            bulk_copy_g2s(ring + s * GV_QB, src + (size_t)i * GV_QB, GV_QB, &full[s]);
+          }
+          __syncwarp();
           armed |= 1u << s;
           par = (par & ~(1u << s)) | (((i / ST) & 1u) << s);
         }
-        if (*abort)
+        if (__any_sync(0xFFFFFFFFu, *abort))
           for (int i = 0; i < ST; ++i)
             if ((armed >> i) & 1u) {
               const int never = 0;

@@ -552,8 +552,10 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
 
   if (warp == W_CODE) {
     // ------------------------------------------------------------ packed weight blocks, CPS chunks per copy
-    // (none under the MOE_STALL_WEIGHT_COPIES test hook: the consumers' waits run out)
-    if (lane == 0 && !(p.status && (p.status->stall & MOE_STALL_WEIGHT_COPIES))) {
+    // (none under the MOE_STALL_WEIGHT_COPIES test hook: the consumers' waits run out).
+    // Like the MMA issuers, the producers walk their loops as a whole warp
+    // and one elected lane issues the copies.
+    if (!(p.status && (p.status->stall & MOE_STALL_WEIGHT_COPIES))) {
       uint32_t it = 0;
       // stages with a copy issued, and the phase parity each was armed for
       // (bit masks: a per-thread array indexed by the stage would live in
@@ -578,34 +580,37 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         const uint8_t* src = unit_codes(u, nst);
         for (int st = 0; st < nst; ++st, ++it) {
           const int sc = it % C::SC;
-          if (!mbar_wait(&S.code_empty[sc], ((it / C::SC) & 1) ^ 1, abort, WAIT_NS)) {
-            note_timeout(p.status, abort, GATEUP ? 31 : 41);
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.code_empty[sc], ((it / C::SC) & 1) ^ 1, abort, WAIT_NS))) {
+            if (lane == 0) note_timeout(p.status, abort, GATEUP ? 31 : 41);
             stop = true;
             break;
           }
-          mbar_arrive_expect_tx(&S.code_full[sc], C::C_STAGE);
-          if constexpr (MODE == MODE_DN2) {
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&S.code_full[sc], C::C_STAGE);
+            if constexpr (MODE == MODE_DN2) {
 #pragma unroll
-            for (int c = 0; c < CPS; ++c)
+              for (int c = 0; c < CPS; ++c)
 #pragma unroll
-              for (int m = 0; m < 2; ++m)
-                bulk_load(c_s + sc * C::C_STAGE + (c * 2 + m) * QB, src + m * m2 + (size_t)(st * CPS + c) * QB, QB,
-                          &S.code_full[sc]);
-          } else {
-            bulk_load(c_s + sc * C::C_STAGE, src + (size_t)st * C::C_STAGE, C::C_STAGE, &S.code_full[sc]);
+                for (int m = 0; m < 2; ++m)
+                  bulk_load(c_s + sc * C::C_STAGE + (c * 2 + m) * QB, src + m * m2 + (size_t)(st * CPS + c) * QB, QB,
+                            &S.code_full[sc]);
+            } else {
+              bulk_load(c_s + sc * C::C_STAGE, src + (size_t)st * C::C_STAGE, C::C_STAGE, &S.code_full[sc]);
+            }
           }
+          __syncwarp();
           armed |= 1u << sc;
           par = (par & ~(1u << sc)) | (((it / C::SC) & 1u) << sc);
         }
-        if (*abort) stop = true;
+        if (__any_sync(0xFFFFFFFFu, *abort)) stop = true;
       }
-      if (*abort)
+      if (__any_sync(0xFFFFFFFFu, *abort))
         for (int i = 0; i < C::SC; ++i)
           if ((armed >> i) & 1u) drain_wait(&S.code_full[i], (par >> i) & 1u);
     }
   } else if (warp == W_B) {
     // ------------------------------------------------------------ token images
-    if (lane == 0) {
+    {
       uint32_t it = 0;
       uint32_t armed = 0, par = 0;  // as for the code stages
       bool stop = false;
@@ -615,20 +620,23 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
                                     : reinterpret_cast<const uint8_t*>(p.hg + (size_t)U.pad * P.kmax);
         for (int kc0 = 0; kc0 < U.nkc; kc0 += U.kps, ++it) {
           const int sb = it % SB;
-          if (!mbar_wait(&S.b_empty[sb], ((it / SB) & 1) ^ 1, abort, WAIT_NS)) {
-            note_timeout(p.status, abort, GATEUP ? 32 : 42);
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.b_empty[sb], ((it / SB) & 1) ^ 1, abort, WAIT_NS))) {
+            if (lane == 0) note_timeout(p.status, abort, GATEUP ? 32 : 42);
             stop = true;
             break;
           }
           const uint32_t bytes = (uint32_t)(min(U.kps, U.nkc - kc0) * U.Nm * 128);
-          mbar_arrive_expect_tx(&S.b_full[sb], bytes);
-          bulk_load(b_s + sb * B_STAGE, src + (size_t)kc0 * U.Nm * 128, bytes, &S.b_full[sb]);
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&S.b_full[sb], bytes);
+            bulk_load(b_s + sb * B_STAGE, src + (size_t)kc0 * U.Nm * 128, bytes, &S.b_full[sb]);
+          }
+          __syncwarp();
           armed |= 1u << sb;
           par = (par & ~(1u << sb)) | (((it / SB) & 1u) << sb);
         }
-        if (*abort) stop = true;
+        if (__any_sync(0xFFFFFFFFu, *abort)) stop = true;
       }
-      if (*abort)
+      if (__any_sync(0xFFFFFFFFu, *abort))
         for (int i = 0; i < SB; ++i)
           if ((armed >> i) & 1u) drain_wait(&S.b_full[i], (par >> i) & 1u);
     }

@@ -131,16 +131,18 @@ route_score_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant
           if ((armed >> i) & 1u) rs_drain_wait(&full[i], (par >> i) & 1u);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(128, NT);
-      bool ok = true;
-      for (int i = 0; i < nkc; ++i) {
-        const int s = i % RS_STAGES;
-        if (!mbar_wait(&full[s], (i / RS_STAGES) & 1, abort, RS_WAIT_NS)) {
-          rs_timeout(P.st, abort, 52);
-          ok = false;
-          break;
-        }
+    // MMA issuer: the whole warp walks the loop, one elected lane (the same
+    // one every time, so the commits track its MMAs) issues
+    const uint32_t idesc = idesc_bf16(128, NT);
+    bool ok = true;
+    for (int i = 0; i < nkc; ++i) {
+      const int s = i % RS_STAGES;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], (i / RS_STAGES) & 1, abort, RS_WAIT_NS))) {
+        if (lane == 0) rs_timeout(P.st, abort, 52);
+        ok = false;
+        break;
+      }
+      if (elect_one()) {
         tc_fence_after();
         const uint32_t sa = smem_u32(base + s * st_bytes);
         const uint64_t ad = desc_sw128(sa), bd = desc_sw128(sa + RS_A_BYTES);
@@ -148,13 +150,11 @@ route_score_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant
         for (int kk = 0; kk < RS_KC / 16; ++kk) mma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (i | kk) != 0);
         mma_commit(&empty[s]);
       }
-      if (ok) {
-        mma_commit(&accf);
-      } else {
-        mma_commit(&drain);
-        rs_drain_wait(&drain, 0);
-      }
+      __syncwarp();
     }
+    if (elect_one()) mma_commit(ok ? &accf : &drain);
+    __syncwarp();
+    if (!ok) rs_drain_wait(&drain, 0);
   } else {
     // Squared norms of this column's router rows, spread over the CTAs that
     // share the column (rows r = 4 * li + ew, stepping by 4 * nl).
