@@ -801,19 +801,17 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         // the a_full of the first A stage it serves completes.  Later A
         // stages of the same B stage are ordered after that observation by
         // the issuer's own earlier wait, so only the first one checks.
-        if (b_first) {
-          bool b_ok = true;
-          if (lane == 0 && !mbar_test(&S.b_full[bst % SB], (bst / SB) & 1))
-            b_ok = mbar_wait(&S.b_full[bst % SB], (bst / SB) & 1, abort, WAIT_NS);
-          b_ok = __shfl_sync(0xFFFFFFFFu, b_ok, 0);
-          if (!b_ok) {
+        if (b_first) {  // warp-uniform: every lane tests, waits only if it has not landed
+          uint64_t* bf = &S.b_full[bst % SB];
+          const uint32_t bpar = (bst / SB) & 1;
+          if (!__all_sync(0xFFFFFFFFu, mbar_test(bf, bpar) || mbar_wait(bf, bpar, abort, WAIT_NS))) {
             if (lane == 0) note_timeout(p.status, abort, GATEUP ? 34 : 44);
             ok = false;
             break;
           }
         }
-        __syncwarp();
-        if (lane == 0) {
+        __syncwarp();  // every lane's stores and fence are done
+        if (elect_one()) {
           mbar_arrive(&S.a_full[sa]);
           mbar_arrive(&S.code_empty[sc]);
         }
