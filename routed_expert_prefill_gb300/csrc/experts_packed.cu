@@ -1018,14 +1018,14 @@ cudaError_t launch_packed_gemms(const PParams& P, cudaStream_t stream) {
   constexpr int GU_CP = PT > 128 ? 1 : CPS_DEFAULT;
   cudaError_t err = launch_packed_gemm<MODE_GU, PT, GU_CP, BITS>(P, stream);
   if (err != cudaSuccess) return err;
-  // down on tiles of 128 rows or more and a long inner dimension: two output
-  // tiles per unit (the token image is read once for both), staged like
-  // gate/up.  Its accumulators then take the TMEM of the double buffer, so
-  // each unit's drain is exposed: with inter 768 that cost more than the
-  // halved ingest saved (t4096 skewed: 150 -> 162 us), with 1536 less (t4096
-  // h4096: 517 -> 499 us).
+  // down on tiles of 128 rows or more and an inner dimension of 512 or
+  // more: two output tiles per unit (the token image is read once for both),
+  // staged like gate/up.  Its accumulators then take the TMEM of the double
+  // buffer, so part of each unit's drain is exposed; the halved ingest pays
+  // for it from inter 768 on (t4096 skewed: 133 -> 127 us; t4096 h4096:
+  // 517 -> 499 us when it was introduced).
   if constexpr (PT >= 128)
-    if (P.p.h % 256 == 0 && max(P.p.I, P.p.Is) >= 1024)
+    if (P.p.h % 256 == 0 && max(P.p.I, P.p.Is) >= 512)
       return launch_packed_gemm<MODE_DN2, PT, GU_CP, BITS>(P, stream);
   if constexpr (PT <= 128 && BITS <= 4)
     if (P.p.I % 256 == 0 && P.p.Is % 256 == 0) return launch_packed_gemm<MODE_DN, PT, 4, BITS>(P, stream);
