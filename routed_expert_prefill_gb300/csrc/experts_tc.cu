@@ -403,10 +403,7 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
       prefetch_tmap(&tm_codes);
       if (p.Is > 0) prefetch_tmap(&tm_scodes);
       uint32_t it = 0;
-      bool armed[C::SC];
-      uint32_t par[C::SC];
-#pragma unroll
-      for (int i = 0; i < C::SC; ++i) armed[i] = false, par[i] = 0;
+      uint32_t armed = 0, par = 0;  // per stage: copy issued, its phase parity (bit masks, not local memory)
       bool stop = false;
       for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
         const Unit U = decode_unit<GATEUP>(p, u);
@@ -427,14 +424,14 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
           for (int m = 0; m < C::NMAT; ++m)
             tma_load_2d(c_s + sc * C::C_STAGE + m * 128 * C::CPS * 32, tm, kc0 * 32, row0 + m * mstride,
                         &S.code_full[sc]);
-          armed[sc] = true;
-          par[sc] = (it / C::SC) & 1;
+          armed |= 1u << sc;
+          par = (par & ~(1u << sc)) | (((it / C::SC) & 1u) << sc);
         }
         if (*abort) stop = true;
       }
       if (*abort)
         for (int i = 0; i < C::SC; ++i)
-          if (armed[i]) drain_wait(&S.code_full[i], par[i]);
+          if ((armed >> i) & 1u) drain_wait(&S.code_full[i], (par >> i) & 1u);
     }
   } else if (warp == W_B) {
     // ------------------------------------------------------------ B producer
@@ -443,10 +440,7 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
       if (p.Is > 0) prefetch_tmap(&tm_sb);
     }
     uint32_t it = 0;
-    bool armed[SB];
-    uint32_t par[SB];
-#pragma unroll
-    for (int i = 0; i < SB; ++i) armed[i] = false, par[i] = 0;
+    uint32_t armed = 0, par = 0;  // as for the code stages
     for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
       const Unit U = decode_unit<GATEUP>(p, u);
       if (GATEUP) {
@@ -479,63 +473,68 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
                 tma_load_2d(sub + g * 2048, tm, (kc0 + s) * KC, U.start + 16 * g, &S.b_full[sb]);
             }
           }
-          armed[sb] = true;
-          par[sb] = (it / SB) & 1;
+          armed |= 1u << sb;
+          par = (par & ~(1u << sb)) | (((it / SB) & 1u) << sb);
         }
       }
       __syncwarp();
     }
     if (lane == 0 && *abort)
       for (int i = 0; i < SB; ++i)
-        if (armed[i]) drain_wait(&S.b_full[i], par[i]);
+        if ((armed >> i) & 1u) drain_wait(&S.b_full[i], (par >> i) & 1u);
   } else if (warp == W_MMA) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp walks the loop and waits; one elected lane (the same
+    // lane every time, so its commits track its own MMAs) issues.
+    {
       uint32_t ait = 0, bit = 0, uit = 0;
-      for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++uit) {
+      for (int u = blockIdx.x; u < n_units && !__any_sync(0xFFFFFFFFu, *abort); u += gridDim.x, ++uit) {
         const Unit U = decode_unit<GATEUP>(p, u);
         const uint32_t idesc = idesc_bf16(128, U.Nm);
-        if (uit > 0 && !mbar_wait(&S.acc_empty, (uit - 1) & 1, abort, WAIT_NS)) {
-          note_timeout(p.status, abort, GATEUP ? 13 : 23);
+        if (uit > 0 && !__all_sync(0xFFFFFFFFu, mbar_wait(&S.acc_empty, (uit - 1) & 1, abort, WAIT_NS))) {
+          if (lane == 0) note_timeout(p.status, abort, GATEUP ? 13 : 23);
           break;
         }
-        tc_fence_after();
         bool ok = true;
-        for (int kc = 0; kc < U.nkc && ok; ++kc) {
+        for (int kc = 0; kc < U.nkc; ++kc) {
           const int sub = kc % U.kps;
           const int sb = bit % SB;
-          if (sub == 0 && !mbar_wait(&S.b_full[sb], (bit / SB) & 1, abort, WAIT_NS)) {
-            note_timeout(p.status, abort, GATEUP ? 14 : 24);
+          if (sub == 0 && !__all_sync(0xFFFFFFFFu, mbar_wait(&S.b_full[sb], (bit / SB) & 1, abort, WAIT_NS))) {
+            if (lane == 0) note_timeout(p.status, abort, GATEUP ? 14 : 24);
             ok = false;
             break;
           }
           const int sa = ait % SA;
-          if (!mbar_wait(&S.a_full[sa], (ait / SA) & 1, abort, WAIT_NS)) {
-            note_timeout(p.status, abort, GATEUP ? 15 : 25);
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.a_full[sa], (ait / SA) & 1, abort, WAIT_NS))) {
+            if (lane == 0) note_timeout(p.status, abort, GATEUP ? 15 : 25);
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint64_t bd = desc_sw128(smem_u32(b_s + sb * B_STAGE + sub * U.Nm * 128));
+          const bool last_of_b = sub == U.kps - 1 || kc == U.nkc - 1;
+          if (elect_one()) {
+            tc_fence_after();
+            const uint64_t bd = desc_sw128(smem_u32(b_s + sb * B_STAGE + sub * U.Nm * 128));
 #pragma unroll
-          for (int m = 0; m < C::NMAT; ++m) {
-            const uint64_t ad = desc_sw128(smem_u32(a_s + sa * C::A_STAGE + m * 128 * 128));
+            for (int m = 0; m < C::NMAT; ++m) {
+              const uint64_t ad = desc_sw128(smem_u32(a_s + sa * C::A_STAGE + m * 128 * 128));
 #pragma unroll
-            for (int kk = 0; kk < KC / 16; ++kk)
-              mma_bf16(tmem + m * 256, ad + 2 * kk, bd + 2 * kk, idesc, (kc | kk) != 0);
+              for (int kk = 0; kk < KC / 16; ++kk)
+                mma_bf16(tmem + m * 256, ad + 2 * kk, bd + 2 * kk, idesc, (kc | kk) != 0);
+            }
+            mma_commit(&S.a_empty[sa]);
+            if (last_of_b) mma_commit(&S.b_empty[sb]);
           }
-          mma_commit(&S.a_empty[sa]);
+          __syncwarp();
           ++ait;
-          if (sub == U.kps - 1 || kc == U.nkc - 1) {
-            mma_commit(&S.b_empty[sb]);
-            ++bit;
-          }
+          if (last_of_b) ++bit;
         }
         if (!ok) break;
-        mma_commit(&S.acc_full);
+        if (elect_one()) mma_commit(&S.acc_full);
+        __syncwarp();
       }
-      if (*abort) {
-        mma_commit(&S.drain);  // completes once every MMA issued so far has
+      if (__any_sync(0xFFFFFFFFu, *abort)) {
+        if (elect_one()) mma_commit(&S.drain);  // completes once every MMA issued so far has
+        __syncwarp();
         drain_wait(&S.drain, 0);
       }
     }
