@@ -339,13 +339,14 @@ def test_one_expert_takes_every_row_and_shared_gate(moe, flags):
 
 
 @pytest.mark.parametrize("t,E,tile", [(1000, 8, 160), (410, 10, 128)])
-@pytest.mark.parametrize("inter", [256, 1280])
+@pytest.mark.parametrize("inter", [256, 512, 768, 1280])
 @pytest.mark.parametrize("det", [False, True])
 def test_packed_large_tiles(moe, t, E, tile, inter, det):
     """Tiles of up to 160 rows (experts see 250 rows on average) and of up to
     128 rows (80 on average); a router bias sends every row to expert 0 first,
-    so it spans several tiles with a ragged last one.  Down runs two epilogue
-    warpgroups at inter 256 and one at 1280; gate/up two."""
+    so it spans several tiles with a ragged last one.  From inter 512 on the
+    down pass is the paired one (two output tiles per unit; 8, 12 and 20 K
+    chunks); at inter 256 one output tile per unit."""
     w = synth.Workload("tl", t, 256, inter, E, 2, 256, 41 + inter + t)
     inp = synth.make_inputs(w)
     inp["rbias"] = np.zeros(E, np.float32)
