@@ -120,13 +120,16 @@ struct PCfg {
   static constexpr int B_STAGE =
       PT > 128 ? CP * PT * 128 : (CP * PT * 128 > 32768 ? 65536 : 32768);
   static constexpr int EPI_BYTES = (GATEUP ? 1 : 8) * PT * 8 + 8 * (GATEUP ? 16 * 16 : 16 * 32) * 4;
-  // Code stages (as many as leave two token stages): twelve on gate/up and
+  // Code stages (as many as leave enough token stages): twelve on gate/up and
   // eight on the paired down pass and on 64-row tiles, where the weight
   // stream is what the stages wait for (at t4096 h4096 E256 against four:
   // gate/up 618 -> 601 us with eight, 598 with twelve; paired down 405 ->
   // 387 us with eight, 403 with twelve, its token ring then too short);
   // four on the single-matrix down pass with larger tiles.
-  static constexpr int SC_FIT = (SMEM_MAX - 2048 - EPI_BYTES - 2 * B_STAGE) / C_STAGE;
+  // (on tiles over 128 rows at least five token stages stay: with wider
+  // codes the code stages would otherwise leave the token ring too short)
+  static constexpr int SB_MIN = PT > 128 ? 5 : 2;
+  static constexpr int SC_FIT = (SMEM_MAX - 2048 - EPI_BYTES - SB_MIN * B_STAGE) / C_STAGE;
   static constexpr int SC_WANT = PT <= 64 ? 8 : GATEUP ? 12 : PAIRED ? 8 : 4;
   static constexpr int SC = SC_WANT < SC_FIT ? SC_WANT : (SC_FIT < 4 ? 4 : SC_FIT);
   static constexpr int SB_FIT = (SMEM_MAX - 1024 - SC * C_STAGE - EPI_BYTES - 1024) / B_STAGE;
