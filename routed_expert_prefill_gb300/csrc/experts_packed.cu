@@ -65,7 +65,6 @@ constexpr int KC = 64;      // K per chunk = one quantisation group
 // One packed 128 x 64 block at BITS bits per code: 128 rows of 8 * BITS
 // code bytes, then 128 bf16 scales and 128 bf16 biases.
 __host__ __device__ constexpr int qb_bytes(int bits) { return 1024 * bits + 512; }
-constexpr int QB = qb_bytes(4);  // the 4-bit block
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
 constexpr int W_CODE = 0, W_MMA = 1, W_DQ0 = 2, W_B = 10, W_EPI0 = 11, W_MMA2 = 15, W_EPI1 = 16;
@@ -76,6 +75,7 @@ constexpr int W_CODE = 0, W_MMA = 1, W_DQ0 = 2, W_B = 10, W_EPI0 = 11, W_MMA2 = 
 // (128-row tiles; for down, a short inter), and otherwise only takes issue
 // slots from the dequantisation warps.
 constexpr int KWARPS = 20;
+static_assert(W_EPI0 + 4 == W_MMA2 && W_MMA2 + 1 == W_EPI1 && W_EPI1 + 4 == KWARPS, "warp roles");
 constexpr int KTHREADS = KWARPS * 32;
 constexpr int KTHREADS_1 = 16 * 32;
 constexpr int SMEM_MAX = 232448;      // dynamic shared memory of one CTA (227 KB)
@@ -830,7 +830,6 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     const int q = warp & 3;
     const int half = warp >= W_EPI1 ? 1 : 0;
     const int ew = half * 4 + q;  // epilogue warp index: staging buffer, row copy
-    const int o = q * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t uit = 0;
     for (int u = unit0; u < n_units && !*abort; u += ustride, ++uit) {
