@@ -63,6 +63,33 @@ def test_step_work_counts():
     assert work["bytes"] >= 4 * rec  # three touched records and the shared one, plus activations
 
 
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
+def test_step_work_bytes_follow_the_code_width(bits):
+    """Weight bytes of the work model at each code width: bits/8 bytes per
+    weight plus a 2-byte scale and bias per 64 weights, for the touched
+    records and the shared one; flops do not depend on the width."""
+    w = synth.Workload("m", 4, 256, 128, 4, 2, 128, 1, bits=bits)
+    w4 = synth.Workload("m", 4, 256, 128, 4, 2, 128, 1)
+    counts = np.array([3, 0, 4, 1])
+    work, work4 = bench.step_work(w, counts), bench.step_work(w4, counts)
+    h, inter = 256, 128
+    per_weight = bits / 8 + 4 / 64
+    assert bench.record_bytes(h, inter, bits) == 3 * h * inter * per_weight
+    assert work["by_kernel"]["gateup"]["bytes"] - work4["by_kernel"]["gateup"]["bytes"] == (
+        (3 + 1) * 2 * h * inter * (bits - 4) // 8)
+    assert work["by_kernel"]["down"]["bytes"] - work4["by_kernel"]["down"]["bytes"] == (
+        (3 + 1) * h * inter * (bits - 4) // 8)
+    assert work["flops"] == work4["flops"]
+
+
+def test_low_bit_headline_workloads_exist():
+    for b in (2, 3, 8):
+        w = synth.WORKLOADS[f"t4096_h4096_e256_b{b}"]
+        base = synth.WORKLOADS["t4096_h4096_e256"]
+        assert w.bits == b and (w.t, w.h, w.inter, w.E, w.k, w.shared_inter, w.seed) == (
+            base.t, base.h, base.inter, base.E, base.k, base.shared_inter, base.seed)
+
+
 def test_job_throughput_and_single_rank_max():
     # every rank processes its own chunk: value = world * rows / max time
     assert bench.job_tokens_per_s(1, 512, 0.2) == pytest.approx(512 / 0.2e-3)
