@@ -42,7 +42,7 @@ constexpr uint64_t RS_WAIT_NS = 2000000000ull;
 constexpr int RS_TARGET_CTAS = 152;  // about one CTA per SM of a GB300
 constexpr int RS_KS_MAX = 4;         // K slices: each costs the refinement one more load per score
 constexpr int RF_WARPS = 8;  // 4 rows per CTA, two warps each
-constexpr int RF_NB = 4;  // exact logits computed together per warp
+constexpr int RF_NB = 2;  // exact logits computed together per warp (4 measured slower: fewer batches, but spills)
 
 struct ScoreParams {
   int t, h, E, Ep, NT, nkc_split;
