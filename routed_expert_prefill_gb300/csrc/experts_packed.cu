@@ -135,13 +135,12 @@ struct PCfg {
   static constexpr int SB_FIT = (SMEM_MAX - 1024 - SC * C_STAGE - EPI_BYTES - 1024) / B_STAGE;
   static constexpr int SB = SB_FIT > 16 ? 16 : SB_FIT;
   static constexpr int B_RING = SB * B_STAGE;
-  // A-ring slots released block by block (an empty barrier per block,
-  // committed after that block's MMAs) rather than per stage: lets a
-  // dequantisation group start rewriting a slot while the tensor pipe still
-  // reads its later blocks.  Pays for the extra waits and commits on the
-  // gate/up pass with tiles of 128 rows or more only.
-  static constexpr bool BLK_REL = PAIRED && PT >= 128;
-  static constexpr int NREL = BLK_REL ? CPS * NMAT : 1;  // empty barriers per slot
+  // A-ring slots are released per stage (one empty barrier each, committed
+  // by every issuer after the stage's MMAs).  Releasing them block by block,
+  // so that a group could rewrite a slot while the tensor pipe still read its
+  // later blocks, paid on the paired passes before their issue loops were
+  // warp-uniform; since then it costs more than it gains (gate/up 592 ->
+  // 584 us, paired down 385 -> 376 us without it at t4096 h4096 E256).
   // Paired down pass: each output tile's accumulator has its own full and
   // empty barriers, and the epilogue drains tile 0 first, so tile 0's
   // issuer starts the next unit while tile 1 is still drained (as far as
@@ -474,7 +473,7 @@ struct PSmem {
   using C = PCfg<MODE, PT, CP, BITS>;
   uint64_t code_full[C::SC], code_empty[C::SC];
   uint64_t a_full[C::SA];
-  uint64_t a_empty[C::SA][C::NREL];
+  uint64_t a_empty[C::SA];
   uint64_t b_full[C::SB], b_empty[C::SB];
   uint64_t acc_full[2], acc_empty[2];  // per buffer, or per matrix (ACC_SPLIT)
   uint64_t drain[2];
@@ -529,7 +528,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
     }
     for (int i = 0; i < C::SA; ++i) {
       mbar_init(&S.a_full[i], 4);
-      for (int j = 0; j < C::NREL; ++j) mbar_init(&S.a_empty[i][j], C::BLK_REL ? 1 : C::NISS);
+      mbar_init(&S.a_empty[i], C::NISS);
     }
     for (int i = 0; i < SB; ++i) {
       mbar_init(&S.b_full[i], 1);
@@ -696,7 +695,6 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
 #pragma unroll
               for (int kk = 0; kk < KC / 16; ++kk)
                 mma_bf16_ta(acc + m * PT, a_st + (c * C::NMAT + m) * 32 + 8 * kk, bd + 2 * kk, idesc, (kc | kk) != 0);
-              if constexpr (C::BLK_REL) mma_commit(&S.a_empty[sa][c * C::NMAT + m]);
             }
             bd += nm8;
             if (++sub == U.kps || kc == U.nkc - 1) {
@@ -705,9 +703,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
               sub = 0;
             }
           }
-          if constexpr (!C::BLK_REL) {
-            if (leader) mma_commit(&S.a_empty[sa][0]);
-          }
+          if (leader) mma_commit(&S.a_empty[sa]);
           __syncwarp();
         }
         if (!ok) break;
@@ -745,7 +741,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
         // warp-uniform verdicts: the TMEM stores below are .sync.aligned, so
         // no lane may leave the loop alone when a wait gives up
         const bool got = mbar_wait(&S.code_full[sc], (ast / C::SC) & 1, abort, WAIT_NS) &&
-                         (C::BLK_REL || mbar_wait(&S.a_empty[sa][0], a_par, abort, WAIT_NS));
+                         mbar_wait(&S.a_empty[sa], a_par, abort, WAIT_NS);
         if (!__all_sync(0xFFFFFFFFu, got)) {
           if (lane == 0) note_timeout(p.status, abort, GATEUP ? 36 : 46);
           ok = false;
@@ -776,14 +772,6 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
             for (int v = 0; v < NV; ++v) nw[v] = reinterpret_cast<const CW*>(nb + o * C::ROWB)[v];
             ns = reinterpret_cast<const __nv_bfloat16*>(nb + 128 * C::ROWB)[o];
             nbv = reinterpret_cast<const __nv_bfloat16*>(nb + 128 * C::ROWB + 256)[o];
-          }
-          if constexpr (C::BLK_REL) {
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.a_empty[sa][cm], a_par, abort, WAIT_NS))) {
-              if (lane == 0) note_timeout(p.status, abort, 38);
-              ok = false;
-              break;
-            }
-            tc_fence_after();
           }
           uint32_t r[32];
           dequant_bits<BITS>(reinterpret_cast<const uint32_t*>(cw), __halves2bfloat162(sv, sv),
