@@ -54,6 +54,10 @@ DEFAULT_WORKLOAD = "t4096_h4096_e256"
 EXTRA_WORKLOADS = ("t4096_h2048_e128_skewed", "t512_h2048_e128", "decode_t1_h2048_e128",
                    "decode_t2_h2048_e128", "decode_t4_h2048_e128", "decode_t8_h2048_e128",
                    "t4096_h4096_e256_b2", "t4096_h4096_e256_b3", "t4096_h4096_e256_b8")
+# The streamed-experts line: the headline chunk with its routed records in
+# host memory, half of them resident in a device pool after the first chunk.
+STREAMED = "t4096_h4096_e256_streamed"
+STREAMED_CFG = dict(pool_slots=128, ring_slots=64, group=32)
 L2_BYTES = 129 * 2 ** 20
 SUSTAIN_S, SUSTAIN_MIN_RUNS, SUSTAIN_MAX_RUNS = 1.0, 50, 20000
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -590,6 +594,92 @@ def measure(ctx: Ctx, w: synth.Workload, inp: dict, headline: bool) -> dict:
         graph=graph is not None, flags=flags)
 
 
+def measure_streamed(ctx: Ctx, w: synth.Workload, inp: dict) -> dict:
+    """Time moe_forward_streamed on workload ``w`` in its steady state (the
+    pool filled by the warm-up chunks): every step routes, plans, fetches the
+    non-resident records from pinned host memory over the host link and runs
+    the batches.  Bound: the host-to-device copy rate, measured here on the
+    same pinned buffer."""
+    torch, moe, args = ctx.torch, ctx.moe, ctx.args
+    flags = MOE_PACKED_WEIGHTS
+    dev = ctx.device_inputs(w, inp, flags)
+    dims = moe.dims_of(w.t, w.h, w.inter, w.E, w.k, w.shared_inter, w.bits)
+    host = dev["packed"].cpu().pin_memory()
+    st = moe.Streamer(dims, STREAMED_CFG["pool_slots"], STREAMED_CFG["ring_slots"], STREAMED_CFG["group"], host,
+                      ctx.dev)
+    ws = moe.new_workspace(dims, flags, ctx.dev)
+    out = torch.empty((w.t, w.h), dtype=torch.bfloat16, device=ctx.dev)
+    bufs = dict(route=(torch.empty((w.t, w.k), dtype=torch.int32, device=ctx.dev),
+                       torch.empty((w.t, w.k), dtype=torch.float32, device=ctx.dev)),
+                csr=moe.Csr(torch.empty(w.E + 1, dtype=torch.int32, device=ctx.dev),
+                            torch.empty(w.t * w.k, dtype=torch.int32, device=ctx.dev),
+                            torch.empty(w.t * w.k, dtype=torch.float32, device=ctx.dev),
+                            torch.empty(w.t * w.k, dtype=torch.int32, device=ctx.dev)))
+    stream = torch.cuda.current_stream()
+
+    def step():
+        return moe.moe_forward_streamed(dev, dims, st, flags, ws=ws, out=out, bufs=bufs)
+
+    for _ in range(args.warmup):
+        res = step()
+    torch.cuda.synchronize()
+    if moe.read_device_status(ws) != 0:
+        raise RuntimeError(f"{STREAMED}: device-side status after warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stats = []
+    for i in range(args.steps):
+        ctx.flush.fill_(float(i))
+        starts[i].record(stream)
+        res = step()
+        ends[i].record(stream)
+        stats.append(res["stats"])
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms = max_over_ranks(statistics.median(step_ms), ctx.dev)
+    moe.profile_enable(True)
+    for _ in range(3):
+        step()
+    moe.profile_enable(False)
+    prof = moe.profile_read()
+    kernel_ms = sum(v[1] for v in prof.values()) / 3
+    if moe.read_device_status(ws) != 0:
+        raise RuntimeError(f"{STREAMED}: device-side status set during the timed runs")
+    st.close()
+    # the host-to-device copy rate of this pinned buffer: 1 GiB, best of 3
+    n = min(1 << 30, host.numel())
+    dst = torch.empty(n, dtype=torch.uint8, device=ctx.dev)
+    rates = []
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dst.copy_(host[:n], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        rates.append(n / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    del dst
+    h2d_gbs = max(rates)
+    last = stats[-1]
+    moved = last["bytes"]
+    ach = moved / (ms * 1e-3) / 1e9
+    return dict(
+        value=job_tokens_per_s(ctx.world, w.t, ms), unit="tokens/s", ms_per_step=ms,
+        config={"workload": STREAMED, "t": w.t, "h": w.h, "inter": w.inter, "E": w.E, "k": w.k,
+                "shared_inter": w.shared_inter, "bits": w.bits, **STREAMED_CFG,
+                "records": "packed routed records in pinned host memory; shared record on the device",
+                "resident_experts": last["resident"], "filled_per_step": last["filled"],
+                "streamed_per_step": last["streamed"], "fetch_batches": last["batches"],
+                "bytes_copied_per_step": moved, "step_ms_min": min(step_ms), "step_ms_max": max(step_ms),
+                "kernel_ms_per_step": kernel_ms,
+                "timing": "median of the K steps, CUDA events around each call (the call waits once "
+                          "for the routing on the host); L2 flushed between steps"},
+        roofline={"bound": "h2d", "achieved": ach, "peak": h2d_gbs, "unit": "GB/s", "frac": ach / h2d_gbs,
+                  "traffic": None, "peak_source": "1 GiB host-to-device copy from the same pinned buffer, "
+                                                  "measured in this run (best of 3)"},
+        gpu_launches=sum(v[0] for v in prof.values()) // 3,
+        kernels={k: {"launches": v[0], "ms": v[1]} for k, v in prof.items()})
+
+
 def workload_config(w: synth.Workload, m: dict) -> dict:
     work, sr = m["work"], m["step_roofline"]
     return {"workload": w.name, "t": w.t, "h": w.h, "inter": w.inter, "E": w.E, "k": w.k,
@@ -606,7 +696,13 @@ def run_ours(args, w: synth.Workload, pool):
     inp = pool.inp if pool is not None else synth.make_inputs(w)
     m = measure(ctx, w, inp, True)
     extras = {}
+    if STREAMED in args.extra:
+        extras[STREAMED] = measure_streamed(ctx, synth.WORKLOADS[DEFAULT_WORKLOAD],
+                                            inp if w.name == DEFAULT_WORKLOAD else
+                                            synth.make_inputs(synth.WORKLOADS[DEFAULT_WORKLOAD]))
     for name in args.extra:
+        if name == STREAMED:
+            continue
         wx = synth.WORKLOADS[name]
         mx = measure(ctx, wx, synth.make_inputs(wx), False)
         extras[name] = dict(
@@ -673,13 +769,14 @@ def main():
         ap.error("--warmup must be at least 3")
     w = synth.WORKLOADS[args.workload]
     if args.workloads == "default":
-        args.extra = [n for n in EXTRA_WORKLOADS if n != w.name] if w.name == DEFAULT_WORKLOAD else []
+        args.extra = ([STREAMED] + [n for n in EXTRA_WORKLOADS if n != w.name]
+                      if w.name == DEFAULT_WORKLOAD else [])
     elif args.workloads == "none":
         args.extra = []
     else:
         args.extra = [n for n in args.workloads.split(",") if n]
         for n in args.extra:
-            if n not in synth.WORKLOADS:
+            if n not in synth.WORKLOADS and n != STREAMED:
                 ap.error(f"unknown workload {n}")
     if args.impl == "reference":
         run_reference(args, w)

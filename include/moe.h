@@ -16,13 +16,16 @@
  *
  * Conventions shared by every entry point
  *   - Every array pointer is a DEVICE pointer on the current CUDA device,
- *     allocated and owned by the caller; the library keeps no model state
- *     and never allocates, frees or retains caller memory.
+ *     allocated and owned by the caller, unless its description says host;
+ *     the library keeps no model state and never allocates, frees or
+ *     retains caller memory (the one object it allocates is the streaming
+ *     context of moe_streamer_create).
  *   - bf16 and fp16 values are passed as their 16-bit patterns (uint16_t).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls only enqueue work on it: they return before the GPU
- *     has run, never synchronise the host (except moe_read_device_status),
- *     and results are valid once the stream has reached that point.
+ *     has run, never synchronise the host (except moe_read_device_status,
+ *     moe_noalloc_read_status and moe_forward_streamed), and results are
+ *     valid once the stream has reached that point.
  *   - Return value: MOE_OK (0) or a negative moe_status.  Nothing throws or
  *     aborts across the ABI.  Host-side argument checks run before any work
  *     is enqueued; on failure nothing is enqueued.  moe_last_error() gives a
@@ -311,6 +314,122 @@ int moe_build_csr_noalloc(const int32_t* idx, const float* w, const moe_dims* di
 size_t moe_packed_bytes(const moe_dims* dims, int shared);
 int moe_pack_experts(const moe_qweights* src, const moe_dims* dims, int shared, void* dst, size_t dst_bytes,
                      void* stream);
+
+/*
+ * Streamed experts (prefill.rs module doc and its RING / GROUP constants:
+ * records stream through a ring of pool slots, a fetch side filling batches
+ * ahead of the GPU with two events per batch; prefill/experts.rs,
+ * prepare_expert_jobs: the chunk's most-used experts stay resident, the
+ * rest take ring slots; pf_experts: the batch protocol).  The routed
+ * records (moe_pack_experts output) live in host memory -- on a Grace
+ * machine in its LPDDR, read over NVLink-C2C -- and a device buffer of
+ * pool_slots + ring_slots record slots holds the resident set and the ring.
+ *
+ * The residency plan of one chunk (moe_plan_residency; host code only):
+ *   1. the experts with rows are ranked by row count, descending, equal
+ *      counts in ascending id order; the first pool_slots form the keep set;
+ *   2. a kept expert that is not resident takes the lowest free pool slot,
+ *      else the slot of the least recently used resident whose expert has
+ *      no rows in this chunk (lower slot on ties), which is evicted; with
+ *      neither it streams for this chunk.  Residents used by the chunk are
+ *      never evicted.  Every pool slot used gets last-use = `call`;
+ *   3. in ascending expert order, an expert already resident reads its pool
+ *      slot without a copy (batch 0); a newly kept one is copied into its
+ *      pool slot; every other expert is copied into ring slot
+ *      ring_pos % ring_slots (ring_pos counting the ring jobs);
+ *   4. the copies, in that order, form fetch batches 1, 2, ... of `group`
+ *      copies each; fetch batch b overwrites ring slots only after batch
+ *      wait_for[b] = b - ring_slots / group (when >= 1) has finished.
+ */
+typedef struct {
+  int32_t pool_slots; /* >= 0: record slots whose contents persist across calls */
+  int32_t ring_slots; /* a positive multiple of group: slots refilled by every call */
+  int32_t group;      /* >= 1: records per fetch batch */
+} moe_stream_cfg;
+
+/* One chunk's plan; every pointer is a caller-owned HOST array. */
+typedef struct {
+  int32_t* pool_expert; /* [pool_slots] in/out: expert in each pool slot, -1 = free */
+  int64_t* pool_last;   /* [pool_slots] in/out: call number of each slot's last use */
+  int32_t* rec;         /* [E] out: record slot of each expert (pool slot, or
+                           pool_slots + ring slot); -1 when it has no rows */
+  int32_t* batch;       /* [E] out: 0 resident, b >= 1 its fetch batch, -1 no rows */
+  int32_t* copy_expert; /* [E] out: experts whose record is copied, in copy order */
+  int32_t* copy_slot;   /* [E] out: the record slot each copy writes */
+  int32_t* wait_for;    /* [E + 1] out: per batch, the batch it waits for (0 = none) */
+  int32_t n_copies;     /* out */
+  int32_t n_batches;    /* out: 1 + the number of fetch batches */
+} moe_residency_plan;
+
+/* counts: host int32 [E], rows routed to each expert (negative read as 0).
+ * `call` must exceed the call numbers already in pool_last.  Host only: no
+ * CUDA call, no allocation.  Errors: MOE_EINVAL (null pointer, bad cfg, a
+ * pool entry outside [-1, E) or held twice), MOE_ESHAPE (E outside
+ * [1, 1024]). */
+int moe_plan_residency(const int32_t* counts, int32_t E, const moe_stream_cfg* cfg, int64_t call,
+                       moe_residency_plan* plan);
+
+/* A streaming context: the pool table and call counter, a copy stream,
+ * the events of the batch protocol, pinned staging for the expert counts
+ * and a small device array for the per-chunk record and batch maps.  The
+ * one object this library allocates; create it once per model layer and
+ * device (it serves the current device at creation).  Errors: MOE_EINVAL,
+ * MOE_ESHAPE, MOE_ECUDA. */
+typedef struct moe_streamer moe_streamer;
+int moe_streamer_create(const moe_dims* dims, const moe_stream_cfg* cfg, moe_streamer** out);
+int moe_streamer_destroy(moe_streamer* st); /* waits for its copy stream; NULL is a no-op */
+/* The pool table: the expert held by each pool slot (-1 = free) into
+ * pool_expert[0 .. min(n, pool_slots)); returns that count or a negative
+ * moe_status. */
+int moe_streamer_pool(const moe_streamer* st, int32_t* pool_expert, int32_t n);
+
+typedef struct {
+  int32_t resident; /* experts that read a resident record (no copy) */
+  int32_t filled;   /* records copied into pool slots */
+  int32_t streamed; /* records copied into ring slots */
+  int32_t batches;  /* fetch batches */
+  int64_t bytes;    /* bytes copied host -> device */
+} moe_stream_stats;
+
+/*
+ * moe_forward with the routed records streamed from host memory: the same
+ * idx, w and csr as moe_route_csr, and `out` within the same tolerance as
+ * moe_experts_fwd on the packed records (bit for bit with
+ * MOE_DETERMINISTIC: each row sums its terms in the same fixed order).
+ *
+ *   1. router and grouping on `stream`; the per-expert counts are copied to
+ *      the host and the host waits for them (the one point where this call
+ *      blocks the host);
+ *   2. the residency plan (moe_plan_residency, call numbers 1, 2, ... per
+ *      streamer), and the record and batch maps copied to the device;
+ *   3. batch 0 (resident experts and the shared expert) runs on `stream`
+ *      while the streamer's copy stream fetches batch 1;
+ *   4. per fetch batch b: the copy stream waits for event "done" of batch
+ *      wait_for[b], issues one host -> device copy per record and records
+ *      event "fetched"; `stream` waits for "fetched", runs the batch's
+ *      experts (tile schedule, gather, gate/up, down) and records "done".
+ *   5. the last batch finalises `out`.
+ *
+ * host_records: E packed routed records (moe_packed_bytes(dims, 0) bytes),
+ *   in page-locked host memory (cudaHostAlloc) for the copies to run
+ *   asynchronously; on a Grace machine any memory the GPU can address.
+ * slots: device buffer of (pool_slots + ring_slots) * moe_packed_bytes(dims,
+ *   0) / E bytes, 16-byte aligned, used only through `st` (its pool slots
+ *   keep their records between calls).
+ * shared: the packed shared record on the device (MOE_PACKED_WEIGHTS
+ *   layout), or NULL when shared_inter == 0.
+ * flags: MOE_PACKED_WEIGHTS (required) and optionally MOE_DETERMINISTIC;
+ *   the tensor-core kernels always run.  ws: moe_workspace_bytes(dims, flags).
+ * stats: host, may be NULL.
+ * Calls on one streamer must be ordered: issue them on one stream from one
+ * thread.  After a failed call the pool is emptied (the next call refetches).
+ * Errors: MOE_EINVAL, MOE_ESHAPE (dims other than the streamer's), MOE_EWORKSPACE,
+ * MOE_ECUDA.
+ */
+int moe_forward_streamed(const uint16_t* x, const uint16_t* wr, const float* rbias, const uint8_t* host_records,
+                         uint8_t* slots, const moe_shared* shared, const moe_dims* dims, uint32_t flags,
+                         int32_t* idx, float* w, const moe_csr* csr, uint16_t* out, void* ws, size_t ws_bytes,
+                         moe_streamer* st, void* stream, moe_stream_stats* stats);
 
 /* Workspace bytes needed by moe_build_csr and moe_experts_fwd for `dims` and
  * `flags` (one buffer serves both calls on one stream).  0 on bad dims. */

@@ -41,6 +41,18 @@ __host__ __device__ inline size_t packed_rec_bytes(int h, int I) {
   return packed_gu_bytes(h, I) + (size_t)(h / 128) * (I / 64) * PACK_QB;
 }
 
+// One batch of a chunk whose routed records sit in record slots (streamed
+// experts): only the experts e with batch_of[e] == batch (E = the shared
+// expert) run, reading record rec_map[e] of n_rec.  The first batch zeroes
+// the block accumulator and evaluates the shared gate; the last finalises.
+struct PackedBatch {
+  const int32_t* rec_map;
+  int n_rec;
+  const int32_t* batch_of;
+  int batch;
+  bool first, last;
+};
+
 cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t stream);
 cudaError_t launch_finalize(const ExpertsArgs& a, bool deterministic, cudaStream_t stream);
 cudaError_t launch_experts_simple(const ExpertsArgs& a, bool deterministic, cudaStream_t stream);

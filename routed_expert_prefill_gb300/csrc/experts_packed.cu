@@ -455,9 +455,25 @@ struct PParams {
   TcParams p;
   const uint8_t* packed;    // routed records
   const uint8_t* s_packed;  // shared record
+  // Record slots (streamed records): when non-null, expert e's record is
+  // record rec_map[e] of `packed`, which holds n_rec records.
+  const int32_t* rec_map;
+  int n_rec;
   const uint16_t* xg;       // gathered token images
   int kmax;                 // max(I, Is): hg row pitch in the padded space
 };
+
+// Record index of routed expert e: e itself, or its slot in the streamed
+// layout (a slot outside [0, n_rec) is flagged and read as slot 0).
+__device__ __forceinline__ int record_of(const PParams& P, int e) {
+  if (!P.rec_map) return e;
+  const int r = P.rec_map[e];
+  if (r < 0 || r >= P.n_rec) {
+    raise_flag(P.p.status, FLAG_BAD_OFFSETS);
+    return 0;
+  }
+  return r;
+}
 
 template <int MODE, int PT, int CP, int BITS>
 struct PSmem {
@@ -515,7 +531,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
   const int egroups = blockDim.x > KTHREADS_1 ? 2 : 1;  // epilogue warpgroups
   const int unit0 = blockIdx.x, ustride = gridDim.x;
 
-  if (GATEUP && (!p.deterministic || p.Is == 0)) {
+  if (GATEUP && p.zero_acc) {
     float4* acc4 = reinterpret_cast<float4*>(p.acc);
     const size_t n4 = (size_t)p.t * h / 4;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x)
@@ -571,7 +587,7 @@ __global__ void __launch_bounds__(KTHREADS, 1) packed_gemm_kernel(PParams P) {
       auto unit_codes = [&](int u, int& nst) -> const uint8_t* {
         const PUnit U = decode_punit<MODE, CP, C::B_STAGE>(p, u);
         const int Iu = U.shared ? p.Is : p.I;
-        const uint8_t* rec = U.shared ? P.s_packed : P.packed + (size_t)U.e * rec_bytes(h, p.I, BITS);
+        const uint8_t* rec = U.shared ? P.s_packed : P.packed + (size_t)record_of(P, U.e) * rec_bytes(h, p.I, BITS);
         nst = U.nkc / CPS;
         m2 = (size_t)(Iu / KC) * QB;
         if (GATEUP) return rec + (size_t)(U.f0 / 128) * (h / KC) * 2 * QB;
@@ -1030,7 +1046,7 @@ cudaError_t launch_packed_pt(const PParams& P, int pt, cudaStream_t stream) {
 }
 
 cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, const uint8_t* s_packed,
-                                  uint16_t* xg, bool deterministic, cudaStream_t stream) {
+                                  uint16_t* xg, bool deterministic, cudaStream_t stream, const PackedBatch* pb) {
   moe_dims d{a.t, a.h, a.I, a.E, a.k, a.Is};
   const size_t mt = packed_max_tiles(d);
   const int fmax = (a.I > a.Is ? a.I : a.Is) / 128;
@@ -1060,8 +1076,16 @@ cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, c
   p.tiles = tiles;
   p.units_gu = units;
   p.status = a.status;
+  const bool first = !pb || pb->first, last = !pb || pb->last;
+  // the fp32 block accumulator starts at zero (before the first batch)
+  // unless deterministic mode's shared expert writes every element of it
+  p.zero_acc = first && (!deterministic || a.Is == 0) ? 1 : 0;
+  p.batch_of = pb ? pb->batch_of : nullptr;
+  p.batch = pb ? pb->batch : 0;
   P.packed = packed;
   P.s_packed = s_packed;
+  P.rec_map = pb ? pb->rec_map : nullptr;
+  P.n_rec = pb ? pb->n_rec : a.E;
   P.xg = xg;
   P.kmax = a.I > a.Is ? a.I : a.Is;
 
@@ -1074,7 +1098,8 @@ cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, c
   const int pt = pairs <= 40L * a.E ? PTILE_SMALL : pairs <= 96L * a.E ? PTILE : PTILE_LARGE;
   cudaError_t err;
   if ((err = launch_schedule(p, hdr, tiles, units, (int)mt, pt, stream)) != cudaSuccess) return err;
-  if (p.gate_vals && (err = launch_shared_gate(a.x, a.s_gate, a.t, a.h, gate_vals, stream)) != cudaSuccess)
+  if (first && p.gate_vals &&
+      (err = launch_shared_gate(a.x, a.s_gate, a.t, a.h, gate_vals, stream)) != cudaSuccess)
     return err;
   MOE_LAUNCH("gather", stream,
              launch_k(gather_kernel, dim3((unsigned)mt, pt / 8), 256, 0, stream, a.x, a.rows, hdr, tiles, a.t, a.h, a.E,
@@ -1085,7 +1110,7 @@ cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, c
                       : launch_packed_pt<4>(P, pt, stream);
   if (err != cudaSuccess) return err;
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  return launch_finalize(a, deterministic, stream);
+  return last ? launch_finalize(a, deterministic, stream) : cudaSuccess;
 }
 
 }  // namespace moe

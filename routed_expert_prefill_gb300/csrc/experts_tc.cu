@@ -119,6 +119,7 @@ schedule_kernel(TcParams p, SchedHdr* hdr, int4* tiles, int* units_gu, int max_t
   __syncthreads();
   // pass 1: count tiles per size bucket (bucket = ceil(size / 16) - 1)
   for (int e = tid; e < nexp; e += blockDim.x) {
+    if (p.batch_of && p.batch_of[e] != p.batch) continue;
     int n;
     if (e < p.E) {
       n = p.offsets[e + 1] - p.offsets[e];
@@ -150,6 +151,7 @@ schedule_kernel(TcParams p, SchedHdr* hdr, int4* tiles, int* units_gu, int max_t
   __syncthreads();
   // pass 2: place tiles
   for (int e = tid; e < nexp; e += blockDim.x) {
+    if (p.batch_of && p.batch_of[e] != p.batch) continue;
     int n, start;
     if (e < p.E) {
       n = p.offsets[e + 1] - p.offsets[e];
@@ -360,7 +362,7 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = p.h;
 
-  if (GATEUP && (!p.deterministic || p.Is == 0)) {
+  if (GATEUP && p.zero_acc) {
     // The fp32 block accumulator starts at zero (atomic mode, or no shared
     // expert to initialise it); the down kernel runs after this one.
     float4* acc4 = reinterpret_cast<float4*>(p.acc);
@@ -808,6 +810,9 @@ cudaError_t launch_experts_tc(const ExpertsArgs& a, bool deterministic, cudaStre
   p.tiles = tiles;
   p.units_gu = units;
   p.status = a.status;
+  // the fp32 block accumulator starts at zero unless deterministic mode's
+  // shared expert writes every element of it
+  p.zero_acc = (!deterministic || a.Is == 0) ? 1 : 0;
 
   CUtensorMap tm_codes_gu, tm_scodes_gu, tm_x, tm_codes_dn, tm_scodes_dn, tm_hg, tm_hgs;
   cudaError_t err;

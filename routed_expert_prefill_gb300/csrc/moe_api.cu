@@ -3,8 +3,11 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "experts.cuh"
+#include "residency.cuh"
 
 namespace moe {
 
@@ -26,7 +29,8 @@ size_t packed_pad_rows(const moe_dims& d);
 cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, const uint16_t* biases, int h, int I,
                         int nrec, int bits, uint8_t* dst, cudaStream_t stream);
 cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, const uint8_t* s_packed,
-                                  uint16_t* xg, bool deterministic, cudaStream_t stream);
+                                  uint16_t* xg, bool deterministic, cudaStream_t stream,
+                                  const PackedBatch* pb = nullptr);
 cudaError_t launch_experts_gemv(const ExpertsArgs& a, bool packed, bool deterministic, cudaStream_t stream);
 size_t gemv_part_bytes(const moe_dims& d);
 bool decode_fused_ok(const moe_dims& d, uint32_t flags);
@@ -243,6 +247,46 @@ int moe_route_csr(const uint16_t* x, const uint16_t* wr, const float* rbias, con
                      "moe_route_csr launch");
 }
 
+// The expert kernels' arguments for one call (pointers already checked).
+static ExpertsArgs experts_args(const uint16_t* x, const moe_csr* csr, const moe_qweights* experts,
+                                const moe_shared* shared, uint16_t* out, const moe_dims* dims, uint32_t flags,
+                                unsigned char* wsb, const WsLayout& L) {
+  ExpertsArgs a{};
+  a.x = x;
+  a.t = dims->t;
+  a.h = dims->h;
+  a.I = dims->inter;
+  a.Is = dims->shared_inter;
+  a.E = dims->E;
+  a.k = dims->k;
+  a.n_pairs = dims->t * dims->k;
+  a.offsets = csr->offsets;
+  a.rows = csr->rows;
+  a.weights = csr->weights;
+  a.slot_of = csr->slot_of;
+  a.codes = experts ? experts->codes : nullptr;
+  a.scales = experts ? experts->scales : nullptr;
+  a.biases = experts ? experts->biases : nullptr;
+  a.bits = dims_bits(dims);
+  a.rec_bytes = (size_t)3 * dims->inter * dims->h * a.bits / 8;
+  a.rec_groups = (size_t)3 * dims->inter * dims->h / 64;
+  if (dims->shared_inter > 0) {
+    a.s_codes = shared->codes;
+    a.s_scales = shared->scales;
+    a.s_biases = shared->biases;
+    a.s_gate = shared->gate;
+  }
+  a.acc = (float*)(wsb + L.acc);
+  a.hg = (uint16_t*)(wsb + L.hg);
+  a.hgs = (uint16_t*)(wsb + L.hgs);
+  a.ybuf = (flags & MOE_DETERMINISTIC) ? (float*)(wsb + L.ybuf) : nullptr;
+  a.sched = wsb + L.sched;
+  a.gvpart = gemv_part_bytes(*dims) ? (float*)(wsb + L.gvpart) : nullptr;
+  a.status = (DeviceStatus*)(wsb + L.status);
+  a.out = out;
+  return a;
+}
+
 static int check_flags(uint32_t flags) {
   const uint32_t known =
       MOE_DETERMINISTIC | MOE_FORCE_SMALL_T | MOE_FORCE_LARGE_T | MOE_SIMPLE_KERNELS | MOE_PACKED_WEIGHTS |
@@ -282,40 +326,7 @@ int moe_experts_fwd(const uint16_t* x, const moe_csr* csr, const moe_qweights* e
   TRY(check_ws(dims, flags, ws, ws_bytes));
   const WsLayout L = ws_layout(*dims, flags);
   unsigned char* wsb = (unsigned char*)ws;
-
-  ExpertsArgs a{};
-  a.x = x;
-  a.t = dims->t;
-  a.h = dims->h;
-  a.I = dims->inter;
-  a.Is = dims->shared_inter;
-  a.E = dims->E;
-  a.k = dims->k;
-  a.n_pairs = dims->t * dims->k;
-  a.offsets = csr->offsets;
-  a.rows = csr->rows;
-  a.weights = csr->weights;
-  a.slot_of = csr->slot_of;
-  a.codes = experts->codes;
-  a.scales = experts->scales;
-  a.biases = experts->biases;
-  a.bits = dims_bits(dims);
-  a.rec_bytes = (size_t)3 * dims->inter * dims->h * a.bits / 8;
-  a.rec_groups = (size_t)3 * dims->inter * dims->h / 64;
-  if (dims->shared_inter > 0) {
-    a.s_codes = shared->codes;
-    a.s_scales = shared->scales;
-    a.s_biases = shared->biases;
-    a.s_gate = shared->gate;
-  }
-  a.acc = (float*)(wsb + L.acc);
-  a.hg = (uint16_t*)(wsb + L.hg);
-  a.hgs = (uint16_t*)(wsb + L.hgs);
-  a.ybuf = (flags & MOE_DETERMINISTIC) ? (float*)(wsb + L.ybuf) : nullptr;
-  a.sched = wsb + L.sched;
-  a.gvpart = gemv_part_bytes(*dims) ? (float*)(wsb + L.gvpart) : nullptr;
-  a.status = (DeviceStatus*)(wsb + L.status);
-  a.out = out;
+  const ExpertsArgs a = experts_args(x, csr, experts, shared, out, dims, flags, wsb, L);
 
   cudaStream_t s = (cudaStream_t)stream;
   if (a.bits != 4 && (!packed || (flags & MOE_FORCE_SMALL_T)))
@@ -372,6 +383,116 @@ int moe_forward(const uint16_t* x, const uint16_t* wr, const float* rbias, const
                           dims->shared_inter > 0 ? shared->gate : nullptr, idx, w, *csr, out, wsb + L.fused,
                           (DeviceStatus*)(wsb + L.status), (cudaStream_t)stream),
       "moe_forward launch");
+}
+
+int moe_forward_streamed(const uint16_t* x, const uint16_t* wr, const float* rbias, const uint8_t* host_records,
+                         uint8_t* slots, const moe_shared* shared, const moe_dims* dims, uint32_t flags,
+                         int32_t* idx, float* w, const moe_csr* csr, uint16_t* out, void* ws, size_t ws_bytes,
+                         moe_streamer* st, void* stream, moe_stream_stats* stats) {
+  TRY(check_dims(dims));
+  if (!st) return set_error(MOE_EINVAL, "streamer is NULL");
+  if (flags & ~(MOE_PACKED_WEIGHTS | MOE_DETERMINISTIC | MOE_FORCE_LARGE_T))
+    return set_error(MOE_EINVAL, "flags 0x%x: moe_forward_streamed takes MOE_PACKED_WEIGHTS and MOE_DETERMINISTIC",
+                     flags);
+  if (!(flags & MOE_PACKED_WEIGHTS)) return set_error(MOE_EINVAL, "moe_forward_streamed needs MOE_PACKED_WEIGHTS");
+  const moe_dims& sd = st->dims;
+  if (dims->E != sd.E || dims->h != sd.h || dims->inter != sd.inter || dims_bits(dims) != dims_bits(&sd))
+    return set_error(MOE_ESHAPE, "dims (E=%d h=%d inter=%d bits=%d) differ from the streamer's (%d %d %d %d)",
+                     dims->E, dims->h, dims->inter, dims_bits(dims), sd.E, sd.h, sd.inter, dims_bits(&sd));
+  int dev = -1;
+  TRY(cuda_status(cudaGetDevice(&dev), "cudaGetDevice"));
+  if (dev != st->device)
+    return set_error(MOE_EINVAL, "the streamer serves device %d, the current device is %d", st->device, dev);
+  TRY(check_ptr(host_records, "host_records", 16));
+  TRY(check_ptr(slots, "slots", 16));
+  TRY(check_ptr(out, "out", 16));
+  if (dims->shared_inter > 0) {
+    if (!shared) return set_error(MOE_EINVAL, "shared is NULL but shared_inter > 0");
+    TRY(check_ptr(shared->codes, "shared->codes", 16));
+    TRY(check_ptr(shared->gate, "shared->gate", 16, true));
+  }
+  TRY(check_ws(dims, flags, ws, ws_bytes));
+  // router and grouping: checks the remaining pointers before enqueueing
+  cudaStream_t s = (cudaStream_t)stream;
+  TRY(moe_route_csr(x, wr, rbias, dims, idx, w, csr, ws, ws_bytes, stream));
+
+  const int E = dims->E, P = st->cfg.pool_slots, R = st->cfg.ring_slots, lag = R / st->cfg.group;
+  // after a failure the pool's contents are unknown: empty it
+  auto fail = [&](cudaError_t e, const char* what) {
+    std::fill(st->pool_expert.begin(), st->pool_expert.end(), -1);
+    return set_error(MOE_ECUDA, "moe_forward_streamed: %s: %s", what, cudaGetErrorString(e));
+  };
+  cudaError_t e;
+  // 1. the chunk's expert counts on the host
+  if ((e = cudaMemcpyAsync(st->h_offsets, csr->offsets, (E + 1) * sizeof(int32_t), cudaMemcpyDeviceToHost, s)) !=
+      cudaSuccess)
+    return fail(e, "offsets copy");
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return fail(e, "stream sync");
+  for (int i = 0; i < E; ++i) {
+    const int32_t n = st->h_offsets[i + 1] - st->h_offsets[i];
+    st->counts[i] = n > 0 ? n : 0;  // bad offsets: flagged on the device, nothing runs
+  }
+  // 2. the plan, and the record and batch maps on the device
+  int32_t* rec = st->h_maps;
+  int32_t* batch_of = st->h_maps + E;
+  moe_residency_plan pl{};
+  pl.pool_expert = st->pool_expert.data();
+  pl.pool_last = st->pool_last.data();
+  pl.rec = rec;
+  pl.batch = batch_of;
+  pl.copy_expert = st->copy_expert.data();
+  pl.copy_slot = st->copy_slot.data();
+  pl.wait_for = st->wait_for.data();
+  const int ps = plan_residency(st->counts.data(), E, st->cfg, ++st->call, pl);
+  if (ps != MOE_OK) {
+    std::fill(st->pool_expert.begin(), st->pool_expert.end(), -1);
+    return ps;
+  }
+  batch_of[E] = 0;  // the shared expert runs with the resident ones
+  if ((e = cudaMemcpyAsync(st->d_maps, st->h_maps, (2 * E + 1) * sizeof(int32_t), cudaMemcpyHostToDevice, s)) !=
+      cudaSuccess)
+    return fail(e, "map copy");
+
+  const WsLayout L = ws_layout(*dims, flags);
+  unsigned char* wsb = (unsigned char*)ws;
+  const ExpertsArgs a = experts_args(x, csr, nullptr, shared, out, dims, flags, wsb, L);
+  const bool det = (flags & MOE_DETERMINISTIC) != 0;
+  const uint8_t* s_packed = dims->shared_inter > 0 ? shared->codes : nullptr;
+  uint16_t* xg = (uint16_t*)(wsb + L.xg);
+  PackedBatch pb{st->d_maps, P + R, st->d_maps + E, 0, true, pl.n_batches == 1};
+  // 3. batch 0: the resident experts and the shared expert, no fetch
+  if ((e = launch_experts_packed(a, slots, s_packed, xg, det, s, &pb)) != cudaSuccess) return fail(e, "batch 0");
+  // 4. the fetch batches, two events each
+  size_t copied = 0;
+  int nc = 0;
+  for (int b = 1; b < pl.n_batches; ++b) {
+    if (pl.wait_for[b] >= 1 && (e = cudaStreamWaitEvent(st->copy, st->done[pl.wait_for[b] % lag], 0)) != cudaSuccess)
+      return fail(e, "copy-stream wait");
+    for (; nc < pl.n_copies && batch_of[pl.copy_expert[nc]] == b; ++nc) {
+      const size_t rb = st->rec_bytes;
+      if ((e = cudaMemcpyAsync(slots + (size_t)pl.copy_slot[nc] * rb, host_records + (size_t)pl.copy_expert[nc] * rb,
+                               rb, cudaMemcpyHostToDevice, st->copy)) != cudaSuccess)
+        return fail(e, "record copy");
+      copied += rb;
+    }
+    if ((e = cudaEventRecord(st->fetched, st->copy)) != cudaSuccess) return fail(e, "event record");
+    if ((e = cudaStreamWaitEvent(s, st->fetched, 0)) != cudaSuccess) return fail(e, "stream wait");
+    pb.batch = b;
+    pb.first = false;
+    pb.last = b == pl.n_batches - 1;
+    if ((e = launch_experts_packed(a, slots, s_packed, xg, det, s, &pb)) != cudaSuccess) return fail(e, "batch");
+    if ((e = cudaEventRecord(st->done[b % lag], s)) != cudaSuccess) return fail(e, "event record");
+  }
+  if (stats) {
+    stats->resident = 0;
+    stats->filled = 0;
+    for (int i = 0; i < E; ++i) stats->resident += batch_of[i] == 0;
+    for (int i = 0; i < pl.n_copies; ++i) stats->filled += pl.copy_slot[i] < P;
+    stats->streamed = pl.n_copies - stats->filled;
+    stats->batches = pl.n_batches - 1;
+    stats->bytes = (int64_t)copied;
+  }
+  return MOE_OK;
 }
 
 size_t moe_packed_bytes(const moe_dims* dims, int shared) {

@@ -34,6 +34,11 @@ struct TcParams {
   const int4* tiles;       // {expert (E = shared), start, rows, padded-row offset}
   const int* units_gu;     // (tile << 8) | feature tile
   DeviceStatus* status;
+  int zero_acc;            // the gate/up kernel zeroes the fp32 block accumulator first
+  // Expert subset (streamed records): when non-null, the schedule keeps only
+  // the experts e (E = the shared expert) with batch_of[e] == batch.
+  const int32_t* batch_of;
+  int batch;
 };
 
 

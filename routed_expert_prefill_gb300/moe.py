@@ -51,6 +51,11 @@ EXPORTS = (
     "moe_noalloc_read_status",
     "moe_forward",
     "moe_debug_stall",
+    "moe_plan_residency",
+    "moe_streamer_create",
+    "moe_streamer_destroy",
+    "moe_streamer_pool",
+    "moe_forward_streamed",
 )
 
 
@@ -76,6 +81,21 @@ class MoeShared(ctypes.Structure):
 
 class MoeProfileEntry(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int32), ("total_ms", ctypes.c_double)]
+
+
+class MoeStreamCfg(ctypes.Structure):
+    _fields_ = [("pool_slots", ctypes.c_int32), ("ring_slots", ctypes.c_int32), ("group", ctypes.c_int32)]
+
+
+class MoeResidencyPlan(ctypes.Structure):
+    _fields_ = [("pool_expert", ctypes.c_void_p), ("pool_last", ctypes.c_void_p), ("rec", ctypes.c_void_p),
+                ("batch", ctypes.c_void_p), ("copy_expert", ctypes.c_void_p), ("copy_slot", ctypes.c_void_p),
+                ("wait_for", ctypes.c_void_p), ("n_copies", ctypes.c_int32), ("n_batches", ctypes.c_int32)]
+
+
+class MoeStreamStats(ctypes.Structure):
+    _fields_ = [("resident", ctypes.c_int32), ("filled", ctypes.c_int32), ("streamed", ctypes.c_int32),
+                ("batches", ctypes.c_int32), ("bytes", ctypes.c_int64)]
 
 
 class MoeError(RuntimeError):
@@ -131,6 +151,20 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_forward.restype = ctypes.c_int
     lib.moe_forward.argtypes = [vp, vp, vp, ctypes.POINTER(MoeQWeights), ctypes.POINTER(MoeShared),
                                 ctypes.POINTER(MoeDims), u32, vp, vp, ctypes.POINTER(MoeCsr), vp, vp, sz, vp]
+    lib.moe_plan_residency.restype = ctypes.c_int
+    lib.moe_plan_residency.argtypes = [vp, i32, ctypes.POINTER(MoeStreamCfg), ctypes.c_int64,
+                                       ctypes.POINTER(MoeResidencyPlan)]
+    lib.moe_streamer_create.restype = ctypes.c_int
+    lib.moe_streamer_create.argtypes = [ctypes.POINTER(MoeDims), ctypes.POINTER(MoeStreamCfg),
+                                        ctypes.POINTER(ctypes.c_void_p)]
+    lib.moe_streamer_destroy.restype = ctypes.c_int
+    lib.moe_streamer_destroy.argtypes = [vp]
+    lib.moe_streamer_pool.restype = ctypes.c_int
+    lib.moe_streamer_pool.argtypes = [vp, vp, i32]
+    lib.moe_forward_streamed.restype = ctypes.c_int
+    lib.moe_forward_streamed.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(MoeShared), ctypes.POINTER(MoeDims), u32,
+                                         vp, vp, ctypes.POINTER(MoeCsr), vp, vp, sz, vp, vp,
+                                         ctypes.POINTER(MoeStreamStats)]
     lib.moe_pack_experts.restype = ctypes.c_int
     lib.moe_pack_experts.argtypes = [ctypes.POINTER(MoeQWeights), ctypes.POINTER(MoeDims), ctypes.c_int, vp, sz, vp]
     _lib = lib
@@ -581,3 +615,139 @@ def moe_forward(dev: dict, dims: MoeDims, flags: int = MOE_PACKED_WEIGHTS, ws: t
                            ctypes.byref(dims), flags, _ptr(idx), _ptr(w), ctypes.byref(c), _ptr(out), _ptr(ws),
                            ws.numel(), _stream(stream)))
     return dict(idx=idx, w=w, csr=csr, out=out, ws=ws)
+
+
+# ---------------------------------------------------------------------------
+# Streamed experts: records in host memory, a device pool and ring of slots.
+# ---------------------------------------------------------------------------
+
+def plan_residency(counts, pool_expert, pool_last, call: int, ring: int, group: int) -> dict:
+    """One chunk's residency plan (host code of the library, no GPU).
+
+    counts int [E]; pool_expert int [P] and pool_last int [P] are the pool
+    table before the chunk.  Returns the plan with the updated table, in
+    the keys rec, batch, copies [(expert, slot)], n_batches, wait_for,
+    pool_expert, pool_last."""
+    import numpy as np
+
+    lib = load_library()
+    counts = np.ascontiguousarray(counts, dtype=np.int32)
+    E = counts.size
+    pe = np.array(pool_expert, dtype=np.int32)
+    pl_ = np.array(pool_last, dtype=np.int64)
+    rec = np.empty(E, np.int32)
+    batch = np.empty(E, np.int32)
+    ce = np.empty(E, np.int32)
+    cs = np.empty(E, np.int32)
+    wf = np.empty(E + 1, np.int32)
+    cfg = MoeStreamCfg(pe.size, ring, group)
+    addr = lambda a: a.ctypes.data if a.size else None  # noqa: E731
+    plan = MoeResidencyPlan(addr(pe), addr(pl_), rec.ctypes.data, batch.ctypes.data, ce.ctypes.data,
+                            cs.ctypes.data, wf.ctypes.data, 0, 0)
+    _check(lib.moe_plan_residency(counts.ctypes.data, E, ctypes.byref(cfg), call, ctypes.byref(plan)))
+    nc, nb = plan.n_copies, plan.n_batches
+    return dict(rec=rec.tolist(), batch=batch.tolist(), copies=list(zip(ce[:nc].tolist(), cs[:nc].tolist())),
+                n_batches=nb, wait_for=wf[:nb].tolist(), pool_expert=pe.tolist(), pool_last=pl_.tolist())
+
+
+class Streamer:
+    """The library's streaming context (moe_streamer) with the device slot
+    buffer and the host copy of the packed routed records it streams from.
+
+    host_records: uint8 tensor of the E packed records in page-locked host
+    memory (``packed.cpu().pin_memory()``).  The slot buffer is allocated
+    on the current device: (pool_slots + ring_slots) records."""
+
+    def __init__(self, dims: MoeDims, pool_slots: int, ring_slots: int, group: int, host_records: torch.Tensor,
+                 device=None):
+        lib = load_library()
+        n = lib.moe_packed_bytes(ctypes.byref(dims), 0)
+        if n == 0:
+            raise MoeError(-2, "bad dims for a streamer")
+        _need(host_records, "host_records", (torch.uint8,), min_numel=n)
+        if host_records.device.type != "cpu":
+            raise ValueError("host_records must be a host (CPU) tensor")
+        self.dims = MoeDims(*(getattr(dims, f) for f, _ in MoeDims._fields_))
+        self.cfg = MoeStreamCfg(pool_slots, ring_slots, group)
+        self.rec_bytes = n // dims.E
+        self.host_records = host_records
+        self.slots = torch.empty((pool_slots + ring_slots) * self.rec_bytes, dtype=torch.uint8,
+                                 device=device or "cuda")
+        h = ctypes.c_void_p()
+        _check(lib.moe_streamer_create(ctypes.byref(self.dims), ctypes.byref(self.cfg), ctypes.byref(h)))
+        self._h = h
+
+    def pool(self) -> list:
+        import numpy as np
+
+        out = np.empty(max(self.cfg.pool_slots, 1), np.int32)
+        m = load_library().moe_streamer_pool(self._h, out.ctypes.data, self.cfg.pool_slots)
+        if m < 0:
+            _check(m)
+        return out[:m].tolist()
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            load_library().moe_streamer_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def moe_forward_streamed(dev: dict, dims: MoeDims, st: Streamer, flags: int = MOE_PACKED_WEIGHTS,
+                         ws: torch.Tensor | None = None, out: torch.Tensor | None = None, stream=None,
+                         bufs: dict | None = None) -> dict:
+    """The whole block through moe_forward_streamed: the routed records come
+    from ``st.host_records`` through the streamer's pool and ring; the
+    shared record (dev["shared_packed"]) stays on the device.  Returns the
+    intermediate tensors and the streaming statistics."""
+    lib = load_library()
+    flags |= MOE_PACKED_WEIGHTS
+    x, wr, rbias = dev["x"], dev["wr"], dev.get("rbias")
+    t, h, E, k, Is = dims.t, dims.h, dims.E, dims.k, dims.shared_inter
+    _need(x, "x", _BF16, shape=(t, h))
+    _need(wr, "wr", _BF16, shape=(E, h))
+    if rbias is not None:
+        _need(rbias, "rbias", (torch.float32,), shape=(E,))
+    shared = None
+    if Is > 0:
+        sp = dev["shared_packed"]
+        _need(sp, "shared_packed", (torch.uint8,), min_numel=lib.moe_packed_bytes(ctypes.byref(dims), 1))
+        g = dev.get("shared_gate")
+        if g is not None:
+            _need(g, "shared gate", _BF16, shape=(h,))
+        shared = MoeShared(sp.data_ptr(), None, None, None if g is None else g.data_ptr())
+    b = bufs or {}
+    d = x.device
+    idx, w = b.get("route") or (torch.empty((t, k), dtype=torch.int32, device=d),
+                                torch.empty((t, k), dtype=torch.float32, device=d))
+    csr = b.get("csr") or Csr(torch.empty(E + 1, dtype=torch.int32, device=d),
+                              torch.empty(t * k, dtype=torch.int32, device=d),
+                              torch.empty(t * k, dtype=torch.float32, device=d),
+                              torch.empty(t * k, dtype=torch.int32, device=d))
+    _need(idx, "idx", (torch.int32,), shape=(t, k))
+    _need(w, "w", (torch.float32,), shape=(t, k))
+    _need_csr(csr, "csr", E, t * k)
+    if ws is None:
+        ws = new_workspace(dims, flags, d, stream)
+    else:
+        _need_ws(ws, dims, flags)
+    if out is None:
+        out = torch.empty((t, h), dtype=torch.bfloat16, device=d)
+    else:
+        _need(out, "out", _BF16, shape=(t, h))
+    _on_current_device(x=x, wr=wr, rbias=rbias, idx=idx, w=w, ws=ws, out=out, slots=st.slots,
+                       shared_packed=dev.get("shared_packed") if Is > 0 else None, **_csr_named(csr, "csr"))
+    stats = MoeStreamStats()
+    c = csr.c()
+    _check(lib.moe_forward_streamed(_ptr(x), _ptr(wr), _ptr(rbias), st.host_records.data_ptr(), _ptr(st.slots),
+                                    ctypes.byref(shared) if shared is not None else None, ctypes.byref(dims), flags,
+                                    _ptr(idx), _ptr(w), ctypes.byref(c), _ptr(out), _ptr(ws), ws.numel(),
+                                    _stream(stream), st._h, ctypes.byref(stats)))
+    return dict(idx=idx, w=w, csr=csr, out=out, ws=ws,
+                stats=dict(resident=stats.resident, filled=stats.filled, streamed=stats.streamed,
+                           batches=stats.batches, bytes=stats.bytes))

@@ -1,0 +1,226 @@
+"""Streamed experts on the GPU: moe_forward_streamed against the oracle and
+against the device-resident path, and its residency bookkeeping against the
+oracle's plan (cherenkov ``qwen4_exp``, ``prefill/experts.rs``,
+``prepare_expert_jobs`` / ``pf_experts``; ``prefill.rs`` RING / GROUP).
+
+* outputs within the block tolerance of the oracle;
+* with MOE_DETERMINISTIC, bit for bit equal to the resident tensor-core
+  path: streaming changes where a record is read from, not the arithmetic;
+* the pool table and the copy counts after every chunk equal the oracle's
+  plan for the chunk's expert counts;
+* a ring of one batch (every fetch waits for the batch before it), no pool
+  at all, and a pool that holds every expert.
+"""
+
+import numpy as np
+import pytest
+
+from oracle import moe_oracle as O
+from oracle import residency as R
+from routed_expert_prefill_gb300 import synth
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+TOL_REL, TOL_ABS = 1e-2, 1e-3
+
+
+@pytest.fixture(scope="module")
+def moe():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from routed_expert_prefill_gb300 import build
+
+    build.build()
+    from routed_expert_prefill_gb300 import moe as m
+
+    m.load_library()
+    return m
+
+
+def _dims(moe, w):
+    return moe.dims_of(w.t, w.h, w.inter, w.E, w.k, w.shared_inter, w.bits)
+
+
+def _setup(moe, w, seed_shift=0):
+    inp = synth.make_inputs(w.replace(seed=w.seed + seed_shift) if seed_shift else w)
+    dev = moe.upload_inputs(inp)
+    moe.add_packed(dev, _dims(moe, w))
+    return inp, dev
+
+
+def _streamer(moe, w, dev, pool, ring, group):
+    host = dev["packed"].cpu().pin_memory()
+    return moe.Streamer(_dims(moe, w), pool, ring, group, host)
+
+
+def _resident(moe, w, dev, flags):
+    res = moe.moe_forward(dev, _dims(moe, w), moe.MOE_PACKED_WEIGHTS | moe.MOE_FORCE_LARGE_T | flags)
+    torch.cuda.synchronize()
+    assert moe.read_device_status(res["ws"]) == 0
+    return res
+
+
+def _streamed(moe, w, dev, st, flags):
+    res = moe.moe_forward_streamed(dev, _dims(moe, w), st, moe.MOE_PACKED_WEIGHTS | flags)
+    torch.cuda.synchronize()
+    assert moe.read_device_status(res["ws"]) == 0
+    return res
+
+
+def _check_plan(res, st, E, oracle_state, call):
+    """Stats and pool table equal the oracle's plan for the chunk's counts."""
+    offs = res["csr"].offsets.cpu().numpy().astype(np.int64)
+    counts = np.diff(offs)
+    pool, last = oracle_state
+    p = R.plan(counts, pool, last, call=call, ring=st.cfg.ring_slots, group=st.cfg.group)
+    P = st.cfg.pool_slots
+    n_fill = sum(1 for _, s in p["copies"] if s < P)
+    s = res["stats"]
+    assert s["resident"] == sum(1 for b in p["batch"] if b == 0)
+    assert s["filled"] == n_fill
+    assert s["streamed"] == len(p["copies"]) - n_fill
+    assert s["batches"] == p["n_batches"] - 1
+    assert s["bytes"] == len(p["copies"]) * st.rec_bytes
+    assert st.pool() == p["pool_expert"]
+    return p["pool_expert"], p["pool_last"]
+
+
+CASES = [
+    # workload, pool slots, ring slots, group
+    ("tiny_t16_h256_e8", 2, 4, 2),
+    ("t512_h2048_e128", 32, 16, 8),
+    ("t4096_h2048_e128_skewed", 16, 32, 16),
+]
+
+
+@pytest.mark.parametrize("name,pool,ring,group", CASES)
+def test_streamed_matches_oracle(moe, name, pool, ring, group):
+    w = synth.WORKLOADS[name]
+    inp, dev = _setup(moe, w)
+    st = _streamer(moe, w, dev, pool, ring, group)
+    res = _streamed(moe, w, dev, st, 0)
+    if w.t <= 512:
+        ref = O.moe_forward(inp, w.k, w.h, w.inter, w.shared_inter)
+        np.testing.assert_array_equal(res["idx"].cpu().numpy(), ref["idx"])
+        rows = np.arange(w.t)
+    else:
+        rows = np.random.default_rng([w.seed, 77]).choice(w.t, 48, replace=False)
+        sub = dict(inp)
+        sub["x"] = inp["x"][rows]
+        ref = O.moe_forward(sub, w.k, w.h, w.inter, w.shared_inter)
+        np.testing.assert_array_equal(res["idx"].cpu().numpy()[rows], ref["idx"])
+    got = res["out"].float().cpu().numpy().astype(np.float64)[rows]
+    err = np.abs(got - ref["out"]).max()
+    tol = TOL_REL * np.abs(ref["out"]).max() + TOL_ABS
+    assert err <= tol, f"max|gpu-oracle| = {err:.4g} > {tol:.4g}"
+    _check_plan(res, st, w.E, ([-1] * pool, [0] * pool), 1)
+    st.close()
+
+
+@pytest.mark.parametrize("name,pool,ring,group", CASES)
+def test_streamed_deterministic_equals_resident_bitwise(moe, name, pool, ring, group):
+    w = synth.WORKLOADS[name]
+    _, dev = _setup(moe, w)
+    ref = _resident(moe, w, dev, moe.MOE_DETERMINISTIC)
+    st = _streamer(moe, w, dev, pool, ring, group)
+    res = _streamed(moe, w, dev, st, moe.MOE_DETERMINISTIC)
+    np.testing.assert_array_equal(res["idx"].cpu().numpy(), ref["idx"].cpu().numpy())
+    np.testing.assert_array_equal(res["csr"].offsets.cpu().numpy(), ref["csr"].offsets.cpu().numpy())
+    np.testing.assert_array_equal(res["out"].view(torch.int16).cpu().numpy(),
+                                  ref["out"].view(torch.int16).cpu().numpy())
+    st.close()
+
+
+def test_pool_persists_across_chunks(moe):
+    # five chunks of 32 rows (about an eighth of the experts idle in each, so
+    # resident records get evicted) through one streamer: every output bit
+    # for bit the resident path's, the pool table the oracle's after each
+    w = synth.WORKLOADS["t512_h2048_e128"].replace(t=32)
+    _, dev = _setup(moe, w)
+    x0 = dev["x"]
+    st = _streamer(moe, w, dev, 24, 16, 8)
+    state = ([-1] * 24, [0] * 24)
+    evicted = 0
+    for call in range(1, 6):
+        dev["x"] = torch.roll(x0, shifts=call * 5, dims=1).contiguous()  # new rows, new routing
+        before = set(state[0])
+        ref = _resident(moe, w, dev, moe.MOE_DETERMINISTIC)
+        res = _streamed(moe, w, dev, st, moe.MOE_DETERMINISTIC)
+        np.testing.assert_array_equal(res["out"].view(torch.int16).cpu().numpy(),
+                                      ref["out"].view(torch.int16).cpu().numpy())
+        state = _check_plan(res, st, w.E, state, call)
+        evicted += len(before - set(state[0]) - {-1})
+    assert evicted > 0
+    st.close()
+
+
+@pytest.mark.parametrize("pool,ring,group", [(0, 4, 4), (0, 8, 1), (8, 4, 4)])
+def test_single_batch_ring_and_no_pool(moe, pool, ring, group):
+    # ring == group: every fetch batch overwrites the slots the previous
+    # batch read, so it must wait for that batch; a read before its fetch
+    # completed would see another expert's record
+    w = synth.WORKLOADS["t512_h2048_e128"]
+    _, dev = _setup(moe, w)
+    ref = _resident(moe, w, dev, moe.MOE_DETERMINISTIC)
+    st = _streamer(moe, w, dev, pool, ring, group)
+    for call in (1, 2):
+        res = _streamed(moe, w, dev, st, moe.MOE_DETERMINISTIC)
+        np.testing.assert_array_equal(res["out"].view(torch.int16).cpu().numpy(),
+                                      ref["out"].view(torch.int16).cpu().numpy())
+    st.close()
+
+
+def test_pool_of_every_expert_stops_copying(moe):
+    w = synth.WORKLOADS["tiny_t16_h256_e8"]
+    _, dev = _setup(moe, w)
+    ref = _resident(moe, w, dev, moe.MOE_DETERMINISTIC)
+    st = _streamer(moe, w, dev, w.E, 2, 2)
+    first = _streamed(moe, w, dev, st, moe.MOE_DETERMINISTIC)
+    second = _streamed(moe, w, dev, st, moe.MOE_DETERMINISTIC)
+    assert first["stats"]["filled"] == int((first["csr"].offsets.diff() > 0).sum())
+    assert second["stats"]["bytes"] == 0 and second["stats"]["batches"] == 0
+    for r in (first, second):
+        np.testing.assert_array_equal(r["out"].view(torch.int16).cpu().numpy(),
+                                      ref["out"].view(torch.int16).cpu().numpy())
+    st.close()
+
+
+@pytest.mark.parametrize("bits", [3, 8])
+def test_streamed_low_bit_records(moe, bits):
+    w = synth.WORKLOADS["t512_h2048_e128"].replace(bits=bits)
+    _, dev = _setup(moe, w)
+    ref = _resident(moe, w, dev, moe.MOE_DETERMINISTIC)
+    st = _streamer(moe, w, dev, 16, 32, 16)
+    res = _streamed(moe, w, dev, st, moe.MOE_DETERMINISTIC)
+    np.testing.assert_array_equal(res["out"].view(torch.int16).cpu().numpy(),
+                                  ref["out"].view(torch.int16).cpu().numpy())
+    st.close()
+
+
+def test_headline_half_resident(moe):
+    # t = 4096, h = 4096, inter = 1536, E = 256, half the records resident
+    # after the first chunk.  Deterministic mode bit for bit the resident
+    # path's; atomic mode within the tolerance of the oracle on sampled rows.
+    w = synth.WORKLOADS["t4096_h4096_e256"]
+    inp, dev = _setup(moe, w)
+    ref = _resident(moe, w, dev, moe.MOE_DETERMINISTIC)
+    st = _streamer(moe, w, dev, 128, 64, 32)
+    state = ([-1] * 128, [0] * 128)
+    res = _streamed(moe, w, dev, st, moe.MOE_DETERMINISTIC)
+    np.testing.assert_array_equal(res["out"].view(torch.int16).cpu().numpy(),
+                                  ref["out"].view(torch.int16).cpu().numpy())
+    state = _check_plan(res, st, w.E, state, 1)
+    res = _streamed(moe, w, dev, st, 0)
+    state = _check_plan(res, st, w.E, state, 2)
+    assert res["stats"]["streamed"] == 128 and res["stats"]["resident"] == 128
+    rows = np.random.default_rng([w.seed, 78]).choice(w.t, 16, replace=False)
+    sub = dict(inp)
+    sub["x"] = inp["x"][rows]
+    oref = O.moe_forward(sub, w.k, w.h, w.inter, w.shared_inter)
+    got = res["out"].float().cpu().numpy().astype(np.float64)[rows]
+    err = np.abs(got - oref["out"]).max()
+    tol = TOL_REL * np.abs(oref["out"]).max() + TOL_ABS
+    assert err <= tol, f"max|gpu-oracle| = {err:.4g} > {tol:.4g}"
+    st.close()
