@@ -747,7 +747,7 @@ def moe_forward_streamed(dev: dict, dims: MoeDims, st: Streamer, flags: int = MO
     _check(lib.moe_forward_streamed(_ptr(x), _ptr(wr), _ptr(rbias), st.host_records.data_ptr(), _ptr(st.slots),
                                     ctypes.byref(shared) if shared is not None else None, ctypes.byref(dims), flags,
                                     _ptr(idx), _ptr(w), ctypes.byref(c), _ptr(out), _ptr(ws), ws.numel(),
-                                    _stream(stream), st._h, ctypes.byref(stats)))
+                                    st._h, _stream(stream), ctypes.byref(stats)))
     return dict(idx=idx, w=w, csr=csr, out=out, ws=ws,
                 stats=dict(resident=stats.resident, filled=stats.filled, streamed=stats.streamed,
                            batches=stats.batches, bytes=stats.bytes))
