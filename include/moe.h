@@ -405,7 +405,8 @@ typedef struct {
  *   3. batch 0 (resident experts and the shared expert) runs on `stream`
  *      while the streamer's copy stream fetches batch 1;
  *   4. per fetch batch b: the copy stream waits for event "done" of batch
- *      wait_for[b], issues one host -> device copy per record and records
+ *      wait_for[b], issues one host -> device copy per record (one per run
+ *      of consecutive experts bound for consecutive slots) and records
  *      event "fetched"; `stream` waits for "fetched", runs the batch's
  *      experts (tile schedule, gather, gate/up, down) and records "done".
  *   5. the last batch finalises `out`.

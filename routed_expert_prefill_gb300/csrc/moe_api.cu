@@ -460,22 +460,36 @@ int moe_forward_streamed(const uint16_t* x, const uint16_t* wr, const float* rbi
   const uint8_t* s_packed = dims->shared_inter > 0 ? shared->codes : nullptr;
   uint16_t* xg = (uint16_t*)(wsb + L.xg);
   PackedBatch pb{st->d_maps, P + R, st->d_maps + E, 0, true, pl.n_batches == 1};
-  // 3. batch 0: the resident experts and the shared expert, no fetch
-  if ((e = launch_experts_packed(a, slots, s_packed, xg, det, s, &pb)) != cudaSuccess) return fail(e, "batch 0");
-  // 4. the fetch batches, two events each
+  // 3-4. the fetch batches, two events each, and batch 0 (the resident
+  // experts and the shared expert, no fetch).  Fetch batch 1 is enqueued
+  // first so that the copies start while batch 0's launches are issued.
   size_t copied = 0;
   int nc = 0;
-  for (int b = 1; b < pl.n_batches; ++b) {
-    if (pl.wait_for[b] >= 1 && (e = cudaStreamWaitEvent(st->copy, st->done[pl.wait_for[b] % lag], 0)) != cudaSuccess)
-      return fail(e, "copy-stream wait");
-    for (; nc < pl.n_copies && batch_of[pl.copy_expert[nc]] == b; ++nc) {
-      const size_t rb = st->rec_bytes;
-      if ((e = cudaMemcpyAsync(slots + (size_t)pl.copy_slot[nc] * rb, host_records + (size_t)pl.copy_expert[nc] * rb,
-                               rb, cudaMemcpyHostToDevice, st->copy)) != cudaSuccess)
-        return fail(e, "record copy");
-      copied += rb;
+  // fetch batch b: wait until the batch that last read its ring slots is
+  // done, then one copy per run of records that are adjacent both in host
+  // memory and in the slots (consecutive experts in consecutive ring slots)
+  auto fetch = [&](int b) -> cudaError_t {
+    cudaError_t r;
+    if (pl.wait_for[b] >= 1 && (r = cudaStreamWaitEvent(st->copy, st->done[pl.wait_for[b] % lag], 0)) != cudaSuccess)
+      return r;
+    const size_t rb = st->rec_bytes;
+    while (nc < pl.n_copies && batch_of[pl.copy_expert[nc]] == b) {
+      int run = 1;
+      while (nc + run < pl.n_copies && batch_of[pl.copy_expert[nc + run]] == b &&
+             pl.copy_expert[nc + run] == pl.copy_expert[nc] + run && pl.copy_slot[nc + run] == pl.copy_slot[nc] + run)
+        ++run;
+      if ((r = cudaMemcpyAsync(slots + (size_t)pl.copy_slot[nc] * rb, host_records + (size_t)pl.copy_expert[nc] * rb,
+                               run * rb, cudaMemcpyHostToDevice, st->copy)) != cudaSuccess)
+        return r;
+      copied += run * rb;
+      nc += run;
     }
-    if ((e = cudaEventRecord(st->fetched, st->copy)) != cudaSuccess) return fail(e, "event record");
+    return cudaEventRecord(st->fetched, st->copy);
+  };
+  if (pl.n_batches > 1 && (e = fetch(1)) != cudaSuccess) return fail(e, "record fetch");
+  if ((e = launch_experts_packed(a, slots, s_packed, xg, det, s, &pb)) != cudaSuccess) return fail(e, "batch 0");
+  for (int b = 1; b < pl.n_batches; ++b) {
+    if (b > 1 && (e = fetch(b)) != cudaSuccess) return fail(e, "record fetch");
     if ((e = cudaStreamWaitEvent(s, st->fetched, 0)) != cudaSuccess) return fail(e, "stream wait");
     pb.batch = b;
     pb.first = false;
