@@ -22,6 +22,10 @@ engine, rustdoc source pages):
   order gathers its rows (``gather_rows``), runs the gate and up quantised
   matmuls, ``silu_mul``, the down quantised matmul, and scatter-adds the
   result times the routing weight (``scatter_add_rows``).
+* ``prefill/experts.rs``, ``prepare_expert_jobs``: a job whose record is a
+  resident pool record of the base kind keeps the base layout; the ring's
+  transient misses take the ``--miss-experts`` store (``experts_fwd``'s
+  optional ``miss`` store).
 * ``prefill/experts.rs``, ``Q { w, s, b, out, inp }``: affine quantisation,
   ``W[o, i] = q[o, i] * s[o, i // 64] + b[o, i // 64]``, with codes of
   ``l.bits`` bits (``pf_experts`` passes the layout's ``bits`` to every
@@ -255,12 +259,20 @@ def ffn(X: np.ndarray, gate: np.ndarray, up: np.ndarray, down: np.ndarray) -> np
 
 def experts_fwd(x_bits, offsets, rows, weights, codes, scales, biases,
                 shared_codes, shared_scales, shared_biases, h: int, inter: int,
-                shared_inter: int, shared_gate_bits=None, bits: int = 4) -> np.ndarray:
+                shared_inter: int, shared_gate_bits=None, bits: int = 4, miss=None) -> np.ndarray:
     """Block output [t, h] in float64.
 
     Zeroed output; the shared expert over all rows (times the optional
     per-row gate); then experts in ascending order: gather the expert's rows,
     gate/up, silu*up, down, and add weight * result into the gathered rows.
+
+    ``miss``: optional second record store for the experts that stream
+    through the ring (``prefill/experts.rs``, ``prepare_expert_jobs``: a
+    job whose record is a resident pool record of the base kind keeps the
+    base layout; every other job, the ring's transient misses, takes the
+    ``--miss-experts`` layout).  A dict with ``codes``, ``scales``,
+    ``biases``, ``bits`` and ``experts``, the ids whose records come from
+    this store; the shared expert always uses the base store.
     """
     X = bf16_to_f64(x_bits)
     t = X.shape[0]
@@ -277,17 +289,21 @@ def experts_fwd(x_bits, offsets, rows, weights, codes, scales, biases,
         if a == b:
             continue
         r = np.asarray(rows[a:b], np.int64)
-        G, U, D = expert_matrices(codes[e], scales[e], biases[e], h, inter, bits)
+        if miss is not None and e in miss["experts"]:
+            G, U, D = expert_matrices(miss["codes"][e], miss["scales"][e], miss["biases"][e], h, inter,
+                                      miss["bits"])
+        else:
+            G, U, D = expert_matrices(codes[e], scales[e], biases[e], h, inter, bits)
         y = ffn(X[r], G, U, D)
         out[r] += np.asarray(weights[a:b], np.float64)[:, None] * y
     return out
 
 
-def moe_forward(inp: dict, k: int, h: int, inter: int, shared_inter: int):
+def moe_forward(inp: dict, k: int, h: int, inter: int, shared_inter: int, miss=None):
     """Router + grouping + experts over the inputs of ``synth.make_inputs``.
 
     Returns a dict with logits, idx, w, the CSR arrays, out (fp64) and
-    out_bf16 (bit patterns).
+    out_bf16 (bit patterns).  ``miss`` as in ``experts_fwd``.
     """
     logits = route_logits(inp["x"], inp["wr"], inp.get("rbias"))
     idx, w = route_topk(logits, k)
@@ -296,6 +312,6 @@ def moe_forward(inp: dict, k: int, h: int, inter: int, shared_inter: int):
     out = experts_fwd(inp["x"], offsets, rows, weights, inp["codes"], inp["scales"],
                       inp["biases"], inp["shared_codes"], inp["shared_scales"],
                       inp["shared_biases"], h, inter, shared_inter, inp.get("shared_gate"),
-                      inp.get("bits", 4))
+                      inp.get("bits", 4), miss)
     return dict(logits=logits, idx=idx, w=w, offsets=offsets, rows=rows, weights=weights,
                 slot_of=slot_of, out=out, out_bf16=f64_to_bf16(out))

@@ -119,3 +119,11 @@ def plan(counts, pool_expert, pool_last, call, ring, group):
     wait_for = [0] + [b - lag if b - lag >= 1 else 0 for b in range(1, n_batches)]
     return dict(rec=rec, batch=batch, copies=copies, n_batches=n_batches, wait_for=wait_for,
                 pool_expert=pool_expert, pool_last=pool_last)
+
+
+def miss_experts(p, pool_slots):
+    """Experts of plan ``p`` whose record this chunk reads from a ring slot:
+    the transient misses, which take the ``--miss-experts`` store
+    (``prepare_expert_jobs``: only a resident pool record keeps the base
+    layout)."""
+    return {e for e, r in enumerate(p["rec"]) if r >= pool_slots}

@@ -407,3 +407,66 @@ def test_low_bit_record_has_the_width_of_its_codes(bits):
     s = inp["scales"][0].astype(np.float64)
     tol = 4 * (2 ** bits / math.sqrt(12)) / math.sqrt(G.size)
     assert abs(G.mean() / s.mean() + 0.5) < tol
+
+
+# ------------------------------------------------- streamed-miss record store
+
+def _miss_store(w, bits):
+    m = synth.make_inputs(w.replace(bits=bits))
+    return m["codes"], m["scales"], m["biases"]
+
+
+def test_miss_store_equal_to_the_base_store_changes_nothing():
+    w = synth.WORKLOADS["tiny_t16_h256_e8"]
+    inp = synth.make_inputs(w)
+    base = O.moe_forward(inp, w.k, w.h, w.inter, w.shared_inter)
+    miss = dict(codes=inp["codes"], scales=inp["scales"], biases=inp["biases"], bits=4, experts={0, 3, 5})
+    mixed = O.moe_forward(inp, w.k, w.h, w.inter, w.shared_inter, miss=miss)
+    np.testing.assert_array_equal(mixed["out"], base["out"])
+
+
+def test_every_expert_from_a_same_width_miss_store_is_that_store():
+    # a second 4-bit store (another draw) serving every routed expert equals
+    # the forward pass over that store, with the same shared expert
+    w = synth.WORKLOADS["tiny_t16_h256_e8"]
+    inp = synth.make_inputs(w)
+    other = synth.make_inputs(w.replace(seed=w.seed + 100))
+    miss = dict(codes=other["codes"], scales=other["scales"], biases=other["biases"], bits=4,
+                experts=set(range(w.E)))
+    mixed = O.moe_forward(inp, w.k, w.h, w.inter, w.shared_inter, miss=miss)
+    swapped = dict(inp, codes=other["codes"], scales=other["scales"], biases=other["biases"])
+    ref = O.moe_forward(swapped, w.k, w.h, w.inter, w.shared_inter)
+    np.testing.assert_array_equal(mixed["out"], ref["out"])
+
+
+def test_mixed_widths_brute_force_per_row():
+    # base records at 4 bits, the misses of experts 1, 2 and 6 at 2 bits:
+    # each row evaluated directly, with each expert's matrices taken from the
+    # store that serves it; and the result differs from both single-store
+    # passes (the selection matters)
+    w = synth.WORKLOADS["tiny_t16_h256_e8"]
+    inp = synth.make_inputs(w)
+    mc, ms, mb = _miss_store(w, 2)
+    streamed = {1, 2, 6}
+    miss = dict(codes=mc, scales=ms, biases=mb, bits=2, experts=streamed)
+    res = O.moe_forward(inp, w.k, w.h, w.inter, w.shared_inter, miss=miss)
+    X = O.bf16_to_f64(inp["x"])
+    S = O.expert_matrices(inp["shared_codes"], inp["shared_scales"], inp["shared_biases"], w.h, w.shared_inter)
+    direct = np.zeros((w.t, w.h))
+    for r in range(w.t):
+        acc = O.ffn(X[r:r + 1], *S)[0]
+        for j in range(w.k):
+            e = int(res["idx"][r, j])
+            if e in streamed:
+                m = O.expert_matrices(mc[e], ms[e], mb[e], w.h, w.inter, 2)
+            else:
+                m = O.expert_matrices(inp["codes"][e], inp["scales"][e], inp["biases"][e], w.h, w.inter)
+            acc = acc + float(res["w"][r, j]) * O.ffn(X[r:r + 1], *m)[0]
+        direct[r] = acc
+    scale = np.abs(direct).max()
+    assert np.abs(res["out"] - direct).max() <= 1e-12 * scale
+    base = O.moe_forward(inp, w.k, w.h, w.inter, w.shared_inter)
+    assert np.abs(res["out"] - base["out"]).max() > 1e-3 * scale
+    all_miss = O.moe_forward(inp, w.k, w.h, w.inter, w.shared_inter,
+                             miss=dict(miss, experts=set(range(w.E))))
+    assert np.abs(res["out"] - all_miss["out"]).max() > 1e-3 * scale
