@@ -57,6 +57,7 @@ EXTRA_WORKLOADS = ("t4096_h2048_e128_skewed", "t512_h2048_e128", "decode_t1_h204
 # The streamed-experts line: the headline chunk with its routed records in
 # host memory, half of them resident in a device pool after the first chunk.
 STREAMED = "t4096_h4096_e256_streamed"
+STREAMED_MISS2 = "t4096_h4096_e256_streamed_miss2"  # the ring's records from a 2-bit miss store
 STREAMED_CFG = dict(pool_slots=128, ring_slots=64, group=32)
 L2_BYTES = 129 * 2 ** 20
 SUSTAIN_S, SUSTAIN_MIN_RUNS, SUSTAIN_MAX_RUNS = 1.0, 50, 20000
@@ -594,19 +595,27 @@ def measure(ctx: Ctx, w: synth.Workload, inp: dict, headline: bool) -> dict:
         graph=graph is not None, flags=flags)
 
 
-def measure_streamed(ctx: Ctx, w: synth.Workload, inp: dict) -> dict:
+def measure_streamed(ctx: Ctx, w: synth.Workload, inp: dict, miss_bits: int = 0) -> dict:
     """Time moe_forward_streamed on workload ``w`` in its steady state (the
     pool filled by the warm-up chunks): every step routes, plans, fetches the
     non-resident records from pinned host memory over the host link and runs
-    the batches.  Bound: the host-to-device copy rate, measured here on the
-    same pinned buffer."""
+    the batches.  With ``miss_bits`` the ring's records come from a store
+    packed at that width (the workload's records drawn at that width).
+    Bound: the host-to-device copy rate, measured here on the same pinned
+    buffer."""
     torch, moe, args = ctx.torch, ctx.moe, ctx.args
     flags = MOE_PACKED_WEIGHTS
+    host_miss = None
+    if miss_bits:
+        wm = w.replace(bits=miss_bits)
+        dm = ctx.device_inputs(wm, synth.make_inputs(wm), flags)
+        host_miss = dm["packed"].cpu().pin_memory()
+        del dm
     dev = ctx.device_inputs(w, inp, flags)
     dims = moe.dims_of(w.t, w.h, w.inter, w.E, w.k, w.shared_inter, w.bits)
     host = dev["packed"].cpu().pin_memory()
     st = moe.Streamer(dims, STREAMED_CFG["pool_slots"], STREAMED_CFG["ring_slots"], STREAMED_CFG["group"], host,
-                      ctx.dev)
+                      ctx.dev, host_miss_records=host_miss, miss_bits=miss_bits)
     ws = moe.new_workspace(dims, flags, ctx.dev)
     out = torch.empty((w.t, w.h), dtype=torch.bfloat16, device=ctx.dev)
     bufs = dict(route=(torch.empty((w.t, w.k), dtype=torch.int32, device=ctx.dev),
@@ -664,9 +673,11 @@ def measure_streamed(ctx: Ctx, w: synth.Workload, inp: dict) -> dict:
     ach = moved / (ms * 1e-3) / 1e9
     return dict(
         value=job_tokens_per_s(ctx.world, w.t, ms), unit="tokens/s", ms_per_step=ms,
-        config={"workload": STREAMED, "t": w.t, "h": w.h, "inter": w.inter, "E": w.E, "k": w.k,
-                "shared_inter": w.shared_inter, "bits": w.bits, **STREAMED_CFG,
-                "records": "packed routed records in pinned host memory; shared record on the device",
+        config={"workload": STREAMED_MISS2 if miss_bits else STREAMED, "t": w.t, "h": w.h, "inter": w.inter,
+                "E": w.E, "k": w.k, "shared_inter": w.shared_inter, "bits": w.bits, **STREAMED_CFG,
+                "miss_bits": miss_bits or w.bits,
+                "records": "packed routed records in pinned host memory; shared record on the device"
+                           + ("; ring records from a 2-bit miss store" if miss_bits else ""),
                 "resident_experts": last["resident"], "filled_per_step": last["filled"],
                 "streamed_per_step": last["streamed"], "fetch_batches": last["batches"],
                 "bytes_copied_per_step": moved, "step_ms_min": min(step_ms), "step_ms_max": max(step_ms),
@@ -696,12 +707,13 @@ def run_ours(args, w: synth.Workload, pool):
     inp = pool.inp if pool is not None else synth.make_inputs(w)
     m = measure(ctx, w, inp, True)
     extras = {}
-    if STREAMED in args.extra:
-        extras[STREAMED] = measure_streamed(ctx, synth.WORKLOADS[DEFAULT_WORKLOAD],
+    for name, mb in ((STREAMED, 0), (STREAMED_MISS2, 2)):
+        if name in args.extra:
+            extras[name] = measure_streamed(ctx, synth.WORKLOADS[DEFAULT_WORKLOAD],
                                             inp if w.name == DEFAULT_WORKLOAD else
-                                            synth.make_inputs(synth.WORKLOADS[DEFAULT_WORKLOAD]))
+                                            synth.make_inputs(synth.WORKLOADS[DEFAULT_WORKLOAD]), mb)
     for name in args.extra:
-        if name == STREAMED:
+        if name in (STREAMED, STREAMED_MISS2):
             continue
         wx = synth.WORKLOADS[name]
         mx = measure(ctx, wx, synth.make_inputs(wx), False)
@@ -769,14 +781,14 @@ def main():
         ap.error("--warmup must be at least 3")
     w = synth.WORKLOADS[args.workload]
     if args.workloads == "default":
-        args.extra = ([STREAMED] + [n for n in EXTRA_WORKLOADS if n != w.name]
+        args.extra = ([STREAMED, STREAMED_MISS2] + [n for n in EXTRA_WORKLOADS if n != w.name]
                       if w.name == DEFAULT_WORKLOAD else [])
     elif args.workloads == "none":
         args.extra = []
     else:
         args.extra = [n for n in args.workloads.split(",") if n]
         for n in args.extra:
-            if n not in synth.WORKLOADS and n != STREAMED:
+            if n not in synth.WORKLOADS and n not in (STREAMED, STREAMED_MISS2):
                 ap.error(f"unknown workload {n}")
     if args.impl == "reference":
         run_reference(args, w)

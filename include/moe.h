@@ -340,11 +340,16 @@ int moe_pack_experts(const moe_qweights* src, const moe_dims* dims, int shared, 
  *   4. the copies, in that order, form fetch batches 1, 2, ... of `group`
  *      copies each; fetch batch b overwrites ring slots only after batch
  *      wait_for[b] = b - ring_slots / group (when >= 1) has finished.
+ * Records read from a pool slot keep the base layout (dims->bits); the
+ * ring's transient misses may come from a second store at another code
+ * width (prefill/experts.rs, prepare_expert_jobs: "--miss-experts"), which
+ * moves fewer bytes over the host link.
  */
 typedef struct {
   int32_t pool_slots; /* >= 0: record slots whose contents persist across calls */
   int32_t ring_slots; /* a positive multiple of group: slots refilled by every call */
   int32_t group;      /* >= 1: records per fetch batch */
+  int32_t miss_bits;  /* code width of the ring's records: 0 (= dims->bits), 2, 3, 4 or 8 */
 } moe_stream_cfg;
 
 /* One chunk's plan; every pointer is a caller-owned HOST array. */
@@ -368,6 +373,11 @@ typedef struct {
  * [1, 1024]). */
 int moe_plan_residency(const int32_t* counts, int32_t E, const moe_stream_cfg* cfg, int64_t call,
                        moe_residency_plan* plan);
+
+/* Bytes of the device slot buffer for `dims` and `cfg`: pool_slots records
+ * at dims->bits, then ring_slots records at the miss width; 0 on bad
+ * arguments.  Host only. */
+size_t moe_stream_slot_bytes(const moe_dims* dims, const moe_stream_cfg* cfg);
 
 /* A streaming context: the pool table and call counter, a copy stream,
  * the events of the batch protocol, pinned staging for the expert counts
@@ -396,6 +406,8 @@ typedef struct {
  * idx, w and csr as moe_route_csr, and `out` within the same tolerance as
  * moe_experts_fwd on the packed records (bit for bit with
  * MOE_DETERMINISTIC: each row sums its terms in the same fixed order).
+ * With a miss store, the experts read from ring slots this chunk use its
+ * records instead (the chunk's output then depends on the plan).
  *
  *   1. router and grouping on `stream`; the per-expert counts are copied to
  *      the host and the host waits for them (the one point where this call
@@ -410,13 +422,20 @@ typedef struct {
  *      event "fetched"; `stream` waits for "fetched", runs the batch's
  *      experts (tile schedule, gather, gate/up, down) and records "done".
  *   5. the last batch finalises `out`.
+ * With a miss store of another width, a batch that holds both pool fills
+ * and ring records runs as two passes of the expert kernels, one per width.
  *
  * host_records: E packed routed records (moe_packed_bytes(dims, 0) bytes),
  *   in page-locked host memory (cudaHostAlloc) for the copies to run
  *   asynchronously; on a Grace machine any memory the GPU can address.
- * slots: device buffer of (pool_slots + ring_slots) * moe_packed_bytes(dims,
- *   0) / E bytes, 16-byte aligned, used only through `st` (its pool slots
- *   keep their records between calls).
+ *   Pool slots are filled from it.
+ * host_miss_records: the miss store, E packed records at the streamer's
+ *   miss width, read for every ring slot; NULL (or ignored) when the miss
+ *   width equals dims->bits, and ring slots are then filled from
+ *   host_records.
+ * slots: device buffer of moe_stream_slot_bytes(dims, cfg) bytes, 16-byte
+ *   aligned, used only through `st` (its pool slots keep their records
+ *   between calls).
  * shared: the packed shared record on the device (MOE_PACKED_WEIGHTS
  *   layout), or NULL when shared_inter == 0.
  * flags: MOE_PACKED_WEIGHTS (required) and optionally MOE_DETERMINISTIC;
@@ -428,7 +447,8 @@ typedef struct {
  * MOE_ECUDA.
  */
 int moe_forward_streamed(const uint16_t* x, const uint16_t* wr, const float* rbias, const uint8_t* host_records,
-                         uint8_t* slots, const moe_shared* shared, const moe_dims* dims, uint32_t flags,
+                         const uint8_t* host_miss_records, uint8_t* slots, const moe_shared* shared,
+                         const moe_dims* dims, uint32_t flags,
                          int32_t* idx, float* w, const moe_csr* csr, uint16_t* out, void* ws, size_t ws_bytes,
                          moe_streamer* st, void* stream, moe_stream_stats* stats);
 

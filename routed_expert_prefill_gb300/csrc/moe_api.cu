@@ -386,9 +386,10 @@ int moe_forward(const uint16_t* x, const uint16_t* wr, const float* rbias, const
 }
 
 int moe_forward_streamed(const uint16_t* x, const uint16_t* wr, const float* rbias, const uint8_t* host_records,
-                         uint8_t* slots, const moe_shared* shared, const moe_dims* dims, uint32_t flags,
-                         int32_t* idx, float* w, const moe_csr* csr, uint16_t* out, void* ws, size_t ws_bytes,
-                         moe_streamer* st, void* stream, moe_stream_stats* stats) {
+                         const uint8_t* host_miss_records, uint8_t* slots, const moe_shared* shared,
+                         const moe_dims* dims, uint32_t flags, int32_t* idx, float* w, const moe_csr* csr,
+                         uint16_t* out, void* ws, size_t ws_bytes, moe_streamer* st, void* stream,
+                         moe_stream_stats* stats) {
   TRY(check_dims(dims));
   if (!st) return set_error(MOE_EINVAL, "streamer is NULL");
   if (flags & ~(MOE_PACKED_WEIGHTS | MOE_DETERMINISTIC | MOE_FORCE_LARGE_T))
@@ -403,7 +404,12 @@ int moe_forward_streamed(const uint16_t* x, const uint16_t* wr, const float* rbi
   TRY(cuda_status(cudaGetDevice(&dev), "cudaGetDevice"));
   if (dev != st->device)
     return set_error(MOE_EINVAL, "the streamer serves device %d, the current device is %d", st->device, dev);
+  // a miss store of another width puts the ring in a region of its own
+  const int base_bits = dims_bits(dims);
+  const bool split = st->miss_bits != base_bits;
   TRY(check_ptr(host_records, "host_records", 16));
+  if (split) TRY(check_ptr(host_miss_records, "host_miss_records", 16));
+  if (!split) host_miss_records = host_records;
   TRY(check_ptr(slots, "slots", 16));
   TRY(check_ptr(out, "out", 16));
   if (dims->shared_inter > 0) {
@@ -417,6 +423,8 @@ int moe_forward_streamed(const uint16_t* x, const uint16_t* wr, const float* rbi
   TRY(moe_route_csr(x, wr, rbias, dims, idx, w, csr, ws, ws_bytes, stream));
 
   const int E = dims->E, P = st->cfg.pool_slots, R = st->cfg.ring_slots, lag = R / st->cfg.group;
+  const size_t rb = st->rec_bytes, rm = st->miss_bytes;
+  uint8_t* ring_base = slots + (size_t)P * rb;
   // after a failure the pool's contents are unknown: empty it
   auto fail = [&](cudaError_t e, const char* what) {
     std::fill(st->pool_expert.begin(), st->pool_expert.end(), -1);
@@ -433,13 +441,11 @@ int moe_forward_streamed(const uint16_t* x, const uint16_t* wr, const float* rbi
     st->counts[i] = n > 0 ? n : 0;  // bad offsets: flagged on the device, nothing runs
   }
   // 2. the plan, and the record and batch maps on the device
-  int32_t* rec = st->h_maps;
-  int32_t* batch_of = st->h_maps + E;
   moe_residency_plan pl{};
   pl.pool_expert = st->pool_expert.data();
   pl.pool_last = st->pool_last.data();
-  pl.rec = rec;
-  pl.batch = batch_of;
+  pl.rec = st->plan_rec.data();
+  pl.batch = st->plan_batch.data();
   pl.copy_expert = st->copy_expert.data();
   pl.copy_slot = st->copy_slot.data();
   pl.wait_for = st->wait_for.data();
@@ -448,7 +454,21 @@ int moe_forward_streamed(const uint16_t* x, const uint16_t* wr, const float* rbi
     std::fill(st->pool_expert.begin(), st->pool_expert.end(), -1);
     return ps;
   }
-  batch_of[E] = 0;  // the shared expert runs with the resident ones
+  // One code width: rec is the record's index in the slot buffer and
+  // batch_of its batch.  Two widths: rec counts within the record's region
+  // (pool or ring) and batch_of = 2 batch + (ring record), so that each pass
+  // of the expert kernels sees one width.  batch_of[E] is the shared expert.
+  int32_t* map_rec = st->h_maps;
+  int32_t* map_batch = st->h_maps + E;
+  std::vector<uint8_t> has_base(pl.n_batches, 0), has_ring(pl.n_batches, 0);
+  for (int i = 0; i < E; ++i) {
+    const int r = st->plan_rec[i], b = st->plan_batch[i];
+    const bool ring = r >= P;
+    map_rec[i] = (split && ring) ? r - P : r;
+    map_batch[i] = (split && b >= 0) ? 2 * b + (ring ? 1 : 0) : b;
+    if (b >= 0) (ring ? has_ring : has_base)[b] = 1;
+  }
+  map_batch[E] = 0;
   if ((e = cudaMemcpyAsync(st->d_maps, st->h_maps, (2 * E + 1) * sizeof(int32_t), cudaMemcpyHostToDevice, s)) !=
       cudaSuccess)
     return fail(e, "map copy");
@@ -459,48 +479,80 @@ int moe_forward_streamed(const uint16_t* x, const uint16_t* wr, const float* rbi
   const bool det = (flags & MOE_DETERMINISTIC) != 0;
   const uint8_t* s_packed = dims->shared_inter > 0 ? shared->codes : nullptr;
   uint16_t* xg = (uint16_t*)(wsb + L.xg);
-  PackedBatch pb{st->d_maps, P + R, st->d_maps + E, 0, true, pl.n_batches == 1};
+  // the passes of the expert kernels, in order: per batch, one pass (one
+  // width) or, with two widths, a pool pass and/or a ring pass
+  struct Pass {
+    int batch, filter;
+    bool ring;
+  };
+  std::vector<Pass> passes;
+  for (int b = 0; b < pl.n_batches; ++b) {
+    if (!split) {
+      passes.push_back({b, b, false});
+      continue;
+    }
+    if (b == 0 || has_base[b]) passes.push_back({b, 2 * b, false});
+    if (has_ring[b]) passes.push_back({b, 2 * b + 1, true});
+  }
+  auto run = [&](size_t i) -> cudaError_t {
+    const Pass& q = passes[i];
+    ExpertsArgs aq = a;
+    aq.bits = q.ring ? st->miss_bits : base_bits;
+    PackedBatch pb{st->d_maps, split ? (q.ring ? R : P) : P + R, st->d_maps + E, q.filter, i == 0,
+                   i + 1 == passes.size()};
+    return launch_experts_packed(aq, q.ring ? ring_base : slots, s_packed, xg, det, s, &pb);
+  };
   // 3-4. the fetch batches, two events each, and batch 0 (the resident
   // experts and the shared expert, no fetch).  Fetch batch 1 is enqueued
   // first so that the copies start while batch 0's launches are issued.
   size_t copied = 0;
   int nc = 0;
+  // the source and destination of a copy: pool slots from the base store,
+  // ring slots from the miss store, each region with its own record size
+  auto src_of = [&](int ex, int slot) {
+    return slot < P ? host_records + (size_t)ex * rb : host_miss_records + (size_t)ex * (split ? rm : rb);
+  };
+  auto dst_of = [&](int slot) {
+    return slot < P ? slots + (size_t)slot * rb : ring_base + (size_t)(slot - P) * (split ? rm : rb);
+  };
   // fetch batch b: wait until the batch that last read its ring slots is
-  // done, then one copy per run of records that are adjacent both in host
-  // memory and in the slots (consecutive experts in consecutive ring slots)
+  // done, then one copy per run of consecutive experts bound for
+  // consecutive slots of one region
   auto fetch = [&](int b) -> cudaError_t {
     cudaError_t r;
     if (pl.wait_for[b] >= 1 && (r = cudaStreamWaitEvent(st->copy, st->done[pl.wait_for[b] % lag], 0)) != cudaSuccess)
       return r;
-    const size_t rb = st->rec_bytes;
-    while (nc < pl.n_copies && batch_of[pl.copy_expert[nc]] == b) {
+    while (nc < pl.n_copies && st->plan_batch[pl.copy_expert[nc]] == b) {
+      const int e0 = pl.copy_expert[nc], s0 = pl.copy_slot[nc];
+      const size_t bytes = s0 < P ? rb : (split ? rm : rb);
       int run = 1;
-      while (nc + run < pl.n_copies && batch_of[pl.copy_expert[nc + run]] == b &&
-             pl.copy_expert[nc + run] == pl.copy_expert[nc] + run && pl.copy_slot[nc + run] == pl.copy_slot[nc] + run)
+      while (nc + run < pl.n_copies && st->plan_batch[pl.copy_expert[nc + run]] == b &&
+             pl.copy_expert[nc + run] == e0 + run && pl.copy_slot[nc + run] == s0 + run &&
+             (pl.copy_slot[nc + run] < P) == (s0 < P))
         ++run;
-      if ((r = cudaMemcpyAsync(slots + (size_t)pl.copy_slot[nc] * rb, host_records + (size_t)pl.copy_expert[nc] * rb,
-                               run * rb, cudaMemcpyHostToDevice, st->copy)) != cudaSuccess)
+      if ((r = cudaMemcpyAsync(dst_of(s0), src_of(e0, s0), run * bytes, cudaMemcpyHostToDevice, st->copy)) !=
+          cudaSuccess)
         return r;
-      copied += run * rb;
+      copied += run * bytes;
       nc += run;
     }
     return cudaEventRecord(st->fetched, st->copy);
   };
+  size_t pi = 0;
   if (pl.n_batches > 1 && (e = fetch(1)) != cudaSuccess) return fail(e, "record fetch");
-  if ((e = launch_experts_packed(a, slots, s_packed, xg, det, s, &pb)) != cudaSuccess) return fail(e, "batch 0");
+  for (; pi < passes.size() && passes[pi].batch == 0; ++pi)
+    if ((e = run(pi)) != cudaSuccess) return fail(e, "batch 0");
   for (int b = 1; b < pl.n_batches; ++b) {
     if (b > 1 && (e = fetch(b)) != cudaSuccess) return fail(e, "record fetch");
     if ((e = cudaStreamWaitEvent(s, st->fetched, 0)) != cudaSuccess) return fail(e, "stream wait");
-    pb.batch = b;
-    pb.first = false;
-    pb.last = b == pl.n_batches - 1;
-    if ((e = launch_experts_packed(a, slots, s_packed, xg, det, s, &pb)) != cudaSuccess) return fail(e, "batch");
+    for (; pi < passes.size() && passes[pi].batch == b; ++pi)
+      if ((e = run(pi)) != cudaSuccess) return fail(e, "batch");
     if ((e = cudaEventRecord(st->done[b % lag], s)) != cudaSuccess) return fail(e, "event record");
   }
   if (stats) {
     stats->resident = 0;
     stats->filled = 0;
-    for (int i = 0; i < E; ++i) stats->resident += batch_of[i] == 0;
+    for (int i = 0; i < E; ++i) stats->resident += st->plan_batch[i] == 0;
     for (int i = 0; i < pl.n_copies; ++i) stats->filled += pl.copy_slot[i] < P;
     stats->streamed = pl.n_copies - stats->filled;
     stats->batches = pl.n_batches - 1;

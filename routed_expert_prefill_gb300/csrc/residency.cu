@@ -118,7 +118,19 @@ int check_cfg(const moe_stream_cfg* cfg) {
   if (cfg->ring_slots < cfg->group || cfg->ring_slots % cfg->group)
     return set_error(MOE_EINVAL, "ring_slots=%d must be a positive multiple of group=%d", cfg->ring_slots,
                      cfg->group);
+  const int mb = cfg->miss_bits;
+  if (mb != 0 && mb != 2 && mb != 3 && mb != 4 && mb != 8)
+    return set_error(MOE_EINVAL, "miss_bits=%d: 0, 2, 3, 4 or 8", mb);
   return MOE_OK;
+}
+
+// Record bytes at the pool's and at the ring's code width (0 on bad dims).
+void record_sizes(const moe_dims* dims, const moe_stream_cfg* cfg, size_t& base, size_t& miss, int& miss_bits) {
+  base = moe_packed_bytes(dims, 0) / dims->E;
+  moe_dims dm = *dims;
+  miss_bits = cfg->miss_bits ? cfg->miss_bits : (dims->bits ? dims->bits : 4);
+  dm.bits = miss_bits;
+  miss = moe_packed_bytes(&dm, 0) / dims->E;
 }
 
 }  // namespace
@@ -137,6 +149,15 @@ int moe_plan_residency(const int32_t* counts, int32_t E, const moe_stream_cfg* c
   return plan_residency(counts, E, *cfg, call, *plan);
 }
 
+size_t moe_stream_slot_bytes(const moe_dims* dims, const moe_stream_cfg* cfg) {
+  if (!dims || dims->E < 1 || dims->E > 1024 || check_cfg(cfg) != MOE_OK) return 0;
+  size_t rec, miss;
+  int miss_bits;
+  record_sizes(dims, cfg, rec, miss, miss_bits);
+  if (rec == 0 || miss == 0) return 0;
+  return (size_t)cfg->pool_slots * rec + (size_t)cfg->ring_slots * miss;
+}
+
 int moe_streamer_create(const moe_dims* dims, const moe_stream_cfg* cfg, moe_streamer** out) {
   if (!out) return set_error(MOE_EINVAL, "out is NULL");
   *out = nullptr;
@@ -144,13 +165,16 @@ int moe_streamer_create(const moe_dims* dims, const moe_stream_cfg* cfg, moe_str
   if (dims->E < 1 || dims->E > 1024) return set_error(MOE_ESHAPE, "E=%d outside [1, 1024]", dims->E);
   int s;
   if ((s = check_cfg(cfg)) != MOE_OK) return s;
-  const size_t all = moe_packed_bytes(dims, 0);  // 0 on bad dims, message set
-  if (all == 0) return MOE_ESHAPE;
-  const size_t rec = all / dims->E;
+  size_t rec, miss;
+  int miss_bits;
+  record_sizes(dims, cfg, rec, miss, miss_bits);  // 0 on bad dims, message set
+  if (rec == 0 || miss == 0) return MOE_ESHAPE;
   moe_streamer* st = new moe_streamer();
   st->dims = *dims;
   st->cfg = *cfg;
   st->rec_bytes = rec;
+  st->miss_bits = miss_bits;
+  st->miss_bytes = miss;
   st->call = 0;
   const int E = dims->E, P = cfg->pool_slots;
   st->pool_expert.assign(P, -1);
@@ -159,6 +183,8 @@ int moe_streamer_create(const moe_dims* dims, const moe_stream_cfg* cfg, moe_str
   st->copy_expert.assign(E, 0);
   st->copy_slot.assign(E, 0);
   st->wait_for.assign(E + 1, 0);
+  st->plan_rec.assign(E, -1);
+  st->plan_batch.assign(E, -1);
   auto fail = [&](cudaError_t e, const char* what) {
     moe_streamer_destroy(st);
     return set_error(MOE_ECUDA, "moe_streamer_create: %s: %s", what, cudaGetErrorString(e));

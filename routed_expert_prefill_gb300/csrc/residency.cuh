@@ -19,12 +19,14 @@ struct moe_streamer {
   int device;
   moe_dims dims;  // E, h, inter, bits fixed at creation (t and k vary per call)
   moe_stream_cfg cfg;
-  size_t rec_bytes;  // one packed routed record
+  size_t rec_bytes;  // one packed routed record at dims.bits (pool slots)
+  int miss_bits;     // code width of the ring's records
+  size_t miss_bytes; // one packed routed record at miss_bits (ring slots)
   int64_t call;      // call number of the last plan
   std::vector<int32_t> pool_expert;
   std::vector<int64_t> pool_last;
   // plan arrays
-  std::vector<int32_t> counts, copy_expert, copy_slot, wait_for;
+  std::vector<int32_t> counts, copy_expert, copy_slot, wait_for, plan_rec, plan_batch;
   int32_t* h_offsets = nullptr;  // pinned [E + 1]: the chunk's CSR offsets
   int32_t* h_maps = nullptr;     // pinned [2E + 1]: rec[E], batch_of[E + 1]
   int32_t* d_maps = nullptr;     // device copy of h_maps

@@ -52,6 +52,7 @@ EXPORTS = (
     "moe_forward",
     "moe_debug_stall",
     "moe_plan_residency",
+    "moe_stream_slot_bytes",
     "moe_streamer_create",
     "moe_streamer_destroy",
     "moe_streamer_pool",
@@ -84,7 +85,8 @@ class MoeProfileEntry(ctypes.Structure):
 
 
 class MoeStreamCfg(ctypes.Structure):
-    _fields_ = [("pool_slots", ctypes.c_int32), ("ring_slots", ctypes.c_int32), ("group", ctypes.c_int32)]
+    _fields_ = [("pool_slots", ctypes.c_int32), ("ring_slots", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("miss_bits", ctypes.c_int32)]
 
 
 class MoeResidencyPlan(ctypes.Structure):
@@ -154,6 +156,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_plan_residency.restype = ctypes.c_int
     lib.moe_plan_residency.argtypes = [vp, i32, ctypes.POINTER(MoeStreamCfg), ctypes.c_int64,
                                        ctypes.POINTER(MoeResidencyPlan)]
+    lib.moe_stream_slot_bytes.restype = sz
+    lib.moe_stream_slot_bytes.argtypes = [ctypes.POINTER(MoeDims), ctypes.POINTER(MoeStreamCfg)]
     lib.moe_streamer_create.restype = ctypes.c_int
     lib.moe_streamer_create.argtypes = [ctypes.POINTER(MoeDims), ctypes.POINTER(MoeStreamCfg),
                                         ctypes.POINTER(ctypes.c_void_p)]
@@ -162,7 +166,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_streamer_pool.restype = ctypes.c_int
     lib.moe_streamer_pool.argtypes = [vp, vp, i32]
     lib.moe_forward_streamed.restype = ctypes.c_int
-    lib.moe_forward_streamed.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(MoeShared), ctypes.POINTER(MoeDims), u32,
+    lib.moe_forward_streamed.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.POINTER(MoeShared), ctypes.POINTER(MoeDims), u32,
                                          vp, vp, ctypes.POINTER(MoeCsr), vp, vp, sz, vp, vp,
                                          ctypes.POINTER(MoeStreamStats)]
     lib.moe_pack_experts.restype = ctypes.c_int
@@ -640,7 +644,7 @@ def plan_residency(counts, pool_expert, pool_last, call: int, ring: int, group: 
     ce = np.empty(E, np.int32)
     cs = np.empty(E, np.int32)
     wf = np.empty(E + 1, np.int32)
-    cfg = MoeStreamCfg(pe.size, ring, group)
+    cfg = MoeStreamCfg(pe.size, ring, group, 0)
     addr = lambda a: a.ctypes.data if a.size else None  # noqa: E731
     plan = MoeResidencyPlan(addr(pe), addr(pl_), rec.ctypes.data, batch.ctypes.data, ce.ctypes.data,
                             cs.ctypes.data, wf.ctypes.data, 0, 0)
@@ -652,27 +656,46 @@ def plan_residency(counts, pool_expert, pool_last, call: int, ring: int, group: 
 
 class Streamer:
     """The library's streaming context (moe_streamer) with the device slot
-    buffer and the host copy of the packed routed records it streams from.
+    buffer and the host copies of the packed routed records it streams from.
 
     host_records: uint8 tensor of the E packed records in page-locked host
-    memory (``packed.cpu().pin_memory()``).  The slot buffer is allocated
-    on the current device: (pool_slots + ring_slots) records."""
+    memory (``packed.cpu().pin_memory()``).  host_miss_records: the miss
+    store, the E records packed at ``miss_bits`` (needed when miss_bits is
+    not 0 and differs from dims.bits), read for every ring slot.  The slot
+    buffer is allocated on the current device: pool_slots records at
+    dims.bits, then ring_slots records at the miss width."""
 
     def __init__(self, dims: MoeDims, pool_slots: int, ring_slots: int, group: int, host_records: torch.Tensor,
-                 device=None):
+                 device=None, host_miss_records: torch.Tensor | None = None, miss_bits: int = 0):
         lib = load_library()
         n = lib.moe_packed_bytes(ctypes.byref(dims), 0)
         if n == 0:
             raise MoeError(-2, "bad dims for a streamer")
-        _need(host_records, "host_records", (torch.uint8,), min_numel=n)
-        if host_records.device.type != "cpu":
-            raise ValueError("host_records must be a host (CPU) tensor")
+        self.cfg = MoeStreamCfg(pool_slots, ring_slots, group, miss_bits)
+        self.split = miss_bits not in (0, _code_bits(dims))
+        for name, t, bits in (("host_records", host_records, _code_bits(dims)),
+                              ("host_miss_records", host_miss_records if self.split else None, miss_bits)):
+            if t is None:
+                if name == "host_records" or self.split:
+                    raise ValueError(f"{name} is required")
+                continue
+            nb = lib.moe_packed_bytes(ctypes.byref(MoeDims(dims.t, dims.h, dims.inter, dims.E, dims.k,
+                                                           dims.shared_inter, bits)), 0)
+            _need(t, name, (torch.uint8,), min_numel=nb)
+            if t.device.type != "cpu":
+                raise ValueError(f"{name} must be a host (CPU) tensor")
         self.dims = MoeDims(*(getattr(dims, f) for f, _ in MoeDims._fields_))
-        self.cfg = MoeStreamCfg(pool_slots, ring_slots, group)
         self.rec_bytes = n // dims.E
+        self.miss_rec_bytes = self.rec_bytes
+        if self.split:
+            self.miss_rec_bytes = lib.moe_packed_bytes(ctypes.byref(MoeDims(
+                dims.t, dims.h, dims.inter, dims.E, dims.k, dims.shared_inter, miss_bits)), 0) // dims.E
         self.host_records = host_records
-        self.slots = torch.empty((pool_slots + ring_slots) * self.rec_bytes, dtype=torch.uint8,
-                                 device=device or "cuda")
+        self.host_miss_records = host_miss_records if self.split else None
+        nslot = lib.moe_stream_slot_bytes(ctypes.byref(self.dims), ctypes.byref(self.cfg))
+        if nslot == 0:
+            raise MoeError(-1, "bad streaming configuration")
+        self.slots = torch.empty(nslot, dtype=torch.uint8, device=device or "cuda")
         h = ctypes.c_void_p()
         _check(lib.moe_streamer_create(ctypes.byref(self.dims), ctypes.byref(self.cfg), ctypes.byref(h)))
         self._h = h
@@ -744,7 +767,8 @@ def moe_forward_streamed(dev: dict, dims: MoeDims, st: Streamer, flags: int = MO
                        shared_packed=dev.get("shared_packed") if Is > 0 else None, **_csr_named(csr, "csr"))
     stats = MoeStreamStats()
     c = csr.c()
-    _check(lib.moe_forward_streamed(_ptr(x), _ptr(wr), _ptr(rbias), st.host_records.data_ptr(), _ptr(st.slots),
+    miss = st.host_miss_records.data_ptr() if st.host_miss_records is not None else None
+    _check(lib.moe_forward_streamed(_ptr(x), _ptr(wr), _ptr(rbias), st.host_records.data_ptr(), miss, _ptr(st.slots),
                                     ctypes.byref(shared) if shared is not None else None, ctypes.byref(dims), flags,
                                     _ptr(idx), _ptr(w), ctypes.byref(c), _ptr(out), _ptr(ws), ws.numel(),
                                     st._h, _stream(stream), ctypes.byref(stats)))

@@ -50,9 +50,24 @@ def _setup(moe, w, seed_shift=0):
     return inp, dev
 
 
-def _streamer(moe, w, dev, pool, ring, group):
+def _streamer(moe, w, dev, pool, ring, group, miss=None):
     host = dev["packed"].cpu().pin_memory()
-    return moe.Streamer(_dims(moe, w), pool, ring, group, host)
+    if miss is None:
+        return moe.Streamer(_dims(moe, w), pool, ring, group, host)
+    bits, miss_packed = miss
+    return moe.Streamer(_dims(moe, w), pool, ring, group, host, host_miss_records=miss_packed.cpu().pin_memory(),
+                        miss_bits=bits)
+
+
+def _miss_store(moe, w, bits):
+    """The miss store: the workload's records drawn at another code width
+    (host arrays for the oracle, packed device records for the streamer)."""
+    wm = w.replace(bits=bits)
+    m = synth.make_inputs(wm)
+    dm = moe.upload_inputs(m)
+    packed = moe.pack_experts(dm["codes"], dm["scales"], dm["biases"], _dims(moe, wm))
+    torch.cuda.synchronize()
+    return dict(codes=m["codes"], scales=m["scales"], biases=m["biases"], bits=bits), packed
 
 
 def _resident(moe, w, dev, flags):
@@ -82,9 +97,9 @@ def _check_plan(res, st, E, oracle_state, call):
     assert s["filled"] == n_fill
     assert s["streamed"] == len(p["copies"]) - n_fill
     assert s["batches"] == p["n_batches"] - 1
-    assert s["bytes"] == len(p["copies"]) * st.rec_bytes
+    assert s["bytes"] == n_fill * st.rec_bytes + (len(p["copies"]) - n_fill) * st.miss_rec_bytes
     assert st.pool() == p["pool_expert"]
-    return p["pool_expert"], p["pool_last"]
+    return p["pool_expert"], p["pool_last"], R.miss_experts(p, P)
 
 
 CASES = [
@@ -119,6 +134,31 @@ def test_streamed_matches_oracle(moe, name, pool, ring, group):
     st.close()
 
 
+@pytest.mark.parametrize("bits", [2, 3, 8])
+@pytest.mark.parametrize("flags", [0, 1])
+def test_miss_store_matches_oracle(moe, bits, flags):
+    # 4-bit pool records, the ring's misses from a store at `bits`: the first
+    # chunk mixes pool fills and ring copies in one batch (two kernel passes,
+    # one per width), the second streams only misses; each chunk's output
+    # against the oracle with that chunk's misses taken from the miss store
+    w = synth.WORKLOADS["t512_h2048_e128"]
+    inp, dev = _setup(moe, w)
+    miss, miss_packed = _miss_store(moe, w, bits)
+    st = _streamer(moe, w, dev, 32, 16, 8, miss=(bits, miss_packed))
+    state = ([-1] * 32, [0] * 32)
+    for call in (1, 2):
+        res = _streamed(moe, w, dev, st, flags)
+        pool, last, streamed = _check_plan(res, st, w.E, state[:2], call)
+        state = (pool, last)
+        assert 0 < len(streamed) < w.E
+        ref = O.moe_forward(inp, w.k, w.h, w.inter, w.shared_inter, miss=dict(miss, experts=streamed))
+        got = res["out"].float().cpu().numpy().astype(np.float64)
+        err = np.abs(got - ref["out"]).max()
+        tol = TOL_REL * np.abs(ref["out"]).max() + TOL_ABS
+        assert err <= tol, f"call {call}: max|gpu-oracle| = {err:.4g} > {tol:.4g}"
+    st.close()
+
+
 @pytest.mark.parametrize("name,pool,ring,group", CASES)
 def test_streamed_deterministic_equals_resident_bitwise(moe, name, pool, ring, group):
     w = synth.WORKLOADS[name]
@@ -141,7 +181,7 @@ def test_pool_persists_across_chunks(moe):
     _, dev = _setup(moe, w)
     x0 = dev["x"]
     st = _streamer(moe, w, dev, 24, 16, 8)
-    state = ([-1] * 24, [0] * 24)
+    state = ([-1] * 24, [0] * 24, set())
     evicted = 0
     for call in range(1, 6):
         dev["x"] = torch.roll(x0, shifts=call * 5, dims=1).contiguous()  # new rows, new routing
@@ -150,7 +190,7 @@ def test_pool_persists_across_chunks(moe):
         res = _streamed(moe, w, dev, st, moe.MOE_DETERMINISTIC)
         np.testing.assert_array_equal(res["out"].view(torch.int16).cpu().numpy(),
                                       ref["out"].view(torch.int16).cpu().numpy())
-        state = _check_plan(res, st, w.E, state, call)
+        state = _check_plan(res, st, w.E, state[:2], call)
         evicted += len(before - set(state[0]) - {-1})
     assert evicted > 0
     st.close()
@@ -211,14 +251,38 @@ def test_headline_half_resident(moe):
     res = _streamed(moe, w, dev, st, moe.MOE_DETERMINISTIC)
     np.testing.assert_array_equal(res["out"].view(torch.int16).cpu().numpy(),
                                   ref["out"].view(torch.int16).cpu().numpy())
-    state = _check_plan(res, st, w.E, state, 1)
+    state = _check_plan(res, st, w.E, state, 1)[:2]
     res = _streamed(moe, w, dev, st, 0)
-    state = _check_plan(res, st, w.E, state, 2)
+    state = _check_plan(res, st, w.E, state, 2)[:2]
     assert res["stats"]["streamed"] == 128 and res["stats"]["resident"] == 128
     rows = np.random.default_rng([w.seed, 78]).choice(w.t, 16, replace=False)
     sub = dict(inp)
     sub["x"] = inp["x"][rows]
     oref = O.moe_forward(sub, w.k, w.h, w.inter, w.shared_inter)
+    got = res["out"].float().cpu().numpy().astype(np.float64)[rows]
+    err = np.abs(got - oref["out"]).max()
+    tol = TOL_REL * np.abs(oref["out"]).max() + TOL_ABS
+    assert err <= tol, f"max|gpu-oracle| = {err:.4g} > {tol:.4g}"
+    st.close()
+
+
+def test_headline_miss_store_two_bits(moe):
+    # the headline chunk with 2-bit misses after the first chunk: the oracle
+    # on sampled rows with the second chunk's misses from the 2-bit store
+    w = synth.WORKLOADS["t4096_h4096_e256"]
+    inp, dev = _setup(moe, w)
+    miss, miss_packed = _miss_store(moe, w, 2)
+    st = _streamer(moe, w, dev, 128, 64, 32, miss=(2, miss_packed))
+    state = ([-1] * 128, [0] * 128)
+    for call in (1, 2):
+        res = _streamed(moe, w, dev, st, 0)
+        pool, last, streamed = _check_plan(res, st, w.E, state, call)
+        state = (pool, last)
+    assert len(streamed) == 128 and res["stats"]["bytes"] == 128 * st.miss_rec_bytes
+    rows = np.random.default_rng([w.seed, 79]).choice(w.t, 16, replace=False)
+    sub = dict(inp)
+    sub["x"] = inp["x"][rows]
+    oref = O.moe_forward(sub, w.k, w.h, w.inter, w.shared_inter, miss=dict(miss, experts=streamed))
     got = res["out"].float().cpu().numpy().astype(np.float64)[rows]
     err = np.abs(got - oref["out"]).max()
     tol = TOL_REL * np.abs(oref["out"]).max() + TOL_ABS

@@ -106,6 +106,23 @@ def test_streamer_create_rejects_bad_config(lib):
 
 def test_forward_streamed_rejects_a_null_streamer(lib):
     dims = moe.MoeDims(16, 256, 256, 8, 2, 0, 4)
-    st = lib.moe_forward_streamed(None, None, None, None, None, None, ctypes.byref(dims), moe.MOE_PACKED_WEIGHTS,
+    st = lib.moe_forward_streamed(None, None, None, None, None, None, None, ctypes.byref(dims), moe.MOE_PACKED_WEIGHTS,
                                   None, None, None, None, None, 0, None, None, None)
     assert st == -1
+
+
+def test_slot_bytes_and_miss_width_checks(lib):
+    dims = moe.MoeDims(16, 256, 256, 8, 2, 0, 4)
+    rec4 = lib.moe_packed_bytes(ctypes.byref(dims), 0) // 8
+    rec2 = lib.moe_packed_bytes(ctypes.byref(moe.MoeDims(16, 256, 256, 8, 2, 0, 2)), 0) // 8
+    assert rec2 < rec4
+    same = moe.MoeStreamCfg(3, 4, 2, 0)
+    assert lib.moe_stream_slot_bytes(ctypes.byref(dims), ctypes.byref(same)) == 7 * rec4
+    miss = moe.MoeStreamCfg(3, 4, 2, 2)
+    assert lib.moe_stream_slot_bytes(ctypes.byref(dims), ctypes.byref(miss)) == 3 * rec4 + 4 * rec2
+    h = ctypes.c_void_p()
+    for bad in (1, 5, 16, -2):
+        cfg = moe.MoeStreamCfg(3, 4, 2, bad)
+        assert lib.moe_stream_slot_bytes(ctypes.byref(dims), ctypes.byref(cfg)) == 0
+        assert lib.moe_streamer_create(ctypes.byref(dims), ctypes.byref(cfg), ctypes.byref(h)) == -1
+        assert not h.value
