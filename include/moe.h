@@ -387,7 +387,7 @@ size_t moe_stream_slot_bytes(const moe_dims* dims, const moe_stream_cfg* cfg);
  * MOE_ESHAPE, MOE_ECUDA. */
 typedef struct moe_streamer moe_streamer;
 int moe_streamer_create(const moe_dims* dims, const moe_stream_cfg* cfg, moe_streamer** out);
-int moe_streamer_destroy(moe_streamer* st); /* waits for its copy stream; NULL is a no-op */
+int moe_streamer_destroy(moe_streamer* st); /* synchronises the device first; NULL is a no-op */
 /* The pool table: the expert held by each pool slot (-1 = free) into
  * pool_expert[0 .. min(n, pool_slots)); returns that count or a negative
  * moe_status. */

@@ -209,7 +209,9 @@ int moe_streamer_create(const moe_dims* dims, const moe_stream_cfg* cfg, moe_str
 
 int moe_streamer_destroy(moe_streamer* st) {
   if (!st) return MOE_OK;
-  if (st->copy) cudaStreamSynchronize(st->copy);
+  // kernels of earlier calls may still read the device maps, and copies
+  // the pinned staging: let the device finish first
+  cudaDeviceSynchronize();
   for (auto ev : st->done)
     if (ev) cudaEventDestroy(ev);
   if (st->fetched) cudaEventDestroy(st->fetched);
