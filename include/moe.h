@@ -398,7 +398,9 @@ typedef struct {
   int32_t filled;   /* records copied into pool slots */
   int32_t streamed; /* records copied into ring slots */
   int32_t batches;  /* fetch batches */
-  int64_t bytes;    /* bytes copied host -> device */
+  int64_t bytes;    /* bytes copied host -> device (speculative copies included) */
+  int32_t prefetched;    /* records fetched speculatively while the chunk was routed */
+  int32_t prefetch_used; /* 1 when they were the plan's first fetch batch */
 } moe_stream_stats;
 
 /*
@@ -411,7 +413,12 @@ typedef struct {
  *
  *   1. router and grouping on `stream`; the per-expert counts are copied to
  *      the host and the host waits for them (the one point where this call
- *      blocks the host);
+ *      blocks the host).  Meanwhile the copy stream, once the previous call
+ *      has finished on `stream`, fetches again the previous call's first
+ *      fetch batch when it held ring records only (the steady state repeats
+ *      the plan): if this call's first fetch batch is the same, its copies
+ *      are done; if not, the plan's own copies rewrite those slots before
+ *      any batch reads them;
  *   2. the residency plan (moe_plan_residency, call numbers 1, 2, ... per
  *      streamer), and the record and batch maps copied to the device;
  *   3. batch 0 (resident experts and the shared expert) runs on `stream`

@@ -423,14 +423,48 @@ int moe_forward_streamed(const uint16_t* x, const uint16_t* wr, const float* rbi
   TRY(moe_route_csr(x, wr, rbias, dims, idx, w, csr, ws, ws_bytes, stream));
 
   const int E = dims->E, P = st->cfg.pool_slots, R = st->cfg.ring_slots, lag = R / st->cfg.group;
-  const size_t rb = st->rec_bytes, rm = st->miss_bytes;
+  const size_t rb = st->rec_bytes, rm = split ? st->miss_bytes : st->rec_bytes;
   uint8_t* ring_base = slots + (size_t)P * rb;
-  // after a failure the pool's contents are unknown: empty it
+  // after a failure the pool's contents are unknown: empty it, and guess no
+  // first fetch batch for the next call
   auto fail = [&](cudaError_t e, const char* what) {
     std::fill(st->pool_expert.begin(), st->pool_expert.end(), -1);
+    st->spec_expert.clear();
+    st->spec_slot.clear();
     return set_error(MOE_ECUDA, "moe_forward_streamed: %s: %s", what, cudaGetErrorString(e));
   };
   cudaError_t e;
+  size_t copied = 0;
+  // the source and destination of a copy: pool slots from the base store,
+  // ring slots from the miss store, each region with its own record size
+  auto src_of = [&](int ex, int slot) {
+    return slot < P ? host_records + (size_t)ex * rb : host_miss_records + (size_t)ex * rm;
+  };
+  auto dst_of = [&](int slot) { return slot < P ? slots + (size_t)slot * rb : ring_base + (size_t)(slot - P) * rm; };
+  // one copy per run of consecutive experts bound for consecutive slots of
+  // one region, over copies [i, n) of the lists
+  auto copy_runs = [&](const int32_t* ex, const int32_t* sl, int i, int n) -> cudaError_t {
+    while (i < n) {
+      const int e0 = ex[i], s0 = sl[i];
+      const size_t bytes = s0 < P ? rb : rm;
+      int run = 1;
+      while (i + run < n && ex[i + run] == e0 + run && sl[i + run] == s0 + run && (sl[i + run] < P) == (s0 < P))
+        ++run;
+      cudaError_t r = cudaMemcpyAsync(dst_of(s0), src_of(e0, s0), run * bytes, cudaMemcpyHostToDevice, st->copy);
+      if (r != cudaSuccess) return r;
+      copied += run * bytes;
+      i += run;
+    }
+    return cudaSuccess;
+  };
+  // 0. while the chunk is routed, fetch again the last call's first fetch
+  // batch (ring slots only), once the last call's kernels are done with them
+  const int n_spec = (int)st->spec_expert.size();
+  if (n_spec > 0) {
+    if ((e = cudaStreamWaitEvent(st->copy, st->call_done, 0)) != cudaSuccess) return fail(e, "copy-stream wait");
+    if ((e = copy_runs(st->spec_expert.data(), st->spec_slot.data(), 0, n_spec)) != cudaSuccess)
+      return fail(e, "speculative fetch");
+  }
   // 1. the chunk's expert counts on the host
   if ((e = cudaMemcpyAsync(st->h_offsets, csr->offsets, (E + 1) * sizeof(int32_t), cudaMemcpyDeviceToHost, s)) !=
       cudaSuccess)
@@ -505,36 +539,23 @@ int moe_forward_streamed(const uint16_t* x, const uint16_t* wr, const float* rbi
   // 3-4. the fetch batches, two events each, and batch 0 (the resident
   // experts and the shared expert, no fetch).  Fetch batch 1 is enqueued
   // first so that the copies start while batch 0's launches are issued.
-  size_t copied = 0;
-  int nc = 0;
-  // the source and destination of a copy: pool slots from the base store,
-  // ring slots from the miss store, each region with its own record size
-  auto src_of = [&](int ex, int slot) {
-    return slot < P ? host_records + (size_t)ex * rb : host_miss_records + (size_t)ex * (split ? rm : rb);
-  };
-  auto dst_of = [&](int slot) {
-    return slot < P ? slots + (size_t)slot * rb : ring_base + (size_t)(slot - P) * (split ? rm : rb);
-  };
+  // Copies of batch b are the list entries [first[b], first[b + 1]).
+  std::vector<int> first(pl.n_batches + 1, pl.n_copies);
+  for (int i = pl.n_copies - 1; i >= 0; --i) first[st->plan_batch[pl.copy_expert[i]]] = i;
+  for (int b = pl.n_batches - 1; b >= 1; --b) first[b] = std::min(first[b], first[b + 1]);
+  // the speculative copies are batch 1 when they match it entry for entry
+  bool spec_used = n_spec > 0 && pl.n_batches > 1 && first[2] - first[1] == n_spec;
+  for (int i = 0; spec_used && i < n_spec; ++i)
+    spec_used = pl.copy_expert[first[1] + i] == st->spec_expert[i] && pl.copy_slot[first[1] + i] == st->spec_slot[i];
   // fetch batch b: wait until the batch that last read its ring slots is
-  // done, then one copy per run of consecutive experts bound for
-  // consecutive slots of one region
+  // done, copy, and signal "fetched"
   auto fetch = [&](int b) -> cudaError_t {
     cudaError_t r;
-    if (pl.wait_for[b] >= 1 && (r = cudaStreamWaitEvent(st->copy, st->done[pl.wait_for[b] % lag], 0)) != cudaSuccess)
-      return r;
-    while (nc < pl.n_copies && st->plan_batch[pl.copy_expert[nc]] == b) {
-      const int e0 = pl.copy_expert[nc], s0 = pl.copy_slot[nc];
-      const size_t bytes = s0 < P ? rb : (split ? rm : rb);
-      int run = 1;
-      while (nc + run < pl.n_copies && st->plan_batch[pl.copy_expert[nc + run]] == b &&
-             pl.copy_expert[nc + run] == e0 + run && pl.copy_slot[nc + run] == s0 + run &&
-             (pl.copy_slot[nc + run] < P) == (s0 < P))
-        ++run;
-      if ((r = cudaMemcpyAsync(dst_of(s0), src_of(e0, s0), run * bytes, cudaMemcpyHostToDevice, st->copy)) !=
-          cudaSuccess)
+    if (!(b == 1 && spec_used)) {
+      if (pl.wait_for[b] >= 1 &&
+          (r = cudaStreamWaitEvent(st->copy, st->done[pl.wait_for[b] % lag], 0)) != cudaSuccess)
         return r;
-      copied += run * bytes;
-      nc += run;
+      if ((r = copy_runs(pl.copy_expert, pl.copy_slot, first[b], first[b + 1])) != cudaSuccess) return r;
     }
     return cudaEventRecord(st->fetched, st->copy);
   };
@@ -549,6 +570,20 @@ int moe_forward_streamed(const uint16_t* x, const uint16_t* wr, const float* rbi
       if ((e = run(pi)) != cudaSuccess) return fail(e, "batch");
     if ((e = cudaEventRecord(st->done[b % lag], s)) != cudaSuccess) return fail(e, "event record");
   }
+  if ((e = cudaEventRecord(st->call_done, s)) != cudaSuccess) return fail(e, "event record");
+  // the guess for the next call: this call's first fetch batch, when it
+  // holds ring records only
+  st->spec_expert.clear();
+  st->spec_slot.clear();
+  if (pl.n_batches > 1) {
+    bool ring_only = true;
+    for (int i = first[1]; i < first[2]; ++i) ring_only = ring_only && pl.copy_slot[i] >= P;
+    if (ring_only)
+      for (int i = first[1]; i < first[2]; ++i) {
+        st->spec_expert.push_back(pl.copy_expert[i]);
+        st->spec_slot.push_back(pl.copy_slot[i]);
+      }
+  }
   if (stats) {
     stats->resident = 0;
     stats->filled = 0;
@@ -557,6 +592,8 @@ int moe_forward_streamed(const uint16_t* x, const uint16_t* wr, const float* rbi
     stats->streamed = pl.n_copies - stats->filled;
     stats->batches = pl.n_batches - 1;
     stats->bytes = (int64_t)copied;
+    stats->prefetched = n_spec;
+    stats->prefetch_used = spec_used ? 1 : 0;
   }
   return MOE_OK;
 }

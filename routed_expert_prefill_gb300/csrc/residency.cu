@@ -200,6 +200,8 @@ int moe_streamer_create(const moe_dims* dims, const moe_stream_cfg* cfg, moe_str
     return fail(e, "cudaStreamCreate");
   if ((e = cudaEventCreateWithFlags(&st->fetched, cudaEventDisableTiming)) != cudaSuccess)
     return fail(e, "cudaEventCreate");
+  if ((e = cudaEventCreateWithFlags(&st->call_done, cudaEventDisableTiming)) != cudaSuccess)
+    return fail(e, "cudaEventCreate");
   st->done.assign(cfg->ring_slots / cfg->group, nullptr);
   for (auto& ev : st->done)
     if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) return fail(e, "cudaEventCreate");
@@ -215,6 +217,7 @@ int moe_streamer_destroy(moe_streamer* st) {
   for (auto ev : st->done)
     if (ev) cudaEventDestroy(ev);
   if (st->fetched) cudaEventDestroy(st->fetched);
+  if (st->call_done) cudaEventDestroy(st->call_done);
   if (st->copy) cudaStreamDestroy(st->copy);
   if (st->d_maps) cudaFree(st->d_maps);
   if (st->h_maps) cudaFreeHost(st->h_maps);

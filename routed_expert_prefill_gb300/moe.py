@@ -97,7 +97,8 @@ class MoeResidencyPlan(ctypes.Structure):
 
 class MoeStreamStats(ctypes.Structure):
     _fields_ = [("resident", ctypes.c_int32), ("filled", ctypes.c_int32), ("streamed", ctypes.c_int32),
-                ("batches", ctypes.c_int32), ("bytes", ctypes.c_int64)]
+                ("batches", ctypes.c_int32), ("bytes", ctypes.c_int64), ("prefetched", ctypes.c_int32),
+                ("prefetch_used", ctypes.c_int32)]
 
 
 class MoeError(RuntimeError):
@@ -774,4 +775,5 @@ def moe_forward_streamed(dev: dict, dims: MoeDims, st: Streamer, flags: int = MO
                                     st._h, _stream(stream), ctypes.byref(stats)))
     return dict(idx=idx, w=w, csr=csr, out=out, ws=ws,
                 stats=dict(resident=stats.resident, filled=stats.filled, streamed=stats.streamed,
-                           batches=stats.batches, bytes=stats.bytes))
+                           batches=stats.batches, bytes=stats.bytes, prefetched=stats.prefetched,
+                           prefetch_used=stats.prefetch_used))

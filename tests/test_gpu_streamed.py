@@ -84,22 +84,36 @@ def _streamed(moe, w, dev, st, flags):
     return res
 
 
-def _check_plan(res, st, E, oracle_state, call):
-    """Stats and pool table equal the oracle's plan for the chunk's counts."""
+def _state(pool):
+    """The oracle's view of a fresh streamer with `pool` pool slots."""
+    return dict(pool=[-1] * pool, last=[0] * pool, spec=[])
+
+
+def _check_plan(res, st, state, call):
+    """Stats and pool table equal the oracle's plan for the chunk's counts;
+    the speculative copies are the last call's first fetch batch (when it
+    held ring records only) and count as this call's first batch exactly
+    when they are its copies.  Returns the state after the call, with the
+    experts read from ring slots under "miss"."""
     offs = res["csr"].offsets.cpu().numpy().astype(np.int64)
     counts = np.diff(offs)
-    pool, last = oracle_state
-    p = R.plan(counts, pool, last, call=call, ring=st.cfg.ring_slots, group=st.cfg.group)
+    p = R.plan(counts, state["pool"], state["last"], call=call, ring=st.cfg.ring_slots, group=st.cfg.group)
     P = st.cfg.pool_slots
     n_fill = sum(1 for _, s in p["copies"] if s < P)
+    first = [(e, sl) for e, sl in p["copies"] if p["batch"][e] == 1]
     s = res["stats"]
     assert s["resident"] == sum(1 for b in p["batch"] if b == 0)
     assert s["filled"] == n_fill
     assert s["streamed"] == len(p["copies"]) - n_fill
     assert s["batches"] == p["n_batches"] - 1
-    assert s["bytes"] == n_fill * st.rec_bytes + (len(p["copies"]) - n_fill) * st.miss_rec_bytes
+    assert s["prefetched"] == len(state["spec"])
+    assert s["prefetch_used"] == int(bool(state["spec"]) and state["spec"] == first)
+    wasted = 0 if s["prefetch_used"] else s["prefetched"] * st.miss_rec_bytes
+    assert s["bytes"] == n_fill * st.rec_bytes + (len(p["copies"]) - n_fill) * st.miss_rec_bytes + wasted
     assert st.pool() == p["pool_expert"]
-    return p["pool_expert"], p["pool_last"], R.miss_experts(p, P)
+    spec = first if first and all(sl >= P for _, sl in first) else []
+    return dict(pool=p["pool_expert"], last=p["pool_last"], spec=spec, miss=R.miss_experts(p, P),
+                used=s["prefetch_used"])
 
 
 CASES = [
@@ -130,7 +144,7 @@ def test_streamed_matches_oracle(moe, name, pool, ring, group):
     err = np.abs(got - ref["out"]).max()
     tol = TOL_REL * np.abs(ref["out"]).max() + TOL_ABS
     assert err <= tol, f"max|gpu-oracle| = {err:.4g} > {tol:.4g}"
-    _check_plan(res, st, w.E, ([-1] * pool, [0] * pool), 1)
+    _check_plan(res, st, _state(pool), 1)
     st.close()
 
 
@@ -145,11 +159,11 @@ def test_miss_store_matches_oracle(moe, bits, flags):
     inp, dev = _setup(moe, w)
     miss, miss_packed = _miss_store(moe, w, bits)
     st = _streamer(moe, w, dev, 32, 16, 8, miss=(bits, miss_packed))
-    state = ([-1] * 32, [0] * 32)
+    state = _state(32)
     for call in (1, 2):
         res = _streamed(moe, w, dev, st, flags)
-        pool, last, streamed = _check_plan(res, st, w.E, state[:2], call)
-        state = (pool, last)
+        state = _check_plan(res, st, state, call)
+        streamed = state["miss"]
         assert 0 < len(streamed) < w.E
         ref = O.moe_forward(inp, w.k, w.h, w.inter, w.shared_inter, miss=dict(miss, experts=streamed))
         got = res["out"].float().cpu().numpy().astype(np.float64)
@@ -181,17 +195,17 @@ def test_pool_persists_across_chunks(moe):
     _, dev = _setup(moe, w)
     x0 = dev["x"]
     st = _streamer(moe, w, dev, 24, 16, 8)
-    state = ([-1] * 24, [0] * 24, set())
+    state = _state(24)
     evicted = 0
     for call in range(1, 6):
         dev["x"] = torch.roll(x0, shifts=call * 5, dims=1).contiguous()  # new rows, new routing
-        before = set(state[0])
+        before = set(state["pool"])
         ref = _resident(moe, w, dev, moe.MOE_DETERMINISTIC)
         res = _streamed(moe, w, dev, st, moe.MOE_DETERMINISTIC)
         np.testing.assert_array_equal(res["out"].view(torch.int16).cpu().numpy(),
                                       ref["out"].view(torch.int16).cpu().numpy())
-        state = _check_plan(res, st, w.E, state[:2], call)
-        evicted += len(before - set(state[0]) - {-1})
+        state = _check_plan(res, st, state, call)
+        evicted += len(before - set(state["pool"]) - {-1})
     assert evicted > 0
     st.close()
 
@@ -200,15 +214,44 @@ def test_pool_persists_across_chunks(moe):
 def test_single_batch_ring_and_no_pool(moe, pool, ring, group):
     # ring == group: every fetch batch overwrites the slots the previous
     # batch read, so it must wait for that batch; a read before its fetch
-    # completed would see another expert's record
+    # completed would see another expert's record.  From the second call on
+    # the first fetch batch is fetched again while the chunk is routed, into
+    # the slots the previous call's last batch read.
     w = synth.WORKLOADS["t512_h2048_e128"]
     _, dev = _setup(moe, w)
     ref = _resident(moe, w, dev, moe.MOE_DETERMINISTIC)
     st = _streamer(moe, w, dev, pool, ring, group)
-    for call in (1, 2):
+    state = _state(pool)
+    for call in (1, 2, 3):
         res = _streamed(moe, w, dev, st, moe.MOE_DETERMINISTIC)
         np.testing.assert_array_equal(res["out"].view(torch.int16).cpu().numpy(),
                                       ref["out"].view(torch.int16).cpu().numpy())
+        state = _check_plan(res, st, state, call)
+        if call == 3:
+            assert res["stats"]["prefetch_used"] == 1 and res["stats"]["prefetched"] == group
+    st.close()
+
+
+def test_wrong_guess_of_the_first_batch(moe):
+    # chunks of 16 rows (a third of the experts idle) whose routing differs
+    # from the last one's: the speculative copies of the last call's first
+    # batch are then not this call's, and the plan's own copies overwrite
+    # those slots before any batch reads them; a repeated chunk uses them
+    w = synth.WORKLOADS["t512_h2048_e128"].replace(t=16)
+    _, dev = _setup(moe, w)
+    x0 = dev["x"]
+    st = _streamer(moe, w, dev, 0, 8, 4)
+    state = _state(0)
+    used = []
+    for call, shift in enumerate((0, 7, 7, 13, 29), start=1):
+        dev["x"] = torch.roll(x0, shifts=shift, dims=1).contiguous()
+        ref = _resident(moe, w, dev, moe.MOE_DETERMINISTIC)
+        res = _streamed(moe, w, dev, st, moe.MOE_DETERMINISTIC)
+        np.testing.assert_array_equal(res["out"].view(torch.int16).cpu().numpy(),
+                                      ref["out"].view(torch.int16).cpu().numpy())
+        state = _check_plan(res, st, state, call)
+        used.append(state["used"])
+    assert used[2] == 1 and 0 in used[1:]
     st.close()
 
 
@@ -247,13 +290,13 @@ def test_headline_half_resident(moe):
     inp, dev = _setup(moe, w)
     ref = _resident(moe, w, dev, moe.MOE_DETERMINISTIC)
     st = _streamer(moe, w, dev, 128, 64, 32)
-    state = ([-1] * 128, [0] * 128)
+    state = _state(128)
     res = _streamed(moe, w, dev, st, moe.MOE_DETERMINISTIC)
     np.testing.assert_array_equal(res["out"].view(torch.int16).cpu().numpy(),
                                   ref["out"].view(torch.int16).cpu().numpy())
-    state = _check_plan(res, st, w.E, state, 1)[:2]
+    state = _check_plan(res, st, state, 1)
     res = _streamed(moe, w, dev, st, 0)
-    state = _check_plan(res, st, w.E, state, 2)[:2]
+    state = _check_plan(res, st, state, 2)
     assert res["stats"]["streamed"] == 128 and res["stats"]["resident"] == 128
     rows = np.random.default_rng([w.seed, 78]).choice(w.t, 16, replace=False)
     sub = dict(inp)
@@ -273,12 +316,15 @@ def test_headline_miss_store_two_bits(moe):
     inp, dev = _setup(moe, w)
     miss, miss_packed = _miss_store(moe, w, 2)
     st = _streamer(moe, w, dev, 128, 64, 32, miss=(2, miss_packed))
-    state = ([-1] * 128, [0] * 128)
-    for call in (1, 2):
+    state = _state(128)
+    for call in (1, 2, 3):
         res = _streamed(moe, w, dev, st, 0)
-        pool, last, streamed = _check_plan(res, st, w.E, state, call)
-        state = (pool, last)
+        state = _check_plan(res, st, state, call)
+    streamed = state["miss"]
+    # the third chunk repeats the second's plan: its first batch was fetched
+    # while it was routed
     assert len(streamed) == 128 and res["stats"]["bytes"] == 128 * st.miss_rec_bytes
+    assert res["stats"]["prefetch_used"] == 1
     rows = np.random.default_rng([w.seed, 79]).choice(w.t, 16, replace=False)
     sub = dict(inp)
     sub["x"] = inp["x"][rows]
