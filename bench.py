@@ -58,7 +58,7 @@ EXTRA_WORKLOADS = ("t4096_h2048_e128_skewed", "t512_h2048_e128", "decode_t1_h204
 # host memory, half of them resident in a device pool after the first chunk.
 STREAMED = "t4096_h4096_e256_streamed"
 STREAMED_MISS2 = "t4096_h4096_e256_streamed_miss2"  # the ring's records from a 2-bit miss store
-STREAMED_CFG = dict(pool_slots=128, ring_slots=64, group=32)
+STREAMED_CFG = dict(pool_slots=128, ring_slots=64, group=8)  # prefill.rs RING and GROUP
 L2_BYTES = 129 * 2 ** 20
 SUSTAIN_S, SUSTAIN_MIN_RUNS, SUSTAIN_MAX_RUNS = 1.0, 50, 20000
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
