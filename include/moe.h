@@ -448,8 +448,10 @@ typedef struct {
  * flags: MOE_PACKED_WEIGHTS (required) and optionally MOE_DETERMINISTIC;
  *   the tensor-core kernels always run.  ws: moe_workspace_bytes(dims, flags).
  * stats: host, may be NULL.
- * Calls on one streamer must be ordered: issue them on one stream from one
- * thread.  After a failed call the pool is emptied (the next call refetches).
+ * Calls on one streamer are issued from one thread; each call's work, its
+ * copies included, waits for the end of the previous call on the streamer,
+ * on whatever stream that call ran.  After a failed call the pool is emptied
+ * (the next call refetches).
  * Errors: MOE_EINVAL, MOE_ESHAPE (dims other than the streamer's), MOE_EWORKSPACE,
  * MOE_ECUDA.
  */

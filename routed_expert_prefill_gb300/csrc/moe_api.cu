@@ -418,8 +418,11 @@ int moe_forward_streamed(const uint16_t* x, const uint16_t* wr, const float* rbi
     TRY(check_ptr(shared->gate, "shared->gate", 16, true));
   }
   TRY(check_ws(dims, flags, ws, ws_bytes));
-  // router and grouping: checks the remaining pointers before enqueueing
   cudaStream_t s = (cudaStream_t)stream;
+  // the call follows the previous call on this streamer, on whatever
+  // stream that one ran (its batches read the slots this call refills)
+  if (st->call_done_recorded) TRY(cuda_status(cudaStreamWaitEvent(s, st->call_done, 0), "stream wait"));
+  // router and grouping: checks the remaining pointers before enqueueing
   TRY(moe_route_csr(x, wr, rbias, dims, idx, w, csr, ws, ws_bytes, stream));
 
   const int E = dims->E, P = st->cfg.pool_slots, R = st->cfg.ring_slots, lag = R / st->cfg.group;
@@ -457,14 +460,15 @@ int moe_forward_streamed(const uint16_t* x, const uint16_t* wr, const float* rbi
     }
     return cudaSuccess;
   };
+  // every copy of this call follows the end of the last call, whose kernels
+  // read the slots (on its own stream, which need not be this one)
+  if (st->call_done_recorded && (e = cudaStreamWaitEvent(st->copy, st->call_done, 0)) != cudaSuccess)
+    return fail(e, "copy-stream wait");
   // 0. while the chunk is routed, fetch again the last call's first fetch
-  // batch (ring slots only), once the last call's kernels are done with them
+  // batch (ring slots only)
   const int n_spec = (int)st->spec_expert.size();
-  if (n_spec > 0) {
-    if ((e = cudaStreamWaitEvent(st->copy, st->call_done, 0)) != cudaSuccess) return fail(e, "copy-stream wait");
-    if ((e = copy_runs(st->spec_expert.data(), st->spec_slot.data(), 0, n_spec)) != cudaSuccess)
-      return fail(e, "speculative fetch");
-  }
+  if (n_spec > 0 && (e = copy_runs(st->spec_expert.data(), st->spec_slot.data(), 0, n_spec)) != cudaSuccess)
+    return fail(e, "speculative fetch");
   // 1. the chunk's expert counts on the host
   if ((e = cudaMemcpyAsync(st->h_offsets, csr->offsets, (E + 1) * sizeof(int32_t), cudaMemcpyDeviceToHost, s)) !=
       cudaSuccess)
@@ -571,6 +575,7 @@ int moe_forward_streamed(const uint16_t* x, const uint16_t* wr, const float* rbi
     if ((e = cudaEventRecord(st->done[b % lag], s)) != cudaSuccess) return fail(e, "event record");
   }
   if ((e = cudaEventRecord(st->call_done, s)) != cudaSuccess) return fail(e, "event record");
+  st->call_done_recorded = true;
   // the guess for the next call: this call's first fetch batch, when it
   // holds ring records only
   st->spec_expert.clear();

@@ -34,6 +34,7 @@ struct moe_streamer {
   cudaEvent_t fetched = nullptr;  // copy stream -> compute stream, per batch
   std::vector<cudaEvent_t> done;  // compute stream -> copy stream, batch b in done[b % lag]
   cudaEvent_t call_done = nullptr;  // end of the last call on its stream
+  bool call_done_recorded = false;
   // the last call's first fetch batch when it held ring records only: the
   // next call fetches it again while it routes (expert, ring slot)
   std::vector<int32_t> spec_expert, spec_slot;

@@ -334,3 +334,36 @@ def test_headline_miss_store_two_bits(moe):
     tol = TOL_REL * np.abs(oref["out"]).max() + TOL_ABS
     assert err <= tol, f"max|gpu-oracle| = {err:.4g} > {tol:.4g}"
     st.close()
+
+
+def test_calls_on_two_streams_follow_each_other(moe):
+    # consecutive calls on one streamer issued on two streams, each with its
+    # own workspace and output, the host not waiting between them: every
+    # call's work (pool fills, speculative copies, batches) follows the
+    # previous call, so every output is the resident path's, bit for bit
+    w = synth.WORKLOADS["t512_h2048_e128"].replace(t=32)
+    _, dev = _setup(moe, w)
+    x0 = dev["x"]
+    st = _streamer(moe, w, dev, 24, 8, 4)
+    dims = _dims(moe, w)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    xs = [torch.roll(x0, shifts=sh, dims=1).contiguous() for sh in (0, 5, 5, 11, 3, 3)]
+    refs = []
+    for x in xs:
+        dev["x"] = x
+        refs.append(_resident(moe, w, dev, moe.MOE_DETERMINISTIC)["out"].clone())
+    torch.cuda.synchronize()
+    outs = []
+    for i, x in enumerate(xs):
+        s = streams[i % 2]
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            ws = moe.new_workspace(dims, moe.MOE_PACKED_WEIGHTS | moe.MOE_DETERMINISTIC, stream=s)
+            res = moe.moe_forward_streamed(dict(dev, x=x), dims, st,
+                                           moe.MOE_PACKED_WEIGHTS | moe.MOE_DETERMINISTIC, ws=ws, stream=s)
+            outs.append((res["out"], res["ws"]))
+    torch.cuda.synchronize()
+    for (o, ws), ref in zip(outs, refs):
+        assert moe.read_device_status(ws) == 0
+        np.testing.assert_array_equal(o.view(torch.int16).cpu().numpy(), ref.view(torch.int16).cpu().numpy())
+    st.close()
