@@ -121,3 +121,14 @@ def test_step_roofline_picks_the_slower_bound():
     assert sr["frac"] == pytest.approx(0.5)
     sr = bench.step_roofline({"flops": 4e12, "bytes": 8e9}, 4.0, peaks)
     assert sr["bound"] == "tensor" and sr["frac"] == pytest.approx(0.5)
+
+
+def test_streamed_entries_follow_the_pages_ring():
+    # the streamed bench entries stream the headline chunk through the pages'
+    # ring (prefill.rs: RING = 64 slots, GROUP = 8 experts per batch) with
+    # half of the 256 records resident, and the miss entry uses 2-bit records
+    assert bench.STREAMED_CFG == dict(pool_slots=128, ring_slots=64, group=8)
+    assert bench.STREAMED != bench.STREAMED_MISS2
+    assert bench.DEFAULT_WORKLOAD == "t4096_h4096_e256"
+    assert synth.WORKLOADS[bench.DEFAULT_WORKLOAD].E == 2 * bench.STREAMED_CFG["pool_slots"]
+    assert "t4096_h4096_e256_b2" in synth.WORKLOADS
