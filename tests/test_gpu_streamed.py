@@ -367,3 +367,42 @@ def test_calls_on_two_streams_follow_each_other(moe):
         assert moe.read_device_status(ws) == 0
         np.testing.assert_array_equal(o.view(torch.int16).cpu().numpy(), ref.view(torch.int16).cpu().numpy())
     st.close()
+
+
+@pytest.mark.parametrize("t", [1, 3])
+def test_decode_sized_chunks(moe, t):
+    # chunks of 1 and 3 rows through the streamed path (the tensor-core
+    # kernels on 64-row tiles): bit for bit the resident tensor-core path's,
+    # and within the tolerance of the oracle
+    w = synth.WORKLOADS["t512_h2048_e128"].replace(t=t)
+    inp, dev = _setup(moe, w)
+    ref = _resident(moe, w, dev, moe.MOE_DETERMINISTIC)
+    st = _streamer(moe, w, dev, 4, 8, 4)
+    state = _state(4)
+    for call in (1, 2):
+        res = _streamed(moe, w, dev, st, moe.MOE_DETERMINISTIC)
+        np.testing.assert_array_equal(res["out"].view(torch.int16).cpu().numpy(),
+                                      ref["out"].view(torch.int16).cpu().numpy())
+        state = _check_plan(res, st, state, call)
+    oref = O.moe_forward(inp, w.k, w.h, w.inter, w.shared_inter)
+    got = res["out"].float().cpu().numpy().astype(np.float64)
+    assert np.abs(got - oref["out"]).max() <= TOL_REL * np.abs(oref["out"]).max() + TOL_ABS
+    st.close()
+
+
+def test_no_shared_expert_and_odd_expert_count(moe):
+    # E = 40 (not a multiple of 32), k = 8, no shared expert, t = 300
+    w = synth.Workload("st_e40", 300, 512, 256, 40, 8, 0, 91)
+    inp, dev = _setup(moe, w)
+    ref = _resident(moe, w, dev, moe.MOE_DETERMINISTIC)
+    st = _streamer(moe, w, dev, 10, 6, 3)
+    state = _state(10)
+    for call in (1, 2):
+        res = _streamed(moe, w, dev, st, moe.MOE_DETERMINISTIC)
+        np.testing.assert_array_equal(res["out"].view(torch.int16).cpu().numpy(),
+                                      ref["out"].view(torch.int16).cpu().numpy())
+        state = _check_plan(res, st, state, call)
+    oref = O.moe_forward(inp, w.k, w.h, w.inter, w.shared_inter)
+    got = res["out"].float().cpu().numpy().astype(np.float64)
+    assert np.abs(got - oref["out"]).max() <= TOL_REL * np.abs(oref["out"]).max() + TOL_ABS
+    st.close()
