@@ -208,7 +208,8 @@ int moe_route_csr(const uint16_t* x, const uint16_t* wr, const float* rbias,
  *
  * Kernel choice (the result meets the same tolerance either way):
  *   - weight-streaming small-t kernels when t <= 16 and t * k * inter / 128
- *     < 152 (too few expert tiles to occupy the GPU), or MOE_FORCE_SMALL_T;
+ *     < 64 on packed records (few expert tiles: at inter = 768 and k = 8, a
+ *     chunk of one row), < 152 on row-major records, or MOE_FORCE_SMALL_T;
  *   - otherwise the tensor-core grouped kernels (MOE_FORCE_LARGE_T forces
  *     them), on packed weights with MOE_PACKED_WEIGHTS, or on the row-major
  *     records;

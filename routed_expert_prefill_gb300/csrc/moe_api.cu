@@ -41,14 +41,21 @@ cudaError_t launch_decode_fused(const uint16_t* x, const uint16_t* wr, const flo
                                 DeviceStatus* st, cudaStream_t stream);
 
 // Chunks of at most SMALL_T_MAX rows whose (expert, 128-row tile) units are
-// too few to occupy the GPU (t * k * inter / 128 below SMALL_T_UNITS, about
-// one per SM of a GB300) take the weight-streaming small-t kernels, unless
-// MOE_FORCE_LARGE_T.  With more units the tensor-core kernels are faster:
-// their only per-weight work is the dequantisation, where the CUDA-core dot
-// products of the streaming kernels cost several more instructions per
-// weight and row.
+// few (t * k * inter / 128 below SMALL_T_UNITS on packed records,
+// SMALL_T_UNITS_ROWMAJOR on row-major ones) take the weight-streaming
+// small-t kernels, unless MOE_FORCE_LARGE_T.  With more units the
+// tensor-core kernels are faster: their only per-weight work is the
+// dequantisation, where the CUDA-core dot products of the streaming kernels
+// cost several more instructions per weight and row.  Graph-timed steps on
+// packed records on a GB300: h2048 inter768 E128 k8, t = 1 (48 units)
+// 36.0 us streaming against 40.1 on the tensor cores, t = 2 (96) 48.3
+// against 42.1, t = 3 (144) 68.6 against 48.3; h4096 inter1536 E256 k8,
+// t = 1 (96 units) 91.3 against 58.5.  The row-major tensor-core kernels
+// gather token rows with four-row TMA loads and keep the threshold of one
+// unit per SM.
 constexpr int SMALL_T_MAX = 16;
-constexpr int SMALL_T_UNITS = 152;
+constexpr int SMALL_T_UNITS = 64;
+constexpr int SMALL_T_UNITS_ROWMAJOR = 152;
 
 // Scheduler scratch: room for the larger of the two tensor-core paths' tile
 // lists (the packed path's, on its smallest tiles, or the row-major path's).
@@ -335,7 +342,8 @@ int moe_experts_fwd(const uint16_t* x, const moe_csr* csr, const moe_qweights* e
   const bool small_t =
       a.bits == 4 && !(flags & (MOE_FORCE_LARGE_T | MOE_SIMPLE_KERNELS)) &&
       ((flags & MOE_FORCE_SMALL_T) ||
-       (dims->t <= SMALL_T_MAX && (long)dims->t * dims->k * (dims->inter / 128) < SMALL_T_UNITS));
+       (dims->t <= SMALL_T_MAX &&
+        (long)dims->t * dims->k * (dims->inter / 128) < (packed ? SMALL_T_UNITS : SMALL_T_UNITS_ROWMAJOR)));
   if (small_t)
     return cuda_status(launch_experts_gemv(a, packed, (flags & MOE_DETERMINISTIC) != 0, s), "moe_experts_fwd launch");
   if (packed)
