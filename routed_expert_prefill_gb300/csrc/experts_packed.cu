@@ -40,7 +40,6 @@
 // records MOE_ETIMEOUT, raises a CTA-wide abort flag, lets in-flight copies
 // and MMAs land, frees TMEM and returns.
 #include <type_traits>
-#include "schedule.cuh"
 #include "tc_common.cuh"
 #include "tc_ptx.cuh"
 
@@ -296,36 +295,6 @@ gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ rows, 
     const uint4 v = ok ? reinterpret_cast<const uint4*>(x + (size_t)r * h)[pc] : make_uint4(0, 0, 0, 0);
     const int kc = pc >> 3, c = pc & 7;
     *reinterpret_cast<uint4*>(base + (size_t)kc * Nm * 128 + sw128_off(j, c)) = v;
-  }
-}
-
-// Small chunks: the tile schedule and the gather in one block of 1024
-// threads, one launch fewer on decode-sized chunks; the gather walks every
-// tile with one warp per row.
-__global__ void __launch_bounds__(1024)
-prep_small_kernel(TcParams p, SchedHdr* hdr, int4* tiles, int* units_gu, int max_tiles, int tile_max,
-                  const uint16_t* __restrict__ x, uint16_t* __restrict__ xg) {
-  pdl_wait();
-  pdl_trigger();
-  schedule_block(p, hdr, tiles, units_gu, max_tiles, tile_max);
-  __syncthreads();  // the tiles and the header are written
-  const int n_tiles = hdr->n_tiles;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  const int h = p.h, npieces = h / 8;
-  for (int tile = 0; tile < n_tiles; ++tile) {
-    const int4 T = tiles[tile];
-    const int n = T.z, Nm = (n + 15) & ~15;
-    uint8_t* base = reinterpret_cast<uint8_t*>(xg + (size_t)T.w * h);
-    for (int j = warp; j < Nm; j += nwarps) {
-      const int jj = min(j, n - 1);
-      const int r = (T.x == p.E) ? T.y + jj : p.rows[T.y + jj];
-      const bool ok = (r >= 0 && r < p.t);
-      if (!ok && lane == 0) raise_flag(p.status, FLAG_BAD_ROW);
-      for (int pc = lane; pc < npieces; pc += 32) {
-        const uint4 v = ok ? reinterpret_cast<const uint4*>(x + (size_t)r * h)[pc] : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(base + (size_t)(pc >> 3) * Nm * 128 + sw128_off(j, pc & 7)) = v;
-      }
-    }
   }
 }
 
@@ -1076,8 +1045,6 @@ cudaError_t launch_packed_pt(const PParams& P, int pt, cudaStream_t stream) {
                            : launch_packed_gemms<PTILE_SMALL, BITS>(P, stream);
 }
 
-constexpr long SMALL_PREP_ROWS = 96;
-
 cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, const uint8_t* s_packed,
                                   uint16_t* xg, bool deterministic, cudaStream_t stream, const PackedBatch* pb) {
   moe_dims d{a.t, a.h, a.I, a.E, a.k, a.Is};
@@ -1130,21 +1097,13 @@ cudaError_t launch_experts_packed(const ExpertsArgs& a, const uint8_t* packed, c
   const long pairs = (long)a.t * a.k;
   const int pt = pairs <= 40L * a.E ? PTILE_SMALL : pairs <= 96L * a.E ? PTILE : PTILE_LARGE;
   cudaError_t err;
-  // chunks of at most SMALL_PREP_ROWS gathered rows (a decode step of up
-  // to ten rows at k = 8) build the schedule and gather in one launch
-  const bool small_prep = pairs + a.t <= SMALL_PREP_ROWS;
-  if (small_prep)
-    MOE_LAUNCH("schedule_gather", stream,
-               launch_k(prep_small_kernel, 1, 1024, 0, stream, p, hdr, tiles, units, (int)mt, pt, a.x, xg));
-  else if ((err = launch_schedule(p, hdr, tiles, units, (int)mt, pt, stream)) != cudaSuccess)
-    return err;
+  if ((err = launch_schedule(p, hdr, tiles, units, (int)mt, pt, stream)) != cudaSuccess) return err;
   if (first && p.gate_vals &&
       (err = launch_shared_gate(a.x, a.s_gate, a.t, a.h, gate_vals, stream)) != cudaSuccess)
     return err;
-  if (!small_prep)
-    MOE_LAUNCH("gather", stream,
-               launch_k(gather_kernel, dim3((unsigned)mt, pt / 8), 256, 0, stream, a.x, a.rows, hdr, tiles, a.t, a.h,
-                        a.E, xg, a.status));
+  MOE_LAUNCH("gather", stream,
+             launch_k(gather_kernel, dim3((unsigned)mt, pt / 8), 256, 0, stream, a.x, a.rows, hdr, tiles, a.t, a.h, a.E,
+                                                                          xg, a.status));
   err = a.bits == 2   ? launch_packed_pt<2>(P, pt, stream)
         : a.bits == 3 ? launch_packed_pt<3>(P, pt, stream)
         : a.bits == 8 ? launch_packed_pt<8>(P, pt, stream)
