@@ -284,11 +284,13 @@ gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ rows, 
   const int n = T.z, Nm = (n + 15) & ~15;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = blockIdx.y * 8 + warp;
-  if (j >= Nm) return;
+  // rows n .. Nm-1 pad the tile to the MMA's 16-column granule: they feed
+  // only accumulator columns that the epilogues drop, so they are left as
+  // they are (a one-row decode tile copies one row, not sixteen)
+  if (j >= n) return;
   uint8_t* base = reinterpret_cast<uint8_t*>(xg + (size_t)T.w * h);
   const int npieces = h / 8;
-  const int jj = min(j, n - 1);
-  const int r = (T.x == E) ? T.y + jj : rows[T.y + jj];
+  const int r = (T.x == E) ? T.y + j : rows[T.y + j];
   const bool ok = (r >= 0 && r < t);
   if (!ok && lane == 0) raise_flag(st, FLAG_BAD_ROW);
   for (int pc = lane; pc < npieces; pc += 32) {
